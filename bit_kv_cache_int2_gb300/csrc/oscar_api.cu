@@ -1,0 +1,397 @@
+// Host side of the liboscar C ABI: argument checks, context, rotation tables
+// and kernel launches.  See include/oscar.h for the contract of each call.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "oscar_internal.cuh"
+
+using namespace oscar;
+
+struct oscar_ctx {
+  oscar_config cfg;
+  int device = 0;
+  int num_sms = 0;
+  int G = 0, NG = 0;
+  float* d_rot = nullptr;  // [layers][3][Hkv][128][128]: U_K, U_V, U_V^T
+  float* d_clip = nullptr;  // [layers][2][Hkv]
+  std::vector<int> mode;
+  int* d_err = nullptr;
+  int* d_req_counter = nullptr;  // [max_batch]
+  int impl = 0;
+  int ctas_per_sm = 2;
+  int items_per_cta = 3;
+};
+
+namespace {
+
+constexpr int VERSION = 10000;
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+oscar_status check_cfg(const oscar_config* c) {
+  if (!c) return OSCAR_ERR_INVALID_ARG;
+  if (c->head_dim != D || c->page_size != PAGE || c->sink_tokens != SINK ||
+      c->recent_tokens != RECENT)
+    return OSCAR_ERR_UNSUPPORTED;
+  if (c->group_size != 32 && c->group_size != 64 && c->group_size != 128)
+    return OSCAR_ERR_UNSUPPORTED;
+  if (c->num_layers < 1 || c->num_q_heads < 1 || c->num_kv_heads < 1 || c->max_batch < 1 ||
+      c->max_pages_per_req < 1 || c->num_pages < 1)
+    return OSCAR_ERR_INVALID_ARG;
+  if (c->num_q_heads % c->num_kv_heads) return OSCAR_ERR_INVALID_ARG;
+  const int G = c->num_q_heads / c->num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return OSCAR_ERR_UNSUPPORTED;
+  if ((long long)c->max_batch * c->num_q_heads > (1LL << 24)) return OSCAR_ERR_INVALID_ARG;
+  if ((long long)c->max_pages_per_req * PAGE > (1LL << 30)) return OSCAR_ERR_INVALID_ARG;
+  return OSCAR_OK;
+}
+
+size_t scratch_for(const oscar_ctx* ctx, int B, int target) {
+  return decode_scratch_bytes(B, ctx->cfg.num_q_heads, ctx->cfg.num_kv_heads, ctx->G, target);
+}
+
+int target_items(const oscar_ctx* ctx) {
+  int t = ctx->num_sms * ctx->ctas_per_sm * ctx->items_per_cta;
+  if (t > MAX_TARGET_ITEMS) t = MAX_TARGET_ITEMS;
+  if (t < 1) t = 1;
+  return t;
+}
+
+bool cache_ok(const oscar_cache* c, bool need_pool) {
+  if (!c) return false;
+  if (need_pool && (!c->pool || !c->page_table || !aligned(c->pool, 256))) return false;
+  if (!c->sink_k || !c->sink_v || !c->ring_k || !c->ring_v || !c->seq_lens || !c->hist_lens)
+    return false;
+  return aligned(c->sink_k, 16) && aligned(c->sink_v, 16) && aligned(c->ring_k, 16) &&
+         aligned(c->ring_v, 16) && aligned(c->seq_lens, 4) && aligned(c->hist_lens, 4);
+}
+
+CacheView make_view(const oscar_ctx* ctx, const oscar_cache* c, bool bf16_history) {
+  CacheView v;
+  v.pool = (uint8_t*)c->pool;
+  v.page_table = c->page_table;
+  v.sink_k = (__nv_bfloat16*)c->sink_k;
+  v.sink_v = (__nv_bfloat16*)c->sink_v;
+  v.ring_k = (__nv_bfloat16*)c->ring_k;
+  v.ring_v = (__nv_bfloat16*)c->ring_v;
+  v.seq_lens = c->seq_lens;
+  v.hist_lens = c->hist_lens;
+  v.Hq = ctx->cfg.num_q_heads;
+  v.Hkv = ctx->cfg.num_kv_heads;
+  v.G = ctx->G;
+  v.g = ctx->cfg.group_size;
+  v.NG = ctx->NG;
+  v.max_pages_per_req = ctx->cfg.max_pages_per_req;
+  v.num_pages = ctx->cfg.num_pages;
+  v.head_bytes = bf16_history ? BF16_HEAD_BYTES : int2_head_bytes(ctx->cfg.group_size);
+  v.page_bytes = (long long)v.head_bytes * ctx->cfg.num_kv_heads;
+  v.err = ctx->d_err;
+  return v;
+}
+
+LayerRot layer_rot(const oscar_ctx* ctx, int layer) {
+  const size_t mat = (size_t)ctx->cfg.num_kv_heads * D * D;
+  LayerRot r;
+  r.U_K = ctx->d_rot + (size_t)layer * 3 * mat;
+  r.U_V = r.U_K + mat;
+  r.Ut_V = r.U_V + mat;
+  r.clip_k = ctx->d_clip + (size_t)layer * 2 * ctx->cfg.num_kv_heads;
+  r.clip_v = r.clip_k + ctx->cfg.num_kv_heads;
+  r.mode = ctx->mode[layer];
+  return r;
+}
+
+oscar_status cuda_status(cudaError_t e) { return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA; }
+
+oscar_status decode_common(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* q,
+                           void* out, float* lse, void* scratch, size_t scratch_bytes, int batch,
+                           oscar_stream_t stream, bool bf16_history) {
+  if (!ctx || !cache_ok(cache, true) || !q || !out || !scratch) return OSCAR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
+  if (batch < 0 || batch > ctx->cfg.max_batch) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(scratch, 256) ||
+      (lse && !aligned(lse, 4)))
+    return OSCAR_ERR_INVALID_ARG;
+  if (batch == 0) return OSCAR_OK;
+  const int target = target_items(ctx);
+  if (scratch_bytes < scratch_for(ctx, batch, target)) return OSCAR_ERR_INVALID_ARG;
+  DecodeArgs a;
+  a.cv = make_view(ctx, cache, bf16_history);
+  a.q = (const __nv_bfloat16*)q;
+  a.out = (__nv_bfloat16*)out;
+  a.lse = lse;
+  a.counter = (int*)scratch;
+  a.qrot = (float*)((uint8_t*)scratch + 256);
+  const size_t qbytes = (((size_t)batch * ctx->cfg.num_q_heads * D * 4) + 255) & ~(size_t)255;
+  a.part = (float*)((uint8_t*)scratch + 256 + qbytes);
+  a.B = batch;
+  a.target_items = target;
+  a.impl = ctx->impl;
+  a.bf16_history = bf16_history ? 1 : 0;
+  a.rot = layer_rot(ctx, layer);
+  const int grid = ctx->num_sms * ctx->ctas_per_sm;
+  return cuda_status(launch_decode(a, grid, (cudaStream_t)stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int oscar_version(void) { return VERSION; }
+
+const char* oscar_status_string(int s) {
+  switch (s) {
+    case OSCAR_OK: return "ok";
+    case OSCAR_ERR_INVALID_ARG: return "invalid argument";
+    case OSCAR_ERR_UNSUPPORTED: return "unsupported configuration";
+    case OSCAR_ERR_NO_PAGE: return "page-table entry is -1";
+    case OSCAR_ERR_RANGE: return "page id, length or scale out of range";
+    case OSCAR_ERR_TIMEOUT: return "bounded device wait ran out";
+    case OSCAR_ERR_CUDA: return "CUDA runtime error";
+    case OSCAR_ERR_STATE: return "cache state does not allow the call";
+    default: return "unknown status";
+  }
+}
+
+oscar_status oscar_layout(const oscar_config* cfg, oscar_layout_info* out) {
+  const oscar_status s = check_cfg(cfg);
+  if (s != OSCAR_OK) return s;
+  if (!out) return OSCAR_ERR_INVALID_ARG;
+  const int g = cfg->group_size;
+  const int G = cfg->num_q_heads / cfg->num_kv_heads;
+  out->int2_head_bytes = (size_t)int2_head_bytes(g);
+  out->int2_page_bytes = out->int2_head_bytes * cfg->num_kv_heads;
+  out->off_k_codes = 0;
+  out->off_v_codes = 2048;
+  out->off_k_sz = (size_t)off_k_sz();
+  out->off_v_sz = (size_t)off_v_sz(g);
+  out->bf16_head_bytes = BF16_HEAD_BYTES;
+  out->bf16_page_bytes = (size_t)BF16_HEAD_BYTES * cfg->num_kv_heads;
+  out->sink_bytes = (size_t)cfg->max_batch * cfg->num_kv_heads * SINK * D * 2;
+  out->ring_bytes = (size_t)cfg->max_batch * cfg->num_kv_heads * RECENT * D * 2;
+  out->decode_scratch_bytes = decode_scratch_bytes(cfg->max_batch, cfg->num_q_heads,
+                                                   cfg->num_kv_heads, G, MAX_TARGET_ITEMS);
+  return OSCAR_OK;
+}
+
+oscar_status oscar_create(const oscar_config* cfg, oscar_ctx** out) {
+  if (!out) return OSCAR_ERR_INVALID_ARG;
+  *out = nullptr;
+  const oscar_status s = check_cfg(cfg);
+  if (s != OSCAR_OK) return s;
+  oscar_ctx* ctx = new (std::nothrow) oscar_ctx();
+  if (!ctx) return OSCAR_ERR_INVALID_ARG;
+  ctx->cfg = *cfg;
+  ctx->G = cfg->num_q_heads / cfg->num_kv_heads;
+  ctx->NG = D / cfg->group_size;
+  ctx->mode.assign(cfg->num_layers, (int)OSCAR_ROT_NONE);
+  cudaError_t e = cudaGetDevice(&ctx->device);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device);
+  const size_t mat = (size_t)cfg->num_kv_heads * D * D;
+  const size_t rot_bytes = (size_t)cfg->num_layers * 3 * mat * sizeof(float);
+  const size_t clip_bytes = (size_t)cfg->num_layers * 2 * cfg->num_kv_heads * sizeof(float);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_rot, rot_bytes);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_clip, clip_bytes);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_err, sizeof(int));
+  if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_req_counter, sizeof(int) * cfg->max_batch);
+  if (e == cudaSuccess) e = cudaMemset(ctx->d_err, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(ctx->d_req_counter, 0, sizeof(int) * cfg->max_batch);
+  if (e == cudaSuccess) {
+    // identity rotation and clip 1.0 until oscar_set_rotation is called
+    std::vector<float> eye(3 * mat, 0.f);
+    for (int t = 0; t < 3; ++t)
+      for (int h = 0; h < cfg->num_kv_heads; ++h)
+        for (int i = 0; i < D; ++i) eye[t * mat + (size_t)h * D * D + (size_t)i * D + i] = 1.f;
+    for (int l = 0; l < cfg->num_layers && e == cudaSuccess; ++l)
+      e = cudaMemcpy(ctx->d_rot + (size_t)l * 3 * mat, eye.data(), 3 * mat * sizeof(float),
+                     cudaMemcpyHostToDevice);
+    std::vector<float> ones((size_t)cfg->num_layers * 2 * cfg->num_kv_heads, 1.f);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(ctx->d_clip, ones.data(), clip_bytes, cudaMemcpyHostToDevice);
+  }
+  if (e != cudaSuccess) {
+    oscar_destroy(ctx);
+    return OSCAR_ERR_CUDA;
+  }
+  *out = ctx;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_destroy(oscar_ctx* ctx) {
+  if (!ctx) return OSCAR_ERR_INVALID_ARG;
+  cudaDeviceSynchronize();
+  if (ctx->d_rot) cudaFree(ctx->d_rot);
+  if (ctx->d_clip) cudaFree(ctx->d_clip);
+  if (ctx->d_err) cudaFree(ctx->d_err);
+  if (ctx->d_req_counter) cudaFree(ctx->d_req_counter);
+  delete ctx;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_set_option(oscar_ctx* ctx, int option, int value) {
+  if (!ctx) return OSCAR_ERR_INVALID_ARG;
+  switch (option) {
+    case OSCAR_OPT_DECODE_IMPL:
+      if (value != 0 && value != 1) return OSCAR_ERR_INVALID_ARG;
+      ctx->impl = value;
+      return OSCAR_OK;
+    case OSCAR_OPT_CTAS_PER_SM:
+      if (value < 1 || value > 4) return OSCAR_ERR_INVALID_ARG;
+      ctx->ctas_per_sm = value;
+      return OSCAR_OK;
+    case OSCAR_OPT_ITEMS_PER_CTA:
+      if (value < 1 || value > 8) return OSCAR_ERR_INVALID_ARG;
+      ctx->items_per_cta = value;
+      return OSCAR_OK;
+    default:
+      return OSCAR_ERR_INVALID_ARG;
+  }
+}
+
+oscar_status oscar_set_rotation(oscar_ctx* ctx, int layer, const float* U_K, const float* U_V,
+                                const float* clip_k, const float* clip_v, int rot_mode,
+                                oscar_stream_t stream) {
+  if (!ctx || layer < 0 || layer >= ctx->cfg.num_layers || !clip_k || !clip_v)
+    return OSCAR_ERR_INVALID_ARG;
+  if (rot_mode != OSCAR_ROT_OSCAR && rot_mode != OSCAR_ROT_HADAMARD && rot_mode != OSCAR_ROT_NONE)
+    return OSCAR_ERR_INVALID_ARG;
+  if (rot_mode == OSCAR_ROT_OSCAR && (!U_K || !U_V)) return OSCAR_ERR_INVALID_ARG;
+  const int Hkv = ctx->cfg.num_kv_heads;
+  for (int h = 0; h < Hkv; ++h)
+    if (!(clip_k[h] > 0.f && clip_k[h] <= 1.f) || !(clip_v[h] > 0.f && clip_v[h] <= 1.f))
+      return OSCAR_ERR_INVALID_ARG;
+  const size_t mat = (size_t)Hkv * D * D;
+  std::vector<float> host(3 * mat, 0.f);
+  if (rot_mode == OSCAR_ROT_OSCAR) {
+    memcpy(host.data(), U_K, mat * sizeof(float));
+    memcpy(host.data() + mat, U_V, mat * sizeof(float));
+    for (int h = 0; h < Hkv; ++h)
+      for (int i = 0; i < D; ++i)
+        for (int j = 0; j < D; ++j)
+          host[2 * mat + (size_t)h * D * D + (size_t)j * D + i] = U_V[(size_t)h * D * D + (size_t)i * D + j];
+  } else {
+    for (int t = 0; t < 3; ++t)
+      for (int h = 0; h < Hkv; ++h)
+        for (int i = 0; i < D; ++i) host[t * mat + (size_t)h * D * D + (size_t)i * D + i] = 1.f;
+  }
+  std::vector<float> clips(2 * Hkv);
+  memcpy(clips.data(), clip_k, Hkv * sizeof(float));
+  memcpy(clips.data() + Hkv, clip_v, Hkv * sizeof(float));
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(ctx->d_rot + (size_t)layer * 3 * mat, host.data(),
+                                  3 * mat * sizeof(float), cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(ctx->d_clip + (size_t)layer * 2 * Hkv, clips.data(), 2 * Hkv * sizeof(float),
+                        cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return OSCAR_ERR_CUDA;
+  ctx->mode[layer] = rot_mode;
+  return OSCAR_OK;
+}
+
+static oscar_status append_common(oscar_ctx* ctx, int layer, const oscar_cache* cache,
+                                  const void* k, const void* v, int batch, oscar_stream_t stream,
+                                  int do_append) {
+  if (!ctx || !cache_ok(cache, true)) return OSCAR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
+  if (batch < 0 || batch > ctx->cfg.max_batch) return OSCAR_ERR_INVALID_ARG;
+  if (do_append && (!k || !v || !aligned(k, 16) || !aligned(v, 16))) return OSCAR_ERR_INVALID_ARG;
+  if (batch == 0) return OSCAR_OK;
+  const CacheView cv = make_view(ctx, cache, false);
+  return cuda_status(launch_append(cv, layer_rot(ctx, layer), (const __nv_bfloat16*)k,
+                                   (const __nv_bfloat16*)v, batch, do_append, ctx->d_req_counter,
+                                   (cudaStream_t)stream));
+}
+
+oscar_status oscar_append(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* k_new,
+                          const void* v_new, int batch, oscar_stream_t stream) {
+  return append_common(ctx, layer, cache, k_new, v_new, batch, stream, 1);
+}
+
+oscar_status oscar_demote(oscar_ctx* ctx, int layer, const oscar_cache* cache, int batch,
+                          oscar_stream_t stream) {
+  return append_common(ctx, layer, cache, nullptr, nullptr, batch, stream, 0);
+}
+
+static oscar_status import_common(oscar_ctx* ctx, int layer, const oscar_cache* cache,
+                                  const void* K, const void* V, int batch, int n,
+                                  oscar_stream_t stream, int bf16_history) {
+  if (!ctx || !cache_ok(cache, true) || !K || !V) return OSCAR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
+  if (batch < 0 || batch > ctx->cfg.max_batch || n < 0) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned(K, 16) || !aligned(V, 16)) return OSCAR_ERR_INVALID_ARG;
+  const long long hist = n > SINK + RECENT ? (long long)n - SINK - RECENT : 0;
+  if ((hist + PAGE - 1) / PAGE > ctx->cfg.max_pages_per_req) return OSCAR_ERR_INVALID_ARG;
+  if (batch == 0 || n == 0) return OSCAR_OK;
+  const CacheView cv = make_view(ctx, cache, bf16_history != 0);
+  return cuda_status(launch_import(cv, layer_rot(ctx, layer), (const __nv_bfloat16*)K,
+                                   (const __nv_bfloat16*)V, batch, n, bf16_history,
+                                   (cudaStream_t)stream));
+}
+
+oscar_status oscar_import_tokens(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* K,
+                                 const void* V, int batch, int n, oscar_stream_t stream) {
+  return import_common(ctx, layer, cache, K, V, batch, n, stream, 0);
+}
+
+oscar_status oscar_import_bf16_history(oscar_ctx* ctx, const oscar_cache* cache, const void* K,
+                                       const void* V, int batch, int n, oscar_stream_t stream) {
+  return import_common(ctx, 0, cache, K, V, batch, n, stream, 1);
+}
+
+oscar_status oscar_decode(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* q,
+                          void* out, float* lse, void* scratch, size_t scratch_bytes, int batch,
+                          oscar_stream_t stream) {
+  return decode_common(ctx, layer, cache, q, out, lse, scratch, scratch_bytes, batch, stream, false);
+}
+
+oscar_status oscar_decode_bf16_history(oscar_ctx* ctx, const oscar_cache* cache, const void* q,
+                                       void* out, float* lse, void* scratch, size_t scratch_bytes,
+                                       int batch, oscar_stream_t stream) {
+  return decode_common(ctx, 0, cache, q, out, lse, scratch, scratch_bytes, batch, stream, true);
+}
+
+oscar_status oscar_quantize_rotated_f32(const float* x, int n, int group_size, float clip,
+                                        int which, uint8_t* codes, void* sz,
+                                        oscar_stream_t stream) {
+  if (!x || !codes || !sz || n < 0) return OSCAR_ERR_INVALID_ARG;
+  if (group_size != 32 && group_size != 64 && group_size != 128) return OSCAR_ERR_UNSUPPORTED;
+  if (which != 0 && which != 1) return OSCAR_ERR_INVALID_ARG;
+  if (which == 1 && (n % PAGE)) return OSCAR_ERR_INVALID_ARG;
+  if (!(clip > 0.f && clip <= 1.f)) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(sz, 4)) return OSCAR_ERR_INVALID_ARG;
+  if (n == 0) return OSCAR_OK;
+  return cuda_status(
+      launch_quantize_hook(x, n, group_size, clip, which, codes, (__half2*)sz, (cudaStream_t)stream));
+}
+
+oscar_status oscar_debug_rotate(oscar_ctx* ctx, int layer, int which, int kv_head, const void* x,
+                                float* x_rot, int n, oscar_stream_t stream) {
+  if (!ctx || !x || !x_rot || n < 0 || (which != 0 && which != 1)) return OSCAR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
+  if (kv_head < 0 || kv_head >= ctx->cfg.num_kv_heads) return OSCAR_ERR_INVALID_ARG;
+  if (n == 0) return OSCAR_OK;
+  const LayerRot r = layer_rot(ctx, layer);
+  const float* U = (which == 0 ? r.U_K : r.U_V) + (size_t)kv_head * D * D;
+  return cuda_status(launch_debug_rotate(U, r.mode, (const __nv_bfloat16*)x, x_rot, n,
+                                         (cudaStream_t)stream));
+}
+
+oscar_status oscar_get_error(oscar_ctx* ctx, oscar_stream_t stream, int* code) {
+  if (!ctx || !code) return OSCAR_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  int h = 0;
+  cudaError_t e = cudaMemcpyAsync(&h, ctx->d_err, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d_err, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return OSCAR_ERR_CUDA;
+  *code = h;
+  return OSCAR_OK;
+}
+
+}  // extern "C"

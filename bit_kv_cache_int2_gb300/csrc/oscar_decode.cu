@@ -1,0 +1,929 @@
+// Decode attention over the three-region INT2 KV cache (sm_103a).
+//
+// Follows the decode paragraph under the pipeline figure "从离线校准到在线推理的
+// pipeline" of "超越TurboQuant：Together AI把2-bit KV Cache推向真实服务": the INT2
+// segment is unpacked, dequantised with its scale / zero point and accumulated
+// in floating point; the BF16 sink/recent segment is handled separately; the
+// parts are merged by online softmax.  Keys and values of the history live in
+// the rotated basis x' = x·R [News "Together AI 开源 OSCAR…", section "OSCAR 的
+// 不同之处"], so the query is rotated by R_K first and the history output is
+// un-rotated by R_V^T before the final merge.
+//
+// Kernels (one stream, in order):
+//   prep_kernel      q' = q·U_K·H·P_br for every query head; resets the work counter
+//   decode_kernel    persistent split-K: work items are (request, kv head, S pages)
+//                    of INT2 (or BF16) history, or one BF16 window per (request,
+//                    kv head); each item writes an online-softmax partial
+//   merge_kernel     per (request, kv head): LSE-merge of the history partials,
+//                    un-rotation by R_V^T, LSE-merge with the window partial
+#include "oscar_internal.cuh"
+
+namespace oscar {
+
+namespace {
+
+constexpr int NW = 4;     // warps per decode CTA
+constexpr int DEPTH = 4;  // bulk-copy stages per warp
+
+// ------------------------------------------------------------------- prep
+// grid = B * Hkv (INT2) or 1 (BF16 history), block 128.
+__global__ void __launch_bounds__(128) prep_kernel(const __nv_bfloat16* __restrict__ q, float* qrot,
+                                                   int* counter, LayerRot rot, int Hq, int Hkv,
+                                                   int G, int do_rotate) {
+  __shared__ float xs[D];
+  __shared__ float tmp[D];
+  if (blockIdx.x == 0 && threadIdx.x == 0) *counter = 0;
+  if (!do_rotate) return;
+  const int b = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv, j = threadIdx.x;
+  const float* U = rot.U_K + (size_t)kvh * D * D;
+  for (int n = 0; n < G; ++n) {
+    const size_t row = (size_t)b * Hq + kvh * G + n;
+    xs[j] = __bfloat162float(q[row * D + j]);
+    __syncthreads();
+    qrot[row * D + j] = rotate128(xs, U, rot.mode, j, tmp, 1);
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------ smem layout
+struct SmemLayout {
+  int stage_bytes;   // per stage
+  int off_stage, off_mbar, off_qb, off_consts, off_qf, off_vs, off_pre, off_red, off_misc, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int head_bytes, int B, int impl) {
+  SmemLayout L;
+  L.stage_bytes = (head_bytes + 127) & ~127;
+  int o = 0;
+  L.off_stage = o;
+  int stage_total = NW * DEPTH * L.stage_bytes;
+  const int wo_bytes = NW * MAX_G * D * 4 + 2 * NW * MAX_G * 4;  // warp results alias the stages
+  if (stage_total < wo_bytes) stage_total = wo_bytes;
+  o += stage_total;
+  L.off_mbar = o;
+  o += NW * DEPTH * 8;
+  L.off_qb = o;
+  o += MAX_G * D * 2;  // f16 B operand
+  L.off_consts = o;
+  o += MAX_G * (1 + 4 + 4) * 4;
+  L.off_qf = o;
+  if (impl == 1) o += MAX_G * D * 4;  // fp32 q' (CUDA-core path, storage order)
+  L.off_vs = o;
+  if (impl == 1) o += NW * (MAX_G * PAGE + 2 * 4 * PAGE) * 4;  // CUDA-core per-warp p and s/z
+  L.off_pre = o;
+  o += ((B + 1) * 4 + 15) & ~15;
+  L.off_red = o;
+  o += 64 * 4;
+  L.off_misc = o;
+  o += 16;
+  L.total = o;
+  return L;
+}
+
+// ------------------------------------------------- per-warp decode state
+template <int NG>
+struct Int2State {
+  float oacc[8][4];  // o'^T: m-tile j, rows channels 16j+gid / 16j+8+gid, cols heads 2tq, 2tq+1
+  float m[2];        // running max (log2 units) of heads 2tq, 2tq+1
+  float l[2];        // this thread's part of the running sum
+  float bs[2][NG];   // this thread's part of sum of B_V values (offset removal)
+  float zs[2][NG];   // this thread's part of sum p * z_v
+  uint32_t bq[8][2];  // q' B fragments (column = head gid)
+  float ka[2];        // logit scale per column head
+  float kb[2][NG];    // logit offset per column head and group
+  float kg[2][NG];    // z-term weight per column head and group
+};
+
+// One INT2 page (64 tokens) of one kv head on tensor cores.  stage: the page's
+// head block in smem; nv: valid tokens.
+template <int NG>
+__device__ __forceinline__ void int2_page_mma(Int2State<NG>& S, const uint8_t* stage, int nv,
+                                              int lane) {
+  const int gid = lane >> 2, tq = lane & 3;
+  constexpr int KPG = 8 / NG;   // k-steps per group (QK)
+  constexpr int MPG = 8 / NG;   // m-tiles per group (SV)
+  const uint8_t* kc = stage;
+  const uint8_t* vc = stage + 2048;
+  const __half2* ksz = (const __half2*)(stage + 4096);
+  const __half2* vsz = (const __half2*)(stage + 4096 + PAGE * NG * 4);
+
+  float lam[4][4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int ta = 16 * s + gid, tb = ta + 8;
+    const uint2 wa = *(const uint2*)(kc + ta * 32 + 8 * tq);
+    const uint2 wb = *(const uint2*)(kc + tb * 32 + 8 * tq);
+    float acc[NG][4];
+#pragma unroll
+    for (int gr = 0; gr < NG; ++gr) acc[gr][0] = acc[gr][1] = acc[gr][2] = acc[gr][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t xa = kk < 4 ? wa.x : wa.y;
+      const uint32_t xb = kk < 4 ? wb.x : wb.y;
+      uint32_t a0, a1, a2, a3;
+      switch (kk & 3) {
+        case 0: a0 = code_pair<0>(xa); a1 = code_pair<0>(xb); a2 = code_pair<1>(xa); a3 = code_pair<1>(xb); break;
+        case 1: a0 = code_pair<2>(xa); a1 = code_pair<2>(xb); a2 = code_pair<3>(xa); a3 = code_pair<3>(xb); break;
+        case 2: a0 = code_pair<4>(xa); a1 = code_pair<4>(xb); a2 = code_pair<5>(xa); a3 = code_pair<5>(xb); break;
+        default: a0 = code_pair<6>(xa); a1 = code_pair<6>(xb); a2 = code_pair<7>(xa); a3 = code_pair<7>(xb); break;
+      }
+      mma_f16(acc[kk / KPG], a0, a1, a2, a3, S.bq[kk][0], S.bq[kk][1]);
+    }
+    // logits (log2 units): sum_gr s*(acc*alpha + beta) + z*gamma
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int row = e < 2 ? ta : tb;
+      const int hc = e & 1;
+      float v = 0.f;
+#pragma unroll
+      for (int gr = 0; gr < NG; ++gr) {
+        const float2 sz = __half22float2(ksz[row * NG + gr]);
+        v = fmaf(sz.x, fmaf(acc[gr][e], S.ka[hc], S.kb[hc][gr]), fmaf(sz.y, S.kg[hc][gr], v));
+      }
+      lam[s][e] = row < nv ? v : -INFINITY;
+    }
+  }
+  // page max per column head, over all 64 tokens
+  float pm[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int s = 0; s < 4; ++s)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pm[e & 1] = fmaxf(pm[e & 1], lam[s][e]);
+#pragma unroll
+  for (int hc = 0; hc < 2; ++hc) {
+    pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 4));
+    pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 8));
+    pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 16));
+    const float mn = fmaxf(S.m[hc], pm[hc]);
+    const float al = ex2(S.m[hc] - mn);
+    S.m[hc] = mn;
+    S.l[hc] *= al;
+#pragma unroll
+    for (int gr = 0; gr < NG; ++gr) {
+      S.bs[hc][gr] *= al;
+      S.zs[hc][gr] *= al;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      S.oacc[j][hc] *= al;
+      S.oacc[j][hc + 2] *= al;
+    }
+  }
+  // V code words: rows 16j+gid and 16j+8+gid, word tq (all 4 tiles)
+  uint32_t vw[8][2];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    vw[j][0] = *(const uint32_t*)(vc + (16 * j + gid) * 16 + 4 * tq);
+    vw[j][1] = *(const uint32_t*)(vc + (16 * j + 8 + gid) * 16 + 4 * tq);
+  }
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int ta = 16 * s + gid, tb = ta + 8;
+    const bool va = ta < nv, vb = tb < nv;
+    float p[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      p[e] = ex2(lam[s][e] - S.m[e & 1]);
+      S.l[e & 1] += p[e];
+    }
+    // scale of the code's bit position: rows < 8 use bit pair 2s, rows >= 8 use 2s+1
+    const float fa = (float)(1 << (8 - code_exp_rt(2 * s)));
+    const float fb = (float)(1 << (8 - code_exp_rt(2 * s + 1)));
+#pragma unroll
+    for (int gr = 0; gr < NG; ++gr) {
+      const float2 sa = __half22float2(vsz[ta * NG + gr]);
+      const float2 sb = __half22float2(vsz[tb * NG + gr]);
+      const float s_a = va ? sa.x * fa : 0.f, z_a = va ? sa.y : 0.f;
+      const float s_b = vb ? sb.x * fb : 0.f, z_b = vb ? sb.y : 0.f;
+      const __half2 h0 = __floats2half2_rn(p[0] * s_a, p[1] * s_a);
+      const __half2 h1 = __floats2half2_rn(p[2] * s_b, p[3] * s_b);
+      const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+      S.bs[0][gr] += f0.x + f1.x;
+      S.bs[1][gr] += f0.y + f1.y;
+      S.zs[0][gr] = fmaf(p[0], z_a, fmaf(p[2], z_b, S.zs[0][gr]));
+      S.zs[1][gr] = fmaf(p[1], z_a, fmaf(p[3], z_b, S.zs[1][gr]));
+      const uint32_t b0 = movmatrix_t(*(const uint32_t*)&h0);
+      const uint32_t b1 = movmatrix_t(*(const uint32_t*)&h1);
+#pragma unroll
+      for (int jj = 0; jj < MPG; ++jj) {
+        const int j = gr * MPG + jj;
+        uint32_t a0, a1, a2, a3;
+        switch (s) {
+          case 0: a0 = code_pair<0>(vw[j][0]); a1 = code_pair<0>(vw[j][1]); a2 = code_pair<1>(vw[j][0]); a3 = code_pair<1>(vw[j][1]); break;
+          case 1: a0 = code_pair<2>(vw[j][0]); a1 = code_pair<2>(vw[j][1]); a2 = code_pair<3>(vw[j][0]); a3 = code_pair<3>(vw[j][1]); break;
+          case 2: a0 = code_pair<4>(vw[j][0]); a1 = code_pair<4>(vw[j][1]); a2 = code_pair<5>(vw[j][0]); a3 = code_pair<5>(vw[j][1]); break;
+          default: a0 = code_pair<6>(vw[j][0]); a1 = code_pair<6>(vw[j][1]); a2 = code_pair<7>(vw[j][0]); a3 = code_pair<7>(vw[j][1]); break;
+        }
+        mma_f16(S.oacc[j], a0, a1, a2, a3, b0, b1);
+      }
+    }
+  }
+}
+
+// ----------------------------------------------- CUDA-core INT2 page (fp32)
+// Lane l scores tokens l and l+32, then accumulates channels 4l..4l+3.
+struct CoreState {
+  float o[MAX_G][4];
+  float m[MAX_G];
+  float l[MAX_G];
+};
+
+template <int NG>
+__device__ __forceinline__ void int2_page_core(CoreState& S, const uint8_t* stage, int nv, int lane,
+                                               int G, const float* qst /*[G][128] storage order*/,
+                                               const float* kgm /*[MAX_G][4] z weights, log2 units*/,
+                                               float* ps /*[G][64]*/,
+                                               float* vsz_s /*[2][NG][64]*/) {
+  const uint32_t* kc = (const uint32_t*)stage;
+  const uint32_t* vc = (const uint32_t*)(stage + 2048);
+  const __half2* ksz = (const __half2*)(stage + 4096);
+  const __half2* vsz = (const __half2*)(stage + 4096 + PAGE * NG * 4);
+  const float cst = LOG2E * INV_SQRT_D;
+  float lam[2][MAX_G];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int t = lane + 32 * r;
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = kc[t * 8 + k];
+    for (int n = 0; n < G; ++n) {
+      float acc[NG];
+#pragma unroll
+      for (int gr = 0; gr < NG; ++gr) acc[gr] = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+#pragma unroll
+        for (int pos = 0; pos < 16; ++pos) {
+          // storage slot (word k, bit 2*pos) holds channel 64A+16B+8C+2D+E with
+          // k = 2D+A, pos = 8E+2B+C; its group is channel / g
+          const int A = k & 1, B = (pos >> 1) & 3;
+          const int gr = NG == 1 ? 0 : NG == 2 ? A : (2 * A + (B >> 1));
+          const float code = (float)((w[k] >> (2 * pos)) & 3u);
+          acc[gr] = fmaf(code, qst[n * D + k * 16 + pos], acc[gr]);
+        }
+      }
+      float v = 0.f;
+#pragma unroll
+      for (int gr = 0; gr < NG; ++gr) {
+        const float2 sz = __half22float2(ksz[t * NG + gr]);
+        v = fmaf(sz.x, acc[gr] * cst, fmaf(sz.y, kgm[n * 4 + gr], v));
+      }
+      lam[r][n] = t < nv ? v : -INFINITY;
+    }
+  }
+  // V scale / zero of the page into smem (select out invalid tokens)
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int t = lane + 32 * r;
+    for (int gr = 0; gr < NG; ++gr) {
+      const float2 sz = __half22float2(vsz[t * NG + gr]);
+      vsz_s[gr * PAGE + t] = t < nv ? sz.x : 0.f;
+      vsz_s[(NG + gr) * PAGE + t] = t < nv ? sz.y : 0.f;
+    }
+  }
+  for (int n = 0; n < G; ++n) {
+    float pm = fmaxf(lam[0][n], lam[1][n]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, o));
+    const float mn = fmaxf(S.m[n], pm);
+    const float al = ex2(S.m[n] - mn);
+    S.m[n] = mn;
+    const float p0 = ex2(lam[0][n] - mn), p1 = ex2(lam[1][n] - mn);
+    float ls = p0 + p1;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+    S.l[n] = S.l[n] * al + ls;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) S.o[n][c] *= al;
+    ps[n * PAGE + lane] = p0;
+    ps[n * PAGE + lane + 32] = p1;
+  }
+  __syncwarp();
+  // channels 4*lane .. 4*lane+3 (one group)
+  const int gr = (4 * lane) / (D / NG);
+  uint32_t rows[4][4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) rows[c][k] = vc[(4 * lane + c) * 4 + k];
+  for (int t = 0; t < PAGE; ++t) {
+    const int wsel = v_word(t), sh = v_bit(t);
+    const float s = vsz_s[gr * PAGE + t], z = vsz_s[(NG + gr) * PAGE + t];
+    float vh[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t word = rows[c][0];
+      word = wsel == 1 ? rows[c][1] : word;
+      word = wsel == 2 ? rows[c][2] : word;
+      word = wsel == 3 ? rows[c][3] : word;
+      vh[c] = fmaf((float)((word >> sh) & 3u), s, z);
+    }
+    for (int n = 0; n < G; ++n) {
+      const float p = ps[n * PAGE + t];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) S.o[n][c] = fmaf(p, vh[c], S.o[n][c]);
+    }
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------ BF16 chunk (mma)
+struct Bf16State {
+  float oacc[8][4];  // o^T: m-tile j rows channel 16gid+2j / 16gid+2j+1, cols heads 2tq, 2tq+1
+  float m[2];
+  float l[2];
+  uint32_t bq[8][2];  // raw q (bf16) B fragments, column = head gid
+};
+
+__device__ __forceinline__ uint4 ldg_nc(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// 64 tokens of BF16 keys/values, row-major [64][128] at Kb / Vb; token t is
+// used iff bit t of `valid` is set.
+__device__ __forceinline__ void bf16_chunk_mma(Bf16State& S, const __nv_bfloat16* Kb,
+                                               const __nv_bfloat16* Vb, uint64_t valid, int lane) {
+  const int gid = lane >> 2, tq = lane & 3;
+  const float cst = LOG2E * INV_SQRT_D;
+  float lam[4][4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int ta = 16 * s + gid, tb = ta + 8;
+    uint4 ka[4], kb[4];
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd) {
+      ka[qd] = ldg_nc(Kb + ta * D + 32 * tq + 8 * qd);
+      kb[qd] = ldg_nc(Kb + tb * D + 32 * tq + 8 * qd);
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint4& xa = ka[kk >> 1];
+      const uint4& xb = kb[kk >> 1];
+      const uint32_t a0 = (kk & 1) ? xa.z : xa.x, a2 = (kk & 1) ? xa.w : xa.y;
+      const uint32_t a1 = (kk & 1) ? xb.z : xb.x, a3 = (kk & 1) ? xb.w : xb.y;
+      mma_bf16(acc, a0, a1, a2, a3, S.bq[kk][0], S.bq[kk][1]);
+    }
+    const bool va = (valid >> ta) & 1, vb = (valid >> tb) & 1;
+    lam[s][0] = va ? acc[0] * cst : -INFINITY;
+    lam[s][1] = va ? acc[1] * cst : -INFINITY;
+    lam[s][2] = vb ? acc[2] * cst : -INFINITY;
+    lam[s][3] = vb ? acc[3] * cst : -INFINITY;
+  }
+  float pm[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int s = 0; s < 4; ++s)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pm[e & 1] = fmaxf(pm[e & 1], lam[s][e]);
+#pragma unroll
+  for (int hc = 0; hc < 2; ++hc) {
+    pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 4));
+    pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 8));
+    pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 16));
+    const float mn = fmaxf(S.m[hc], pm[hc]);
+    const float al = ex2(S.m[hc] - mn);
+    S.m[hc] = mn;
+    S.l[hc] *= al;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      S.oacc[j][hc] *= al;
+      S.oacc[j][hc + 2] *= al;
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    float p[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) p[e] = ex2(lam[s][e] - S.m[e & 1]);
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(p[0], p[1]);
+    const __nv_bfloat162 h1 = __floats2bfloat162_rn(p[2], p[3]);
+    const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+    S.l[0] += f0.x + f1.x;
+    S.l[1] += f0.y + f1.y;
+    const uint32_t b0 = movmatrix_t(*(const uint32_t*)&h0);
+    const uint32_t b1 = movmatrix_t(*(const uint32_t*)&h1);
+    // V rows of the 4 tokens of this thread's k-slots, channels 16gid..16gid+15
+    const int t0 = 16 * s + 2 * tq, t2 = t0 + 8;
+    const int tk[4] = {t0, t0 + 1, t2, t2 + 1};
+    uint4 vv[4][2];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool ok = (valid >> tk[u]) & 1;
+      const __nv_bfloat16* src = Vb + tk[u] * D + 16 * gid;
+      vv[u][0] = ok ? ldg_nc(src) : make_uint4(0, 0, 0, 0);
+      vv[u][1] = ok ? ldg_nc(src + 8) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t* w0 = (const uint32_t*)&vv[0][j >> 2];
+      const uint32_t* w1 = (const uint32_t*)&vv[1][j >> 2];
+      const uint32_t* w2 = (const uint32_t*)&vv[2][j >> 2];
+      const uint32_t* w3 = (const uint32_t*)&vv[3][j >> 2];
+      const uint32_t x0 = w0[j & 3], x1 = w1[j & 3], x2 = w2[j & 3], x3 = w3[j & 3];
+      mma_bf16(S.oacc[j], prmt(x0, x1, 0x5410), prmt(x0, x1, 0x7632), prmt(x2, x3, 0x5410),
+               prmt(x2, x3, 0x7632), b0, b1);
+    }
+  }
+}
+
+// ----------------------------------------------------------------- decode
+struct ItemCtx {
+  int b, kvh, slot;
+};
+
+__device__ __forceinline__ void cta_combine_write(const DecodeArgs& a, uint8_t* smem,
+                                                 const SmemLayout& L, int slot) {
+  // warp results: wm[NW][MAX_G], wl[NW][MAX_G], wo[NW][MAX_G][D] aliased on the stages
+  float* wm = (float*)(smem + L.off_stage);
+  float* wl = wm + NW * MAX_G;
+  float* wo = wl + NW * MAX_G;
+  const int c = threadIdx.x;  // NW * 32 == 128 threads, one channel each
+  const int G = a.cv.G;
+  for (int n = 0; n < G; ++n) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, wm[w * MAX_G + n]);
+    float Ls = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float mw = wm[w * MAX_G + n];
+        const float f = mw == -INFINITY ? 0.f : ex2(mw - M);
+        Ls = fmaf(wl[w * MAX_G + n], f, Ls);
+        O = fmaf(wo[(w * MAX_G + n) * D + c], f, O);
+      }
+    }
+    float* rec = a.part + ((size_t)slot * G + n) * PART_STRIDE;
+    if (c == 0) {
+      rec[0] = M;
+      rec[1] = Ls;
+    }
+    rec[2 + c] = O;
+  }
+}
+
+template <int NG, int IMPL>
+__global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const CacheView& cv = a.cv;
+  const SmemLayout L = smem_layout(cv.head_bytes, a.B, IMPL);
+  uint64_t* mbar = (uint64_t*)(smem + L.off_mbar);
+  __half* qb = (__half*)(smem + L.off_qb);
+  float* kconst = (float*)(smem + L.off_consts);  // [MAX_G] alpha, [MAX_G][4] beta, [MAX_G][4] gamma
+  float* qf = (float*)(smem + L.off_qf);
+  float* vsw = (float*)(smem + L.off_vs);
+  int* pre = (int*)(smem + L.off_pre);
+  int* red = (int*)(smem + L.off_red);
+  int* misc = (int*)(smem + L.off_misc);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tq = lane & 3;
+  const int G = cv.G, Hkv = cv.Hkv;
+
+  if (threadIdx.x < NW * DEPTH) mbar_init(&mbar[threadIdx.x], 1);
+  if (threadIdx.x == 0) misc[1] = 0;
+  fence_proxy_async();
+  __syncthreads();
+
+  const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
+  const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, unit, pre, red);
+  const int total = sc.n_hist + sc.n_win;
+  uint32_t seq = 0;  // stages consumed by this warp so far
+
+  float* wm = (float*)(smem + L.off_stage);
+  float* wl = wm + NW * MAX_G;
+  float* wo = wl + NW * MAX_G;
+
+  for (;;) {
+    if (threadIdx.x == 0) misc[0] = atomicAdd(a.counter, 1);
+    __syncthreads();
+    const int it = misc[0];
+    __syncthreads();
+    if (it >= total) break;
+    bool is_win;
+    int idx;
+    if (sc.win_first) {
+      is_win = it < sc.n_win;
+      idx = is_win ? it : it - sc.n_win;
+    } else {
+      is_win = it >= sc.n_hist;
+      idx = is_win ? it - sc.n_hist : it;
+    }
+    int b, kvh, jj = 0, slot;
+    if (is_win) {
+      b = idx / Hkv;
+      kvh = idx % Hkv;
+      slot = sc.n_hist + idx;
+    } else {
+      hist_item_coords(idx, pre, a.B, Hkv, cv.hist_lens, sc.S, b, kvh, jj);
+      slot = idx;
+    }
+    const int hist_b = cv.hist_lens[b];
+    const int pages_b = (hist_b + PAGE - 1) / PAGE;
+
+    if (is_win || a.bf16_history) {
+      // ---------------------------------------------------- BF16 tokens
+      Bf16State S;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) S.oacc[j][0] = S.oacc[j][1] = S.oacc[j][2] = S.oacc[j][3] = 0.f;
+      S.m[0] = S.m[1] = -INFINITY;
+      S.l[0] = S.l[1] = 0.f;
+      {
+        const bool hv = gid < G;
+        const __nv_bfloat16* qrow = a.q + ((size_t)b * cv.Hq + kvh * G + (hv ? gid : 0)) * D + 32 * tq;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          S.bq[kk][0] = hv ? *(const uint32_t*)(qrow + 4 * kk) : 0u;
+          S.bq[kk][1] = hv ? *(const uint32_t*)(qrow + 4 * kk + 2) : 0u;
+        }
+      }
+      const size_t head = (size_t)b * Hkv + kvh;
+      if (is_win) {
+        const int Lq = cv.seq_lens[b];
+        const int nsink = Lq < SINK ? Lq : SINK;
+        const int recent = Lq > SINK ? Lq - SINK - hist_b : 0;
+        const int h0 = hist_b % RECENT;
+        for (int ch = warp; ch < 5; ch += NW) {
+          uint64_t valid = 0;
+          const __nv_bfloat16 *Kb, *Vb;
+          if (ch == 0) {
+            valid = nsink >= 64 ? ~0ull : ((1ull << nsink) - 1ull);
+            Kb = cv.sink_k + head * SINK * D;
+            Vb = cv.sink_v + head * SINK * D;
+          } else {
+            for (int t = 0; t < 64; ++t) {
+              const int slot_r = 64 * (ch - 1) + t;
+              if (((slot_r - h0 + RECENT) % RECENT) < recent) valid |= 1ull << t;
+            }
+            Kb = cv.ring_k + (head * RECENT + 64 * (ch - 1)) * D;
+            Vb = cv.ring_v + (head * RECENT + 64 * (ch - 1)) * D;
+          }
+          if (valid) bf16_chunk_mma(S, Kb, Vb, valid, lane);
+        }
+      } else {
+        const int p0 = jj * sc.S;
+        int p1 = p0 + sc.S;
+        if (p1 > pages_b) p1 = pages_b;
+        for (int p = p0 + warp; p < p1; p += NW) {
+          const int pid = cv.page_table[(size_t)b * cv.max_pages_per_req + p];
+          if (pid < 0 || pid >= cv.num_pages) {
+            if (lane == 0) record_error(cv.err, pid < 0 ? OSCAR_ERR_NO_PAGE : OSCAR_ERR_RANGE);
+            continue;
+          }
+          const int nv = (p == pages_b - 1) ? hist_b - p * PAGE : PAGE;
+          const uint64_t valid = nv >= 64 ? ~0ull : ((1ull << nv) - 1ull);
+          const __nv_bfloat16* Kb =
+              (const __nv_bfloat16*)(cv.pool + (size_t)pid * cv.page_bytes + (size_t)kvh * BF16_HEAD_BYTES);
+          bf16_chunk_mma(S, Kb, Kb + PAGE * D, valid, lane);
+        }
+      }
+      // finalize this warp
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 4);
+        S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 8);
+        S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 16);
+      }
+      __syncthreads();  // everyone is done with the previous item's results
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        const int n = 2 * tq + hc;
+        if (n < G) {
+          if (gid == 0) {
+            wm[warp * MAX_G + n] = S.m[hc];
+            wl[warp * MAX_G + n] = S.l[hc];
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            wo[(warp * MAX_G + n) * D + 16 * gid + 2 * j] = S.oacc[j][hc];
+            wo[(warp * MAX_G + n) * D + 16 * gid + 2 * j + 1] = S.oacc[j][hc + 2];
+          }
+        }
+      }
+      __syncthreads();
+      cta_combine_write(a, smem, L, slot);
+      __syncthreads();
+      continue;
+    }
+
+    // -------------------------------------------------------- INT2 history
+    // Prologue (whole CTA): fp16 B operand of q' and the logit constants.
+    {
+      const int c = threadIdx.x;  // channel
+      const int i = 2 * ((c >> 4) & 3) + ((c >> 3) & 1);  // bit pair holding channel c in QK
+      const float f = (float)(1 << (8 - code_exp_rt(i)));
+      float* ka = kconst;
+      float* kb = kconst + MAX_G;
+      float* kgm = kconst + MAX_G * 5;
+      for (int n = 0; n < MAX_G; ++n) {
+        float qv = 0.f;
+        if (n < G) qv = a.qrot[((size_t)b * cv.Hq + kvh * G + n) * D + c];
+        float am = fabsf(qv);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        if (lane == 0) ((float*)red)[warp] = am;
+        __syncthreads();
+        am = fmaxf(fmaxf(((float*)red)[0], ((float*)red)[1]), fmaxf(((float*)red)[2], ((float*)red)[3]));
+        int ex = 0;
+        frexpf(am, &ex);
+        const int sig = am > 0.f ? ex - 10 : 0;  // |q'| * 16 * 2^-sig < 2^14
+        const __half hb = __float2half_rn(ldexpf(qv, -sig) * f);
+        qb[n * D + c] = hb;
+        if (IMPL == 1) {
+          // CUDA-core path: q' in K storage order (word k_word(c), pos k_bit(c)/2)
+          qf[n * D + k_word(c) * 16 + k_bit(c) / 2] = qv;
+        }
+        // group sums of the B values and of q'
+        float bsv = __half2float(hb), qsv = qv;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          bsv += __shfl_xor_sync(0xffffffffu, bsv, o);
+          qsv += __shfl_xor_sync(0xffffffffu, qsv, o);
+        }
+        __syncthreads();
+        if (lane == 0) {
+          ((float*)red)[warp] = bsv;
+          ((float*)red)[4 + warp] = qsv;
+        }
+        __syncthreads();
+        if (threadIdx.x < NG) {
+          const int gr = threadIdx.x, wpg = NW / NG;
+          float bsum = 0.f, qsum = 0.f;
+          for (int w = gr * wpg; w < (gr + 1) * wpg; ++w) {
+            bsum += ((float*)red)[w];
+            qsum += ((float*)red)[4 + w];
+          }
+          const float alpha = ldexpf(1.f, sig) * LOG2E * INV_SQRT_D * (1.f / 256.f);
+          if (gr == 0) ka[n] = n < G ? alpha : 0.f;
+          kb[n * 4 + gr] = n < G ? -1024.f * bsum * alpha : 0.f;
+          kgm[n * 4 + gr] = n < G ? qsum * LOG2E * INV_SQRT_D : 0.f;
+        }
+        __syncthreads();
+      }
+    }
+    // pages of this item, dealt round-robin to the warps
+    const int p0 = jj * sc.S;
+    int p1 = p0 + sc.S;
+    if (p1 > pages_b) p1 = pages_b;
+    const int nw_pages = (p1 - p0 - warp + NW - 1) / NW > 0 ? (p1 - p0 - warp + NW - 1) / NW : 0;
+    uint8_t* my_stage = smem + L.off_stage + (size_t)warp * DEPTH * L.stage_bytes;
+    uint64_t* my_bar = mbar + warp * DEPTH;
+    auto issue = [&](int k) {  // lane 0 only: k-th page of this warp
+      const int p = p0 + warp + k * NW;
+      const int st = (int)((seq + k) % DEPTH);
+      const int pid = cv.page_table[(size_t)b * cv.max_pages_per_req + p];
+      if (pid >= 0 && pid < cv.num_pages) {
+        mbar_expect_tx(&my_bar[st], (uint32_t)cv.head_bytes);
+        bulk_g2s(my_stage + (size_t)st * L.stage_bytes,
+                 cv.pool + (size_t)pid * cv.page_bytes + (size_t)kvh * cv.head_bytes,
+                 (uint32_t)cv.head_bytes, &my_bar[st]);
+      } else {
+        record_error(cv.err, pid < 0 ? OSCAR_ERR_NO_PAGE : OSCAR_ERR_RANGE);
+        mbar_expect_tx(&my_bar[st], 0u);
+      }
+    };
+    if (lane == 0) {
+      fence_proxy_async();
+      for (int k = 0; k < DEPTH && k < nw_pages; ++k) issue(k);
+    }
+
+    bool timed_out = false;
+    int k_fail = 0;
+    if (IMPL == 0) {
+      Int2State<NG> S;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) S.oacc[j][0] = S.oacc[j][1] = S.oacc[j][2] = S.oacc[j][3] = 0.f;
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        S.m[hc] = -INFINITY;
+        S.l[hc] = 0.f;
+        const int n = 2 * tq + hc;
+        S.ka[hc] = kconst[n];
+#pragma unroll
+        for (int gr = 0; gr < NG; ++gr) {
+          S.bs[hc][gr] = 0.f;
+          S.zs[hc][gr] = 0.f;
+          S.kb[hc][gr] = kconst[MAX_G + n * 4 + gr];
+          S.kg[hc][gr] = kconst[MAX_G * 5 + n * 4 + gr];
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        S.bq[kk][0] = *(const uint32_t*)(qb + gid * D + 16 * kk + 2 * tq);
+        S.bq[kk][1] = *(const uint32_t*)(qb + gid * D + 16 * kk + 8 + 2 * tq);
+      }
+      for (int k = 0; k < nw_pages; ++k) {
+        const int st = (int)((seq + k) % DEPTH);
+        const uint32_t ph = ((seq + k) / DEPTH) & 1u;
+        if (!mbar_wait(&my_bar[st], ph)) {
+          timed_out = true;
+          k_fail = k;
+          break;
+        }
+        const int p = p0 + warp + k * NW;
+        const int pid = cv.page_table[(size_t)b * cv.max_pages_per_req + p];
+        if (pid >= 0 && pid < cv.num_pages) {
+          const int nv = (p == pages_b - 1) ? hist_b - p * PAGE : PAGE;
+          int2_page_mma<NG>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
+        }
+        __syncwarp();
+        if (lane == 0 && k + DEPTH < nw_pages) {
+          fence_proxy_async();
+          issue(k + DEPTH);
+        }
+      }
+      // finalize: reduce the thread parts over the 8 row groups
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], o);
+#pragma unroll
+          for (int gr = 0; gr < NG; ++gr) {
+            S.bs[hc][gr] += __shfl_xor_sync(0xffffffffu, S.bs[hc][gr], o);
+            S.zs[hc][gr] += __shfl_xor_sync(0xffffffffu, S.zs[hc][gr], o);
+          }
+        }
+      }
+      __syncthreads();  // all warps are past their stages: results may alias them
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        const int n = 2 * tq + hc;
+        if (n < G) {
+          if (gid == 0) {
+            wm[warp * MAX_G + n] = S.m[hc];
+            wl[warp * MAX_G + n] = S.l[hc];
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int gr = j / (8 / NG);
+            const float off = 1024.f * S.bs[hc][gr];
+            const float z = S.zs[hc][gr];
+            wo[(warp * MAX_G + n) * D + 16 * j + gid] = fmaf(S.oacc[j][hc] - off, 1.f / 256.f, z);
+            wo[(warp * MAX_G + n) * D + 16 * j + 8 + gid] = fmaf(S.oacc[j][hc + 2] - off, 1.f / 256.f, z);
+          }
+        }
+      }
+    } else {
+      CoreState S;
+      for (int n = 0; n < MAX_G; ++n) {
+        S.m[n] = -INFINITY;
+        S.l[n] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) S.o[n][c] = 0.f;
+      }
+      float* ps = vsw + warp * (MAX_G * PAGE + 2 * 4 * PAGE);
+      float* vs = ps + MAX_G * PAGE;
+      for (int k = 0; k < nw_pages; ++k) {
+        const int st = (int)((seq + k) % DEPTH);
+        const uint32_t ph = ((seq + k) / DEPTH) & 1u;
+        if (!mbar_wait(&my_bar[st], ph)) {
+          timed_out = true;
+          k_fail = k;
+          break;
+        }
+        const int p = p0 + warp + k * NW;
+        const int pid = cv.page_table[(size_t)b * cv.max_pages_per_req + p];
+        if (pid >= 0 && pid < cv.num_pages) {
+          const int nv = (p == pages_b - 1) ? hist_b - p * PAGE : PAGE;
+          int2_page_core<NG>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane, G, qf,
+                             kconst + MAX_G * 5, ps, vs);
+        }
+        __syncwarp();
+        if (lane == 0 && k + DEPTH < nw_pages) {
+          fence_proxy_async();
+          issue(k + DEPTH);
+        }
+      }
+      __syncthreads();
+      for (int n = 0; n < G; ++n) {
+        if (lane == 0) {
+          wm[warp * MAX_G + n] = S.m[n];
+          wl[warp * MAX_G + n] = S.l[n];
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) wo[(warp * MAX_G + n) * D + 4 * lane + c] = S.o[n][c];
+      }
+    }
+    if (timed_out) {
+      // Record, wait (bounded) for this warp's copies still in flight, and
+      // make the whole CTA leave after this item.
+      if (lane == 0) {
+        record_error(cv.err, OSCAR_ERR_TIMEOUT);
+        misc[1] = 1;
+      }
+      const int issued = (k_fail + DEPTH) < nw_pages ? k_fail + DEPTH : nw_pages;
+      for (int kk = k_fail; kk < issued; ++kk)
+        mbar_wait(&my_bar[(seq + kk) % DEPTH], ((seq + kk) / DEPTH) & 1u);
+    }
+    seq += (uint32_t)nw_pages;
+    __syncthreads();
+    cta_combine_write(a, smem, L, slot);
+    __syncthreads();
+    if (misc[1]) break;
+  }
+}
+
+// ------------------------------------------------------------------ merge
+// grid = B * Hkv, block = 128 * GP (GP head groups of 128 threads).
+__global__ void __launch_bounds__(512) merge_kernel(DecodeArgs a, int GP) {
+  extern __shared__ __align__(16) uint8_t msm[];
+  float* tmp = (float*)msm;             // [GP][128]
+  float* tmp2 = tmp + GP * D;           // [GP][128]
+  int* red = (int*)(tmp2 + GP * D);     // [32]
+  int* pre = red + 32;                  // [B + 1]
+  const CacheView& cv = a.cv;
+  const int b = blockIdx.x / cv.Hkv, kvh = blockIdx.x % cv.Hkv;
+  const int grp = threadIdx.x >> 7, c = threadIdx.x & 127, bar = 1 + grp;
+  const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
+  const Sched sc = make_sched(cv.hist_lens, a.B, cv.Hkv, a.target_items, unit, pre, red);
+  const int G = cv.G;
+  const int pages_b = (cv.hist_lens[b] + PAGE - 1) / PAGE;
+  const int nb = (pages_b + sc.S - 1) / sc.S;
+  const int base = pre[b] + kvh * nb;
+  const float* Ut = a.rot.Ut_V + (size_t)kvh * D * D;
+  for (int n0 = 0; n0 < G; n0 += GP) {
+    const int n = n0 + grp;
+    const bool active = n < G;
+    float M = -INFINITY, Ls = 0.f, O = 0.f;
+    if (active) {
+      for (int j = 0; j < nb; ++j) {
+        const float* rec = a.part + ((size_t)(base + j) * G + n) * PART_STRIDE;
+        const float mj = rec[0], lj = rec[1];
+        if (lj > 0.f) {
+          const float mx = fmaxf(M, mj);
+          const float fo = M == -INFINITY ? 0.f : ex2(M - mx);
+          const float fn = ex2(mj - mx);
+          Ls = Ls * fo + lj * fn;
+          O = O * fo + rec[2 + c] * fn;
+          M = mx;
+        }
+      }
+    }
+    if (!a.bf16_history) O = unrotate128(O, Ut, a.rot.mode, c, tmp + grp * D, tmp2 + grp * D, bar);
+    if (active) {
+      const float* w = a.part + ((size_t)(sc.n_hist + b * cv.Hkv + kvh) * G + n) * PART_STRIDE;
+      const float mw = w[0], lw = w[1], ow = w[2 + c];
+      const float M2 = fmaxf(M, lw > 0.f ? mw : -INFINITY);
+      float o = 0.f, lse = -INFINITY;
+      if (M2 != -INFINITY) {
+        const float fh = (M == -INFINITY) ? 0.f : ex2(M - M2);
+        const float fw = lw > 0.f ? ex2(mw - M2) : 0.f;
+        const float lt = Ls * fh + lw * fw;
+        o = (O * fh + ow * fw) / lt;
+        lse = (M2 + log2f(lt)) * LN2;
+      }
+      const size_t row = (size_t)b * cv.Hq + kvh * G + n;
+      a.out[row * D + c] = __float2bfloat16_rn(o);
+      if (a.lse && c == 0) a.lse[row] = lse;
+    }
+  }
+}
+
+template <int NG, int IMPL>
+cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t st) {
+  const SmemLayout L = smem_layout(a.cv.head_bytes, a.B, IMPL);
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<NG, IMPL>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  if (e != cudaSuccess) return e;
+  decode_kernel<NG, IMPL><<<grid, NW * 32, L.total, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t decode_scratch_bytes(int B, int Hq, int Hkv, int G, int max_target_items) {
+  const size_t head = 256;
+  const size_t qrot = (((size_t)B * Hq * D * 4) + 255) & ~(size_t)255;
+  const size_t slots = (size_t)max_target_items + 2 * (size_t)B * Hkv;
+  return head + qrot + slots * G * PART_STRIDE * 4;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a0, int grid, cudaStream_t st) {
+  DecodeArgs a = a0;
+  const CacheView& cv = a.cv;
+  prep_kernel<<<a.bf16_history ? 1 : a.B * cv.Hkv, 128, 0, st>>>(a.q, a.qrot, a.counter, a.rot,
+                                                                  cv.Hq, cv.Hkv, cv.G,
+                                                                  !a.bf16_history);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (a.impl == 1 && !a.bf16_history) {
+    if (cv.NG == 1) e = launch_decode_t<1, 1>(a, grid, st);
+    else if (cv.NG == 2) e = launch_decode_t<2, 1>(a, grid, st);
+    else e = launch_decode_t<4, 1>(a, grid, st);
+  } else {
+    if (cv.NG == 1) e = launch_decode_t<1, 0>(a, grid, st);
+    else if (cv.NG == 2) e = launch_decode_t<2, 0>(a, grid, st);
+    else e = launch_decode_t<4, 0>(a, grid, st);
+  }
+  if (e != cudaSuccess) return e;
+  const int GP = cv.G < 4 ? cv.G : 4;
+  const size_t msm = (size_t)2 * GP * D * 4 + 32 * 4 + ((size_t)a.B + 1) * 4;
+  merge_kernel<<<a.B * cv.Hkv, 128 * GP, msm, st>>>(a, GP);
+  return cudaGetLastError();
+}
+
+}  // namespace oscar

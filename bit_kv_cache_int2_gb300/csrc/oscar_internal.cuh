@@ -1,0 +1,426 @@
+// Internal device helpers and kernel entry points of liboscar (sm_103a).
+//
+// Sources, cited by page title and section:
+//  [News] "Together AI 开源 OSCAR：一种面向长上下文 LLM 服务的注意力感知 2 位 KV 缓存量化系统"
+//  [Blog] "超越TurboQuant：Together AI把2-bit KV Cache推向真实服务"
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/oscar.h"
+
+namespace oscar {
+
+constexpr int D = 128;       // head_dim
+constexpr int PAGE = 64;     // tokens per page
+constexpr int SINK = 64;     // BF16 sink tokens   [News, "服务系统：混合精度缓存布局"]
+constexpr int RECENT = 256;  // BF16 recent tokens [News, "服务系统：混合精度缓存布局"]
+constexpr int MAX_G = 8;     // query heads per KV head handled by one mma column tile
+constexpr int PART_STRIDE = D + 2;  // partial record per head: m, l, o[128]
+constexpr int MAX_TARGET_ITEMS = 2048;
+constexpr int WIN_BYTES_PER_HEAD = (SINK + RECENT) * D * 2 * 2;  // K and V
+constexpr int BF16_HEAD_BYTES = PAGE * D * 2 * 2;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+constexpr float INV_SQRT_D = 0.08838834764831845f;  // 1/sqrt(128)
+
+__host__ __device__ constexpr int int2_head_bytes(int g) { return 4096 + PAGE * (D / g) * 8; }
+__host__ __device__ constexpr int off_k_sz() { return 4096; }
+__host__ __device__ constexpr int off_v_sz(int g) { return 4096 + PAGE * (D / g) * 4; }
+
+// Per-layer rotation tables on the device (owned by the context).
+struct LayerRot {
+  const float* U_K;   // [Hkv][128][128]  x' = x·U·H·P
+  const float* U_V;   // [Hkv][128][128]
+  const float* Ut_V;  // [Hkv][128][128]  transpose of U_V, for o = o'·P·H·U_V^T
+  const float* clip_k;  // [Hkv]
+  const float* clip_v;  // [Hkv]
+  int mode;
+};
+
+// Everything a kernel needs to know about the cache and the configuration.
+struct CacheView {
+  uint8_t* pool;
+  const int32_t* page_table;
+  __nv_bfloat16* sink_k;
+  __nv_bfloat16* sink_v;
+  __nv_bfloat16* ring_k;
+  __nv_bfloat16* ring_v;
+  int32_t* seq_lens;
+  int32_t* hist_lens;
+  int Hq, Hkv, G, g, NG;
+  int max_pages_per_req, num_pages;
+  long long page_bytes;  // bytes per page (all heads)
+  int head_bytes;        // bytes of one head's block
+  int* err;
+};
+
+__device__ __forceinline__ void record_error(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// ---------------------------------------------------------------- layouts
+// K codes, token-major: channel c = 64A+16B+8C+2D+E -> word 2D+A, bit 16E+2(2B+C).
+__host__ __device__ __forceinline__ int k_word(int c) { return 2 * ((c >> 1) & 3) + (c >> 6); }
+__host__ __device__ __forceinline__ int k_bit(int c) {
+  return 16 * (c & 1) + 2 * (2 * ((c >> 4) & 3) + ((c >> 3) & 1));
+}
+// V codes, channel-major: token slot t = 16S+8A+2T+E -> word T, bit 16E+2(2S+A).
+__host__ __device__ __forceinline__ int v_word(int t) { return (t >> 1) & 3; }
+__host__ __device__ __forceinline__ int v_bit(int t) {
+  return 16 * (t & 1) + 2 * (2 * (t >> 4) + ((t >> 3) & 1));
+}
+
+// ------------------------------------------------------- 128-thread groups
+// A "group" is 128 consecutive threads (4 full warps) holding one 128-channel
+// vector, one channel per thread.  Named barrier `bar` (1..15) syncs it.
+__device__ __forceinline__ void group_sync(int bar) {
+  asm volatile("bar.sync %0, 128;" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ int bitrev7(int j) { return (int)(__brev((unsigned)j) >> 25); }
+
+// y = x·H for the normalised Sylvester Hadamard of order 128, one element per
+// thread (channel j = thread index in the group).  tmp: 128 floats of smem.
+__device__ __forceinline__ float fwht128(float v, int j, float* tmp, int bar) {
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {
+    float o = __shfl_xor_sync(0xffffffffu, v, h);
+    v = (j & h) ? (o - v) : (v + o);
+  }
+#pragma unroll
+  for (int h = 32; h < 128; h <<= 1) {
+    tmp[j] = v;
+    group_sync(bar);
+    float o = tmp[j ^ h];
+    group_sync(bar);
+    v = (j & h) ? (o - v) : (v + o);
+  }
+  return v * INV_SQRT_D;
+}
+
+// x' = x·R for R = U·H·P_br (OSCAR), H (HADAMARD) or I (NONE), one channel
+// per thread [News, "OSCAR 的不同之处"].  x_s: the input vector in smem
+// (read only); U: [128][128] row-major in global memory; tmp: 128 floats smem.
+// Returns x'_j for j = thread index in the group.
+__device__ __forceinline__ float rotate128(const float* x_s, const float* U, int mode, int j,
+                                           float* tmp, int bar) {
+  if (mode == OSCAR_ROT_NONE) return x_s[j];
+  float t;
+  if (mode == OSCAR_ROT_OSCAR) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < D; i += 4) {
+      a0 = fmaf(x_s[i + 0], __ldg(U + (i + 0) * D + j), a0);
+      a1 = fmaf(x_s[i + 1], __ldg(U + (i + 1) * D + j), a1);
+      a2 = fmaf(x_s[i + 2], __ldg(U + (i + 2) * D + j), a2);
+      a3 = fmaf(x_s[i + 3], __ldg(U + (i + 3) * D + j), a3);
+    }
+    t = (a0 + a1) + (a2 + a3);
+  } else {
+    t = x_s[j];
+  }
+  t = fwht128(t, j, tmp, bar);
+  if (mode == OSCAR_ROT_OSCAR) {
+    tmp[j] = t;
+    group_sync(bar);
+    t = tmp[bitrev7(j)];
+    group_sync(bar);
+  }
+  return t;
+}
+
+// o = o'·R^T: o'·P_br, then ·H, then ·U^T (Ut = U^T, row-major).
+__device__ __forceinline__ float unrotate128(float v, const float* Ut, int mode, int j,
+                                             float* tmp, float* tmp2, int bar) {
+  if (mode == OSCAR_ROT_NONE) return v;
+  if (mode == OSCAR_ROT_OSCAR) {
+    tmp[j] = v;
+    group_sync(bar);
+    v = tmp[bitrev7(j)];
+    group_sync(bar);
+  }
+  v = fwht128(v, j, tmp, bar);
+  if (mode != OSCAR_ROT_OSCAR) return v;
+  tmp2[j] = v;
+  group_sync(bar);
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 4
+  for (int i = 0; i < D; i += 4) {
+    a0 = fmaf(tmp2[i + 0], __ldg(Ut + (i + 0) * D + j), a0);
+    a1 = fmaf(tmp2[i + 1], __ldg(Ut + (i + 1) * D + j), a1);
+    a2 = fmaf(tmp2[i + 2], __ldg(Ut + (i + 2) * D + j), a2);
+    a3 = fmaf(tmp2[i + 3], __ldg(Ut + (i + 3) * D + j), a3);
+  }
+  group_sync(bar);
+  return (a0 + a1) + (a2 + a3);
+}
+
+// --------------------------------------------------------------- quantiser
+// [Blog, pipeline figure paragraph: rotate -> clip -> quantize -> pack].
+// Each step is one IEEE float32 operation rounded to nearest even; the scale
+// and zero point are fp16 (round to nearest even, saturated at +-65504).
+__device__ __forceinline__ __half half_rn_sat(float x) {
+  __half h = __float2half_rn(x);
+  if (__hisinf(h)) h = __float2half_rn(x > 0.f ? 65504.f : -65504.f);
+  return h;
+}
+
+struct QParams {
+  __half s, z;
+};
+
+__device__ __forceinline__ QParams quant_params(float mn, float mx, float clip) {
+  const float mx_c = __fmul_rn(clip, mx);
+  const float mn_c = __fmul_rn(clip, mn);
+  const float s32 = __fdiv_rn(__fsub_rn(mx_c, mn_c), 3.0f);
+  QParams p;
+  p.s = half_rn_sat(s32);
+  p.z = half_rn_sat(mn_c);
+  return p;
+}
+
+__device__ __forceinline__ uint32_t quant_code(float x, QParams p) {
+  const float sf = __half2float(p.s);
+  if (sf == 0.f) return 0u;
+  const float t = __fdiv_rn(__fsub_rn(x, __half2float(p.z)), sf);
+  const float r = fminf(fmaxf(rintf(t), 0.f), 3.f);
+  return (uint32_t)r;
+}
+
+// min and max over each group of g consecutive channels (g = 32, 64, 128),
+// one channel per thread of a 128-thread group.  red: 8 floats of smem.
+__device__ __forceinline__ void group_minmax(float x, int j, int g, float* red, int bar,
+                                             float& mn, float& mx) {
+  float a = x, b = x;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = fminf(b, __shfl_xor_sync(0xffffffffu, b, o));
+  }
+  if (g == 32) {
+    mx = a;
+    mn = b;
+    return;
+  }
+  const int w = j >> 5;
+  if ((j & 31) == 0) {
+    red[w] = a;
+    red[4 + w] = b;
+  }
+  group_sync(bar);
+  const int wpg = g >> 5;
+  const int w0 = (w / wpg) * wpg;
+  mx = red[w0];
+  mn = red[4 + w0];
+  for (int k = 1; k < wpg; ++k) {
+    mx = fmaxf(mx, red[w0 + k]);
+    mn = fminf(mn, red[4 + w0 + k]);
+  }
+  group_sync(bar);
+}
+
+// ------------------------------------------------------- tensor-core helpers
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;\n" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// Two 2-bit codes -> f16x2 without a conversion instruction: the code pair at
+// bit pair I of each 16-bit half of w is moved into mantissa bits 4..9 and
+// OR-ed with the exponent of 1024, giving 1024 + code * 2^E(I) exactly, with
+// E = {4,6,4,6,8,4,6,8}[I].  Callers fold 2^-E and the 1024 offset into the
+// other operand.
+template <int I>
+__device__ __forceinline__ uint32_t code_pair(uint32_t w) {
+  constexpr uint32_t M = (I == 0 || I == 2 || I == 5) ? 0x00300030u
+                         : (I == 1 || I == 3 || I == 6) ? 0x00C000C0u
+                                                        : 0x03000300u;
+  const uint32_t src = (I <= 1) ? (w << 4) : (I <= 4) ? w : (w >> 6);
+  return (src & M) | 0x64006400u;
+}
+template <int I>
+__host__ __device__ constexpr int code_exp() {
+  return (I == 0 || I == 2 || I == 5) ? 4 : (I == 1 || I == 3 || I == 6) ? 6 : 8;
+}
+__host__ __device__ __forceinline__ int code_exp_rt(int i) {
+  return (i == 0 || i == 2 || i == 5) ? 4 : (i == 1 || i == 3 || i == 6) ? 6 : 8;
+}
+
+// ----------------------------------------------------- bounded mbarrier use
+__device__ __forceinline__ void mbar_init(uint64_t* bar, int count) {
+  uint32_t a = (uint32_t)__cvta_generic_to_shared(bar);
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(a), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  uint32_t a = (uint32_t)__cvta_generic_to_shared(bar);
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(a), "r"(bytes)
+               : "memory");
+}
+
+// Returns false when the wait ran out of its iteration budget.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase) {
+  uint32_t a = (uint32_t)__cvta_generic_to_shared(bar);
+  for (int it = 0; it < (1 << 22); ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(a), "r"(phase)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
+// Plain (non-multicast) bulk copy global -> this CTA's shared memory,
+// completing on an mbarrier.  dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  uint32_t b = (uint32_t)__cvta_generic_to_shared(bar);
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          d),
+      "l"(src), "r"(bytes), "r"(b)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// ----------------------------------------------------------- work schedule
+// The decode work is a list of items: one BF16 window item per (request, kv
+// head) and history items of S consecutive pages.  Every CTA of the decode
+// kernel and the merge kernel derive the same list from the device-resident
+// history lengths, so no host round trip is needed.
+struct Sched {
+  int S;            // pages per history item
+  int n_hist;       // number of history items
+  int n_win;        // number of window items (B * Hkv)
+  int win_first;    // window items are handed out before history items
+};
+
+// pre: smem int[B + 1]; filled with Hkv * (history items of requests < b).
+// Must be called by all threads of the block.
+__device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int target,
+                                   int hist_item_unit_bytes, int* pre, int* red) {
+  const int tid = threadIdx.x;
+  // total history pages (over requests), times Hkv
+  long long local = 0;
+  for (int b = tid; b < B; b += blockDim.x) local += (hist_lens[b] + PAGE - 1) / PAGE;
+  // block reduce (red: >= 32 ints)
+  for (int o = 16; o; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
+  if ((tid & 31) == 0) red[tid >> 5] = (int)local;
+  __syncthreads();
+  long long total = 0;
+  for (int w = 0; w < (int)(blockDim.x + 31) / 32; ++w) total += red[w];
+  __syncthreads();
+  total *= Hkv;
+  Sched s;
+  s.n_win = B * Hkv;
+  int th = target - s.n_win;
+  if (th < (target + 1) / 2) th = (target + 1) / 2;
+  long long S = (total + th - 1) / th;
+  if (S < 1) S = 1;
+  s.S = (int)S;
+  if (tid == 0) {
+    int acc = 0;
+    for (int b = 0; b < B; ++b) {
+      pre[b] = acc;
+      const int pages = (hist_lens[b] + PAGE - 1) / PAGE;
+      acc += Hkv * ((pages + s.S - 1) / s.S);
+    }
+    pre[B] = acc;
+  }
+  __syncthreads();
+  s.n_hist = pre[B];
+  s.win_first = (long long)WIN_BYTES_PER_HEAD > (long long)s.S * hist_item_unit_bytes;
+  return s;
+}
+
+// history item q -> (b, kvh, j); pre has B + 1 entries.
+__device__ __forceinline__ void hist_item_coords(int q, const int* pre, int B, int Hkv,
+                                                 const int32_t* hist_lens, int S, int& b,
+                                                 int& kvh, int& j) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {  // largest b with pre[b] <= q
+    int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= q) lo = mid; else hi = mid - 1;
+  }
+  b = lo;
+  const int pages = (hist_lens[b] + PAGE - 1) / PAGE;
+  const int nb = (pages + S - 1) / S;
+  const int r = q - pre[b];
+  kvh = r / nb;
+  j = r % nb;
+}
+
+// ------------------------------------------------------------- launchers
+struct DecodeArgs {
+  CacheView cv;
+  const __nv_bfloat16* q;  // [B][Hq][128]
+  __nv_bfloat16* out;      // [B][Hq][128]
+  float* lse;              // [B][Hq] or null
+  float* qrot;             // scratch [B][Hq][128]
+  float* part;             // scratch partials
+  int* counter;            // scratch work counter
+  int B;
+  int target_items;
+  int impl;  // 0 tensor-core, 1 CUDA-core
+  int bf16_history;
+  LayerRot rot;
+};
+
+cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st);
+size_t decode_scratch_bytes(int B, int Hq, int Hkv, int G, int max_target_items);
+
+cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* k,
+                          const __nv_bfloat16* v, int B, int do_append, int* req_counter,
+                          cudaStream_t st);
+cudaError_t launch_import(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* K,
+                          const __nv_bfloat16* V, int B, int n, int bf16_history,
+                          cudaStream_t st);
+cudaError_t launch_quantize_hook(const float* x, int n, int g, float clip, int which,
+                                 uint8_t* codes, __half2* sz, cudaStream_t st);
+cudaError_t launch_debug_rotate(const float* U, int mode, const __nv_bfloat16* x, float* y,
+                                int n, cudaStream_t st);
+
+}  // namespace oscar

@@ -1,0 +1,397 @@
+// Demotion, bulk import and quantiser test hooks of liboscar (sm_103a).
+//
+// The demotion step follows the pipeline figure of "超越TurboQuant：Together AI把
+// 2-bit KV Cache推向真实服务" ("从离线校准到在线推理的pipeline" and the paragraph
+// under it): a new token is written to the BF16 recent window, and the oldest
+// recent token is rotated, clipped, quantised and packed 4 codes per byte into
+// INT2 history.  Region sizes (sink 64, recent 256) are from "Together AI 开源
+// OSCAR：一种面向长上下文 LLM 服务的注意力感知 2 位 KV 缓存量化系统", section
+// "服务系统：混合精度缓存布局".
+#include "oscar_internal.cuh"
+
+namespace oscar {
+
+namespace {
+
+// Quantise the rotated value y (channel j of a 128-thread group) and place its
+// code in a K row (kw: 8 words of smem, zeroed) or in a V block word in smem
+// (vblk: 512 words, channel-major, zeroed) for token row t.  Writes (s, z)
+// through sz_out (token row t of an [64][NG] half2 array) for the group leader.
+__device__ __forceinline__ void quant_pack(float y, int j, int g, float clip, float* red, int bar,
+                                           bool is_v, int t, uint32_t* kw, uint32_t* vblk,
+                                           __half2* sz_row) {
+  float mn, mx;
+  group_minmax(y, j, g, red, bar, mn, mx);
+  const QParams qp = quant_params(mn, mx, clip);
+  const uint32_t code = quant_code(y, qp);
+  if (!is_v) {
+    atomicOr(&kw[k_word(j)], code << k_bit(j));
+  } else {
+    atomicOr(&vblk[j * 4 + v_word(t)], code << v_bit(t));
+  }
+  if ((j % g) == 0) sz_row[j / g] = __halves2half2(qp.s, qp.z);
+}
+
+// Same, but writing a single token's V code straight into a V block in global
+// memory with a read-modify-write of the owning word (one writer per word).
+__device__ __forceinline__ void quant_store_v_global(float y, int j, int g, float clip, float* red,
+                                                     int bar, int t, uint32_t* vblk_g,
+                                                     __half2* sz_row) {
+  float mn, mx;
+  group_minmax(y, j, g, red, bar, mn, mx);
+  const QParams qp = quant_params(mn, mx, clip);
+  const uint32_t code = quant_code(y, qp);
+  uint32_t* wp = vblk_g + j * 4 + v_word(t);
+  const uint32_t sh = (uint32_t)v_bit(t);
+  *wp = (*wp & ~(3u << sh)) | (code << sh);
+  if ((j % g) == 0) sz_row[j / g] = __halves2half2(qp.s, qp.z);
+}
+
+// ------------------------------------------------------------------ append
+// grid = B * Hkv, block = 256: threads 0..127 handle K, 128..255 handle V.
+__global__ void __launch_bounds__(256) append_kernel(CacheView cv, LayerRot rot,
+                                                     const __nv_bfloat16* __restrict__ knew,
+                                                     const __nv_bfloat16* __restrict__ vnew,
+                                                     int do_append, int* req_counter) {
+  __shared__ float xs[2][D];
+  __shared__ float tmp[2][D];
+  __shared__ float red[2][8];
+  __shared__ uint32_t kw[8];
+  __shared__ int st[6];
+  const int b = blockIdx.x / cv.Hkv, h = blockIdx.x % cv.Hkv;
+  const int grp = threadIdx.x >> 7, j = threadIdx.x & 127, bar = 1 + grp;
+  if (threadIdx.x == 0) {
+    const int L = cv.seq_lens[b], H = cv.hist_lens[b];
+    const int recent = L > SINK ? L - SINK - H : 0;
+    int ok = (L >= 0 && H >= 0 && H <= (L > SINK ? L - SINK : 0) && recent <= RECENT);
+    if (!ok) record_error(cv.err, OSCAR_ERR_STATE);
+    const int demote = ok && (do_append ? (recent == RECENT) : (recent > 0));
+    int page = -1;
+    if (demote) {
+      const int pi = H / PAGE;
+      if (pi >= cv.max_pages_per_req) {
+        ok = 0;
+        record_error(cv.err, OSCAR_ERR_RANGE);
+      } else {
+        page = cv.page_table[(size_t)b * cv.max_pages_per_req + pi];
+        if (page < 0) {
+          ok = 0;
+          record_error(cv.err, OSCAR_ERR_NO_PAGE);
+        } else if (page >= cv.num_pages) {
+          ok = 0;
+          record_error(cv.err, OSCAR_ERR_RANGE);
+        }
+      }
+    }
+    st[0] = L;
+    st[1] = H;
+    st[2] = ok && demote;
+    st[3] = page;
+    st[4] = ok;
+  }
+  if (threadIdx.x < 8) kw[threadIdx.x] = 0u;
+  __syncthreads();
+  const int L = st[0], H = st[1], demote = st[2], page = st[3], ok = st[4];
+
+  if (demote) {
+    const int ring_slot = H % RECENT;  // absolute position 64 + H
+    const __nv_bfloat16* src =
+        (grp == 0 ? cv.ring_k : cv.ring_v) + ((size_t)(b * cv.Hkv + h) * RECENT + ring_slot) * D;
+    xs[grp][j] = __bfloat162float(src[j]);
+    __syncthreads();
+    const float* U = (grp == 0 ? rot.U_K : rot.U_V) + (size_t)h * D * D;
+    const float y = rotate128(xs[grp], U, rot.mode, j, tmp[grp], bar);
+    const float clip = (grp == 0 ? rot.clip_k : rot.clip_v)[h];
+    uint8_t* blk = cv.pool + (size_t)page * cv.page_bytes + (size_t)h * cv.head_bytes;
+    const int t = H % PAGE;
+    if (grp == 0) {
+      quant_pack(y, j, cv.g, clip, red[0], bar, false, t, kw, nullptr,
+                 (__half2*)(blk + off_k_sz()) + t * cv.NG);
+    } else {
+      quant_store_v_global(y, j, cv.g, clip, red[1], bar, t, (uint32_t*)(blk + 2048),
+                           (__half2*)(blk + off_v_sz(cv.g)) + t * cv.NG);
+    }
+    __syncthreads();
+    if (threadIdx.x < 8) ((uint32_t*)(blk + t * 32))[threadIdx.x] = kw[threadIdx.x];
+  }
+  __syncthreads();  // the evicted ring slot is fully read before it is overwritten
+
+  if (do_append && ok) {
+    const size_t head = (size_t)(b * cv.Hkv + h);
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    if (L < SINK) {
+      dk = cv.sink_k + (head * SINK + L) * D;
+      dv = cv.sink_v + (head * SINK + L) * D;
+    } else {
+      const int slot = (L - SINK) % RECENT;
+      dk = cv.ring_k + (head * RECENT + slot) * D;
+      dv = cv.ring_v + (head * RECENT + slot) * D;
+    }
+    const size_t src = head * D;
+    if (threadIdx.x < 16) {
+      ((uint4*)dk)[threadIdx.x] = ((const uint4*)(knew + src))[threadIdx.x];
+    } else if (threadIdx.x < 32) {
+      ((uint4*)dv)[threadIdx.x - 16] = ((const uint4*)(vnew + src))[threadIdx.x - 16];
+    }
+  }
+  // The last CTA of request b to finish updates its lengths: every CTA of the
+  // request has read the old lengths before it increments the counter.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int old = atomicAdd(&req_counter[b], 1);
+    if (old == cv.Hkv - 1) {
+      req_counter[b] = 0;
+      if (ok) {
+        cv.seq_lens[b] = L + (do_append ? 1 : 0);
+        cv.hist_lens[b] = H + demote;
+      }
+      __threadfence();
+    }
+  }
+}
+
+// ------------------------------------------------------------------ import
+// Copies the sink and recent tokens of an n-token prefix; checks emptiness.
+// grid = B * Hkv, block = 256.
+__global__ void __launch_bounds__(256) import_window_kernel(CacheView cv,
+                                                            const __nv_bfloat16* __restrict__ K,
+                                                            const __nv_bfloat16* __restrict__ V,
+                                                            int n) {
+  const int b = blockIdx.x / cv.Hkv, h = blockIdx.x % cv.Hkv;
+  if (cv.seq_lens[b] != 0) {
+    if (threadIdx.x == 0 && h == 0) record_error(cv.err, OSCAR_ERR_STATE);
+    return;
+  }
+  const size_t head = (size_t)(b * cv.Hkv + h);
+  const uint4* srcK = (const uint4*)(K + head * (size_t)n * D);
+  const uint4* srcV = (const uint4*)(V + head * (size_t)n * D);
+  const int nsink = n < SINK ? n : SINK;
+  const int r0 = (n - RECENT) > SINK ? n - RECENT : SINK;  // first recent position
+  const int nrec = n > r0 ? n - r0 : 0;
+  // 16 uint4 per token row
+  for (int idx = threadIdx.x; idx < nsink * 16; idx += blockDim.x) {
+    const int p = idx >> 4, c = idx & 15;
+    ((uint4*)(cv.sink_k + (head * SINK + p) * D))[c] = srcK[(size_t)p * 16 + c];
+    ((uint4*)(cv.sink_v + (head * SINK + p) * D))[c] = srcV[(size_t)p * 16 + c];
+  }
+  for (int idx = threadIdx.x; idx < nrec * 16; idx += blockDim.x) {
+    const int p = r0 + (idx >> 4), c = idx & 15;
+    const int slot = (p - SINK) % RECENT;
+    ((uint4*)(cv.ring_k + (head * RECENT + slot) * D))[c] = srcK[(size_t)p * 16 + c];
+    ((uint4*)(cv.ring_v + (head * RECENT + slot) * D))[c] = srcV[(size_t)p * 16 + c];
+  }
+}
+
+__device__ __forceinline__ uint8_t* lookup_page(const CacheView& cv, int b, int pi, bool report) {
+  if (pi >= cv.max_pages_per_req) {
+    if (report) record_error(cv.err, OSCAR_ERR_RANGE);
+    return nullptr;
+  }
+  const int page = cv.page_table[(size_t)b * cv.max_pages_per_req + pi];
+  if (page < 0) {
+    if (report) record_error(cv.err, OSCAR_ERR_NO_PAGE);
+    return nullptr;
+  }
+  if (page >= cv.num_pages) {
+    if (report) record_error(cv.err, OSCAR_ERR_RANGE);
+    return nullptr;
+  }
+  return cv.pool + (size_t)page * cv.page_bytes;
+}
+
+constexpr int IMP_NT = 8;  // tokens rotated together (one U load feeds 8 FMAs)
+
+// Quantises one history page of one kv head: grid (B * Hkv, pages), block 256.
+__global__ void __launch_bounds__(256) import_int2_pages_kernel(CacheView cv, LayerRot rot,
+                                                                const __nv_bfloat16* __restrict__ K,
+                                                                const __nv_bfloat16* __restrict__ V,
+                                                                int n) {
+  __shared__ float xs[2][IMP_NT][D];
+  __shared__ float tmp[2][D];
+  __shared__ float red[2][8];
+  __shared__ __align__(16) uint32_t kwords[PAGE * 8];
+  __shared__ __align__(16) uint32_t vwords[D * 4];
+  __shared__ __align__(16) __half2 szs[2][PAGE * 4];
+  const int b = blockIdx.x / cv.Hkv, h = blockIdx.x % cv.Hkv, pg = blockIdx.y;
+  const int hist = n > SINK + RECENT ? n - SINK - RECENT : 0;
+  const int t0 = pg * PAGE;
+  if (t0 >= hist) return;
+  if (cv.seq_lens[b] != 0) return;  // reported by import_window_kernel
+  uint8_t* page = lookup_page(cv, b, pg, h == 0 && threadIdx.x == 0);
+  if (!page) return;
+  uint8_t* blk = page + (size_t)h * cv.head_bytes;
+  const int nt = (hist - t0) < PAGE ? hist - t0 : PAGE;
+  const int grp = threadIdx.x >> 7, j = threadIdx.x & 127, bar = 1 + grp;
+  for (int i = threadIdx.x; i < PAGE * 8; i += 256) kwords[i] = 0u;
+  for (int i = threadIdx.x; i < D * 4; i += 256) vwords[i] = 0u;
+  for (int i = threadIdx.x; i < 2 * PAGE * 4; i += 256) (&szs[0][0])[i] = __halves2half2(__float2half(0.f), __float2half(0.f));
+  const size_t head = (size_t)(b * cv.Hkv + h);
+  const __nv_bfloat16* src = (grp == 0 ? K : V) + (head * (size_t)n + SINK + t0) * D;
+  const float* U = (grp == 0 ? rot.U_K : rot.U_V) + (size_t)h * D * D;
+  const float clip = (grp == 0 ? rot.clip_k : rot.clip_v)[h];
+  __syncthreads();
+  for (int tb = 0; tb < nt; tb += IMP_NT) {
+    const int cnt = (nt - tb) < IMP_NT ? nt - tb : IMP_NT;
+    for (int k = 0; k < IMP_NT; ++k)
+      xs[grp][k][j] = k < cnt ? __bfloat162float(src[(size_t)(tb + k) * D + j]) : 0.f;
+    group_sync(bar);
+    float acc[IMP_NT];
+    if (rot.mode == OSCAR_ROT_OSCAR) {
+#pragma unroll
+      for (int k = 0; k < IMP_NT; ++k) acc[k] = 0.f;
+      for (int i = 0; i < D; ++i) {
+        const float u = __ldg(U + i * D + j);
+#pragma unroll
+        for (int k = 0; k < IMP_NT; ++k) acc[k] = fmaf(xs[grp][k][i], u, acc[k]);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < IMP_NT; ++k) acc[k] = xs[grp][k][j];
+    }
+    for (int k = 0; k < cnt; ++k) {
+      float y = acc[k];
+      if (rot.mode != OSCAR_ROT_NONE) {
+        y = fwht128(y, j, tmp[grp], bar);
+        if (rot.mode == OSCAR_ROT_OSCAR) {
+          tmp[grp][j] = y;
+          group_sync(bar);
+          y = tmp[grp][bitrev7(j)];
+          group_sync(bar);
+        }
+      }
+      const int t = tb + k;
+      quant_pack(y, j, cv.g, clip, red[grp], bar, grp == 1, t, kwords + t * 8, vwords,
+                 &szs[grp][t * cv.NG]);
+    }
+    group_sync(bar);
+  }
+  __syncthreads();
+  // write the block: K codes 2048 B, V codes 2048 B, K s/z, V s/z
+  uint4* dst = (uint4*)blk;
+  for (int i = threadIdx.x; i < 128; i += 256) dst[i] = ((const uint4*)kwords)[i];
+  for (int i = threadIdx.x; i < 128; i += 256) dst[128 + i] = ((const uint4*)vwords)[i];
+  const int szq = PAGE * cv.NG * 4 / 16;  // uint4 per s/z array
+  for (int i = threadIdx.x; i < szq; i += 256) {
+    ((uint4*)(blk + off_k_sz()))[i] = ((const uint4*)szs[0])[i];
+    ((uint4*)(blk + off_v_sz(cv.g)))[i] = ((const uint4*)szs[1])[i];
+  }
+}
+
+// Copies BF16 history tokens into a BF16 page: grid (B * Hkv, pages), block 256.
+__global__ void __launch_bounds__(256) import_bf16_pages_kernel(CacheView cv,
+                                                                const __nv_bfloat16* __restrict__ K,
+                                                                const __nv_bfloat16* __restrict__ V,
+                                                                int n) {
+  const int b = blockIdx.x / cv.Hkv, h = blockIdx.x % cv.Hkv, pg = blockIdx.y;
+  const int hist = n > SINK + RECENT ? n - SINK - RECENT : 0;
+  const int t0 = pg * PAGE;
+  if (t0 >= hist) return;
+  if (cv.seq_lens[b] != 0) return;
+  uint8_t* page = lookup_page(cv, b, pg, h == 0 && threadIdx.x == 0);
+  if (!page) return;
+  uint4* kdst = (uint4*)(page + (size_t)h * BF16_HEAD_BYTES);
+  uint4* vdst = kdst + PAGE * D * 2 / 16;
+  const int nt = (hist - t0) < PAGE ? hist - t0 : PAGE;
+  const size_t head = (size_t)(b * cv.Hkv + h);
+  const uint4* ks = (const uint4*)(K + (head * (size_t)n + SINK + t0) * D);
+  const uint4* vs = (const uint4*)(V + (head * (size_t)n + SINK + t0) * D);
+  for (int i = threadIdx.x; i < nt * 16; i += blockDim.x) {
+    kdst[i] = ks[i];
+    vdst[i] = vs[i];
+  }
+}
+
+__global__ void import_set_lengths_kernel(int32_t* seq, int32_t* hist, int B, int n) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  if (seq[b] != 0) return;
+  seq[b] = n;
+  hist[b] = n > SINK + RECENT ? n - SINK - RECENT : 0;
+}
+
+// --------------------------------------------------------------- test hooks
+// grid = ceil(n / 64), block 128: each CTA quantises up to 64 rotated vectors.
+__global__ void __launch_bounds__(128) quantize_hook_kernel(const float* __restrict__ x, int n,
+                                                            int g, float clip, int which,
+                                                            uint8_t* __restrict__ codes,
+                                                            __half2* __restrict__ sz) {
+  __shared__ float red[8];
+  __shared__ __align__(16) uint32_t kwords[PAGE * 8];
+  __shared__ __align__(16) uint32_t vwords[D * 4];
+  const int j = threadIdx.x;
+  const int i0 = blockIdx.x * PAGE;
+  const int cnt = (n - i0) < PAGE ? n - i0 : PAGE;
+  const int NG = D / g;
+  for (int i = j; i < PAGE * 8; i += 128) kwords[i] = 0u;
+  for (int i = j; i < D * 4; i += 128) vwords[i] = 0u;
+  __syncthreads();
+  for (int t = 0; t < cnt; ++t) {
+    const float y = x[(size_t)(i0 + t) * D + j];
+    quant_pack(y, j, g, clip, red, 1, which == 1, t, kwords + t * 8, vwords,
+               sz + (size_t)(i0 + t) * NG);
+  }
+  __syncthreads();
+  if (which == 0) {
+    for (int i = j; i < cnt * 8; i += 128) ((uint32_t*)codes)[(size_t)i0 * 8 + i] = kwords[i];
+  } else {
+    for (int i = j; i < D * 4; i += 128) ((uint32_t*)codes)[(size_t)blockIdx.x * 512 + i] = vwords[i];
+  }
+}
+
+// grid = n, block 128
+__global__ void __launch_bounds__(128) debug_rotate_kernel(const float* __restrict__ U, int mode,
+                                                           const __nv_bfloat16* __restrict__ x,
+                                                           float* __restrict__ y) {
+  __shared__ float xs[D];
+  __shared__ float tmp[D];
+  const int j = threadIdx.x;
+  xs[j] = __bfloat162float(x[(size_t)blockIdx.x * D + j]);
+  __syncthreads();
+  y[(size_t)blockIdx.x * D + j] = rotate128(xs, U, mode, j, tmp, 1);
+}
+
+}  // namespace
+
+cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* k,
+                          const __nv_bfloat16* v, int B, int do_append, int* req_counter,
+                          cudaStream_t st) {
+  append_kernel<<<B * cv.Hkv, 256, 0, st>>>(cv, rot, k, v, do_append, req_counter);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_import(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* K,
+                          const __nv_bfloat16* V, int B, int n, int bf16_history,
+                          cudaStream_t st) {
+  import_window_kernel<<<B * cv.Hkv, 256, 0, st>>>(cv, K, V, n);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int hist = n > SINK + RECENT ? n - SINK - RECENT : 0;
+  const int pages = (hist + PAGE - 1) / PAGE;
+  if (pages > 0) {
+    dim3 grid(B * cv.Hkv, pages);
+    if (bf16_history)
+      import_bf16_pages_kernel<<<grid, 256, 0, st>>>(cv, K, V, n);
+    else
+      import_int2_pages_kernel<<<grid, 256, 0, st>>>(cv, rot, K, V, n);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  import_set_lengths_kernel<<<(B + 127) / 128, 128, 0, st>>>(cv.seq_lens, cv.hist_lens, B, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_hook(const float* x, int n, int g, float clip, int which,
+                                 uint8_t* codes, __half2* sz, cudaStream_t st) {
+  quantize_hook_kernel<<<(n + PAGE - 1) / PAGE, 128, 0, st>>>(x, n, g, clip, which, codes, sz);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_rotate(const float* U, int mode, const __nv_bfloat16* x, float* y, int n,
+                                cudaStream_t st) {
+  debug_rotate_kernel<<<n, 128, 0, st>>>(U, mode, x, y);
+  return cudaGetLastError();
+}
+
+}  // namespace oscar

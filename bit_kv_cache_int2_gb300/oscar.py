@@ -1,0 +1,274 @@
+"""Python binding of liboscar's C ABI (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does no
+computation of its own: it turns torch tensors into device pointers, streams
+into ``cudaStream_t`` handles and non-OK statuses into ``OscarError``.  All
+work runs in the CUDA library.  If the library is missing this module raises;
+there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "liboscar.so")
+
+HEAD_DIM = 128
+PAGE_SIZE = 64
+SINK_TOKENS = 64
+RECENT_TOKENS = 256
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_NO_PAGE = 3
+ERR_RANGE = 4
+ERR_TIMEOUT = 5
+ERR_CUDA = 6
+ERR_STATE = 7
+
+ROT_OSCAR = 0
+ROT_HADAMARD = 1
+ROT_NONE = 2
+
+OPT_DECODE_IMPL = 0
+OPT_CTAS_PER_SM = 1
+OPT_ITEMS_PER_CTA = 2
+
+
+class OscarError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+class oscar_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "num_layers", "num_q_heads", "num_kv_heads", "head_dim", "group_size", "page_size",
+        "sink_tokens", "recent_tokens", "max_batch", "max_pages_per_req", "num_pages")]
+
+
+class oscar_layout_info(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "int2_head_bytes", "int2_page_bytes", "off_k_codes", "off_v_codes", "off_k_sz", "off_v_sz",
+        "bf16_head_bytes", "bf16_page_bytes", "sink_bytes", "ring_bytes", "decode_scratch_bytes")]
+
+
+class oscar_cache(ctypes.Structure):
+    _fields_ = [("pool", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
+                ("sink_k", ctypes.c_void_p), ("sink_v", ctypes.c_void_p),
+                ("ring_k", ctypes.c_void_p), ("ring_v", ctypes.c_void_p),
+                ("seq_lens", ctypes.c_void_p), ("hist_lens", ctypes.c_void_p)]
+
+
+_lib = None
+
+_SIGS = {
+    "oscar_version": ([], ctypes.c_int),
+    "oscar_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "oscar_layout": ([ctypes.POINTER(oscar_config), ctypes.POINTER(oscar_layout_info)], ctypes.c_int),
+    "oscar_create": ([ctypes.POINTER(oscar_config), ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
+    "oscar_destroy": ([ctypes.c_void_p], ctypes.c_int),
+    "oscar_set_option": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_int], ctypes.c_int),
+    "oscar_set_rotation": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
+    "oscar_append": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(oscar_cache), ctypes.c_void_p,
+                      ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
+    "oscar_demote": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(oscar_cache), ctypes.c_int,
+                      ctypes.c_void_p], ctypes.c_int),
+    "oscar_import_tokens": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(oscar_cache), ctypes.c_void_p,
+                             ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
+    "oscar_decode": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(oscar_cache), ctypes.c_void_p,
+                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
+                      ctypes.c_void_p], ctypes.c_int),
+    "oscar_decode_bf16_history": ([ctypes.c_void_p, ctypes.POINTER(oscar_cache), ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                   ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
+    "oscar_import_bf16_history": ([ctypes.c_void_p, ctypes.POINTER(oscar_cache), ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
+    "oscar_quantize_rotated_f32": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "oscar_debug_rotate": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                            ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
+    "oscar_get_error": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
+}
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+def lib():
+    """Load liboscar.so (built in-tree by ``bit_kv_cache_int2_gb300.build``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with bit_kv_cache_int2_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(st: int, where: str):
+    if st != OK:
+        raise OscarError(st, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def status_string(st: int) -> str:
+    try:
+        return lib().oscar_status_string(st).decode()
+    except RuntimeError:
+        return f"status {st}"
+
+
+def oscar_version() -> int:
+    return lib().oscar_version()
+
+
+def make_config(num_layers=1, num_q_heads=32, num_kv_heads=8, group_size=128, max_batch=1,
+                max_pages_per_req=1, num_pages=1) -> oscar_config:
+    return oscar_config(num_layers, num_q_heads, num_kv_heads, HEAD_DIM, group_size, PAGE_SIZE,
+                        SINK_TOKENS, RECENT_TOKENS, max_batch, max_pages_per_req, num_pages)
+
+
+def oscar_layout(cfg: oscar_config) -> oscar_layout_info:
+    info = oscar_layout_info()
+    _check(lib().oscar_layout(ctypes.byref(cfg), ctypes.byref(info)), "oscar_layout")
+    return info
+
+
+def oscar_create(cfg: oscar_config) -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    _check(lib().oscar_create(ctypes.byref(cfg), ctypes.byref(h)), "oscar_create")
+    return h
+
+
+def oscar_destroy(ctx):
+    _check(lib().oscar_destroy(ctx), "oscar_destroy")
+
+
+def oscar_set_option(ctx, option: int, value: int):
+    _check(lib().oscar_set_option(ctx, option, value), "oscar_set_option")
+
+
+def oscar_set_rotation(ctx, layer, U_K, U_V, clip_k, clip_v, rot_mode=ROT_OSCAR, stream=None):
+    """U_K, U_V: host float32 [Hkv][128][128] (numpy or CPU tensor) or None; clips: host float32 [Hkv]."""
+    import numpy as np
+
+    def host(a):
+        if a is None:
+            return None, None
+        a = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+        return a, a.ctypes.data_as(ctypes.c_void_p)
+
+    uk, puk = host(U_K)
+    uv, puv = host(U_V)
+    ck, pck = host(clip_k)
+    cv, pcv = host(clip_v)
+    _check(lib().oscar_set_rotation(ctx, layer, puk, puv, pck, pcv, rot_mode, _stream(stream)),
+           "oscar_set_rotation")
+
+
+def _cache_struct(c: dict) -> oscar_cache:
+    return oscar_cache(*(c[k].data_ptr() if c.get(k) is not None else None for k in
+                         ("pool", "page_table", "sink_k", "sink_v", "ring_k", "ring_v", "seq_lens", "hist_lens")))
+
+
+def oscar_append(ctx, layer, cache: dict, k_new, v_new, batch, stream=None):
+    cs = _cache_struct(cache)
+    _check(lib().oscar_append(ctx, layer, ctypes.byref(cs), _ptr(k_new), _ptr(v_new), batch, _stream(stream)),
+           "oscar_append")
+
+
+def oscar_demote(ctx, layer, cache: dict, batch, stream=None):
+    cs = _cache_struct(cache)
+    _check(lib().oscar_demote(ctx, layer, ctypes.byref(cs), batch, _stream(stream)), "oscar_demote")
+
+
+def oscar_import_tokens(ctx, layer, cache: dict, K, V, batch, n, stream=None):
+    cs = _cache_struct(cache)
+    _check(lib().oscar_import_tokens(ctx, layer, ctypes.byref(cs), _ptr(K), _ptr(V), batch, n, _stream(stream)),
+           "oscar_import_tokens")
+
+
+def oscar_decode(ctx, layer, cache: dict, q, out, lse, scratch, batch, stream=None):
+    cs = _cache_struct(cache)
+    _check(lib().oscar_decode(ctx, layer, ctypes.byref(cs), _ptr(q), _ptr(out), _ptr(lse), _ptr(scratch),
+                              scratch.numel() * scratch.element_size(), batch, _stream(stream)),
+           "oscar_decode")
+
+
+def oscar_decode_bf16_history(ctx, cache: dict, q, out, lse, scratch, batch, stream=None):
+    cs = _cache_struct(cache)
+    _check(lib().oscar_decode_bf16_history(ctx, ctypes.byref(cs), _ptr(q), _ptr(out), _ptr(lse), _ptr(scratch),
+                                           scratch.numel() * scratch.element_size(), batch, _stream(stream)),
+           "oscar_decode_bf16_history")
+
+
+def oscar_import_bf16_history(ctx, cache: dict, K, V, batch, n, stream=None):
+    cs = _cache_struct(cache)
+    _check(lib().oscar_import_bf16_history(ctx, ctypes.byref(cs), _ptr(K), _ptr(V), batch, n, _stream(stream)),
+           "oscar_import_bf16_history")
+
+
+def oscar_quantize_rotated_f32(x, group_size, clip, which, codes, sz, stream=None):
+    _check(lib().oscar_quantize_rotated_f32(_ptr(x), x.shape[0], group_size, float(clip), which, _ptr(codes),
+                                            _ptr(sz), _stream(stream)), "oscar_quantize_rotated_f32")
+
+
+def oscar_debug_rotate(ctx, layer, which, kv_head, x, x_rot, stream=None):
+    _check(lib().oscar_debug_rotate(ctx, layer, which, kv_head, _ptr(x), _ptr(x_rot), x.shape[0], _stream(stream)),
+           "oscar_debug_rotate")
+
+
+def oscar_get_error(ctx, stream=None) -> int:
+    code = ctypes.c_int(0)
+    _check(lib().oscar_get_error(ctx, _stream(stream), ctypes.byref(code)), "oscar_get_error")
+    return code.value
+
+
+# ---------------------------------------------------------------- plumbing
+def alloc_cache(cfg: oscar_config, device="cuda", bf16_history=False, zero=True):
+    """Device buffers of one layer's cache (torch allocations, caller-owned)."""
+    import torch
+
+    info = oscar_layout(cfg)
+    page_bytes = info.bf16_page_bytes if bf16_history else info.int2_page_bytes
+    mk = torch.zeros if zero else torch.empty
+    B, Hkv = cfg.max_batch, cfg.num_kv_heads
+    return {
+        "pool": mk(cfg.num_pages * page_bytes, dtype=torch.uint8, device=device),
+        "page_table": torch.full((B, cfg.max_pages_per_req), -1, dtype=torch.int32, device=device),
+        "sink_k": mk(B, Hkv, SINK_TOKENS, HEAD_DIM, dtype=torch.bfloat16, device=device),
+        "sink_v": mk(B, Hkv, SINK_TOKENS, HEAD_DIM, dtype=torch.bfloat16, device=device),
+        "ring_k": mk(B, Hkv, RECENT_TOKENS, HEAD_DIM, dtype=torch.bfloat16, device=device),
+        "ring_v": mk(B, Hkv, RECENT_TOKENS, HEAD_DIM, dtype=torch.bfloat16, device=device),
+        "seq_lens": torch.zeros(B, dtype=torch.int32, device=device),
+        "hist_lens": torch.zeros(B, dtype=torch.int32, device=device),
+    }
+
+
+def alloc_scratch(cfg: oscar_config, device="cuda"):
+    import torch
+
+    n = oscar_layout(cfg).decode_scratch_bytes
+    return torch.empty((n + 255) // 256 * 256, dtype=torch.uint8, device=device)

@@ -1,0 +1,279 @@
+/*
+ * oscar.h -- C ABI of liboscar: OSCAR INT2 KV-cache decode attention for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes (cited by page title and section):
+ *
+ *  [News]     "Together AI 开源 OSCAR：一种面向长上下文 LLM 服务的注意力感知
+ *              2 位 KV 缓存量化系统"
+ *  [Blog]     "超越TurboQuant：Together AI把2-bit KV Cache推向真实服务"
+ *  [Telegram] "OSCAR: открытая система двухбитного сжатия KV-кэша"
+ *
+ *  - Each request's KV cache has three regions: the first 64 tokens (sink) in
+ *    BF16, the newest 256 tokens (recent window) in BF16, and every token in
+ *    between (history) in INT2 after rotation and clipping [News, section
+ *    "服务系统：混合精度缓存布局"; Telegram, paragraph on the first 64 / last
+ *    256 tokens].
+ *  - The rotation is R_K = U_Q·H·P_br for keys and R_V = U_S·H·P_br for values,
+ *    per layer and per KV head (U: eigenvectors of the query covariance /
+ *    score-weighted value covariance, H: normalised Sylvester Hadamard, P_br:
+ *    bit-reversal permutation) [News, section "OSCAR 的不同之处"; Blog, section
+ *    "OSCAR把旋转对准attention"].
+ *  - A new token is written to the recent window; the oldest recent token is
+ *    rotated, clipped, quantised (asymmetric INT2 with an fp16 scale and zero
+ *    point per group) and packed 4 codes per byte into history.  Decoding runs
+ *    the INT2 segment and the BF16 segments separately and merges them by
+ *    online softmax [Blog, pipeline figure "从离线校准到在线推理的pipeline" and
+ *    the paragraph under it].
+ *
+ * Conventions
+ *  - Every call returns an oscar_status; no exception crosses the ABI.
+ *  - Device pointers are raw CUDA device addresses; host pointers are marked
+ *    "host".  BF16 and FP16 data are passed as their 16-bit patterns (void*).
+ *    All arrays are dense, row-major, and must be 16-byte aligned.
+ *  - Calls that take a stream are asynchronous on that stream (NULL = legacy
+ *    default stream).  Argument errors are detected on the host and reported
+ *    before anything is launched.  Errors found by a kernel (a page-table
+ *    entry that is -1 or out of range, a window overflow, a scale out of the
+ *    kernel's range, a wait that timed out) are written to a per-context
+ *    device error word; kernels never trap.  oscar_get_error reads it.
+ *  - Ownership: the caller allocates and owns every device buffer it passes
+ *    (page pools, page tables, windows, lengths, q, out, scratch).  The
+ *    context owns only its rotation tables and its error word, which
+ *    oscar_destroy frees.
+ *  - Fixed shape: head_dim = 128, page_size = 64, sink = 64, recent = 256.
+ *    group_size is 32, 64 or 128; num_q_heads / num_kv_heads is 1, 2, 4 or 8.
+ *
+ * Page layouts (one pool per layer; a page holds the same 64 history token
+ * slots for every KV head):
+ *  INT2 page  = num_kv_heads blocks, one per KV head, each
+ *     [K codes 64 x 32 B][V codes 128 x 16 B][K s/z 64 x (128/g) x 4 B]
+ *     [V s/z 64 x (128/g) x 4 B]
+ *   = 4608 B per head at g = 128, 5120 B at g = 64, 6144 B at g = 32.
+ *   A code at bit position b of a little-endian 32-bit word sits in byte b/8
+ *   at bits b%8 and b%8+1.
+ *   K codes are token-major: 8 words per token.  Rotated channel
+ *     c = 64A + 16B + 8C + 2D + E is stored in word 2D + A at bit 16E + 2(2B + C).
+ *   V codes are channel-major: 4 words per rotated channel per page.  Token
+ *     slot t = 16S + 8A + 2T + E is stored in word T at bit 16E + 2(2S + A).
+ *   s/z: one (scale, zero) fp16 pair per token and group, scale first.
+ *   Groups are g consecutive rotated channels.  Dequantisation: x' = code*s + z.
+ *  BF16 page (baseline history) = num_kv_heads blocks of
+ *     [K 64 x 128 bf16][V 64 x 128 bf16] = 32768 B per head.
+ *  Windows: sink_k/sink_v bf16 [max_batch][num_kv_heads][64][128];
+ *           ring_k/ring_v bf16 [max_batch][num_kv_heads][256][128];
+ *  absolute position p of request b lives in sink[p] (p < 64), in history
+ *  slot p - 64 (64 <= p < 64 + hist_lens[b]) or in ring slot (p - 64) % 256.
+ */
+#ifndef OSCAR_H
+#define OSCAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define OSCAR_HEAD_DIM 128
+#define OSCAR_PAGE_SIZE 64
+#define OSCAR_SINK_TOKENS 64
+#define OSCAR_RECENT_TOKENS 256
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* oscar_stream_t;
+
+typedef enum {
+  OSCAR_OK = 0,
+  OSCAR_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned buffer     */
+  OSCAR_ERR_UNSUPPORTED = 2, /* head_dim != 128, group size or GQA ratio      */
+  OSCAR_ERR_NO_PAGE = 3,     /* device: page-table entry is -1                */
+  OSCAR_ERR_RANGE = 4,       /* device: page id, length or scale out of range */
+  OSCAR_ERR_TIMEOUT = 5,     /* device: a bounded wait ran out                */
+  OSCAR_ERR_CUDA = 6,        /* a CUDA runtime call failed                    */
+  OSCAR_ERR_STATE = 7        /* device: cache state does not allow the call   */
+} oscar_status;
+
+typedef enum {
+  OSCAR_ROT_OSCAR = 0,    /* R = U·H·P_br                          */
+  OSCAR_ROT_HADAMARD = 1, /* R = H (Hadamard-only baseline)        */
+  OSCAR_ROT_NONE = 2      /* R = I (naive INT2)                    */
+} oscar_rot_mode;
+
+typedef enum {
+  OSCAR_OPT_DECODE_IMPL = 0, /* 0: tensor-core INT2 kernel (default); 1: CUDA-core fp32 kernel */
+  OSCAR_OPT_CTAS_PER_SM = 1, /* persistent decode CTAs per SM, 1..4 (default 2)               */
+  OSCAR_OPT_ITEMS_PER_CTA = 2 /* work items per decode CTA the scheduler aims for, 1..8 (default 3) */
+} oscar_option;
+
+typedef struct {
+  int num_layers;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;          /* must be 128 */
+  int group_size;        /* 32, 64 or 128 */
+  int page_size;         /* must be 64 */
+  int sink_tokens;       /* must be 64 */
+  int recent_tokens;     /* must be 256 */
+  int max_batch;         /* largest batch any call will pass */
+  int max_pages_per_req; /* row length of every page table */
+  int num_pages;         /* pages in each layer's pool */
+} oscar_config;
+
+typedef struct {
+  size_t int2_head_bytes;   /* one KV head's block in an INT2 page          */
+  size_t int2_page_bytes;   /* whole INT2 page (num_kv_heads blocks)        */
+  size_t off_k_codes;       /* offsets inside a head block                  */
+  size_t off_v_codes;
+  size_t off_k_sz;
+  size_t off_v_sz;
+  size_t bf16_head_bytes;   /* one KV head's block in a BF16 page (32768)   */
+  size_t bf16_page_bytes;
+  size_t sink_bytes;        /* bytes of sink_k (or sink_v) at max_batch     */
+  size_t ring_bytes;        /* bytes of ring_k (or ring_v) at max_batch     */
+  size_t decode_scratch_bytes; /* scratch oscar_decode* needs at max_batch  */
+} oscar_layout_info;
+
+/* One layer's cache.  Every pointer is a device pointer owned by the caller.
+ * seq_lens[b] = tokens cached for request b; hist_lens[b] = how many of them
+ * are in INT2 history.  Both are read and updated by the kernels, so each
+ * layer needs its own pair of arrays. */
+typedef struct {
+  void* pool;              /* INT2 pool (or BF16 pool for the baseline calls) */
+  const int32_t* page_table; /* [max_batch][max_pages_per_req]; -1 = no page */
+  void* sink_k;
+  void* sink_v;
+  void* ring_k;
+  void* ring_v;
+  int32_t* seq_lens;       /* [max_batch] */
+  int32_t* hist_lens;      /* [max_batch] */
+} oscar_cache;
+
+typedef struct oscar_ctx oscar_ctx;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int oscar_version(void);
+
+/* Static text for a status code. */
+const char* oscar_status_string(int status);
+
+/* Sizes and offsets of every buffer for a configuration.  Host only; needs
+ * no GPU.  Returns OSCAR_ERR_UNSUPPORTED / OSCAR_ERR_INVALID_ARG for
+ * configurations the kernels do not support. */
+oscar_status oscar_layout(const oscar_config* cfg, oscar_layout_info* out);
+
+/* Create a context on the current CUDA device: validates cfg, allocates the
+ * rotation tables (identity rotation, clip 1.0 for every layer and head) and
+ * the error word.  *out receives the context. */
+oscar_status oscar_create(const oscar_config* cfg, oscar_ctx** out);
+
+/* Free a context and everything it owns.  Synchronises the device first. */
+oscar_status oscar_destroy(oscar_ctx* ctx);
+
+/* Set a tuning option (oscar_option).  Host only. */
+oscar_status oscar_set_option(oscar_ctx* ctx, int option, int value);
+
+/* Load one layer's rotation and clip ratios [News, "OSCAR 的不同之处";
+ * Blog, "OSCAR把旋转对准attention": fixed per layer and head after offline
+ * calibration].
+ *   U_K, U_V : host float [num_kv_heads][128][128], row-major; column i is
+ *              the i-th eigenvector (descending eigenvalue).  The rotation
+ *              applied is x' = x·U·H·P_br (OSCAR mode).  Ignored (may be NULL)
+ *              in HADAMARD and NONE modes.
+ *   clip_k, clip_v : host float [num_kv_heads], ratios in (0, 1].
+ *   rot_mode : oscar_rot_mode.
+ * Copies host memory on `stream` and synchronises it before returning. */
+oscar_status oscar_set_rotation(oscar_ctx* ctx, int layer, const float* U_K,
+                                const float* U_V, const float* clip_k,
+                                const float* clip_v, int rot_mode,
+                                oscar_stream_t stream);
+
+/* Append one token per request [Blog, pipeline figure paragraph]: for each
+ * b < batch and KV head, if the recent window already holds 256 tokens, its
+ * oldest token is first rotated, clipped, quantised and packed into history
+ * slot hist_lens[b] (page page_table[b][slot/64], row slot%64; hist_lens[b]
+ * += 1); then the new token is written to sink[L] (L < 64) or ring slot
+ * (L - 64) % 256, and seq_lens[b] += 1.
+ *   k_new, v_new : device bf16 [batch][num_kv_heads][128].
+ * Device errors: OSCAR_ERR_NO_PAGE if the history page is -1,
+ * OSCAR_ERR_RANGE if the page id is >= num_pages or the slot is beyond
+ * max_pages_per_req; the request is then left unchanged. */
+oscar_status oscar_append(oscar_ctx* ctx, int layer, const oscar_cache* cache,
+                          const void* k_new, const void* v_new, int batch,
+                          oscar_stream_t stream);
+
+/* Demote the oldest recent token of every request into history without
+ * appending (the window shrinks by one).  Requests with an empty window are
+ * left unchanged. */
+oscar_status oscar_demote(oscar_ctx* ctx, int layer, const oscar_cache* cache,
+                          int batch, oscar_stream_t stream);
+
+/* Bulk import of n tokens into empty requests (seq_lens[b] must be 0):
+ * the same cache state as n appends.  K, V: device bf16 [batch][num_kv_heads]
+ * [n][128].  Device error OSCAR_ERR_STATE if a request is not empty. */
+oscar_status oscar_import_tokens(oscar_ctx* ctx, int layer,
+                                 const oscar_cache* cache, const void* K,
+                                 const void* V, int batch, int n,
+                                 oscar_stream_t stream);
+
+/* Decode attention for one new query token per request over the three
+ * regions [Blog, pipeline figure paragraph: INT2 kernel unpack + scale/zero
+ * dequantisation + float accumulation, BF16 kernel for sink/recent, online
+ * softmax merge].  q' = q·R_K is formed on the device; the history partial
+ * is un-rotated by R_V^T before the merge.
+ *   q   : device bf16 [batch][num_q_heads][128]
+ *   out : device bf16 [batch][num_q_heads][128]
+ *   lse : device float [batch][num_q_heads] natural-log log-sum-exp of the
+ *         scaled logits, or NULL
+ *   scratch : device buffer of at least decode_scratch_bytes
+ *             (oscar_layout) bytes, 256-byte aligned; no initial contents
+ *             needed; not to be shared by calls that may overlap.
+ * Requests with seq_lens[b] == 0 produce zeros and lse = -inf. */
+oscar_status oscar_decode(oscar_ctx* ctx, int layer, const oscar_cache* cache,
+                          const void* q, void* out, float* lse, void* scratch,
+                          size_t scratch_bytes, int batch,
+                          oscar_stream_t stream);
+
+/* Baseline with the same split-K design, over a BF16 history pool (no
+ * rotation, no quantisation): the comparison point for the speedup the
+ * pages report against BF16 KV [News, "结果"; Blog, paragraph after
+ * "精度只是第一关"].  Same arguments as oscar_decode; cache->pool is a
+ * BF16 pool. */
+oscar_status oscar_decode_bf16_history(oscar_ctx* ctx, const oscar_cache* cache,
+                                       const void* q, void* out, float* lse,
+                                       void* scratch, size_t scratch_bytes,
+                                       int batch, oscar_stream_t stream);
+
+/* Bulk import of n tokens into empty requests of a BF16-history cache
+ * (history stored unrotated in bf16).  Arguments as oscar_import_tokens. */
+oscar_status oscar_import_bf16_history(oscar_ctx* ctx, const oscar_cache* cache,
+                                       const void* K, const void* V, int batch,
+                                       int n, oscar_stream_t stream);
+
+/* Test hook: the demotion's quantiser and packer on given rotated fp32
+ * vectors, so that codes and bytes can be compared bit for bit.
+ *   x : device float [n][128] rotated channels
+ *   which = 0: codes -> device uint8 [n][32] K rows (K layout);
+ *   which = 1: codes -> device uint8 [n/64][2048] V blocks (token i in slot
+ *              i%64 of block i/64); n must be a multiple of 64.
+ *   sz : device fp16 pairs [n][128/group_size][2] (scale, zero). */
+oscar_status oscar_quantize_rotated_f32(const float* x, int n, int group_size,
+                                        float clip, int which, uint8_t* codes,
+                                        void* sz, oscar_stream_t stream);
+
+/* Test hook: rotate n bf16 vectors of one KV head with the layer's R_K
+ * (which = 0) or R_V (which = 1): x_rot = x·R.  x: device bf16 [n][128];
+ * x_rot: device float [n][128]. */
+oscar_status oscar_debug_rotate(oscar_ctx* ctx, int layer, int which,
+                                int kv_head, const void* x, float* x_rot,
+                                int n, oscar_stream_t stream);
+
+/* Synchronise `stream`, return the first device-side error recorded since
+ * the last call in *code (OSCAR_OK if none) and clear it. */
+oscar_status oscar_get_error(oscar_ctx* ctx, oscar_stream_t stream, int* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSCAR_H */

@@ -319,13 +319,16 @@ def int2_head_block_bytes(g: int, d: int = 128) -> int:
 
 
 def parse_head_block(block: np.ndarray, g: int, d: int = 128):
-    """One page's block for one kv head -> dict of codes and fp16 s/z arrays."""
-    block = np.asarray(block, dtype=np.uint8)
+    """Head blocks [..][bytes] of INT2 pages -> dict of codes and fp16 s/z arrays
+    (k_codes [..][64][128], v_codes [..][64 tokens][128], *_s / *_z [..][64][d/g])."""
+    block = np.ascontiguousarray(np.asarray(block, dtype=np.uint8))
+    lead = block.shape[:-1]
     ng = d // g
-    kc = block[0:2048].reshape(64, 32)
-    vc = block[2048:4096]
-    ksz = block[4096:4096 + 64 * ng * 4].view(np.float16).reshape(64, ng, 2)
-    vsz = block[4096 + 64 * ng * 4:4096 + 2 * 64 * ng * 4].view(np.float16).reshape(64, ng, 2)
+    kc = block[..., 0:2048].reshape(lead + (64, 32))
+    vc = block[..., 2048:4096]
+    szb = 64 * ng * 4
+    ksz = np.ascontiguousarray(block[..., 4096:4096 + szb]).view(np.float16).reshape(lead + (64, ng, 2))
+    vsz = np.ascontiguousarray(block[..., 4096 + szb:4096 + 2 * szb]).view(np.float16).reshape(lead + (64, ng, 2))
     return {
         "k_codes": unpack_k_rows(kc),
         "v_codes": unpack_v_blocks(vc),

@@ -1,0 +1,112 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every
+symbol include/oscar.h declares, and rejects bad arguments on the host."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from bit_kv_cache_int2_gb300 import build as B
+from bit_kv_cache_int2_gb300 import oscar
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return oscar.lib()
+
+
+def header_functions():
+    with open(os.path.join(ROOT, "include", "oscar.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:oscar_status|int|const char\*)\s+(oscar_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for n in ("oscar_create", "oscar_destroy", "oscar_layout", "oscar_set_rotation", "oscar_append",
+              "oscar_demote", "oscar_import_tokens", "oscar_decode", "oscar_decode_bf16_history",
+              "oscar_quantize_rotated_f32", "oscar_debug_rotate", "oscar_get_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", oscar.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (oscar_\w+)", out))
+    for n in header_functions():
+        assert n in exported, n
+        assert hasattr(lib, n)
+    assert set(oscar.exported_symbols()) <= exported
+
+
+def test_version_and_status_strings(lib):
+    assert oscar.oscar_version() >= 10000
+    assert oscar.status_string(oscar.OK) == "ok"
+    assert "page" in oscar.status_string(oscar.ERR_NO_PAGE)
+
+
+@pytest.mark.parametrize("g,head", [(128, 4608), (64, 5120), (32, 6144)])
+def test_layout_sizes(lib, g, head):
+    cfg = oscar.make_config(1, 32, 8, g, max_batch=4, max_pages_per_req=100, num_pages=400)
+    info = oscar.oscar_layout(cfg)
+    assert info.int2_head_bytes == head
+    assert info.int2_page_bytes == 8 * head
+    assert (info.off_k_codes, info.off_v_codes, info.off_k_sz) == (0, 2048, 4096)
+    assert info.off_v_sz == 4096 + 64 * (128 // g) * 4
+    assert info.bf16_head_bytes == 32768
+    assert info.sink_bytes == 4 * 8 * 64 * 128 * 2
+    assert info.ring_bytes == 4 * 8 * 256 * 128 * 2
+    assert info.decode_scratch_bytes > 4 * 32 * 128 * 4
+
+
+def test_layout_rejects_unsupported(lib):
+    for kw, st in ((dict(group_size=16), oscar.ERR_UNSUPPORTED), (dict(num_q_heads=48), oscar.ERR_UNSUPPORTED),
+                   (dict(num_q_heads=30), oscar.ERR_INVALID_ARG), (dict(max_batch=0), oscar.ERR_INVALID_ARG)):
+        args = dict(num_layers=1, num_q_heads=32, num_kv_heads=8, group_size=128, max_batch=1,
+                    max_pages_per_req=1, num_pages=1)
+        args.update(kw)
+        with pytest.raises(oscar.OscarError) as e:
+            oscar.oscar_layout(oscar.make_config(**args))
+        assert e.value.status == st
+    cfg = oscar.make_config()
+    cfg.head_dim = 64
+    with pytest.raises(oscar.OscarError) as e:
+        oscar.oscar_layout(cfg)
+    assert e.value.status == oscar.ERR_UNSUPPORTED
+
+
+def test_null_and_bad_arguments_rejected_on_host(lib):
+    L = lib
+    cs = oscar.oscar_cache()
+    assert L.oscar_decode(None, 0, ctypes.byref(cs), None, None, None, None, 0, 1, None) == oscar.ERR_INVALID_ARG
+    assert L.oscar_append(None, 0, ctypes.byref(cs), None, None, 1, None) == oscar.ERR_INVALID_ARG
+    assert L.oscar_destroy(None) == oscar.ERR_INVALID_ARG
+    assert L.oscar_get_error(None, None, None) == oscar.ERR_INVALID_ARG
+    assert L.oscar_set_option(None, 0, 0) == oscar.ERR_INVALID_ARG
+    # quantiser hook validation happens before any device work
+    fake = ctypes.c_void_p(256)
+    assert L.oscar_quantize_rotated_f32(fake, 10, 16, 1.0, 0, fake, fake, None) == oscar.ERR_UNSUPPORTED
+    assert L.oscar_quantize_rotated_f32(fake, 10, 128, 1.0, 1, fake, fake, None) == oscar.ERR_INVALID_ARG
+    assert L.oscar_quantize_rotated_f32(fake, 64, 128, 1.5, 1, fake, fake, None) == oscar.ERR_INVALID_ARG
+    assert L.oscar_quantize_rotated_f32(fake, 64, 128, 0.0, 0, fake, fake, None) == oscar.ERR_INVALID_ARG
+    assert L.oscar_quantize_rotated_f32(None, 64, 128, 1.0, 0, fake, fake, None) == oscar.ERR_INVALID_ARG
+
+
+def test_create_without_gpu_reports_cuda_error(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(oscar.OscarError) as e:
+        oscar.oscar_create(oscar.make_config())
+    assert e.value.status == oscar.ERR_CUDA
+
+
+def test_binding_fails_loudly_without_library(monkeypatch):
+    monkeypatch.setattr(oscar, "_lib", None)
+    monkeypatch.setattr(oscar, "LIB_PATH", "/nonexistent/liboscar.so")
+    with pytest.raises(RuntimeError):
+        oscar.lib()
