@@ -11,6 +11,42 @@
 
 using namespace oscar;
 
+namespace oscar {
+// Event pairs recorded around kernel launches while profiling is on.
+struct Profiler {
+  bool on = false;
+  std::vector<cudaEvent_t> pool;  // created lazily, reused
+  std::vector<int> kid;           // kernel id per recorded pair
+  size_t used = 0;                // events in use (2 per pair)
+  cudaEvent_t pending = nullptr;
+};
+
+void prof_begin(Profiler* p, int, cudaStream_t st) {
+  if (!p || !p->on) return;
+  if (p->used + 2 > p->pool.size()) {
+    if (p->pool.size() >= 2 * 65536) return;
+    cudaEvent_t a, b;
+    if (cudaEventCreate(&a) != cudaSuccess) return;
+    if (cudaEventCreate(&b) != cudaSuccess) {
+      cudaEventDestroy(a);
+      return;
+    }
+    p->pool.push_back(a);
+    p->pool.push_back(b);
+  }
+  p->pending = p->pool[p->used];
+  cudaEventRecord(p->pending, st);
+}
+
+void prof_end(Profiler* p, int kernel_id, cudaStream_t st) {
+  if (!p || !p->on || !p->pending) return;
+  cudaEventRecord(p->pool[p->used + 1], st);
+  p->kid.push_back(kernel_id);
+  p->used += 2;
+  p->pending = nullptr;
+}
+}  // namespace oscar
+
 struct oscar_ctx {
   oscar_config cfg;
   int device = 0;
@@ -24,6 +60,7 @@ struct oscar_ctx {
   int impl = 0;
   int ctas_per_sm = 2;
   int items_per_cta = 3;
+  Profiler prof;
 };
 
 namespace {
@@ -105,7 +142,10 @@ LayerRot layer_rot(const oscar_ctx* ctx, int layer) {
   return r;
 }
 
-oscar_status cuda_status(cudaError_t e) { return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA; }
+oscar_status cuda_status(cudaError_t e) {
+  if (e != cudaSuccess) (void)cudaGetLastError();  // leave no stale error for the next call
+  return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
 
 oscar_status decode_common(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* q,
                            void* out, float* lse, void* scratch, size_t scratch_bytes, int batch,
@@ -134,7 +174,7 @@ oscar_status decode_common(oscar_ctx* ctx, int layer, const oscar_cache* cache, 
   a.bf16_history = bf16_history ? 1 : 0;
   a.rot = layer_rot(ctx, layer);
   const int grid = ctx->num_sms * ctx->ctas_per_sm;
-  return cuda_status(launch_decode(a, grid, (cudaStream_t)stream));
+  return cuda_status(launch_decode(a, grid, (cudaStream_t)stream, &ctx->prof));
 }
 
 }  // namespace
@@ -229,6 +269,7 @@ oscar_status oscar_destroy(oscar_ctx* ctx) {
   if (ctx->d_clip) cudaFree(ctx->d_clip);
   if (ctx->d_err) cudaFree(ctx->d_err);
   if (ctx->d_req_counter) cudaFree(ctx->d_req_counter);
+  for (cudaEvent_t e : ctx->prof.pool) cudaEventDestroy(e);
   delete ctx;
   return OSCAR_OK;
 }
@@ -305,7 +346,7 @@ static oscar_status append_common(oscar_ctx* ctx, int layer, const oscar_cache* 
   const CacheView cv = make_view(ctx, cache, false);
   return cuda_status(launch_append(cv, layer_rot(ctx, layer), (const __nv_bfloat16*)k,
                                    (const __nv_bfloat16*)v, batch, do_append, ctx->d_req_counter,
-                                   (cudaStream_t)stream));
+                                   (cudaStream_t)stream, &ctx->prof));
 }
 
 oscar_status oscar_append(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* k_new,
@@ -331,7 +372,7 @@ static oscar_status import_common(oscar_ctx* ctx, int layer, const oscar_cache* 
   const CacheView cv = make_view(ctx, cache, bf16_history != 0);
   return cuda_status(launch_import(cv, layer_rot(ctx, layer), (const __nv_bfloat16*)K,
                                    (const __nv_bfloat16*)V, batch, n, bf16_history,
-                                   (cudaStream_t)stream));
+                                   (cudaStream_t)stream, &ctx->prof));
 }
 
 oscar_status oscar_import_tokens(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* K,
@@ -391,6 +432,37 @@ oscar_status oscar_get_error(oscar_ctx* ctx, oscar_stream_t stream, int* code) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return OSCAR_ERR_CUDA;
   *code = h;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_profile_enable(oscar_ctx* ctx, int enable) {
+  if (!ctx) return OSCAR_ERR_INVALID_ARG;
+  ctx->prof.on = enable != 0;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_profile_read(oscar_ctx* ctx, int kernel_id, int* launches, double* total_ms,
+                                int reset) {
+  if (!ctx || !launches || !total_ms || kernel_id < 0 || kernel_id >= OSCAR_KERNEL_COUNT)
+    return OSCAR_ERR_INVALID_ARG;
+  Profiler& p = ctx->prof;
+  int n = 0;
+  double ms = 0.0;
+  for (size_t i = 0; i < p.kid.size(); ++i) {
+    if (p.kid[i] != kernel_id) continue;
+    if (cudaEventSynchronize(p.pool[2 * i + 1]) != cudaSuccess) return cuda_status(cudaErrorUnknown);
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, p.pool[2 * i], p.pool[2 * i + 1]) != cudaSuccess)
+      return cuda_status(cudaErrorUnknown);
+    ms += t;
+    ++n;
+  }
+  *launches = n;
+  *total_ms = ms;
+  if (reset) {
+    p.kid.clear();
+    p.used = 0;
+  }
   return OSCAR_OK;
 }
 

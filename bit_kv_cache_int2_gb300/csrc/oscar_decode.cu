@@ -51,9 +51,11 @@ struct SmemLayout {
   int off_stage, off_mbar, off_qb, off_consts, off_qf, off_vs, off_pre, off_red, off_misc, total;
 };
 
+// impl: 0 tensor-core INT2, 1 CUDA-core INT2, 2 BF16 history (no INT2 pages)
 __host__ __device__ inline SmemLayout smem_layout(int head_bytes, int B, int impl) {
   SmemLayout L;
-  L.stage_bytes = (head_bytes + 127) & ~127;
+  // BF16 paths read global memory directly; only INT2 pages use stages
+  L.stage_bytes = impl == 2 ? 0 : (head_bytes + 127) & ~127;
   int o = 0;
   L.off_stage = o;
   int stage_total = NW * DEPTH * L.stage_bytes;
@@ -470,7 +472,7 @@ template <int NG, int IMPL>
 __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheView& cv = a.cv;
-  const SmemLayout L = smem_layout(cv.head_bytes, a.B, IMPL);
+  const SmemLayout L = smem_layout(cv.head_bytes, a.B, a.bf16_history ? 2 : IMPL);
   uint64_t* mbar = (uint64_t*)(smem + L.off_mbar);
   __half* qb = (__half*)(smem + L.off_qb);
   float* kconst = (float*)(smem + L.off_consts);  // [MAX_G] alpha, [MAX_G][4] beta, [MAX_G][4] gamma
@@ -885,7 +887,7 @@ __global__ void __launch_bounds__(512) merge_kernel(DecodeArgs a, int GP) {
 
 template <int NG, int IMPL>
 cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t st) {
-  const SmemLayout L = smem_layout(a.cv.head_bytes, a.B, IMPL);
+  const SmemLayout L = smem_layout(a.cv.head_bytes, a.B, a.bf16_history ? 2 : IMPL);
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<NG, IMPL>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (e != cudaSuccess) return e;
@@ -902,14 +904,17 @@ size_t decode_scratch_bytes(int B, int Hq, int Hkv, int G, int max_target_items)
   return head + qrot + slots * G * PART_STRIDE * 4;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a0, int grid, cudaStream_t st) {
+cudaError_t launch_decode(const DecodeArgs& a0, int grid, cudaStream_t st, Profiler* prof) {
   DecodeArgs a = a0;
   const CacheView& cv = a.cv;
+  prof_begin(prof, OSCAR_KERNEL_DECODE_PREP, st);
   prep_kernel<<<a.bf16_history ? 1 : a.B * cv.Hkv, 128, 0, st>>>(a.q, a.qrot, a.counter, a.rot,
                                                                   cv.Hq, cv.Hkv, cv.G,
                                                                   !a.bf16_history);
+  prof_end(prof, OSCAR_KERNEL_DECODE_PREP, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  prof_begin(prof, OSCAR_KERNEL_DECODE_MAIN, st);
   if (a.impl == 1 && !a.bf16_history) {
     if (cv.NG == 1) e = launch_decode_t<1, 1>(a, grid, st);
     else if (cv.NG == 2) e = launch_decode_t<2, 1>(a, grid, st);
@@ -919,10 +924,13 @@ cudaError_t launch_decode(const DecodeArgs& a0, int grid, cudaStream_t st) {
     else if (cv.NG == 2) e = launch_decode_t<2, 0>(a, grid, st);
     else e = launch_decode_t<4, 0>(a, grid, st);
   }
+  prof_end(prof, OSCAR_KERNEL_DECODE_MAIN, st);
   if (e != cudaSuccess) return e;
   const int GP = cv.G < 4 ? cv.G : 4;
   const size_t msm = (size_t)2 * GP * D * 4 + 32 * 4 + ((size_t)a.B + 1) * 4;
+  prof_begin(prof, OSCAR_KERNEL_DECODE_MERGE, st);
   merge_kernel<<<a.B * cv.Hkv, 128 * GP, msm, st>>>(a, GP);
+  prof_end(prof, OSCAR_KERNEL_DECODE_MERGE, st);
   return cudaGetLastError();
 }
 

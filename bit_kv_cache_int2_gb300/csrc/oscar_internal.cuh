@@ -394,6 +394,11 @@ __device__ __forceinline__ void hist_item_coords(int q, const int* pre, int B, i
 }
 
 // ------------------------------------------------------------- launchers
+// Optional per-kernel event recording (see oscar_profile_enable).
+struct Profiler;
+void prof_begin(Profiler* p, int kernel_id, cudaStream_t st);
+void prof_end(Profiler* p, int kernel_id, cudaStream_t st);
+
 struct DecodeArgs {
   CacheView cv;
   const __nv_bfloat16* q;  // [B][Hq][128]
@@ -409,15 +414,15 @@ struct DecodeArgs {
   LayerRot rot;
 };
 
-cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof);
 size_t decode_scratch_bytes(int B, int Hq, int Hkv, int G, int max_target_items);
 
 cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* k,
                           const __nv_bfloat16* v, int B, int do_append, int* req_counter,
-                          cudaStream_t st);
+                          cudaStream_t st, Profiler* prof);
 cudaError_t launch_import(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* K,
                           const __nv_bfloat16* V, int B, int n, int bf16_history,
-                          cudaStream_t st);
+                          cudaStream_t st, Profiler* prof);
 cudaError_t launch_quantize_hook(const float* x, int n, int g, float clip, int which,
                                  uint8_t* codes, __half2* sz, cudaStream_t st);
 cudaError_t launch_debug_rotate(const float* U, int mode, const __nv_bfloat16* x, float* y,

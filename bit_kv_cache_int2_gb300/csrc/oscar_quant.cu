@@ -356,14 +356,17 @@ __global__ void __launch_bounds__(128) debug_rotate_kernel(const float* __restri
 
 cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* k,
                           const __nv_bfloat16* v, int B, int do_append, int* req_counter,
-                          cudaStream_t st) {
+                          cudaStream_t st, Profiler* prof) {
+  prof_begin(prof, OSCAR_KERNEL_APPEND, st);
   append_kernel<<<B * cv.Hkv, 256, 0, st>>>(cv, rot, k, v, do_append, req_counter);
+  prof_end(prof, OSCAR_KERNEL_APPEND, st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_import(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* K,
                           const __nv_bfloat16* V, int B, int n, int bf16_history,
-                          cudaStream_t st) {
+                          cudaStream_t st, Profiler* prof) {
+  prof_begin(prof, OSCAR_KERNEL_IMPORT, st);
   import_window_kernel<<<B * cv.Hkv, 256, 0, st>>>(cv, K, V, n);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -379,6 +382,7 @@ cudaError_t launch_import(const CacheView& cv, const LayerRot& rot, const __nv_b
     if (e != cudaSuccess) return e;
   }
   import_set_lengths_kernel<<<(B + 127) / 128, 128, 0, st>>>(cv.seq_lens, cv.hist_lens, B, n);
+  prof_end(prof, OSCAR_KERNEL_IMPORT, st);
   return cudaGetLastError();
 }
 

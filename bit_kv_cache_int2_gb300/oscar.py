@@ -92,7 +92,17 @@ _SIGS = {
     "oscar_debug_rotate": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                             ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
     "oscar_get_error": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
+    "oscar_profile_enable": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
+    "oscar_profile_read": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                            ctypes.POINTER(ctypes.c_double), ctypes.c_int], ctypes.c_int),
 }
+
+KERNEL_APPEND = 0
+KERNEL_IMPORT = 1
+KERNEL_DECODE_PREP = 2
+KERNEL_DECODE_MAIN = 3
+KERNEL_DECODE_MERGE = 4
+KERNEL_NAMES = {0: "append", 1: "import", 2: "decode_prep", 3: "decode_main", 4: "decode_merge"}
 
 
 def exported_symbols():
@@ -244,6 +254,19 @@ def oscar_get_error(ctx, stream=None) -> int:
     code = ctypes.c_int(0)
     _check(lib().oscar_get_error(ctx, _stream(stream), ctypes.byref(code)), "oscar_get_error")
     return code.value
+
+
+def oscar_profile_enable(ctx, enable: bool):
+    _check(lib().oscar_profile_enable(ctx, 1 if enable else 0), "oscar_profile_enable")
+
+
+def oscar_profile_read(ctx, kernel_id: int, reset: bool = False):
+    """(launches, total_ms) of one kernel since the last reset."""
+    n = ctypes.c_int(0)
+    ms = ctypes.c_double(0.0)
+    _check(lib().oscar_profile_read(ctx, kernel_id, ctypes.byref(n), ctypes.byref(ms), 1 if reset else 0),
+           "oscar_profile_read")
+    return n.value, ms.value
 
 
 # ---------------------------------------------------------------- plumbing

@@ -272,6 +272,26 @@ oscar_status oscar_debug_rotate(oscar_ctx* ctx, int layer, int which,
  * the last call in *code (OSCAR_OK if none) and clear it. */
 oscar_status oscar_get_error(oscar_ctx* ctx, oscar_stream_t stream, int* code);
 
+/* Kernel timing (tracing).  The pages describe no profiler; this is the
+ * library's own instrumentation.  While enabled, every kernel the context
+ * launches is bracketed by a pair of CUDA events recorded on the launching
+ * stream (at most 65536 launches are kept).  oscar_profile_read waits for the
+ * recorded events, returns for kernel `kernel_id` (oscar_kernel) the number
+ * of launches and their summed device time in milliseconds, and with
+ * reset != 0 forgets everything recorded so far. */
+typedef enum {
+  OSCAR_KERNEL_APPEND = 0,      /* append / demote                      */
+  OSCAR_KERNEL_IMPORT = 1,      /* all bulk-import kernels              */
+  OSCAR_KERNEL_DECODE_PREP = 2, /* q rotation, work-counter reset       */
+  OSCAR_KERNEL_DECODE_MAIN = 3, /* split-K decode over history + window */
+  OSCAR_KERNEL_DECODE_MERGE = 4,/* partial merge + un-rotation          */
+  OSCAR_KERNEL_COUNT = 5
+} oscar_kernel;
+
+oscar_status oscar_profile_enable(oscar_ctx* ctx, int enable);
+oscar_status oscar_profile_read(oscar_ctx* ctx, int kernel_id, int* launches,
+                                double* total_ms, int reset);
+
 #ifdef __cplusplus
 }
 #endif
