@@ -164,10 +164,14 @@ oscar_status decode_common(oscar_ctx* ctx, int layer, const oscar_cache* cache, 
   a.q = (const __nv_bfloat16*)q;
   a.out = (__nv_bfloat16*)out;
   a.lse = lse;
-  a.counter = (int*)scratch;
-  a.qrot = (float*)((uint8_t*)scratch + 256);
-  const size_t qbytes = (((size_t)batch * ctx->cfg.num_q_heads * D * 4) + 255) & ~(size_t)255;
-  a.part = (float*)((uint8_t*)scratch + 256 + qbytes);
+  const ScratchLayout sl =
+      scratch_layout(batch, ctx->cfg.num_q_heads, ctx->cfg.num_kv_heads, ctx->G, target);
+  uint8_t* sp = (uint8_t*)scratch;
+  a.counter = (int*)(sp + sl.off_counter);
+  a.done = (int*)(sp + sl.off_done);
+  a.qrot = (float*)(sp + sl.off_qrot);
+  a.qpack = sp + sl.off_qpack;
+  a.part = (float*)(sp + sl.off_part);
   a.B = batch;
   a.target_items = target;
   a.impl = ctx->impl;

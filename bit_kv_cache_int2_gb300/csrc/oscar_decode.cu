@@ -10,12 +10,16 @@
 // un-rotated by R_V^T before the final merge.
 //
 // Kernels (one stream, in order):
-//   prep_kernel      q' = q·U_K·H·P_br for every query head; resets the work counter
-//   decode_kernel    persistent split-K: work items are (request, kv head, S pages)
-//                    of INT2 (or BF16) history, or one BF16 window per (request,
-//                    kv head); each item writes an online-softmax partial
-//   merge_kernel     per (request, kv head): LSE-merge of the history partials,
-//                    un-rotation by R_V^T, LSE-merge with the window partial
+//   prep_kernel    q' = q·U_K·H·P_br for every query head, packed as the fp16
+//                  B operand of the tensor-core QK^T plus per-head logit
+//                  constants; resets the work and merge counters
+//   decode_kernel  persistent split-K, launched as a programmatic dependent of
+//                  prep_kernel: each CTA starts fetching its first pages before
+//                  waiting for q'.  Work items are (request, kv head, S pages)
+//                  of history or one BF16 window per (request, kv head); each
+//                  item writes an online-softmax partial, and the last CTA to
+//                  finish an item of a (request, kv head) merges its partials,
+//                  un-rotates the history part by R_V^T and writes the output.
 #include "oscar_internal.cuh"
 
 namespace oscar {
@@ -25,30 +29,121 @@ namespace {
 constexpr int NW = 4;     // warps per decode CTA
 constexpr int DEPTH = 4;  // bulk-copy stages per warp
 
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+// Per (request, query head) record of the packed query (QPACK_BYTES):
+//   half  qb[128]   q'_c * 2^-sigma * 2^(8 - E(c)), the QK^T B operand
+//   float alpha     2^sigma * log2(e) / (256 sqrt(d))
+//   float beta[4]   -1024 * (sum of qb over group) * alpha
+//   float gamma[4]  (sum of q' over group) * log2(e) / sqrt(d)
+constexpr int QPACK_ALPHA = 256, QPACK_BETA = 260, QPACK_GAMMA = 276;
+
 // ------------------------------------------------------------------- prep
-// grid = B * Hkv (INT2) or 1 (BF16 history), block 128.
-__global__ void __launch_bounds__(128) prep_kernel(const __nv_bfloat16* __restrict__ q, float* qrot,
-                                                   int* counter, LayerRot rot, int Hq, int Hkv,
-                                                   int G, int do_rotate) {
-  __shared__ float xs[D];
-  __shared__ float tmp[D];
-  if (blockIdx.x == 0 && threadIdx.x == 0) *counter = 0;
-  if (!do_rotate) return;
-  const int b = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv, j = threadIdx.x;
-  const float* U = rot.U_K + (size_t)kvh * D * D;
-  for (int n = 0; n < G; ++n) {
-    const size_t row = (size_t)b * Hq + kvh * G + n;
-    xs[j] = __bfloat162float(q[row * D + j]);
-    __syncthreads();
-    qrot[row * D + j] = rotate128(xs, U, rot.mode, j, tmp, 1);
-    __syncthreads();
+// grid = B * Hkv, block = 512: four parts of 128 threads split the 128-row
+// matvec x·U; then part p rotates heads p, p + 4.
+__global__ void __launch_bounds__(512) prep_kernel(DecodeArgs a) {
+  pdl_launch_dependents();
+  __shared__ float xs[MAX_G][D];
+  __shared__ float part[4][MAX_G][D];
+  __shared__ float tmp[4][D];
+  __shared__ float red[4][8];
+  const CacheView& cv = a.cv;
+  const int b = blockIdx.x / cv.Hkv, kvh = blockIdx.x % cv.Hkv, t = threadIdx.x;
+  if (t == 0) {
+    a.done[blockIdx.x] = 0;
+    if (blockIdx.x == 0) *a.counter = 0;
+  }
+  if (a.bf16_history) return;
+  const int G = cv.G;
+  for (int e = t; e < G * D; e += 512)
+    xs[e / D][e % D] = __bfloat162float(a.q[((size_t)b * cv.Hq + kvh * G) * D + e]);
+  __syncthreads();
+  const int j = t & 127, pp = t >> 7;
+  float acc[MAX_G];
+#pragma unroll
+  for (int n = 0; n < MAX_G; ++n) acc[n] = 0.f;
+  if (a.rot.mode == OSCAR_ROT_OSCAR) {
+    const float* U = a.rot.U_K + (size_t)kvh * D * D + (size_t)(32 * pp) * D + j;
+    float u[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) u[k] = __ldg(U + k * D);
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+#pragma unroll
+      for (int n = 0; n < MAX_G; ++n)
+        if (n < G) acc[n] = fmaf(xs[n][32 * pp + k], u[k], acc[n]);
+  } else if (pp == 0) {
+#pragma unroll
+    for (int n = 0; n < MAX_G; ++n)
+      if (n < G) acc[n] = xs[n][j];
+  }
+#pragma unroll
+  for (int n = 0; n < MAX_G; ++n) part[pp][n][j] = acc[n];
+  __syncthreads();
+  const int bar = 1 + pp, w4 = j >> 5, lane = j & 31;
+  const int i = 2 * ((j >> 4) & 3) + ((j >> 3) & 1);  // bit pair holding channel j in QK
+  const float f = (float)(1 << (8 - code_exp_rt(i)));
+  for (int n = pp; n < G; n += 4) {
+    float y = (part[0][n][j] + part[1][n][j]) + (part[2][n][j] + part[3][n][j]);
+    if (a.rot.mode != OSCAR_ROT_NONE) {
+      y = fwht128(y, j, tmp[pp], bar);
+      if (a.rot.mode == OSCAR_ROT_OSCAR) {
+        tmp[pp][j] = y;
+        group_sync(bar);
+        y = tmp[pp][bitrev7(j)];
+        group_sync(bar);
+      }
+    }
+    const size_t row = (size_t)b * cv.Hq + kvh * G + n;
+    a.qrot[row * D + j] = y;
+    // power-of-two prescale so that |q'| * 16 stays below 2^14 in fp16
+    float am = fabsf(y);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    if (lane == 0) red[pp][w4] = am;
+    group_sync(bar);
+    am = fmaxf(fmaxf(red[pp][0], red[pp][1]), fmaxf(red[pp][2], red[pp][3]));
+    group_sync(bar);
+    int ex = 0;
+    frexpf(am, &ex);
+    const int sig = am > 0.f ? ex - 10 : 0;
+    const __half hb = __float2half_rn(ldexpf(y, -sig) * f);
+    uint8_t* rec = a.qpack + row * QPACK_BYTES;
+    ((__half*)rec)[j] = hb;
+    float bs = __half2float(hb), qs = y;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      bs += __shfl_xor_sync(0xffffffffu, bs, o);
+      qs += __shfl_xor_sync(0xffffffffu, qs, o);
+    }
+    if (lane == 0) {
+      red[pp][w4] = bs;
+      red[pp][4 + w4] = qs;
+    }
+    group_sync(bar);
+    if (j < cv.NG) {
+      const int wpg = 4 / cv.NG;
+      float bsum = 0.f, qsum = 0.f;
+      for (int w = j * wpg; w < (j + 1) * wpg; ++w) {
+        bsum += red[pp][w];
+        qsum += red[pp][4 + w];
+      }
+      const float alpha = ldexpf(1.f, sig) * LOG2E * INV_SQRT_D * (1.f / 256.f);
+      if (j == 0) *(float*)(rec + QPACK_ALPHA) = alpha;
+      ((float*)(rec + QPACK_BETA))[j] = -1024.f * bsum * alpha;
+      ((float*)(rec + QPACK_GAMMA))[j] = qsum * LOG2E * INV_SQRT_D;
+    }
+    group_sync(bar);
   }
 }
 
 // ------------------------------------------------------------ smem layout
 struct SmemLayout {
   int stage_bytes;   // per stage
-  int off_stage, off_mbar, off_qb, off_consts, off_qf, off_vs, off_pre, off_red, off_misc, total;
+  int off_stage, off_mbar, off_qf, off_vs, off_pre, off_red, off_misc, total;
 };
 
 // impl: 0 tensor-core INT2, 1 CUDA-core INT2, 2 BF16 history (no INT2 pages)
@@ -59,17 +154,16 @@ __host__ __device__ inline SmemLayout smem_layout(int head_bytes, int B, int imp
   int o = 0;
   L.off_stage = o;
   int stage_total = NW * DEPTH * L.stage_bytes;
-  const int wo_bytes = NW * MAX_G * D * 4 + 2 * NW * MAX_G * 4;  // warp results alias the stages
+  // warp results and the merge's working set alias the stages
+  const int wo_bytes = NW * MAX_G * D * 4 + 2 * NW * MAX_G * 4;
+  const int merge_bytes = (2 * MAX_G * D + 2 * D + 4 * MAX_G) * 4;
   if (stage_total < wo_bytes) stage_total = wo_bytes;
+  if (stage_total < merge_bytes) stage_total = merge_bytes;
   o += stage_total;
   L.off_mbar = o;
   o += NW * DEPTH * 8;
-  L.off_qb = o;
-  o += MAX_G * D * 2;  // f16 B operand
-  L.off_consts = o;
-  o += MAX_G * (1 + 4 + 4) * 4;
   L.off_qf = o;
-  if (impl == 1) o += MAX_G * D * 4;  // fp32 q' (CUDA-core path, storage order)
+  if (impl == 1) o += MAX_G * D * 4 + MAX_G * 4 * 4;  // fp32 q' in K storage order + z weights
   L.off_vs = o;
   if (impl == 1) o += NW * (MAX_G * PAGE + 2 * 4 * PAGE) * 4;  // CUDA-core per-warp p and s/z
   L.off_pre = o;
@@ -432,17 +526,11 @@ __device__ __forceinline__ void bf16_chunk_mma(Bf16State& S, const __nv_bfloat16
   }
 }
 
-// ----------------------------------------------------------------- decode
-struct ItemCtx {
-  int b, kvh, slot;
-};
 
-__device__ __forceinline__ void cta_combine_write(const DecodeArgs& a, uint8_t* smem,
-                                                 const SmemLayout& L, int slot) {
-  // warp results: wm[NW][MAX_G], wl[NW][MAX_G], wo[NW][MAX_G][D] aliased on the stages
-  float* wm = (float*)(smem + L.off_stage);
-  float* wl = wm + NW * MAX_G;
-  float* wo = wl + NW * MAX_G;
+// ----------------------------------------------------------------- decode
+// Combine the CTA's warp results (wm, wl, wo) into partial record `slot`.
+__device__ __forceinline__ void cta_combine_write(const DecodeArgs& a, const float* wm,
+                                                 const float* wl, const float* wo, int slot) {
   const int c = threadIdx.x;  // NW * 32 == 128 threads, one channel each
   const int G = a.cv.G;
   for (int n = 0; n < G; ++n) {
@@ -468,19 +556,132 @@ __device__ __forceinline__ void cta_combine_write(const DecodeArgs& a, uint8_t* 
   }
 }
 
+// Final merge of one (request, kv head), by one CTA of 128 threads: LSE-merge
+// of the history partials, un-rotation o = o'·P_br·H·U_V^T, LSE-merge with the
+// window partial, bf16 output.  sm: smem working area (merge_bytes).
+__device__ void merge_bkvh(const DecodeArgs& a, const Sched& sc, const int* pre, int b, int kvh,
+                           float* sm) {
+  const CacheView& cv = a.cv;
+  const int G = cv.G, c = threadIdx.x;
+  float* oh = sm;                  // [MAX_G][D] history output (rotated, then un-rotated)
+  float* y = oh + MAX_G * D;       // [MAX_G][D] un-rotation input
+  float* tmp = y + MAX_G * D;      // [D]
+  float* tmp2 = tmp + D;           // [D]
+  float* mh = tmp2 + D;            // [MAX_G]
+  float* lh = mh + MAX_G;          // [MAX_G]
+  const int pages_b = (cv.hist_lens[b] + PAGE - 1) / PAGE;
+  const int nb = (pages_b + sc.S - 1) / sc.S;
+  const int base = pre[b] + kvh * nb;
+  for (int n = 0; n < G; ++n) {
+    float M = -INFINITY;
+    for (int q = 0; q < nb; ++q) {
+      const float* rec = a.part + ((size_t)(base + q) * G + n) * PART_STRIDE;
+      if (__ldcg(rec + 1) > 0.f) M = fmaxf(M, __ldcg(rec));
+    }
+    float Ls = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+      int q = 0;
+      for (; q + 4 <= nb; q += 4) {
+        float m4[4], l4[4], o4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float* rec = a.part + ((size_t)(base + q + u) * G + n) * PART_STRIDE;
+          m4[u] = __ldcg(rec);
+          l4[u] = __ldcg(rec + 1);
+          o4[u] = __ldcg(rec + 2 + c);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (l4[u] > 0.f) {
+            const float w = ex2(m4[u] - M);
+            Ls = fmaf(l4[u], w, Ls);
+            O = fmaf(o4[u], w, O);
+          }
+      }
+      for (; q < nb; ++q) {
+        const float* rec = a.part + ((size_t)(base + q) * G + n) * PART_STRIDE;
+        const float lq = __ldcg(rec + 1);
+        if (lq > 0.f) {
+          const float w = ex2(__ldcg(rec) - M);
+          Ls = fmaf(lq, w, Ls);
+          O = fmaf(__ldcg(rec + 2 + c), w, O);
+        }
+      }
+    }
+    oh[n * D + c] = O;
+    if (c == 0) {
+      mh[n] = M;
+      lh[n] = Ls;
+    }
+  }
+  __syncthreads();
+  if (!a.bf16_history && a.rot.mode != OSCAR_ROT_NONE) {
+    // o'·P_br then ·H, per head
+    for (int n = 0; n < G; ++n) {
+      float v = oh[n * D + (a.rot.mode == OSCAR_ROT_OSCAR ? bitrev7(c) : c)];
+      v = fwht128(v, c, tmp, 1);
+      y[n * D + c] = v;
+    }
+    __syncthreads();
+    if (a.rot.mode == OSCAR_ROT_OSCAR) {
+      // ·U_V^T for all heads at once: one load of Ut feeds G FMAs
+      const float* Ut = a.rot.Ut_V + (size_t)kvh * D * D + c;
+      float acc[MAX_G];
+#pragma unroll
+      for (int n = 0; n < MAX_G; ++n) acc[n] = 0.f;
+      for (int i0 = 0; i0 < D; i0 += 16) {
+        float u[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) u[k] = __ldg(Ut + (i0 + k) * D);
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+#pragma unroll
+          for (int n = 0; n < MAX_G; ++n)
+            if (n < G) acc[n] = fmaf(y[n * D + i0 + k], u[k], acc[n]);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int n = 0; n < MAX_G; ++n)
+        if (n < G) oh[n * D + c] = acc[n];
+    } else {
+      for (int n = 0; n < G; ++n) oh[n * D + c] = y[n * D + c];
+    }
+    __syncthreads();
+  }
+  const int wslot = sc.n_hist + b * cv.Hkv + kvh;
+  for (int n = 0; n < G; ++n) {
+    const float* w = a.part + ((size_t)wslot * G + n) * PART_STRIDE;
+    const float mw = __ldcg(w), lw = __ldcg(w + 1), ow = __ldcg(w + 2 + c);
+    const float M = mh[n], Ls = lh[n], O = oh[n * D + c];
+    const float M2 = fmaxf(Ls > 0.f ? M : -INFINITY, lw > 0.f ? mw : -INFINITY);
+    float o = 0.f, lse = -INFINITY;
+    if (M2 != -INFINITY) {
+      const float fh = Ls > 0.f ? ex2(M - M2) : 0.f;
+      const float fw = lw > 0.f ? ex2(mw - M2) : 0.f;
+      const float lt = Ls * fh + lw * fw;
+      o = (O * fh + ow * fw) / lt;
+      lse = (M2 + log2f(lt)) * LN2;
+    }
+    const size_t row = (size_t)b * cv.Hq + kvh * G + n;
+    a.out[row * D + c] = __float2bfloat16_rn(o);
+    if (a.lse && c == 0) a.lse[row] = lse;
+  }
+}
+
 template <int NG, int IMPL>
 __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheView& cv = a.cv;
   const SmemLayout L = smem_layout(cv.head_bytes, a.B, a.bf16_history ? 2 : IMPL);
   uint64_t* mbar = (uint64_t*)(smem + L.off_mbar);
-  __half* qb = (__half*)(smem + L.off_qb);
-  float* kconst = (float*)(smem + L.off_consts);  // [MAX_G] alpha, [MAX_G][4] beta, [MAX_G][4] gamma
-  float* qf = (float*)(smem + L.off_qf);
+  float* qf = (float*)(smem + L.off_qf);  // CUDA-core path: [MAX_G][D] q' + [MAX_G][4] z weights
   float* vsw = (float*)(smem + L.off_vs);
   int* pre = (int*)(smem + L.off_pre);
   int* red = (int*)(smem + L.off_red);
   int* misc = (int*)(smem + L.off_misc);
+  float* wm = (float*)(smem + L.off_stage);
+  float* wl = wm + NW * MAX_G;
+  float* wo = wl + NW * MAX_G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tq = lane & 3;
   const int G = cv.G, Hkv = cv.Hkv;
@@ -490,21 +691,16 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
   fence_proxy_async();
   __syncthreads();
 
+  // history lengths and page tables come from earlier stream work: readable
+  // before the wait on prep_kernel
   const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
   const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, unit, pre, red);
   const int total = sc.n_hist + sc.n_win;
   uint32_t seq = 0;  // stages consumed by this warp so far
+  bool waited = false;
+  int it = blockIdx.x;  // first item static, later ones from the work counter
 
-  float* wm = (float*)(smem + L.off_stage);
-  float* wl = wm + NW * MAX_G;
-  float* wo = wl + NW * MAX_G;
-
-  for (;;) {
-    if (threadIdx.x == 0) misc[0] = atomicAdd(a.counter, 1);
-    __syncthreads();
-    const int it = misc[0];
-    __syncthreads();
-    if (it >= total) break;
+  while (it < total) {
     bool is_win;
     int idx;
     if (sc.win_first) {
@@ -556,12 +752,17 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
             Kb = cv.sink_k + head * SINK * D;
             Vb = cv.sink_v + head * SINK * D;
           } else {
-            for (int t = 0; t < 64; ++t) {
-              const int slot_r = 64 * (ch - 1) + t;
-              if (((slot_r - h0 + RECENT) % RECENT) < recent) valid |= 1ull << t;
+            const int s0 = 64 * (ch - 1);
+            // slots s0..s0+63 valid where (slot - h0) mod 256 < recent
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const int t = lane + 32 * half;
+              const bool v = ((s0 + t - h0 + RECENT) % RECENT) < recent;
+              const uint32_t bits = __ballot_sync(0xffffffffu, v);
+              valid |= (uint64_t)bits << (32 * half);
             }
-            Kb = cv.ring_k + (head * RECENT + 64 * (ch - 1)) * D;
-            Vb = cv.ring_v + (head * RECENT + 64 * (ch - 1)) * D;
+            Kb = cv.ring_k + (head * RECENT + s0) * D;
+            Vb = cv.ring_v + (head * RECENT + s0) * D;
           }
           if (valid) bf16_chunk_mma(S, Kb, Vb, valid, lane);
         }
@@ -582,14 +783,13 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
           bf16_chunk_mma(S, Kb, Kb + PAGE * D, valid, lane);
         }
       }
-      // finalize this warp
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
         S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 4);
         S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 8);
         S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 16);
       }
-      __syncthreads();  // everyone is done with the previous item's results
+      __syncthreads();  // everyone is done with the stage area
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
         const int n = 2 * tq + hc;
@@ -605,284 +805,216 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
           }
         }
       }
-      __syncthreads();
-      cta_combine_write(a, smem, L, slot);
-      __syncthreads();
-      continue;
-    }
-
-    // -------------------------------------------------------- INT2 history
-    // Prologue (whole CTA): fp16 B operand of q' and the logit constants.
-    {
-      const int c = threadIdx.x;  // channel
-      const int i = 2 * ((c >> 4) & 3) + ((c >> 3) & 1);  // bit pair holding channel c in QK
-      const float f = (float)(1 << (8 - code_exp_rt(i)));
-      float* ka = kconst;
-      float* kb = kconst + MAX_G;
-      float* kgm = kconst + MAX_G * 5;
-      for (int n = 0; n < MAX_G; ++n) {
-        float qv = 0.f;
-        if (n < G) qv = a.qrot[((size_t)b * cv.Hq + kvh * G + n) * D + c];
-        float am = fabsf(qv);
-#pragma unroll
-        for (int o = 16; o; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-        if (lane == 0) ((float*)red)[warp] = am;
-        __syncthreads();
-        am = fmaxf(fmaxf(((float*)red)[0], ((float*)red)[1]), fmaxf(((float*)red)[2], ((float*)red)[3]));
-        int ex = 0;
-        frexpf(am, &ex);
-        const int sig = am > 0.f ? ex - 10 : 0;  // |q'| * 16 * 2^-sig < 2^14
-        const __half hb = __float2half_rn(ldexpf(qv, -sig) * f);
-        qb[n * D + c] = hb;
-        if (IMPL == 1) {
-          // CUDA-core path: q' in K storage order (word k_word(c), pos k_bit(c)/2)
-          qf[n * D + k_word(c) * 16 + k_bit(c) / 2] = qv;
-        }
-        // group sums of the B values and of q'
-        float bsv = __half2float(hb), qsv = qv;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-          bsv += __shfl_xor_sync(0xffffffffu, bsv, o);
-          qsv += __shfl_xor_sync(0xffffffffu, qsv, o);
-        }
-        __syncthreads();
-        if (lane == 0) {
-          ((float*)red)[warp] = bsv;
-          ((float*)red)[4 + warp] = qsv;
-        }
-        __syncthreads();
-        if (threadIdx.x < NG) {
-          const int gr = threadIdx.x, wpg = NW / NG;
-          float bsum = 0.f, qsum = 0.f;
-          for (int w = gr * wpg; w < (gr + 1) * wpg; ++w) {
-            bsum += ((float*)red)[w];
-            qsum += ((float*)red)[4 + w];
-          }
-          const float alpha = ldexpf(1.f, sig) * LOG2E * INV_SQRT_D * (1.f / 256.f);
-          if (gr == 0) ka[n] = n < G ? alpha : 0.f;
-          kb[n * 4 + gr] = n < G ? -1024.f * bsum * alpha : 0.f;
-          kgm[n * 4 + gr] = n < G ? qsum * LOG2E * INV_SQRT_D : 0.f;
-        }
-        __syncthreads();
-      }
-    }
-    // pages of this item, dealt round-robin to the warps
-    const int p0 = jj * sc.S;
-    int p1 = p0 + sc.S;
-    if (p1 > pages_b) p1 = pages_b;
-    const int nw_pages = (p1 - p0 - warp + NW - 1) / NW > 0 ? (p1 - p0 - warp + NW - 1) / NW : 0;
-    uint8_t* my_stage = smem + L.off_stage + (size_t)warp * DEPTH * L.stage_bytes;
-    uint64_t* my_bar = mbar + warp * DEPTH;
-    auto issue = [&](int k) {  // lane 0 only: k-th page of this warp
-      const int p = p0 + warp + k * NW;
-      const int st = (int)((seq + k) % DEPTH);
-      const int pid = cv.page_table[(size_t)b * cv.max_pages_per_req + p];
-      if (pid >= 0 && pid < cv.num_pages) {
-        mbar_expect_tx(&my_bar[st], (uint32_t)cv.head_bytes);
-        bulk_g2s(my_stage + (size_t)st * L.stage_bytes,
-                 cv.pool + (size_t)pid * cv.page_bytes + (size_t)kvh * cv.head_bytes,
-                 (uint32_t)cv.head_bytes, &my_bar[st]);
-      } else {
-        record_error(cv.err, pid < 0 ? OSCAR_ERR_NO_PAGE : OSCAR_ERR_RANGE);
-        mbar_expect_tx(&my_bar[st], 0u);
-      }
-    };
-    if (lane == 0) {
-      fence_proxy_async();
-      for (int k = 0; k < DEPTH && k < nw_pages; ++k) issue(k);
-    }
-
-    bool timed_out = false;
-    int k_fail = 0;
-    if (IMPL == 0) {
-      Int2State<NG> S;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) S.oacc[j][0] = S.oacc[j][1] = S.oacc[j][2] = S.oacc[j][3] = 0.f;
-#pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        S.m[hc] = -INFINITY;
-        S.l[hc] = 0.f;
-        const int n = 2 * tq + hc;
-        S.ka[hc] = kconst[n];
-#pragma unroll
-        for (int gr = 0; gr < NG; ++gr) {
-          S.bs[hc][gr] = 0.f;
-          S.zs[hc][gr] = 0.f;
-          S.kb[hc][gr] = kconst[MAX_G + n * 4 + gr];
-          S.kg[hc][gr] = kconst[MAX_G * 5 + n * 4 + gr];
-        }
-      }
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        S.bq[kk][0] = *(const uint32_t*)(qb + gid * D + 16 * kk + 2 * tq);
-        S.bq[kk][1] = *(const uint32_t*)(qb + gid * D + 16 * kk + 8 + 2 * tq);
-      }
-      for (int k = 0; k < nw_pages; ++k) {
-        const int st = (int)((seq + k) % DEPTH);
-        const uint32_t ph = ((seq + k) / DEPTH) & 1u;
-        if (!mbar_wait(&my_bar[st], ph)) {
-          timed_out = true;
-          k_fail = k;
-          break;
-        }
-        const int p = p0 + warp + k * NW;
-        const int pid = cv.page_table[(size_t)b * cv.max_pages_per_req + p];
-        if (pid >= 0 && pid < cv.num_pages) {
-          const int nv = (p == pages_b - 1) ? hist_b - p * PAGE : PAGE;
-          int2_page_mma<NG>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
-        }
-        __syncwarp();
-        if (lane == 0 && k + DEPTH < nw_pages) {
-          fence_proxy_async();
-          issue(k + DEPTH);
-        }
-      }
-      // finalize: reduce the thread parts over the 8 row groups
-#pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], o);
-#pragma unroll
-          for (int gr = 0; gr < NG; ++gr) {
-            S.bs[hc][gr] += __shfl_xor_sync(0xffffffffu, S.bs[hc][gr], o);
-            S.zs[hc][gr] += __shfl_xor_sync(0xffffffffu, S.zs[hc][gr], o);
-          }
-        }
-      }
-      __syncthreads();  // all warps are past their stages: results may alias them
-#pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        const int n = 2 * tq + hc;
-        if (n < G) {
-          if (gid == 0) {
-            wm[warp * MAX_G + n] = S.m[hc];
-            wl[warp * MAX_G + n] = S.l[hc];
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int gr = j / (8 / NG);
-            const float off = 1024.f * S.bs[hc][gr];
-            const float z = S.zs[hc][gr];
-            wo[(warp * MAX_G + n) * D + 16 * j + gid] = fmaf(S.oacc[j][hc] - off, 1.f / 256.f, z);
-            wo[(warp * MAX_G + n) * D + 16 * j + 8 + gid] = fmaf(S.oacc[j][hc + 2] - off, 1.f / 256.f, z);
-          }
-        }
-      }
     } else {
-      CoreState S;
-      for (int n = 0; n < MAX_G; ++n) {
-        S.m[n] = -INFINITY;
-        S.l[n] = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) S.o[n][c] = 0.f;
-      }
-      float* ps = vsw + warp * (MAX_G * PAGE + 2 * 4 * PAGE);
-      float* vs = ps + MAX_G * PAGE;
-      for (int k = 0; k < nw_pages; ++k) {
-        const int st = (int)((seq + k) % DEPTH);
-        const uint32_t ph = ((seq + k) / DEPTH) & 1u;
-        if (!mbar_wait(&my_bar[st], ph)) {
-          timed_out = true;
-          k_fail = k;
-          break;
-        }
+      // ------------------------------------------------------ INT2 history
+      const int p0 = jj * sc.S;
+      int p1 = p0 + sc.S;
+      if (p1 > pages_b) p1 = pages_b;
+      const int nw_pages = (p1 - p0 - warp + NW - 1) / NW > 0 ? (p1 - p0 - warp + NW - 1) / NW : 0;
+      uint8_t* my_stage = smem + L.off_stage + (size_t)warp * DEPTH * L.stage_bytes;
+      uint64_t* my_bar = mbar + warp * DEPTH;
+      auto issue = [&](int k) {  // lane 0 only: k-th page of this warp
         const int p = p0 + warp + k * NW;
+        const int st = (int)((seq + k) % DEPTH);
         const int pid = cv.page_table[(size_t)b * cv.max_pages_per_req + p];
         if (pid >= 0 && pid < cv.num_pages) {
-          const int nv = (p == pages_b - 1) ? hist_b - p * PAGE : PAGE;
-          int2_page_core<NG>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane, G, qf,
-                             kconst + MAX_G * 5, ps, vs);
+          mbar_expect_tx(&my_bar[st], (uint32_t)cv.head_bytes);
+          bulk_g2s(my_stage + (size_t)st * L.stage_bytes,
+                   cv.pool + (size_t)pid * cv.page_bytes + (size_t)kvh * cv.head_bytes,
+                   (uint32_t)cv.head_bytes, &my_bar[st]);
+        } else {
+          record_error(cv.err, pid < 0 ? OSCAR_ERR_NO_PAGE : OSCAR_ERR_RANGE);
+          mbar_expect_tx(&my_bar[st], 0u);
         }
-        __syncwarp();
-        if (lane == 0 && k + DEPTH < nw_pages) {
-          fence_proxy_async();
-          issue(k + DEPTH);
-        }
+      };
+      __syncthreads();  // the previous item's results in the stage area are consumed
+      if (lane == 0) {
+        fence_proxy_async();
+        for (int k = 0; k < DEPTH && k < nw_pages; ++k) issue(k);
       }
-      __syncthreads();
-      for (int n = 0; n < G; ++n) {
-        if (lane == 0) {
-          wm[warp * MAX_G + n] = S.m[n];
-          wl[warp * MAX_G + n] = S.l[n];
+      if (!waited) {
+        pdl_wait();  // q' (prep_kernel) is ready from here on
+        waited = true;
+      }
+      bool timed_out = false;
+      int k_fail = 0;
+      if (IMPL == 0) {
+        Int2State<NG> S;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) S.oacc[j][0] = S.oacc[j][1] = S.oacc[j][2] = S.oacc[j][3] = 0.f;
+        {
+          const uint8_t* qrec = a.qpack + ((size_t)b * cv.Hq + kvh * G + (gid < G ? gid : 0)) * QPACK_BYTES;
+          const __half* qbh = (const __half*)qrec;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            S.bq[kk][0] = gid < G ? __ldcg((const unsigned int*)(qbh + 16 * kk + 2 * tq)) : 0u;
+            S.bq[kk][1] = gid < G ? __ldcg((const unsigned int*)(qbh + 16 * kk + 8 + 2 * tq)) : 0u;
+          }
+#pragma unroll
+          for (int hc = 0; hc < 2; ++hc) {
+            const int n = 2 * tq + hc;
+            const bool hv = n < G;
+            const uint8_t* r = a.qpack + ((size_t)b * cv.Hq + kvh * G + (hv ? n : 0)) * QPACK_BYTES;
+            S.m[hc] = -INFINITY;
+            S.l[hc] = 0.f;
+            S.ka[hc] = hv ? __ldcg((const float*)(r + QPACK_ALPHA)) : 0.f;
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr) {
+              S.bs[hc][gr] = 0.f;
+              S.zs[hc][gr] = 0.f;
+              S.kb[hc][gr] = hv ? __ldcg((const float*)(r + QPACK_BETA) + gr) : 0.f;
+              S.kg[hc][gr] = hv ? __ldcg((const float*)(r + QPACK_GAMMA) + gr) : 0.f;
+            }
+          }
+        }
+        for (int k = 0; k < nw_pages; ++k) {
+          const int st = (int)((seq + k) % DEPTH);
+          const uint32_t ph = ((seq + k) / DEPTH) & 1u;
+          if (!__all_sync(0xffffffffu, mbar_wait(&my_bar[st], ph))) {
+            timed_out = true;
+            k_fail = k;
+            break;
+          }
+          const int p = p0 + warp + k * NW;
+          const int pid = cv.page_table[(size_t)b * cv.max_pages_per_req + p];
+          if (pid >= 0 && pid < cv.num_pages) {
+            const int nv = (p == pages_b - 1) ? hist_b - p * PAGE : PAGE;
+            int2_page_mma<NG>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
+          }
+          __syncwarp();
+          if (lane == 0 && k + DEPTH < nw_pages) {
+            fence_proxy_async();
+            issue(k + DEPTH);
+          }
         }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) wo[(warp * MAX_G + n) * D + 4 * lane + c] = S.o[n][c];
-      }
-    }
-    if (timed_out) {
-      // Record, wait (bounded) for this warp's copies still in flight, and
-      // make the whole CTA leave after this item.
-      if (lane == 0) {
-        record_error(cv.err, OSCAR_ERR_TIMEOUT);
-        misc[1] = 1;
-      }
-      const int issued = (k_fail + DEPTH) < nw_pages ? k_fail + DEPTH : nw_pages;
-      for (int kk = k_fail; kk < issued; ++kk)
-        mbar_wait(&my_bar[(seq + kk) % DEPTH], ((seq + kk) / DEPTH) & 1u);
-    }
-    seq += (uint32_t)nw_pages;
-    __syncthreads();
-    cta_combine_write(a, smem, L, slot);
-    __syncthreads();
-    if (misc[1]) break;
-  }
-}
-
-// ------------------------------------------------------------------ merge
-// grid = B * Hkv, block = 128 * GP (GP head groups of 128 threads).
-__global__ void __launch_bounds__(512) merge_kernel(DecodeArgs a, int GP) {
-  extern __shared__ __align__(16) uint8_t msm[];
-  float* tmp = (float*)msm;             // [GP][128]
-  float* tmp2 = tmp + GP * D;           // [GP][128]
-  int* red = (int*)(tmp2 + GP * D);     // [32]
-  int* pre = red + 32;                  // [B + 1]
-  const CacheView& cv = a.cv;
-  const int b = blockIdx.x / cv.Hkv, kvh = blockIdx.x % cv.Hkv;
-  const int grp = threadIdx.x >> 7, c = threadIdx.x & 127, bar = 1 + grp;
-  const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
-  const Sched sc = make_sched(cv.hist_lens, a.B, cv.Hkv, a.target_items, unit, pre, red);
-  const int G = cv.G;
-  const int pages_b = (cv.hist_lens[b] + PAGE - 1) / PAGE;
-  const int nb = (pages_b + sc.S - 1) / sc.S;
-  const int base = pre[b] + kvh * nb;
-  const float* Ut = a.rot.Ut_V + (size_t)kvh * D * D;
-  for (int n0 = 0; n0 < G; n0 += GP) {
-    const int n = n0 + grp;
-    const bool active = n < G;
-    float M = -INFINITY, Ls = 0.f, O = 0.f;
-    if (active) {
-      for (int j = 0; j < nb; ++j) {
-        const float* rec = a.part + ((size_t)(base + j) * G + n) * PART_STRIDE;
-        const float mj = rec[0], lj = rec[1];
-        if (lj > 0.f) {
-          const float mx = fmaxf(M, mj);
-          const float fo = M == -INFINITY ? 0.f : ex2(M - mx);
-          const float fn = ex2(mj - mx);
-          Ls = Ls * fo + lj * fn;
-          O = O * fo + rec[2 + c] * fn;
-          M = mx;
+        for (int hc = 0; hc < 2; ++hc) {
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], o);
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr) {
+              S.bs[hc][gr] += __shfl_xor_sync(0xffffffffu, S.bs[hc][gr], o);
+              S.zs[hc][gr] += __shfl_xor_sync(0xffffffffu, S.zs[hc][gr], o);
+            }
+          }
+        }
+        if (timed_out) {
+          if (lane == 0) {
+            record_error(cv.err, OSCAR_ERR_TIMEOUT);
+            misc[1] = 1;
+          }
+          const int issued = (k_fail + DEPTH) < nw_pages ? k_fail + DEPTH : nw_pages;
+          for (int kk = k_fail; kk < issued; ++kk)
+            mbar_wait(&my_bar[(seq + kk) % DEPTH], ((seq + kk) / DEPTH) & 1u);
+        }
+        __syncthreads();  // all warps are past their stages: results may alias them
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+          const int n = 2 * tq + hc;
+          if (n < G) {
+            if (gid == 0) {
+              wm[warp * MAX_G + n] = S.m[hc];
+              wl[warp * MAX_G + n] = S.l[hc];
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int gr = j / (8 / NG);
+              const float off = 1024.f * S.bs[hc][gr];
+              const float z = S.zs[hc][gr];
+              wo[(warp * MAX_G + n) * D + 16 * j + gid] = fmaf(S.oacc[j][hc] - off, 1.f / 256.f, z);
+              wo[(warp * MAX_G + n) * D + 16 * j + 8 + gid] = fmaf(S.oacc[j][hc + 2] - off, 1.f / 256.f, z);
+            }
+          }
+        }
+      } else {
+        // CUDA-core path: q' in K storage order and the z weights, in smem
+        float* kgm = qf + MAX_G * D;
+        for (int e = threadIdx.x; e < G * D; e += NW * 32) {
+          const int n = e / D, c = e % D;
+          qf[n * D + k_word(c) * 16 + k_bit(c) / 2] =
+              __ldcg(a.qrot + ((size_t)b * cv.Hq + kvh * G + n) * D + c);
+        }
+        for (int e = threadIdx.x; e < G * 4; e += NW * 32) {
+          const int n = e / 4, gr = e % 4;
+          kgm[e] = __ldcg((const float*)(a.qpack + ((size_t)b * cv.Hq + kvh * G + n) * QPACK_BYTES +
+                                         QPACK_GAMMA) + gr);
+        }
+        __syncthreads();
+        CoreState S;
+        for (int n = 0; n < MAX_G; ++n) {
+          S.m[n] = -INFINITY;
+          S.l[n] = 0.f;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) S.o[n][c] = 0.f;
+        }
+        float* ps = vsw + warp * (MAX_G * PAGE + 2 * 4 * PAGE);
+        float* vs = ps + MAX_G * PAGE;
+        for (int k = 0; k < nw_pages; ++k) {
+          const int st = (int)((seq + k) % DEPTH);
+          const uint32_t ph = ((seq + k) / DEPTH) & 1u;
+          if (!__all_sync(0xffffffffu, mbar_wait(&my_bar[st], ph))) {
+            timed_out = true;
+            k_fail = k;
+            break;
+          }
+          const int p = p0 + warp + k * NW;
+          const int pid = cv.page_table[(size_t)b * cv.max_pages_per_req + p];
+          if (pid >= 0 && pid < cv.num_pages) {
+            const int nv = (p == pages_b - 1) ? hist_b - p * PAGE : PAGE;
+            int2_page_core<NG>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane, G, qf, kgm, ps, vs);
+          }
+          __syncwarp();
+          if (lane == 0 && k + DEPTH < nw_pages) {
+            fence_proxy_async();
+            issue(k + DEPTH);
+          }
+        }
+        if (timed_out) {
+          if (lane == 0) {
+            record_error(cv.err, OSCAR_ERR_TIMEOUT);
+            misc[1] = 1;
+          }
+          const int issued = (k_fail + DEPTH) < nw_pages ? k_fail + DEPTH : nw_pages;
+          for (int kk = k_fail; kk < issued; ++kk)
+            mbar_wait(&my_bar[(seq + kk) % DEPTH], ((seq + kk) / DEPTH) & 1u);
+        }
+        __syncthreads();
+        for (int n = 0; n < G; ++n) {
+          if (lane == 0) {
+            wm[warp * MAX_G + n] = S.m[n];
+            wl[warp * MAX_G + n] = S.l[n];
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) wo[(warp * MAX_G + n) * D + 4 * lane + c] = S.o[n][c];
         }
       }
+      seq += (uint32_t)nw_pages;
     }
-    if (!a.bf16_history) O = unrotate128(O, Ut, a.rot.mode, c, tmp + grp * D, tmp2 + grp * D, bar);
-    if (active) {
-      const float* w = a.part + ((size_t)(sc.n_hist + b * cv.Hkv + kvh) * G + n) * PART_STRIDE;
-      const float mw = w[0], lw = w[1], ow = w[2 + c];
-      const float M2 = fmaxf(M, lw > 0.f ? mw : -INFINITY);
-      float o = 0.f, lse = -INFINITY;
-      if (M2 != -INFINITY) {
-        const float fh = (M == -INFINITY) ? 0.f : ex2(M - M2);
-        const float fw = lw > 0.f ? ex2(mw - M2) : 0.f;
-        const float lt = Ls * fh + lw * fw;
-        o = (O * fh + ow * fw) / lt;
-        lse = (M2 + log2f(lt)) * LN2;
-      }
-      const size_t row = (size_t)b * cv.Hq + kvh * G + n;
-      a.out[row * D + c] = __float2bfloat16_rn(o);
-      if (a.lse && c == 0) a.lse[row] = lse;
+    __syncthreads();
+    cta_combine_write(a, wm, wl, wo, slot);
+    if (!waited) {
+      pdl_wait();
+      waited = true;
     }
+    // Last finisher of this (request, kv head) merges it.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const int nb = (pages_b + sc.S - 1) / sc.S;
+      const int old = atomicAdd(&a.done[b * Hkv + kvh], 1);
+      misc[2] = (old == nb) ? 1 : 0;  // nb history items + 1 window item
+      __threadfence();
+    }
+    __syncthreads();
+    if (misc[2]) merge_bkvh(a, sc, pre, b, kvh, wm);
+    if (misc[1]) break;
+    __syncthreads();
+    if (threadIdx.x == 0) misc[0] = (int)gridDim.x + atomicAdd(a.counter, 1);
+    __syncthreads();
+    it = misc[0];
   }
+  if (!waited) pdl_wait();
 }
 
 template <int NG, int IMPL>
@@ -891,26 +1023,42 @@ cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<NG, IMPL>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (e != cudaSuccess) return e;
-  decode_kernel<NG, IMPL><<<grid, NW * 32, L.total, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(NW * 32);
+  lc.dynamicSmemBytes = L.total;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, decode_kernel<NG, IMPL>, a);
 }
 
 }  // namespace
 
-size_t decode_scratch_bytes(int B, int Hq, int Hkv, int G, int max_target_items) {
-  const size_t head = 256;
-  const size_t qrot = (((size_t)B * Hq * D * 4) + 255) & ~(size_t)255;
+ScratchLayout scratch_layout(int B, int Hq, int Hkv, int G, int max_target_items) {
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  ScratchLayout s;
+  s.off_counter = 0;
+  s.off_done = 256;
+  s.off_qrot = s.off_done + up((size_t)B * Hkv * 4);
+  s.off_qpack = s.off_qrot + up((size_t)B * Hq * D * 4);
+  s.off_part = s.off_qpack + up((size_t)B * Hq * QPACK_BYTES);
   const size_t slots = (size_t)max_target_items + 2 * (size_t)B * Hkv;
-  return head + qrot + slots * G * PART_STRIDE * 4;
+  s.total = s.off_part + slots * G * PART_STRIDE * 4;
+  return s;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a0, int grid, cudaStream_t st, Profiler* prof) {
-  DecodeArgs a = a0;
+size_t decode_scratch_bytes(int B, int Hq, int Hkv, int G, int max_target_items) {
+  return scratch_layout(B, Hq, Hkv, G, max_target_items).total;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof) {
   const CacheView& cv = a.cv;
   prof_begin(prof, OSCAR_KERNEL_DECODE_PREP, st);
-  prep_kernel<<<a.bf16_history ? 1 : a.B * cv.Hkv, 128, 0, st>>>(a.q, a.qrot, a.counter, a.rot,
-                                                                  cv.Hq, cv.Hkv, cv.G,
-                                                                  !a.bf16_history);
+  prep_kernel<<<a.B * cv.Hkv, 512, 0, st>>>(a);
   prof_end(prof, OSCAR_KERNEL_DECODE_PREP, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -925,13 +1073,7 @@ cudaError_t launch_decode(const DecodeArgs& a0, int grid, cudaStream_t st, Profi
     else e = launch_decode_t<4, 0>(a, grid, st);
   }
   prof_end(prof, OSCAR_KERNEL_DECODE_MAIN, st);
-  if (e != cudaSuccess) return e;
-  const int GP = cv.G < 4 ? cv.G : 4;
-  const size_t msm = (size_t)2 * GP * D * 4 + 32 * 4 + ((size_t)a.B + 1) * 4;
-  prof_begin(prof, OSCAR_KERNEL_DECODE_MERGE, st);
-  merge_kernel<<<a.B * cv.Hkv, 128 * GP, msm, st>>>(a, GP);
-  prof_end(prof, OSCAR_KERNEL_DECODE_MERGE, st);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace oscar

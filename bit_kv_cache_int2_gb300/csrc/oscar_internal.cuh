@@ -21,6 +21,7 @@ constexpr int RECENT = 256;  // BF16 recent tokens [News, "服务系统：混合
 constexpr int MAX_G = 8;     // query heads per KV head handled by one mma column tile
 constexpr int PART_STRIDE = D + 2;  // partial record per head: m, l, o[128]
 constexpr int MAX_TARGET_ITEMS = 2048;
+constexpr int QPACK_BYTES = 320;  // packed query record per (request, query head)
 constexpr int WIN_BYTES_PER_HEAD = (SINK + RECENT) * D * 2 * 2;  // K and V
 constexpr int BF16_HEAD_BYTES = PAGE * D * 2 * 2;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -362,6 +363,16 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
   if (S < 1) S = 1;
   s.S = (int)S;
   if (tid == 0) {
+    // per-request rounding can add up to B*Hkv items: grow S until they fit
+    for (int iter = 0; iter < 32; ++iter) {
+      long long n = 0;
+      for (int b = 0; b < B; ++b) {
+        const int pages = (hist_lens[b] + PAGE - 1) / PAGE;
+        n += (long long)Hkv * ((pages + s.S - 1) / s.S);
+      }
+      if (n + s.n_win <= target || n <= (long long)B * Hkv) break;
+      s.S += s.S / 8 > 1 ? s.S / 8 : 1;
+    }
     int acc = 0;
     for (int b = 0; b < B; ++b) {
       pre[b] = acc;
@@ -369,7 +380,10 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
       acc += Hkv * ((pages + s.S - 1) / s.S);
     }
     pre[B] = acc;
+    red[0] = s.S;
   }
+  __syncthreads();
+  s.S = red[0];
   __syncthreads();
   s.n_hist = pre[B];
   s.win_first = (long long)WIN_BYTES_PER_HEAD > (long long)s.S * hist_item_unit_bytes;
@@ -404,9 +418,11 @@ struct DecodeArgs {
   const __nv_bfloat16* q;  // [B][Hq][128]
   __nv_bfloat16* out;      // [B][Hq][128]
   float* lse;              // [B][Hq] or null
-  float* qrot;             // scratch [B][Hq][128]
+  float* qrot;             // scratch [B][Hq][128] rotated queries (fp32)
+  uint8_t* qpack;          // scratch [B][Hq] packed query records
   float* part;             // scratch partials
   int* counter;            // scratch work counter
+  int* done;               // scratch [B][Hkv] finished-item counters
   int B;
   int target_items;
   int impl;  // 0 tensor-core, 1 CUDA-core
@@ -415,6 +431,12 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof);
+
+// Decode scratch: [work counter][done counters][q' fp32][packed q][partials]
+struct ScratchLayout {
+  size_t off_counter, off_done, off_qrot, off_qpack, off_part, total;
+};
+ScratchLayout scratch_layout(int B, int Hq, int Hkv, int G, int max_target_items);
 size_t decode_scratch_bytes(int B, int Hq, int Hkv, int G, int max_target_items);
 
 cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* k,

@@ -48,19 +48,22 @@ __device__ __forceinline__ void quant_store_v_global(float y, int j, int g, floa
 }
 
 // ------------------------------------------------------------------ append
-// grid = B * Hkv, block = 256: threads 0..127 handle K, 128..255 handle V.
-__global__ void __launch_bounds__(256) append_kernel(CacheView cv, LayerRot rot,
+// grid = (B * Hkv, 2): blockIdx.y = 0 handles K, 1 handles V.  block = 512:
+// four parts of 128 threads split the rotation's 128-row matvec so that all
+// of U's loads are in flight at once; threads 0..127 then finish the token.
+__global__ void __launch_bounds__(512) append_kernel(CacheView cv, LayerRot rot,
                                                      const __nv_bfloat16* __restrict__ knew,
                                                      const __nv_bfloat16* __restrict__ vnew,
                                                      int do_append, int* req_counter) {
-  __shared__ float xs[2][D];
-  __shared__ float tmp[2][D];
-  __shared__ float red[2][8];
+  __shared__ float xs[D];
+  __shared__ float part[4][D];
+  __shared__ float tmp[D];
+  __shared__ float red[8];
   __shared__ uint32_t kw[8];
   __shared__ int st[6];
-  const int b = blockIdx.x / cv.Hkv, h = blockIdx.x % cv.Hkv;
-  const int grp = threadIdx.x >> 7, j = threadIdx.x & 127, bar = 1 + grp;
-  if (threadIdx.x == 0) {
+  const int b = blockIdx.x / cv.Hkv, h = blockIdx.x % cv.Hkv, isv = blockIdx.y;
+  const int t = threadIdx.x, j = t & 127, pp = t >> 7;
+  if (t == 0) {
     const int L = cv.seq_lens[b], H = cv.hist_lens[b];
     const int recent = L > SINK ? L - SINK - H : 0;
     int ok = (L >= 0 && H >= 0 && H <= (L > SINK ? L - SINK : 0) && recent <= RECENT);
@@ -89,59 +92,72 @@ __global__ void __launch_bounds__(256) append_kernel(CacheView cv, LayerRot rot,
     st[3] = page;
     st[4] = ok;
   }
-  if (threadIdx.x < 8) kw[threadIdx.x] = 0u;
+  if (t < 8) kw[t] = 0u;
   __syncthreads();
   const int L = st[0], H = st[1], demote = st[2], page = st[3], ok = st[4];
+  const size_t head = (size_t)(b * cv.Hkv + h);
+  __nv_bfloat16* ring = isv ? cv.ring_v : cv.ring_k;
 
   if (demote) {
     const int ring_slot = H % RECENT;  // absolute position 64 + H
-    const __nv_bfloat16* src =
-        (grp == 0 ? cv.ring_k : cv.ring_v) + ((size_t)(b * cv.Hkv + h) * RECENT + ring_slot) * D;
-    xs[grp][j] = __bfloat162float(src[j]);
+    if (t < D) xs[t] = __bfloat162float(ring[(head * RECENT + ring_slot) * D + t]);
     __syncthreads();
-    const float* U = (grp == 0 ? rot.U_K : rot.U_V) + (size_t)h * D * D;
-    const float y = rotate128(xs[grp], U, rot.mode, j, tmp[grp], bar);
-    const float clip = (grp == 0 ? rot.clip_k : rot.clip_v)[h];
-    uint8_t* blk = cv.pool + (size_t)page * cv.page_bytes + (size_t)h * cv.head_bytes;
-    const int t = H % PAGE;
-    if (grp == 0) {
-      quant_pack(y, j, cv.g, clip, red[0], bar, false, t, kw, nullptr,
-                 (__half2*)(blk + off_k_sz()) + t * cv.NG);
-    } else {
-      quant_store_v_global(y, j, cv.g, clip, red[1], bar, t, (uint32_t*)(blk + 2048),
-                           (__half2*)(blk + off_v_sz(cv.g)) + t * cv.NG);
+    float acc = 0.f;
+    if (rot.mode == OSCAR_ROT_OSCAR) {
+      const float* U = (isv ? rot.U_V : rot.U_K) + (size_t)h * D * D + (size_t)(32 * pp) * D + j;
+      float u[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) u[k] = __ldg(U + k * D);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) acc = fmaf(xs[32 * pp + k], u[k], acc);
+    } else if (pp == 0) {
+      acc = xs[j];
     }
+    part[pp][j] = acc;
     __syncthreads();
-    if (threadIdx.x < 8) ((uint32_t*)(blk + t * 32))[threadIdx.x] = kw[threadIdx.x];
+    if (pp == 0) {
+      float y = (part[0][j] + part[1][j]) + (part[2][j] + part[3][j]);
+      if (rot.mode != OSCAR_ROT_NONE) {
+        y = fwht128(y, j, tmp, 1);
+        if (rot.mode == OSCAR_ROT_OSCAR) {
+          tmp[j] = y;
+          group_sync(1);
+          y = tmp[bitrev7(j)];
+          group_sync(1);
+        }
+      }
+      const float clip = (isv ? rot.clip_v : rot.clip_k)[h];
+      uint8_t* blk = cv.pool + (size_t)page * cv.page_bytes + (size_t)h * cv.head_bytes;
+      const int tr = H % PAGE;
+      if (!isv) {
+        quant_pack(y, j, cv.g, clip, red, 1, false, tr, kw, nullptr,
+                   (__half2*)(blk + off_k_sz()) + tr * cv.NG);
+        group_sync(1);
+        if (t < 8) ((uint32_t*)(blk + tr * 32))[t] = kw[t];
+      } else {
+        quant_store_v_global(y, j, cv.g, clip, red, 1, tr, (uint32_t*)(blk + 2048),
+                             (__half2*)(blk + off_v_sz(cv.g)) + tr * cv.NG);
+      }
+    }
   }
   __syncthreads();  // the evicted ring slot is fully read before it is overwritten
 
-  if (do_append && ok) {
-    const size_t head = (size_t)(b * cv.Hkv + h);
-    __nv_bfloat16* dk;
-    __nv_bfloat16* dv;
-    if (L < SINK) {
-      dk = cv.sink_k + (head * SINK + L) * D;
-      dv = cv.sink_v + (head * SINK + L) * D;
-    } else {
-      const int slot = (L - SINK) % RECENT;
-      dk = cv.ring_k + (head * RECENT + slot) * D;
-      dv = cv.ring_v + (head * RECENT + slot) * D;
-    }
-    const size_t src = head * D;
-    if (threadIdx.x < 16) {
-      ((uint4*)dk)[threadIdx.x] = ((const uint4*)(knew + src))[threadIdx.x];
-    } else if (threadIdx.x < 32) {
-      ((uint4*)dv)[threadIdx.x - 16] = ((const uint4*)(vnew + src))[threadIdx.x - 16];
-    }
+  if (do_append && ok && t < 16) {
+    const __nv_bfloat16* src = (isv ? vnew : knew) + head * D;
+    __nv_bfloat16* dst;
+    if (L < SINK)
+      dst = (isv ? cv.sink_v : cv.sink_k) + (head * SINK + L) * D;
+    else
+      dst = ring + (head * RECENT + (L - SINK) % RECENT) * D;
+    ((uint4*)dst)[t] = ((const uint4*)src)[t];
   }
   // The last CTA of request b to finish updates its lengths: every CTA of the
   // request has read the old lengths before it increments the counter.
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (t == 0) {
     __threadfence();
     const int old = atomicAdd(&req_counter[b], 1);
-    if (old == cv.Hkv - 1) {
+    if (old == 2 * cv.Hkv - 1) {
       req_counter[b] = 0;
       if (ok) {
         cv.seq_lens[b] = L + (do_append ? 1 : 0);
@@ -358,7 +374,7 @@ cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_b
                           const __nv_bfloat16* v, int B, int do_append, int* req_counter,
                           cudaStream_t st, Profiler* prof) {
   prof_begin(prof, OSCAR_KERNEL_APPEND, st);
-  append_kernel<<<B * cv.Hkv, 256, 0, st>>>(cv, rot, k, v, do_append, req_counter);
+  append_kernel<<<dim3(B * cv.Hkv, 2), 512, 0, st>>>(cv, rot, k, v, do_append, req_counter);
   prof_end(prof, OSCAR_KERNEL_APPEND, st);
   return cudaGetLastError();
 }
