@@ -59,7 +59,7 @@ struct oscar_ctx {
   int* d_req_counter = nullptr;  // [max_batch]
   int impl = 0;
   int ctas_per_sm = 2;
-  int items_per_cta = 3;
+  int items_per_cta = 1;
   Profiler prof;
 };
 

@@ -156,9 +156,12 @@ __host__ __device__ inline SmemLayout smem_layout(int head_bytes, int B, int imp
   int stage_total = NW * DEPTH * L.stage_bytes;
   // warp results and the merge's working set alias the stages
   const int wo_bytes = NW * MAX_G * D * 4 + 2 * NW * MAX_G * 4;
-  const int merge_bytes = (2 * MAX_G * D + 2 * D + 4 * MAX_G) * 4;
+  // merge: history/un-rotation buffers, m and l per head, one weight per
+  // history partial of a (request, kv head) (at most MAX_TARGET_ITEMS + B*Hkv)
+  const int merge_bytes = (2 * MAX_G * D + 2 * D + 2 * MAX_G + MAX_TARGET_ITEMS + B + 8) * 4;
   if (stage_total < wo_bytes) stage_total = wo_bytes;
   if (stage_total < merge_bytes) stage_total = merge_bytes;
+  stage_total = (stage_total + 127) & ~127;  // mbarriers that follow need 8-byte alignment
   o += stage_total;
   L.off_mbar = o;
   o += NW * DEPTH * 8;
@@ -439,93 +442,107 @@ __device__ __forceinline__ uint4 ldg_nc(const void* p) {
   return r;
 }
 
-// 64 tokens of BF16 keys/values, row-major [64][128] at Kb / Vb; token t is
-// used iff bit t of `valid` is set.
-__device__ __forceinline__ void bf16_chunk_mma(Bf16State& S, const __nv_bfloat16* Kb,
-                                               const __nv_bfloat16* Vb, uint64_t valid, int lane) {
-  const int gid = lane >> 2, tq = lane & 3;
-  const float cst = LOG2E * INV_SQRT_D;
-  float lam[4][4];
+// One 16-token tile of BF16 keys/values in registers: the rows this thread
+// feeds to the tensor cores.
+struct Bf16Tile {
+  uint4 ka[4], kb[4];  // K rows 16s+gid and 16s+gid+8, channels 32tq..32tq+31
+  uint4 vv[4][2];      // V rows of tokens 16s+{2tq, 2tq+1, 2tq+8, 2tq+9}, channels 16gid..16gid+15
+};
+
+__device__ __forceinline__ void bf16_tile_load(Bf16Tile& T, const __nv_bfloat16* Kb,
+                                               const __nv_bfloat16* Vb, uint64_t valid, int s,
+                                               int gid, int tq) {
+  const int ta = 16 * s + gid, tb = ta + 8;
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    const int ta = 16 * s + gid, tb = ta + 8;
-    uint4 ka[4], kb[4];
-#pragma unroll
-    for (int qd = 0; qd < 4; ++qd) {
-      ka[qd] = ldg_nc(Kb + ta * D + 32 * tq + 8 * qd);
-      kb[qd] = ldg_nc(Kb + tb * D + 32 * tq + 8 * qd);
-    }
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint4& xa = ka[kk >> 1];
-      const uint4& xb = kb[kk >> 1];
-      const uint32_t a0 = (kk & 1) ? xa.z : xa.x, a2 = (kk & 1) ? xa.w : xa.y;
-      const uint32_t a1 = (kk & 1) ? xb.z : xb.x, a3 = (kk & 1) ? xb.w : xb.y;
-      mma_bf16(acc, a0, a1, a2, a3, S.bq[kk][0], S.bq[kk][1]);
-    }
-    const bool va = (valid >> ta) & 1, vb = (valid >> tb) & 1;
-    lam[s][0] = va ? acc[0] * cst : -INFINITY;
-    lam[s][1] = va ? acc[1] * cst : -INFINITY;
-    lam[s][2] = vb ? acc[2] * cst : -INFINITY;
-    lam[s][3] = vb ? acc[3] * cst : -INFINITY;
+  for (int qd = 0; qd < 4; ++qd) {
+    T.ka[qd] = ldg_nc(Kb + ta * D + 32 * tq + 8 * qd);
+    T.kb[qd] = ldg_nc(Kb + tb * D + 32 * tq + 8 * qd);
   }
-  float pm[2] = {-INFINITY, -INFINITY};
+  const int t0 = 16 * s + 2 * tq, t2 = t0 + 8;
+  const int tk[4] = {t0, t0 + 1, t2, t2 + 1};
 #pragma unroll
-  for (int s = 0; s < 4; ++s)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) pm[e & 1] = fmaxf(pm[e & 1], lam[s][e]);
-#pragma unroll
-  for (int hc = 0; hc < 2; ++hc) {
-    pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 4));
-    pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 8));
-    pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 16));
-    const float mn = fmaxf(S.m[hc], pm[hc]);
-    const float al = ex2(S.m[hc] - mn);
-    S.m[hc] = mn;
-    S.l[hc] *= al;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      S.oacc[j][hc] *= al;
-      S.oacc[j][hc + 2] *= al;
-    }
-  }
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    float p[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) p[e] = ex2(lam[s][e] - S.m[e & 1]);
-    const __nv_bfloat162 h0 = __floats2bfloat162_rn(p[0], p[1]);
-    const __nv_bfloat162 h1 = __floats2bfloat162_rn(p[2], p[3]);
-    const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
-    S.l[0] += f0.x + f1.x;
-    S.l[1] += f0.y + f1.y;
-    const uint32_t b0 = movmatrix_t(*(const uint32_t*)&h0);
-    const uint32_t b1 = movmatrix_t(*(const uint32_t*)&h1);
-    // V rows of the 4 tokens of this thread's k-slots, channels 16gid..16gid+15
-    const int t0 = 16 * s + 2 * tq, t2 = t0 + 8;
-    const int tk[4] = {t0, t0 + 1, t2, t2 + 1};
-    uint4 vv[4][2];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const bool ok = (valid >> tk[u]) & 1;
-      const __nv_bfloat16* src = Vb + tk[u] * D + 16 * gid;
-      vv[u][0] = ok ? ldg_nc(src) : make_uint4(0, 0, 0, 0);
-      vv[u][1] = ok ? ldg_nc(src + 8) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t* w0 = (const uint32_t*)&vv[0][j >> 2];
-      const uint32_t* w1 = (const uint32_t*)&vv[1][j >> 2];
-      const uint32_t* w2 = (const uint32_t*)&vv[2][j >> 2];
-      const uint32_t* w3 = (const uint32_t*)&vv[3][j >> 2];
-      const uint32_t x0 = w0[j & 3], x1 = w1[j & 3], x2 = w2[j & 3], x3 = w3[j & 3];
-      mma_bf16(S.oacc[j], prmt(x0, x1, 0x5410), prmt(x0, x1, 0x7632), prmt(x2, x3, 0x5410),
-               prmt(x2, x3, 0x7632), b0, b1);
-    }
+  for (int u = 0; u < 4; ++u) {
+    const bool ok = (valid >> tk[u]) & 1;
+    const __nv_bfloat16* src = Vb + tk[u] * D + 16 * gid;
+    T.vv[u][0] = ok ? ldg_nc(src) : make_uint4(0, 0, 0, 0);
+    T.vv[u][1] = ok ? ldg_nc(src + 8) : make_uint4(0, 0, 0, 0);
   }
 }
 
+__device__ __forceinline__ void bf16_tile_compute(Bf16State& S, const Bf16Tile& T, uint64_t valid,
+                                                  int s, int gid) {
+  const float cst = LOG2E * INV_SQRT_D;
+  const int ta = 16 * s + gid, tb = ta + 8;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint4& xa = T.ka[kk >> 1];
+    const uint4& xb = T.kb[kk >> 1];
+    const uint32_t a0 = (kk & 1) ? xa.z : xa.x, a2 = (kk & 1) ? xa.w : xa.y;
+    const uint32_t a1 = (kk & 1) ? xb.z : xb.x, a3 = (kk & 1) ? xb.w : xb.y;
+    mma_bf16(acc, a0, a1, a2, a3, S.bq[kk][0], S.bq[kk][1]);
+  }
+  const bool va = (valid >> ta) & 1, vb = (valid >> tb) & 1;
+  float lam[4];
+  lam[0] = va ? acc[0] * cst : -INFINITY;
+  lam[1] = va ? acc[1] * cst : -INFINITY;
+  lam[2] = vb ? acc[2] * cst : -INFINITY;
+  lam[3] = vb ? acc[3] * cst : -INFINITY;
+#pragma unroll
+  for (int hc = 0; hc < 2; ++hc) {
+    float pm = fmaxf(lam[hc], lam[hc + 2]);
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+    const float mn = fmaxf(S.m[hc], pm);
+    if (mn > S.m[hc]) {  // rescale only when the running max moves
+      const float al = ex2(S.m[hc] - mn);
+      S.m[hc] = mn;
+      S.l[hc] *= al;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        S.oacc[j][hc] *= al;
+        S.oacc[j][hc + 2] *= al;
+      }
+    }
+  }
+  float p[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) p[e] = ex2(lam[e] - S.m[e & 1]);
+  const __nv_bfloat162 h0 = __floats2bfloat162_rn(p[0], p[1]);
+  const __nv_bfloat162 h1 = __floats2bfloat162_rn(p[2], p[3]);
+  const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+  S.l[0] += f0.x + f1.x;
+  S.l[1] += f0.y + f1.y;
+  const uint32_t b0 = movmatrix_t(*(const uint32_t*)&h0);
+  const uint32_t b1 = movmatrix_t(*(const uint32_t*)&h1);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t x0 = ((const uint32_t*)&T.vv[0][j >> 2])[j & 3];
+    const uint32_t x1 = ((const uint32_t*)&T.vv[1][j >> 2])[j & 3];
+    const uint32_t x2 = ((const uint32_t*)&T.vv[2][j >> 2])[j & 3];
+    const uint32_t x3 = ((const uint32_t*)&T.vv[3][j >> 2])[j & 3];
+    mma_bf16(S.oacc[j], prmt(x0, x1, 0x5410), prmt(x0, x1, 0x7632), prmt(x2, x3, 0x5410),
+             prmt(x2, x3, 0x7632), b0, b1);
+  }
+}
+
+// 64 tokens of BF16 keys/values, row-major [64][128] at Kb / Vb; token t is
+// used iff bit t of `valid` is set.  Tiles of 16 tokens, the next tile's
+// loads in flight while the current one is computed.
+__device__ __forceinline__ void bf16_chunk_mma(Bf16State& S, const __nv_bfloat16* Kb,
+                                               const __nv_bfloat16* Vb, uint64_t valid, int lane) {
+  const int gid = lane >> 2, tq = lane & 3;
+  Bf16Tile A, Bt;
+  bf16_tile_load(A, Kb, Vb, valid, 0, gid, tq);
+#pragma unroll
+  for (int s = 0; s < 4; s += 2) {
+    bf16_tile_load(Bt, Kb, Vb, valid, s + 1, gid, tq);
+    if ((valid >> (16 * s)) & 0xFFFFull) bf16_tile_compute(S, A, valid, s, gid);
+    if (s + 2 < 4) bf16_tile_load(A, Kb, Vb, valid, s + 2, gid, tq);
+    if ((valid >> (16 * (s + 1))) & 0xFFFFull) bf16_tile_compute(S, Bt, valid, s + 1, gid);
+  }
+}
 
 // ----------------------------------------------------------------- decode
 // Combine the CTA's warp results (wm, wl, wo) into partial record `slot`.
@@ -572,47 +589,54 @@ __device__ void merge_bkvh(const DecodeArgs& a, const Sched& sc, const int* pre,
   const int pages_b = (cv.hist_lens[b] + PAGE - 1) / PAGE;
   const int nb = (pages_b + sc.S - 1) / sc.S;
   const int base = pre[b] + kvh * nb;
+  float* wq = lh + MAX_G;  // [nb] weights of the history partials
+  float* rs = wq + nb;     // [8] block reductions
+  const int warp = c >> 5, lane = c & 31;
   for (int n = 0; n < G; ++n) {
-    float M = -INFINITY;
-    for (int q = 0; q < nb; ++q) {
+    // 1) M = max of the partial maxima (all partials read in parallel)
+    float mloc = -INFINITY;
+    for (int q = c; q < nb; q += 128) {
       const float* rec = a.part + ((size_t)(base + q) * G + n) * PART_STRIDE;
-      if (__ldcg(rec + 1) > 0.f) M = fmaxf(M, __ldcg(rec));
+      const float mq = __ldcg(rec), lq = __ldcg(rec + 1);
+      wq[q] = lq > 0.f ? mq : -INFINITY;
+      if (lq > 0.f) mloc = fmaxf(mloc, mq);
     }
-    float Ls = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-      int q = 0;
-      for (; q + 4 <= nb; q += 4) {
-        float m4[4], l4[4], o4[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float* rec = a.part + ((size_t)(base + q + u) * G + n) * PART_STRIDE;
-          m4[u] = __ldcg(rec);
-          l4[u] = __ldcg(rec + 1);
-          o4[u] = __ldcg(rec + 2 + c);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (l4[u] > 0.f) {
-            const float w = ex2(m4[u] - M);
-            Ls = fmaf(l4[u], w, Ls);
-            O = fmaf(o4[u], w, O);
-          }
-      }
-      for (; q < nb; ++q) {
-        const float* rec = a.part + ((size_t)(base + q) * G + n) * PART_STRIDE;
-        const float lq = __ldcg(rec + 1);
-        if (lq > 0.f) {
-          const float w = ex2(__ldcg(rec) - M);
-          Ls = fmaf(lq, w, Ls);
-          O = fmaf(__ldcg(rec + 2 + c), w, O);
-        }
-      }
+    for (int o = 16; o; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+    if (lane == 0) rs[warp] = mloc;
+    __syncthreads();
+    const float M = fmaxf(fmaxf(rs[0], rs[1]), fmaxf(rs[2], rs[3]));
+    // 2) weights l_q * 2^(m_q - M) and their sum
+    float lloc = 0.f;
+    for (int q = c; q < nb; q += 128) {
+      const float* rec = a.part + ((size_t)(base + q) * G + n) * PART_STRIDE;
+      const float mq = wq[q];
+      const float w = mq == -INFINITY ? 0.f : ex2(mq - M);
+      wq[q] = w;
+      lloc = fmaf(__ldcg(rec + 1), w, lloc);
     }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, o);
+    if (lane == 0) rs[4 + warp] = lloc;
+    __syncthreads();
+    const float Ls = (rs[4] + rs[5]) + (rs[6] + rs[7]);
+    // 3) O[c] = sum_q w_q o_q[c], 8 independent loads at a time
+    float O = 0.f;
+    int q = 0;
+    for (; q + 8 <= nb; q += 8) {
+      float o8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) o8[u] = __ldcg(a.part + ((size_t)(base + q + u) * G + n) * PART_STRIDE + 2 + c);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) O = fmaf(o8[u], wq[q + u], O);
+    }
+    for (; q < nb; ++q) O = fmaf(__ldcg(a.part + ((size_t)(base + q) * G + n) * PART_STRIDE + 2 + c), wq[q], O);
     oh[n * D + c] = O;
     if (c == 0) {
-      mh[n] = M;
+      mh[n] = Ls > 0.f ? M : -INFINITY;
       lh[n] = Ls;
     }
+    __syncthreads();
   }
   __syncthreads();
   if (!a.bf16_history && a.rot.mode != OSCAR_ROT_NONE) {
@@ -1020,6 +1044,7 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
 template <int NG, int IMPL>
 cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t st) {
   const SmemLayout L = smem_layout(a.cv.head_bytes, a.B, a.bf16_history ? 2 : IMPL);
+  if ((L.off_mbar % 8) || (L.off_stage % 128) || (L.off_pre % 16)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<NG, IMPL>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (e != cudaSuccess) return e;

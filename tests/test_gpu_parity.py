@@ -276,6 +276,7 @@ def test_missing_page_is_reported_not_faulted():
         oscar.oscar_append(sc.ctx, 0, sc.cache, k, v, 1)
         assert oscar.oscar_get_error(sc.ctx) == oscar.ERR_NO_PAGE
         assert int(sc.cache["seq_lens"][0]) == 500  # request left unchanged
+        pt.copy_(saved)
         # decode over a history whose page is missing: error word, no fault
         pt[0, 0] = -1
         q = GS.queries(sc, seed=7)
