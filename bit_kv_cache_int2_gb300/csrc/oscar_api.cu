@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <new>
+#include <mutex>
 #include <vector>
 
 #include "oscar_internal.cuh"
@@ -183,6 +184,33 @@ oscar_status decode_common(oscar_ctx* ctx, int layer, const oscar_cache* cache, 
 
 }  // namespace
 
+
+// ----------------------------------------------- decode without allocation
+// The working memory of oscar_decode_noalloc: one buffer per device that the
+// library holds for the life of the process.  In host code the symbol is only
+// a stand-in; its device address is looked up once per device.
+namespace {
+static __device__ __align__(256) uint8_t g_noalloc_scratch[OSCAR_NOALLOC_SCRATCH_BYTES];
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
+
+oscar_status noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cuda_status(cudaErrorInvalidDevice);
+  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return OSCAR_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return cuda_status(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return OSCAR_OK;
+}
+}  // namespace
+
 extern "C" {
 
 int oscar_version(void) { return VERSION; }
@@ -197,6 +225,7 @@ const char* oscar_status_string(int s) {
     case OSCAR_ERR_TIMEOUT: return "bounded device wait ran out";
     case OSCAR_ERR_CUDA: return "CUDA runtime error";
     case OSCAR_ERR_STATE: return "cache state does not allow the call";
+    case OSCAR_ERR_TOO_LARGE: return "request needs more than the built-in no-allocation scratch";
     default: return "unknown status";
   }
 }
@@ -393,6 +422,19 @@ oscar_status oscar_decode(oscar_ctx* ctx, int layer, const oscar_cache* cache, c
                           void* out, float* lse, void* scratch, size_t scratch_bytes, int batch,
                           oscar_stream_t stream) {
   return decode_common(ctx, layer, cache, q, out, lse, scratch, scratch_bytes, batch, stream, false);
+}
+
+oscar_status oscar_decode_noalloc(oscar_ctx* ctx, int layer, const oscar_cache* cache,
+                                  const void* q, void* out, float* lse, int batch,
+                                  oscar_stream_t stream) {
+  if (!ctx || batch < 0 || batch > ctx->cfg.max_batch) return OSCAR_ERR_INVALID_ARG;
+  if (scratch_for(ctx, batch, target_items(ctx)) > (size_t)OSCAR_NOALLOC_SCRATCH_BYTES)
+    return OSCAR_ERR_TOO_LARGE;
+  void* scratch = nullptr;
+  const oscar_status st = noalloc_scratch(&scratch);
+  if (st != OSCAR_OK) return st;
+  return decode_common(ctx, layer, cache, q, out, lse, scratch, OSCAR_NOALLOC_SCRATCH_BYTES, batch,
+                       stream, false);
 }
 
 oscar_status oscar_decode_bf16_history(oscar_ctx* ctx, const oscar_cache* cache, const void* q,

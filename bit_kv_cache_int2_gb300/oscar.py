@@ -27,6 +27,8 @@ ERR_RANGE = 4
 ERR_TIMEOUT = 5
 ERR_CUDA = 6
 ERR_STATE = 7
+ERR_TOO_LARGE = 8
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 ROT_OSCAR = 0
 ROT_HADAMARD = 1
@@ -82,6 +84,8 @@ _SIGS = {
     "oscar_decode": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(oscar_cache), ctypes.c_void_p,
                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
                       ctypes.c_void_p], ctypes.c_int),
+    "oscar_decode_noalloc": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(oscar_cache), ctypes.c_void_p,
+                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
     "oscar_decode_bf16_history": ([ctypes.c_void_p, ctypes.POINTER(oscar_cache), ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                    ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
@@ -225,6 +229,14 @@ def oscar_decode(ctx, layer, cache: dict, q, out, lse, scratch, batch, stream=No
     _check(lib().oscar_decode(ctx, layer, ctypes.byref(cs), _ptr(q), _ptr(out), _ptr(lse), _ptr(scratch),
                               scratch.numel() * scratch.element_size(), batch, _stream(stream)),
            "oscar_decode")
+
+
+def oscar_decode_noalloc(ctx, layer, cache: dict, q, out, lse, batch, stream=None):
+    """oscar_decode with the library's own built-in working memory: the caller
+    passes no scratch and nothing is allocated."""
+    cs = _cache_struct(cache)
+    _check(lib().oscar_decode_noalloc(ctx, layer, ctypes.byref(cs), _ptr(q), _ptr(out), _ptr(lse), batch,
+                                      _stream(stream)), "oscar_decode_noalloc")
 
 
 def oscar_decode_bf16_history(ctx, cache: dict, q, out, lse, scratch, batch, stream=None):

@@ -91,7 +91,8 @@ typedef enum {
   OSCAR_ERR_RANGE = 4,       /* device: page id, length or scale out of range */
   OSCAR_ERR_TIMEOUT = 5,     /* device: a bounded wait ran out                */
   OSCAR_ERR_CUDA = 6,        /* a CUDA runtime call failed                    */
-  OSCAR_ERR_STATE = 7        /* device: cache state does not allow the call   */
+  OSCAR_ERR_STATE = 7,       /* device: cache state does not allow the call   */
+  OSCAR_ERR_TOO_LARGE = 8    /* request needs more than the built-in scratch  */
 } oscar_status;
 
 typedef enum {
@@ -233,6 +234,34 @@ oscar_status oscar_decode(oscar_ctx* ctx, int layer, const oscar_cache* cache,
                           const void* q, void* out, float* lse, void* scratch,
                           size_t scratch_bytes, int batch,
                           oscar_stream_t stream);
+
+/* Decode without any device allocation (the pages have no counterpart: this
+ * is a deployment convenience of this library).  Same computation, arguments
+ * and results as oscar_decode, but the working memory comes from a buffer of
+ * OSCAR_NOALLOC_SCRATCH_BYTES that the library itself holds in device memory,
+ * so the caller passes no scratch.  It is meant for callers that cannot or
+ * must not call cudaMalloc on the decode path: engines that reserve (nearly)
+ * all device memory for their KV pools at start-up and forbid later
+ * allocations so that serving can never fail for lack of memory, code paths
+ * where an allocation would block on or synchronise with other work on the
+ * device, and plain C callers with no device allocator of their own.
+ *  - Every GPU that loads the library holds this buffer until the process
+ *    exits, whether or not the call is used.
+ *  - The first call on each device (the device current at the call) looks up
+ *    the buffer's device address once; make that first call before any
+ *    stream capture begins.
+ *  - All calls share the one buffer and it keeps the last call's contents.
+ *    The kernels reset everything that must start at zero themselves.  Calls
+ *    that may run at the same time on the GPU (different streams, different
+ *    host threads) race on it: serialise them.
+ *  - Returns OSCAR_ERR_TOO_LARGE, launching nothing, if the request's working
+ *    memory (decode_scratch_bytes for `batch` at the context's current
+ *    options) exceeds OSCAR_NOALLOC_SCRATCH_BYTES.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+#define OSCAR_NOALLOC_SCRATCH_BYTES (8u << 20)
+oscar_status oscar_decode_noalloc(oscar_ctx* ctx, int layer, const oscar_cache* cache,
+                                  const void* q, void* out, float* lse, int batch,
+                                  oscar_stream_t stream);
 
 /* Baseline with the same split-K design, over a BF16 history pool (no
  * rotation, no quantisation): the comparison point for the speedup the
