@@ -59,7 +59,7 @@ struct oscar_ctx {
   int* d_err = nullptr;
   int* d_req_counter = nullptr;  // [max_batch]
   int impl = 0;
-  int ctas_per_sm = 2;
+  int ctas_per_sm = 4;
   int items_per_cta = 1;
   Profiler prof;
 };
@@ -92,8 +92,22 @@ size_t scratch_for(const oscar_ctx* ctx, int B, int target) {
   return decode_scratch_bytes(B, ctx->cfg.num_q_heads, ctx->cfg.num_kv_heads, ctx->G, target);
 }
 
-int target_items(const oscar_ctx* ctx) {
-  int t = ctx->num_sms * ctx->ctas_per_sm * ctx->items_per_cta;
+// Persistent decode CTAs per SM: the option, capped by what the kernel variant
+// for this call can keep resident.
+int decode_ctas(const oscar_ctx* ctx, int batch, bool bf16_history) {
+  DecodeArgs a = {};
+  a.cv.head_bytes = bf16_history ? BF16_HEAD_BYTES : int2_head_bytes(ctx->cfg.group_size);
+  a.cv.NG = ctx->NG;
+  a.B = batch;
+  a.impl = ctx->impl;
+  a.bf16_history = bf16_history ? 1 : 0;
+  int occ = decode_ctas_per_sm(a);
+  if (occ < 1) occ = 1;
+  return ctx->ctas_per_sm < occ ? ctx->ctas_per_sm : occ;
+}
+
+int target_items(const oscar_ctx* ctx, int batch, bool bf16_history) {
+  int t = ctx->num_sms * decode_ctas(ctx, batch, bf16_history) * ctx->items_per_cta;
   if (t > MAX_TARGET_ITEMS) t = MAX_TARGET_ITEMS;
   if (t < 1) t = 1;
   return t;
@@ -158,7 +172,7 @@ oscar_status decode_common(oscar_ctx* ctx, int layer, const oscar_cache* cache, 
       (lse && !aligned(lse, 4)))
     return OSCAR_ERR_INVALID_ARG;
   if (batch == 0) return OSCAR_OK;
-  const int target = target_items(ctx);
+  const int target = target_items(ctx, batch, bf16_history);
   if (scratch_bytes < scratch_for(ctx, batch, target)) return OSCAR_ERR_INVALID_ARG;
   DecodeArgs a;
   a.cv = make_view(ctx, cache, bf16_history);
@@ -178,7 +192,7 @@ oscar_status decode_common(oscar_ctx* ctx, int layer, const oscar_cache* cache, 
   a.impl = ctx->impl;
   a.bf16_history = bf16_history ? 1 : 0;
   a.rot = layer_rot(ctx, layer);
-  const int grid = ctx->num_sms * ctx->ctas_per_sm;
+  const int grid = ctx->num_sms * decode_ctas(ctx, batch, bf16_history);
   return cuda_status(launch_decode(a, grid, (cudaStream_t)stream, &ctx->prof));
 }
 
@@ -428,7 +442,7 @@ oscar_status oscar_decode_noalloc(oscar_ctx* ctx, int layer, const oscar_cache* 
                                   const void* q, void* out, float* lse, int batch,
                                   oscar_stream_t stream) {
   if (!ctx || batch < 0 || batch > ctx->cfg.max_batch) return OSCAR_ERR_INVALID_ARG;
-  if (scratch_for(ctx, batch, target_items(ctx)) > (size_t)OSCAR_NOALLOC_SCRATCH_BYTES)
+  if (scratch_for(ctx, batch, target_items(ctx, batch, false)) > (size_t)OSCAR_NOALLOC_SCRATCH_BYTES)
     return OSCAR_ERR_TOO_LARGE;
   void* scratch = nullptr;
   const oscar_status st = noalloc_scratch(&scratch);

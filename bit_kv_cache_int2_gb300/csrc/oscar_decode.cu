@@ -58,18 +58,23 @@ __global__ void __launch_bounds__(512) prep_kernel(DecodeArgs a) {
   }
   if (a.bf16_history) return;
   const int G = cv.G;
+  const int j = t & 127, pp = t >> 7;
+  float u[32];
+  if (a.rot.mode == OSCAR_ROT_OSCAR) {
+    // U_K loads first (independent of q); U_V^T rows into L2 for the merge
+    const float* U = a.rot.U_K + (size_t)kvh * D * D + (size_t)(32 * pp) * D + j;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) u[k] = __ldg(U + k * D);
+    const char* ut = (const char*)(a.rot.Ut_V + (size_t)kvh * D * D) + (size_t)t * 128;
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(ut));
+  }
   for (int e = t; e < G * D; e += 512)
     xs[e / D][e % D] = __bfloat162float(a.q[((size_t)b * cv.Hq + kvh * G) * D + e]);
   __syncthreads();
-  const int j = t & 127, pp = t >> 7;
   float acc[MAX_G];
 #pragma unroll
   for (int n = 0; n < MAX_G; ++n) acc[n] = 0.f;
   if (a.rot.mode == OSCAR_ROT_OSCAR) {
-    const float* U = a.rot.U_K + (size_t)kvh * D * D + (size_t)(32 * pp) * D + j;
-    float u[32];
-#pragma unroll
-    for (int k = 0; k < 32; ++k) u[k] = __ldg(U + k * D);
 #pragma unroll
     for (int k = 0; k < 32; ++k)
 #pragma unroll
@@ -156,15 +161,14 @@ __host__ __device__ inline SmemLayout smem_layout(int head_bytes, int B, int imp
   int stage_total = NW * DEPTH * L.stage_bytes;
   // warp results and the merge's working set alias the stages
   const int wo_bytes = NW * MAX_G * D * 4 + 2 * NW * MAX_G * 4;
-  // merge: history/un-rotation buffers, m and l per head, one weight per
-  // history partial of a (request, kv head) (at most MAX_TARGET_ITEMS + B*Hkv)
-  const int merge_bytes = (2 * MAX_G * D + 2 * D + 2 * MAX_G + MAX_TARGET_ITEMS + B + 8) * 4;
+  // merge: U_V^T (64 KB), the heads' history/window outputs, m and l per head
+  const int merge_bytes = D * D * 4 + MAX_G * D * 4 + 4 * MAX_G * 4;
   if (stage_total < wo_bytes) stage_total = wo_bytes;
   if (stage_total < merge_bytes) stage_total = merge_bytes;
   stage_total = (stage_total + 127) & ~127;  // mbarriers that follow need 8-byte alignment
   o += stage_total;
   L.off_mbar = o;
-  o += NW * DEPTH * 8;
+  o += NW * DEPTH * 8 + 16;  // pipeline stages + the merge's U_V^T copy
   L.off_qf = o;
   if (impl == 1) o += MAX_G * D * 4 + MAX_G * 4 * 4;  // fp32 q' in K storage order + z weights
   L.off_vs = o;
@@ -195,7 +199,7 @@ struct Int2State {
 
 // One INT2 page (64 tokens) of one kv head on tensor cores.  stage: the page's
 // head block in smem; nv: valid tokens.
-template <int NG>
+template <int NG, bool FULL>
 __device__ __forceinline__ void int2_page_mma(Int2State<NG>& S, const uint8_t* stage, int nv,
                                               int lane) {
   const int gid = lane >> 2, tq = lane & 3;
@@ -206,19 +210,25 @@ __device__ __forceinline__ void int2_page_mma(Int2State<NG>& S, const uint8_t* s
   const __half2* ksz = (const __half2*)(stage + 4096);
   const __half2* vsz = (const __half2*)(stage + 4096 + PAGE * NG * 4);
 
-  float lam[4][4];
+  // QK^T of the 4 tiles with the tiles interleaved, so that the 4
+  // accumulator chains are independent
+  uint2 wa[4], wb[4];
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
-    const int ta = 16 * s + gid, tb = ta + 8;
-    const uint2 wa = *(const uint2*)(kc + ta * 32 + 8 * tq);
-    const uint2 wb = *(const uint2*)(kc + tb * 32 + 8 * tq);
-    float acc[NG][4];
+    wa[s] = *(const uint2*)(kc + (16 * s + gid) * 32 + 8 * tq);
+    wb[s] = *(const uint2*)(kc + (16 * s + gid + 8) * 32 + 8 * tq);
+  }
+  float acc[4][NG][4];
 #pragma unroll
-    for (int gr = 0; gr < NG; ++gr) acc[gr][0] = acc[gr][1] = acc[gr][2] = acc[gr][3] = 0.f;
+  for (int s = 0; s < 4; ++s)
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t xa = kk < 4 ? wa.x : wa.y;
-      const uint32_t xb = kk < 4 ? wb.x : wb.y;
+    for (int gr = 0; gr < NG; ++gr) acc[s][gr][0] = acc[s][gr][1] = acc[s][gr][2] = acc[s][gr][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const uint32_t xa = kk < 4 ? wa[s].x : wa[s].y;
+      const uint32_t xb = kk < 4 ? wb[s].x : wb[s].y;
       uint32_t a0, a1, a2, a3;
       switch (kk & 3) {
         case 0: a0 = code_pair<0>(xa); a1 = code_pair<0>(xb); a2 = code_pair<1>(xa); a3 = code_pair<1>(xb); break;
@@ -226,8 +236,13 @@ __device__ __forceinline__ void int2_page_mma(Int2State<NG>& S, const uint8_t* s
         case 2: a0 = code_pair<4>(xa); a1 = code_pair<4>(xb); a2 = code_pair<5>(xa); a3 = code_pair<5>(xb); break;
         default: a0 = code_pair<6>(xa); a1 = code_pair<6>(xb); a2 = code_pair<7>(xa); a3 = code_pair<7>(xb); break;
       }
-      mma_f16(acc[kk / KPG], a0, a1, a2, a3, S.bq[kk][0], S.bq[kk][1]);
+      mma_f16(acc[s][kk / KPG], a0, a1, a2, a3, S.bq[kk][0], S.bq[kk][1]);
     }
+  }
+  float lam[4][4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int ta = 16 * s + gid, tb = ta + 8;
     // logits (log2 units): sum_gr s*(acc*alpha + beta) + z*gamma
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -237,9 +252,9 @@ __device__ __forceinline__ void int2_page_mma(Int2State<NG>& S, const uint8_t* s
 #pragma unroll
       for (int gr = 0; gr < NG; ++gr) {
         const float2 sz = __half22float2(ksz[row * NG + gr]);
-        v = fmaf(sz.x, fmaf(acc[gr][e], S.ka[hc], S.kb[hc][gr]), fmaf(sz.y, S.kg[hc][gr], v));
+        v = fmaf(sz.x, fmaf(acc[s][gr][e], S.ka[hc], S.kb[hc][gr]), fmaf(sz.y, S.kg[hc][gr], v));
       }
-      lam[s][e] = row < nv ? v : -INFINITY;
+      lam[s][e] = (FULL || row < nv) ? v : -INFINITY;
     }
   }
   // page max per column head, over all 64 tokens
@@ -253,19 +268,31 @@ __device__ __forceinline__ void int2_page_mma(Int2State<NG>& S, const uint8_t* s
     pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 4));
     pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 8));
     pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 16));
-    const float mn = fmaxf(S.m[hc], pm[hc]);
-    const float al = ex2(S.m[hc] - mn);
-    S.m[hc] = mn;
-    S.l[hc] *= al;
+  }
+  // rescale the running sums only when some lane's maximum moved
+  {
+    const float mn0 = fmaxf(S.m[0], pm[0]), mn1 = fmaxf(S.m[1], pm[1]);
+    const bool moved = (mn0 > S.m[0]) || (mn1 > S.m[1]);
+    if (__any_sync(0xffffffffu, moved)) {
+      const float al0 = ex2(S.m[0] - mn0), al1 = ex2(S.m[1] - mn1);
+      S.m[0] = mn0;
+      S.m[1] = mn1;
+      S.l[0] *= al0;
+      S.l[1] *= al1;
 #pragma unroll
-    for (int gr = 0; gr < NG; ++gr) {
-      S.bs[hc][gr] *= al;
-      S.zs[hc][gr] *= al;
-    }
+      for (int gr = 0; gr < NG; ++gr) {
+        S.bs[0][gr] *= al0;
+        S.zs[0][gr] *= al0;
+        S.bs[1][gr] *= al1;
+        S.zs[1][gr] *= al1;
+      }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      S.oacc[j][hc] *= al;
-      S.oacc[j][hc + 2] *= al;
+      for (int j = 0; j < 8; ++j) {
+        S.oacc[j][0] *= al0;
+        S.oacc[j][2] *= al0;
+        S.oacc[j][1] *= al1;
+        S.oacc[j][3] *= al1;
+      }
     }
   }
   // V code words: rows 16j+gid and 16j+8+gid, word tq (all 4 tiles)
@@ -278,7 +305,7 @@ __device__ __forceinline__ void int2_page_mma(Int2State<NG>& S, const uint8_t* s
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const int ta = 16 * s + gid, tb = ta + 8;
-    const bool va = ta < nv, vb = tb < nv;
+    const bool va = FULL || ta < nv, vb = FULL || tb < nv;
     float p[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -527,21 +554,71 @@ __device__ __forceinline__ void bf16_tile_compute(Bf16State& S, const Bf16Tile& 
   }
 }
 
-// 64 tokens of BF16 keys/values, row-major [64][128] at Kb / Vb; token t is
-// used iff bit t of `valid` is set.  Tiles of 16 tokens, the next tile's
-// loads in flight while the current one is computed.
+// Tiles s0 .. s0+ns-1 (16 tokens each) of 64 BF16 keys/values, row-major
+// [64][128] at Kb / Vb; token t is used iff bit t of `valid` is set.  With DB
+// the next tile's loads are in flight while the current one is computed (more
+// registers); without, tiles are loaded one at a time.
+template <bool DB>
+__device__ __forceinline__ void bf16_span_mma(Bf16State& S, const __nv_bfloat16* Kb,
+                                              const __nv_bfloat16* Vb, uint64_t valid, int lane,
+                                              int s0, int ns) {
+  const int gid = lane >> 2, tq = lane & 3;
+  if (DB) {
+    Bf16Tile A, Bt;
+    bf16_tile_load(A, Kb, Vb, valid, s0, gid, tq);
+    for (int s = s0; s < s0 + ns; s += 2) {
+      if (s + 1 < s0 + ns) bf16_tile_load(Bt, Kb, Vb, valid, s + 1, gid, tq);
+      if ((valid >> (16 * s)) & 0xFFFFull) bf16_tile_compute(S, A, valid, s, gid);
+      if (s + 2 < s0 + ns) bf16_tile_load(A, Kb, Vb, valid, s + 2, gid, tq);
+      if (s + 1 < s0 + ns && ((valid >> (16 * (s + 1))) & 0xFFFFull))
+        bf16_tile_compute(S, Bt, valid, s + 1, gid);
+    }
+  } else {
+    for (int s = s0; s < s0 + ns; ++s) {
+      if (!((valid >> (16 * s)) & 0xFFFFull)) continue;
+      Bf16Tile A;
+      bf16_tile_load(A, Kb, Vb, valid, s, gid, tq);
+      bf16_tile_compute(S, A, valid, s, gid);
+    }
+  }
+}
+
+template <bool DB>
 __device__ __forceinline__ void bf16_chunk_mma(Bf16State& S, const __nv_bfloat16* Kb,
                                                const __nv_bfloat16* Vb, uint64_t valid, int lane) {
-  const int gid = lane >> 2, tq = lane & 3;
-  Bf16Tile A, Bt;
-  bf16_tile_load(A, Kb, Vb, valid, 0, gid, tq);
-#pragma unroll
-  for (int s = 0; s < 4; s += 2) {
-    bf16_tile_load(Bt, Kb, Vb, valid, s + 1, gid, tq);
-    if ((valid >> (16 * s)) & 0xFFFFull) bf16_tile_compute(S, A, valid, s, gid);
-    if (s + 2 < 4) bf16_tile_load(A, Kb, Vb, valid, s + 2, gid, tq);
-    if ((valid >> (16 * (s + 1))) & 0xFFFFull) bf16_tile_compute(S, Bt, valid, s + 1, gid);
-  }
+  bf16_span_mma<DB>(S, Kb, Vb, valid, lane, 0, 4);
+}
+
+// Page ids of a warp's pages k = 0, 1, ... (page p0 + warp + k*NW of request
+// b), held 32 at a time in registers (lane i keeps page 32*blk + i) so that
+// no page waits on a dependent page-table load.
+struct PageIds {
+  int cur, a, b;
+};
+
+__device__ __forceinline__ int page_id_load(const CacheView& cv, int b, int first, int k, int n) {
+  return k < n ? __ldg(cv.page_table + (size_t)b * cv.max_pages_per_req + first + k * NW) : -1;
+}
+
+__device__ __forceinline__ void page_ids_init(PageIds& P, const CacheView& cv, int b, int first, int n,
+                                              int lane) {
+  P.cur = 0;
+  P.a = page_id_load(cv, b, first, lane, n);
+  P.b = page_id_load(cv, b, first, 32 + lane, n);
+}
+
+// All lanes call; k must lie in the current block or the next one.
+__device__ __forceinline__ int page_id_at(const PageIds& P, int k) {
+  const int v = ((k >> 5) == P.cur) ? P.a : P.b;
+  return __shfl_sync(0xffffffffu, v, k & 31);
+}
+
+// Call when page k (k % 32 == 0, k > 0) is reached.
+__device__ __forceinline__ void page_ids_advance(PageIds& P, const CacheView& cv, int b, int first,
+                                                 int n, int lane) {
+  P.a = P.b;
+  ++P.cur;
+  P.b = page_id_load(cv, b, first, 32 * (P.cur + 1) + lane, n);
 }
 
 // ----------------------------------------------------------------- decode
@@ -569,134 +646,235 @@ __device__ __forceinline__ void cta_combine_write(const DecodeArgs& a, const flo
       rec[0] = M;
       rec[1] = Ls;
     }
-    rec[2 + c] = O;
+    rec[PART_O + c] = O;
   }
+  fence_acq_rel_gpu();  // this thread's part of the record is visible before the item is counted
 }
 
-// Final merge of one (request, kv head), by one CTA of 128 threads: LSE-merge
-// of the history partials, un-rotation o = o'·P_br·H·U_V^T, LSE-merge with the
-// window partial, bf16 output.  sm: smem working area (merge_bytes).
+// Final merge of one (request, kv head) by one CTA of 128 threads.  Thread 0
+// first starts a bulk copy of U_V^T (64 KB) into shared memory.  Meanwhile warp
+// w takes heads w, w + 4: it LSE-merges the history partials into (M, L, O')
+// and the window partials into (M_w, L_w, O_w) with all loads of a round in
+// flight (each lane holds channels 4*lane .. 4*lane+3 and the weights of
+// partials lane, lane+32, ...), and applies o'·P_br·H in registers.  Then the
+// CTA applies ·U_V^T from shared memory to every head at once, and each warp
+// writes its heads' LSE-merge of history and window.
+constexpr int MERGE_KQ = 4;  // partial weights held per lane: nb <= 32 * MERGE_KQ in registers
+
+__device__ __forceinline__ float4 fma4(float4 o, float w, float4 acc) {
+  acc.x = fmaf(o.x, w, acc.x);
+  acc.y = fmaf(o.y, w, acc.y);
+  acc.z = fmaf(o.z, w, acc.z);
+  acc.w = fmaf(o.w, w, acc.w);
+  return acc;
+}
+
 __device__ void merge_bkvh(const DecodeArgs& a, const Sched& sc, const int* pre, int b, int kvh,
-                           float* sm) {
+                           float* sm, uint64_t* ubar, uint32_t uphase) {
   const CacheView& cv = a.cv;
-  const int G = cv.G, c = threadIdx.x;
-  float* oh = sm;                  // [MAX_G][D] history output (rotated, then un-rotated)
-  float* y = oh + MAX_G * D;       // [MAX_G][D] un-rotation input
-  float* tmp = y + MAX_G * D;      // [D]
-  float* tmp2 = tmp + D;           // [D]
-  float* mh = tmp2 + D;            // [MAX_G]
-  float* lh = mh + MAX_G;          // [MAX_G]
+  const int G = cv.G, t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  float* Us = sm;              // [128][128] U_V^T (OSCAR mode)
+  float* y = Us + D * D;       // [MAX_G][128] history part, then its un-rotation
+  float* hM = y + MAX_G * D;   // [MAX_G] history max and sum
+  float* hL = hM + MAX_G;
+  const bool unrot = !a.bf16_history && a.rot.mode != OSCAR_ROT_NONE;
+  const bool dense = unrot && a.rot.mode == OSCAR_ROT_OSCAR;
+  if (dense && t == 0) {
+    fence_proxy_async();
+    mbar_expect_tx(ubar, D * D * 4);
+    bulk_g2s(Us, a.rot.Ut_V + (size_t)kvh * D * D, D * D * 4, ubar);
+  }
   const int pages_b = (cv.hist_lens[b] + PAGE - 1) / PAGE;
   const int nb = (pages_b + sc.S - 1) / sc.S;
   const int base = pre[b] + kvh * nb;
-  float* wq = lh + MAX_G;  // [nb] weights of the history partials
-  float* rs = wq + nb;     // [8] block reductions
-  const int warp = c >> 5, lane = c & 31;
-  for (int n = 0; n < G; ++n) {
-    // 1) M = max of the partial maxima (all partials read in parallel)
+  const int wslot = sc.n_hist + (b * cv.Hkv + kvh) * sc.wch;
+  float4 Ow[2];   // window output of this warp's heads
+  float mwv[2], lwv[2];
+  for (int hh = 0; hh * NW + warp < G; ++hh) {
+    const int n = hh * NW + warp;
+    // ---- round 1: m and l of every partial (history: q = lane + 32k; window: lane < wch)
+    float mq[MERGE_KQ], lq[MERGE_KQ];
     float mloc = -INFINITY;
-    for (int q = c; q < nb; q += 128) {
+#pragma unroll
+    for (int k = 0; k < MERGE_KQ; ++k) {
+      const int q = lane + 32 * k;
+      mq[k] = -INFINITY;
+      lq[k] = 0.f;
+      if (q < nb) {
+        const float* rec = a.part + ((size_t)(base + q) * G + n) * PART_STRIDE;
+        mq[k] = __ldcg(rec);
+        lq[k] = __ldcg(rec + 1);
+      }
+    }
+    const float* wrec = a.part + ((size_t)(wslot + (lane < sc.wch ? lane : 0)) * G + n) * PART_STRIDE;
+    const float mu = lane < sc.wch ? __ldcg(wrec) : -INFINITY;
+    const float lu = lane < sc.wch ? __ldcg(wrec + 1) : 0.f;
+#pragma unroll
+    for (int k = 0; k < MERGE_KQ; ++k)
+      if (lq[k] > 0.f) mloc = fmaxf(mloc, mq[k]);
+    // partials beyond 32 * MERGE_KQ (only with very many items): read again
+    for (int q = lane + 32 * MERGE_KQ; q < nb; q += 32) {
       const float* rec = a.part + ((size_t)(base + q) * G + n) * PART_STRIDE;
-      const float mq = __ldcg(rec), lq = __ldcg(rec + 1);
-      wq[q] = lq > 0.f ? mq : -INFINITY;
-      if (lq > 0.f) mloc = fmaxf(mloc, mq);
+      if (__ldcg(rec + 1) > 0.f) mloc = fmaxf(mloc, __ldcg(rec));
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
-    if (lane == 0) rs[warp] = mloc;
-    __syncthreads();
-    const float M = fmaxf(fmaxf(rs[0], rs[1]), fmaxf(rs[2], rs[3]));
-    // 2) weights l_q * 2^(m_q - M) and their sum
+    const float M = mloc;
+    float wk[MERGE_KQ];
     float lloc = 0.f;
-    for (int q = c; q < nb; q += 128) {
+#pragma unroll
+    for (int k = 0; k < MERGE_KQ; ++k) {
+      wk[k] = lq[k] > 0.f ? ex2(mq[k] - M) : 0.f;
+      lloc = fmaf(lq[k], wk[k], lloc);
+    }
+    for (int q = lane + 32 * MERGE_KQ; q < nb; q += 32) {
       const float* rec = a.part + ((size_t)(base + q) * G + n) * PART_STRIDE;
-      const float mq = wq[q];
-      const float w = mq == -INFINITY ? 0.f : ex2(mq - M);
-      wq[q] = w;
-      lloc = fmaf(__ldcg(rec + 1), w, lloc);
+      const float l2 = __ldcg(rec + 1);
+      if (l2 > 0.f) lloc = fmaf(l2, ex2(__ldcg(rec) - M), lloc);
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, o);
-    if (lane == 0) rs[4 + warp] = lloc;
-    __syncthreads();
-    const float Ls = (rs[4] + rs[5]) + (rs[6] + rs[7]);
-    // 3) O[c] = sum_q w_q o_q[c], 8 independent loads at a time
-    float O = 0.f;
-    int q = 0;
-    for (; q + 8 <= nb; q += 8) {
-      float o8[8];
+    float mw = lu > 0.f ? mu : -INFINITY;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) o8[u] = __ldcg(a.part + ((size_t)(base + q + u) * G + n) * PART_STRIDE + 2 + c);
+    for (int o = 16; o; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+    const float wu = lu > 0.f ? ex2(mu - mw) : 0.f;
+    float lw = lu * wu;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) O = fmaf(o8[u], wq[q + u], O);
+    for (int o = 16; o; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+    // ---- round 2+: o of the partials, 32 at a time (window with the first batch)
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 OW = make_float4(0.f, 0.f, 0.f, 0.f);
+    {
+      float4 o5[5];
+#pragma unroll
+      for (int u = 0; u < 5; ++u)
+        o5[u] = u < sc.wch ? __ldcg((const float4*)(a.part + ((size_t)(wslot + u) * G + n) * PART_STRIDE + PART_O) + lane)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 5; ++u) OW = fma4(o5[u], __shfl_sync(0xffffffffu, wu, u), OW);
     }
-    for (; q < nb; ++q) O = fmaf(__ldcg(a.part + ((size_t)(base + q) * G + n) * PART_STRIDE + 2 + c), wq[q], O);
-    oh[n * D + c] = O;
-    if (c == 0) {
-      mh[n] = Ls > 0.f ? M : -INFINITY;
-      lh[n] = Ls;
+    for (int q0 = 0; q0 < nb; q0 += 32) {
+      float4 o32[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u)
+        o32[u] = (q0 + u < nb)
+                     ? __ldcg((const float4*)(a.part + ((size_t)(base + q0 + u) * G + n) * PART_STRIDE + PART_O) + lane)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      const int kb = q0 >> 5;  // weights of partials q0..q0+31 sit in wk[kb] of lanes 0..31
+      float wsel = 0.f;
+      if (kb < MERGE_KQ) {
+#pragma unroll
+        for (int k = 0; k < MERGE_KQ; ++k)
+          if (k == kb) wsel = wk[k];
+      } else {
+        const int q = q0 + lane;
+        if (q < nb) {
+          const float* rec = a.part + ((size_t)(base + q) * G + n) * PART_STRIDE;
+          wsel = __ldcg(rec + 1) > 0.f ? ex2(__ldcg(rec) - M) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 32; ++u) O = fma4(o32[u], __shfl_sync(0xffffffffu, wsel, u), O);
     }
-    __syncthreads();
+    // ---- o'·P_br·H in registers (channel c = 4*lane + k)
+    float v[4] = {O.x, O.y, O.z, O.w};
+    if (unrot) {
+      if (a.rot.mode == OSCAR_ROT_OSCAR) {
+        ((float4*)(y + n * D))[lane] = O;
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = y[n * D + bitrev7(4 * lane + k)];
+        __syncwarp();
+      }
+#pragma unroll
+      for (int k = 0; k < 4; k += 2) {
+        const float p0 = v[k], p1 = v[k + 1];
+        v[k] = p0 + p1;
+        v[k + 1] = p0 - p1;
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float p0 = v[k], p1 = v[k + 2];
+        v[k] = p0 + p1;
+        v[k + 2] = p0 - p1;
+      }
+#pragma unroll
+      for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float o = __shfl_xor_sync(0xffffffffu, v[k], h);
+          v[k] = (lane & h) ? (o - v[k]) : (v[k] + o);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] *= INV_SQRT_D;
+    }
+    ((float4*)(y + n * D))[lane] = make_float4(v[0], v[1], v[2], v[3]);
+    if (lane == 0) {
+      hM[n] = lloc > 0.f ? M : -INFINITY;
+      hL[n] = lloc;
+    }
+    Ow[hh] = OW;
+    mwv[hh] = mw;
+    lwv[hh] = lw;
   }
   __syncthreads();
-  if (!a.bf16_history && a.rot.mode != OSCAR_ROT_NONE) {
-    // o'·P_br then ·H, per head
-    for (int n = 0; n < G; ++n) {
-      float v = oh[n * D + (a.rot.mode == OSCAR_ROT_OSCAR ? bitrev7(c) : c)];
-      v = fwht128(v, c, tmp, 1);
-      y[n * D + c] = v;
-    }
-    __syncthreads();
-    if (a.rot.mode == OSCAR_ROT_OSCAR) {
-      // ·U_V^T for all heads at once: one load of Ut feeds G FMAs
-      const float* Ut = a.rot.Ut_V + (size_t)kvh * D * D + c;
-      float acc[MAX_G];
+  // ---- ·U_V^T from shared memory for all heads (thread t = output channel)
+  if (dense) {
+    if (!mbar_wait(ubar, uphase)) record_error(cv.err, OSCAR_ERR_TIMEOUT);
+    float acc[MAX_G];
 #pragma unroll
-      for (int n = 0; n < MAX_G; ++n) acc[n] = 0.f;
-      for (int i0 = 0; i0 < D; i0 += 16) {
-        float u[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) u[k] = __ldg(Ut + (i0 + k) * D);
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-#pragma unroll
-          for (int n = 0; n < MAX_G; ++n)
-            if (n < G) acc[n] = fmaf(y[n * D + i0 + k], u[k], acc[n]);
-      }
-      __syncthreads();
+    for (int n = 0; n < MAX_G; ++n) acc[n] = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < D; ++i) {
+      const float u = Us[i * D + t];
 #pragma unroll
       for (int n = 0; n < MAX_G; ++n)
-        if (n < G) oh[n * D + c] = acc[n];
-    } else {
-      for (int n = 0; n < G; ++n) oh[n * D + c] = y[n * D + c];
+        if (n < G) acc[n] = fmaf(y[n * D + i], u, acc[n]);
     }
     __syncthreads();
+#pragma unroll
+    for (int n = 0; n < MAX_G; ++n)
+      if (n < G) y[n * D + t] = acc[n];
+    __syncthreads();
   }
-  const int wslot = sc.n_hist + b * cv.Hkv + kvh;
-  for (int n = 0; n < G; ++n) {
-    const float* w = a.part + ((size_t)wslot * G + n) * PART_STRIDE;
-    const float mw = __ldcg(w), lw = __ldcg(w + 1), ow = __ldcg(w + 2 + c);
-    const float M = mh[n], Ls = lh[n], O = oh[n * D + c];
+  // ---- per warp: LSE-merge of history and window for its heads
+  for (int hh = 0; hh * NW + warp < G; ++hh) {
+    const int n = hh * NW + warp;
+    const float M = hM[n], Ls = hL[n], mw = mwv[hh], lw = lwv[hh];
+    const float4 Oh = ((const float4*)(y + n * D))[lane];
     const float M2 = fmaxf(Ls > 0.f ? M : -INFINITY, lw > 0.f ? mw : -INFINITY);
-    float o = 0.f, lse = -INFINITY;
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    float lse = -INFINITY;
     if (M2 != -INFINITY) {
       const float fh = Ls > 0.f ? ex2(M - M2) : 0.f;
       const float fw = lw > 0.f ? ex2(mw - M2) : 0.f;
-      const float lt = Ls * fh + lw * fw;
-      o = (O * fh + ow * fw) / lt;
-      lse = (M2 + log2f(lt)) * LN2;
+      const float inv = 1.f / (Ls * fh + lw * fw);
+      o[0] = (Oh.x * fh + Ow[hh].x * fw) * inv;
+      o[1] = (Oh.y * fh + Ow[hh].y * fw) * inv;
+      o[2] = (Oh.z * fh + Ow[hh].z * fw) * inv;
+      o[3] = (Oh.w * fh + Ow[hh].w * fw) * inv;
+      lse = (M2 + log2f(Ls * fh + lw * fw)) * LN2;
     }
     const size_t row = (size_t)b * cv.Hq + kvh * G + n;
-    a.out[row * D + c] = __float2bfloat16_rn(o);
-    if (a.lse && c == 0) a.lse[row] = lse;
+    __nv_bfloat162 o01 = __floats2bfloat162_rn(o[0], o[1]);
+    __nv_bfloat162 o23 = __floats2bfloat162_rn(o[2], o[3]);
+    uint2 pk;
+    pk.x = *(const uint32_t*)&o01;
+    pk.y = *(const uint32_t*)&o23;
+    *(uint2*)(a.out + row * D + 4 * lane) = pk;
+    if (a.lse && lane == 0) a.lse[row] = lse;
   }
 }
 
+// IMPL: 0 INT2 history on tensor cores, 1 INT2 history on CUDA cores,
+// 2 BF16 history (the baseline; no INT2 code, double-buffered BF16 tiles).
 template <int NG, int IMPL>
-__global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(NW * 32, IMPL == 0 ? 3 : 2) decode_kernel(DecodeArgs a) {
+  constexpr bool BF16H = (IMPL == 2);
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheView& cv = a.cv;
-  const SmemLayout L = smem_layout(cv.head_bytes, a.B, a.bf16_history ? 2 : IMPL);
+  const SmemLayout L = smem_layout(cv.head_bytes, a.B, IMPL);
   uint64_t* mbar = (uint64_t*)(smem + L.off_mbar);
   float* qf = (float*)(smem + L.off_qf);  // CUDA-core path: [MAX_G][D] q' + [MAX_G][4] z weights
   float* vsw = (float*)(smem + L.off_vs);
@@ -710,8 +888,11 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
   const int gid = lane >> 2, tq = lane & 3;
   const int G = cv.G, Hkv = cv.Hkv;
 
-  if (threadIdx.x < NW * DEPTH) mbar_init(&mbar[threadIdx.x], 1);
-  if (threadIdx.x == 0) misc[1] = 0;
+  if (threadIdx.x < NW * DEPTH + 1) mbar_init(&mbar[threadIdx.x], 1);
+  if (threadIdx.x == 0) {
+    misc[1] = 0;
+    misc[3] = 0;  // merges done by this CTA (phase of the merge barrier)
+  }
   fence_proxy_async();
   __syncthreads();
 
@@ -735,9 +916,11 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
       idx = is_win ? it - sc.n_hist : it;
     }
     int b, kvh, jj = 0, slot;
+    int wc = 0;  // window chunk of this item (wch == 5)
     if (is_win) {
-      b = idx / Hkv;
-      kvh = idx % Hkv;
+      b = idx / (Hkv * sc.wch);
+      kvh = (idx / sc.wch) % Hkv;
+      wc = idx % sc.wch;
       slot = sc.n_hist + idx;
     } else {
       hist_item_coords(idx, pre, a.B, Hkv, cv.hist_lens, sc.S, b, kvh, jj);
@@ -746,7 +929,7 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
     const int hist_b = cv.hist_lens[b];
     const int pages_b = (hist_b + PAGE - 1) / PAGE;
 
-    if (is_win || a.bf16_history) {
+    if (is_win || BF16H) {
       // ---------------------------------------------------- BF16 tokens
       Bf16State S;
 #pragma unroll
@@ -768,7 +951,11 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
         const int nsink = Lq < SINK ? Lq : SINK;
         const int recent = Lq > SINK ? Lq - SINK - hist_b : 0;
         const int h0 = hist_b % RECENT;
-        for (int ch = warp; ch < 5; ch += NW) {
+        // wch == 1: warps take the 5 chunks in turn; wch == 5: this item is
+        // chunk wc and warp w takes its 16-token tile w
+        const int ch_begin = sc.wch == 1 ? warp : wc;
+        const int ch_step = sc.wch == 1 ? NW : 5;
+        for (int ch = ch_begin; ch < 5; ch += ch_step) {
           uint64_t valid = 0;
           const __nv_bfloat16 *Kb, *Vb;
           if (ch == 0) {
@@ -788,14 +975,23 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
             Kb = cv.ring_k + (head * RECENT + s0) * D;
             Vb = cv.ring_v + (head * RECENT + s0) * D;
           }
-          if (valid) bf16_chunk_mma(S, Kb, Vb, valid, lane);
+          if (sc.wch == 1) {
+            if (valid) bf16_chunk_mma<BF16H>(S, Kb, Vb, valid, lane);
+          } else if ((valid >> (16 * warp)) & 0xFFFFull) {
+            bf16_span_mma<BF16H>(S, Kb, Vb, valid, lane, warp, 1);
+          }
         }
       } else {
         const int p0 = jj * sc.S;
         int p1 = p0 + sc.S;
         if (p1 > pages_b) p1 = pages_b;
-        for (int p = p0 + warp; p < p1; p += NW) {
-          const int pid = cv.page_table[(size_t)b * cv.max_pages_per_req + p];
+        const int nwp = (p1 - p0 - warp + NW - 1) / NW > 0 ? (p1 - p0 - warp + NW - 1) / NW : 0;
+        PageIds P;
+        page_ids_init(P, cv, b, p0 + warp, nwp, lane);
+        for (int k = 0; k < nwp; ++k) {
+          if (k > 0 && (k & 31) == 0) page_ids_advance(P, cv, b, p0 + warp, nwp, lane);
+          const int p = p0 + warp + k * NW;
+          const int pid = page_id_at(P, k);
           if (pid < 0 || pid >= cv.num_pages) {
             if (lane == 0) record_error(cv.err, pid < 0 ? OSCAR_ERR_NO_PAGE : OSCAR_ERR_RANGE);
             continue;
@@ -804,7 +1000,7 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
           const uint64_t valid = nv >= 64 ? ~0ull : ((1ull << nv) - 1ull);
           const __nv_bfloat16* Kb =
               (const __nv_bfloat16*)(cv.pool + (size_t)pid * cv.page_bytes + (size_t)kvh * BF16_HEAD_BYTES);
-          bf16_chunk_mma(S, Kb, Kb + PAGE * D, valid, lane);
+          bf16_chunk_mma<BF16H>(S, Kb, Kb + PAGE * D, valid, lane);
         }
       }
 #pragma unroll
@@ -829,7 +1025,7 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
           }
         }
       }
-    } else {
+    } else if constexpr (!BF16H) {
       // ------------------------------------------------------ INT2 history
       const int p0 = jj * sc.S;
       int p1 = p0 + sc.S;
@@ -837,10 +1033,10 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
       const int nw_pages = (p1 - p0 - warp + NW - 1) / NW > 0 ? (p1 - p0 - warp + NW - 1) / NW : 0;
       uint8_t* my_stage = smem + L.off_stage + (size_t)warp * DEPTH * L.stage_bytes;
       uint64_t* my_bar = mbar + warp * DEPTH;
-      auto issue = [&](int k) {  // lane 0 only: k-th page of this warp
-        const int p = p0 + warp + k * NW;
+      PageIds P;
+      page_ids_init(P, cv, b, p0 + warp, nw_pages, lane);
+      auto issue = [&](int k, int pid) {  // lane 0 only: k-th page of this warp
         const int st = (int)((seq + k) % DEPTH);
-        const int pid = cv.page_table[(size_t)b * cv.max_pages_per_req + p];
         if (pid >= 0 && pid < cv.num_pages) {
           mbar_expect_tx(&my_bar[st], (uint32_t)cv.head_bytes);
           bulk_g2s(my_stage + (size_t)st * L.stage_bytes,
@@ -852,9 +1048,10 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
         }
       };
       __syncthreads();  // the previous item's results in the stage area are consumed
-      if (lane == 0) {
-        fence_proxy_async();
-        for (int k = 0; k < DEPTH && k < nw_pages; ++k) issue(k);
+      if (lane == 0) fence_proxy_async();
+      for (int k = 0; k < DEPTH && k < nw_pages; ++k) {
+        const int pid = page_id_at(P, k);
+        if (lane == 0) issue(k, pid);
       }
       if (!waited) {
         pdl_wait();  // q' (prep_kernel) is ready from here on
@@ -862,7 +1059,7 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
       }
       bool timed_out = false;
       int k_fail = 0;
-      if (IMPL == 0) {
+      if constexpr (IMPL == 0) {
         Int2State<NG> S;
 #pragma unroll
         for (int j = 0; j < 8; ++j) S.oacc[j][0] = S.oacc[j][1] = S.oacc[j][2] = S.oacc[j][3] = 0.f;
@@ -899,16 +1096,23 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
             k_fail = k;
             break;
           }
+          if (k > 0 && (k & 31) == 0) page_ids_advance(P, cv, b, p0 + warp, nw_pages, lane);
           const int p = p0 + warp + k * NW;
-          const int pid = cv.page_table[(size_t)b * cv.max_pages_per_req + p];
+          const int pid = page_id_at(P, k);
           if (pid >= 0 && pid < cv.num_pages) {
             const int nv = (p == pages_b - 1) ? hist_b - p * PAGE : PAGE;
-            int2_page_mma<NG>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
+            if (nv == PAGE)
+              int2_page_mma<NG, true>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
+            else
+              int2_page_mma<NG, false>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
           }
           __syncwarp();
-          if (lane == 0 && k + DEPTH < nw_pages) {
-            fence_proxy_async();
-            issue(k + DEPTH);
+          if (k + DEPTH < nw_pages) {
+            const int pid_next = page_id_at(P, k + DEPTH);
+            if (lane == 0) {
+              fence_proxy_async();
+              issue(k + DEPTH, pid_next);
+            }
           }
         }
 #pragma unroll
@@ -982,16 +1186,20 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
             k_fail = k;
             break;
           }
+          if (k > 0 && (k & 31) == 0) page_ids_advance(P, cv, b, p0 + warp, nw_pages, lane);
           const int p = p0 + warp + k * NW;
-          const int pid = cv.page_table[(size_t)b * cv.max_pages_per_req + p];
+          const int pid = page_id_at(P, k);
           if (pid >= 0 && pid < cv.num_pages) {
             const int nv = (p == pages_b - 1) ? hist_b - p * PAGE : PAGE;
             int2_page_core<NG>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane, G, qf, kgm, ps, vs);
           }
           __syncwarp();
-          if (lane == 0 && k + DEPTH < nw_pages) {
-            fence_proxy_async();
-            issue(k + DEPTH);
+          if (k + DEPTH < nw_pages) {
+            const int pid_next = page_id_at(P, k + DEPTH);
+            if (lane == 0) {
+              fence_proxy_async();
+              issue(k + DEPTH, pid_next);
+            }
           }
         }
         if (timed_out) {
@@ -1024,14 +1232,18 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
     // Last finisher of this (request, kv head) merges it.
     __syncthreads();
     if (threadIdx.x == 0) {
-      __threadfence();
       const int nb = (pages_b + sc.S - 1) / sc.S;
       const int old = atomicAdd(&a.done[b * Hkv + kvh], 1);
-      misc[2] = (old == nb) ? 1 : 0;  // nb history items + 1 window item
-      __threadfence();
+      misc[2] = (old == nb + sc.wch - 1) ? 1 : 0;  // nb history items + wch window items
+      fence_acq_rel_gpu();  // acquire: the other CTAs' records are read after this
     }
     __syncthreads();
-    if (misc[2]) merge_bkvh(a, sc, pre, b, kvh, wm);
+    if (misc[2]) {
+      merge_bkvh(a, sc, pre, b, kvh, wm, &mbar[NW * DEPTH], (uint32_t)misc[3] & 1u);
+      __syncthreads();
+      // the merge's U_V^T copy completed one phase of its barrier
+      if (threadIdx.x == 0 && !BF16H && a.rot.mode == OSCAR_ROT_OSCAR) misc[3] += 1;
+    }
     if (misc[1]) break;
     __syncthreads();
     if (threadIdx.x == 0) misc[0] = (int)gridDim.x + atomicAdd(a.counter, 1);
@@ -1043,7 +1255,7 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_kernel(DecodeArgs a) {
 
 template <int NG, int IMPL>
 cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t st) {
-  const SmemLayout L = smem_layout(a.cv.head_bytes, a.B, a.bf16_history ? 2 : IMPL);
+  const SmemLayout L = smem_layout(a.cv.head_bytes, a.B, IMPL);
   if ((L.off_mbar % 8) || (L.off_stage % 128) || (L.off_pre % 16)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<NG, IMPL>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
@@ -1080,6 +1292,36 @@ size_t decode_scratch_bytes(int B, int Hq, int Hkv, int G, int max_target_items)
   return scratch_layout(B, Hq, Hkv, G, max_target_items).total;
 }
 
+// Resident decode CTAs per SM for this launch's kernel and shared memory
+// (cached per kernel variant and shared-memory size).
+template <int NG, int IMPL>
+int occupancy_t(const DecodeArgs& a) {
+  static int cached_smem = -1, cached_occ = 0;
+  const SmemLayout L = smem_layout(a.cv.head_bytes, a.B, IMPL);
+  if (cached_smem == L.total) return cached_occ;
+  if (cudaFuncSetAttribute(decode_kernel<NG, IMPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           L.total) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<NG, IMPL>, NW * 32, L.total) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  cached_occ = n;
+  cached_smem = L.total;
+  return n;
+}
+
+int decode_ctas_per_sm(const DecodeArgs& a) {
+  const int NG = a.cv.NG;
+  if (a.bf16_history) return occupancy_t<1, 2>(a);
+  if (a.impl == 1) return NG == 1 ? occupancy_t<1, 1>(a) : NG == 2 ? occupancy_t<2, 1>(a) : occupancy_t<4, 1>(a);
+  return NG == 1 ? occupancy_t<1, 0>(a) : NG == 2 ? occupancy_t<2, 0>(a) : occupancy_t<4, 0>(a);
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof) {
   const CacheView& cv = a.cv;
   prof_begin(prof, OSCAR_KERNEL_DECODE_PREP, st);
@@ -1088,7 +1330,9 @@ cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profil
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_begin(prof, OSCAR_KERNEL_DECODE_MAIN, st);
-  if (a.impl == 1 && !a.bf16_history) {
+  if (a.bf16_history) {
+    e = launch_decode_t<1, 2>(a, grid, st);
+  } else if (a.impl == 1) {
     if (cv.NG == 1) e = launch_decode_t<1, 1>(a, grid, st);
     else if (cv.NG == 2) e = launch_decode_t<2, 1>(a, grid, st);
     else e = launch_decode_t<4, 1>(a, grid, st);

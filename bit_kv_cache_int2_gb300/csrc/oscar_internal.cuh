@@ -19,7 +19,8 @@ constexpr int PAGE = 64;     // tokens per page
 constexpr int SINK = 64;     // BF16 sink tokens   [News, "服务系统：混合精度缓存布局"]
 constexpr int RECENT = 256;  // BF16 recent tokens [News, "服务系统：混合精度缓存布局"]
 constexpr int MAX_G = 8;     // query heads per KV head handled by one mma column tile
-constexpr int PART_STRIDE = D + 2;  // partial record per head: m, l, o[128]
+constexpr int PART_STRIDE = D + 4;  // partial record per head: m, l, 2 pad, o[128] (o 16-byte aligned)
+constexpr int PART_O = 4;            // offset of o in a partial record
 constexpr int MAX_TARGET_ITEMS = 2048;
 constexpr int QPACK_BYTES = 320;  // packed query record per (request, query head)
 constexpr int WIN_BYTES_PER_HEAD = (SINK + RECENT) * D * 2 * 2;  // K and V
@@ -58,6 +59,9 @@ struct CacheView {
   int head_bytes;        // bytes of one head's block
   int* err;
 };
+
+// Release/acquire fence at GPU scope (lighter than a sequentially consistent one).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;\n" ::: "memory"); }
 
 __device__ __forceinline__ void record_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
@@ -266,13 +270,22 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 // OR-ed with the exponent of 1024, giving 1024 + code * 2^E(I) exactly, with
 // E = {4,6,4,6,8,4,6,8}[I].  Callers fold 2^-E and the 1024 offset into the
 // other operand.
+// (a & m) | c in one LOP3 (both constants in registers, so the compiler does
+// not split it into an AND and an OR).
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t m, uint32_t c) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(r) : "r"(a), "r"(m), "r"(c));
+  return r;
+}
+
 template <int I>
 __device__ __forceinline__ uint32_t code_pair(uint32_t w) {
   constexpr uint32_t M = (I == 0 || I == 2 || I == 5) ? 0x00300030u
                          : (I == 1 || I == 3 || I == 6) ? 0x00C000C0u
                                                         : 0x03000300u;
-  const uint32_t src = (I <= 1) ? (w << 4) : (I <= 4) ? w : (w >> 6);
-  return (src & M) | 0x64006400u;
+  // w << 4 as a multiply (FMA pipe), w >> 6 as a shift
+  const uint32_t src = (I <= 1) ? (w * 16u) : (I <= 4) ? w : (w >> 6);
+  return and_or(src, M, 0x64006400u);
 }
 template <int I>
 __host__ __device__ constexpr int code_exp() {
@@ -335,7 +348,8 @@ __device__ __forceinline__ void fence_proxy_async() {
 struct Sched {
   int S;            // pages per history item
   int n_hist;       // number of history items
-  int n_win;        // number of window items (B * Hkv)
+  int n_win;        // number of window items (B * Hkv * wch)
+  int wch;          // window items per (request, kv head): 5 (one per 64-token chunk) or 1
   int win_first;    // window items are handed out before history items
 };
 
@@ -356,7 +370,10 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
   __syncthreads();
   total *= Hkv;
   Sched s;
-  s.n_win = B * Hkv;
+  // small batches split each 320-token window into its 5 chunks so that no
+  // single window item outlasts the history items
+  s.wch = (5LL * B * Hkv * 4 <= target) ? 5 : 1;
+  s.n_win = B * Hkv * s.wch;
   int th = target - s.n_win;
   if (th < (target + 1) / 2) th = (target + 1) / 2;
   long long S = (total + th - 1) / th;
@@ -386,7 +403,7 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
   s.S = red[0];
   __syncthreads();
   s.n_hist = pre[B];
-  s.win_first = (long long)WIN_BYTES_PER_HEAD > (long long)s.S * hist_item_unit_bytes;
+  s.win_first = (long long)WIN_BYTES_PER_HEAD / s.wch > (long long)s.S * hist_item_unit_bytes;
   return s;
 }
 
@@ -431,6 +448,7 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof);
+int decode_ctas_per_sm(const DecodeArgs& a);  // resident CTAs per SM of the decode kernel (0: error)
 
 // Decode scratch: [work counter][done counters][q' fp32][packed q][partials]
 struct ScratchLayout {

@@ -63,6 +63,13 @@ __global__ void __launch_bounds__(512) append_kernel(CacheView cv, LayerRot rot,
   __shared__ int st[6];
   const int b = blockIdx.x / cv.Hkv, h = blockIdx.x % cv.Hkv, isv = blockIdx.y;
   const int t = threadIdx.x, j = t & 127, pp = t >> 7;
+  // U's loads do not depend on the cache state: start them first
+  float u[32];
+  if (rot.mode == OSCAR_ROT_OSCAR) {
+    const float* U = (isv ? rot.U_V : rot.U_K) + (size_t)h * D * D + (size_t)(32 * pp) * D + j;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) u[k] = __ldg(U + k * D);
+  }
   if (t == 0) {
     const int L = cv.seq_lens[b], H = cv.hist_lens[b];
     const int recent = L > SINK ? L - SINK - H : 0;
@@ -104,10 +111,6 @@ __global__ void __launch_bounds__(512) append_kernel(CacheView cv, LayerRot rot,
     __syncthreads();
     float acc = 0.f;
     if (rot.mode == OSCAR_ROT_OSCAR) {
-      const float* U = (isv ? rot.U_V : rot.U_K) + (size_t)h * D * D + (size_t)(32 * pp) * D + j;
-      float u[32];
-#pragma unroll
-      for (int k = 0; k < 32; ++k) u[k] = __ldg(U + k * D);
 #pragma unroll
       for (int k = 0; k < 32; ++k) acc = fmaf(xs[32 * pp + k], u[k], acc);
     } else if (pp == 0) {
@@ -155,15 +158,15 @@ __global__ void __launch_bounds__(512) append_kernel(CacheView cv, LayerRot rot,
   // request has read the old lengths before it increments the counter.
   __syncthreads();
   if (t == 0) {
-    __threadfence();
+    fence_acq_rel_gpu();  // this CTA's reads of the old lengths come before the count
     const int old = atomicAdd(&req_counter[b], 1);
     if (old == 2 * cv.Hkv - 1) {
+      fence_acq_rel_gpu();
       req_counter[b] = 0;
       if (ok) {
         cv.seq_lens[b] = L + (do_append ? 1 : 0);
         cv.hist_lens[b] = H + demote;
       }
-      __threadfence();
     }
   }
 }

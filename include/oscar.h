@@ -103,7 +103,7 @@ typedef enum {
 
 typedef enum {
   OSCAR_OPT_DECODE_IMPL = 0, /* 0: tensor-core INT2 kernel (default); 1: CUDA-core fp32 kernel */
-  OSCAR_OPT_CTAS_PER_SM = 1, /* persistent decode CTAs per SM, 1..4 (default 2)               */
+  OSCAR_OPT_CTAS_PER_SM = 1, /* persistent decode CTAs per SM, 1..4 (default 4), capped by occupancy */
   OSCAR_OPT_ITEMS_PER_CTA = 2 /* work items per decode CTA the scheduler aims for, 1..8 (default 1) */
 } oscar_option;
 
