@@ -346,6 +346,32 @@ __device__ __forceinline__ void int2_page_mma(Int2State<NG>& S, const uint8_t* s
   }
 }
 
+// The SV accumulators carry 1024 * (sum of B values) on top of the signal;
+// over hundreds of pages that offset would cost fp32 accuracy, so it is moved
+// out of them every few pages: oacc -= 1024 * sum_B (all rows of the page
+// group), and the running sum of B restarts at 0.
+template <int NG>
+__device__ __forceinline__ void flush_v_offset(Int2State<NG>& S) {
+  constexpr int MPG = 8 / NG;
+#pragma unroll
+  for (int hc = 0; hc < 2; ++hc) {
+#pragma unroll
+    for (int gr = 0; gr < NG; ++gr) {
+      float t = S.bs[hc][gr];
+      t += __shfl_xor_sync(0xffffffffu, t, 4);
+      t += __shfl_xor_sync(0xffffffffu, t, 8);
+      t += __shfl_xor_sync(0xffffffffu, t, 16);
+      S.bs[hc][gr] = 0.f;
+      const float off = 1024.f * t;
+#pragma unroll
+      for (int jj = 0; jj < MPG; ++jj) {
+        S.oacc[gr * MPG + jj][hc] -= off;
+        S.oacc[gr * MPG + jj][hc + 2] -= off;
+      }
+    }
+  }
+}
+
 // ----------------------------------------------- CUDA-core INT2 page (fp32)
 // Lane l scores tokens l and l+32, then accumulates channels 4l..4l+3.
 struct CoreState {
@@ -1105,6 +1131,7 @@ __global__ void __launch_bounds__(NW * 32, IMPL == 0 ? 3 : 2) decode_kernel(Deco
               int2_page_mma<NG, true>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
             else
               int2_page_mma<NG, false>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
+            if ((k & 7) == 7) flush_v_offset<NG>(S);
           }
           __syncwarp();
           if (k + DEPTH < nw_pages) {

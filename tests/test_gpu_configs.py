@@ -1,0 +1,125 @@
+"""GPU parity at the full sizes of the benchmark workloads, on sampled outputs
+the oracle can compute (all in the library's default launch configuration)."""
+import numpy as np
+import pytest
+import torch
+
+from bit_kv_cache_int2_gb300 import build as B
+from bit_kv_cache_int2_gb300 import oscar, synth
+
+pytestmark = pytest.mark.gpu
+
+import gpu_scenario as GS  # noqa: E402
+
+REL_TOL = 1e-2
+LSE_TOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    B.build()
+    oscar.lib()
+
+
+def _rel(a, b):
+    return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-30))
+
+
+def _append_one(sc, lengths):
+    k = torch.stack([sc.K[b][:, L] for b, L in enumerate(lengths)]).contiguous()
+    v = torch.stack([sc.V[b][:, L] for b, L in enumerate(lengths)]).contiguous()
+    oscar.oscar_append(sc.ctx, 0, sc.cache, k, v, len(lengths))
+
+
+def _check_requests(sc, q, out, lse, requests):
+    hc = GS.HostCache(sc)
+    qn = q.float().cpu().numpy()
+    for b in requests:
+        ref, rlse = GS.oracle_decode(sc, hc, qn, b)
+        got = out[b].float().cpu().numpy()
+        print(f"request {b}: rel err {_rel(got, ref):.2e}, lse err {np.abs(lse[b].cpu().numpy() - rlse).max():.2e}")
+        assert _rel(got, ref) <= REL_TOL, (b, _rel(got, ref))
+        assert np.abs(lse[b].cpu().numpy() - rlse).max() <= LSE_TOL, b
+    return hc
+
+
+def test_qwen3_8b_100k_b1():
+    """32 q / 8 kv heads, g128, 100,000 tokens, random page table; one append
+    (demoting one token) then a decode; every head checked."""
+    sc = GS.build("w100k", [100000], Hq=32, Hkv=8, g=128, extra_tokens=1, calib_n=1024)
+    try:
+        _append_one(sc, [100000])
+        q = GS.queries(sc, seed=21)
+        out, lse = GS.decode(sc, q)
+        assert oscar.oscar_get_error(sc.ctx) == 0
+        hc = _check_requests(sc, q, out, lse, [0])
+        assert (int(hc.seq[0]), int(hc.hist[0])) == (100001, 99681)
+        rng = np.random.default_rng(0)
+        for h in (0, 5):
+            slots = sorted(rng.choice(99681, 1500, replace=False).tolist()) + [99680]
+            n, bad = GS.compare_history(sc, hc, 0, h, [64 + t for t in slots], slots)
+            assert bad <= 1e-4 * n
+    finally:
+        sc.close()
+
+
+def test_qwen3_4b_b32_interleaved_pages():
+    """32 q / 8 kv heads, batch 32, lengths uniform in [8K, 32K], pages dealt
+    round-robin across requests; one append per request then a decode."""
+    lengths = synth.lengths(32, 8192, 32768, synth.stream_seed(0, "w4b", "lengths"))
+    sc = GS.build("w4b", lengths, Hq=32, Hkv=8, g=128, interleave=True, extra_tokens=1, calib_n=1024)
+    try:
+        _append_one(sc, lengths)
+        q = GS.queries(sc, seed=22)
+        out, lse = GS.decode(sc, q)
+        assert oscar.oscar_get_error(sc.ctx) == 0
+        _check_requests(sc, q, out, lse, [0, 7, 19, 31])
+    finally:
+        sc.close()
+
+
+def test_qwen3_32b_131k_b8_int2_and_bf16():
+    """64 q / 8 kv heads (GQA 8), batch 8, 131,072 tokens each, clip 0.9, keys
+    with 8 outlier channels x30: INT2 decode and the BF16-history decode."""
+    lengths = [131072] * 8
+    kw = dict(Hq=64, Hkv=8, g=128, clip_k=0.9, clip_v=0.9, n_out=8, f_key=30.0, calib_n=1024)
+    sc = GS.build("w32b", lengths, **kw)
+    try:
+        q = GS.queries(sc, seed=23)
+        out, lse = GS.decode(sc, q)
+        assert oscar.oscar_get_error(sc.ctx) == 0
+        _check_requests(sc, q, out, lse, [0, 5])
+    finally:
+        sc.close()
+    sb = GS.build("w32b", lengths, bf16_history=True, mode=oscar.ROT_NONE, **kw)
+    try:
+        q = GS.queries(sb, seed=23)
+        out, lse = GS.decode(sb, q)
+        assert oscar.oscar_get_error(sb.ctx) == 0
+        _check_requests(sb, q, out, lse, [3])
+    finally:
+        sb.close()
+
+
+def test_qwen3_8b_stack_g32_two_layers_stepping():
+    """Two layers of the 36-layer g32 stack (batch 16, 65,536 tokens, own
+    rotations per layer): 8 steps of append + decode per layer; the last
+    step's outputs and every demoted token checked on sampled requests."""
+    lengths = [65536] * 16
+    steps = 8
+    for layer in range(2):
+        sc = GS.build(f"stack{layer}", lengths, Hq=32, Hkv=8, g=32, extra_tokens=steps, calib_n=1024)
+        try:
+            for t in range(steps):
+                _append_one(sc, [L + t for L in lengths])
+                q = GS.queries(sc, seed=100 + t)
+                out, lse = GS.decode(sc, q)
+            assert oscar.oscar_get_error(sc.ctx) == 0
+            hc = _check_requests(sc, q, out, lse, [2, 13])
+            H = int(hc.hist[2])
+            assert H == 65536 + steps - 320
+            slots = list(range(H - steps, H))
+            n, bad = GS.compare_history(sc, hc, 2, 6, [64 + s for s in slots], slots)
+            assert bad <= 1e-4 * n or bad == 0
+        finally:
+            sc.close()
