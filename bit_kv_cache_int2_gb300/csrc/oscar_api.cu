@@ -53,7 +53,7 @@ struct oscar_ctx {
   int device = 0;
   int num_sms = 0;
   int G = 0, NG = 0;
-  float* d_rot = nullptr;  // [layers][3][Hkv][128][128]: U_K, U_V, U_V^T
+  float* d_rot = nullptr;  // [layers][4][Hkv][128 * 128 words]: U_K, U_V, R_K, R_V fragments
   float* d_clip = nullptr;  // [layers][2][Hkv]
   std::vector<int> mode;
   int* d_err = nullptr;
@@ -145,12 +145,92 @@ CacheView make_view(const oscar_ctx* ctx, const oscar_cache* c, bool bf16_histor
   return v;
 }
 
+constexpr int ROT_MATS = 4;  // U_K, U_V, R_K, R_V fragments per layer
+static_assert(RV_FRAG_WORDS == D * D, "R_V fragments fill one matrix slot");
+
+// R = U·H·P_br (OSCAR), H (HADAMARD) or I (NONE) for one head, in fp64, in the
+// row-vector convention x' = x·R [News "Together AI 开源 OSCAR…", section
+// "OSCAR 的不同之处"].  H is the normalised Sylvester Hadamard of order 128
+// applied to each row by the fast transform; (x·P_br)_j = x_bitrev(j).
+void compose_rotation(const float* U, int mode, double* R) {
+  for (int i = 0; i < D; ++i) {
+    double row[D];
+    for (int k = 0; k < D; ++k) row[k] = mode == OSCAR_ROT_OSCAR ? (double)U[(size_t)i * D + k] : (i == k);
+    if (mode != OSCAR_ROT_NONE) {
+      for (int h = 1; h < D; h <<= 1)
+        for (int k = 0; k < D; ++k)
+          if (!(k & h)) {
+            const double a = row[k], b = row[k + h];
+            row[k] = a + b;
+            row[k + h] = a - b;
+          }
+      const double sc = 1.0 / sqrt((double)D);
+      for (int k = 0; k < D; ++k) row[k] *= sc;
+    }
+    for (int j = 0; j < D; ++j) {
+      int br = 0;
+      for (int bit = 0; bit < 7; ++bit) br |= ((j >> bit) & 1) << (6 - bit);
+      R[(size_t)i * D + j] = mode == OSCAR_ROT_OSCAR ? row[br] : row[j];
+    }
+  }
+}
+
+uint32_t half_pair(__half lo, __half hi) {
+  return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+}
+
+// A = R (rows: output channel, columns: input channel) as fp16 high / low
+// mma fragments (layout of rv_frag_index).
+void pack_rv_fragments(const double* R, uint32_t* out) {
+  for (int part = 0; part < 2; ++part)
+    for (int mt = 0; mt < 8; ++mt)
+      for (int ks = 0; ks < 8; ++ks)
+        for (int lane = 0; lane < 32; ++lane) {
+          const int gid = lane >> 2, tq = lane & 3;
+          auto el = [&](int r, int c) {
+            const double v = R[(size_t)r * D + c];
+            const __half hi = __float2half_rn((float)v);
+            if (part == 0) return hi;
+            return __float2half_rn((float)(v - (double)__half2float(hi)));
+          };
+          uint32_t* w = out + rv_frag_index(part, mt, ks, lane);
+          const int r0 = 16 * mt + gid, c0 = 16 * ks + 2 * tq;
+          w[0] = half_pair(el(r0, c0), el(r0, c0 + 1));
+          w[1] = half_pair(el(r0 + 8, c0), el(r0 + 8, c0 + 1));
+          w[2] = half_pair(el(r0, c0 + 8), el(r0, c0 + 9));
+          w[3] = half_pair(el(r0 + 8, c0 + 8), el(r0 + 8, c0 + 9));
+        }
+}
+
+// One layer's table (ROT_MATS matrices of Hkv heads) from the eigenbases
+// (nullptr outside OSCAR mode: identity).
+void build_layer_table(const float* U_K, const float* U_V, int mode, int Hkv, std::vector<float>& out) {
+  const size_t hm = (size_t)D * D, mat = (size_t)Hkv * hm;
+  out.assign(ROT_MATS * mat, 0.f);
+  std::vector<double> R(hm);
+  for (int h = 0; h < Hkv; ++h) {
+    for (int t = 0; t < 2; ++t) {
+      const float* U = mode == OSCAR_ROT_OSCAR ? (t == 0 ? U_K : U_V) + h * hm : nullptr;
+      float* dst = out.data() + t * mat + h * hm;
+      for (size_t e = 0; e < hm; ++e) dst[e] = U ? U[e] : ((e / D) == (e % D) ? 1.f : 0.f);
+      compose_rotation(U, mode, R.data());
+      if (t == 0) {
+        float* rk = out.data() + 2 * mat + h * hm;
+        for (size_t e = 0; e < hm; ++e) rk[e] = (float)R[e];
+      } else {
+        pack_rv_fragments(R.data(), (uint32_t*)(out.data() + 3 * mat + h * hm));
+      }
+    }
+  }
+}
+
 LayerRot layer_rot(const oscar_ctx* ctx, int layer) {
   const size_t mat = (size_t)ctx->cfg.num_kv_heads * D * D;
   LayerRot r;
-  r.U_K = ctx->d_rot + (size_t)layer * 3 * mat;
+  r.U_K = ctx->d_rot + (size_t)layer * ROT_MATS * mat;
   r.U_V = r.U_K + mat;
-  r.Ut_V = r.U_V + mat;
+  r.R_K = r.U_V + mat;
+  r.RV_frag = (const uint32_t*)(r.R_K + mat);
   r.clip_k = ctx->d_clip + (size_t)layer * 2 * ctx->cfg.num_kv_heads;
   r.clip_v = r.clip_k + ctx->cfg.num_kv_heads;
   r.mode = ctx->mode[layer];
@@ -280,7 +360,7 @@ oscar_status oscar_create(const oscar_config* cfg, oscar_ctx** out) {
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device);
   const size_t mat = (size_t)cfg->num_kv_heads * D * D;
-  const size_t rot_bytes = (size_t)cfg->num_layers * 3 * mat * sizeof(float);
+  const size_t rot_bytes = (size_t)cfg->num_layers * ROT_MATS * mat * sizeof(float);
   const size_t clip_bytes = (size_t)cfg->num_layers * 2 * cfg->num_kv_heads * sizeof(float);
   if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_rot, rot_bytes);
   if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_clip, clip_bytes);
@@ -290,12 +370,10 @@ oscar_status oscar_create(const oscar_config* cfg, oscar_ctx** out) {
   if (e == cudaSuccess) e = cudaMemset(ctx->d_req_counter, 0, sizeof(int) * cfg->max_batch);
   if (e == cudaSuccess) {
     // identity rotation and clip 1.0 until oscar_set_rotation is called
-    std::vector<float> eye(3 * mat, 0.f);
-    for (int t = 0; t < 3; ++t)
-      for (int h = 0; h < cfg->num_kv_heads; ++h)
-        for (int i = 0; i < D; ++i) eye[t * mat + (size_t)h * D * D + (size_t)i * D + i] = 1.f;
+    std::vector<float> eye;
+    build_layer_table(nullptr, nullptr, OSCAR_ROT_NONE, cfg->num_kv_heads, eye);
     for (int l = 0; l < cfg->num_layers && e == cudaSuccess; ++l)
-      e = cudaMemcpy(ctx->d_rot + (size_t)l * 3 * mat, eye.data(), 3 * mat * sizeof(float),
+      e = cudaMemcpy(ctx->d_rot + (size_t)l * ROT_MATS * mat, eye.data(), ROT_MATS * mat * sizeof(float),
                      cudaMemcpyHostToDevice);
     std::vector<float> ones((size_t)cfg->num_layers * 2 * cfg->num_kv_heads, 1.f);
     if (e == cudaSuccess)
@@ -354,25 +432,14 @@ oscar_status oscar_set_rotation(oscar_ctx* ctx, int layer, const float* U_K, con
     if (!(clip_k[h] > 0.f && clip_k[h] <= 1.f) || !(clip_v[h] > 0.f && clip_v[h] <= 1.f))
       return OSCAR_ERR_INVALID_ARG;
   const size_t mat = (size_t)Hkv * D * D;
-  std::vector<float> host(3 * mat, 0.f);
-  if (rot_mode == OSCAR_ROT_OSCAR) {
-    memcpy(host.data(), U_K, mat * sizeof(float));
-    memcpy(host.data() + mat, U_V, mat * sizeof(float));
-    for (int h = 0; h < Hkv; ++h)
-      for (int i = 0; i < D; ++i)
-        for (int j = 0; j < D; ++j)
-          host[2 * mat + (size_t)h * D * D + (size_t)j * D + i] = U_V[(size_t)h * D * D + (size_t)i * D + j];
-  } else {
-    for (int t = 0; t < 3; ++t)
-      for (int h = 0; h < Hkv; ++h)
-        for (int i = 0; i < D; ++i) host[t * mat + (size_t)h * D * D + (size_t)i * D + i] = 1.f;
-  }
+  std::vector<float> host;
+  build_layer_table(U_K, U_V, rot_mode, Hkv, host);
   std::vector<float> clips(2 * Hkv);
   memcpy(clips.data(), clip_k, Hkv * sizeof(float));
   memcpy(clips.data() + Hkv, clip_v, Hkv * sizeof(float));
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e = cudaMemcpyAsync(ctx->d_rot + (size_t)layer * 3 * mat, host.data(),
-                                  3 * mat * sizeof(float), cudaMemcpyHostToDevice, st);
+  cudaError_t e = cudaMemcpyAsync(ctx->d_rot + (size_t)layer * ROT_MATS * mat, host.data(),
+                                  ROT_MATS * mat * sizeof(float), cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(ctx->d_clip + (size_t)layer * 2 * Hkv, clips.data(), 2 * Hkv * sizeof(float),
                         cudaMemcpyHostToDevice, st);

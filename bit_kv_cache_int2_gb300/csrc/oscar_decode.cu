@@ -29,6 +29,13 @@ namespace {
 constexpr int NW = 4;     // warps per decode CTA
 constexpr int DEPTH = 4;  // bulk-copy stages per warp
 
+// final merge (merge_bkvh)
+constexpr int MERGE_KQ = 4;   // partial weights held per lane: nb <= 32 * MERGE_KQ in registers
+constexpr int YST = 136;      // fp16 row stride of the mma B operand (conflict-free fragment loads)
+constexpr int MERGE_RV_BYTES = RV_FRAG_WORDS * 4;
+constexpr int MERGE_Y_BYTES = 2 * MAX_G * YST * 2 > MAX_G * D * 4 ? 2 * MAX_G * YST * 2 : MAX_G * D * 4;
+constexpr int MERGE_BYTES = MERGE_RV_BYTES + MERGE_Y_BYTES + 2 * MAX_G * 4;
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
@@ -37,111 +44,92 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // Per (request, query head) record of the packed query (QPACK_BYTES):
 //   half  qb[128]   q'_c * 2^-sigma * 2^(8 - E(c)), the QK^T B operand
 //   float alpha     2^sigma * log2(e) / (256 sqrt(d))
-//   float beta[4]   -1024 * (sum of qb over group) * alpha
-//   float gamma[4]  (sum of q' over group) * log2(e) / sqrt(d)
-constexpr int QPACK_ALPHA = 256, QPACK_BETA = 260, QPACK_GAMMA = 276;
+//   float qsum[4]   sum of qb over channels 32k .. 32k + 31
+//   float psum[4]   sum of q' over channels 32k .. 32k + 31
+// A group of g channels takes its logit offset -1024 * alpha * (sum of qb) and
+// its zero-point weight (sum of q') * log2(e) / sqrt(d) from g / 32 quarters.
+constexpr int QPACK_ALPHA = 256, QPACK_QSUM = 260, QPACK_PSUM = 276;
 
 // ------------------------------------------------------------------- prep
-// grid = B * Hkv, block = 512: four parts of 128 threads split the 128-row
-// matvec x·U; then part p rotates heads p, p + 4.
-__global__ void __launch_bounds__(512) prep_kernel(DecodeArgs a) {
+// grid (B * Hkv, 4), block 128: CTA (b * Hkv + kvh, cq) computes channels
+// 32cq .. 32cq + 31 of q' = q·R_K for the G query heads of kv head kvh; warp
+// w sums rows 32w .. 32w + 31 of R_K, lane = channel.  The fp16 prescale
+// sigma comes from |q|, which bounds every |q'_c| (R_K is orthogonal), so the
+// four CTAs of a head agree on it without talking to each other.
+__global__ void __launch_bounds__(128) prep_kernel(DecodeArgs a) {
   pdl_launch_dependents();
   __shared__ float xs[MAX_G][D];
-  __shared__ float part[4][MAX_G][D];
-  __shared__ float tmp[4][D];
-  __shared__ float red[4][8];
+  __shared__ float part[4][MAX_G][32];
+  __shared__ float nrm[MAX_G];
   const CacheView& cv = a.cv;
-  const int b = blockIdx.x / cv.Hkv, kvh = blockIdx.x % cv.Hkv, t = threadIdx.x;
-  if (t == 0) {
-    a.done[blockIdx.x] = 0;
-    if (blockIdx.x == 0) *a.counter = 0;
+  const int bk = blockIdx.x, cq = blockIdx.y;
+  const int b = bk / cv.Hkv, kvh = bk % cv.Hkv, t = threadIdx.x, w = t >> 5, lane = t & 31;
+  if (t == 0 && cq == 0) {
+    a.done[bk] = 0;
+    if (bk == 0) *a.counter = 0;
   }
   if (a.bf16_history) return;
   const int G = cv.G;
-  const int j = t & 127, pp = t >> 7;
-  float u[32];
-  if (a.rot.mode == OSCAR_ROT_OSCAR) {
-    // U_K loads first (independent of q); U_V^T rows into L2 for the merge
-    const float* U = a.rot.U_K + (size_t)kvh * D * D + (size_t)(32 * pp) * D + j;
+  const int c = 32 * cq + lane;
+  // R_K loads first (independent of q); this CTA's quarter of the merge's
+  // R_V fragments into L2
+  float r[32];
+  {
+    const float* R = a.rot.R_K + (size_t)kvh * D * D + (size_t)(32 * w) * D + c;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) u[k] = __ldg(U + k * D);
-    const char* ut = (const char*)(a.rot.Ut_V + (size_t)kvh * D * D) + (size_t)t * 128;
-    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(ut));
+    for (int k = 0; k < 32; ++k) r[k] = __ldg(R + k * D);
+    const char* rv = (const char*)(a.rot.RV_frag + (size_t)kvh * RV_FRAG_WORDS) + (size_t)(cq * 128 + t) * 128;
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(rv));
   }
-  for (int e = t; e < G * D; e += 512)
-    xs[e / D][e % D] = __bfloat162float(a.q[((size_t)b * cv.Hq + kvh * G) * D + e]);
+  const __nv_bfloat16* qg = a.q + ((size_t)b * cv.Hq + kvh * G) * D;
+  for (int e = t; e < G * D; e += 128) xs[e / D][e % D] = __bfloat162float(qg[e]);
   __syncthreads();
-  float acc[MAX_G];
+  for (int n = w; n < G; n += 4) {
+    float sq = 0.f;
 #pragma unroll
-  for (int n = 0; n < MAX_G; ++n) acc[n] = 0.f;
-  if (a.rot.mode == OSCAR_ROT_OSCAR) {
-#pragma unroll
-    for (int k = 0; k < 32; ++k)
-#pragma unroll
-      for (int n = 0; n < MAX_G; ++n)
-        if (n < G) acc[n] = fmaf(xs[n][32 * pp + k], u[k], acc[n]);
-  } else if (pp == 0) {
-#pragma unroll
-    for (int n = 0; n < MAX_G; ++n)
-      if (n < G) acc[n] = xs[n][j];
-  }
-#pragma unroll
-  for (int n = 0; n < MAX_G; ++n) part[pp][n][j] = acc[n];
-  __syncthreads();
-  const int bar = 1 + pp, w4 = j >> 5, lane = j & 31;
-  const int i = 2 * ((j >> 4) & 3) + ((j >> 3) & 1);  // bit pair holding channel j in QK
-  const float f = (float)(1 << (8 - code_exp_rt(i)));
-  for (int n = pp; n < G; n += 4) {
-    float y = (part[0][n][j] + part[1][n][j]) + (part[2][n][j] + part[3][n][j]);
-    if (a.rot.mode != OSCAR_ROT_NONE) {
-      y = fwht128(y, j, tmp[pp], bar);
-      if (a.rot.mode == OSCAR_ROT_OSCAR) {
-        tmp[pp][j] = y;
-        group_sync(bar);
-        y = tmp[pp][bitrev7(j)];
-        group_sync(bar);
-      }
+    for (int k = 0; k < 4; ++k) {
+      const float v = xs[n][lane + 32 * k];
+      sq = fmaf(v, v, sq);
     }
-    const size_t row = (size_t)b * cv.Hq + kvh * G + n;
-    a.qrot[row * D + j] = y;
-    // power-of-two prescale so that |q'| * 16 stays below 2^14 in fp16
-    float am = fabsf(y);
 #pragma unroll
-    for (int o = 16; o; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-    if (lane == 0) red[pp][w4] = am;
-    group_sync(bar);
-    am = fmaxf(fmaxf(red[pp][0], red[pp][1]), fmaxf(red[pp][2], red[pp][3]));
-    group_sync(bar);
+    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if (lane == 0) nrm[n] = sqrtf(sq);
+  }
+#pragma unroll
+  for (int n = 0; n < MAX_G; ++n) {
+    if (n < G) {
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) acc = fmaf(xs[n][32 * w + k], r[k], acc);
+      part[w][n][lane] = acc;
+    }
+  }
+  __syncthreads();
+  const int i = 2 * ((c >> 4) & 3) + ((c >> 3) & 1);  // bit pair holding channel c in QK
+  const float f = (float)(1 << (8 - code_exp_rt(i)));
+  for (int n = w; n < G; n += 4) {
+    const float y = (part[0][n][lane] + part[1][n][lane]) + (part[2][n][lane] + part[3][n][lane]);
+    const size_t row = (size_t)b * cv.Hq + kvh * G + n;
+    a.qrot[row * D + c] = y;
+    // power-of-two prescale so that |q'| * 16 stays below 2^14 in fp16
+    const float am = nrm[n];
     int ex = 0;
     frexpf(am, &ex);
     const int sig = am > 0.f ? ex - 10 : 0;
     const __half hb = __float2half_rn(ldexpf(y, -sig) * f);
     uint8_t* rec = a.qpack + row * QPACK_BYTES;
-    ((__half*)rec)[j] = hb;
-    float bs = __half2float(hb), qs = y;
+    ((__half*)rec)[c] = hb;
+    float bs = __half2float(hb), ps = y;
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
       bs += __shfl_xor_sync(0xffffffffu, bs, o);
-      qs += __shfl_xor_sync(0xffffffffu, qs, o);
+      ps += __shfl_xor_sync(0xffffffffu, ps, o);
     }
     if (lane == 0) {
-      red[pp][w4] = bs;
-      red[pp][4 + w4] = qs;
+      ((float*)(rec + QPACK_QSUM))[cq] = bs;
+      ((float*)(rec + QPACK_PSUM))[cq] = ps;
+      if (cq == 0) *(float*)(rec + QPACK_ALPHA) = ldexpf(1.f, sig) * LOG2E * INV_SQRT_D * (1.f / 256.f);
     }
-    group_sync(bar);
-    if (j < cv.NG) {
-      const int wpg = 4 / cv.NG;
-      float bsum = 0.f, qsum = 0.f;
-      for (int w = j * wpg; w < (j + 1) * wpg; ++w) {
-        bsum += red[pp][w];
-        qsum += red[pp][4 + w];
-      }
-      const float alpha = ldexpf(1.f, sig) * LOG2E * INV_SQRT_D * (1.f / 256.f);
-      if (j == 0) *(float*)(rec + QPACK_ALPHA) = alpha;
-      ((float*)(rec + QPACK_BETA))[j] = -1024.f * bsum * alpha;
-      ((float*)(rec + QPACK_GAMMA))[j] = qsum * LOG2E * INV_SQRT_D;
-    }
-    group_sync(bar);
   }
 }
 
@@ -161,8 +149,8 @@ __host__ __device__ inline SmemLayout smem_layout(int head_bytes, int B, int imp
   int stage_total = NW * DEPTH * L.stage_bytes;
   // warp results and the merge's working set alias the stages
   const int wo_bytes = NW * MAX_G * D * 4 + 2 * NW * MAX_G * 4;
-  // merge: U_V^T (64 KB), the heads' history/window outputs, m and l per head
-  const int merge_bytes = D * D * 4 + MAX_G * D * 4 + 4 * MAX_G * 4;
+  // merge: R_V fragments (64 KB), the heads' history outputs, m and l per head
+  const int merge_bytes = MERGE_BYTES;
   if (stage_total < wo_bytes) stage_total = wo_bytes;
   if (stage_total < merge_bytes) stage_total = merge_bytes;
   stage_total = (stage_total + 127) & ~127;  // mbarriers that follow need 8-byte alignment
@@ -678,14 +666,16 @@ __device__ __forceinline__ void cta_combine_write(const DecodeArgs& a, const flo
 }
 
 // Final merge of one (request, kv head) by one CTA of 128 threads.  Thread 0
-// first starts a bulk copy of U_V^T (64 KB) into shared memory.  Meanwhile warp
-// w takes heads w, w + 4: it LSE-merges the history partials into (M, L, O')
-// and the window partials into (M_w, L_w, O_w) with all loads of a round in
-// flight (each lane holds channels 4*lane .. 4*lane+3 and the weights of
-// partials lane, lane+32, ...), and applies o'·P_br·H in registers.  Then the
-// CTA applies ·U_V^T from shared memory to every head at once, and each warp
-// writes its heads' LSE-merge of history and window.
-constexpr int MERGE_KQ = 4;  // partial weights held per lane: nb <= 32 * MERGE_KQ in registers
+// first starts a bulk copy of the R_V fragments (64 KB) into shared memory.
+// Meanwhile warp w takes heads w, w + 4: it LSE-merges the history partials
+// into (M, L, O') and the window partials into (M_w, L_w, O_w).  Each lane
+// holds channels 4*lane .. 4*lane+3; the first round of loads fetches m and l
+// of every partial, the window and the o of the first 32 history partials
+// together.  The normalised O'/L goes to shared memory as fp16 high and low
+// parts, and o = (O'/L)·R_V^T is three fp16 products per tile (hi·hi, hi·lo,
+// lo·hi) with fp32 accumulation, on tensor cores: warp w owns output
+// channels 32w .. 32w+31.  Then each warp writes its heads' LSE-merge of
+// history and window.
 
 __device__ __forceinline__ float4 fma4(float4 o, float w, float4 acc) {
   acc.x = fmaf(o.x, w, acc.x);
@@ -695,20 +685,30 @@ __device__ __forceinline__ float4 fma4(float4 o, float w, float4 acc) {
   return acc;
 }
 
-__device__ void merge_bkvh(const DecodeArgs& a, const Sched& sc, const int* pre, int b, int kvh,
+__device__ __forceinline__ uint32_t split_hi(float a, float b, uint32_t* lo) {
+  const __half ha = __float2half_rn(a), hb = __float2half_rn(b);
+  const __half la = __float2half_rn(a - __half2float(ha)), lb = __float2half_rn(b - __half2float(hb));
+  *lo = (uint32_t)__half_as_ushort(la) | ((uint32_t)__half_as_ushort(lb) << 16);
+  return (uint32_t)__half_as_ushort(ha) | ((uint32_t)__half_as_ushort(hb) << 16);
+}
+
+__device__ __noinline__ void merge_bkvh(const DecodeArgs& a, const Sched& sc, const int* pre, int b, int kvh,
                            float* sm, uint64_t* ubar, uint32_t uphase) {
   const CacheView& cv = a.cv;
   const int G = cv.G, t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  float* Us = sm;              // [128][128] U_V^T (OSCAR mode)
-  float* y = Us + D * D;       // [MAX_G][128] history part, then its un-rotation
-  float* hM = y + MAX_G * D;   // [MAX_G] history max and sum
+  const int gid = lane >> 2, tq = lane & 3;
+  const uint4* Rf = (const uint4*)sm;                       // R_V fragments
+  uint8_t* ybase = (uint8_t*)sm + MERGE_RV_BYTES;
+  uint32_t* yh = (uint32_t*)ybase;                          // [MAX_G][YST] fp16 high parts
+  uint32_t* yl = yh + MAX_G * YST / 2;                      // [MAX_G][YST] fp16 low parts
+  float* yo = (float*)ybase;                                // [MAX_G][128] history output (aliases yh, yl)
+  float* hM = (float*)(ybase + MERGE_Y_BYTES);              // [MAX_G] history max, sum
   float* hL = hM + MAX_G;
   const bool unrot = !a.bf16_history && a.rot.mode != OSCAR_ROT_NONE;
-  const bool dense = unrot && a.rot.mode == OSCAR_ROT_OSCAR;
-  if (dense && t == 0) {
+  if (unrot && t == 0) {
     fence_proxy_async();
-    mbar_expect_tx(ubar, D * D * 4);
-    bulk_g2s(Us, a.rot.Ut_V + (size_t)kvh * D * D, D * D * 4, ubar);
+    mbar_expect_tx(ubar, MERGE_RV_BYTES);
+    bulk_g2s(sm, a.rot.RV_frag + (size_t)kvh * RV_FRAG_WORDS, MERGE_RV_BYTES, ubar);
   }
   const int pages_b = (cv.hist_lens[b] + PAGE - 1) / PAGE;
   const int nb = (pages_b + sc.S - 1) / sc.S;
@@ -716,11 +716,13 @@ __device__ void merge_bkvh(const DecodeArgs& a, const Sched& sc, const int* pre,
   const int wslot = sc.n_hist + (b * cv.Hkv + kvh) * sc.wch;
   float4 Ow[2];   // window output of this warp's heads
   float mwv[2], lwv[2];
+  float4 Yv[2];   // this warp's heads' normalised history output (own channels)
+  float ysc[2];   // power-of-two scale applied to Yv before the fp16 split
   for (int hh = 0; hh * NW + warp < G; ++hh) {
     const int n = hh * NW + warp;
-    // ---- round 1: m and l of every partial (history: q = lane + 32k; window: lane < wch)
+    // ---- round 1: m, l of every partial (q = lane + 32k), the window, and
+    // the o of history partials 0..31
     float mq[MERGE_KQ], lq[MERGE_KQ];
-    float mloc = -INFINITY;
 #pragma unroll
     for (int k = 0; k < MERGE_KQ; ++k) {
       const int q = lane + 32 * k;
@@ -735,6 +737,17 @@ __device__ void merge_bkvh(const DecodeArgs& a, const Sched& sc, const int* pre,
     const float* wrec = a.part + ((size_t)(wslot + (lane < sc.wch ? lane : 0)) * G + n) * PART_STRIDE;
     const float mu = lane < sc.wch ? __ldcg(wrec) : -INFINITY;
     const float lu = lane < sc.wch ? __ldcg(wrec + 1) : 0.f;
+    float4 o5[5];
+#pragma unroll
+    for (int u = 0; u < 5; ++u)
+      o5[u] = u < sc.wch ? __ldcg((const float4*)(a.part + ((size_t)(wslot + u) * G + n) * PART_STRIDE + PART_O) + lane)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 o32[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u)
+      o32[u] = u < nb ? __ldcg((const float4*)(a.part + ((size_t)(base + u) * G + n) * PART_STRIDE + PART_O) + lane)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    float mloc = -INFINITY;
 #pragma unroll
     for (int k = 0; k < MERGE_KQ; ++k)
       if (lq[k] > 0.f) mloc = fmaxf(mloc, mq[k]);
@@ -767,20 +780,14 @@ __device__ void merge_bkvh(const DecodeArgs& a, const Sched& sc, const int* pre,
     float lw = lu * wu;
 #pragma unroll
     for (int o = 16; o; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
-    // ---- round 2+: o of the partials, 32 at a time (window with the first batch)
-    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
     float4 OW = make_float4(0.f, 0.f, 0.f, 0.f);
-    {
-      float4 o5[5];
 #pragma unroll
-      for (int u = 0; u < 5; ++u)
-        o5[u] = u < sc.wch ? __ldcg((const float4*)(a.part + ((size_t)(wslot + u) * G + n) * PART_STRIDE + PART_O) + lane)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < 5; ++u) OW = fma4(o5[u], __shfl_sync(0xffffffffu, wu, u), OW);
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int u = 0; u < 5; ++u) OW = fma4(o5[u], __shfl_sync(0xffffffffu, wu, u), OW);
-    }
-    for (int q0 = 0; q0 < nb; q0 += 32) {
-      float4 o32[32];
+    for (int u = 0; u < 32; ++u) O = fma4(o32[u], __shfl_sync(0xffffffffu, wk[0], u), O);
+    // ---- further rounds: o of partials 32.., 32 at a time
+    for (int q0 = 32; q0 < nb; q0 += 32) {
 #pragma unroll
       for (int u = 0; u < 32; ++u)
         o32[u] = (q0 + u < nb)
@@ -802,40 +809,18 @@ __device__ void merge_bkvh(const DecodeArgs& a, const Sched& sc, const int* pre,
 #pragma unroll
       for (int u = 0; u < 32; ++u) O = fma4(o32[u], __shfl_sync(0xffffffffu, wsel, u), O);
     }
-    // ---- o'·P_br·H in registers (channel c = 4*lane + k)
-    float v[4] = {O.x, O.y, O.z, O.w};
-    if (unrot) {
-      if (a.rot.mode == OSCAR_ROT_OSCAR) {
-        ((float4*)(y + n * D))[lane] = O;
-        __syncwarp();
+    // normalised history output, then a power-of-two scale that keeps its
+    // largest channel near 2^12 for the fp16 split
+    const float inv = lloc > 0.f ? 1.f / lloc : 0.f;
+    float4 Y = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+    float am = fmaxf(fmaxf(fabsf(Y.x), fabsf(Y.y)), fmaxf(fabsf(Y.z), fabsf(Y.w)));
 #pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = y[n * D + bitrev7(4 * lane + k)];
-        __syncwarp();
-      }
-#pragma unroll
-      for (int k = 0; k < 4; k += 2) {
-        const float p0 = v[k], p1 = v[k + 1];
-        v[k] = p0 + p1;
-        v[k + 1] = p0 - p1;
-      }
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const float p0 = v[k], p1 = v[k + 2];
-        v[k] = p0 + p1;
-        v[k + 2] = p0 - p1;
-      }
-#pragma unroll
-      for (int h = 1; h < 32; h <<= 1) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float o = __shfl_xor_sync(0xffffffffu, v[k], h);
-          v[k] = (lane & h) ? (o - v[k]) : (v[k] + o);
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] *= INV_SQRT_D;
-    }
-    ((float4*)(y + n * D))[lane] = make_float4(v[0], v[1], v[2], v[3]);
+    for (int o = 16; o; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    int ex = 0;
+    frexpf(am, &ex);
+    const float up = am > 0.f ? ldexpf(1.f, min(12 - ex, 100)) : 1.f;
+    Yv[hh] = Y;
+    ysc[hh] = up;
     if (lane == 0) {
       hM[n] = lloc > 0.f ? M : -INFINITY;
       hL[n] = lloc;
@@ -844,43 +829,76 @@ __device__ void merge_bkvh(const DecodeArgs& a, const Sched& sc, const int* pre,
     mwv[hh] = mw;
     lwv[hh] = lw;
   }
-  __syncthreads();
-  // ---- ·U_V^T from shared memory for all heads (thread t = output channel)
-  if (dense) {
-    if (!mbar_wait(ubar, uphase)) record_error(cv.err, OSCAR_ERR_TIMEOUT);
-    float acc[MAX_G];
-#pragma unroll
-    for (int n = 0; n < MAX_G; ++n) acc[n] = 0.f;
-#pragma unroll 8
-    for (int i = 0; i < D; ++i) {
-      const float u = Us[i * D + t];
-#pragma unroll
-      for (int n = 0; n < MAX_G; ++n)
-        if (n < G) acc[n] = fmaf(y[n * D + i], u, acc[n]);
+  if (unrot) {
+    // heads of this warp into the fp16 B operand; rows of absent heads are 0
+    for (int n = warp; n < MAX_G; n += NW) {
+      const int hh = n / NW;
+      uint32_t h0 = 0u, h1 = 0u, l0 = 0u, l1 = 0u;
+      if (n < G) {
+        const float4 Y = hh == 0 ? Yv[0] : Yv[1];
+        const float up = hh == 0 ? ysc[0] : ysc[1];
+        h0 = split_hi(Y.x * up, Y.y * up, &l0);
+        h1 = split_hi(Y.z * up, Y.w * up, &l1);
+      }
+      *(uint2*)(yh + n * (YST / 2) + 2 * lane) = make_uint2(h0, h1);
+      *(uint2*)(yl + n * (YST / 2) + 2 * lane) = make_uint2(l0, l1);
     }
     __syncthreads();
+    if (!mbar_wait(ubar, uphase)) record_error(cv.err, OSCAR_ERR_TIMEOUT);
+    float d[2][4];
 #pragma unroll
-    for (int n = 0; n < MAX_G; ++n)
-      if (n < G) y[n * D + t] = acc[n];
-    __syncthreads();
+    for (int mi = 0; mi < 2; ++mi) d[mi][0] = d[mi][1] = d[mi][2] = d[mi][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t bh0 = yh[gid * (YST / 2) + 8 * ks + tq], bh1 = yh[gid * (YST / 2) + 8 * ks + 4 + tq];
+      const uint32_t bl0 = yl[gid * (YST / 2) + 8 * ks + tq], bl1 = yl[gid * (YST / 2) + 8 * ks + 4 + tq];
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi) {
+        const int mt = 2 * warp + mi;
+        const uint4 ah = Rf[rv_frag_index(0, mt, ks, lane) / 4];
+        const uint4 al = Rf[rv_frag_index(1, mt, ks, lane) / 4];
+        mma_f16(d[mi], ah.x, ah.y, ah.z, ah.w, bh0, bh1);
+        mma_f16(d[mi], ah.x, ah.y, ah.z, ah.w, bl0, bl1);
+        mma_f16(d[mi], al.x, al.y, al.z, al.w, bh0, bh1);
+      }
+    }
+    __syncthreads();  // B operands consumed: yo may overwrite them
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi) {
+      const int c = 32 * warp + 16 * mi + gid;
+      yo[(2 * tq) * D + c] = d[mi][0];
+      yo[(2 * tq + 1) * D + c] = d[mi][1];
+      yo[(2 * tq) * D + c + 8] = d[mi][2];
+      yo[(2 * tq + 1) * D + c + 8] = d[mi][3];
+    }
+  } else {
+    for (int hh = 0; hh * NW + warp < G; ++hh) {
+      const int n = hh * NW + warp;
+      const float up = ysc[hh];
+      ((float4*)(yo + n * D))[lane] = make_float4(Yv[hh].x * up, Yv[hh].y * up, Yv[hh].z * up, Yv[hh].w * up);
+    }
   }
+  __syncthreads();
   // ---- per warp: LSE-merge of history and window for its heads
   for (int hh = 0; hh * NW + warp < G; ++hh) {
     const int n = hh * NW + warp;
     const float M = hM[n], Ls = hL[n], mw = mwv[hh], lw = lwv[hh];
-    const float4 Oh = ((const float4*)(y + n * D))[lane];
+    const float down = 1.f / ysc[hh];
+    float4 Oh = ((const float4*)(yo + n * D))[lane];
     const float M2 = fmaxf(Ls > 0.f ? M : -INFINITY, lw > 0.f ? mw : -INFINITY);
     float o[4] = {0.f, 0.f, 0.f, 0.f};
     float lse = -INFINITY;
     if (M2 != -INFINITY) {
       const float fh = Ls > 0.f ? ex2(M - M2) : 0.f;
       const float fw = lw > 0.f ? ex2(mw - M2) : 0.f;
-      const float inv = 1.f / (Ls * fh + lw * fw);
-      o[0] = (Oh.x * fh + Ow[hh].x * fw) * inv;
-      o[1] = (Oh.y * fh + Ow[hh].y * fw) * inv;
-      o[2] = (Oh.z * fh + Ow[hh].z * fw) * inv;
-      o[3] = (Oh.w * fh + Ow[hh].w * fw) * inv;
-      lse = (M2 + log2f(Ls * fh + lw * fw)) * LN2;
+      const float den = Ls * fh + lw * fw;
+      const float inv = 1.f / den;
+      const float hw = Ls * fh * down;  // history output is normalised and scaled by ysc
+      o[0] = fmaf(Oh.x, hw, Ow[hh].x * fw) * inv;
+      o[1] = fmaf(Oh.y, hw, Ow[hh].y * fw) * inv;
+      o[2] = fmaf(Oh.z, hw, Ow[hh].z * fw) * inv;
+      o[3] = fmaf(Oh.w, hw, Ow[hh].w * fw) * inv;
+      lse = (M2 + log2f(den)) * LN2;
     }
     const size_t row = (size_t)b * cv.Hq + kvh * G + n;
     __nv_bfloat162 o01 = __floats2bfloat162_rn(o[0], o[1]);
@@ -1104,13 +1122,20 @@ __global__ void __launch_bounds__(NW * 32, IMPL == 0 ? 3 : 2) decode_kernel(Deco
             const uint8_t* r = a.qpack + ((size_t)b * cv.Hq + kvh * G + (hv ? n : 0)) * QPACK_BYTES;
             S.m[hc] = -INFINITY;
             S.l[hc] = 0.f;
-            S.ka[hc] = hv ? __ldcg((const float*)(r + QPACK_ALPHA)) : 0.f;
+            const float al = hv ? __ldcg((const float*)(r + QPACK_ALPHA)) : 0.f;
+            S.ka[hc] = al;
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
+              float qs = 0.f, ps = 0.f;
+#pragma unroll
+              for (int k = gr * (4 / NG); k < (gr + 1) * (4 / NG); ++k) {
+                qs += hv ? __ldcg((const float*)(r + QPACK_QSUM) + k) : 0.f;
+                ps += hv ? __ldcg((const float*)(r + QPACK_PSUM) + k) : 0.f;
+              }
               S.bs[hc][gr] = 0.f;
               S.zs[hc][gr] = 0.f;
-              S.kb[hc][gr] = hv ? __ldcg((const float*)(r + QPACK_BETA) + gr) : 0.f;
-              S.kg[hc][gr] = hv ? __ldcg((const float*)(r + QPACK_GAMMA) + gr) : 0.f;
+              S.kb[hc][gr] = -1024.f * qs * al;
+              S.kg[hc][gr] = ps * LOG2E * INV_SQRT_D;
             }
           }
         }
@@ -1192,8 +1217,11 @@ __global__ void __launch_bounds__(NW * 32, IMPL == 0 ? 3 : 2) decode_kernel(Deco
         }
         for (int e = threadIdx.x; e < G * 4; e += NW * 32) {
           const int n = e / 4, gr = e % 4;
-          kgm[e] = __ldcg((const float*)(a.qpack + ((size_t)b * cv.Hq + kvh * G + n) * QPACK_BYTES +
-                                         QPACK_GAMMA) + gr);
+          const float* ps = (const float*)(a.qpack + ((size_t)b * cv.Hq + kvh * G + n) * QPACK_BYTES + QPACK_PSUM);
+          float sum = 0.f;
+          if (gr < NG)
+            for (int k = gr * (4 / NG); k < (gr + 1) * (4 / NG); ++k) sum += __ldcg(ps + k);
+          kgm[e] = sum * LOG2E * INV_SQRT_D;
         }
         __syncthreads();
         CoreState S;
@@ -1268,8 +1296,8 @@ __global__ void __launch_bounds__(NW * 32, IMPL == 0 ? 3 : 2) decode_kernel(Deco
     if (misc[2]) {
       merge_bkvh(a, sc, pre, b, kvh, wm, &mbar[NW * DEPTH], (uint32_t)misc[3] & 1u);
       __syncthreads();
-      // the merge's U_V^T copy completed one phase of its barrier
-      if (threadIdx.x == 0 && !BF16H && a.rot.mode == OSCAR_ROT_OSCAR) misc[3] += 1;
+      // the merge's R_V copy completed one phase of its barrier
+      if (threadIdx.x == 0 && !BF16H && a.rot.mode != OSCAR_ROT_NONE) misc[3] += 1;
     }
     if (misc[1]) break;
     __syncthreads();
@@ -1352,7 +1380,7 @@ int decode_ctas_per_sm(const DecodeArgs& a) {
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof) {
   const CacheView& cv = a.cv;
   prof_begin(prof, OSCAR_KERNEL_DECODE_PREP, st);
-  prep_kernel<<<a.B * cv.Hkv, 512, 0, st>>>(a);
+  prep_kernel<<<dim3(a.B * cv.Hkv, 4), 128, 0, st>>>(a);
   prof_end(prof, OSCAR_KERNEL_DECODE_PREP, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -34,12 +34,29 @@ __host__ __device__ constexpr int off_k_sz() { return 4096; }
 __host__ __device__ constexpr int off_v_sz(int g) { return 4096 + PAGE * (D / g) * 4; }
 
 // Per-layer rotation tables on the device (owned by the context).
+// R_V in mma.m16n8k16 A-fragment order, for o = o'·R_V^T on tensor cores
+// (A = R_V, rows = output channels, columns = input channels): per kv head,
+// part (0: fp16 of R_V, 1: fp16 of the remainder R_V - part 0), m-tile mt,
+// k-step ks and lane (gid, tq), the four words a0..a3 hold
+// R_V[16mt+gid(+8)][16ks+2tq(+8) +0/+1], lower column in the low half.
+constexpr int RV_FRAG_WORDS = 2 * 8 * 8 * 32 * 4;  // per kv head: 64 KB
+
+__host__ __device__ __forceinline__ int rv_frag_index(int part, int mt, int ks, int lane) {
+  return (((part * 8 + mt) * 8 + ks) * 32 + lane) * 4;
+}
+
+// Per-layer rotation table.  U_K, U_V: the eigenbases (identity outside
+// OSCAR mode) for the demotion path, which applies U, then H, then P_br.
+// R_K = rotation(U_K, mode) composed in fp64 on the host, for the query;
+// RV_frag: R_V = rotation(U_V, mode) as fp16 high/low fragments, for the
+// output.
 struct LayerRot {
-  const float* U_K;   // [Hkv][128][128]  x' = x·U·H·P
-  const float* U_V;   // [Hkv][128][128]
-  const float* Ut_V;  // [Hkv][128][128]  transpose of U_V, for o = o'·P·H·U_V^T
-  const float* clip_k;  // [Hkv]
-  const float* clip_v;  // [Hkv]
+  const float* U_K;         // [Hkv][128][128]  x' = x·U·H·P
+  const float* U_V;         // [Hkv][128][128]
+  const float* R_K;         // [Hkv][128][128]  q' = q·R_K
+  const uint32_t* RV_frag;  // [Hkv][RV_FRAG_WORDS]
+  const float* clip_k;      // [Hkv]
+  const float* clip_v;      // [Hkv]
   int mode;
 };
 
@@ -136,32 +153,6 @@ __device__ __forceinline__ float rotate128(const float* x_s, const float* U, int
     group_sync(bar);
   }
   return t;
-}
-
-// o = o'·R^T: o'·P_br, then ·H, then ·U^T (Ut = U^T, row-major).
-__device__ __forceinline__ float unrotate128(float v, const float* Ut, int mode, int j,
-                                             float* tmp, float* tmp2, int bar) {
-  if (mode == OSCAR_ROT_NONE) return v;
-  if (mode == OSCAR_ROT_OSCAR) {
-    tmp[j] = v;
-    group_sync(bar);
-    v = tmp[bitrev7(j)];
-    group_sync(bar);
-  }
-  v = fwht128(v, j, tmp, bar);
-  if (mode != OSCAR_ROT_OSCAR) return v;
-  tmp2[j] = v;
-  group_sync(bar);
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 4
-  for (int i = 0; i < D; i += 4) {
-    a0 = fmaf(tmp2[i + 0], __ldg(Ut + (i + 0) * D + j), a0);
-    a1 = fmaf(tmp2[i + 1], __ldg(Ut + (i + 1) * D + j), a1);
-    a2 = fmaf(tmp2[i + 2], __ldg(Ut + (i + 2) * D + j), a2);
-    a3 = fmaf(tmp2[i + 3], __ldg(Ut + (i + 3) * D + j), a3);
-  }
-  group_sync(bar);
-  return (a0 + a1) + (a2 + a3);
 }
 
 // --------------------------------------------------------------- quantiser
