@@ -92,6 +92,15 @@ size_t scratch_for(const oscar_ctx* ctx, int B, int target) {
   return decode_scratch_bytes(B, ctx->cfg.num_q_heads, ctx->cfg.num_kv_heads, ctx->G, target);
 }
 
+// Decode kernel variant: 1 CUDA-core INT2; 3 tensor cores, pages in pairs as
+// two softmax streams per tile (needs G <= 4); 0 tensor cores, one page at a
+// time.
+int kernel_impl(const oscar_ctx* ctx) {
+  if (ctx->impl == OSCAR_DECODE_CUDA_CORE) return 1;
+  if (ctx->impl == OSCAR_DECODE_TENSOR_SINGLE || ctx->G > 4) return 0;
+  return 3;
+}
+
 // Persistent decode CTAs per SM: the option, capped by what the kernel variant
 // for this call can keep resident.
 int decode_ctas(const oscar_ctx* ctx, int batch, bool bf16_history) {
@@ -99,7 +108,7 @@ int decode_ctas(const oscar_ctx* ctx, int batch, bool bf16_history) {
   a.cv.head_bytes = bf16_history ? BF16_HEAD_BYTES : int2_head_bytes(ctx->cfg.group_size);
   a.cv.NG = ctx->NG;
   a.B = batch;
-  a.impl = ctx->impl;
+  a.impl = kernel_impl(ctx);
   a.bf16_history = bf16_history ? 1 : 0;
   int occ = decode_ctas_per_sm(a);
   if (occ < 1) occ = 1;
@@ -269,7 +278,7 @@ oscar_status decode_common(oscar_ctx* ctx, int layer, const oscar_cache* cache, 
   a.part = (float*)(sp + sl.off_part);
   a.B = batch;
   a.target_items = target;
-  a.impl = ctx->impl;
+  a.impl = kernel_impl(ctx);
   a.bf16_history = bf16_history ? 1 : 0;
   a.rot = layer_rot(ctx, layer);
   const int grid = ctx->num_sms * decode_ctas(ctx, batch, bf16_history);
@@ -403,7 +412,8 @@ oscar_status oscar_set_option(oscar_ctx* ctx, int option, int value) {
   if (!ctx) return OSCAR_ERR_INVALID_ARG;
   switch (option) {
     case OSCAR_OPT_DECODE_IMPL:
-      if (value != 0 && value != 1) return OSCAR_ERR_INVALID_ARG;
+      if (value != OSCAR_DECODE_TENSOR && value != OSCAR_DECODE_CUDA_CORE && value != OSCAR_DECODE_TENSOR_SINGLE)
+        return OSCAR_ERR_INVALID_ARG;
       ctx->impl = value;
       return OSCAR_OK;
     case OSCAR_OPT_CTAS_PER_SM:

@@ -29,12 +29,10 @@ namespace {
 constexpr int NW = 4;     // warps per decode CTA
 constexpr int DEPTH = 4;  // bulk-copy stages per warp
 
-// final merge (merge_bkvh)
-constexpr int MERGE_KQ = 4;   // partial weights held per lane: nb <= 32 * MERGE_KQ in registers
+// final merge (merge_kernel)
 constexpr int YST = 136;      // fp16 row stride of the mma B operand (conflict-free fragment loads)
 constexpr int MERGE_RV_BYTES = RV_FRAG_WORDS * 4;
 constexpr int MERGE_Y_BYTES = 2 * MAX_G * YST * 2 > MAX_G * D * 4 ? 2 * MAX_G * YST * 2 : MAX_G * D * 4;
-constexpr int MERGE_BYTES = MERGE_RV_BYTES + MERGE_Y_BYTES + 2 * MAX_G * 4;
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
@@ -64,10 +62,7 @@ __global__ void __launch_bounds__(128) prep_kernel(DecodeArgs a) {
   const CacheView& cv = a.cv;
   const int bk = blockIdx.x, cq = blockIdx.y;
   const int b = bk / cv.Hkv, kvh = bk % cv.Hkv, t = threadIdx.x, w = t >> 5, lane = t & 31;
-  if (t == 0 && cq == 0) {
-    a.done[bk] = 0;
-    if (bk == 0) *a.counter = 0;
-  }
+  if (t == 0 && cq == 0 && bk == 0) *a.counter = 0;
   if (a.bf16_history) return;
   const int G = cv.G;
   const int c = 32 * cq + lane;
@@ -147,16 +142,13 @@ __host__ __device__ inline SmemLayout smem_layout(int head_bytes, int B, int imp
   int o = 0;
   L.off_stage = o;
   int stage_total = NW * DEPTH * L.stage_bytes;
-  // warp results and the merge's working set alias the stages
+  // the warp results alias the stages
   const int wo_bytes = NW * MAX_G * D * 4 + 2 * NW * MAX_G * 4;
-  // merge: R_V fragments (64 KB), the heads' history outputs, m and l per head
-  const int merge_bytes = MERGE_BYTES;
   if (stage_total < wo_bytes) stage_total = wo_bytes;
-  if (stage_total < merge_bytes) stage_total = merge_bytes;
   stage_total = (stage_total + 127) & ~127;  // mbarriers that follow need 8-byte alignment
   o += stage_total;
   L.off_mbar = o;
-  o += NW * DEPTH * 8 + 16;  // pipeline stages + the merge's U_V^T copy
+  o += NW * DEPTH * 8;  // pipeline stages
   L.off_qf = o;
   if (impl == 1) o += MAX_G * D * 4 + MAX_G * 4 * 4;  // fp32 q' in K storage order + z weights
   L.off_vs = o;
@@ -356,6 +348,210 @@ __device__ __forceinline__ void flush_v_offset(Int2State<NG>& S) {
         S.oacc[gr * MPG + jj][hc] -= off;
         S.oacc[gr * MPG + jj][hc + 2] -= off;
       }
+    }
+  }
+}
+
+// ------------------------------------- two INT2 pages as two streams (G <= 4)
+// With at most 4 query heads per kv head, half of the m16n8 tile's columns
+// would carry padding.  Instead a warp takes its pages two at a time: page A's
+// logits fill columns 0..3 and page B's columns 4..7 of the same QK^T tile,
+// each column keeps its own online-softmax state, and the SV^T products read
+// the shared P tile with the other page's columns masked to zero.  Column n
+// of the B operands lives in the lanes with gid == n, so the masks are
+// per-lane constants: mA = all ones where gid < 4.  At the end of an item the
+// two streams of a head (columns n and n + 4, lanes tq and tq ^ 2) are merged.
+template <int NG>
+__device__ __forceinline__ void qk_page_masked(float (&acc)[4][NG][4], const uint8_t* kc,
+                                               const uint32_t (&bq)[8][2], uint32_t mask, int gid,
+                                               int tq) {
+  constexpr int KPG = 8 / NG;
+  uint2 wa[4], wb[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    wa[s] = *(const uint2*)(kc + (16 * s + gid) * 32 + 8 * tq);
+    wb[s] = *(const uint2*)(kc + (16 * s + gid + 8) * 32 + 8 * tq);
+  }
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t b0 = bq[kk][0] & mask, b1 = bq[kk][1] & mask;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const uint32_t xa = kk < 4 ? wa[s].x : wa[s].y;
+      const uint32_t xb = kk < 4 ? wb[s].x : wb[s].y;
+      uint32_t a0, a1, a2, a3;
+      switch (kk & 3) {
+        case 0: a0 = code_pair<0>(xa); a1 = code_pair<0>(xb); a2 = code_pair<1>(xa); a3 = code_pair<1>(xb); break;
+        case 1: a0 = code_pair<2>(xa); a1 = code_pair<2>(xb); a2 = code_pair<3>(xa); a3 = code_pair<3>(xb); break;
+        case 2: a0 = code_pair<4>(xa); a1 = code_pair<4>(xb); a2 = code_pair<5>(xa); a3 = code_pair<5>(xb); break;
+        default: a0 = code_pair<6>(xa); a1 = code_pair<6>(xb); a2 = code_pair<7>(xa); a3 = code_pair<7>(xb); break;
+      }
+      mma_f16(acc[s][kk / KPG], a0, a1, a2, a3, b0, b1);
+    }
+  }
+}
+
+template <int NG, bool FULL>
+__device__ __forceinline__ void int2_pair_mma(Int2State<NG>& S, const uint8_t* stA, int nvA,
+                                              const uint8_t* stB, int nvB, bool hasB, int lane,
+                                              uint32_t mA) {
+  const int gid = lane >> 2, tq = lane & 3;
+  constexpr int MPG = 8 / NG;
+  float acc[4][NG][4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s)
+#pragma unroll
+    for (int gr = 0; gr < NG; ++gr) acc[s][gr][0] = acc[s][gr][1] = acc[s][gr][2] = acc[s][gr][3] = 0.f;
+  qk_page_masked<NG>(acc, stA, S.bq, mA, gid, tq);
+  if (hasB) qk_page_masked<NG>(acc, stB, S.bq, ~mA, gid, tq);
+  // this lane's columns 2tq, 2tq + 1 belong to page A when tq < 2
+  const bool own_a = tq < 2;
+  const uint8_t* st = own_a ? stA : stB;
+  const int nv = own_a ? nvA : nvB;
+  const __half2* ksz = (const __half2*)(st + 4096);
+  const __half2* vsz = (const __half2*)(st + 4096 + PAGE * NG * 4);
+  float lam[4][4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int ta = 16 * s + gid, tb = ta + 8;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int row = e < 2 ? ta : tb;
+      const int hc = e & 1;
+      float v = 0.f;
+#pragma unroll
+      for (int gr = 0; gr < NG; ++gr) {
+        const float2 sz = __half22float2(ksz[row * NG + gr]);
+        v = fmaf(sz.x, fmaf(acc[s][gr][e], S.ka[hc], S.kb[hc][gr]), fmaf(sz.y, S.kg[hc][gr], v));
+      }
+      lam[s][e] = (FULL || row < nv) ? v : -INFINITY;
+    }
+  }
+  float pm[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int s = 0; s < 4; ++s)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pm[e & 1] = fmaxf(pm[e & 1], lam[s][e]);
+#pragma unroll
+  for (int hc = 0; hc < 2; ++hc) {
+    pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 4));
+    pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 8));
+    pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 16));
+  }
+  {
+    const float mn0 = fmaxf(S.m[0], pm[0]), mn1 = fmaxf(S.m[1], pm[1]);
+    const bool moved = (mn0 > S.m[0]) || (mn1 > S.m[1]);
+    if (__any_sync(0xffffffffu, moved)) {
+      const float al0 = ex2(S.m[0] - mn0), al1 = ex2(S.m[1] - mn1);
+      S.m[0] = mn0;
+      S.m[1] = mn1;
+      S.l[0] *= al0;
+      S.l[1] *= al1;
+#pragma unroll
+      for (int gr = 0; gr < NG; ++gr) {
+        S.bs[0][gr] *= al0;
+        S.zs[0][gr] *= al0;
+        S.bs[1][gr] *= al1;
+        S.zs[1][gr] *= al1;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        S.oacc[j][0] *= al0;
+        S.oacc[j][2] *= al0;
+        S.oacc[j][1] *= al1;
+        S.oacc[j][3] *= al1;
+      }
+    }
+  }
+  const uint8_t* vcA = stA + 2048;
+  const uint8_t* vcB = stB + 2048;
+  uint32_t va_w[8][2], vb_w[8][2];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    va_w[j][0] = *(const uint32_t*)(vcA + (16 * j + gid) * 16 + 4 * tq);
+    va_w[j][1] = *(const uint32_t*)(vcA + (16 * j + 8 + gid) * 16 + 4 * tq);
+    vb_w[j][0] = *(const uint32_t*)(vcB + (16 * j + gid) * 16 + 4 * tq);
+    vb_w[j][1] = *(const uint32_t*)(vcB + (16 * j + 8 + gid) * 16 + 4 * tq);
+  }
+  const uint32_t mB = ~mA;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int ta = 16 * s + gid, tb = ta + 8;
+    const bool va = FULL || ta < nv, vb = FULL || tb < nv;
+    float p[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      p[e] = ex2(lam[s][e] - S.m[e & 1]);
+      S.l[e & 1] += p[e];
+    }
+    const float fa = (float)(1 << (8 - code_exp_rt(2 * s)));
+    const float fb = (float)(1 << (8 - code_exp_rt(2 * s + 1)));
+#pragma unroll
+    for (int gr = 0; gr < NG; ++gr) {
+      const float2 sa = __half22float2(vsz[ta * NG + gr]);
+      const float2 sb = __half22float2(vsz[tb * NG + gr]);
+      const float s_a = va ? sa.x * fa : 0.f, z_a = va ? sa.y : 0.f;
+      const float s_b = vb ? sb.x * fb : 0.f, z_b = vb ? sb.y : 0.f;
+      const __half2 h0 = __floats2half2_rn(p[0] * s_a, p[1] * s_a);
+      const __half2 h1 = __floats2half2_rn(p[2] * s_b, p[3] * s_b);
+      const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+      S.bs[0][gr] += f0.x + f1.x;
+      S.bs[1][gr] += f0.y + f1.y;
+      S.zs[0][gr] = fmaf(p[0], z_a, fmaf(p[2], z_b, S.zs[0][gr]));
+      S.zs[1][gr] = fmaf(p[1], z_a, fmaf(p[3], z_b, S.zs[1][gr]));
+      const uint32_t b0 = movmatrix_t(*(const uint32_t*)&h0);
+      const uint32_t b1 = movmatrix_t(*(const uint32_t*)&h1);
+      const uint32_t b0a = b0 & mA, b1a = b1 & mA, b0b = b0 & mB, b1b = b1 & mB;
+#pragma unroll
+      for (int jj = 0; jj < MPG; ++jj) {
+        const int j = gr * MPG + jj;
+        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+        switch (s) {
+          case 0:
+            a0 = code_pair<0>(va_w[j][0]); a1 = code_pair<0>(va_w[j][1]); a2 = code_pair<1>(va_w[j][0]); a3 = code_pair<1>(va_w[j][1]);
+            c0 = code_pair<0>(vb_w[j][0]); c1 = code_pair<0>(vb_w[j][1]); c2 = code_pair<1>(vb_w[j][0]); c3 = code_pair<1>(vb_w[j][1]);
+            break;
+          case 1:
+            a0 = code_pair<2>(va_w[j][0]); a1 = code_pair<2>(va_w[j][1]); a2 = code_pair<3>(va_w[j][0]); a3 = code_pair<3>(va_w[j][1]);
+            c0 = code_pair<2>(vb_w[j][0]); c1 = code_pair<2>(vb_w[j][1]); c2 = code_pair<3>(vb_w[j][0]); c3 = code_pair<3>(vb_w[j][1]);
+            break;
+          case 2:
+            a0 = code_pair<4>(va_w[j][0]); a1 = code_pair<4>(va_w[j][1]); a2 = code_pair<5>(va_w[j][0]); a3 = code_pair<5>(va_w[j][1]);
+            c0 = code_pair<4>(vb_w[j][0]); c1 = code_pair<4>(vb_w[j][1]); c2 = code_pair<5>(vb_w[j][0]); c3 = code_pair<5>(vb_w[j][1]);
+            break;
+          default:
+            a0 = code_pair<6>(va_w[j][0]); a1 = code_pair<6>(va_w[j][1]); a2 = code_pair<7>(va_w[j][0]); a3 = code_pair<7>(va_w[j][1]);
+            c0 = code_pair<6>(vb_w[j][0]); c1 = code_pair<6>(vb_w[j][1]); c2 = code_pair<7>(vb_w[j][0]); c3 = code_pair<7>(vb_w[j][1]);
+            break;
+        }
+        mma_f16(S.oacc[j], a0, a1, a2, a3, b0a, b1a);
+        if (hasB) mma_f16(S.oacc[j], c0, c1, c2, c3, b0b, b1b);
+      }
+    }
+  }
+}
+
+// Merge the two streams of each head (columns n and n + 4 live in lanes tq and
+// tq ^ 2) into the lanes with tq < 2, after l, bs and zs were summed over the
+// gid lanes.  Stream states start at m = -1e30, so an empty stream has weight 0.
+template <int NG>
+__device__ __forceinline__ void merge_pair_streams(Int2State<NG>& S) {
+#pragma unroll
+  for (int hc = 0; hc < 2; ++hc) {
+    const float mo = __shfl_xor_sync(0xffffffffu, S.m[hc], 2);
+    const float M = fmaxf(S.m[hc], mo);
+    const float fa = ex2(S.m[hc] - M), fb = ex2(mo - M);
+    S.m[hc] = M;
+    S.l[hc] = S.l[hc] * fa + __shfl_xor_sync(0xffffffffu, S.l[hc], 2) * fb;
+#pragma unroll
+    for (int gr = 0; gr < NG; ++gr) {
+      S.bs[hc][gr] = S.bs[hc][gr] * fa + __shfl_xor_sync(0xffffffffu, S.bs[hc][gr], 2) * fb;
+      S.zs[hc][gr] = S.zs[hc][gr] * fa + __shfl_xor_sync(0xffffffffu, S.zs[hc][gr], 2) * fb;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      S.oacc[j][hc] = S.oacc[j][hc] * fa + __shfl_xor_sync(0xffffffffu, S.oacc[j][hc], 2) * fb;
+      S.oacc[j][hc + 2] = S.oacc[j][hc + 2] * fa + __shfl_xor_sync(0xffffffffu, S.oacc[j][hc + 2], 2) * fb;
     }
   }
 }
@@ -662,20 +858,7 @@ __device__ __forceinline__ void cta_combine_write(const DecodeArgs& a, const flo
     }
     rec[PART_O + c] = O;
   }
-  fence_acq_rel_gpu();  // this thread's part of the record is visible before the item is counted
 }
-
-// Final merge of one (request, kv head) by one CTA of 128 threads.  Thread 0
-// first starts a bulk copy of the R_V fragments (64 KB) into shared memory.
-// Meanwhile warp w takes heads w, w + 4: it LSE-merges the history partials
-// into (M, L, O') and the window partials into (M_w, L_w, O_w).  Each lane
-// holds channels 4*lane .. 4*lane+3; the first round of loads fetches m and l
-// of every partial, the window and the o of the first 32 history partials
-// together.  The normalised O'/L goes to shared memory as fp16 high and low
-// parts, and o = (O'/L)·R_V^T is three fp16 products per tile (hi·hi, hi·lo,
-// lo·hi) with fp32 accumulation, on tensor cores: warp w owns output
-// channels 32w .. 32w+31.  Then each warp writes its heads' LSE-merge of
-// history and window.
 
 __device__ __forceinline__ float4 fma4(float4 o, float w, float4 acc) {
   acc.x = fmaf(o.x, w, acc.x);
@@ -685,6 +868,10 @@ __device__ __forceinline__ float4 fma4(float4 o, float w, float4 acc) {
   return acc;
 }
 
+__device__ __forceinline__ float4 scale4(float4 o, float w) {
+  return make_float4(o.x * w, o.y * w, o.z * w, o.w * w);
+}
+
 __device__ __forceinline__ uint32_t split_hi(float a, float b, uint32_t* lo) {
   const __half ha = __float2half_rn(a), hb = __float2half_rn(b);
   const __half la = __float2half_rn(a - __half2float(ha)), lb = __float2half_rn(b - __half2float(hb));
@@ -692,199 +879,236 @@ __device__ __forceinline__ uint32_t split_hi(float a, float b, uint32_t* lo) {
   return (uint32_t)__half_as_ushort(ha) | ((uint32_t)__half_as_ushort(hb) << 16);
 }
 
-__device__ __noinline__ void merge_bkvh(const DecodeArgs& a, const Sched& sc, const int* pre, int b, int kvh,
-                           float* sm, uint64_t* ubar, uint32_t uphase) {
+// ------------------------------------------------------------------ merge
+// grid = B * Hkv, block = MW * 32, launched as a programmatic dependent of
+// decode_kernel.  CTA (b, kvh) merges the partial records of request b, kv
+// head kvh [Blog, pipeline paragraph: the INT2 and BF16 parts are combined by
+// online softmax]:
+//   * before waiting for the decode kernel it derives the work list (the same
+//     one the decode kernel used) and starts a bulk copy of the R_V fragments
+//     (64 KB) into shared memory;
+//   * the MW / G warps of head n's team each LSE-merge every (MW / G)-th
+//     history partial with all of their loads in one round (each lane holds
+//     channels 4*lane .. 4*lane+3); the first warp of a team also merges the
+//     window partials;
+//   * warp n combines its team into (M, L, O'), normalises O'/L and writes it
+//     as fp16 high and low parts; o = (O'/L)·R_V^T is three fp16 products per
+//     tile (hi·hi, hi·lo, lo·hi) with fp32 accumulation, warp w owning output
+//     channels 16w .. 16w+15;
+//   * warp n writes head n's LSE-merge of history and window.
+constexpr int MW = 8;        // warps of the merge kernel
+constexpr int MERGE_MQ = 16;  // history partials per warp and round
+
+struct MergeLayout {
+  int off_rv, off_y, off_tm, off_to, off_win, off_wo, off_h, off_mbar, off_red, off_pre, total;
+};
+
+__host__ __device__ inline MergeLayout merge_layout(int B) {
+  MergeLayout L;
+  int o = 0;
+  L.off_rv = o;
+  o += MERGE_RV_BYTES;
+  L.off_y = o;
+  o += MERGE_Y_BYTES;
+  L.off_tm = o;               // team m, l: [2][MW]
+  o += 2 * MW * 4;
+  L.off_to = o;               // team o: [MW][128]
+  o += MW * D * 4;
+  L.off_win = o;              // window m, l: [2][MAX_G]
+  o += 2 * MAX_G * 4;
+  L.off_wo = o;               // window o: [MAX_G][128]
+  o += MAX_G * D * 4;
+  L.off_h = o;                // history M, L, fp16 scale: [3][MAX_G]
+  o += 3 * MAX_G * 4 + 8;
+  L.off_mbar = (o + 7) & ~7;
+  o = L.off_mbar + 16;
+  L.off_red = o;
+  o += 64 * 4;
+  L.off_pre = o;
+  o += ((B + 1) * 4 + 15) & ~15;
+  L.total = o;
+  return L;
+}
+
+__global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
   const CacheView& cv = a.cv;
-  const int G = cv.G, t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int G = cv.G, Hkv = cv.Hkv, t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int gid = lane >> 2, tq = lane & 3;
-  const uint4* Rf = (const uint4*)sm;                       // R_V fragments
-  uint8_t* ybase = (uint8_t*)sm + MERGE_RV_BYTES;
-  uint32_t* yh = (uint32_t*)ybase;                          // [MAX_G][YST] fp16 high parts
-  uint32_t* yl = yh + MAX_G * YST / 2;                      // [MAX_G][YST] fp16 low parts
-  float* yo = (float*)ybase;                                // [MAX_G][128] history output (aliases yh, yl)
-  float* hM = (float*)(ybase + MERGE_Y_BYTES);              // [MAX_G] history max, sum
+  const int b = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv;
+  const MergeLayout ML = merge_layout(a.B);
+  const uint4* Rf = (const uint4*)(smem + ML.off_rv);
+  uint32_t* yh = (uint32_t*)(smem + ML.off_y);  // [MAX_G][YST] fp16 high parts
+  uint32_t* yl = yh + MAX_G * YST / 2;          // [MAX_G][YST] fp16 low parts
+  float* yo = (float*)(smem + ML.off_y);        // [MAX_G][128] history output (aliases yh, yl)
+  float* tm = (float*)(smem + ML.off_tm);
+  float* tl = tm + MW;
+  float* to = (float*)(smem + ML.off_to);
+  float* wmv = (float*)(smem + ML.off_win);
+  float* wlv = wmv + MAX_G;
+  float* wov = (float*)(smem + ML.off_wo);
+  float* hM = (float*)(smem + ML.off_h);
   float* hL = hM + MAX_G;
+  float* ysc = hL + MAX_G;
+  uint64_t* mbar = (uint64_t*)(smem + ML.off_mbar);
+  int* red = (int*)(smem + ML.off_red);
+  int* pre = (int*)(smem + ML.off_pre);
   const bool unrot = !a.bf16_history && a.rot.mode != OSCAR_ROT_NONE;
+  if (t == 0) mbar_init(mbar, 1);
+  fence_proxy_async();
+  __syncthreads();
   if (unrot && t == 0) {
-    fence_proxy_async();
-    mbar_expect_tx(ubar, MERGE_RV_BYTES);
-    bulk_g2s(sm, a.rot.RV_frag + (size_t)kvh * RV_FRAG_WORDS, MERGE_RV_BYTES, ubar);
+    mbar_expect_tx(mbar, MERGE_RV_BYTES);
+    bulk_g2s(smem + ML.off_rv, a.rot.RV_frag + (size_t)kvh * RV_FRAG_WORDS, MERGE_RV_BYTES, mbar);
   }
+  // history lengths come from earlier stream work: the work list can be
+  // derived before the wait
+  const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
+  const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, unit, pre, red);
+  pdl_wait();  // the decode kernel's partial records are complete and visible
   const int pages_b = (cv.hist_lens[b] + PAGE - 1) / PAGE;
   const int nb = (pages_b + sc.S - 1) / sc.S;
   const int base = pre[b] + kvh * nb;
-  const int wslot = sc.n_hist + (b * cv.Hkv + kvh) * sc.wch;
-  float4 Ow[2];   // window output of this warp's heads
-  float mwv[2], lwv[2];
-  float4 Yv[2];   // this warp's heads' normalised history output (own channels)
-  float ysc[2];   // power-of-two scale applied to Yv before the fp16 split
-  for (int hh = 0; hh * NW + warp < G; ++hh) {
-    const int n = hh * NW + warp;
-    // ---- round 1: m, l of every partial (q = lane + 32k), the window, and
-    // the o of history partials 0..31
-    float mq[MERGE_KQ], lq[MERGE_KQ];
-#pragma unroll
-    for (int k = 0; k < MERGE_KQ; ++k) {
-      const int q = lane + 32 * k;
-      mq[k] = -INFINITY;
-      lq[k] = 0.f;
-      if (q < nb) {
-        const float* rec = a.part + ((size_t)(base + q) * G + n) * PART_STRIDE;
-        mq[k] = __ldcg(rec);
-        lq[k] = __ldcg(rec + 1);
-      }
-    }
-    const float* wrec = a.part + ((size_t)(wslot + (lane < sc.wch ? lane : 0)) * G + n) * PART_STRIDE;
-    const float mu = lane < sc.wch ? __ldcg(wrec) : -INFINITY;
-    const float lu = lane < sc.wch ? __ldcg(wrec + 1) : 0.f;
-    float4 o5[5];
-#pragma unroll
-    for (int u = 0; u < 5; ++u)
-      o5[u] = u < sc.wch ? __ldcg((const float4*)(a.part + ((size_t)(wslot + u) * G + n) * PART_STRIDE + PART_O) + lane)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 o32[32];
-#pragma unroll
-    for (int u = 0; u < 32; ++u)
-      o32[u] = u < nb ? __ldcg((const float4*)(a.part + ((size_t)(base + u) * G + n) * PART_STRIDE + PART_O) + lane)
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-    float mloc = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < MERGE_KQ; ++k)
-      if (lq[k] > 0.f) mloc = fmaxf(mloc, mq[k]);
-    // partials beyond 32 * MERGE_KQ (only with very many items): read again
-    for (int q = lane + 32 * MERGE_KQ; q < nb; q += 32) {
-      const float* rec = a.part + ((size_t)(base + q) * G + n) * PART_STRIDE;
-      if (__ldcg(rec + 1) > 0.f) mloc = fmaxf(mloc, __ldcg(rec));
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
-    const float M = mloc;
-    float wk[MERGE_KQ];
-    float lloc = 0.f;
-#pragma unroll
-    for (int k = 0; k < MERGE_KQ; ++k) {
-      wk[k] = lq[k] > 0.f ? ex2(mq[k] - M) : 0.f;
-      lloc = fmaf(lq[k], wk[k], lloc);
-    }
-    for (int q = lane + 32 * MERGE_KQ; q < nb; q += 32) {
-      const float* rec = a.part + ((size_t)(base + q) * G + n) * PART_STRIDE;
-      const float l2 = __ldcg(rec + 1);
-      if (l2 > 0.f) lloc = fmaf(l2, ex2(__ldcg(rec) - M), lloc);
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, o);
-    float mw = lu > 0.f ? mu : -INFINITY;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
-    const float wu = lu > 0.f ? ex2(mu - mw) : 0.f;
-    float lw = lu * wu;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
-    float4 OW = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int u = 0; u < 5; ++u) OW = fma4(o5[u], __shfl_sync(0xffffffffu, wu, u), OW);
+  const int wslot = sc.n_hist + (b * Hkv + kvh) * sc.wch;
+  const int WPH = MW / G;  // warps per head
+  const int n = warp / WPH, r = warp % WPH;
+
+  // ---- team member: history partials q = r, r + WPH, ...
+  if (n < G) {
+    float M = -INFINITY, Ls = 0.f;
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q0 = r; q0 < nb; q0 += WPH * MERGE_MQ) {
+      float mq[MERGE_MQ], lq[MERGE_MQ];
+      float4 oq[MERGE_MQ];
 #pragma unroll
-    for (int u = 0; u < 32; ++u) O = fma4(o32[u], __shfl_sync(0xffffffffu, wk[0], u), O);
-    // ---- further rounds: o of partials 32.., 32 at a time
-    for (int q0 = 32; q0 < nb; q0 += 32) {
+      for (int u = 0; u < MERGE_MQ; ++u) {
+        const int q = q0 + u * WPH;
+        const float* rec = a.part + ((size_t)(base + (q < nb ? q : 0)) * G + n) * PART_STRIDE;
+        mq[u] = q < nb ? __ldcg(rec) : -INFINITY;
+        lq[u] = q < nb ? __ldcg(rec + 1) : 0.f;
+        oq[u] = q < nb ? __ldcg((const float4*)(rec + PART_O) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float mx = M;
 #pragma unroll
-      for (int u = 0; u < 32; ++u)
-        o32[u] = (q0 + u < nb)
-                     ? __ldcg((const float4*)(a.part + ((size_t)(base + q0 + u) * G + n) * PART_STRIDE + PART_O) + lane)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-      const int kb = q0 >> 5;  // weights of partials q0..q0+31 sit in wk[kb] of lanes 0..31
-      float wsel = 0.f;
-      if (kb < MERGE_KQ) {
+      for (int u = 0; u < MERGE_MQ; ++u)
+        if (lq[u] > 0.f) mx = fmaxf(mx, mq[u]);
+      if (mx != -INFINITY) {
+        const float f = M == -INFINITY ? 0.f : ex2(M - mx);
+        Ls *= f;
+        O = scale4(O, f);
+        M = mx;
 #pragma unroll
-        for (int k = 0; k < MERGE_KQ; ++k)
-          if (k == kb) wsel = wk[k];
-      } else {
-        const int q = q0 + lane;
-        if (q < nb) {
-          const float* rec = a.part + ((size_t)(base + q) * G + n) * PART_STRIDE;
-          wsel = __ldcg(rec + 1) > 0.f ? ex2(__ldcg(rec) - M) : 0.f;
+        for (int u = 0; u < MERGE_MQ; ++u) {
+          const float w = lq[u] > 0.f ? ex2(mq[u] - M) : 0.f;
+          Ls = fmaf(lq[u], w, Ls);
+          O = fma4(oq[u], w, O);
         }
       }
-#pragma unroll
-      for (int u = 0; u < 32; ++u) O = fma4(o32[u], __shfl_sync(0xffffffffu, wsel, u), O);
     }
-    // normalised history output, then a power-of-two scale that keeps its
-    // largest channel near 2^12 for the fp16 split
-    const float inv = lloc > 0.f ? 1.f / lloc : 0.f;
-    float4 Y = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+    if (lane == 0) {
+      tm[warp] = M;
+      tl[warp] = Ls;
+    }
+    ((float4*)(to + warp * D))[lane] = O;
+    if (r == 0) {
+      // window partials (lane u < wch holds m and l of chunk u)
+      const float* wrec = a.part + ((size_t)(wslot + (lane < sc.wch ? lane : 0)) * G + n) * PART_STRIDE;
+      const float mu = lane < sc.wch ? __ldcg(wrec) : -INFINITY;
+      const float lu = lane < sc.wch ? __ldcg(wrec + 1) : 0.f;
+      float4 o5[5];
+#pragma unroll
+      for (int u = 0; u < 5; ++u)
+        o5[u] = u < sc.wch ? __ldcg((const float4*)(a.part + ((size_t)(wslot + u) * G + n) * PART_STRIDE + PART_O) + lane)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      float mw = lu > 0.f ? mu : -INFINITY;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+      const float wu = lu > 0.f ? ex2(mu - mw) : 0.f;
+      float lw = lu * wu;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+      float4 OW = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 5; ++u) OW = fma4(o5[u], __shfl_sync(0xffffffffu, wu, u), OW);
+      if (lane == 0) {
+        wmv[n] = mw;
+        wlv[n] = lw;
+      }
+      ((float4*)(wov + n * D))[lane] = OW;
+    }
+  }
+  __syncthreads();
+  // ---- warp n: head n's history total, normalised and scaled for the fp16 split
+  if (warp < G) {
+    const int h = warp;
+    float M = -INFINITY;
+    for (int k = 0; k < WPH; ++k)
+      if (tl[h * WPH + k] > 0.f) M = fmaxf(M, tm[h * WPH + k]);
+    float Ls = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+      for (int k = 0; k < WPH; ++k) {
+        const float l = tl[h * WPH + k];
+        const float w = l > 0.f ? ex2(tm[h * WPH + k] - M) : 0.f;
+        Ls = fmaf(l, w, Ls);
+        O = fma4(((const float4*)(to + (h * WPH + k) * D))[lane], w, O);
+      }
+    }
+    const float4 Y = scale4(O, Ls > 0.f ? 1.f / Ls : 0.f);
     float am = fmaxf(fmaxf(fabsf(Y.x), fabsf(Y.y)), fmaxf(fabsf(Y.z), fabsf(Y.w)));
 #pragma unroll
     for (int o = 16; o; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
     int ex = 0;
     frexpf(am, &ex);
     const float up = am > 0.f ? ldexpf(1.f, min(12 - ex, 100)) : 1.f;
-    Yv[hh] = Y;
-    ysc[hh] = up;
     if (lane == 0) {
-      hM[n] = lloc > 0.f ? M : -INFINITY;
-      hL[n] = lloc;
+      hM[h] = Ls > 0.f ? M : -INFINITY;
+      hL[h] = Ls;
+      ysc[h] = up;
     }
-    Ow[hh] = OW;
-    mwv[hh] = mw;
-    lwv[hh] = lw;
+    if (unrot) {
+      uint32_t l0, l1;
+      const uint32_t h0 = split_hi(Y.x * up, Y.y * up, &l0);
+      const uint32_t h1 = split_hi(Y.z * up, Y.w * up, &l1);
+      *(uint2*)(yh + h * (YST / 2) + 2 * lane) = make_uint2(h0, h1);
+      *(uint2*)(yl + h * (YST / 2) + 2 * lane) = make_uint2(l0, l1);
+    } else {
+      ((float4*)(yo + h * D))[lane] = scale4(Y, up);
+    }
+  } else if (unrot) {
+    // B operand rows of absent heads are 0
+    *(uint2*)(yh + warp * (YST / 2) + 2 * lane) = make_uint2(0u, 0u);
+    *(uint2*)(yl + warp * (YST / 2) + 2 * lane) = make_uint2(0u, 0u);
   }
+  __syncthreads();
   if (unrot) {
-    // heads of this warp into the fp16 B operand; rows of absent heads are 0
-    for (int n = warp; n < MAX_G; n += NW) {
-      const int hh = n / NW;
-      uint32_t h0 = 0u, h1 = 0u, l0 = 0u, l1 = 0u;
-      if (n < G) {
-        const float4 Y = hh == 0 ? Yv[0] : Yv[1];
-        const float up = hh == 0 ? ysc[0] : ysc[1];
-        h0 = split_hi(Y.x * up, Y.y * up, &l0);
-        h1 = split_hi(Y.z * up, Y.w * up, &l1);
-      }
-      *(uint2*)(yh + n * (YST / 2) + 2 * lane) = make_uint2(h0, h1);
-      *(uint2*)(yl + n * (YST / 2) + 2 * lane) = make_uint2(l0, l1);
-    }
-    __syncthreads();
-    if (!mbar_wait(ubar, uphase)) record_error(cv.err, OSCAR_ERR_TIMEOUT);
-    float d[2][4];
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi) d[mi][0] = d[mi][1] = d[mi][2] = d[mi][3] = 0.f;
+    if (!mbar_wait(mbar, 0)) record_error(cv.err, OSCAR_ERR_TIMEOUT);
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       const uint32_t bh0 = yh[gid * (YST / 2) + 8 * ks + tq], bh1 = yh[gid * (YST / 2) + 8 * ks + 4 + tq];
       const uint32_t bl0 = yl[gid * (YST / 2) + 8 * ks + tq], bl1 = yl[gid * (YST / 2) + 8 * ks + 4 + tq];
-#pragma unroll
-      for (int mi = 0; mi < 2; ++mi) {
-        const int mt = 2 * warp + mi;
-        const uint4 ah = Rf[rv_frag_index(0, mt, ks, lane) / 4];
-        const uint4 al = Rf[rv_frag_index(1, mt, ks, lane) / 4];
-        mma_f16(d[mi], ah.x, ah.y, ah.z, ah.w, bh0, bh1);
-        mma_f16(d[mi], ah.x, ah.y, ah.z, ah.w, bl0, bl1);
-        mma_f16(d[mi], al.x, al.y, al.z, al.w, bh0, bh1);
-      }
+      const uint4 ah = Rf[rv_frag_index(0, warp, ks, lane) / 4];
+      const uint4 al = Rf[rv_frag_index(1, warp, ks, lane) / 4];
+      mma_f16(d, ah.x, ah.y, ah.z, ah.w, bh0, bh1);
+      mma_f16(d, ah.x, ah.y, ah.z, ah.w, bl0, bl1);
+      mma_f16(d, al.x, al.y, al.z, al.w, bh0, bh1);
     }
     __syncthreads();  // B operands consumed: yo may overwrite them
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi) {
-      const int c = 32 * warp + 16 * mi + gid;
-      yo[(2 * tq) * D + c] = d[mi][0];
-      yo[(2 * tq + 1) * D + c] = d[mi][1];
-      yo[(2 * tq) * D + c + 8] = d[mi][2];
-      yo[(2 * tq + 1) * D + c + 8] = d[mi][3];
-    }
-  } else {
-    for (int hh = 0; hh * NW + warp < G; ++hh) {
-      const int n = hh * NW + warp;
-      const float up = ysc[hh];
-      ((float4*)(yo + n * D))[lane] = make_float4(Yv[hh].x * up, Yv[hh].y * up, Yv[hh].z * up, Yv[hh].w * up);
-    }
+    const int c = 16 * warp + gid;
+    yo[(2 * tq) * D + c] = d[0];
+    yo[(2 * tq + 1) * D + c] = d[1];
+    yo[(2 * tq) * D + c + 8] = d[2];
+    yo[(2 * tq + 1) * D + c + 8] = d[3];
+    __syncthreads();
   }
-  __syncthreads();
-  // ---- per warp: LSE-merge of history and window for its heads
-  for (int hh = 0; hh * NW + warp < G; ++hh) {
-    const int n = hh * NW + warp;
-    const float M = hM[n], Ls = hL[n], mw = mwv[hh], lw = lwv[hh];
-    const float down = 1.f / ysc[hh];
-    float4 Oh = ((const float4*)(yo + n * D))[lane];
+  // ---- warp n: LSE-merge of history and window for head n
+  if (warp < G) {
+    const int h = warp;
+    const float M = hM[h], Ls = hL[h], mw = wmv[h], lw = wlv[h];
+    const float down = 1.f / ysc[h];
+    const float4 Oh = ((const float4*)(yo + h * D))[lane];
+    const float4 Ow = ((const float4*)(wov + h * D))[lane];
     const float M2 = fmaxf(Ls > 0.f ? M : -INFINITY, lw > 0.f ? mw : -INFINITY);
     float o[4] = {0.f, 0.f, 0.f, 0.f};
     float lse = -INFINITY;
@@ -893,14 +1117,14 @@ __device__ __noinline__ void merge_bkvh(const DecodeArgs& a, const Sched& sc, co
       const float fw = lw > 0.f ? ex2(mw - M2) : 0.f;
       const float den = Ls * fh + lw * fw;
       const float inv = 1.f / den;
-      const float hw = Ls * fh * down;  // history output is normalised and scaled by ysc
-      o[0] = fmaf(Oh.x, hw, Ow[hh].x * fw) * inv;
-      o[1] = fmaf(Oh.y, hw, Ow[hh].y * fw) * inv;
-      o[2] = fmaf(Oh.z, hw, Ow[hh].z * fw) * inv;
-      o[3] = fmaf(Oh.w, hw, Ow[hh].w * fw) * inv;
+      const float hw = Ls * fh * down;  // the history output is normalised and scaled by ysc
+      o[0] = fmaf(Oh.x, hw, Ow.x * fw) * inv;
+      o[1] = fmaf(Oh.y, hw, Ow.y * fw) * inv;
+      o[2] = fmaf(Oh.z, hw, Ow.z * fw) * inv;
+      o[3] = fmaf(Oh.w, hw, Ow.w * fw) * inv;
       lse = (M2 + log2f(den)) * LN2;
     }
-    const size_t row = (size_t)b * cv.Hq + kvh * G + n;
+    const size_t row = (size_t)b * cv.Hq + kvh * G + h;
     __nv_bfloat162 o01 = __floats2bfloat162_rn(o[0], o[1]);
     __nv_bfloat162 o23 = __floats2bfloat162_rn(o[2], o[3]);
     uint2 pk;
@@ -914,7 +1138,7 @@ __device__ __noinline__ void merge_bkvh(const DecodeArgs& a, const Sched& sc, co
 // IMPL: 0 INT2 history on tensor cores, 1 INT2 history on CUDA cores,
 // 2 BF16 history (the baseline; no INT2 code, double-buffered BF16 tiles).
 template <int NG, int IMPL>
-__global__ void __launch_bounds__(NW * 32, IMPL == 0 ? 3 : 2) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) decode_kernel(DecodeArgs a) {
   constexpr bool BF16H = (IMPL == 2);
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheView& cv = a.cv;
@@ -932,11 +1156,9 @@ __global__ void __launch_bounds__(NW * 32, IMPL == 0 ? 3 : 2) decode_kernel(Deco
   const int gid = lane >> 2, tq = lane & 3;
   const int G = cv.G, Hkv = cv.Hkv;
 
-  if (threadIdx.x < NW * DEPTH + 1) mbar_init(&mbar[threadIdx.x], 1);
-  if (threadIdx.x == 0) {
-    misc[1] = 0;
-    misc[3] = 0;  // merges done by this CTA (phase of the merge barrier)
-  }
+  pdl_launch_dependents();  // merge_kernel may be scheduled as CTAs of this grid retire
+  if (threadIdx.x < NW * DEPTH) mbar_init(&mbar[threadIdx.x], 1);
+  if (threadIdx.x == 0) misc[1] = 0;
   fence_proxy_async();
   __syncthreads();
 
@@ -1103,24 +1325,29 @@ __global__ void __launch_bounds__(NW * 32, IMPL == 0 ? 3 : 2) decode_kernel(Deco
       }
       bool timed_out = false;
       int k_fail = 0;
-      if constexpr (IMPL == 0) {
+      if constexpr (IMPL == 0 || IMPL == 3) {
+        // IMPL 3: pages in pairs, two streams per tile (G <= 4)
+        constexpr bool PAIR = (IMPL == 3);
         Int2State<NG> S;
 #pragma unroll
         for (int j = 0; j < 8; ++j) S.oacc[j][0] = S.oacc[j][1] = S.oacc[j][2] = S.oacc[j][3] = 0.f;
         {
-          const uint8_t* qrec = a.qpack + ((size_t)b * cv.Hq + kvh * G + (gid < G ? gid : 0)) * QPACK_BYTES;
+          // B column gid carries head gid (PAIR: head gid & 3 in both halves)
+          const int qh = PAIR ? (gid & 3) : gid;
+          const bool qv = qh < G;
+          const uint8_t* qrec = a.qpack + ((size_t)b * cv.Hq + kvh * G + (qv ? qh : 0)) * QPACK_BYTES;
           const __half* qbh = (const __half*)qrec;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            S.bq[kk][0] = gid < G ? __ldcg((const unsigned int*)(qbh + 16 * kk + 2 * tq)) : 0u;
-            S.bq[kk][1] = gid < G ? __ldcg((const unsigned int*)(qbh + 16 * kk + 8 + 2 * tq)) : 0u;
+            S.bq[kk][0] = qv ? __ldcg((const unsigned int*)(qbh + 16 * kk + 2 * tq)) : 0u;
+            S.bq[kk][1] = qv ? __ldcg((const unsigned int*)(qbh + 16 * kk + 8 + 2 * tq)) : 0u;
           }
 #pragma unroll
           for (int hc = 0; hc < 2; ++hc) {
-            const int n = 2 * tq + hc;
+            const int n = PAIR ? ((2 * tq + hc) & 3) : 2 * tq + hc;
             const bool hv = n < G;
             const uint8_t* r = a.qpack + ((size_t)b * cv.Hq + kvh * G + (hv ? n : 0)) * QPACK_BYTES;
-            S.m[hc] = -INFINITY;
+            S.m[hc] = PAIR ? -1e30f : -INFINITY;
             S.l[hc] = 0.f;
             const float al = hv ? __ldcg((const float*)(r + QPACK_ALPHA)) : 0.f;
             S.ka[hc] = al;
@@ -1139,31 +1366,72 @@ __global__ void __launch_bounds__(NW * 32, IMPL == 0 ? 3 : 2) decode_kernel(Deco
             }
           }
         }
-        for (int k = 0; k < nw_pages; ++k) {
-          const int st = (int)((seq + k) % DEPTH);
-          const uint32_t ph = ((seq + k) / DEPTH) & 1u;
-          if (!__all_sync(0xffffffffu, mbar_wait(&my_bar[st], ph))) {
-            timed_out = true;
-            k_fail = k;
-            break;
+        if constexpr (PAIR) {
+          const uint32_t mA = gid < 4 ? 0xffffffffu : 0u;  // B columns 0..3: page A
+          for (int k = 0; k < nw_pages; k += 2) {
+            const bool hasB = k + 1 < nw_pages;
+            const int sa = (int)((seq + k) % DEPTH), sb = (int)((seq + k + 1) % DEPTH);
+            bool ok = mbar_wait(&my_bar[sa], ((seq + k) / DEPTH) & 1u);
+            if (hasB && ok) ok = mbar_wait(&my_bar[sb], ((seq + k + 1) / DEPTH) & 1u);
+            if (!__all_sync(0xffffffffu, ok)) {
+              timed_out = true;
+              k_fail = k;
+              break;
+            }
+            if (k > 0 && (k & 31) == 0) page_ids_advance(P, cv, b, p0 + warp, nw_pages, lane);
+            const int pa = p0 + warp + k * NW, pb = pa + NW;
+            const int pida = page_id_at(P, k);
+            const int pidb = page_id_at(P, hasB ? k + 1 : k);
+            const bool oka = pida >= 0 && pida < cv.num_pages;
+            const bool okb = hasB && pidb >= 0 && pidb < cv.num_pages;
+            const int nva = oka ? ((pa == pages_b - 1) ? hist_b - pa * PAGE : PAGE) : 0;
+            const int nvb = okb ? ((pb == pages_b - 1) ? hist_b - pb * PAGE : PAGE) : 0;
+            const uint8_t* sta = my_stage + (size_t)sa * L.stage_bytes;
+            const uint8_t* stb = hasB ? my_stage + (size_t)sb * L.stage_bytes : sta;
+            if (nva == PAGE && nvb == PAGE)
+              int2_pair_mma<NG, true>(S, sta, nva, stb, nvb, true, lane, mA);
+            else if (nva > 0 || nvb > 0)
+              int2_pair_mma<NG, false>(S, sta, nva, stb, nvb, hasB, lane, mA);
+            if ((k & 7) == 6) flush_v_offset<NG>(S);
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              if (k + u + DEPTH < nw_pages) {
+                const int pid_next = page_id_at(P, k + u + DEPTH);
+                if (lane == 0) {
+                  fence_proxy_async();
+                  issue(k + u + DEPTH, pid_next);
+                }
+              }
+            }
           }
-          if (k > 0 && (k & 31) == 0) page_ids_advance(P, cv, b, p0 + warp, nw_pages, lane);
-          const int p = p0 + warp + k * NW;
-          const int pid = page_id_at(P, k);
-          if (pid >= 0 && pid < cv.num_pages) {
-            const int nv = (p == pages_b - 1) ? hist_b - p * PAGE : PAGE;
-            if (nv == PAGE)
-              int2_page_mma<NG, true>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
-            else
-              int2_page_mma<NG, false>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
-            if ((k & 7) == 7) flush_v_offset<NG>(S);
-          }
-          __syncwarp();
-          if (k + DEPTH < nw_pages) {
-            const int pid_next = page_id_at(P, k + DEPTH);
-            if (lane == 0) {
-              fence_proxy_async();
-              issue(k + DEPTH, pid_next);
+        } else {
+          for (int k = 0; k < nw_pages; ++k) {
+            const int st = (int)((seq + k) % DEPTH);
+            const uint32_t ph = ((seq + k) / DEPTH) & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait(&my_bar[st], ph))) {
+              timed_out = true;
+              k_fail = k;
+              break;
+            }
+            if (k > 0 && (k & 31) == 0) page_ids_advance(P, cv, b, p0 + warp, nw_pages, lane);
+            const int p = p0 + warp + k * NW;
+            const int pid = page_id_at(P, k);
+            if (pid >= 0 && pid < cv.num_pages) {
+              const int nv = (p == pages_b - 1) ? hist_b - p * PAGE : PAGE;
+              if (nv == PAGE)
+                int2_page_mma<NG, true>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
+              else
+                int2_page_mma<NG, false>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
+              if ((k & 7) == 7) flush_v_offset<NG>(S);
+            }
+            __syncwarp();
+            if (k + DEPTH < nw_pages) {
+              const int pid_next = page_id_at(P, k + DEPTH);
+              if (lane == 0) {
+                fence_proxy_async();
+                issue(k + DEPTH, pid_next);
+              }
             }
           }
         }
@@ -1179,6 +1447,7 @@ __global__ void __launch_bounds__(NW * 32, IMPL == 0 ? 3 : 2) decode_kernel(Deco
             }
           }
         }
+        if constexpr (PAIR) merge_pair_streams<NG>(S);
         if (timed_out) {
           if (lane == 0) {
             record_error(cv.err, OSCAR_ERR_TIMEOUT);
@@ -1284,21 +1553,6 @@ __global__ void __launch_bounds__(NW * 32, IMPL == 0 ? 3 : 2) decode_kernel(Deco
       pdl_wait();
       waited = true;
     }
-    // Last finisher of this (request, kv head) merges it.
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const int nb = (pages_b + sc.S - 1) / sc.S;
-      const int old = atomicAdd(&a.done[b * Hkv + kvh], 1);
-      misc[2] = (old == nb + sc.wch - 1) ? 1 : 0;  // nb history items + wch window items
-      fence_acq_rel_gpu();  // acquire: the other CTAs' records are read after this
-    }
-    __syncthreads();
-    if (misc[2]) {
-      merge_bkvh(a, sc, pre, b, kvh, wm, &mbar[NW * DEPTH], (uint32_t)misc[3] & 1u);
-      __syncthreads();
-      // the merge's R_V copy completed one phase of its barrier
-      if (threadIdx.x == 0 && !BF16H && a.rot.mode != OSCAR_ROT_NONE) misc[3] += 1;
-    }
     if (misc[1]) break;
     __syncthreads();
     if (threadIdx.x == 0) misc[0] = (int)gridDim.x + atomicAdd(a.counter, 1);
@@ -1326,6 +1580,29 @@ cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t st) {
   lc.attrs = attr;
   lc.numAttrs = 1;
   return cudaLaunchKernelEx(&lc, decode_kernel<NG, IMPL>, a);
+}
+
+cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t st) {
+  const MergeLayout ML = merge_layout(a.B);
+  if ((ML.off_mbar % 8) || (ML.off_y % 16) || (ML.off_to % 16) || (ML.off_wo % 16)) return cudaErrorInvalidValue;
+  static int configured = -1;  // dynamic shared memory size the kernel was last configured for
+  if (configured < ML.total) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ML.total);
+    if (e != cudaSuccess) return e;
+    configured = ML.total;
+  }
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(a.B * a.cv.Hkv);
+  lc.blockDim = dim3(MW * 32);
+  lc.dynamicSmemBytes = ML.total;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, merge_kernel, a);
 }
 
 }  // namespace
@@ -1374,6 +1651,7 @@ int decode_ctas_per_sm(const DecodeArgs& a) {
   const int NG = a.cv.NG;
   if (a.bf16_history) return occupancy_t<1, 2>(a);
   if (a.impl == 1) return NG == 1 ? occupancy_t<1, 1>(a) : NG == 2 ? occupancy_t<2, 1>(a) : occupancy_t<4, 1>(a);
+  if (a.impl == 3) return NG == 1 ? occupancy_t<1, 3>(a) : NG == 2 ? occupancy_t<2, 3>(a) : occupancy_t<4, 3>(a);
   return NG == 1 ? occupancy_t<1, 0>(a) : NG == 2 ? occupancy_t<2, 0>(a) : occupancy_t<4, 0>(a);
 }
 
@@ -1391,12 +1669,20 @@ cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profil
     if (cv.NG == 1) e = launch_decode_t<1, 1>(a, grid, st);
     else if (cv.NG == 2) e = launch_decode_t<2, 1>(a, grid, st);
     else e = launch_decode_t<4, 1>(a, grid, st);
+  } else if (a.impl == 3) {
+    if (cv.NG == 1) e = launch_decode_t<1, 3>(a, grid, st);
+    else if (cv.NG == 2) e = launch_decode_t<2, 3>(a, grid, st);
+    else e = launch_decode_t<4, 3>(a, grid, st);
   } else {
     if (cv.NG == 1) e = launch_decode_t<1, 0>(a, grid, st);
     else if (cv.NG == 2) e = launch_decode_t<2, 0>(a, grid, st);
     else e = launch_decode_t<4, 0>(a, grid, st);
   }
   prof_end(prof, OSCAR_KERNEL_DECODE_MAIN, st);
+  if (e != cudaSuccess) return e;
+  prof_begin(prof, OSCAR_KERNEL_DECODE_MERGE, st);
+  e = launch_merge(a, st);
+  prof_end(prof, OSCAR_KERNEL_DECODE_MERGE, st);
   return e;
 }
 

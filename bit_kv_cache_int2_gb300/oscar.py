@@ -35,6 +35,9 @@ ROT_HADAMARD = 1
 ROT_NONE = 2
 
 OPT_DECODE_IMPL = 0
+DECODE_TENSOR = 0  # tensor cores; two pages per tile at G <= 4
+DECODE_CUDA_CORE = 1
+DECODE_TENSOR_SINGLE = 2  # tensor cores, one page per tile
 OPT_CTAS_PER_SM = 1
 OPT_ITEMS_PER_CTA = 2
 

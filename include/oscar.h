@@ -101,8 +101,16 @@ typedef enum {
   OSCAR_ROT_NONE = 2      /* R = I (naive INT2)                    */
 } oscar_rot_mode;
 
+/* INT2 history decode kernels (the BF16-history baseline has one kernel). */
 typedef enum {
-  OSCAR_OPT_DECODE_IMPL = 0, /* 0: tensor-core INT2 kernel (default); 1: CUDA-core fp32 kernel */
+  OSCAR_DECODE_TENSOR = 0,        /* tensor cores; with at most 4 query heads per kv head a warp
+                                     takes two pages per tile as two softmax streams (default) */
+  OSCAR_DECODE_CUDA_CORE = 1,     /* fp32 CUDA cores, one page per warp at a time */
+  OSCAR_DECODE_TENSOR_SINGLE = 2  /* tensor cores, one page per tile at any group size */
+} oscar_decode_impl;
+
+typedef enum {
+  OSCAR_OPT_DECODE_IMPL = 0, /* an oscar_decode_impl value (default OSCAR_DECODE_TENSOR) */
   OSCAR_OPT_CTAS_PER_SM = 1, /* persistent decode CTAs per SM, 1..4 (default 4), capped by occupancy */
   OSCAR_OPT_ITEMS_PER_CTA = 2 /* work items per decode CTA the scheduler aims for, 1..8 (default 1) */
 } oscar_option;
