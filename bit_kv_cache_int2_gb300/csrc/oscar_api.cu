@@ -281,6 +281,10 @@ oscar_status decode_common(oscar_ctx* ctx, int layer, const oscar_cache* cache, 
   a.impl = kernel_impl(ctx);
   a.bf16_history = bf16_history ? 1 : 0;
   a.rot = layer_rot(ctx, layer);
+  // heads per merge CTA: halve while the merge would not cover the SMs
+  a.merge_hpc = ctx->G;
+  while (a.merge_hpc % 2 == 0 && batch * ctx->cfg.num_kv_heads * (ctx->G / a.merge_hpc) < ctx->num_sms)
+    a.merge_hpc /= 2;
   const int grid = ctx->num_sms * decode_ctas(ctx, batch, bf16_history);
   return cuda_status(launch_decode(a, grid, (cudaStream_t)stream, &ctx->prof));
 }

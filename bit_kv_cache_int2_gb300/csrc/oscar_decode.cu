@@ -131,11 +131,11 @@ __global__ void __launch_bounds__(128) prep_kernel(DecodeArgs a) {
 // ------------------------------------------------------------ smem layout
 struct SmemLayout {
   int stage_bytes;   // per stage
-  int off_stage, off_mbar, off_qf, off_vs, off_pre, off_red, off_misc, total;
+  int off_stage, off_mbar, off_qpk, off_qf, off_vs, off_pre, off_red, off_misc, total;
 };
 
 // impl: 0 tensor-core INT2, 1 CUDA-core INT2, 2 BF16 history (no INT2 pages)
-__host__ __device__ inline SmemLayout smem_layout(int head_bytes, int B, int impl) {
+__host__ __device__ inline SmemLayout smem_layout(int head_bytes, int B, int impl, int G) {
   SmemLayout L;
   // BF16 paths read global memory directly; only INT2 pages use stages
   L.stage_bytes = impl == 2 ? 0 : (head_bytes + 127) & ~127;
@@ -149,6 +149,8 @@ __host__ __device__ inline SmemLayout smem_layout(int head_bytes, int B, int imp
   o += stage_total;
   L.off_mbar = o;
   o += NW * DEPTH * 8;  // pipeline stages
+  L.off_qpk = o;        // tensor-core paths: the G packed query records of the item's kv head
+  if (impl == 0 || impl == 3) o += G * QPACK_BYTES;
   L.off_qf = o;
   if (impl == 1) o += MAX_G * D * 4 + MAX_G * 4 * 4;  // fp32 q' in K storage order + z weights
   L.off_vs = o;
@@ -156,7 +158,7 @@ __host__ __device__ inline SmemLayout smem_layout(int head_bytes, int B, int imp
   L.off_pre = o;
   o += ((B + 1) * 4 + 15) & ~15;
   L.off_red = o;
-  o += 64 * 4;
+  o += 2 * NW * 4;  // block reductions of the work-list derivation
   L.off_misc = o;
   o += 16;
   L.total = o;
@@ -402,8 +404,9 @@ __device__ __forceinline__ void int2_pair_mma(Int2State<NG>& S, const uint8_t* s
   for (int s = 0; s < 4; ++s)
 #pragma unroll
     for (int gr = 0; gr < NG; ++gr) acc[s][gr][0] = acc[s][gr][1] = acc[s][gr][2] = acc[s][gr][3] = 0.f;
+  const uint32_t mB = ~mA;
   qk_page_masked<NG>(acc, stA, S.bq, mA, gid, tq);
-  if (hasB) qk_page_masked<NG>(acc, stB, S.bq, ~mA, gid, tq);
+  if (hasB) qk_page_masked<NG>(acc, stB, S.bq, mB, gid, tq);
   // this lane's columns 2tq, 2tq + 1 belong to page A when tq < 2
   const bool own_a = tq < 2;
   const uint8_t* st = own_a ? stA : stB;
@@ -473,7 +476,6 @@ __device__ __forceinline__ void int2_pair_mma(Int2State<NG>& S, const uint8_t* s
     vb_w[j][0] = *(const uint32_t*)(vcB + (16 * j + gid) * 16 + 4 * tq);
     vb_w[j][1] = *(const uint32_t*)(vcB + (16 * j + 8 + gid) * 16 + 4 * tq);
   }
-  const uint32_t mB = ~mA;
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const int ta = 16 * s + gid, tb = ta + 8;
@@ -880,24 +882,26 @@ __device__ __forceinline__ uint32_t split_hi(float a, float b, uint32_t* lo) {
 }
 
 // ------------------------------------------------------------------ merge
-// grid = B * Hkv, block = MW * 32, launched as a programmatic dependent of
-// decode_kernel.  CTA (b, kvh) merges the partial records of request b, kv
-// head kvh [Blog, pipeline paragraph: the INT2 and BF16 parts are combined by
-// online softmax]:
+// grid = B * Hkv * (G / hpc), block = MW * 32, launched as a programmatic
+// dependent of decode_kernel.  CTA (b, kvh, head group) merges the partial
+// records of query heads h0 .. h0 + hpc - 1 of request b, kv head kvh [Blog,
+// pipeline paragraph: the INT2 and BF16 parts are combined by online
+// softmax].  A merge reads every partial record of its heads once, so small
+// batches spread it over more CTAs (hpc < G) to use more SMs' load bandwidth:
 //   * before waiting for the decode kernel it derives the work list (the same
 //     one the decode kernel used) and starts a bulk copy of the R_V fragments
 //     (64 KB) into shared memory;
-//   * the MW / G warps of head n's team each LSE-merge every (MW / G)-th
-//     history partial with all of their loads in one round (each lane holds
-//     channels 4*lane .. 4*lane+3); the first warp of a team also merges the
-//     window partials;
+//   * the MW / hpc warps of head n's team take every (MW / hpc)-th record of the
+//     list (history partials, then window partials) and LSE-merge history and
+//     window separately, with all of their loads in one round (each lane
+//     holds channels 4*lane .. 4*lane+3);
 //   * warp n combines its team into (M, L, O'), normalises O'/L and writes it
 //     as fp16 high and low parts; o = (O'/L)·R_V^T is three fp16 products per
-//     tile (hi·hi, hi·lo, lo·hi) with fp32 accumulation, warp w owning output
-//     channels 16w .. 16w+15;
+//     tile (hi·hi, hi·lo, lo·hi) with fp32 accumulation, warp w < 8 owning
+//     output channels 16w .. 16w+15;
 //   * warp n writes head n's LSE-merge of history and window.
-constexpr int MW = 8;        // warps of the merge kernel
-constexpr int MERGE_MQ = 16;  // history partials per warp and round
+constexpr int MW = 16;       // warps of the merge kernel
+constexpr int MERGE_MQ = 4;   // records per warp and round of loads
 
 struct MergeLayout {
   int off_rv, off_y, off_tm, off_to, off_win, off_wo, off_h, off_mbar, off_red, off_pre, total;
@@ -910,10 +914,10 @@ __host__ __device__ inline MergeLayout merge_layout(int B) {
   o += MERGE_RV_BYTES;
   L.off_y = o;
   o += MERGE_Y_BYTES;
-  L.off_tm = o;               // team m, l: [2][MW]
-  o += 2 * MW * 4;
-  L.off_to = o;               // team o: [MW][128]
-  o += MW * D * 4;
+  L.off_tm = o;               // team m, l of history and window: [4][MW]
+  o += 4 * MW * 4;
+  L.off_to = o;               // team o of history and window: [2][MW][128]
+  o += 2 * MW * D * 4;
   L.off_win = o;              // window m, l: [2][MAX_G]
   o += 2 * MAX_G * 4;
   L.off_wo = o;               // window o: [MAX_G][128]
@@ -935,7 +939,9 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
   const CacheView& cv = a.cv;
   const int G = cv.G, Hkv = cv.Hkv, t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int gid = lane >> 2, tq = lane & 3;
-  const int b = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv;
+  const int HPC = a.merge_hpc, NHG = G / HPC;
+  const int h0 = (blockIdx.x % NHG) * HPC;
+  const int b = (blockIdx.x / NHG) / Hkv, kvh = (blockIdx.x / NHG) % Hkv;
   const MergeLayout ML = merge_layout(a.B);
   const uint4* Rf = (const uint4*)(smem + ML.off_rv);
   uint32_t* yh = (uint32_t*)(smem + ML.off_y);  // [MAX_G][YST] fp16 high parts
@@ -965,95 +971,117 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
   // derived before the wait
   const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
   const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, unit, pre, red);
-  pdl_wait();  // the decode kernel's partial records are complete and visible
   const int pages_b = (cv.hist_lens[b] + PAGE - 1) / PAGE;
   const int nb = (pages_b + sc.S - 1) / sc.S;
   const int base = pre[b] + kvh * nb;
   const int wslot = sc.n_hist + (b * Hkv + kvh) * sc.wch;
-  const int WPH = MW / G;  // warps per head
-  const int n = warp / WPH, r = warp % WPH;
+  const int WPH = MW / HPC;  // warps per head
+  const int n = warp / WPH, r = warp % WPH;  // head h0 + n of the kv group
+  if (n < HPC && lane == 0 && r < nb + sc.wch) {
+    // warm the address translation of this warp's records while the decode
+    // kernel finishes (the line is written again before it is read)
+    const int slot = r < nb ? base + r : wslot + (r - nb);
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a.part + ((size_t)slot * G + h0 + n) * PART_STRIDE));
+  }
+  pdl_wait();  // the decode kernel's partial records are complete and visible
 
-  // ---- team member: history partials q = r, r + WPH, ...
-  if (n < G) {
-    float M = -INFINITY, Ls = 0.f;
-    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q0 = r; q0 < nb; q0 += WPH * MERGE_MQ) {
+  // ---- team member: records q = r, r + WPH, ... of the list (history
+  // partials 0..nb-1, then window partials nb..nb+wch-1)
+  float* tmw = tl + MW;
+  float* tlw = tmw + MW;
+  float* tow = to + MW * D;
+  if (n < HPC) {
+    float M = -INFINITY, Ls = 0.f, Mw = -INFINITY, Lw = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f), OW = O;
+    const int nrec = nb + sc.wch;
+    for (int q0 = r; q0 < nrec; q0 += WPH * MERGE_MQ) {
       float mq[MERGE_MQ], lq[MERGE_MQ];
       float4 oq[MERGE_MQ];
 #pragma unroll
       for (int u = 0; u < MERGE_MQ; ++u) {
         const int q = q0 + u * WPH;
-        const float* rec = a.part + ((size_t)(base + (q < nb ? q : 0)) * G + n) * PART_STRIDE;
-        mq[u] = q < nb ? __ldcg(rec) : -INFINITY;
-        lq[u] = q < nb ? __ldcg(rec + 1) : 0.f;
-        oq[u] = q < nb ? __ldcg((const float4*)(rec + PART_O) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int slot = q < nb ? base + q : wslot + (q - nb);
+        const float* rec = a.part + ((size_t)(q < nrec ? slot : base) * G + h0 + n) * PART_STRIDE;
+        mq[u] = q < nrec ? __ldcg(rec) : -INFINITY;
+        lq[u] = q < nrec ? __ldcg(rec + 1) : 0.f;
+        oq[u] = q < nrec ? __ldcg((const float4*)(rec + PART_O) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      float mx = M;
+      float mx = M, mxw = Mw;
 #pragma unroll
-      for (int u = 0; u < MERGE_MQ; ++u)
-        if (lq[u] > 0.f) mx = fmaxf(mx, mq[u]);
-      if (mx != -INFINITY) {
-        const float f = M == -INFINITY ? 0.f : ex2(M - mx);
-        Ls *= f;
-        O = scale4(O, f);
-        M = mx;
+      for (int u = 0; u < MERGE_MQ; ++u) {
+        const bool hist = q0 + u * WPH < nb;
+        if (lq[u] > 0.f) {
+          if (hist) mx = fmaxf(mx, mq[u]);
+          else mxw = fmaxf(mxw, mq[u]);
+        }
+      }
+      const float f = (M == -INFINITY || mx == -INFINITY) ? 0.f : ex2(M - mx);
+      const float fw = (Mw == -INFINITY || mxw == -INFINITY) ? 0.f : ex2(Mw - mxw);
+      Ls *= f;
+      O = scale4(O, f);
+      Lw *= fw;
+      OW = scale4(OW, fw);
+      M = mx;
+      Mw = mxw;
 #pragma unroll
-        for (int u = 0; u < MERGE_MQ; ++u) {
-          const float w = lq[u] > 0.f ? ex2(mq[u] - M) : 0.f;
+      for (int u = 0; u < MERGE_MQ; ++u) {
+        const bool hist = q0 + u * WPH < nb;
+        const float w = lq[u] > 0.f ? ex2(mq[u] - (hist ? M : Mw)) : 0.f;
+        if (hist) {
           Ls = fmaf(lq[u], w, Ls);
           O = fma4(oq[u], w, O);
+        } else {
+          Lw = fmaf(lq[u], w, Lw);
+          OW = fma4(oq[u], w, OW);
         }
       }
     }
     if (lane == 0) {
       tm[warp] = M;
       tl[warp] = Ls;
+      tmw[warp] = Mw;
+      tlw[warp] = Lw;
     }
     ((float4*)(to + warp * D))[lane] = O;
-    if (r == 0) {
-      // window partials (lane u < wch holds m and l of chunk u)
-      const float* wrec = a.part + ((size_t)(wslot + (lane < sc.wch ? lane : 0)) * G + n) * PART_STRIDE;
-      const float mu = lane < sc.wch ? __ldcg(wrec) : -INFINITY;
-      const float lu = lane < sc.wch ? __ldcg(wrec + 1) : 0.f;
-      float4 o5[5];
-#pragma unroll
-      for (int u = 0; u < 5; ++u)
-        o5[u] = u < sc.wch ? __ldcg((const float4*)(a.part + ((size_t)(wslot + u) * G + n) * PART_STRIDE + PART_O) + lane)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-      float mw = lu > 0.f ? mu : -INFINITY;
-#pragma unroll
-      for (int o = 16; o; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
-      const float wu = lu > 0.f ? ex2(mu - mw) : 0.f;
-      float lw = lu * wu;
-#pragma unroll
-      for (int o = 16; o; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
-      float4 OW = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int u = 0; u < 5; ++u) OW = fma4(o5[u], __shfl_sync(0xffffffffu, wu, u), OW);
-      if (lane == 0) {
-        wmv[n] = mw;
-        wlv[n] = lw;
-      }
-      ((float4*)(wov + n * D))[lane] = OW;
-    }
+    ((float4*)(tow + warp * D))[lane] = OW;
   }
   __syncthreads();
-  // ---- warp n: head n's history total, normalised and scaled for the fp16 split
-  if (warp < G) {
+  // ---- warp n: head h0 + n's history total, normalised and scaled for the fp16 split
+  if (warp < HPC) {
     const int h = warp;
-    float M = -INFINITY;
-    for (int k = 0; k < WPH; ++k)
-      if (tl[h * WPH + k] > 0.f) M = fmaxf(M, tm[h * WPH + k]);
-    float Ls = 0.f;
-    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-      for (int k = 0; k < WPH; ++k) {
-        const float l = tl[h * WPH + k];
-        const float w = l > 0.f ? ex2(tm[h * WPH + k] - M) : 0.f;
-        Ls = fmaf(l, w, Ls);
+    // team member k's m and l in lane k
+    const float lk = lane < WPH ? tl[h * WPH + lane] : 0.f;
+    const float mk = lane < WPH ? tm[h * WPH + lane] : -INFINITY;
+    const float lwk = lane < WPH ? tlw[h * WPH + lane] : 0.f;
+    const float mwk = lane < WPH ? tmw[h * WPH + lane] : -INFINITY;
+    float M = lk > 0.f ? mk : -INFINITY, Mw = lwk > 0.f ? mwk : -INFINITY;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, o));
+    }
+    const float wk = lk > 0.f ? ex2(mk - M) : 0.f;
+    const float wwk = lwk > 0.f ? ex2(mwk - Mw) : 0.f;
+    float Ls = lk * wk, Lw = lwk * wwk;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+      Lw += __shfl_xor_sync(0xffffffffu, Lw, o);
+    }
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f), OW = O;
+#pragma unroll
+    for (int k = 0; k < MW; ++k) {
+      const float w = __shfl_sync(0xffffffffu, wk, k), ww = __shfl_sync(0xffffffffu, wwk, k);
+      if (k < WPH) {
         O = fma4(((const float4*)(to + (h * WPH + k) * D))[lane], w, O);
+        OW = fma4(((const float4*)(tow + (h * WPH + k) * D))[lane], ww, OW);
       }
     }
+    if (lane == 0) {
+      wmv[h] = Mw;
+      wlv[h] = Lw;
+    }
+    ((float4*)(wov + h * D))[lane] = OW;
     const float4 Y = scale4(O, Ls > 0.f ? 1.f / Ls : 0.f);
     float am = fmaxf(fmaxf(fabsf(Y.x), fabsf(Y.y)), fmaxf(fabsf(Y.z), fabsf(Y.w)));
 #pragma unroll
@@ -1075,7 +1103,7 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
     } else {
       ((float4*)(yo + h * D))[lane] = scale4(Y, up);
     }
-  } else if (unrot) {
+  } else if (unrot && warp < MAX_G) {
     // B operand rows of absent heads are 0
     *(uint2*)(yh + warp * (YST / 2) + 2 * lane) = make_uint2(0u, 0u);
     *(uint2*)(yl + warp * (YST / 2) + 2 * lane) = make_uint2(0u, 0u);
@@ -1084,26 +1112,30 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
   if (unrot) {
     if (!mbar_wait(mbar, 0)) record_error(cv.err, OSCAR_ERR_TIMEOUT);
     float d[4] = {0.f, 0.f, 0.f, 0.f};
+    if (warp < 8) {
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t bh0 = yh[gid * (YST / 2) + 8 * ks + tq], bh1 = yh[gid * (YST / 2) + 8 * ks + 4 + tq];
-      const uint32_t bl0 = yl[gid * (YST / 2) + 8 * ks + tq], bl1 = yl[gid * (YST / 2) + 8 * ks + 4 + tq];
-      const uint4 ah = Rf[rv_frag_index(0, warp, ks, lane) / 4];
-      const uint4 al = Rf[rv_frag_index(1, warp, ks, lane) / 4];
-      mma_f16(d, ah.x, ah.y, ah.z, ah.w, bh0, bh1);
-      mma_f16(d, ah.x, ah.y, ah.z, ah.w, bl0, bl1);
-      mma_f16(d, al.x, al.y, al.z, al.w, bh0, bh1);
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t bh0 = yh[gid * (YST / 2) + 8 * ks + tq], bh1 = yh[gid * (YST / 2) + 8 * ks + 4 + tq];
+        const uint32_t bl0 = yl[gid * (YST / 2) + 8 * ks + tq], bl1 = yl[gid * (YST / 2) + 8 * ks + 4 + tq];
+        const uint4 ah = Rf[rv_frag_index(0, warp, ks, lane) / 4];
+        const uint4 al = Rf[rv_frag_index(1, warp, ks, lane) / 4];
+        mma_f16(d, ah.x, ah.y, ah.z, ah.w, bh0, bh1);
+        mma_f16(d, ah.x, ah.y, ah.z, ah.w, bl0, bl1);
+        mma_f16(d, al.x, al.y, al.z, al.w, bh0, bh1);
+      }
     }
     __syncthreads();  // B operands consumed: yo may overwrite them
-    const int c = 16 * warp + gid;
-    yo[(2 * tq) * D + c] = d[0];
-    yo[(2 * tq + 1) * D + c] = d[1];
-    yo[(2 * tq) * D + c + 8] = d[2];
-    yo[(2 * tq + 1) * D + c + 8] = d[3];
+    if (warp < 8) {
+      const int c = 16 * warp + gid;
+      yo[(2 * tq) * D + c] = d[0];
+      yo[(2 * tq + 1) * D + c] = d[1];
+      yo[(2 * tq) * D + c + 8] = d[2];
+      yo[(2 * tq + 1) * D + c + 8] = d[3];
+    }
     __syncthreads();
   }
-  // ---- warp n: LSE-merge of history and window for head n
-  if (warp < G) {
+  // ---- warp n: LSE-merge of history and window for head h0 + n
+  if (warp < HPC) {
     const int h = warp;
     const float M = hM[h], Ls = hL[h], mw = wmv[h], lw = wlv[h];
     const float down = 1.f / ysc[h];
@@ -1124,7 +1156,7 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
       o[3] = fmaf(Oh.w, hw, Ow.w * fw) * inv;
       lse = (M2 + log2f(den)) * LN2;
     }
-    const size_t row = (size_t)b * cv.Hq + kvh * G + h;
+    const size_t row = (size_t)b * cv.Hq + kvh * G + h0 + h;
     __nv_bfloat162 o01 = __floats2bfloat162_rn(o[0], o[1]);
     __nv_bfloat162 o23 = __floats2bfloat162_rn(o[2], o[3]);
     uint2 pk;
@@ -1142,7 +1174,7 @@ __global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) dec
   constexpr bool BF16H = (IMPL == 2);
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheView& cv = a.cv;
-  const SmemLayout L = smem_layout(cv.head_bytes, a.B, IMPL);
+  const SmemLayout L = smem_layout(cv.head_bytes, a.B, IMPL, cv.G);
   uint64_t* mbar = (uint64_t*)(smem + L.off_mbar);
   float* qf = (float*)(smem + L.off_qf);  // CUDA-core path: [MAX_G][D] q' + [MAX_G][4] z weights
   float* vsw = (float*)(smem + L.off_vs);
@@ -1158,6 +1190,7 @@ __global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) dec
 
   pdl_launch_dependents();  // merge_kernel may be scheduled as CTAs of this grid retire
   if (threadIdx.x < NW * DEPTH) mbar_init(&mbar[threadIdx.x], 1);
+  uint8_t* qpk = smem + L.off_qpk;
   if (threadIdx.x == 0) misc[1] = 0;
   fence_proxy_async();
   __syncthreads();
@@ -1315,7 +1348,11 @@ __global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) dec
       };
       __syncthreads();  // the previous item's results in the stage area are consumed
       if (lane == 0) fence_proxy_async();
-      for (int k = 0; k < DEPTH && k < nw_pages; ++k) {
+      // the tensor-core paths issue their first page pair now (overlapping
+      // prep_kernel) and the rest once the packed query is in shared memory,
+      // so that its load does not queue behind a full wave of page copies
+      constexpr int EARLY = (IMPL == 1) ? DEPTH : 2;
+      for (int k = 0; k < EARLY && k < nw_pages; ++k) {
         const int pid = page_id_at(P, k);
         if (lane == 0) issue(k, pid);
       }
@@ -1328,6 +1365,19 @@ __global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) dec
       if constexpr (IMPL == 0 || IMPL == 3) {
         // IMPL 3: pages in pairs, two streams per tile (G <= 4)
         constexpr bool PAIR = (IMPL == 3);
+        // the kv head's G packed query records, copied to shared memory by warp
+        // 0 with coalesced 16-byte loads (every warp of every CTA reads them;
+        // scattered per-lane loads pile the whole grid onto a few L2 lines,
+        // and a bulk copy would queue behind this CTA's page copies)
+        if (warp == 0) {
+          const uint4* src = (const uint4*)(a.qpack + ((size_t)b * cv.Hq + kvh * G) * QPACK_BYTES);
+          for (int e = lane; e < G * QPACK_BYTES / 16; e += 32) ((uint4*)qpk)[e] = __ldcg(src + e);
+        }
+        for (int k = EARLY; k < DEPTH && k < nw_pages; ++k) {
+          const int pid = page_id_at(P, k);
+          if (lane == 0) issue(k, pid);
+        }
+        __syncthreads();
         Int2State<NG> S;
 #pragma unroll
         for (int j = 0; j < 8; ++j) S.oacc[j][0] = S.oacc[j][1] = S.oacc[j][2] = S.oacc[j][3] = 0.f;
@@ -1335,29 +1385,28 @@ __global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) dec
           // B column gid carries head gid (PAIR: head gid & 3 in both halves)
           const int qh = PAIR ? (gid & 3) : gid;
           const bool qv = qh < G;
-          const uint8_t* qrec = a.qpack + ((size_t)b * cv.Hq + kvh * G + (qv ? qh : 0)) * QPACK_BYTES;
-          const __half* qbh = (const __half*)qrec;
+          const __half* qbh = (const __half*)(qpk + (qv ? qh : 0) * QPACK_BYTES);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            S.bq[kk][0] = qv ? __ldcg((const unsigned int*)(qbh + 16 * kk + 2 * tq)) : 0u;
-            S.bq[kk][1] = qv ? __ldcg((const unsigned int*)(qbh + 16 * kk + 8 + 2 * tq)) : 0u;
+            S.bq[kk][0] = qv ? *(const unsigned int*)(qbh + 16 * kk + 2 * tq) : 0u;
+            S.bq[kk][1] = qv ? *(const unsigned int*)(qbh + 16 * kk + 8 + 2 * tq) : 0u;
           }
 #pragma unroll
           for (int hc = 0; hc < 2; ++hc) {
             const int n = PAIR ? ((2 * tq + hc) & 3) : 2 * tq + hc;
             const bool hv = n < G;
-            const uint8_t* r = a.qpack + ((size_t)b * cv.Hq + kvh * G + (hv ? n : 0)) * QPACK_BYTES;
+            const uint8_t* r = qpk + (hv ? n : 0) * QPACK_BYTES;
             S.m[hc] = PAIR ? -1e30f : -INFINITY;
             S.l[hc] = 0.f;
-            const float al = hv ? __ldcg((const float*)(r + QPACK_ALPHA)) : 0.f;
+            const float al = hv ? *(const float*)(r + QPACK_ALPHA) : 0.f;
             S.ka[hc] = al;
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
               float qs = 0.f, ps = 0.f;
 #pragma unroll
               for (int k = gr * (4 / NG); k < (gr + 1) * (4 / NG); ++k) {
-                qs += hv ? __ldcg((const float*)(r + QPACK_QSUM) + k) : 0.f;
-                ps += hv ? __ldcg((const float*)(r + QPACK_PSUM) + k) : 0.f;
+                qs += hv ? ((const float*)(r + QPACK_QSUM))[k] : 0.f;
+                ps += hv ? ((const float*)(r + QPACK_PSUM))[k] : 0.f;
               }
               S.bs[hc][gr] = 0.f;
               S.zs[hc][gr] = 0.f;
@@ -1371,8 +1420,8 @@ __global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) dec
           for (int k = 0; k < nw_pages; k += 2) {
             const bool hasB = k + 1 < nw_pages;
             const int sa = (int)((seq + k) % DEPTH), sb = (int)((seq + k + 1) % DEPTH);
-            bool ok = mbar_wait(&my_bar[sa], ((seq + k) / DEPTH) & 1u);
-            if (hasB && ok) ok = mbar_wait(&my_bar[sb], ((seq + k + 1) / DEPTH) & 1u);
+            bool ok = mbar_wait2(&my_bar[sa], ((seq + k) / DEPTH) & 1u, &my_bar[hasB ? sb : sa],
+                                 (hasB ? (seq + k + 1) / DEPTH : (seq + k) / DEPTH) & 1u);
             if (!__all_sync(0xffffffffu, ok)) {
               timed_out = true;
               k_fail = k;
@@ -1397,11 +1446,10 @@ __global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) dec
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
               if (k + u + DEPTH < nw_pages) {
+                // the stage's generic-proxy reads have completed (their values
+                // were consumed before __syncwarp): no proxy fence is needed
                 const int pid_next = page_id_at(P, k + u + DEPTH);
-                if (lane == 0) {
-                  fence_proxy_async();
-                  issue(k + u + DEPTH, pid_next);
-                }
+                if (lane == 0) issue(k + u + DEPTH, pid_next);
               }
             }
           }
@@ -1428,10 +1476,7 @@ __global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) dec
             __syncwarp();
             if (k + DEPTH < nw_pages) {
               const int pid_next = page_id_at(P, k + DEPTH);
-              if (lane == 0) {
-                fence_proxy_async();
-                issue(k + DEPTH, pid_next);
-              }
+              if (lane == 0) issue(k + DEPTH, pid_next);  // reads of the stage are complete
             }
           }
         }
@@ -1520,10 +1565,7 @@ __global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) dec
           __syncwarp();
           if (k + DEPTH < nw_pages) {
             const int pid_next = page_id_at(P, k + DEPTH);
-            if (lane == 0) {
-              fence_proxy_async();
-              issue(k + DEPTH, pid_next);
-            }
+            if (lane == 0) issue(k + DEPTH, pid_next);  // reads of the stage are complete
           }
         }
         if (timed_out) {
@@ -1564,7 +1606,7 @@ __global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) dec
 
 template <int NG, int IMPL>
 cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t st) {
-  const SmemLayout L = smem_layout(a.cv.head_bytes, a.B, IMPL);
+  const SmemLayout L = smem_layout(a.cv.head_bytes, a.B, IMPL, a.cv.G);
   if ((L.off_mbar % 8) || (L.off_stage % 128) || (L.off_pre % 16)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<NG, IMPL>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
@@ -1593,7 +1635,8 @@ cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t st) {
     configured = ML.total;
   }
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(a.B * a.cv.Hkv);
+  if (a.merge_hpc < 1 || a.cv.G % a.merge_hpc) return cudaErrorInvalidValue;
+  lc.gridDim = dim3(a.B * a.cv.Hkv * (a.cv.G / a.merge_hpc));
   lc.blockDim = dim3(MW * 32);
   lc.dynamicSmemBytes = ML.total;
   lc.stream = st;
@@ -1629,7 +1672,7 @@ size_t decode_scratch_bytes(int B, int Hq, int Hkv, int G, int max_target_items)
 template <int NG, int IMPL>
 int occupancy_t(const DecodeArgs& a) {
   static int cached_smem = -1, cached_occ = 0;
-  const SmemLayout L = smem_layout(a.cv.head_bytes, a.B, IMPL);
+  const SmemLayout L = smem_layout(a.cv.head_bytes, a.B, IMPL, a.cv.G);
   if (cached_smem == L.total) return cached_occ;
   if (cudaFuncSetAttribute(decode_kernel<NG, IMPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            L.total) != cudaSuccess) {

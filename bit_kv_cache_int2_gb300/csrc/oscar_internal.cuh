@@ -298,6 +298,36 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
+// Both phases complete (the two polls are issued together); false when the
+// wait ran out of its iteration budget.
+__device__ __forceinline__ bool mbar_wait2(uint64_t* bar0, uint32_t phase0, uint64_t* bar1,
+                                           uint32_t phase1) {
+  const uint32_t a0 = (uint32_t)__cvta_generic_to_shared(bar0);
+  const uint32_t a1 = (uint32_t)__cvta_generic_to_shared(bar1);
+  uint32_t done0 = 0, done1 = 0;
+  for (int it = 0; it < (1 << 22); ++it) {
+    uint32_t ok0 = 1, ok1 = 1;
+    if (!done0)
+      asm volatile(
+          "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+          " selp.u32 %0, 1, 0, p;\n}\n"
+          : "=r"(ok0)
+          : "r"(a0), "r"(phase0)
+          : "memory");
+    if (!done1)
+      asm volatile(
+          "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+          " selp.u32 %0, 1, 0, p;\n}\n"
+          : "=r"(ok1)
+          : "r"(a1), "r"(phase1)
+          : "memory");
+    done0 |= ok0;
+    done1 |= ok1;
+    if (done0 && done1) return true;
+  }
+  return false;
+}
+
 // Returns false when the wait ran out of its iteration budget.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase) {
   uint32_t a = (uint32_t)__cvta_generic_to_shared(bar);
@@ -352,7 +382,7 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
   // total history pages (over requests), times Hkv
   long long local = 0;
   for (int b = tid; b < B; b += blockDim.x) local += (hist_lens[b] + PAGE - 1) / PAGE;
-  // block reduce (red: >= 32 ints)
+  // block reduce (red: one int per warp)
   for (int o = 16; o; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
   if ((tid & 31) == 0) red[tid >> 5] = (int)local;
   __syncthreads();
@@ -433,8 +463,9 @@ struct DecodeArgs {
   int* done;               // scratch [B][Hkv] finished-item counters
   int B;
   int target_items;
-  int impl;  // 0 tensor-core, 1 CUDA-core
+  int impl;  // decode kernel variant: 0 tensor-core, 1 CUDA-core, 3 tensor-core page pairs
   int bf16_history;
+  int merge_hpc;  // query heads per merge CTA (divides G)
   LayerRot rot;
 };
 
