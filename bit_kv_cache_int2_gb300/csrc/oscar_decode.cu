@@ -1437,10 +1437,9 @@ __global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) dec
             const int nvb = okb ? ((pb == pages_b - 1) ? hist_b - pb * PAGE : PAGE) : 0;
             const uint8_t* sta = my_stage + (size_t)sa * L.stage_bytes;
             const uint8_t* stb = hasB ? my_stage + (size_t)sb * L.stage_bytes : sta;
-            if (nva == PAGE && nvb == PAGE)
-              int2_pair_mma<NG, true>(S, sta, nva, stb, nvb, true, lane, mA);
-            else if (nva > 0 || nvb > 0)
-              int2_pair_mma<NG, false>(S, sta, nva, stb, nvb, hasB, lane, mA);
+            // one (masked) variant for full and partial pages keeps the
+            // unrolled loop body small enough for the instruction cache
+            if (nva > 0 || nvb > 0) int2_pair_mma<NG, false>(S, sta, nva, stb, nvb, hasB, lane, mA);
             if ((k & 7) == 6) flush_v_offset<NG>(S);
             __syncwarp();
 #pragma unroll
