@@ -107,6 +107,7 @@ int decode_ctas(const oscar_ctx* ctx, int batch, bool bf16_history) {
   DecodeArgs a = {};
   a.cv.head_bytes = bf16_history ? BF16_HEAD_BYTES : int2_head_bytes(ctx->cfg.group_size);
   a.cv.NG = ctx->NG;
+  a.cv.G = ctx->G;
   a.B = batch;
   a.impl = kernel_impl(ctx);
   a.bf16_history = bf16_history ? 1 : 0;
@@ -246,9 +247,13 @@ LayerRot layer_rot(const oscar_ctx* ctx, int layer) {
   return r;
 }
 
+thread_local int g_last_cuda_error = 0;
+
 oscar_status cuda_status(cudaError_t e) {
-  if (e != cudaSuccess) (void)cudaGetLastError();  // leave no stale error for the next call
-  return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+  if (e == cudaSuccess) return OSCAR_OK;
+  g_last_cuda_error = (int)e;
+  (void)cudaGetLastError();  // leave no stale error for the next call
+  return OSCAR_ERR_CUDA;
 }
 
 oscar_status decode_common(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* q,
@@ -563,6 +568,8 @@ oscar_status oscar_debug_rotate(oscar_ctx* ctx, int layer, int which, int kv_hea
   return cuda_status(launch_debug_rotate(U, r.mode, (const __nv_bfloat16*)x, x_rot, n,
                                          (cudaStream_t)stream));
 }
+
+int oscar_last_cuda_error(void) { return g_last_cuda_error; }
 
 oscar_status oscar_get_error(oscar_ctx* ctx, oscar_stream_t stream, int* code) {
   if (!ctx || !code) return OSCAR_ERR_INVALID_ARG;

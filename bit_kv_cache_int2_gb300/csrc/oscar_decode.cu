@@ -34,10 +34,6 @@ constexpr int YST = 136;      // fp16 row stride of the mma B operand (conflict-
 constexpr int MERGE_RV_BYTES = RV_FRAG_WORDS * 4;
 constexpr int MERGE_Y_BYTES = 2 * MAX_G * YST * 2 > MAX_G * D * 4 ? 2 * MAX_G * YST * 2 : MAX_G * D * 4;
 
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-}
 
 // Per (request, query head) record of the packed query (QPACK_BYTES):
 //   half  qb[128]   q'_c * 2^-sigma * 2^(8 - E(c)), the QK^T B operand
@@ -55,27 +51,31 @@ constexpr int QPACK_ALPHA = 256, QPACK_QSUM = 260, QPACK_PSUM = 276;
 // sigma comes from |q|, which bounds every |q'_c| (R_K is orthogonal), so the
 // four CTAs of a head agree on it without talking to each other.
 __global__ void __launch_bounds__(128) prep_kernel(DecodeArgs a) {
-  pdl_launch_dependents();
   __shared__ float xs[MAX_G][D];
   __shared__ float part[4][MAX_G][32];
   __shared__ float nrm[MAX_G];
   const CacheView& cv = a.cv;
   const int bk = blockIdx.x, cq = blockIdx.y;
   const int b = bk / cv.Hkv, kvh = bk % cv.Hkv, t = threadIdx.x, w = t >> 5, lane = t & 31;
-  if (t == 0 && cq == 0 && bk == 0) *a.counter = 0;
-  if (a.bf16_history) return;
   const int G = cv.G;
   const int c = 32 * cq + lane;
-  // R_K loads first (independent of q); this CTA's quarter of the merge's
-  // R_V fragments into L2
+  // rotation-table loads first (written synchronously by oscar_set_rotation):
+  // R_K, and this CTA's quarter of the merge's R_V fragments into L2
   float r[32];
-  {
+  if (!a.bf16_history) {
     const float* R = a.rot.R_K + (size_t)kvh * D * D + (size_t)(32 * w) * D + c;
 #pragma unroll
     for (int k = 0; k < 32; ++k) r[k] = __ldg(R + k * D);
     const char* rv = (const char*)(a.rot.RV_frag + (size_t)kvh * RV_FRAG_WORDS) + (size_t)(cq * 128 + t) * 128;
     asm volatile("prefetch.global.L2 [%0];\n" ::"l"(rv));
   }
+  // q, the cache state and the counters belong to earlier stream work (the
+  // append or the previous decode): wait for it, then let decode_kernel start
+  // its pre-wait work (it reads the cache state)
+  pdl_wait();
+  pdl_launch_dependents();
+  if (t == 0 && cq == 0 && bk == 0) *a.counter = 0;
+  if (a.bf16_history) return;
   const __nv_bfloat16* qg = a.q + ((size_t)b * cv.Hq + kvh * G) * D;
   for (int e = t; e < G * D; e += 128) xs[e / D][e % D] = __bfloat162float(qg[e]);
   __syncthreads();
@@ -960,6 +960,7 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
   int* red = (int*)(smem + ML.off_red);
   int* pre = (int*)(smem + ML.off_pre);
   const bool unrot = !a.bf16_history && a.rot.mode != OSCAR_ROT_NONE;
+  pdl_launch_dependents();  // the next stream work waits for this grid before it reads
   if (t == 0) mbar_init(mbar, 1);
   fence_proxy_async();
   __syncthreads();
@@ -1603,29 +1604,32 @@ __global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) dec
   if (!waited) pdl_wait();
 }
 
+// Raise decode_kernel<NG, IMPL>'s dynamic shared-memory limit to `bytes` if it
+// is lower (never lowered: launches and occupancy queries of other sizes
+// share it).
+template <int NG, int IMPL>
+cudaError_t ensure_decode_smem(int bytes) {
+  static int current = -1;
+  if (bytes <= current) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(decode_kernel<NG, IMPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) current = bytes;
+  return e;
+}
+
 template <int NG, int IMPL>
 cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t st) {
   const SmemLayout L = smem_layout(a.cv.head_bytes, a.B, IMPL, a.cv.G);
-  if ((L.off_mbar % 8) || (L.off_stage % 128) || (L.off_pre % 16)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<NG, IMPL>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  if ((L.off_mbar % 8) || (L.off_stage % 128) || (L.off_pre % 16) || (L.off_qpk % 16)) return cudaErrorInvalidValue;
+  const cudaError_t e = ensure_decode_smem<NG, IMPL>(L.total);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(grid);
-  lc.blockDim = dim3(NW * 32);
-  lc.dynamicSmemBytes = L.total;
-  lc.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, decode_kernel<NG, IMPL>, a);
+  return launch_pdl(decode_kernel<NG, IMPL>, dim3(grid), dim3(NW * 32), L.total, st, a);
 }
 
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t st) {
   const MergeLayout ML = merge_layout(a.B);
   if ((ML.off_mbar % 8) || (ML.off_y % 16) || (ML.off_to % 16) || (ML.off_wo % 16)) return cudaErrorInvalidValue;
+  if (a.merge_hpc < 1 || a.cv.G % a.merge_hpc) return cudaErrorInvalidValue;
   static int configured = -1;  // dynamic shared memory size the kernel was last configured for
   if (configured < ML.total) {
     const cudaError_t e =
@@ -1633,18 +1637,7 @@ cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured = ML.total;
   }
-  cudaLaunchConfig_t lc = {};
-  if (a.merge_hpc < 1 || a.cv.G % a.merge_hpc) return cudaErrorInvalidValue;
-  lc.gridDim = dim3(a.B * a.cv.Hkv * (a.cv.G / a.merge_hpc));
-  lc.blockDim = dim3(MW * 32);
-  lc.dynamicSmemBytes = ML.total;
-  lc.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, merge_kernel, a);
+  return launch_pdl(merge_kernel, dim3(a.B * a.cv.Hkv * (a.cv.G / a.merge_hpc)), dim3(MW * 32), ML.total, st, a);
 }
 
 }  // namespace
@@ -1673,8 +1666,7 @@ int occupancy_t(const DecodeArgs& a) {
   static int cached_smem = -1, cached_occ = 0;
   const SmemLayout L = smem_layout(a.cv.head_bytes, a.B, IMPL, a.cv.G);
   if (cached_smem == L.total) return cached_occ;
-  if (cudaFuncSetAttribute(decode_kernel<NG, IMPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           L.total) != cudaSuccess) {
+  if (ensure_decode_smem<NG, IMPL>(L.total) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
   }
@@ -1700,9 +1692,8 @@ int decode_ctas_per_sm(const DecodeArgs& a) {
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof) {
   const CacheView& cv = a.cv;
   prof_begin(prof, OSCAR_KERNEL_DECODE_PREP, st);
-  prep_kernel<<<dim3(a.B * cv.Hkv, 4), 128, 0, st>>>(a);
+  cudaError_t e = launch_pdl(prep_kernel, dim3(a.B * cv.Hkv, 4), dim3(128), 0, st, a);
   prof_end(prof, OSCAR_KERNEL_DECODE_PREP, st);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_begin(prof, OSCAR_KERNEL_DECODE_MAIN, st);
   if (a.bf16_history) {

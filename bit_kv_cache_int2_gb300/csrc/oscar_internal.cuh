@@ -10,6 +10,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/oscar.h"
 
 namespace oscar {
@@ -284,6 +286,34 @@ __host__ __device__ constexpr int code_exp() {
 }
 __host__ __device__ __forceinline__ int code_exp_rt(int i) {
   return (i == 0 || i == 2 || i == 5) ? 4 : (i == 1 || i == 3 || i == 6) ? 6 : 8;
+}
+
+// ------------------------------------------- programmatic dependent launch
+// Every hot-path kernel is launched as a programmatic dependent of the work
+// before it on the stream.  A kernel waits (griddepcontrol.wait) before it
+// reads anything earlier stream work may still write, and signals its own
+// dependents (griddepcontrol.launch_dependents) only once their pre-wait work
+// is safe: the rotation table, written synchronously by oscar_set_rotation,
+// may be read before the wait.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...);
 }
 
 // ----------------------------------------------------- bounded mbarrier use

@@ -63,13 +63,17 @@ __global__ void __launch_bounds__(512) append_kernel(CacheView cv, LayerRot rot,
   __shared__ int st[6];
   const int b = blockIdx.x / cv.Hkv, h = blockIdx.x % cv.Hkv, isv = blockIdx.y;
   const int t = threadIdx.x, j = t & 127, pp = t >> 7;
-  // U's loads do not depend on the cache state: start them first
+  // U's loads do not depend on earlier stream work: start them first
   float u[32];
   if (rot.mode == OSCAR_ROT_OSCAR) {
     const float* U = (isv ? rot.U_V : rot.U_K) + (size_t)h * D * D + (size_t)(32 * pp) * D + j;
 #pragma unroll
     for (int k = 0; k < 32; ++k) u[k] = __ldg(U + k * D);
   }
+  // the new tokens, the lengths and the cache belong to earlier stream work;
+  // the decode's prep_kernel waits for this grid before it reads anything
+  pdl_wait();
+  pdl_launch_dependents();
   if (t == 0) {
     const int L = cv.seq_lens[b], H = cv.hist_lens[b];
     const int recent = L > SINK ? L - SINK - H : 0;
@@ -377,9 +381,10 @@ cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_b
                           const __nv_bfloat16* v, int B, int do_append, int* req_counter,
                           cudaStream_t st, Profiler* prof) {
   prof_begin(prof, OSCAR_KERNEL_APPEND, st);
-  append_kernel<<<dim3(B * cv.Hkv, 2), 512, 0, st>>>(cv, rot, k, v, do_append, req_counter);
+  const cudaError_t e =
+      launch_pdl(append_kernel, dim3(B * cv.Hkv, 2), dim3(512), 0, st, cv, rot, k, v, do_append, req_counter);
   prof_end(prof, OSCAR_KERNEL_APPEND, st);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_import(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* K,

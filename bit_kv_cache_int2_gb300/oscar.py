@@ -99,6 +99,7 @@ _SIGS = {
     "oscar_debug_rotate": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                             ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
     "oscar_get_error": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
+    "oscar_last_cuda_error": ([], ctypes.c_int),
     "oscar_profile_enable": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "oscar_profile_read": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                             ctypes.POINTER(ctypes.c_double), ctypes.c_int], ctypes.c_int),
@@ -133,6 +134,8 @@ def lib():
 
 def _check(st: int, where: str):
     if st != OK:
+        if st == ERR_CUDA:
+            where = f"{where} [cudaError {lib().oscar_last_cuda_error()}]"
         raise OscarError(st, where)
 
 

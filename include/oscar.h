@@ -309,6 +309,11 @@ oscar_status oscar_debug_rotate(oscar_ctx* ctx, int layer, int which,
  * the last call in *code (OSCAR_OK if none) and clear it. */
 oscar_status oscar_get_error(oscar_ctx* ctx, oscar_stream_t stream, int* code);
 
+/* The CUDA runtime error code (a cudaError_t value) behind the most recent
+ * OSCAR_ERR_CUDA returned to the calling host thread, 0 if there was none.
+ * The pages describe no error reporting; this is the library's own. */
+int oscar_last_cuda_error(void);
+
 /* Kernel timing (tracing).  The pages describe no profiler; this is the
  * library's own instrumentation.  While enabled, every kernel the context
  * launches is bracketed by a pair of CUDA events recorded on the launching
