@@ -237,6 +237,34 @@ def oscar_decode(ctx, layer, cache: dict, q, out, lse, scratch, batch, stream=No
            "oscar_decode")
 
 
+def bind_append(ctx, layer, cache: dict, batch, stream=None):
+    """oscar_append with the cache and stream marshalled once, for tight loops:
+    returns f(k_new_ptr, v_new_ptr) taking raw device addresses (ints)."""
+    cs = _cache_struct(cache)
+    csr, st, fn = ctypes.byref(cs), _stream(stream), lib().oscar_append
+
+    def call(k_ptr: int, v_ptr: int):
+        _check(fn(ctx, layer, csr, ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr), batch, st), "oscar_append")
+
+    call._keep = cs  # the struct must outlive the closure's byref
+    return call
+
+
+def bind_decode(ctx, layer, cache: dict, q, out, lse, scratch, batch, stream=None):
+    """oscar_decode with every argument marshalled once, for tight loops:
+    returns a no-argument callable."""
+    cs = _cache_struct(cache)
+    args = (ctx, layer, ctypes.byref(cs), _ptr(q), _ptr(out), _ptr(lse), _ptr(scratch),
+            scratch.numel() * scratch.element_size(), batch, _stream(stream))
+    fn = lib().oscar_decode
+
+    def call():
+        _check(fn(*args), "oscar_decode")
+
+    call._keep = cs
+    return call
+
+
 def oscar_decode_noalloc(ctx, layer, cache: dict, q, out, lse, batch, stream=None):
     """oscar_decode with the library's own built-in working memory: the caller
     passes no scratch and nothing is allocated."""
