@@ -53,7 +53,7 @@ struct oscar_ctx {
   int device = 0;
   int num_sms = 0;
   int G = 0, NG = 0;
-  float* d_rot = nullptr;  // [layers][4][Hkv][128 * 128 words]: U_K, U_V, R_K, R_V fragments
+  float* d_rot = nullptr;  // [layers][3][Hkv][128 * 128 words]: R_K, R_V, R_V fragments
   float* d_clip = nullptr;  // [layers][2][Hkv]
   std::vector<int> mode;
   int* d_err = nullptr;
@@ -155,7 +155,7 @@ CacheView make_view(const oscar_ctx* ctx, const oscar_cache* c, bool bf16_histor
   return v;
 }
 
-constexpr int ROT_MATS = 4;  // U_K, U_V, R_K, R_V fragments per layer
+constexpr int ROT_MATS = 3;  // R_K, R_V, R_V fragments per layer
 static_assert(RV_FRAG_WORDS == D * D, "R_V fragments fill one matrix slot");
 
 // R = U·H·P_br (OSCAR), H (HADAMARD) or I (NONE) for one head, in fp64, in the
@@ -213,7 +213,8 @@ void pack_rv_fragments(const double* R, uint32_t* out) {
 }
 
 // One layer's table (ROT_MATS matrices of Hkv heads) from the eigenbases
-// (nullptr outside OSCAR mode: identity).
+// (nullptr outside OSCAR mode: identity): R_K, R_V in fp32, then R_V as fp16
+// high/low mma fragments.
 void build_layer_table(const float* U_K, const float* U_V, int mode, int Hkv, std::vector<float>& out) {
   const size_t hm = (size_t)D * D, mat = (size_t)Hkv * hm;
   out.assign(ROT_MATS * mat, 0.f);
@@ -221,15 +222,10 @@ void build_layer_table(const float* U_K, const float* U_V, int mode, int Hkv, st
   for (int h = 0; h < Hkv; ++h) {
     for (int t = 0; t < 2; ++t) {
       const float* U = mode == OSCAR_ROT_OSCAR ? (t == 0 ? U_K : U_V) + h * hm : nullptr;
-      float* dst = out.data() + t * mat + h * hm;
-      for (size_t e = 0; e < hm; ++e) dst[e] = U ? U[e] : ((e / D) == (e % D) ? 1.f : 0.f);
       compose_rotation(U, mode, R.data());
-      if (t == 0) {
-        float* rk = out.data() + 2 * mat + h * hm;
-        for (size_t e = 0; e < hm; ++e) rk[e] = (float)R[e];
-      } else {
-        pack_rv_fragments(R.data(), (uint32_t*)(out.data() + 3 * mat + h * hm));
-      }
+      float* dst = out.data() + t * mat + h * hm;
+      for (size_t e = 0; e < hm; ++e) dst[e] = (float)R[e];
+      if (t == 1) pack_rv_fragments(R.data(), (uint32_t*)(out.data() + 2 * mat + h * hm));
     }
   }
 }
@@ -237,10 +233,9 @@ void build_layer_table(const float* U_K, const float* U_V, int mode, int Hkv, st
 LayerRot layer_rot(const oscar_ctx* ctx, int layer) {
   const size_t mat = (size_t)ctx->cfg.num_kv_heads * D * D;
   LayerRot r;
-  r.U_K = ctx->d_rot + (size_t)layer * ROT_MATS * mat;
-  r.U_V = r.U_K + mat;
-  r.R_K = r.U_V + mat;
-  r.RV_frag = (const uint32_t*)(r.R_K + mat);
+  r.R_K = ctx->d_rot + (size_t)layer * ROT_MATS * mat;
+  r.R_V = r.R_K + mat;
+  r.RV_frag = (const uint32_t*)(r.R_V + mat);
   r.clip_k = ctx->d_clip + (size_t)layer * 2 * ctx->cfg.num_kv_heads;
   r.clip_v = r.clip_k + ctx->cfg.num_kv_heads;
   r.mode = ctx->mode[layer];
@@ -564,8 +559,8 @@ oscar_status oscar_debug_rotate(oscar_ctx* ctx, int layer, int which, int kv_hea
   if (kv_head < 0 || kv_head >= ctx->cfg.num_kv_heads) return OSCAR_ERR_INVALID_ARG;
   if (n == 0) return OSCAR_OK;
   const LayerRot r = layer_rot(ctx, layer);
-  const float* U = (which == 0 ? r.U_K : r.U_V) + (size_t)kv_head * D * D;
-  return cuda_status(launch_debug_rotate(U, r.mode, (const __nv_bfloat16*)x, x_rot, n,
+  const float* R = (which == 0 ? r.R_K : r.R_V) + (size_t)kv_head * D * D;
+  return cuda_status(launch_debug_rotate(R, (const __nv_bfloat16*)x, x_rot, n,
                                          (cudaStream_t)stream));
 }
 

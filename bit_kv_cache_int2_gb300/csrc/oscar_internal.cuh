@@ -47,16 +47,14 @@ __host__ __device__ __forceinline__ int rv_frag_index(int part, int mt, int ks, 
   return (((part * 8 + mt) * 8 + ks) * 32 + lane) * 4;
 }
 
-// Per-layer rotation table.  U_K, U_V: the eigenbases (identity outside
-// OSCAR mode) for the demotion path, which applies U, then H, then P_br.
-// R_K = rotation(U_K, mode) composed in fp64 on the host, for the query;
-// RV_frag: R_V = rotation(U_V, mode) as fp16 high/low fragments, for the
+// Per-layer rotation table, composed in fp64 on the host from the eigenbases:
+// R_K = rotation(U_K, mode) and R_V = rotation(U_V, mode) in fp32 for the
+// demotion and the query, and R_V again as fp16 high/low fragments for the
 // output.
 struct LayerRot {
-  const float* U_K;         // [Hkv][128][128]  x' = x·U·H·P
-  const float* U_V;         // [Hkv][128][128]
-  const float* R_K;         // [Hkv][128][128]  q' = q·R_K
-  const uint32_t* RV_frag;  // [Hkv][RV_FRAG_WORDS]
+  const float* R_K;         // [Hkv][128][128]  k' = k·R_K, q' = q·R_K
+  const float* R_V;         // [Hkv][128][128]  v' = v·R_V
+  const uint32_t* RV_frag;  // [Hkv][RV_FRAG_WORDS]  o = o'·R_V^T
   const float* clip_k;      // [Hkv]
   const float* clip_v;      // [Hkv]
   int mode;
@@ -82,6 +80,13 @@ struct CacheView {
 // Release/acquire fence at GPU scope (lighter than a sequentially consistent one).
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;\n" ::: "memory"); }
 
+// atomicAdd with acquire-release semantics at GPU scope.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;\n" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void record_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
@@ -106,56 +111,6 @@ __device__ __forceinline__ void group_sync(int bar) {
 }
 
 __device__ __forceinline__ int bitrev7(int j) { return (int)(__brev((unsigned)j) >> 25); }
-
-// y = x·H for the normalised Sylvester Hadamard of order 128, one element per
-// thread (channel j = thread index in the group).  tmp: 128 floats of smem.
-__device__ __forceinline__ float fwht128(float v, int j, float* tmp, int bar) {
-#pragma unroll
-  for (int h = 1; h < 32; h <<= 1) {
-    float o = __shfl_xor_sync(0xffffffffu, v, h);
-    v = (j & h) ? (o - v) : (v + o);
-  }
-#pragma unroll
-  for (int h = 32; h < 128; h <<= 1) {
-    tmp[j] = v;
-    group_sync(bar);
-    float o = tmp[j ^ h];
-    group_sync(bar);
-    v = (j & h) ? (o - v) : (v + o);
-  }
-  return v * INV_SQRT_D;
-}
-
-// x' = x·R for R = U·H·P_br (OSCAR), H (HADAMARD) or I (NONE), one channel
-// per thread [News, "OSCAR 的不同之处"].  x_s: the input vector in smem
-// (read only); U: [128][128] row-major in global memory; tmp: 128 floats smem.
-// Returns x'_j for j = thread index in the group.
-__device__ __forceinline__ float rotate128(const float* x_s, const float* U, int mode, int j,
-                                           float* tmp, int bar) {
-  if (mode == OSCAR_ROT_NONE) return x_s[j];
-  float t;
-  if (mode == OSCAR_ROT_OSCAR) {
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 4
-    for (int i = 0; i < D; i += 4) {
-      a0 = fmaf(x_s[i + 0], __ldg(U + (i + 0) * D + j), a0);
-      a1 = fmaf(x_s[i + 1], __ldg(U + (i + 1) * D + j), a1);
-      a2 = fmaf(x_s[i + 2], __ldg(U + (i + 2) * D + j), a2);
-      a3 = fmaf(x_s[i + 3], __ldg(U + (i + 3) * D + j), a3);
-    }
-    t = (a0 + a1) + (a2 + a3);
-  } else {
-    t = x_s[j];
-  }
-  t = fwht128(t, j, tmp, bar);
-  if (mode == OSCAR_ROT_OSCAR) {
-    tmp[j] = t;
-    group_sync(bar);
-    t = tmp[bitrev7(j)];
-    group_sync(bar);
-  }
-  return t;
-}
 
 // --------------------------------------------------------------- quantiser
 // [Blog, pipeline figure paragraph: rotate -> clip -> quantize -> pack].
@@ -517,7 +472,7 @@ cudaError_t launch_import(const CacheView& cv, const LayerRot& rot, const __nv_b
                           cudaStream_t st, Profiler* prof);
 cudaError_t launch_quantize_hook(const float* x, int n, int g, float clip, int which,
                                  uint8_t* codes, __half2* sz, cudaStream_t st);
-cudaError_t launch_debug_rotate(const float* U, int mode, const __nv_bfloat16* x, float* y,
-                                int n, cudaStream_t st);
+cudaError_t launch_debug_rotate(const float* R, const __nv_bfloat16* x, float* y, int n,
+                                cudaStream_t st);
 
 }  // namespace oscar

@@ -49,26 +49,25 @@ __device__ __forceinline__ void quant_store_v_global(float y, int j, int g, floa
 
 // ------------------------------------------------------------------ append
 // grid = (B * Hkv, 2): blockIdx.y = 0 handles K, 1 handles V.  block = 512:
-// four parts of 128 threads split the rotation's 128-row matvec so that all
-// of U's loads are in flight at once; threads 0..127 then finish the token.
+// four parts of 128 threads split the 128-row matvec x·R so that all of R's
+// loads are in flight at once; threads 0..127 then finish the token.
 __global__ void __launch_bounds__(512) append_kernel(CacheView cv, LayerRot rot,
                                                      const __nv_bfloat16* __restrict__ knew,
                                                      const __nv_bfloat16* __restrict__ vnew,
                                                      int do_append, int* req_counter) {
   __shared__ float xs[D];
   __shared__ float part[4][D];
-  __shared__ float tmp[D];
   __shared__ float red[8];
   __shared__ uint32_t kw[8];
   __shared__ int st[6];
   const int b = blockIdx.x / cv.Hkv, h = blockIdx.x % cv.Hkv, isv = blockIdx.y;
   const int t = threadIdx.x, j = t & 127, pp = t >> 7;
-  // U's loads do not depend on earlier stream work: start them first
+  // R's loads do not depend on earlier stream work: start them first
   float u[32];
-  if (rot.mode == OSCAR_ROT_OSCAR) {
-    const float* U = (isv ? rot.U_V : rot.U_K) + (size_t)h * D * D + (size_t)(32 * pp) * D + j;
+  {
+    const float* R = (isv ? rot.R_V : rot.R_K) + (size_t)h * D * D + (size_t)(32 * pp) * D + j;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) u[k] = __ldg(U + k * D);
+    for (int k = 0; k < 32; ++k) u[k] = __ldg(R + k * D);
   }
   // the new tokens, the lengths and the cache belong to earlier stream work;
   // the decode's prep_kernel waits for this grid before it reads anything
@@ -114,25 +113,12 @@ __global__ void __launch_bounds__(512) append_kernel(CacheView cv, LayerRot rot,
     if (t < D) xs[t] = __bfloat162float(ring[(head * RECENT + ring_slot) * D + t]);
     __syncthreads();
     float acc = 0.f;
-    if (rot.mode == OSCAR_ROT_OSCAR) {
 #pragma unroll
-      for (int k = 0; k < 32; ++k) acc = fmaf(xs[32 * pp + k], u[k], acc);
-    } else if (pp == 0) {
-      acc = xs[j];
-    }
+    for (int k = 0; k < 32; ++k) acc = fmaf(xs[32 * pp + k], u[k], acc);
     part[pp][j] = acc;
     __syncthreads();
     if (pp == 0) {
-      float y = (part[0][j] + part[1][j]) + (part[2][j] + part[3][j]);
-      if (rot.mode != OSCAR_ROT_NONE) {
-        y = fwht128(y, j, tmp, 1);
-        if (rot.mode == OSCAR_ROT_OSCAR) {
-          tmp[j] = y;
-          group_sync(1);
-          y = tmp[bitrev7(j)];
-          group_sync(1);
-        }
-      }
+      const float y = (part[0][j] + part[1][j]) + (part[2][j] + part[3][j]);
       const float clip = (isv ? rot.clip_v : rot.clip_k)[h];
       uint8_t* blk = cv.pool + (size_t)page * cv.page_bytes + (size_t)h * cv.head_bytes;
       const int tr = H % PAGE;
@@ -162,10 +148,10 @@ __global__ void __launch_bounds__(512) append_kernel(CacheView cv, LayerRot rot,
   // request has read the old lengths before it increments the counter.
   __syncthreads();
   if (t == 0) {
-    fence_acq_rel_gpu();  // this CTA's reads of the old lengths come before the count
-    const int old = atomicAdd(&req_counter[b], 1);
+    // release: this CTA's reads of the old lengths come before the count;
+    // acquire: the last CTA writes the lengths after every CTA's reads
+    const int old = atomic_add_acq_rel_gpu(&req_counter[b], 1);
     if (old == 2 * cv.Hkv - 1) {
-      fence_acq_rel_gpu();
       req_counter[b] = 0;
       if (ok) {
         cv.seq_lens[b] = L + (do_append ? 1 : 0);
@@ -232,7 +218,6 @@ __global__ void __launch_bounds__(256) import_int2_pages_kernel(CacheView cv, La
                                                                 const __nv_bfloat16* __restrict__ V,
                                                                 int n) {
   __shared__ float xs[2][IMP_NT][D];
-  __shared__ float tmp[2][D];
   __shared__ float red[2][8];
   __shared__ __align__(16) uint32_t kwords[PAGE * 8];
   __shared__ __align__(16) uint32_t vwords[D * 4];
@@ -252,7 +237,7 @@ __global__ void __launch_bounds__(256) import_int2_pages_kernel(CacheView cv, La
   for (int i = threadIdx.x; i < 2 * PAGE * 4; i += 256) (&szs[0][0])[i] = __halves2half2(__float2half(0.f), __float2half(0.f));
   const size_t head = (size_t)(b * cv.Hkv + h);
   const __nv_bfloat16* src = (grp == 0 ? K : V) + (head * (size_t)n + SINK + t0) * D;
-  const float* U = (grp == 0 ? rot.U_K : rot.U_V) + (size_t)h * D * D;
+  const float* R = (grp == 0 ? rot.R_K : rot.R_V) + (size_t)h * D * D;
   const float clip = (grp == 0 ? rot.clip_k : rot.clip_v)[h];
   __syncthreads();
   for (int tb = 0; tb < nt; tb += IMP_NT) {
@@ -261,29 +246,15 @@ __global__ void __launch_bounds__(256) import_int2_pages_kernel(CacheView cv, La
       xs[grp][k][j] = k < cnt ? __bfloat162float(src[(size_t)(tb + k) * D + j]) : 0.f;
     group_sync(bar);
     float acc[IMP_NT];
-    if (rot.mode == OSCAR_ROT_OSCAR) {
 #pragma unroll
-      for (int k = 0; k < IMP_NT; ++k) acc[k] = 0.f;
-      for (int i = 0; i < D; ++i) {
-        const float u = __ldg(U + i * D + j);
+    for (int k = 0; k < IMP_NT; ++k) acc[k] = 0.f;
+    for (int i = 0; i < D; ++i) {
+      const float r = __ldg(R + i * D + j);
 #pragma unroll
-        for (int k = 0; k < IMP_NT; ++k) acc[k] = fmaf(xs[grp][k][i], u, acc[k]);
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < IMP_NT; ++k) acc[k] = xs[grp][k][j];
+      for (int k = 0; k < IMP_NT; ++k) acc[k] = fmaf(xs[grp][k][i], r, acc[k]);
     }
     for (int k = 0; k < cnt; ++k) {
-      float y = acc[k];
-      if (rot.mode != OSCAR_ROT_NONE) {
-        y = fwht128(y, j, tmp[grp], bar);
-        if (rot.mode == OSCAR_ROT_OSCAR) {
-          tmp[grp][j] = y;
-          group_sync(bar);
-          y = tmp[grp][bitrev7(j)];
-          group_sync(bar);
-        }
-      }
+      const float y = acc[k];
       const int t = tb + k;
       quant_pack(y, j, cv.g, clip, red[grp], bar, grp == 1, t, kwords + t * 8, vwords,
                  &szs[grp][t * cv.NG]);
@@ -363,16 +334,18 @@ __global__ void __launch_bounds__(128) quantize_hook_kernel(const float* __restr
   }
 }
 
-// grid = n, block 128
-__global__ void __launch_bounds__(128) debug_rotate_kernel(const float* __restrict__ U, int mode,
+// grid = n, block 128: y = x·R, thread j = output channel j
+__global__ void __launch_bounds__(128) debug_rotate_kernel(const float* __restrict__ R,
                                                            const __nv_bfloat16* __restrict__ x,
                                                            float* __restrict__ y) {
   __shared__ float xs[D];
-  __shared__ float tmp[D];
   const int j = threadIdx.x;
   xs[j] = __bfloat162float(x[(size_t)blockIdx.x * D + j]);
   __syncthreads();
-  y[(size_t)blockIdx.x * D + j] = rotate128(xs, U, mode, j, tmp, 1);
+  float acc = 0.f;
+#pragma unroll 8
+  for (int i = 0; i < D; ++i) acc = fmaf(xs[i], __ldg(R + i * D + j), acc);
+  y[(size_t)blockIdx.x * D + j] = acc;
 }
 
 }  // namespace
@@ -416,9 +389,9 @@ cudaError_t launch_quantize_hook(const float* x, int n, int g, float clip, int w
   return cudaGetLastError();
 }
 
-cudaError_t launch_debug_rotate(const float* U, int mode, const __nv_bfloat16* x, float* y, int n,
+cudaError_t launch_debug_rotate(const float* R, const __nv_bfloat16* x, float* y, int n,
                                 cudaStream_t st) {
-  debug_rotate_kernel<<<n, 128, 0, st>>>(U, mode, x, y);
+  debug_rotate_kernel<<<n, 128, 0, st>>>(R, x, y);
   return cudaGetLastError();
 }
 

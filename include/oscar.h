@@ -191,6 +191,9 @@ oscar_status oscar_set_option(oscar_ctx* ctx, int option, int value);
  *              in HADAMARD and NONE modes.
  *   clip_k, clip_v : host float [num_kv_heads], ratios in (0, 1].
  *   rot_mode : oscar_rot_mode.
+ * R = U·H·P_br (or H, or I) is composed on the host in double precision and
+ * stored in fp32; every kernel applies it as one 128x128 product, so the
+ * demotion, the bulk import and oscar_debug_rotate share one arithmetic.
  * Copies host memory on `stream` and synchronises it before returning. */
 oscar_status oscar_set_rotation(oscar_ctx* ctx, int layer, const float* U_K,
                                 const float* U_V, const float* clip_k,
