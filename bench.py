@@ -344,14 +344,13 @@ def run_ours(args, wl):
     # overhead would otherwise approach the GPU time of a step)
     tok_bytes = Bsz * Hkv * 128 * 2
     k_base, v_base = kv_new[0].data_ptr(), kv_new[1].data_ptr()
-    appends = [oscar.bind_append(ctx, 0, wk["copies"][c], Bsz) for c in range(n_copies)]
+    steps = [oscar.bind_decode_step(ctx, 0, wk["copies"][c], q, out, lse, scratch, Bsz) for c in range(n_copies)]
     decodes = [oscar.bind_decode(ctx, 0, wk["copies"][c], q, out, lse, scratch, Bsz) for c in range(n_copies)]
 
     def step(i):
         c = i % n_copies
         t = state["n"][c]
-        appends[c](k_base + t * tok_bytes, v_base + t * tok_bytes)
-        decodes[c]()
+        steps[c](k_base + t * tok_bytes, v_base + t * tok_bytes)  # oscar_decode_step: append + decode
         state["n"][c] += 1
     stream = torch.cuda.current_stream()
     sampler = ClockSampler(local)
@@ -436,8 +435,7 @@ def run_ours(args, wl):
         q_d.copy_(q_h, non_blocking=True)
         k_d.copy_(knew_h[t], non_blocking=True)
         v_d.copy_(vnew_h[t], non_blocking=True)
-        oscar.oscar_append(ctx, 0, wk["copies"][c], k_d, v_d, Bsz)
-        oscar.oscar_decode(ctx, 0, wk["copies"][c], q_d, out, None, scratch, Bsz)
+        oscar.oscar_decode_step(ctx, 0, wk["copies"][c], k_d, v_d, q_d, out, None, scratch, Bsz)
         out_h.copy_(out, non_blocking=True)
         state["n"][c] += 1
 
@@ -460,7 +458,7 @@ def run_ours(args, wl):
                                   list(range(Hkv)), budget_s=args.cpu_budget)
         cpu = {"value": sec * 1e6, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
                "sample": f"{done} of {Hkv} KV heads of one decode step on the GPU-built cache, scaled to {Hkv}"}
-    n_launch = 4 * K  # append, prep, decode, merge per step
+    n_launch = 3 * K  # append + q rotation, decode, merge per step
     value = ms_per_step * 1e3 / world
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,

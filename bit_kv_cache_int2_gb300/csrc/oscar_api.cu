@@ -251,19 +251,20 @@ oscar_status cuda_status(cudaError_t e) {
   return OSCAR_ERR_CUDA;
 }
 
-oscar_status decode_common(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* q,
-                           void* out, float* lse, void* scratch, size_t scratch_bytes, int batch,
-                           oscar_stream_t stream, bool bf16_history) {
+// Checks the decode arguments and fills `a` and the grid; OSCAR_OK when there
+// is work to launch, OSCAR_ERR_STATE (internal) when batch == 0.
+oscar_status decode_args(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* q, void* out,
+                         float* lse, void* scratch, size_t scratch_bytes, int batch, bool bf16_history,
+                         DecodeArgs& a, int& grid) {
   if (!ctx || !cache_ok(cache, true) || !q || !out || !scratch) return OSCAR_ERR_INVALID_ARG;
   if (layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
   if (batch < 0 || batch > ctx->cfg.max_batch) return OSCAR_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(scratch, 256) ||
       (lse && !aligned(lse, 4)))
     return OSCAR_ERR_INVALID_ARG;
-  if (batch == 0) return OSCAR_OK;
+  if (batch == 0) return OSCAR_ERR_STATE;
   const int target = target_items(ctx, batch, bf16_history);
   if (scratch_bytes < scratch_for(ctx, batch, target)) return OSCAR_ERR_INVALID_ARG;
-  DecodeArgs a;
   a.cv = make_view(ctx, cache, bf16_history);
   a.q = (const __nv_bfloat16*)q;
   a.out = (__nv_bfloat16*)out;
@@ -285,7 +286,19 @@ oscar_status decode_common(oscar_ctx* ctx, int layer, const oscar_cache* cache, 
   a.merge_hpc = ctx->G;
   while (a.merge_hpc % 2 == 0 && batch * ctx->cfg.num_kv_heads * (ctx->G / a.merge_hpc) < ctx->num_sms)
     a.merge_hpc /= 2;
-  const int grid = ctx->num_sms * decode_ctas(ctx, batch, bf16_history);
+  grid = ctx->num_sms * decode_ctas(ctx, batch, bf16_history);
+  return OSCAR_OK;
+}
+
+oscar_status decode_common(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* q,
+                           void* out, float* lse, void* scratch, size_t scratch_bytes, int batch,
+                           oscar_stream_t stream, bool bf16_history) {
+  DecodeArgs a;
+  int grid = 0;
+  const oscar_status s =
+      decode_args(ctx, layer, cache, q, out, lse, scratch, scratch_bytes, batch, bf16_history, a, grid);
+  if (s == OSCAR_ERR_STATE) return OSCAR_OK;  // batch == 0: nothing to do
+  if (s != OSCAR_OK) return s;
   return cuda_status(launch_decode(a, grid, (cudaStream_t)stream, &ctx->prof));
 }
 
@@ -517,6 +530,24 @@ oscar_status oscar_decode(oscar_ctx* ctx, int layer, const oscar_cache* cache, c
                           void* out, float* lse, void* scratch, size_t scratch_bytes, int batch,
                           oscar_stream_t stream) {
   return decode_common(ctx, layer, cache, q, out, lse, scratch, scratch_bytes, batch, stream, false);
+}
+
+oscar_status oscar_decode_step(oscar_ctx* ctx, int layer, const oscar_cache* cache,
+                               const void* k_new, const void* v_new, const void* q, void* out,
+                               float* lse, void* scratch, size_t scratch_bytes, int batch,
+                               oscar_stream_t stream) {
+  if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return OSCAR_ERR_INVALID_ARG;
+  DecodeArgs a;
+  int grid = 0;
+  const oscar_status s =
+      decode_args(ctx, layer, cache, q, out, lse, scratch, scratch_bytes, batch, false, a, grid);
+  if (s == OSCAR_ERR_STATE) return OSCAR_OK;  // batch == 0: nothing to do
+  if (s != OSCAR_OK) return s;
+  const cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = launch_step(a.cv, a.rot, (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, batch,
+                              ctx->d_req_counter, a, st, &ctx->prof);
+  if (e == cudaSuccess) e = launch_decode_after_prep(a, grid, st, &ctx->prof);
+  return cuda_status(e);
 }
 
 oscar_status oscar_decode_noalloc(oscar_ctx* ctx, int layer, const oscar_cache* cache,

@@ -35,97 +35,11 @@ constexpr int MERGE_RV_BYTES = RV_FRAG_WORDS * 4;
 constexpr int MERGE_Y_BYTES = 2 * MAX_G * YST * 2 > MAX_G * D * 4 ? 2 * MAX_G * YST * 2 : MAX_G * D * 4;
 
 
-// Per (request, query head) record of the packed query (QPACK_BYTES):
-//   half  qb[128]   q'_c * 2^-sigma * 2^(8 - E(c)), the QK^T B operand
-//   float alpha     2^sigma * log2(e) / (256 sqrt(d))
-//   float qsum[4]   sum of qb over channels 32k .. 32k + 31
-//   float psum[4]   sum of q' over channels 32k .. 32k + 31
-// A group of g channels takes its logit offset -1024 * alpha * (sum of qb) and
-// its zero-point weight (sum of q') * log2(e) / sqrt(d) from g / 32 quarters.
-constexpr int QPACK_ALPHA = 256, QPACK_QSUM = 260, QPACK_PSUM = 276;
-
 // ------------------------------------------------------------------- prep
-// grid (B * Hkv, 4), block 128: CTA (b * Hkv + kvh, cq) computes channels
-// 32cq .. 32cq + 31 of q' = q·R_K for the G query heads of kv head kvh; warp
-// w sums rows 32w .. 32w + 31 of R_K, lane = channel.  The fp16 prescale
-// sigma comes from |q|, which bounds every |q'_c| (R_K is orthogonal), so the
-// four CTAs of a head agree on it without talking to each other.
+// grid (B * Hkv, 4), block 128: one channel quarter per CTA (prep_body).
 __global__ void __launch_bounds__(128) prep_kernel(DecodeArgs a) {
-  __shared__ float xs[MAX_G][D];
-  __shared__ float part[4][MAX_G][32];
-  __shared__ float nrm[MAX_G];
-  const CacheView& cv = a.cv;
-  const int bk = blockIdx.x, cq = blockIdx.y;
-  const int b = bk / cv.Hkv, kvh = bk % cv.Hkv, t = threadIdx.x, w = t >> 5, lane = t & 31;
-  const int G = cv.G;
-  const int c = 32 * cq + lane;
-  // rotation-table loads first (written synchronously by oscar_set_rotation):
-  // R_K, and this CTA's quarter of the merge's R_V fragments into L2
-  float r[32];
-  if (!a.bf16_history) {
-    const float* R = a.rot.R_K + (size_t)kvh * D * D + (size_t)(32 * w) * D + c;
-#pragma unroll
-    for (int k = 0; k < 32; ++k) r[k] = __ldg(R + k * D);
-    const char* rv = (const char*)(a.rot.RV_frag + (size_t)kvh * RV_FRAG_WORDS) + (size_t)(cq * 128 + t) * 128;
-    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(rv));
-  }
-  // q, the cache state and the counters belong to earlier stream work (the
-  // append or the previous decode): wait for it, then let decode_kernel start
-  // its pre-wait work (it reads the cache state)
-  pdl_wait();
-  pdl_launch_dependents();
-  if (t == 0 && cq == 0 && bk == 0) *a.counter = 0;
-  if (a.bf16_history) return;
-  const __nv_bfloat16* qg = a.q + ((size_t)b * cv.Hq + kvh * G) * D;
-  for (int e = t; e < G * D; e += 128) xs[e / D][e % D] = __bfloat162float(qg[e]);
-  __syncthreads();
-  for (int n = w; n < G; n += 4) {
-    float sq = 0.f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float v = xs[n][lane + 32 * k];
-      sq = fmaf(v, v, sq);
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    if (lane == 0) nrm[n] = sqrtf(sq);
-  }
-#pragma unroll
-  for (int n = 0; n < MAX_G; ++n) {
-    if (n < G) {
-      float acc = 0.f;
-#pragma unroll
-      for (int k = 0; k < 32; ++k) acc = fmaf(xs[n][32 * w + k], r[k], acc);
-      part[w][n][lane] = acc;
-    }
-  }
-  __syncthreads();
-  const int i = 2 * ((c >> 4) & 3) + ((c >> 3) & 1);  // bit pair holding channel c in QK
-  const float f = (float)(1 << (8 - code_exp_rt(i)));
-  for (int n = w; n < G; n += 4) {
-    const float y = (part[0][n][lane] + part[1][n][lane]) + (part[2][n][lane] + part[3][n][lane]);
-    const size_t row = (size_t)b * cv.Hq + kvh * G + n;
-    a.qrot[row * D + c] = y;
-    // power-of-two prescale so that |q'| * 16 stays below 2^14 in fp16
-    const float am = nrm[n];
-    int ex = 0;
-    frexpf(am, &ex);
-    const int sig = am > 0.f ? ex - 10 : 0;
-    const __half hb = __float2half_rn(ldexpf(y, -sig) * f);
-    uint8_t* rec = a.qpack + row * QPACK_BYTES;
-    ((__half*)rec)[c] = hb;
-    float bs = __half2float(hb), ps = y;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      bs += __shfl_xor_sync(0xffffffffu, bs, o);
-      ps += __shfl_xor_sync(0xffffffffu, ps, o);
-    }
-    if (lane == 0) {
-      ((float*)(rec + QPACK_QSUM))[cq] = bs;
-      ((float*)(rec + QPACK_PSUM))[cq] = ps;
-      if (cq == 0) *(float*)(rec + QPACK_ALPHA) = ldexpf(1.f, sig) * LOG2E * INV_SQRT_D * (1.f / 256.f);
-    }
-  }
+  __shared__ PrepSmem sm;
+  prep_body(a, blockIdx.x, blockIdx.y, threadIdx.x, sm, true);
 }
 
 // ------------------------------------------------------------ smem layout
@@ -1689,12 +1603,9 @@ int decode_ctas_per_sm(const DecodeArgs& a) {
   return NG == 1 ? occupancy_t<1, 0>(a) : NG == 2 ? occupancy_t<2, 0>(a) : occupancy_t<4, 0>(a);
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof) {
+cudaError_t launch_decode_after_prep(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof) {
   const CacheView& cv = a.cv;
-  prof_begin(prof, OSCAR_KERNEL_DECODE_PREP, st);
-  cudaError_t e = launch_pdl(prep_kernel, dim3(a.B * cv.Hkv, 4), dim3(128), 0, st, a);
-  prof_end(prof, OSCAR_KERNEL_DECODE_PREP, st);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   prof_begin(prof, OSCAR_KERNEL_DECODE_MAIN, st);
   if (a.bf16_history) {
     e = launch_decode_t<1, 2>(a, grid, st);
@@ -1717,6 +1628,14 @@ cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profil
   e = launch_merge(a, st);
   prof_end(prof, OSCAR_KERNEL_DECODE_MERGE, st);
   return e;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof) {
+  prof_begin(prof, OSCAR_KERNEL_DECODE_PREP, st);
+  const cudaError_t e = launch_pdl(prep_kernel, dim3(a.B * a.cv.Hkv, 4), dim3(128), 0, st, a);
+  prof_end(prof, OSCAR_KERNEL_DECODE_PREP, st);
+  if (e != cudaSuccess) return e;
+  return launch_decode_after_prep(a, grid, st, prof);
 }
 
 }  // namespace oscar

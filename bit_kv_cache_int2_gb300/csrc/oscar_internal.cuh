@@ -454,7 +454,109 @@ struct DecodeArgs {
   LayerRot rot;
 };
 
+// Per (request, query head) record of the packed query (QPACK_BYTES):
+//   half  qb[128]   q'_c * 2^-sigma * 2^(8 - E(c)), the QK^T B operand
+//   float alpha     2^sigma * log2(e) / (256 sqrt(d))
+//   float qsum[4]   sum of qb over channels 32k .. 32k + 31
+//   float psum[4]   sum of q' over channels 32k .. 32k + 31
+// A group of g channels takes its logit offset -1024 * alpha * (sum of qb) and
+// its zero-point weight (sum of q') * log2(e) / sqrt(d) from g / 32 quarters.
+constexpr int QPACK_ALPHA = 256, QPACK_QSUM = 260, QPACK_PSUM = 276;
+
+struct PrepSmem {
+  float xs[MAX_G][D];
+  float part[4][MAX_G][32];
+  float nrm[MAX_G];
+};
+
+// Channels 32cq .. 32cq + 31 of q' = q·R_K for the G query heads of
+// (request, kv head) bk, by 128 threads (t = thread in the group, its own
+// PrepSmem); warp w = t / 32 sums rows 32w .. 32w + 31 of R_K, lane = channel.
+// The fp16 prescale sigma comes from |q|, which bounds every |q'_c| (R_K is
+// orthogonal), so the four quarters of a head agree on it without talking to
+// each other.  The rotation-table loads (written synchronously by
+// oscar_set_rotation) go first, then the body waits for earlier stream work;
+// with `release` it then lets its dependents launch (the decode kernel reads
+// the cache state before its own wait, so it must start only once that work
+// is complete), otherwise the caller releases them later.  All threads of
+// the block call it (it synchronises the block).
+__device__ __forceinline__ void prep_body(const DecodeArgs& a, int bk, int cq, int t, PrepSmem& sm,
+                                          bool release) {
+  const CacheView& cv = a.cv;
+  const int b = bk / cv.Hkv, kvh = bk % cv.Hkv, w = t >> 5, lane = t & 31;
+  const int G = cv.G;
+  const int c = 32 * cq + lane;
+  // R_K, and this CTA's quarter of the merge's R_V fragments into L2
+  float r[32];
+  if (!a.bf16_history) {
+    const float* R = a.rot.R_K + (size_t)kvh * D * D + (size_t)(32 * w) * D + c;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) r[k] = __ldg(R + k * D);
+    const char* rv = (const char*)(a.rot.RV_frag + (size_t)kvh * RV_FRAG_WORDS) + (size_t)(cq * 128 + t) * 128;
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(rv));
+  }
+  pdl_wait();
+  if (release) pdl_launch_dependents();
+  if (t == 0 && cq == 0) {
+    a.done[bk] = 0;
+    if (bk == 0) *a.counter = 0;
+  }
+  if (a.bf16_history) return;
+  const __nv_bfloat16* qg = a.q + ((size_t)b * cv.Hq + kvh * G) * D;
+  for (int e = t; e < G * D; e += 128) sm.xs[e / D][e % D] = __bfloat162float(qg[e]);
+  __syncthreads();
+  for (int n = w; n < G; n += 4) {
+    float sq = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float v = sm.xs[n][lane + 32 * k];
+      sq = fmaf(v, v, sq);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if (lane == 0) sm.nrm[n] = sqrtf(sq);
+  }
+#pragma unroll
+  for (int n = 0; n < MAX_G; ++n) {
+    if (n < G) {
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) acc = fmaf(sm.xs[n][32 * w + k], r[k], acc);
+      sm.part[w][n][lane] = acc;
+    }
+  }
+  __syncthreads();
+  const int i = 2 * ((c >> 4) & 3) + ((c >> 3) & 1);  // bit pair holding channel c in QK
+  const float f = (float)(1 << (8 - code_exp_rt(i)));
+  for (int n = w; n < G; n += 4) {
+    const float y = (sm.part[0][n][lane] + sm.part[1][n][lane]) + (sm.part[2][n][lane] + sm.part[3][n][lane]);
+    const size_t row = (size_t)b * cv.Hq + kvh * G + n;
+    a.qrot[row * D + c] = y;
+    // power-of-two prescale so that |q'| * 16 stays below 2^14 in fp16
+    const float am = sm.nrm[n];
+    int ex = 0;
+    frexpf(am, &ex);
+    const int sig = am > 0.f ? ex - 10 : 0;
+    const __half hb = __float2half_rn(ldexpf(y, -sig) * f);
+    uint8_t* rec = a.qpack + row * QPACK_BYTES;
+    ((__half*)rec)[c] = hb;
+    float bs = __half2float(hb), ps = y;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      bs += __shfl_xor_sync(0xffffffffu, bs, o);
+      ps += __shfl_xor_sync(0xffffffffu, ps, o);
+    }
+    if (lane == 0) {
+      ((float*)(rec + QPACK_QSUM))[cq] = bs;
+      ((float*)(rec + QPACK_PSUM))[cq] = ps;
+      if (cq == 0) *(float*)(rec + QPACK_ALPHA) = ldexpf(1.f, sig) * LOG2E * INV_SQRT_D * (1.f / 256.f);
+    }
+  }
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof);
+// The decode kernel and the merge only (the caller ran the packed query).
+cudaError_t launch_decode_after_prep(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof);
 int decode_ctas_per_sm(const DecodeArgs& a);  // resident CTAs per SM of the decode kernel (0: error)
 
 // Decode scratch: [work counter][done counters][q' fp32][packed q][partials]
@@ -467,6 +569,11 @@ size_t decode_scratch_bytes(int B, int Hq, int Hkv, int G, int max_target_items)
 cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* k,
                           const __nv_bfloat16* v, int B, int do_append, int* req_counter,
                           cudaStream_t st, Profiler* prof);
+// One decode step's first kernel: the append (as launch_append) and the packed
+// query (as prep_kernel) in one grid.
+cudaError_t launch_step(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* k,
+                        const __nv_bfloat16* v, int B, int* req_counter, const DecodeArgs& a,
+                        cudaStream_t st, Profiler* prof);
 cudaError_t launch_import(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* K,
                           const __nv_bfloat16* V, int B, int n, int bf16_history,
                           cudaStream_t st, Profiler* prof);

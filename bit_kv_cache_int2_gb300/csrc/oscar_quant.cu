@@ -51,16 +51,20 @@ __device__ __forceinline__ void quant_store_v_global(float y, int j, int g, floa
 // grid = (B * Hkv, 2): blockIdx.y = 0 handles K, 1 handles V.  block = 512:
 // four parts of 128 threads split the 128-row matvec x·R so that all of R's
 // loads are in flight at once; threads 0..127 then finish the token.
-__global__ void __launch_bounds__(512) append_kernel(CacheView cv, LayerRot rot,
-                                                     const __nv_bfloat16* __restrict__ knew,
-                                                     const __nv_bfloat16* __restrict__ vnew,
-                                                     int do_append, int* req_counter) {
+// One (request, kv head, K|V) of the append, by 512 threads; bk = request *
+// Hkv + kv head, isv = 0 for K, 1 for V.  The body waits for earlier stream
+// work after issuing its rotation-table loads; with `release` it then lets
+// its dependents launch at once, otherwise the caller releases them later.
+__device__ __forceinline__ void append_body(const CacheView& cv, const LayerRot& rot,
+                                            const __nv_bfloat16* __restrict__ knew,
+                                            const __nv_bfloat16* __restrict__ vnew, int do_append,
+                                            int* req_counter, int bk, int isv, bool release) {
   __shared__ float xs[D];
   __shared__ float part[4][D];
   __shared__ float red[8];
   __shared__ uint32_t kw[8];
   __shared__ int st[6];
-  const int b = blockIdx.x / cv.Hkv, h = blockIdx.x % cv.Hkv, isv = blockIdx.y;
+  const int b = bk / cv.Hkv, h = bk % cv.Hkv;
   const int t = threadIdx.x, j = t & 127, pp = t >> 7;
   // R's loads do not depend on earlier stream work: start them first
   float u[32];
@@ -72,7 +76,7 @@ __global__ void __launch_bounds__(512) append_kernel(CacheView cv, LayerRot rot,
   // the new tokens, the lengths and the cache belong to earlier stream work;
   // the decode's prep_kernel waits for this grid before it reads anything
   pdl_wait();
-  pdl_launch_dependents();
+  if (release) pdl_launch_dependents();
   if (t == 0) {
     const int L = cv.seq_lens[b], H = cv.hist_lens[b];
     const int recent = L > SINK ? L - SINK - H : 0;
@@ -159,6 +163,37 @@ __global__ void __launch_bounds__(512) append_kernel(CacheView cv, LayerRot rot,
       }
     }
   }
+}
+
+
+// grid = (B * Hkv, 2): blockIdx.y = 0 handles K, 1 handles V.
+__global__ void __launch_bounds__(512) append_kernel(CacheView cv, LayerRot rot,
+                                                     const __nv_bfloat16* __restrict__ knew,
+                                                     const __nv_bfloat16* __restrict__ vnew,
+                                                     int do_append, int* req_counter) {
+  append_body(cv, rot, knew, vnew, do_append, req_counter, blockIdx.x, blockIdx.y, true);
+}
+
+// One decode step's first kernel, grid = (B * Hkv, 3), block 512: y = 0 / 1
+// append K / V of (request, kv head) x (as append_kernel), y = 2 computes the
+// packed query of x, its four 128-thread parts taking one channel quarter
+// each (as prep_kernel).  The query rotation does not depend on the append,
+// so the two run side by side.  Each CTA releases the decode kernel only once
+// its own writes are done and fenced: the decode kernel reads the cache state
+// (lengths, pages) before it waits for this grid.
+__global__ void __launch_bounds__(512) step_kernel(CacheView cv, LayerRot rot,
+                                                   const __nv_bfloat16* __restrict__ knew,
+                                                   const __nv_bfloat16* __restrict__ vnew,
+                                                   int* req_counter, DecodeArgs a) {
+  __shared__ PrepSmem psm[4];
+  if (blockIdx.y < 2) {
+    append_body(cv, rot, knew, vnew, 1, req_counter, blockIdx.x, blockIdx.y, false);
+  } else {
+    prep_body(a, blockIdx.x, threadIdx.x >> 7, threadIdx.x & 127, psm[threadIdx.x >> 7], false);
+  }
+  __syncthreads();
+  __threadfence();
+  pdl_launch_dependents();
 }
 
 // ------------------------------------------------------------------ import
@@ -357,6 +392,16 @@ cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_b
   const cudaError_t e =
       launch_pdl(append_kernel, dim3(B * cv.Hkv, 2), dim3(512), 0, st, cv, rot, k, v, do_append, req_counter);
   prof_end(prof, OSCAR_KERNEL_APPEND, st);
+  return e;
+}
+
+cudaError_t launch_step(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* k,
+                        const __nv_bfloat16* v, int B, int* req_counter, const DecodeArgs& a,
+                        cudaStream_t st, Profiler* prof) {
+  prof_begin(prof, OSCAR_KERNEL_STEP, st);
+  const cudaError_t e =
+      launch_pdl(step_kernel, dim3(B * cv.Hkv, 3), dim3(512), 0, st, cv, rot, k, v, req_counter, a);
+  prof_end(prof, OSCAR_KERNEL_STEP, st);
   return e;
 }
 

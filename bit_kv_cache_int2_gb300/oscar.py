@@ -100,6 +100,9 @@ _SIGS = {
                             ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
     "oscar_get_error": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
     "oscar_last_cuda_error": ([], ctypes.c_int),
+    "oscar_decode_step": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(oscar_cache), ctypes.c_void_p, ctypes.c_void_p,
+                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                           ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
     "oscar_profile_enable": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "oscar_profile_read": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                             ctypes.POINTER(ctypes.c_double), ctypes.c_int], ctypes.c_int),
@@ -110,7 +113,8 @@ KERNEL_IMPORT = 1
 KERNEL_DECODE_PREP = 2
 KERNEL_DECODE_MAIN = 3
 KERNEL_DECODE_MERGE = 4
-KERNEL_NAMES = {0: "append", 1: "import", 2: "decode_prep", 3: "decode_main", 4: "decode_merge"}
+KERNEL_STEP = 5
+KERNEL_NAMES = {0: "append", 1: "import", 2: "decode_prep", 3: "decode_main", 4: "decode_merge", 5: "step_append_prep"}
 
 
 def exported_symbols():
@@ -235,6 +239,31 @@ def oscar_decode(ctx, layer, cache: dict, q, out, lse, scratch, batch, stream=No
     _check(lib().oscar_decode(ctx, layer, ctypes.byref(cs), _ptr(q), _ptr(out), _ptr(lse), _ptr(scratch),
                               scratch.numel() * scratch.element_size(), batch, _stream(stream)),
            "oscar_decode")
+
+
+def oscar_decode_step(ctx, layer, cache: dict, k_new, v_new, q, out, lse, scratch, batch, stream=None):
+    """oscar_append(k_new, v_new) then oscar_decode(q), with the query rotation
+    run beside the append."""
+    cs = _cache_struct(cache)
+    _check(lib().oscar_decode_step(ctx, layer, ctypes.byref(cs), _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(out),
+                                   _ptr(lse), _ptr(scratch), scratch.numel() * scratch.element_size(), batch,
+                                   _stream(stream)), "oscar_decode_step")
+
+
+def bind_decode_step(ctx, layer, cache: dict, q, out, lse, scratch, batch, stream=None):
+    """oscar_decode_step with everything but the new tokens marshalled once:
+    returns f(k_new_ptr, v_new_ptr) taking raw device addresses (ints)."""
+    cs = _cache_struct(cache)
+    head = (ctx, layer, ctypes.byref(cs))
+    tail = (_ptr(q), _ptr(out), _ptr(lse), _ptr(scratch), scratch.numel() * scratch.element_size(), batch,
+            _stream(stream))
+    fn = lib().oscar_decode_step
+
+    def call(k_ptr: int, v_ptr: int):
+        _check(fn(*head, ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr), *tail), "oscar_decode_step")
+
+    call._keep = cs
+    return call
 
 
 def bind_append(ctx, layer, cache: dict, batch, stream=None):

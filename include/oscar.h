@@ -246,6 +246,20 @@ oscar_status oscar_decode(oscar_ctx* ctx, int layer, const oscar_cache* cache,
                           size_t scratch_bytes, int batch,
                           oscar_stream_t stream);
 
+/* One decode step of one layer: exactly oscar_append(k_new, v_new) followed by
+ * oscar_decode(q) on `stream` (the new token takes part in the attention),
+ * as the pages' serving loop runs them each step [Blog, pipeline figure
+ * paragraph: the new token is written to the recent window, the oldest one
+ * demoted, then attention over sink, INT2 history and recent window].  The
+ * query rotation does not depend on the append, so the library runs the two
+ * side by side in one kernel instead of one after the other.  Arguments,
+ * layouts, ownership and errors are those of the two calls; k_new, v_new and q
+ * must all be complete when the call's work starts on `stream`. */
+oscar_status oscar_decode_step(oscar_ctx* ctx, int layer, const oscar_cache* cache,
+                               const void* k_new, const void* v_new, const void* q, void* out,
+                               float* lse, void* scratch, size_t scratch_bytes, int batch,
+                               oscar_stream_t stream);
+
 /* Decode without any device allocation (the pages have no counterpart: this
  * is a deployment convenience of this library).  Same computation, arguments
  * and results as oscar_decode, but the working memory comes from a buffer of
@@ -330,7 +344,8 @@ typedef enum {
   OSCAR_KERNEL_DECODE_PREP = 2, /* q rotation, work-counter reset       */
   OSCAR_KERNEL_DECODE_MAIN = 3, /* split-K decode over history + window */
   OSCAR_KERNEL_DECODE_MERGE = 4,/* partial merge + un-rotation          */
-  OSCAR_KERNEL_COUNT = 5
+  OSCAR_KERNEL_STEP = 5,        /* oscar_decode_step's append + q rotation */
+  OSCAR_KERNEL_COUNT = 6
 } oscar_kernel;
 
 oscar_status oscar_profile_enable(oscar_ctx* ctx, int enable);

@@ -220,6 +220,46 @@ def test_append_stream_wraps_ring_and_matches_oracle():
         sc.close()
 
 
+def test_decode_step_equals_append_then_decode():
+    """oscar_decode_step (append and query rotation in one kernel) gives the
+    same cache and the same outputs, bit for bit, as oscar_append followed by
+    oscar_decode, across ring wrap and demotions; the outputs match the oracle."""
+    lengths = [300, 64, 1500]
+    scs = [GS.build("stepx", lengths, Hq=8, Hkv=2, g=128, extra_tokens=120, calib_n=512) for _ in range(2)]
+    try:
+        a, b = scs
+        scratch = [oscar.alloc_scratch(s_.cfg) for s_ in scs]
+        for t in range(120):
+            k = torch.stack([a.K[i][:, lengths[i] + t] for i in range(3)]).contiguous()
+            v = torch.stack([a.V[i][:, lengths[i] + t] for i in range(3)]).contiguous()
+            q = GS.queries(a, seed=300 + t)
+            outs = []
+            for j, s_ in enumerate(scs):
+                out = torch.empty_like(q)
+                lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+                if j == 0:
+                    oscar.oscar_decode_step(s_.ctx, 0, s_.cache, k, v, q, out, lse, scratch[j], 3)
+                else:
+                    oscar.oscar_append(s_.ctx, 0, s_.cache, k, v, 3)
+                    oscar.oscar_decode(s_.ctx, 0, s_.cache, q, out, lse, scratch[j], 3)
+                outs.append((out, lse))
+            torch.cuda.synchronize()
+            assert torch.equal(outs[0][0], outs[1][0]), t
+            assert torch.equal(outs[0][1], outs[1][1]), t
+        for s_ in scs:
+            assert oscar.oscar_get_error(s_.ctx) == 0
+        for key in ("pool", "sink_k", "sink_v", "ring_k", "ring_v", "seq_lens", "hist_lens"):
+            assert torch.equal(a.cache[key], b.cache[key]), key
+        hc = GS.HostCache(a)
+        qn = q.float().cpu().numpy()
+        for i in range(3):
+            ref, rlse = GS.oracle_decode(a, hc, qn, i)
+            assert _rel(outs[0][0][i].float().cpu().numpy(), ref) <= REL_TOL, i
+    finally:
+        for s_ in scs:
+            s_.close()
+
+
 def test_demote_then_append():
     sc = GS.build("demote", [400], Hq=4, Hkv=1, g=128, extra_tokens=10, calib_n=512)
     try:
