@@ -325,7 +325,8 @@ def run_ours(args, wl):
     per_copy = algorithmic_bytes(wl["L"] - 320, wl["L"], Hkv, g) * Bsz
     n_copies = max(2, -(-3 * l2 // per_copy))  # rotate over >= 3x L2 of caches
     Kp, nd, ne = min(K, 2000), min(K, 1000), min(K, 1000)
-    total_appends = W + K + Kp + ne
+    na = min(K, 200)  # demotion-only calls
+    total_appends = W + K + Kp + ne + na
     extra = total_appends // n_copies + 16  # appends per cache copy, with margin
     wk = build_workload(wl, dev, n_copies, extra, bf16_copies=2)
     ctx, cfg = wk["ctx"], wk["cfg"]
@@ -419,6 +420,19 @@ def run_ours(args, wl):
     bf16_us = time_calls(lambda i: oscar.oscar_decode_bf16_history(wk["bctx"], wk["bf"][i % 2], q, bf_out, None,
                                                                    bscratch, Bsz), min(nd, 200))
     bf16_bytes = Hkv * Bsz * ((wl["L"] - 320) * 512 + 320 * 512) + ((wl["L"] - 320 + 63) // 64) * 4
+    # ---- demotion alone (oscar_append; one token per request, each demoting one)
+    appends = [oscar.bind_append(ctx, 0, wk["copies"][c], Bsz) for c in range(n_copies)]
+
+    def append_only(i):
+        c = i % n_copies
+        t = state["n"][c]
+        appends[c](k_base + t * tok_bytes, v_base + t * tok_bytes)
+        state["n"][c] += 1
+
+    app_us = time_calls(append_only, na)
+    # per (request, kv head) and K|V: the evicted ring token and the new token in,
+    # the new token into the ring, the codes and scale/zero of the demoted token out
+    app_bytes = Bsz * Hkv * 2 * (3 * 256 + 32 + (128 // g) * 4)
     # ---- end to end through the public API with host buffers
     q_h = q.cpu().pin_memory()
     out_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
@@ -471,6 +485,10 @@ def run_ours(args, wl):
         "decode_us": int2_us, "bf16_history_decode_us": bf16_us, "speedup_vs_bf16": bf16_us / int2_us,
         "bf16_history_hbm_gbs": bf16_bytes / (bf16_us * 1e-6) / 1e9,
         "kernels_us": {k: round(v["avg_us"], 3) for k, v in prof.items()},
+        "demotion": {"us_per_call": app_us, "bytes_per_call": app_bytes,
+                     "achieved_gbs": app_bytes / (app_us * 1e-6) / 1e9,
+                     "frac": app_bytes / (app_us * 1e-6) / 1e9 / peak,
+                     "note": "one token per (request, kv head): latency-bound, not bandwidth-bound"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(), "kernel": "decode_main",
                      "bytes_per_launch": bytes_main, "peak_kind": peak_kind},

@@ -385,6 +385,35 @@ def three_region_attention(q, win_k, win_v, hist_k_rot, hist_v_rot, R_K, R_V):
     return o, (m + np.log(lsum))[..., 0]
 
 
+def chunk_prefill_attention(q_chunk, k_chunk, v_chunk, win_k, win_v, hist_k_rot, hist_v_rot, R_K, R_V):
+    """Chunked prefill over the cache of one kv head, float64: T new tokens
+    (a prefix-hit extension) attend to the cache as it stands -- the BF16 sink
+    and recent window, the INT2 history in the rotated basis -- and causally
+    to the chunk's own BF16 tokens: chunk query t sees chunk tokens 0..t.
+    The chunk is not stored by this step.
+
+    This is the plain reading of the "next" row of the pages' prefix-cache
+    reuse (News, "服务系统：混合精度缓存布局"; Blog, pipeline paragraph): the
+    decode attention of each chunk token with the earlier chunk tokens as extra
+    full-precision window tokens.
+
+    q_chunk [T][G][d]; k_chunk, v_chunk [T][d]; the rest as in
+    three_region_attention.  Returns (o [T][G][d], lse [T][G]).
+    """
+    q_chunk = np.asarray(q_chunk, dtype=np.float64)
+    kc = np.asarray(k_chunk, dtype=np.float64)
+    vc = np.asarray(v_chunk, dtype=np.float64)
+    wk = np.asarray(win_k, dtype=np.float64).reshape(-1, q_chunk.shape[-1])
+    wv = np.asarray(win_v, dtype=np.float64).reshape(-1, q_chunk.shape[-1])
+    outs, lses = [], []
+    for t in range(q_chunk.shape[0]):
+        o, l = three_region_attention(q_chunk[t], np.concatenate([wk, kc[:t + 1]]),
+                                      np.concatenate([wv, vc[:t + 1]]), hist_k_rot, hist_v_rot, R_K, R_V)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs), np.stack(lses)
+
+
 def lse_merge(parts):
     """Merge online-softmax partials (m, l, o) -- o normalised by l -- into one.
 

@@ -342,6 +342,77 @@ def test_three_region_rotated_unquantised_history_is_dense_attention():
     np.testing.assert_allclose(lse, lse2, atol=1e-12)
 
 
+def test_chunk_prefill_causal_brute_force_tiny():
+    # No history: chunk query t is plain softmax attention over the window and
+    # chunk tokens 0..t, computed here element by element.
+    rng = np.random.default_rng(21)
+    d, G, T, nw = 4, 2, 5, 3
+    q = rng.standard_normal((T, G, d))
+    kc, vc = rng.standard_normal((T, d)), rng.standard_normal((T, d))
+    wk, wv = rng.standard_normal((nw, d)), rng.standard_normal((nw, d))
+    R = np.eye(d)
+    o, lse = O.chunk_prefill_attention(q, kc, vc, wk, wv, np.zeros((0, d)), np.zeros((0, d)), R, R)
+    for t in range(T):
+        keys = [wk[i] for i in range(nw)] + [kc[j] for j in range(t + 1)]
+        vals = [wv[i] for i in range(nw)] + [vc[j] for j in range(t + 1)]
+        for h in range(G):
+            logits = [sum(q[t, h, c] * k[c] for c in range(d)) / 2.0 for k in keys]
+            p = _softmax_row(logits)
+            for c in range(d):
+                assert abs(o[t, h, c] - sum(pi * v[c] for pi, v in zip(p, vals))) < 1e-12
+            m = max(logits)
+            assert abs(lse[t, h] - (m + math.log(sum(math.exp(x - m) for x in logits)))) < 1e-12
+
+
+def test_chunk_prefill_truncation_invariance():
+    # Causality: the first t + 1 outputs of a chunk do not depend on later chunk tokens.
+    rng = np.random.default_rng(22)
+    d, G, T = 128, 4, 9
+    q = rng.standard_normal((T, G, d))
+    kc, vc = rng.standard_normal((T, d)), rng.standard_normal((T, d))
+    wk, wv = rng.standard_normal((40, d)), rng.standard_normal((40, d))
+    R = _orthogonal(rng, d)
+    hk, hv = rng.standard_normal((70, d)), rng.standard_normal((70, d))
+    o, lse = O.chunk_prefill_attention(q, kc, vc, wk, wv, hk, hv, R, R)
+    for t in (0, 3, T - 1):
+        o2, lse2 = O.chunk_prefill_attention(q[:t + 1], kc[:t + 1], vc[:t + 1], wk, wv, hk, hv, R, R)
+        np.testing.assert_allclose(o[:t + 1], o2, atol=1e-12)
+        np.testing.assert_allclose(lse[:t + 1], lse2, atol=1e-12)
+
+
+def test_chunk_prefill_equals_sequential_decodes_without_demotion():
+    # While the recent window has room, appending the chunk token by token and
+    # decoding after each append (the cache model's own window walk) gives the
+    # prefill outputs: the chunk tokens join the BF16 window.
+    rng = np.random.default_rng(23)
+    d, G, T = 128, 4, 12
+    cm = O.CacheModel()
+    K0, V0 = rng.standard_normal((400, d)), rng.standard_normal((400, d))
+    cm.import_tokens(K0, V0)
+    for _ in range(20):
+        cm.demote()  # leave room in the recent window
+    assert cm.recent_count() + T <= O.RECENT
+    RK, RV = _orthogonal(rng, d), _orthogonal(rng, d)
+    hk = np.array([cm.tokens_k[p] for p in cm.history_positions()], dtype=np.float64) @ RK
+    hv = np.array([cm.tokens_v[p] for p in cm.history_positions()], dtype=np.float64) @ RV
+    win = cm.window_positions()
+    wk = np.array([cm.tokens_k[p] for p in win])
+    wv = np.array([cm.tokens_v[p] for p in win])
+    q = rng.standard_normal((T, G, d))
+    # the cache model keeps tokens as float32 (their bf16 values): use such values
+    kc = rng.standard_normal((T, d)).astype(np.float32).astype(np.float64)
+    vc = rng.standard_normal((T, d)).astype(np.float32).astype(np.float64)
+    o, lse = O.chunk_prefill_attention(q, kc, vc, wk, wv, hk, hv, RK, RV)
+    for t in range(T):
+        cm.append(kc[t], vc[t])
+        assert [p for p in cm.history_positions()] == list(range(64, 64 + hk.shape[0]))
+        w2 = cm.window_positions()
+        ok, ov = O.three_region_attention(q[t], np.array([cm.tokens_k[p] for p in w2]),
+                                          np.array([cm.tokens_v[p] for p in w2]), hk, hv, RK, RV)
+        np.testing.assert_allclose(o[t], ok, atol=1e-12)
+        np.testing.assert_allclose(lse[t], ov, atol=1e-12)
+
+
 # ---------------------------------------------------------- regions / state
 
 def test_region_walk_and_append_state():
