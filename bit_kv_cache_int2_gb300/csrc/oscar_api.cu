@@ -53,7 +53,7 @@ struct oscar_ctx {
   int device = 0;
   int num_sms = 0;
   int G = 0, NG = 0;
-  float* d_rot = nullptr;  // [layers][3][Hkv][128 * 128 words]: R_K, R_V, R_V fragments
+  float* d_rot = nullptr;  // [layers][4][Hkv][128 * 128 words]: R_K, R_V, R_V fragments, R_V^T
   float* d_clip = nullptr;  // [layers][2][Hkv]
   std::vector<int> mode;
   int* d_err = nullptr;
@@ -155,7 +155,7 @@ CacheView make_view(const oscar_ctx* ctx, const oscar_cache* c, bool bf16_histor
   return v;
 }
 
-constexpr int ROT_MATS = 3;  // R_K, R_V, R_V fragments per layer
+constexpr int ROT_MATS = 4;  // R_K, R_V, R_V fragments, R_V^T per layer
 static_assert(RV_FRAG_WORDS == D * D, "R_V fragments fill one matrix slot");
 
 // R = U·H·P_br (OSCAR), H (HADAMARD) or I (NONE) for one head, in fp64, in the
@@ -213,8 +213,8 @@ void pack_rv_fragments(const double* R, uint32_t* out) {
 }
 
 // One layer's table (ROT_MATS matrices of Hkv heads) from the eigenbases
-// (nullptr outside OSCAR mode: identity): R_K, R_V in fp32, then R_V as fp16
-// high/low mma fragments.
+// (nullptr outside OSCAR mode: identity): R_K, R_V in fp32, R_V as fp16
+// high/low mma fragments, then R_V^T in fp32.
 void build_layer_table(const float* U_K, const float* U_V, int mode, int Hkv, std::vector<float>& out) {
   const size_t hm = (size_t)D * D, mat = (size_t)Hkv * hm;
   out.assign(ROT_MATS * mat, 0.f);
@@ -225,7 +225,12 @@ void build_layer_table(const float* U_K, const float* U_V, int mode, int Hkv, st
       compose_rotation(U, mode, R.data());
       float* dst = out.data() + t * mat + h * hm;
       for (size_t e = 0; e < hm; ++e) dst[e] = (float)R[e];
-      if (t == 1) pack_rv_fragments(R.data(), (uint32_t*)(out.data() + 2 * mat + h * hm));
+      if (t == 1) {
+        pack_rv_fragments(R.data(), (uint32_t*)(out.data() + 2 * mat + h * hm));
+        float* rt = out.data() + 3 * mat + h * hm;
+        for (int i = 0; i < D; ++i)
+          for (int j = 0; j < D; ++j) rt[(size_t)i * D + j] = (float)R[(size_t)j * D + i];
+      }
     }
   }
 }
@@ -236,6 +241,7 @@ LayerRot layer_rot(const oscar_ctx* ctx, int layer) {
   r.R_K = ctx->d_rot + (size_t)layer * ROT_MATS * mat;
   r.R_V = r.R_K + mat;
   r.RV_frag = (const uint32_t*)(r.R_V + mat);
+  r.RVt = r.R_V + 2 * mat;
   r.clip_k = ctx->d_clip + (size_t)layer * 2 * ctx->cfg.num_kv_heads;
   r.clip_v = r.clip_k + ctx->cfg.num_kv_heads;
   r.mode = ctx->mode[layer];
@@ -368,6 +374,14 @@ oscar_status oscar_layout(const oscar_config* cfg, oscar_layout_info* out) {
   out->ring_bytes = (size_t)cfg->max_batch * cfg->num_kv_heads * RECENT * D * 2;
   out->decode_scratch_bytes = decode_scratch_bytes(cfg->max_batch, cfg->num_q_heads,
                                                    cfg->num_kv_heads, G, MAX_TARGET_ITEMS);
+  // the split count (and so the partials) is not monotone in the batch: take the largest
+  size_t pf = 0;
+  for (int b = 1; b <= cfg->max_batch; ++b) {
+    const int ns = prefill_max_splits(b, cfg->num_kv_heads, G, PF_MAX_T);
+    const size_t t = prefill_scratch_layout(b, cfg->num_kv_heads, G, PF_MAX_T, ns).total;
+    if (t > pf) pf = t;
+  }
+  out->prefill_scratch_bytes = pf;
   return OSCAR_OK;
 }
 
@@ -548,6 +562,46 @@ oscar_status oscar_decode_step(oscar_ctx* ctx, int layer, const oscar_cache* cac
                               ctx->d_req_counter, a, st, &ctx->prof);
   if (e == cudaSuccess) e = launch_decode_after_prep(a, grid, st, &ctx->prof);
   return cuda_status(e);
+}
+
+oscar_status oscar_prefill(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* q,
+                           const void* k, const void* v, int T, void* out, float* lse,
+                           void* scratch, size_t scratch_bytes, int batch, oscar_stream_t stream) {
+  if (!ctx || !cache_ok(cache, true) || !q || !k || !v || !out || !scratch) return OSCAR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
+  if (batch < 0 || batch > ctx->cfg.max_batch || T < 1 || T > PF_MAX_T) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(scratch, 256) || (lse && !aligned(lse, 4)))
+    return OSCAR_ERR_INVALID_ARG;
+  if (batch == 0) return OSCAR_OK;
+  const int Hkv = ctx->cfg.num_kv_heads, G = ctx->G;
+  PrefillArgs a;
+  a.RT = (T * G + PF_ROWS - 1) / PF_ROWS;
+  const int tiles = batch * Hkv * a.RT;
+  int occ = 0;
+  const cudaError_t oe = prefill_ctas_per_sm(&occ);
+  if (oe != cudaSuccess) return cuda_status(oe);
+  if (occ < 1) occ = 1;
+  // history splits: enough CTAs for one wave over the SMs, within the scratch bound
+  int ns = (ctx->num_sms * occ + tiles - 1) / tiles;
+  const int cap = prefill_max_splits(batch, Hkv, G, T);
+  a.NS = ns < 1 ? 1 : ns > cap ? cap : ns;
+  const PrefillScratch L = prefill_scratch_layout(batch, Hkv, G, T, a.NS);
+  if (scratch_bytes < L.total) return OSCAR_ERR_INVALID_ARG;
+  a.cv = make_view(ctx, cache, false);
+  a.q = (const __nv_bfloat16*)q;
+  a.k = (const __nv_bfloat16*)k;
+  a.v = (const __nv_bfloat16*)v;
+  a.out = (__nv_bfloat16*)out;
+  a.lse = lse;
+  uint8_t* sp = (uint8_t*)scratch;
+  a.qh = (__half*)(sp + L.off_qh);
+  a.alpha = (float*)(sp + L.off_alpha);
+  a.part = (float*)(sp + L.off_part);
+  a.B = batch;
+  a.T = T;
+  a.rot = layer_rot(ctx, layer);
+  return cuda_status(launch_prefill(a, (cudaStream_t)stream, &ctx->prof));
 }
 
 oscar_status oscar_decode_noalloc(oscar_ctx* ctx, int layer, const oscar_cache* cache,

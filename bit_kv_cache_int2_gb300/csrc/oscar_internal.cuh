@@ -49,12 +49,13 @@ __host__ __device__ __forceinline__ int rv_frag_index(int part, int mt, int ks, 
 
 // Per-layer rotation table, composed in fp64 on the host from the eigenbases:
 // R_K = rotation(U_K, mode) and R_V = rotation(U_V, mode) in fp32 for the
-// demotion and the query, and R_V again as fp16 high/low fragments for the
-// output.
+// demotion and the query, R_V again as fp16 high/low fragments for the
+// decode's output and as fp32 R_V^T for the prefill's output.
 struct LayerRot {
   const float* R_K;         // [Hkv][128][128]  k' = k·R_K, q' = q·R_K
   const float* R_V;         // [Hkv][128][128]  v' = v·R_V
   const uint32_t* RV_frag;  // [Hkv][RV_FRAG_WORDS]  o = o'·R_V^T
+  const float* RVt;         // [Hkv][128][128]  R_V^T, row i = column i of R_V (coalesced un-rotation)
   const float* clip_k;      // [Hkv]
   const float* clip_v;      // [Hkv]
   int mode;
@@ -565,6 +566,35 @@ struct ScratchLayout {
 };
 ScratchLayout scratch_layout(int B, int Hq, int Hkv, int G, int max_target_items);
 size_t decode_scratch_bytes(int B, int Hq, int Hkv, int G, int max_target_items);
+
+// ----------------------------------------------------------------- prefill
+// Chunked prefill over the cache: T new tokens of a request attend to its
+// sink, INT2 history and recent window and causally to each other.
+constexpr int PF_ROWS = 128;       // query rows (token x head of one kv head) per attention CTA
+constexpr int PF_MAX_T = 64;       // chunk tokens per call
+constexpr int PF_MAX_SPLITS = 64;  // history splits per row tile
+
+struct PrefillArgs {
+  CacheView cv;
+  const __nv_bfloat16* q;  // [B][T][Hq][128]
+  const __nv_bfloat16* k;  // [B][T][Hkv][128]
+  const __nv_bfloat16* v;  // [B][T][Hkv][128]
+  __nv_bfloat16* out;      // [B][T][Hq][128]
+  float* lse;              // [B][T][Hq] or null
+  __half* qh;              // scratch [2][B*Hkv][RT*128][128]: q·R_K, q (both * 2^-sigma)
+  float* alpha;            // scratch [B*Hkv][RT*128]: 2^sigma * log2(e) / sqrt(d)
+  float* part;             // scratch [B*Hkv*RT][NS+1][128][PART_STRIDE]
+  int B, T, RT, NS;
+  LayerRot rot;
+};
+
+struct PrefillScratch {
+  size_t off_qh, off_alpha, off_part, total;
+};
+PrefillScratch prefill_scratch_layout(int B, int Hkv, int G, int T, int NS);
+int prefill_max_splits(int B, int Hkv, int G, int T);  // NS bound the scratch is sized for
+cudaError_t prefill_ctas_per_sm(int* n);                  // resident attention CTAs per SM
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st, Profiler* prof);
 
 cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* k,
                           const __nv_bfloat16* v, int B, int do_append, int* req_counter,

@@ -57,7 +57,8 @@ class oscar_config(ctypes.Structure):
 class oscar_layout_info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "int2_head_bytes", "int2_page_bytes", "off_k_codes", "off_v_codes", "off_k_sz", "off_v_sz",
-        "bf16_head_bytes", "bf16_page_bytes", "sink_bytes", "ring_bytes", "decode_scratch_bytes")]
+        "bf16_head_bytes", "bf16_page_bytes", "sink_bytes", "ring_bytes", "decode_scratch_bytes",
+        "prefill_scratch_bytes")]
 
 
 class oscar_cache(ctypes.Structure):
@@ -103,6 +104,9 @@ _SIGS = {
     "oscar_decode_step": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(oscar_cache), ctypes.c_void_p, ctypes.c_void_p,
                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                            ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
+    "oscar_prefill": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(oscar_cache), ctypes.c_void_p, ctypes.c_void_p,
+                       ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                       ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
     "oscar_profile_enable": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "oscar_profile_read": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                             ctypes.POINTER(ctypes.c_double), ctypes.c_int], ctypes.c_int),
@@ -114,7 +118,11 @@ KERNEL_DECODE_PREP = 2
 KERNEL_DECODE_MAIN = 3
 KERNEL_DECODE_MERGE = 4
 KERNEL_STEP = 5
-KERNEL_NAMES = {0: "append", 1: "import", 2: "decode_prep", 3: "decode_main", 4: "decode_merge", 5: "step_append_prep"}
+KERNEL_PREFILL_PREP = 6
+KERNEL_PREFILL_ATTN = 7
+KERNEL_PREFILL_MERGE = 8
+KERNEL_NAMES = {0: "append", 1: "import", 2: "decode_prep", 3: "decode_main", 4: "decode_merge", 5: "step_append_prep",
+                6: "prefill_prep", 7: "prefill_attn", 8: "prefill_merge"}
 
 
 def exported_symbols():
@@ -241,6 +249,15 @@ def oscar_decode(ctx, layer, cache: dict, q, out, lse, scratch, batch, stream=No
            "oscar_decode")
 
 
+def oscar_prefill(ctx, layer, cache: dict, q, k, v, T, out, lse, scratch, batch, stream=None):
+    """Chunked prefill: T new tokens per request attend to the cache and
+    causally to each other (the chunk is not stored)."""
+    cs = _cache_struct(cache)
+    _check(lib().oscar_prefill(ctx, layer, ctypes.byref(cs), _ptr(q), _ptr(k), _ptr(v), T, _ptr(out), _ptr(lse),
+                               _ptr(scratch), scratch.numel() * scratch.element_size(), batch, _stream(stream)),
+           "oscar_prefill")
+
+
 def oscar_decode_step(ctx, layer, cache: dict, k_new, v_new, q, out, lse, scratch, batch, stream=None):
     """oscar_append(k_new, v_new) then oscar_decode(q), with the query rotation
     run beside the append."""
@@ -365,8 +382,9 @@ def alloc_cache(cfg: oscar_config, device="cuda", bf16_history=False, zero=True)
     }
 
 
-def alloc_scratch(cfg: oscar_config, device="cuda"):
+def alloc_scratch(cfg: oscar_config, device="cuda", prefill=False):
     import torch
 
-    n = oscar_layout(cfg).decode_scratch_bytes
+    info = oscar_layout(cfg)
+    n = info.prefill_scratch_bytes if prefill else info.decode_scratch_bytes
     return torch.empty((n + 255) // 256 * 256, dtype=torch.uint8, device=device)

@@ -141,6 +141,8 @@ typedef struct {
   size_t sink_bytes;        /* bytes of sink_k (or sink_v) at max_batch     */
   size_t ring_bytes;        /* bytes of ring_k (or ring_v) at max_batch     */
   size_t decode_scratch_bytes; /* scratch oscar_decode* needs at max_batch  */
+  size_t prefill_scratch_bytes; /* scratch oscar_prefill needs, any batch up to
+                                   max_batch and any chunk up to 64 tokens  */
 } oscar_layout_info;
 
 /* One layer's cache.  Every pointer is a device pointer owned by the caller.
@@ -260,6 +262,33 @@ oscar_status oscar_decode_step(oscar_ctx* ctx, int layer, const oscar_cache* cac
                                float* lse, void* scratch, size_t scratch_bytes, int batch,
                                oscar_stream_t stream);
 
+/* Chunked prefill over the cache (prefix-hit extension) [News,
+ * "服务系统：混合精度缓存布局": the mixed-precision layout serves prefix-cache
+ * reuse; Blog, pipeline figure paragraph: attention over sink, INT2 history
+ * and recent window].  For each b < batch, the T new tokens of request b
+ * attend to the request's cache as it stands (BF16 sink and recent window;
+ * the INT2 history with q' = q·R_K, its output un-rotated by R_V^T) and
+ * causally to the chunk itself: chunk token t sees chunk tokens 0..t.  One
+ * softmax over all of them per (token, query head).  The chunk is NOT stored:
+ * append it afterwards (oscar_append per token, or oscar_import_tokens into an
+ * empty request) if it is to stay in the cache.
+ *   q   : device bf16 [batch][T][num_q_heads][128]
+ *   k, v: device bf16 [batch][T][num_kv_heads][128], the chunk's keys and values
+ *   T   : 1..64 tokens per request (the same for every request of the call)
+ *   out : device bf16 [batch][T][num_q_heads][128]
+ *   lse : device float [batch][T][num_q_heads] natural-log log-sum-exp of the
+ *         scaled logits, or NULL
+ *   scratch : device buffer of at least prefill_scratch_bytes (oscar_layout)
+ *             bytes, 256-byte aligned, no initial contents needed; not to be
+ *             shared by calls that may overlap.
+ * q, k, v, out 16-byte aligned.  Returns OSCAR_ERR_INVALID_ARG for T outside
+ * 1..64.  Device errors as oscar_decode (OSCAR_ERR_NO_PAGE / OSCAR_ERR_RANGE
+ * for a bad history page, whose tokens are then left out). */
+oscar_status oscar_prefill(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* q,
+                           const void* k, const void* v, int T, void* out, float* lse,
+                           void* scratch, size_t scratch_bytes, int batch,
+                           oscar_stream_t stream);
+
 /* Decode without any device allocation (the pages have no counterpart: this
  * is a deployment convenience of this library).  Same computation, arguments
  * and results as oscar_decode, but the working memory comes from a buffer of
@@ -345,7 +374,10 @@ typedef enum {
   OSCAR_KERNEL_DECODE_MAIN = 3, /* split-K decode over history + window */
   OSCAR_KERNEL_DECODE_MERGE = 4,/* partial merge + un-rotation          */
   OSCAR_KERNEL_STEP = 5,        /* oscar_decode_step's append + q rotation */
-  OSCAR_KERNEL_COUNT = 6
+  OSCAR_KERNEL_PREFILL_PREP = 6,  /* prefill: q rotation and scaling       */
+  OSCAR_KERNEL_PREFILL_ATTN = 7,  /* prefill: split attention over regions */
+  OSCAR_KERNEL_PREFILL_MERGE = 8, /* prefill: split merge + un-rotation    */
+  OSCAR_KERNEL_COUNT = 9
 } oscar_kernel;
 
 oscar_status oscar_profile_enable(oscar_ctx* ctx, int enable);

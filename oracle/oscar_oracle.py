@@ -385,7 +385,8 @@ def three_region_attention(q, win_k, win_v, hist_k_rot, hist_v_rot, R_K, R_V):
     return o, (m + np.log(lsum))[..., 0]
 
 
-def chunk_prefill_attention(q_chunk, k_chunk, v_chunk, win_k, win_v, hist_k_rot, hist_v_rot, R_K, R_V):
+def chunk_prefill_attention(q_chunk, k_chunk, v_chunk, win_k, win_v, hist_k_rot, hist_v_rot, R_K, R_V,
+                            tokens=None):
     """Chunked prefill over the cache of one kv head, float64: T new tokens
     (a prefix-hit extension) attend to the cache as it stands -- the BF16 sink
     and recent window, the INT2 history in the rotated basis -- and causally
@@ -398,7 +399,8 @@ def chunk_prefill_attention(q_chunk, k_chunk, v_chunk, win_k, win_v, hist_k_rot,
     full-precision window tokens.
 
     q_chunk [T][G][d]; k_chunk, v_chunk [T][d]; the rest as in
-    three_region_attention.  Returns (o [T][G][d], lse [T][G]).
+    three_region_attention.  Returns (o [T][G][d], lse [T][G]); with `tokens`
+    (a list of chunk positions) only those rows, in that order.
     """
     q_chunk = np.asarray(q_chunk, dtype=np.float64)
     kc = np.asarray(k_chunk, dtype=np.float64)
@@ -406,7 +408,7 @@ def chunk_prefill_attention(q_chunk, k_chunk, v_chunk, win_k, win_v, hist_k_rot,
     wk = np.asarray(win_k, dtype=np.float64).reshape(-1, q_chunk.shape[-1])
     wv = np.asarray(win_v, dtype=np.float64).reshape(-1, q_chunk.shape[-1])
     outs, lses = [], []
-    for t in range(q_chunk.shape[0]):
+    for t in (range(q_chunk.shape[0]) if tokens is None else tokens):
         o, l = three_region_attention(q_chunk[t], np.concatenate([wk, kc[:t + 1]]),
                                       np.concatenate([wv, vc[:t + 1]]), hist_k_rot, hist_v_rot, R_K, R_V)
         outs.append(o)
