@@ -64,6 +64,22 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def tensor_peak():
+    """Dense fp16/bf16 tensor TFLOP/s (burst: the prefill is timed alone)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def prefill_flops(lengths, T, Hq):
+    """Algorithmic FLOPs of one chunked prefill: chunk token t of a request with
+    L cached tokens scores and sums over L + t + 1 keys, 4·d FLOPs each per query head."""
+    return sum(Hq * 4 * 128 * (L + t + 1) for L in lengths for t in range(T))
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
@@ -178,6 +194,13 @@ def build_workload(wl, dev, n_copies, extra, seed=0, bf16_copies=0):
     qs = torch.stack([torch.cat([synth.draw_queries(stats[h], G, synth.stream_seed(seed, "benchQ", b, h), dev)
                                  for h in range(Hkv)]) for b in range(B)]).contiguous()
     return dict(cfg=cfg, ctx=ctx, copies=copies, K=Ks, V=Vs, q=qs, U=(UK, UV), bf=bf, bctx=bctx, stats=stats)
+
+
+def synth_queries(st, T, G, b, h, dev):
+    """Seeded prefill queries of KV head h of request b: [T][G][128]."""
+    from bit_kv_cache_int2_gb300 import synth
+
+    return synth.draw_queries(st, T * G, synth.stream_seed(0, "benchPQ", b, h), dev).view(T, G, 128)
 
 
 # ------------------------------------------------------------- oracle leg
@@ -327,7 +350,7 @@ def run_ours(args, wl):
     Kp, nd, ne = min(K, 2000), min(K, 1000), min(K, 1000)
     na = min(K, 200)  # demotion-only calls
     total_appends = W + K + Kp + ne + na
-    extra = total_appends // n_copies + 16  # appends per cache copy, with margin
+    extra = max(total_appends // n_copies + 16, 80)  # appends per cache copy, with margin; >= a prefill chunk
     wk = build_workload(wl, dev, n_copies, extra, bf16_copies=2)
     ctx, cfg = wk["ctx"], wk["cfg"]
     scratch = oscar.alloc_scratch(cfg, dev)
@@ -433,6 +456,35 @@ def run_ours(args, wl):
     # per (request, kv head) and K|V: the evicted ring token and the new token in,
     # the new token into the ring, the codes and scale/zero of the demoted token out
     app_bytes = Bsz * Hkv * 2 * (3 * 256 + 32 + (128 // g) * 4)
+    # ---- chunked prefill of 64 tokens over the same caches (attention only)
+    T_pf = 64
+    n_pf = min(K, 100)
+    q_pf = torch.stack([torch.cat([synth_queries(wk["stats"][h], T_pf, wl["Hq"] // Hkv, b, h, dev)
+                                   for h in range(Hkv)], dim=1) for b in range(Bsz)]).contiguous()
+    k_pf = wk["K"][:, :, L0:L0 + T_pf].permute(0, 2, 1, 3).contiguous()
+    v_pf = wk["V"][:, :, L0:L0 + T_pf].permute(0, 2, 1, 3).contiguous()
+    out_pf = torch.empty_like(q_pf)
+    pscratch = oscar.alloc_scratch(cfg, dev, prefill=True)
+    pf_lens = [int(c["seq_lens"].sum()) for c in wk["copies"]]
+    for i in range(3):
+        oscar.oscar_prefill(ctx, 0, wk["copies"][i % n_copies], q_pf, k_pf, v_pf, T_pf, out_pf, None, pscratch, Bsz)
+    pf_us = time_calls(lambda i: oscar.oscar_prefill(ctx, 0, wk["copies"][i % n_copies], q_pf, k_pf, v_pf, T_pf,
+                                                     out_pf, None, pscratch, Bsz), n_pf)
+    oscar.oscar_profile_enable(ctx, True)
+    for i in range(min(n_pf, 20)):
+        oscar.oscar_prefill(ctx, 0, wk["copies"][i % n_copies], q_pf, k_pf, v_pf, T_pf, out_pf, None, pscratch, Bsz)
+    torch.cuda.synchronize()
+    pf_prof = {}
+    for kid in (oscar.KERNEL_PREFILL_PREP, oscar.KERNEL_PREFILL_ATTN, oscar.KERNEL_PREFILL_MERGE):
+        n, tot = oscar.oscar_profile_read(ctx, kid)
+        pf_prof[oscar.KERNEL_NAMES[kid]] = round(tot * 1e3 / max(n, 1), 3)
+    oscar.oscar_profile_read(ctx, 0, reset=True)
+    oscar.oscar_profile_enable(ctx, False)
+    assert oscar.oscar_get_error(ctx) == 0
+    assert torch.isfinite(out_pf.float()).all()
+    pf_flops = statistics.mean(prefill_flops([L // Bsz] * Bsz, T_pf, wl["Hq"]) for L in pf_lens)
+    tpk, tpk_kind = tensor_peak()
+    pf_attn_tf = pf_flops / (pf_prof["prefill_attn"] * 1e-6) / 1e12
     # ---- end to end through the public API with host buffers
     q_h = q.cpu().pin_memory()
     out_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
@@ -489,6 +541,12 @@ def run_ours(args, wl):
                      "achieved_gbs": app_bytes / (app_us * 1e-6) / 1e9,
                      "frac": app_bytes / (app_us * 1e-6) / 1e9 / peak,
                      "note": "one token per (request, kv head): latency-bound, not bandwidth-bound"},
+        "prefill": {"chunk_tokens": T_pf, "us_per_call": pf_us, "kernels_us": pf_prof,
+                    "flops_per_call": pf_flops, "tflops": pf_flops / (pf_us * 1e-6) / 1e12,
+                    "attn_tflops": pf_attn_tf, "peak_tflops": tpk, "peak_kind": tpk_kind,
+                    "attn_frac": pf_attn_tf / tpk,
+                    "note": "64 new tokens per request over the same 100K cache; fp16 mma.sync "
+                            "(legacy tensor path), bound: tensor"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(), "kernel": "decode_main",
                      "bytes_per_launch": bytes_main, "peak_kind": peak_kind},

@@ -61,6 +61,7 @@ struct oscar_ctx {
   int impl = 0;
   int ctas_per_sm = 4;
   int items_per_cta = 1;
+  int prefill_impl = OSCAR_PREFILL_TCGEN05;
   Profiler prof;
 };
 
@@ -455,6 +456,10 @@ oscar_status oscar_set_option(oscar_ctx* ctx, int option, int value) {
       if (value < 1 || value > 8) return OSCAR_ERR_INVALID_ARG;
       ctx->items_per_cta = value;
       return OSCAR_OK;
+    case OSCAR_OPT_PREFILL_IMPL:
+      if (value != OSCAR_PREFILL_TCGEN05 && value != OSCAR_PREFILL_MMA_SYNC) return OSCAR_ERR_INVALID_ARG;
+      ctx->prefill_impl = value;
+      return OSCAR_OK;
     default:
       return OSCAR_ERR_INVALID_ARG;
   }
@@ -579,11 +584,11 @@ oscar_status oscar_prefill(oscar_ctx* ctx, int layer, const oscar_cache* cache, 
   a.RT = (T * G + PF_ROWS - 1) / PF_ROWS;
   const int tiles = batch * Hkv * a.RT;
   int occ = 0;
-  const cudaError_t oe = prefill_ctas_per_sm(&occ);
+  const cudaError_t oe = prefill_ctas_per_sm(&occ, ctx->prefill_impl);
   if (oe != cudaSuccess) return cuda_status(oe);
   if (occ < 1) occ = 1;
-  // history splits: enough CTAs for one wave over the SMs, within the scratch bound
-  int ns = (ctx->num_sms * occ + tiles - 1) / tiles;
+  // history splits: history + window CTAs fill one wave over the SMs, within the scratch bound
+  int ns = (ctx->num_sms * occ) / tiles - 1;
   const int cap = prefill_max_splits(batch, Hkv, G, T);
   a.NS = ns < 1 ? 1 : ns > cap ? cap : ns;
   const PrefillScratch L = prefill_scratch_layout(batch, Hkv, G, T, a.NS);
@@ -600,6 +605,7 @@ oscar_status oscar_prefill(oscar_ctx* ctx, int layer, const oscar_cache* cache, 
   a.part = (float*)(sp + L.off_part);
   a.B = batch;
   a.T = T;
+  a.impl = ctx->prefill_impl;
   a.rot = layer_rot(ctx, layer);
   return cuda_status(launch_prefill(a, (cudaStream_t)stream, &ctx->prof));
 }

@@ -585,6 +585,7 @@ struct PrefillArgs {
   float* alpha;            // scratch [B*Hkv][RT*128]: 2^sigma * log2(e) / sqrt(d)
   float* part;             // scratch [B*Hkv*RT][NS+1][128][PART_STRIDE]
   int B, T, RT, NS;
+  int impl;  // an oscar_prefill_impl value
   LayerRot rot;
 };
 
@@ -593,7 +594,7 @@ struct PrefillScratch {
 };
 PrefillScratch prefill_scratch_layout(int B, int Hkv, int G, int T, int NS);
 int prefill_max_splits(int B, int Hkv, int G, int T);  // NS bound the scratch is sized for
-cudaError_t prefill_ctas_per_sm(int* n);                  // resident attention CTAs per SM
+cudaError_t prefill_ctas_per_sm(int* n, int impl);        // resident attention CTAs per SM
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st, Profiler* prof);
 
 cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* k,

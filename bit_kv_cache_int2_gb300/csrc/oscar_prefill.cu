@@ -549,6 +549,605 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(PrefillArgs a) {
   }
 }
 
+
+// ===================================================== tcgen05 attention
+// The same work split and partial records as prefill_attn_kernel, on the
+// fifth-generation tensor cores: S = Q·K^T and O += P·V as tcgen05.mma with
+// M = 128 query rows, operands in shared memory in the 128-byte-swizzled
+// K-major layout, S, P and O in tensor memory.  Warp roles:
+//   warps 0-3  softmax, one query row per thread (row = TMEM lane)
+//   warps 4-7  tile producers: dequantise a copied INT2 page (or convert BF16
+//              window rows) into the K and V^T tiles
+//   warp 8     bulk copies of INT2 pages into shared memory
+//   warp 9     TMEM allocation and the tcgen05.mma issue (one thread)
+// V^T carries 16 extra rows: a row of ones, whose O column accumulates the
+// softmax row sum l from the same fp16 P the numerator uses, and 15 zero rows
+// (N = 144, a multiple of 16).  O is rescaled lazily: only when a row maximum
+// grows by more than LAZY (log2 units); until then P may reach 2^LAZY.
+namespace tc {
+constexpr int THREADS = 320;
+constexpr int DQ0 = 128;  // first producer thread
+constexpr int TMA_WARP = 8, MMA_WARP = 9;
+constexpr int NKV = 3, NRAW = 4;
+constexpr int VT_ROWS = 144;
+constexpr int Q_BYTES = 2 * PF_ROWS * 128;  // two 64-dim regions of 128 rows x 128 B
+constexpr int K_BYTES = 2 * PAGE * 128;     // two 64-dim regions of 64 tokens x 128 B
+constexpr int VT_BYTES = VT_ROWS * 128;     // channels (+16) x 64 tokens
+constexpr int KV_BYTES = K_BYTES + VT_BYTES;
+constexpr int OFF_Q = 0;
+constexpr int OFF_KV = Q_BYTES;
+constexpr int OFF_RAW = OFF_KV + NKV * KV_BYTES;
+constexpr int OFF_PAIRS = OFF_RAW + NRAW * RAW_SLOT;  // [2][4 groups][32 token pairs] (s2, z2)
+constexpr int OFF_BAR = OFF_PAIRS + 2 * 4 * 32 * 8;
+// barriers
+constexpr int B_RAW_FULL = 0, B_RAW_EMPTY = B_RAW_FULL + NRAW, B_KV_FULL = B_RAW_EMPTY + NRAW,
+              B_KV_EMPTY = B_KV_FULL + NKV, B_S_FULL = B_KV_EMPTY + NKV, B_P_FULL = B_S_FULL + 2,
+              B_O_DONE = B_P_FULL + 2, B_O_FINAL = B_O_DONE + 1, B_Q_FULL = B_O_FINAL + 1,
+              B_DRAIN = B_Q_FULL + 1, NBARS = B_DRAIN + 1;
+constexpr int OFF_INFO = OFF_BAR + NBARS * 8;  // per KV buffer {u64 mask, int causal, pad}; then misc ints
+constexpr int OFF_MISC = OFF_INFO + NKV * 16;  // [0] tmem base, [1] abort, [2..2+NRAW) bad page
+constexpr int SMEM_USED = OFF_MISC + 64;
+constexpr int SMEM = SMEM_USED + 1024;  // slack to align the base to 1024 B
+constexpr int TMEM_COLS = 512;
+constexpr int O_COL = 0, S_COL0 = 256;  // S buffer j at S_COL0 + 128 j (64 columns used)
+constexpr float LAZY = 4.f;
+constexpr uint32_t IDESC_S = (1u << 4) | ((uint32_t)(PAGE >> 3) << 17) | ((uint32_t)(PF_ROWS >> 4) << 24);
+constexpr uint32_t IDESC_PV = (1u << 4) | ((uint32_t)(VT_ROWS >> 3) << 17) | ((uint32_t)(PF_ROWS >> 4) << 24);
+static_assert(OFF_KV % 1024 == 0 && KV_BYTES % 1024 == 0 && K_BYTES % 1024 == 0, "swizzle atoms 1024-aligned");
+static_assert(SMEM <= 227 * 1024, "shared memory");
+static_assert(OFF_BAR % 8 == 0 && OFF_INFO % 8 == 0, "alignment");
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 B apart (the leading offset is unused for this layout).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+__device__ __forceinline__ void arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"((uint32_t)__cvta_generic_to_shared(bar))
+               : "memory");
+}
+
+#define OSCAR_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), \
+                    "=r"(r[i + 6]), "=r"(r[i + 7])
+// 32 consecutive 32-bit TMEM columns of this warp's 32 lanes, one lane per thread
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : OSCAR_R8(0), OSCAR_R8(8), OSCAR_R8(16), OSCAR_R8(24)
+      : "r"(taddr));
+}
+#undef OSCAR_R8
+
+#define OSCAR_W8(i) "r"(v[i]), "r"(v[i + 1]), "r"(v[i + 2]), "r"(v[i + 3]), "r"(v[i + 4]), "r"(v[i + 5]), \
+                    "r"(v[i + 6]), "r"(v[i + 7])
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+      OSCAR_W8(0), OSCAR_W8(8), OSCAR_W8(16), OSCAR_W8(24)
+      : "memory");
+}
+#undef OSCAR_W8
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t ex2_h2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(bar);
+  for (int it = 0; it < (1 << 22); ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((it & 63) == 63 && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+
+// The 128 producer threads agree on a wait's outcome (named barrier 2): all
+// go on or all stop, so none is left behind at a later barrier.
+__device__ __forceinline__ bool producers_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 2, 128, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)ok)
+      : "memory");
+  return r != 0;
+}
+
+// TMEM loads complete at tcgen05.wait::ld; the registers pass through the
+// wait so that no use of them is scheduled before it.
+#define OSCAR_P8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), "+r"(r[i + 5]), \
+                    "+r"(r[i + 6]), "+r"(r[i + 7])
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" : OSCAR_P8(0), OSCAR_P8(8), OSCAR_P8(16), OSCAR_P8(24)::"memory");
+}
+__device__ __forceinline__ void regs_after(uint32_t (&r)[32]) {
+  asm volatile("" : OSCAR_P8(0), OSCAR_P8(8), OSCAR_P8(16), OSCAR_P8(24)::"memory");
+}
+#undef OSCAR_P8
+
+// K tile store: channel pair (c, c + 1), c = 64A + 8I + 2D, of token row tr.
+template <int I>
+__device__ __forceinline__ void k_put(uint8_t* Kt, int tr, int A, int D_, uint32_t w, uint32_t s2, uint32_t z2,
+                                      bool ok) {
+  const uint32_t val = ok ? hfma2u(codes_f16x2<I>(w), s2, z2) : 0u;
+  *(uint32_t*)(Kt + A * (PAGE * 128) + tr * 128 + ((I ^ (tr & 7)) << 4) + 4 * D_) = val;
+}
+
+template <int I>
+__device__ __forceinline__ void v_put(uint8_t* Vt, int ch, int T4, uint32_t w, const uint2* pairs, int nv) {
+  const int t = 8 * I + 2 * T4;
+  const uint2 sz = pairs[t >> 1];
+  uint32_t val = hfma2u(codes_f16x2<I>(w), sz.x, sz.y);
+  if (t + 1 >= nv) val = t < nv ? (val & 0xFFFFu) : 0u;
+  *(uint32_t*)(Vt + ch * 128 + ((I ^ (ch & 7)) << 4) + 4 * T4) = val;
+}
+
+template <int I>
+__device__ __forceinline__ void k_put4(uint8_t* Kt, int tr, int wq, uint4 cw, uint32_t s0a, uint32_t z0a,
+                                       uint32_t s0b, uint32_t z0b, uint32_t s1a, uint32_t z1a, uint32_t s1b,
+                                       uint32_t z1b, bool ok) {
+  // words 4wq + {0, 1, 2, 3} = (D 2wq, A 0), (D 2wq, A 1), (D 2wq + 1, A 0), (D 2wq + 1, A 1);
+  // scale/zero: s{A}{a|b} for I < 4 (a) or I >= 4 (b)
+  const uint32_t sA0 = I < 4 ? s0a : s0b, zA0 = I < 4 ? z0a : z0b;
+  const uint32_t sA1 = I < 4 ? s1a : s1b, zA1 = I < 4 ? z1a : z1b;
+  k_put<I>(Kt, tr, 0, 2 * wq, cw.x, sA0, zA0, ok);
+  k_put<I>(Kt, tr, 1, 2 * wq, cw.y, sA1, zA1, ok);
+  k_put<I>(Kt, tr, 0, 2 * wq + 1, cw.z, sA0, zA0, ok);
+  k_put<I>(Kt, tr, 1, 2 * wq + 1, cw.w, sA1, zA1, ok);
+}
+
+// Dequantise one INT2 head block into K (two 64-channel regions) and V^T
+// tiles, by the 128 producer threads (t = 0..127).  nv = valid tokens.
+__device__ __forceinline__ void dequant_page(uint8_t* Kt, uint8_t* Vt, const uint8_t* raw, uint2* pairs, int g,
+                                             int nv, int t) {
+  const int NG = D / g;
+  // (s, z) pairs of consecutive V tokens per channel group
+  if (t < 32 * NG) {
+    const uint32_t* vsz = (const uint32_t*)(raw + off_v_sz(g));
+    const int gp = t >> 5, j = t & 31;
+    const uint32_t a = vsz[(2 * j) * NG + gp], b = vsz[(2 * j + 1) * NG + gp];
+    pairs[gp * 32 + j] = make_uint2(prmt(a, b, 0x5410u), prmt(a, b, 0x7632u));
+  }
+  asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  {  // K: token tr, words 4wq .. 4wq + 3
+    const int tr = t >> 1, wq = t & 1;
+    const uint4 cw = *(const uint4*)(raw + tr * 32 + 16 * wq);
+    const uint32_t* ksz = (const uint32_t*)(raw + off_k_sz()) + tr * NG;
+    const uint32_t a0 = ksz[0], b0 = ksz[32 / g], a1 = ksz[64 / g], b1 = ksz[96 / g];
+    const uint32_t s0a = prmt(a0, a0, 0x1010u), z0a = prmt(a0, a0, 0x3232u);
+    const uint32_t s0b = prmt(b0, b0, 0x1010u), z0b = prmt(b0, b0, 0x3232u);
+    const uint32_t s1a = prmt(a1, a1, 0x1010u), z1a = prmt(a1, a1, 0x3232u);
+    const uint32_t s1b = prmt(b1, b1, 0x1010u), z1b = prmt(b1, b1, 0x3232u);
+    const bool ok = tr < nv;
+    k_put4<0>(Kt, tr, wq, cw, s0a, z0a, s0b, z0b, s1a, z1a, s1b, z1b, ok);
+    k_put4<1>(Kt, tr, wq, cw, s0a, z0a, s0b, z0b, s1a, z1a, s1b, z1b, ok);
+    k_put4<2>(Kt, tr, wq, cw, s0a, z0a, s0b, z0b, s1a, z1a, s1b, z1b, ok);
+    k_put4<3>(Kt, tr, wq, cw, s0a, z0a, s0b, z0b, s1a, z1a, s1b, z1b, ok);
+    k_put4<4>(Kt, tr, wq, cw, s0a, z0a, s0b, z0b, s1a, z1a, s1b, z1b, ok);
+    k_put4<5>(Kt, tr, wq, cw, s0a, z0a, s0b, z0b, s1a, z1a, s1b, z1b, ok);
+    k_put4<6>(Kt, tr, wq, cw, s0a, z0a, s0b, z0b, s1a, z1a, s1b, z1b, ok);
+    k_put4<7>(Kt, tr, wq, cw, s0a, z0a, s0b, z0b, s1a, z1a, s1b, z1b, ok);
+  }
+  {  // V: word T4 of channels chb + 32k
+    const int T4 = t & 3, chb = t >> 2;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int ch = chb + 32 * k;
+      const uint32_t w = *(const uint32_t*)(raw + 2048 + ch * 16 + 4 * T4);
+      const uint2* pr = pairs + (ch / g) * 32;
+      v_put<0>(Vt, ch, T4, w, pr, nv);
+      v_put<1>(Vt, ch, T4, w, pr, nv);
+      v_put<2>(Vt, ch, T4, w, pr, nv);
+      v_put<3>(Vt, ch, T4, w, pr, nv);
+      v_put<4>(Vt, ch, T4, w, pr, nv);
+      v_put<5>(Vt, ch, T4, w, pr, nv);
+      v_put<6>(Vt, ch, T4, w, pr, nv);
+      v_put<7>(Vt, ch, T4, w, pr, nv);
+    }
+  }
+}
+
+// 64 BF16 tokens (row j at Kb + j·stride, Vb + j·stride) into the K and V^T
+// tiles as fp16; rows with a clear bit in `valid` become zeros.
+__device__ __forceinline__ void convert_bf16(uint8_t* Kt, uint8_t* Vt, const __nv_bfloat16* Kb,
+                                             const __nv_bfloat16* Vb, size_t stride, uint64_t valid, int t) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int u = t + 128 * j, tok = u >> 4, c16 = u & 15;
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if ((valid >> tok) & 1ull) x = *(const uint4*)(Kb + tok * stride + 8 * c16);
+    const uint4 y = make_uint4(bf2_to_h2(x.x), bf2_to_h2(x.y), bf2_to_h2(x.z), bf2_to_h2(x.w));
+    *(uint4*)(Kt + (c16 >> 3) * (PAGE * 128) + tok * 128 + (((c16 & 7) ^ (tok & 7)) << 4)) = y;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int u = t + 128 * j, jp = u & 31, k8 = u >> 5;
+    uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
+    if ((valid >> (2 * jp)) & 1ull) x0 = *(const uint4*)(Vb + (2 * jp) * stride + 8 * k8);
+    if ((valid >> (2 * jp + 1)) & 1ull) x1 = *(const uint4*)(Vb + (2 * jp + 1) * stride + 8 * k8);
+    const uint32_t a[4] = {x0.x, x0.y, x0.z, x0.w}, b[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t lo = i & 1 ? (a[i >> 1] & 0xFFFF0000u) : (a[i >> 1] << 16);
+      const uint32_t hi = i & 1 ? (b[i >> 1] & 0xFFFF0000u) : (b[i >> 1] << 16);
+      *(uint32_t*)(Vt + (8 * k8 + i) * 128 + (((jp >> 2) ^ i) << 4) + 4 * (jp & 3)) =
+          f2_to_h2(__uint_as_float(lo), __uint_as_float(hi));
+    }
+  }
+}
+
+// Window tile kinds: 0 sink, 1..4 ring quarters, 5 chunk.  Does [a, a + n)
+// taken mod 256 meet [lo, lo + 64)?
+__device__ __forceinline__ bool ring_meets(int a, int n, int lo) {
+  if (n <= 0) return false;
+  if (n >= RECENT) return true;
+  const int e = a + n;
+  if (a < lo + 64 && e > lo) return true;
+  return e > RECENT && (e - RECENT) > lo;
+}
+}  // namespace tc
+
+__global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(PrefillArgs a) {
+  using namespace tc;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - ((uint32_t)__cvta_generic_to_shared(smem_raw) & 1023)) & 1023);
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
+  const CacheView& cv = a.cv;
+  const int Hkv = cv.Hkv, G = cv.G;
+  const int tile = blockIdx.x, bk = tile / a.RT, rt = tile % a.RT;
+  const int b = bk / Hkv, kvh = bk % Hkv;
+  const int split = blockIdx.y;
+  const bool win = split == a.NS;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int R = a.T * G, RP = a.RT * PF_ROWS;
+  uint64_t* bars = (uint64_t*)(smem + tc::OFF_BAR);
+  uint8_t* info = smem + tc::OFF_INFO;
+  int* misc = (int*)(smem + OFF_MISC);
+  volatile int* abort_flag = misc + 1;
+
+  pdl_launch_dependents();
+  if (tid == 0) {
+    for (int i = 0; i < NRAW; ++i) {
+      mbar_init(&bars[B_RAW_FULL + i], 1);
+      mbar_init(&bars[B_RAW_EMPTY + i], 128);
+    }
+    for (int i = 0; i < NKV; ++i) {
+      mbar_init(&bars[B_KV_FULL + i], 128);
+      mbar_init(&bars[B_KV_EMPTY + i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[B_S_FULL + i], 1);
+      mbar_init(&bars[B_P_FULL + i], 4);
+    }
+    mbar_init(&bars[B_O_DONE], 1);
+    mbar_init(&bars[B_O_FINAL], 1);
+    mbar_init(&bars[B_Q_FULL], 128);
+    mbar_init(&bars[B_DRAIN], 1);
+    misc[1] = 0;
+    for (int i = 0; i < NRAW; ++i) misc[2 + i] = 0;
+  }
+  if (warp == MMA_WARP) {  // whole warp: allocate the tensor memory, publish its address
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(&misc[0])),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
+  fence_proxy_async();
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = (uint32_t)misc[0];
+  pdl_wait();
+
+  // this CTA's tiles
+  const size_t head = (size_t)b * Hkv + kvh;
+  const int hist = cv.hist_lens[b];
+  int pages = hist > 0 ? (hist + PAGE - 1) / PAGE : 0;
+  if (pages > cv.max_pages_per_req) {
+    if (tid == 0 && split == 0) record_error(cv.err, OSCAR_ERR_RANGE);
+    pages = cv.max_pages_per_req;
+  }
+  const int Lq = cv.seq_lens[b];
+  const int nsink = Lq < SINK ? Lq : SINK;
+  const int recent = Lq > SINK ? Lq - SINK - hist : 0;
+  const int h0 = ((hist % RECENT) + RECENT) % RECENT;
+  int p0 = 0, n = 0;
+  int kinds[6];
+  if (!win) {
+    p0 = (int)((long long)split * pages / a.NS);
+    n = (int)((long long)(split + 1) * pages / a.NS) - p0;
+  } else {
+    if (nsink > 0) kinds[n++] = 0;
+    for (int q = 0; q < 4; ++q)
+      if (ring_meets(h0, recent, 64 * q)) kinds[n++] = 1 + q;
+    kinds[n++] = 5;
+  }
+  const int gbytes = cv.head_bytes;
+  const int32_t* ptab = cv.page_table + (size_t)b * cv.max_pages_per_req;
+
+  if (warp == TMA_WARP) {
+    // ------------------------------------------------ page copies
+    int issued = 0;
+    if (!win && lane == 0) {
+      for (int i = 0; i < n; ++i) {
+        const int slot = i % NRAW;
+        if (i >= NRAW && !wait_bar(&bars[B_RAW_EMPTY + slot], ((i / NRAW) - 1) & 1, abort_flag)) break;
+        const int pid = ptab[p0 + i];
+        const bool ok = pid >= 0 && pid < cv.num_pages;
+        misc[2 + slot] = ok ? 0 : 1;
+        if (!ok) {
+          record_error(cv.err, pid < 0 ? OSCAR_ERR_NO_PAGE : OSCAR_ERR_RANGE);
+          mbar_expect_tx(&bars[B_RAW_FULL + slot], 0);
+        } else {
+          mbar_expect_tx(&bars[B_RAW_FULL + slot], (uint32_t)gbytes);
+          bulk_g2s(smem + tc::OFF_RAW + slot * RAW_SLOT, cv.pool + (size_t)pid * cv.page_bytes + (size_t)kvh * gbytes,
+                   (uint32_t)gbytes, &bars[B_RAW_FULL + slot]);
+        }
+        issued = i + 1;
+      }
+      // every copy this CTA started has landed before it exits
+      for (int i = issued - NRAW < 0 ? 0 : issued - NRAW; i < issued; ++i)
+        mbar_wait(&bars[B_RAW_FULL + i % NRAW], (i / NRAW) & 1);
+    }
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------ tcgen05.mma issue
+    if (lane == 0) {
+      bool ok = wait_bar(&bars[B_Q_FULL], 0, abort_flag);
+      const uint32_t qa = sbase + OFF_Q;
+      for (int i = 0; ok && i <= n; ++i) {
+        if (i < n) {  // S(i) = Q·K(i)^T
+          const int kb = i % NKV;
+          if (!wait_bar(&bars[B_KV_FULL + kb], (i / NKV) & 1, abort_flag)) break;
+          fence_after();
+          const uint32_t kaddr = sbase + OFF_KV + kb * KV_BYTES;
+          const uint32_t d = tmem + S_COL0 + 128 * (i & 1);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ss(d, sdesc(qa + (ks >> 2) * (PF_ROWS * 128) + (ks & 3) * 32),
+                   sdesc(kaddr + (ks >> 2) * (PAGE * 128) + (ks & 3) * 32), IDESC_S, ks > 0);
+          commit(&bars[B_S_FULL + (i & 1)]);
+        }
+        if (i >= 1) {  // O += P(i-1)·V(i-1)
+          const int j = i - 1, kb = j % NKV;
+          if (!wait_bar(&bars[B_P_FULL + (j & 1)], (j >> 1) & 1, abort_flag)) break;
+          fence_after();
+          const uint32_t vaddr = sbase + OFF_KV + kb * KV_BYTES + K_BYTES;
+          const uint32_t pa = tmem + S_COL0 + 128 * (j & 1);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + O_COL, pa + 8 * kk, sdesc(vaddr + kk * 32), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+          commit(&bars[B_KV_EMPTY + kb]);
+          commit(&bars[B_O_DONE]);
+          if (j == n - 1) commit(&bars[B_O_FINAL]);
+        }
+      }
+      // all issued MMAs complete before the tensor memory is released
+      commit(&bars[B_DRAIN]);
+      mbar_wait(&bars[B_DRAIN], 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------ tile producers
+    const int t = tid - DQ0;
+    {  // query rows -> Q tile (rotated for history, raw for the window)
+      const __half* qrow =
+          a.qh + ((size_t)(win ? 1 : 0) * a.B * Hkv + bk) * RP * D + (size_t)(rt * PF_ROWS + t) * D;
+#pragma unroll
+      for (int c16 = 0; c16 < 16; ++c16) {
+        const uint4 x = *(const uint4*)(qrow + 8 * c16);
+        *(uint4*)(smem + OFF_Q + (c16 >> 3) * (PF_ROWS * 128) + t * 128 + (((c16 & 7) ^ (t & 7)) << 4)) = x;
+      }
+      // ones row (row sums) and zero rows below the 128 channels of every V^T buffer
+      for (int kb = 0; kb < NKV; ++kb) {
+        const uint32_t v = (t < 8) ? 0x3C003C00u : 0u;
+        *(uint4*)(smem + OFF_KV + kb * KV_BYTES + K_BYTES + 128 * 128 + 16 * t) = make_uint4(v, v, v, v);
+      }
+      fence_proxy_async();
+      arrive(&bars[B_Q_FULL]);
+    }
+    uint2* pairs0 = (uint2*)(smem + OFF_PAIRS);
+    for (int i = 0; i < n; ++i) {
+      const int kb = i % NKV;
+      uint8_t* Kt = smem + OFF_KV + kb * KV_BYTES;
+      uint8_t* Vt = Kt + K_BYTES;
+      bool okw = i < NKV || wait_bar(&bars[B_KV_EMPTY + kb], ((i / NKV) - 1) & 1, abort_flag);
+      if (!win) okw = okw && wait_bar(&bars[B_RAW_FULL + i % NRAW], (i / NRAW) & 1, abort_flag);
+      if (!producers_all(okw)) break;
+      uint64_t mask;
+      int causal = 0;
+      if (!win) {
+        const int slot = i % NRAW;
+        const int pg = p0 + i;
+        int nv = pg == pages - 1 ? hist - pg * PAGE : PAGE;
+        if (misc[2 + slot]) nv = 0;
+        dequant_page(Kt, Vt, smem + tc::OFF_RAW + slot * RAW_SLOT, pairs0 + (i & 1) * 128, cv.g, nv, t);
+        mask = low_mask(nv);
+        arrive(&bars[B_RAW_EMPTY + slot]);
+      } else {
+        const int kind = kinds[i];
+        const __nv_bfloat16 *Kb, *Vb;
+        size_t stride = D;
+        if (kind == 0) {
+          mask = low_mask(nsink);
+          Kb = cv.sink_k + head * SINK * D;
+          Vb = cv.sink_v + head * SINK * D;
+        } else if (kind <= 4) {
+          const int s0 = 64 * (kind - 1);
+          const uint32_t lo = __ballot_sync(0xffffffffu, ((s0 + lane - h0 + RECENT) % RECENT) < recent);
+          const uint32_t hi = __ballot_sync(0xffffffffu, ((s0 + 32 + lane - h0 + RECENT) % RECENT) < recent);
+          mask = ((uint64_t)hi << 32) | lo;
+          Kb = cv.ring_k + (head * RECENT + s0) * D;
+          Vb = cv.ring_v + (head * RECENT + s0) * D;
+        } else {
+          mask = low_mask(a.T);
+          causal = 1;
+          stride = (size_t)Hkv * D;
+          Kb = a.k + ((size_t)b * a.T * Hkv + kvh) * D;
+          Vb = a.v + ((size_t)b * a.T * Hkv + kvh) * D;
+        }
+        convert_bf16(Kt, Vt, Kb, Vb, stride, mask, t);
+      }
+      if (t == 0) {
+        *(uint64_t*)(info + kb * 16) = mask;
+        *(int*)(info + kb * 16 + 8) = causal;
+      }
+      fence_proxy_async();
+      arrive(&bars[B_KV_FULL + kb]);
+    }
+  } else {
+    // ------------------------------------------------ softmax, one row per thread
+    const int row = tid;  // = TMEM lane
+    const int grow = rt * PF_ROWS + row;
+    const float al = a.alpha[(size_t)bk * RP + grow];
+    const int trow = grow / G;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    float m_run = -1e30f;
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      const int kb = i % NKV, sb = i & 1;
+      if (!__all_sync(0xffffffffu, wait_bar(&bars[B_KV_FULL + kb], (i / NKV) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      const uint64_t mask = *(const uint64_t*)(info + kb * 16);
+      const bool causal = *(const int*)(info + kb * 16 + 8) != 0;
+      if (!__all_sync(0xffffffffu, wait_bar(&bars[B_S_FULL + sb], (i >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      fence_after();
+      const uint32_t sa = tmem + lane_base + S_COL0 + 128 * sb;
+      uint32_t r0[32], r1[32];
+      tmem_ld32(sa, r0);
+      tmem_ld32(sa + 32, r1);
+      tmem_ld_wait_regs(r0);
+      regs_after(r1);
+      float x[64];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        x[j] = __uint_as_float(r0[j]) * al;
+        x[32 + j] = __uint_as_float(r1[j]) * al;
+      }
+      if (mask != ~0ull || causal) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          if (!((mask >> j) & 1ull) || (causal && j > trow)) x[j] = -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int j = 1; j < 64; ++j) mx = fmaxf(mx, x[j]);
+      if (i == 0) {
+        m_run = fmaxf(m_run, mx);
+      } else if (__any_sync(0xffffffffu, mx > m_run + LAZY)) {
+        // O must hold P(i-1)·V(i-1) before it is rescaled
+        if (!__all_sync(0xffffffffu, wait_bar(&bars[B_O_DONE], (i - 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        fence_after();
+        const float m_new = fmaxf(m_run, mx);
+        const float f = ex2(m_run - m_new);
+        m_run = m_new;
+        const uint32_t oa = tmem + lane_base + O_COL;
+#pragma unroll 1
+        for (int c = 0; c < 160; c += 32) {  // columns 0..159 (the 144 in use and 16 unused)
+          uint32_t v[32];
+          tmem_ld32(oa + c, v);
+          tmem_ld_wait_regs(v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * f);
+          tmem_st32(oa + c, v);
+          tmem_st_wait();
+        }
+      }
+      uint32_t p[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) p[j] = ex2_h2(f2_to_h2(x[2 * j] - m_run, x[2 * j + 1] - m_run));
+      tmem_st32(sa, p);
+      tmem_st_wait();
+      fence_before();
+      __syncwarp();
+      if (lane == 0) arrive(&bars[B_P_FULL + sb]);
+    }
+    // the partial record: m (log2 units), l, o (unnormalised)
+    if (ok && n > 0) ok = __all_sync(0xffffffffu, wait_bar(&bars[B_O_FINAL], 0, abort_flag));
+    float* rec = a.part + (((size_t)tile * (a.NS + 1) + split) * PF_ROWS + row) * PART_STRIDE;
+    if (ok && n > 0) {
+      fence_after();
+      const uint32_t oa = tmem + lane_base + O_COL;
+#pragma unroll 1
+      for (int c = 0; c < 160; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(oa + c, v);
+        tmem_ld_wait_regs(v);
+        if (grow < R) {
+          if (c < 128) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *(float4*)(rec + PART_O + c + j) = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                                             __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+          } else {
+            rec[0] = m_run;
+            rec[1] = __uint_as_float(v[0]);
+          }
+        }
+      }
+    } else if (grow < R) {  // nothing here (or aborted): an empty partial
+      rec[0] = -1e30f;
+      rec[1] = 0.f;
+      for (int j = 0; j < D; j += 4) *(float4*)(rec + PART_O + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag) record_error(cv.err, OSCAR_ERR_TIMEOUT);
+  if (warp == MMA_WARP) {
+    __syncwarp();
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
 }  // namespace
 
 PrefillScratch prefill_scratch_layout(int B, int Hkv, int G, int T, int NS) {
@@ -577,17 +1176,20 @@ int prefill_max_splits(int B, int Hkv, int G, int T) {
 static cudaError_t ensure_prefill_smem() {
   static int done = 0;  // per process; the attribute is per device function
   if (done) return cudaSuccess;
-  const cudaError_t e =
-      cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM);
+  cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM);
   if (e == cudaSuccess) done = 1;
   return e;
 }
 
-cudaError_t prefill_ctas_per_sm(int* n) {
+cudaError_t prefill_ctas_per_sm(int* n, int impl) {
   *n = 0;
   const cudaError_t e = ensure_prefill_smem();
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, prefill_attn_kernel, PF_THREADS, PF_SMEM);
+  if (impl == OSCAR_PREFILL_MMA_SYNC)
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, prefill_attn_kernel, PF_THREADS, PF_SMEM);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, prefill_tc_kernel, tc::THREADS, tc::SMEM);
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st, Profiler* prof) {
@@ -599,7 +1201,10 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st, Profiler* prof
   prof_end(prof, OSCAR_KERNEL_PREFILL_PREP, st);
   if (e != cudaSuccess) return e;
   prof_begin(prof, OSCAR_KERNEL_PREFILL_ATTN, st);
-  e = launch_pdl(prefill_attn_kernel, dim3(tiles, a.NS + 1), dim3(PF_THREADS), PF_SMEM, st, a);
+  if (a.impl == OSCAR_PREFILL_MMA_SYNC)
+    e = launch_pdl(prefill_attn_kernel, dim3(tiles, a.NS + 1), dim3(PF_THREADS), PF_SMEM, st, a);
+  else
+    e = launch_pdl(prefill_tc_kernel, dim3(tiles, a.NS + 1), dim3(tc::THREADS), tc::SMEM, st, a);
   prof_end(prof, OSCAR_KERNEL_PREFILL_ATTN, st);
   if (e != cudaSuccess) return e;
   prof_begin(prof, OSCAR_KERNEL_PREFILL_MERGE, st);

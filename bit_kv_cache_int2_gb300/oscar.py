@@ -40,6 +40,9 @@ DECODE_CUDA_CORE = 1
 DECODE_TENSOR_SINGLE = 2  # tensor cores, one page per tile
 OPT_CTAS_PER_SM = 1
 OPT_ITEMS_PER_CTA = 2
+OPT_PREFILL_IMPL = 3
+PREFILL_TCGEN05 = 0  # tcgen05.mma, S/P/O in tensor memory
+PREFILL_MMA_SYNC = 1  # mma.sync
 
 
 class OscarError(RuntimeError):

@@ -109,10 +109,17 @@ typedef enum {
   OSCAR_DECODE_TENSOR_SINGLE = 2  /* tensor cores, one page per tile at any group size */
 } oscar_decode_impl;
 
+/* Prefill attention kernels (oscar_prefill). */
+typedef enum {
+  OSCAR_PREFILL_TCGEN05 = 0, /* tcgen05.mma, S/P/O in tensor memory, warp-specialised (default) */
+  OSCAR_PREFILL_MMA_SYNC = 1 /* mma.sync, eight warps share each dequantised page */
+} oscar_prefill_impl;
+
 typedef enum {
   OSCAR_OPT_DECODE_IMPL = 0, /* an oscar_decode_impl value (default OSCAR_DECODE_TENSOR) */
   OSCAR_OPT_CTAS_PER_SM = 1, /* persistent decode CTAs per SM, 1..4 (default 4), capped by occupancy */
-  OSCAR_OPT_ITEMS_PER_CTA = 2 /* work items per decode CTA the scheduler aims for, 1..8 (default 1) */
+  OSCAR_OPT_ITEMS_PER_CTA = 2, /* work items per decode CTA the scheduler aims for, 1..8 (default 1) */
+  OSCAR_OPT_PREFILL_IMPL = 3 /* an oscar_prefill_impl value (default OSCAR_PREFILL_TCGEN05) */
 } oscar_option;
 
 typedef struct {

@@ -43,8 +43,9 @@ def chunk_inputs(sc, T, seed):
     return (torch.stack(qs).contiguous(), torch.stack(ks).contiguous(), torch.stack(vs).contiguous())
 
 
-def run_prefill(sc, q, k, v, with_lse=True):
+def run_prefill(sc, q, k, v, with_lse=True, impl=oscar.PREFILL_TCGEN05):
     Bn, T = q.shape[0], q.shape[1]
+    oscar.oscar_set_option(sc.ctx, oscar.OPT_PREFILL_IMPL, impl)
     out = torch.full_like(q, float("nan"))
     lse = torch.full((Bn, T, sc.Hq), float("nan"), dtype=torch.float32, device="cuda") if with_lse else None
     scratch = oscar.alloc_scratch(sc.cfg, prefill=True)
@@ -97,14 +98,18 @@ CASES = [
 ]
 
 
+IMPLS = [oscar.PREFILL_TCGEN05, oscar.PREFILL_MMA_SYNC]
+
+
+@pytest.mark.parametrize("impl", IMPLS, ids=["tcgen05", "mma_sync"])
 @pytest.mark.parametrize("lengths,T,Hq,Hkv,g,mode", CASES)
-def test_prefill_matches_oracle(lengths, T, Hq, Hkv, g, mode):
+def test_prefill_matches_oracle(lengths, T, Hq, Hkv, g, mode, impl):
     sc = GS.build(f"pf{len(lengths)}_{T}", lengths, Hq=Hq, Hkv=Hkv, g=g, mode=mode, extra_tokens=T, calib_n=512)
     try:
         q, k, v = chunk_inputs(sc, T, seed=31)
         seq0 = sc.cache["seq_lens"].clone()
         hist0 = sc.cache["hist_lens"].clone()
-        out, lse = run_prefill(sc, q, k, v)
+        out, lse = run_prefill(sc, q, k, v, impl=impl)
         assert oscar.oscar_get_error(sc.ctx) == 0
         # the chunk is not stored
         assert torch.equal(sc.cache["seq_lens"], seq0) and torch.equal(sc.cache["hist_lens"], hist0)
@@ -113,12 +118,13 @@ def test_prefill_matches_oracle(lengths, T, Hq, Hkv, g, mode):
         sc.close()
 
 
-def test_prefill_without_lse_and_repeatable():
+@pytest.mark.parametrize("impl", IMPLS, ids=["tcgen05", "mma_sync"])
+def test_prefill_without_lse_and_repeatable(impl):
     sc = GS.build("pf_nolse", [1500], Hq=4, Hkv=1, g=128, extra_tokens=20, calib_n=512)
     try:
         q, k, v = chunk_inputs(sc, 20, seed=32)
-        out_a, lse_a = run_prefill(sc, q, k, v)
-        out_b, _ = run_prefill(sc, q, k, v, with_lse=False)
+        out_a, lse_a = run_prefill(sc, q, k, v, impl=impl)
+        out_b, _ = run_prefill(sc, q, k, v, with_lse=False, impl=impl)
         assert torch.equal(out_a, out_b)  # same work split, same arithmetic
         check_all(sc, q, k, v, out_b, None)
     finally:
@@ -138,13 +144,14 @@ def test_prefill_rejects_bad_chunk_length():
         sc.close()
 
 
-def test_prefill_qwen3_8b_100k_sampled():
+@pytest.mark.parametrize("impl", IMPLS, ids=["tcgen05", "mma_sync"])
+def test_prefill_qwen3_8b_100k_sampled(impl):
     """32 q / 8 kv heads, g128, 100,000 cached tokens, a 64-token chunk: tokens
     0, 31 and 63 of every head checked."""
     sc = GS.build("pf100k", [100000], Hq=32, Hkv=8, g=128, extra_tokens=64, calib_n=1024)
     try:
         q, k, v = chunk_inputs(sc, 64, seed=34)
-        out, lse = run_prefill(sc, q, k, v)
+        out, lse = run_prefill(sc, q, k, v, impl=impl)
         assert oscar.oscar_get_error(sc.ctx) == 0
         hc = GS.HostCache(sc)
         G = 4
