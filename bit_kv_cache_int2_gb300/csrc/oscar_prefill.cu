@@ -475,12 +475,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_attn_kernel(PrefillArgs
 
 __global__ void __launch_bounds__(128) prefill_merge_kernel(PrefillArgs a) {
   __shared__ float xs[MERGE_ROWS][D];
-  __shared__ float wsh[MERGE_ROWS][PF_MAX_SPLITS + 1];
+  __shared__ float wsh[MERGE_ROWS][2 * (PF_MAX_SPLITS + 1)];
   __shared__ float linv[MERGE_ROWS], lsev[MERGE_ROWS];
   const CacheView& cv = a.cv;
   const int tile = blockIdx.x, bk = tile / a.RT, rt = tile % a.RT;
   const int b = bk / cv.Hkv, kvh = bk % cv.Hkv, G = cv.G;
-  const int R = a.T * G, NS = a.NS, NSP = NS + 1;
+  // records per tile: rpc per attention CTA; the last rpc are the window's
+  const int R = a.T * G, NH = a.NS * a.rpc, NSP = (a.NS + 1) * a.rpc;
   const int i0 = MERGE_ROWS * blockIdx.y;
   const int c = threadIdx.x, warp = c >> 5, lane = c & 31;
   pdl_wait();
@@ -490,9 +491,9 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(PrefillArgs a) {
   const size_t ss = (size_t)PF_ROWS * PART_STRIDE;  // between splits
   for (int j = warp; j < MERGE_ROWS; j += 4) {
     const float* rb = base + (size_t)(i0 + j) * PART_STRIDE;
-    float mv[3], lv[3], M = -INFINITY;
+    float mv[5], lv[5], M = -INFINITY;
 #pragma unroll
-    for (int q = 0; q < 3; ++q) {
+    for (int q = 0; q < 5; ++q) {
       const int s = lane + 32 * q;
       mv[q] = s < NSP ? rb[s * ss] : -INFINITY;
       lv[q] = s < NSP ? rb[s * ss + 1] : 0.f;
@@ -502,7 +503,7 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(PrefillArgs a) {
     for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float L = 0.f;
 #pragma unroll
-    for (int q = 0; q < 3; ++q) {
+    for (int q = 0; q < 5; ++q) {
       const int s = lane + 32 * q;
       if (s < NSP) {
         const float w = ex2(mv[q] - M);
@@ -522,10 +523,11 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(PrefillArgs a) {
 #pragma unroll
   for (int j = 0; j < MERGE_ROWS; ++j) {
     const float* rb = base + (size_t)(i0 + j) * PART_STRIDE + PART_O + c;
-    float acc = 0.f;
-    for (int s = 0; s < NS; ++s) acc = fmaf(wsh[j][s], rb[s * ss], acc);
+    float acc = 0.f, aw = 0.f;
+    for (int s = 0; s < NH; ++s) acc = fmaf(wsh[j][s], rb[s * ss], acc);
+    for (int s = NH; s < NSP; ++s) aw = fmaf(wsh[j][s], rb[s * ss], aw);
     xs[j][c] = acc;
-    ow[j] = wsh[j][NS] * rb[NS * ss];
+    ow[j] = aw;
   }
   __syncthreads();
   // o = o'·R_V^T: y_c = sum_k o'_k R_V[c][k], RVt row k = column k of R_V^T
@@ -553,43 +555,46 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(PrefillArgs a) {
 // ===================================================== tcgen05 attention
 // The same work split and partial records as prefill_attn_kernel, on the
 // fifth-generation tensor cores: S = Q·K^T and O += P·V as tcgen05.mma with
-// M = 128 query rows, operands in shared memory in the 128-byte-swizzled
-// K-major layout, S, P and O in tensor memory.  Warp roles:
-//   warps 0-3  softmax, one query row per thread (row = TMEM lane)
-//   warps 4-7  tile producers: dequantise a copied INT2 page (or convert BF16
+// M = 128 query rows; K and V^T in shared memory in the 128-byte-swizzled
+// K-major layout; Q, S, P and O in tensor memory (Q and P are the A operands,
+// so shared memory bandwidth goes to K and V only).  Warp roles:
+//   warps 0-7  softmax, two warpgroups taking alternate pages, one query
+//              row per thread (row = TMEM lane), each with its own O
+//              accumulator (the two are merged like history splits)
+//   warps 8-15 tile producers: dequantise a copied INT2 page (or convert BF16
 //              window rows) into the K and V^T tiles
-//   warp 8     bulk copies of INT2 pages into shared memory
-//   warp 9     TMEM allocation and the tcgen05.mma issue (one thread)
+//   warp 16    TMEM allocation and the tcgen05.mma issue (one thread)
+//   warp 17    bulk copies of the INT2 pages into shared memory
 // V^T carries 16 extra rows: a row of ones, whose O column accumulates the
 // softmax row sum l from the same fp16 P the numerator uses, and 15 zero rows
 // (N = 144, a multiple of 16).  O is rescaled lazily: only when a row maximum
 // grows by more than LAZY (log2 units); until then P may reach 2^LAZY.
 namespace tc {
-constexpr int THREADS = 320;
-constexpr int DQ0 = 128;  // first producer thread
-constexpr int TMA_WARP = 8, MMA_WARP = 9;
-constexpr int NKV = 3, NRAW = 4;
+constexpr int THREADS = 576;
+constexpr int DQ0 = 256;    // first producer thread
+constexpr int NPROD = 256;  // producer threads (warps 8-15)
+constexpr int MMA_WARP = 16, TMA_WARP = 17;
+constexpr int NKV = 4, NRAW = 8;
 constexpr int VT_ROWS = 144;
-constexpr int Q_BYTES = 2 * PF_ROWS * 128;  // two 64-dim regions of 128 rows x 128 B
 constexpr int K_BYTES = 2 * PAGE * 128;     // two 64-dim regions of 64 tokens x 128 B
 constexpr int VT_BYTES = VT_ROWS * 128;     // channels (+16) x 64 tokens
 constexpr int KV_BYTES = K_BYTES + VT_BYTES;
-constexpr int OFF_Q = 0;
-constexpr int OFF_KV = Q_BYTES;
+constexpr int OFF_KV = 0;
 constexpr int OFF_RAW = OFF_KV + NKV * KV_BYTES;
 constexpr int OFF_PAIRS = OFF_RAW + NRAW * RAW_SLOT;  // [2][4 groups][32 token pairs] (s2, z2)
 constexpr int OFF_BAR = OFF_PAIRS + 2 * 4 * 32 * 8;
 // barriers
 constexpr int B_RAW_FULL = 0, B_RAW_EMPTY = B_RAW_FULL + NRAW, B_KV_FULL = B_RAW_EMPTY + NRAW,
-              B_KV_EMPTY = B_KV_FULL + NKV, B_S_FULL = B_KV_EMPTY + NKV, B_P_FULL = B_S_FULL + 2,
-              B_O_DONE = B_P_FULL + 2, B_O_FINAL = B_O_DONE + 1, B_Q_FULL = B_O_FINAL + 1,
-              B_DRAIN = B_Q_FULL + 1, NBARS = B_DRAIN + 1;
+              B_KV_EMPTY = B_KV_FULL + NKV,
+              B_S_FULL = B_KV_EMPTY + NKV, B_P_FULL = B_S_FULL + 2, B_O_FINAL = B_P_FULL + 2,
+              B_Q_FULL = B_O_FINAL + 2, B_DRAIN = B_Q_FULL + 1, NBARS = B_DRAIN + 1;
 constexpr int OFF_INFO = OFF_BAR + NBARS * 8;  // per KV buffer {u64 mask, int causal, pad}; then misc ints
 constexpr int OFF_MISC = OFF_INFO + NKV * 16;  // [0] tmem base, [1] abort, [2..2+NRAW) bad page
 constexpr int SMEM_USED = OFF_MISC + 64;
 constexpr int SMEM = SMEM_USED + 1024;  // slack to align the base to 1024 B
 constexpr int TMEM_COLS = 512;
-constexpr int O_COL = 0, S_COL0 = 256;  // S buffer j at S_COL0 + 128 j (64 columns used)
+// O of warpgroup w at 160 w (144 used), Q at 320, S (and P) buffer j at 384 + 64 j
+constexpr int O_COL0 = 0, Q_COL = 320, S_COL0 = 384;
 constexpr float LAZY = 4.f;
 constexpr uint32_t IDESC_S = (1u << 4) | ((uint32_t)(PAGE >> 3) << 17) | ((uint32_t)(PF_ROWS >> 4) << 24);
 constexpr uint32_t IDESC_PV = (1u << 4) | ((uint32_t)(VT_ROWS >> 3) << 17) | ((uint32_t)(PF_ROWS >> 4) << 24);
@@ -602,13 +607,6 @@ static_assert(OFF_BAR % 8 == 0 && OFF_INFO % 8 == 0, "alignment");
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
 __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -680,12 +678,12 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   return false;
 }
 
-// The 128 producer threads agree on a wait's outcome (named barrier 2): all
-// go on or all stop, so none is left behind at a later barrier.
+// The producer threads agree on a wait's outcome (named barrier 2): all go
+// on or all stop, so none is left behind at a later barrier.
 __device__ __forceinline__ bool producers_all(bool ok) {
   uint32_t r;
   asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 2, 128, p;\n"
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 2, 256, p;\n"
       " selp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(r)
       : "r"((uint32_t)ok)
@@ -705,84 +703,90 @@ __device__ __forceinline__ void regs_after(uint32_t (&r)[32]) {
 }
 #undef OSCAR_P8
 
-// K tile store: channel pair (c, c + 1), c = 64A + 8I + 2D, of token row tr.
+// K chunk I (channels 64A + 8I .. +7) of token tr: words 2D + A, D = 0..3.
 template <int I>
-__device__ __forceinline__ void k_put(uint8_t* Kt, int tr, int A, int D_, uint32_t w, uint32_t s2, uint32_t z2,
-                                      bool ok) {
-  const uint32_t val = ok ? hfma2u(codes_f16x2<I>(w), s2, z2) : 0u;
-  *(uint32_t*)(Kt + A * (PAGE * 128) + tr * 128 + ((I ^ (tr & 7)) << 4) + 4 * D_) = val;
+__device__ __forceinline__ void k_chunk(uint8_t* Kt, int tr, int A, uint32_t w0, uint32_t w1, uint32_t w2,
+                                        uint32_t w3, uint32_t s2, uint32_t z2, bool ok) {
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (ok)
+    v = make_uint4(hfma2u(codes_f16x2<I>(w0), s2, z2), hfma2u(codes_f16x2<I>(w1), s2, z2),
+                   hfma2u(codes_f16x2<I>(w2), s2, z2), hfma2u(codes_f16x2<I>(w3), s2, z2));
+  *(uint4*)(Kt + A * (PAGE * 128) + tr * 128 + ((I ^ (tr & 7)) << 4)) = v;
 }
 
-template <int I>
-__device__ __forceinline__ void v_put(uint8_t* Vt, int ch, int T4, uint32_t w, const uint2* pairs, int nv) {
-  const int t = 8 * I + 2 * T4;
-  const uint2 sz = pairs[t >> 1];
-  uint32_t val = hfma2u(codes_f16x2<I>(w), sz.x, sz.y);
-  if (t + 1 >= nv) val = t < nv ? (val & 0xFFFFu) : 0u;
-  *(uint32_t*)(Vt + ch * 128 + ((I ^ (ch & 7)) << 4) + 4 * T4) = val;
+// V^T chunk I (token slots 8I .. 8I + 7) of channel ch: word T holds slots
+// 8I + 2T and 8I + 2T + 1; pr = the channel group's (s, z) token-pair table.
+template <int I, bool FULL>
+__device__ __forceinline__ void v_chunk(uint8_t* Vt, int ch, uint4 w, const uint2* pr, int nv) {
+  const uint4 p01 = *(const uint4*)(pr + 4 * I), p23 = *(const uint4*)(pr + 4 * I + 2);
+  uint32_t v0 = hfma2u(codes_f16x2<I>(w.x), p01.x, p01.y);
+  uint32_t v1 = hfma2u(codes_f16x2<I>(w.y), p01.z, p01.w);
+  uint32_t v2 = hfma2u(codes_f16x2<I>(w.z), p23.x, p23.y);
+  uint32_t v3 = hfma2u(codes_f16x2<I>(w.w), p23.z, p23.w);
+  if (!FULL) {
+    const int t0 = 8 * I;
+    auto cut = [&](uint32_t v, int t) { return t + 1 < nv ? v : t < nv ? (v & 0xFFFFu) : 0u; };
+    v0 = cut(v0, t0);
+    v1 = cut(v1, t0 + 2);
+    v2 = cut(v2, t0 + 4);
+    v3 = cut(v3, t0 + 6);
+  }
+  *(uint4*)(Vt + ch * 128 + ((I ^ (ch & 7)) << 4)) = make_uint4(v0, v1, v2, v3);
 }
 
-template <int I>
-__device__ __forceinline__ void k_put4(uint8_t* Kt, int tr, int wq, uint4 cw, uint32_t s0a, uint32_t z0a,
-                                       uint32_t s0b, uint32_t z0b, uint32_t s1a, uint32_t z1a, uint32_t s1b,
-                                       uint32_t z1b, bool ok) {
-  // words 4wq + {0, 1, 2, 3} = (D 2wq, A 0), (D 2wq, A 1), (D 2wq + 1, A 0), (D 2wq + 1, A 1);
-  // scale/zero: s{A}{a|b} for I < 4 (a) or I >= 4 (b)
-  const uint32_t sA0 = I < 4 ? s0a : s0b, zA0 = I < 4 ? z0a : z0b;
-  const uint32_t sA1 = I < 4 ? s1a : s1b, zA1 = I < 4 ? z1a : z1b;
-  k_put<I>(Kt, tr, 0, 2 * wq, cw.x, sA0, zA0, ok);
-  k_put<I>(Kt, tr, 1, 2 * wq, cw.y, sA1, zA1, ok);
-  k_put<I>(Kt, tr, 0, 2 * wq + 1, cw.z, sA0, zA0, ok);
-  k_put<I>(Kt, tr, 1, 2 * wq + 1, cw.w, sA1, zA1, ok);
-}
-
-// Dequantise one INT2 head block into K (two 64-channel regions) and V^T
-// tiles, by the 128 producer threads (t = 0..127).  nv = valid tokens.
-__device__ __forceinline__ void dequant_page(uint8_t* Kt, uint8_t* Vt, const uint8_t* raw, uint2* pairs, int g,
-                                             int nv, int t) {
-  const int NG = D / g;
-  // (s, z) pairs of consecutive V tokens per channel group
+// (s, z) of consecutive V token slots (2j, 2j + 1) per channel group, the
+// operands of the V dequantisation, from one INT2 head block: threads
+// t < 32 NG write entry [group t / 32][pair t % 32].
+__device__ __forceinline__ void build_pairs(const uint8_t* raw, uint2* pairs, int NG, int t) {
   if (t < 32 * NG) {
-    const uint32_t* vsz = (const uint32_t*)(raw + off_v_sz(g));
+    const uint32_t* vsz = (const uint32_t*)(raw + 4096 + 256 * NG);  // V (s, z) after the K (s, z)
     const int gp = t >> 5, j = t & 31;
     const uint32_t a = vsz[(2 * j) * NG + gp], b = vsz[(2 * j + 1) * NG + gp];
     pairs[gp * 32 + j] = make_uint2(prmt(a, b, 0x5410u), prmt(a, b, 0x7632u));
   }
-  asm volatile("bar.sync 1, 128;\n" ::: "memory");
-  {  // K: token tr, words 4wq .. 4wq + 3
-    const int tr = t >> 1, wq = t & 1;
-    const uint4 cw = *(const uint4*)(raw + tr * 32 + 16 * wq);
-    const uint32_t* ksz = (const uint32_t*)(raw + off_k_sz()) + tr * NG;
-    const uint32_t a0 = ksz[0], b0 = ksz[32 / g], a1 = ksz[64 / g], b1 = ksz[96 / g];
-    const uint32_t s0a = prmt(a0, a0, 0x1010u), z0a = prmt(a0, a0, 0x3232u);
-    const uint32_t s0b = prmt(b0, b0, 0x1010u), z0b = prmt(b0, b0, 0x3232u);
-    const uint32_t s1a = prmt(a1, a1, 0x1010u), z1a = prmt(a1, a1, 0x3232u);
-    const uint32_t s1b = prmt(b1, b1, 0x1010u), z1b = prmt(b1, b1, 0x3232u);
-    const bool ok = tr < nv;
-    k_put4<0>(Kt, tr, wq, cw, s0a, z0a, s0b, z0b, s1a, z1a, s1b, z1b, ok);
-    k_put4<1>(Kt, tr, wq, cw, s0a, z0a, s0b, z0b, s1a, z1a, s1b, z1b, ok);
-    k_put4<2>(Kt, tr, wq, cw, s0a, z0a, s0b, z0b, s1a, z1a, s1b, z1b, ok);
-    k_put4<3>(Kt, tr, wq, cw, s0a, z0a, s0b, z0b, s1a, z1a, s1b, z1b, ok);
-    k_put4<4>(Kt, tr, wq, cw, s0a, z0a, s0b, z0b, s1a, z1a, s1b, z1b, ok);
-    k_put4<5>(Kt, tr, wq, cw, s0a, z0a, s0b, z0b, s1a, z1a, s1b, z1b, ok);
-    k_put4<6>(Kt, tr, wq, cw, s0a, z0a, s0b, z0b, s1a, z1a, s1b, z1b, ok);
-    k_put4<7>(Kt, tr, wq, cw, s0a, z0a, s0b, z0b, s1a, z1a, s1b, z1b, ok);
+}
+
+// Dequantise one INT2 head block into K (two 64-channel regions) and V^T
+// tiles with 16-byte stores, by the 256 producer threads (t = 0..255): value
+// = s·code + z with the group's fp16 scale and zero, rounded once to fp16.
+// g = 2^lg channels per group, NG = 128 / g groups; pairs = the block's
+// build_pairs table; nv = valid tokens; FULL: all 64 are.
+template <bool FULL>
+__device__ __forceinline__ void dequant_page(uint8_t* Kt, uint8_t* Vt, const uint8_t* raw, const uint2* pairs,
+                                             int lg, int NG, int nv, int t) {
+  {  // K: token tr, channel half A, chunks 4Ih .. 4Ih + 3
+    const int tr = t & 63, A = (t >> 7) & 1, Ih = (t >> 6) & 1;
+    const uint4 lo = *(const uint4*)(raw + tr * 32), hi = *(const uint4*)(raw + tr * 32 + 16);
+    const uint32_t w0 = A ? lo.y : lo.x, w1 = A ? lo.w : lo.z, w2 = A ? hi.y : hi.x, w3 = A ? hi.w : hi.z;
+    const uint32_t sz = ((const uint32_t*)(raw + off_k_sz()))[tr * NG + ((64 * A + 32 * Ih) >> lg)];
+    const uint32_t s2 = prmt(sz, sz, 0x1010u), z2 = prmt(sz, sz, 0x3232u);
+    const bool ok = FULL || tr < nv;
+    if (Ih == 0) {
+      k_chunk<0>(Kt, tr, A, w0, w1, w2, w3, s2, z2, ok);
+      k_chunk<1>(Kt, tr, A, w0, w1, w2, w3, s2, z2, ok);
+      k_chunk<2>(Kt, tr, A, w0, w1, w2, w3, s2, z2, ok);
+      k_chunk<3>(Kt, tr, A, w0, w1, w2, w3, s2, z2, ok);
+    } else {
+      k_chunk<4>(Kt, tr, A, w0, w1, w2, w3, s2, z2, ok);
+      k_chunk<5>(Kt, tr, A, w0, w1, w2, w3, s2, z2, ok);
+      k_chunk<6>(Kt, tr, A, w0, w1, w2, w3, s2, z2, ok);
+      k_chunk<7>(Kt, tr, A, w0, w1, w2, w3, s2, z2, ok);
+    }
   }
-  {  // V: word T4 of channels chb + 32k
-    const int T4 = t & 3, chb = t >> 2;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int ch = chb + 32 * k;
-      const uint32_t w = *(const uint32_t*)(raw + 2048 + ch * 16 + 4 * T4);
-      const uint2* pr = pairs + (ch / g) * 32;
-      v_put<0>(Vt, ch, T4, w, pr, nv);
-      v_put<1>(Vt, ch, T4, w, pr, nv);
-      v_put<2>(Vt, ch, T4, w, pr, nv);
-      v_put<3>(Vt, ch, T4, w, pr, nv);
-      v_put<4>(Vt, ch, T4, w, pr, nv);
-      v_put<5>(Vt, ch, T4, w, pr, nv);
-      v_put<6>(Vt, ch, T4, w, pr, nv);
-      v_put<7>(Vt, ch, T4, w, pr, nv);
+  {  // V: channel ch, chunks 4Ih .. 4Ih + 3
+    const int ch = t & 127, Ih = t >> 7;
+    const uint4 w = *(const uint4*)(raw + 2048 + ch * 16);
+    const uint2* pr = pairs + ((ch >> lg) << 5);
+    if (Ih == 0) {
+      v_chunk<0, FULL>(Vt, ch, w, pr, nv);
+      v_chunk<1, FULL>(Vt, ch, w, pr, nv);
+      v_chunk<2, FULL>(Vt, ch, w, pr, nv);
+      v_chunk<3, FULL>(Vt, ch, w, pr, nv);
+    } else {
+      v_chunk<4, FULL>(Vt, ch, w, pr, nv);
+      v_chunk<5, FULL>(Vt, ch, w, pr, nv);
+      v_chunk<6, FULL>(Vt, ch, w, pr, nv);
+      v_chunk<7, FULL>(Vt, ch, w, pr, nv);
     }
   }
 }
@@ -792,16 +796,16 @@ __device__ __forceinline__ void dequant_page(uint8_t* Kt, uint8_t* Vt, const uin
 __device__ __forceinline__ void convert_bf16(uint8_t* Kt, uint8_t* Vt, const __nv_bfloat16* Kb,
                                              const __nv_bfloat16* Vb, size_t stride, uint64_t valid, int t) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int u = t + 128 * j, tok = u >> 4, c16 = u & 15;
+  for (int j = 0; j < 4; ++j) {
+    const int u = t + NPROD * j, tok = u >> 4, c16 = u & 15;
     uint4 x = make_uint4(0u, 0u, 0u, 0u);
     if ((valid >> tok) & 1ull) x = *(const uint4*)(Kb + tok * stride + 8 * c16);
     const uint4 y = make_uint4(bf2_to_h2(x.x), bf2_to_h2(x.y), bf2_to_h2(x.z), bf2_to_h2(x.w));
     *(uint4*)(Kt + (c16 >> 3) * (PAGE * 128) + tok * 128 + (((c16 & 7) ^ (tok & 7)) << 4)) = y;
   }
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int u = t + 128 * j, jp = u & 31, k8 = u >> 5;
+  for (int j = 0; j < 2; ++j) {
+    const int u = t + NPROD * j, jp = u & 31, k8 = u >> 5;
     uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
     if ((valid >> (2 * jp)) & 1ull) x0 = *(const uint4*)(Vb + (2 * jp) * stride + 8 * k8);
     if ((valid >> (2 * jp + 1)) & 1ull) x1 = *(const uint4*)(Vb + (2 * jp + 1) * stride + 8 * k8);
@@ -849,19 +853,18 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(PrefillArgs 
   if (tid == 0) {
     for (int i = 0; i < NRAW; ++i) {
       mbar_init(&bars[B_RAW_FULL + i], 1);
-      mbar_init(&bars[B_RAW_EMPTY + i], 128);
+      mbar_init(&bars[B_RAW_EMPTY + i], NPROD / 32);
     }
     for (int i = 0; i < NKV; ++i) {
-      mbar_init(&bars[B_KV_FULL + i], 128);
+      mbar_init(&bars[B_KV_FULL + i], NPROD);
       mbar_init(&bars[B_KV_EMPTY + i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[B_S_FULL + i], 1);
       mbar_init(&bars[B_P_FULL + i], 4);
+      mbar_init(&bars[B_O_FINAL + i], 1);
     }
-    mbar_init(&bars[B_O_DONE], 1);
-    mbar_init(&bars[B_O_FINAL], 1);
-    mbar_init(&bars[B_Q_FULL], 128);
+    mbar_init(&bars[B_Q_FULL], 4);
     mbar_init(&bars[B_DRAIN], 1);
     misc[1] = 0;
     for (int i = 0; i < NRAW; ++i) misc[2 + i] = 0;
@@ -906,103 +909,123 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(PrefillArgs 
   const int gbytes = cv.head_bytes;
   const int32_t* ptab = cv.page_table + (size_t)b * cv.max_pages_per_req;
 
-  if (warp == TMA_WARP) {
-    // ------------------------------------------------ page copies
-    int issued = 0;
-    if (!win && lane == 0) {
-      for (int i = 0; i < n; ++i) {
-        const int slot = i % NRAW;
-        if (i >= NRAW && !wait_bar(&bars[B_RAW_EMPTY + slot], ((i / NRAW) - 1) & 1, abort_flag)) break;
-        const int pid = ptab[p0 + i];
-        const bool ok = pid >= 0 && pid < cv.num_pages;
-        misc[2 + slot] = ok ? 0 : 1;
-        if (!ok) {
-          record_error(cv.err, pid < 0 ? OSCAR_ERR_NO_PAGE : OSCAR_ERR_RANGE);
-          mbar_expect_tx(&bars[B_RAW_FULL + slot], 0);
-        } else {
-          mbar_expect_tx(&bars[B_RAW_FULL + slot], (uint32_t)gbytes);
-          bulk_g2s(smem + tc::OFF_RAW + slot * RAW_SLOT, cv.pool + (size_t)pid * cv.page_bytes + (size_t)kvh * gbytes,
-                   (uint32_t)gbytes, &bars[B_RAW_FULL + slot]);
-        }
-        issued = i + 1;
-      }
-      // every copy this CTA started has landed before it exits
-      for (int i = issued - NRAW < 0 ? 0 : issued - NRAW; i < issued; ++i)
-        mbar_wait(&bars[B_RAW_FULL + i % NRAW], (i / NRAW) & 1);
-    }
-  } else if (warp == MMA_WARP) {
+  if (warp == MMA_WARP) {
     // ------------------------------------------------ tcgen05.mma issue
     if (lane == 0) {
       bool ok = wait_bar(&bars[B_Q_FULL], 0, abort_flag);
-      const uint32_t qa = sbase + OFF_Q;
       for (int i = 0; ok && i <= n; ++i) {
-        if (i < n) {  // S(i) = Q·K(i)^T
+        if (i < n) {  // S(i) = Q·K(i)^T into S buffer i % 2
           const int kb = i % NKV;
           if (!wait_bar(&bars[B_KV_FULL + kb], (i / NKV) & 1, abort_flag)) break;
           fence_after();
           const uint32_t kaddr = sbase + OFF_KV + kb * KV_BYTES;
-          const uint32_t d = tmem + S_COL0 + 128 * (i & 1);
+          const uint32_t d = tmem + S_COL0 + 64 * (i & 1);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            mma_ss(d, sdesc(qa + (ks >> 2) * (PF_ROWS * 128) + (ks & 3) * 32),
-                   sdesc(kaddr + (ks >> 2) * (PAGE * 128) + (ks & 3) * 32), IDESC_S, ks > 0);
+            mma_ts(d, tmem + Q_COL + 8 * ks, sdesc(kaddr + (ks >> 2) * (PAGE * 128) + (ks & 3) * 32), IDESC_S,
+                   ks > 0);
           commit(&bars[B_S_FULL + (i & 1)]);
         }
-        if (i >= 1) {  // O += P(i-1)·V(i-1)
-          const int j = i - 1, kb = j % NKV;
-          if (!wait_bar(&bars[B_P_FULL + (j & 1)], (j >> 1) & 1, abort_flag)) break;
+        if (i >= 1) {  // O_w += P(j)·V(j), w = j % 2
+          const int j = i - 1, kb = j % NKV, w = j & 1;
+          if (!wait_bar(&bars[B_P_FULL + w], (j >> 1) & 1, abort_flag)) break;
           fence_after();
           const uint32_t vaddr = sbase + OFF_KV + kb * KV_BYTES + K_BYTES;
-          const uint32_t pa = tmem + S_COL0 + 128 * (j & 1);
+          const uint32_t pa = tmem + S_COL0 + 64 * w;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + O_COL, pa + 8 * kk, sdesc(vaddr + kk * 32), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + O_COL0 + 160 * w, pa + 8 * kk, sdesc(vaddr + kk * 32), IDESC_PV,
+                   (j >= 2 || kk > 0) ? 1u : 0u);
           commit(&bars[B_KV_EMPTY + kb]);
-          commit(&bars[B_O_DONE]);
-          if (j == n - 1) commit(&bars[B_O_FINAL]);
+          if (j >= n - 2) commit(&bars[B_O_FINAL + w]);
         }
       }
       // all issued MMAs complete before the tensor memory is released
       commit(&bars[B_DRAIN]);
       mbar_wait(&bars[B_DRAIN], 0);
     }
-  } else if (warp >= 4) {
+  } else if (warp == TMA_WARP) {
+    // ------------------------------------------------ page copies (lane 0), page ids 32 at a time
+    if (!win) {
+      int issued = 0;
+      int nxt = lane < n ? ptab[p0 + lane] : 0;
+      for (int base = 0; base < n; base += 32) {
+        const int mine = nxt;
+        nxt = base + 32 + lane < n ? ptab[p0 + base + 32 + lane] : 0;
+        const int cnt = n - base < 32 ? n - base : 32;
+        int go = 1;
+        for (int j = 0; j < cnt && go; ++j) {
+          const int pid = __shfl_sync(0xffffffffu, mine, j);
+          if (lane == 0) {
+            const int i = base + j, slot = i % NRAW;
+            if (i >= NRAW && !wait_bar(&bars[B_RAW_EMPTY + slot], ((i / NRAW) - 1) & 1, abort_flag)) {
+              go = 0;
+            } else {
+              const bool ok = pid >= 0 && pid < cv.num_pages;
+              misc[2 + slot] = ok ? 0 : 1;
+              if (!ok) {
+                record_error(cv.err, pid < 0 ? OSCAR_ERR_NO_PAGE : OSCAR_ERR_RANGE);
+                mbar_expect_tx(&bars[B_RAW_FULL + slot], 0);
+              } else {
+                mbar_expect_tx(&bars[B_RAW_FULL + slot], (uint32_t)gbytes);
+                bulk_g2s(smem + tc::OFF_RAW + slot * RAW_SLOT,
+                         cv.pool + (size_t)pid * cv.page_bytes + (size_t)kvh * gbytes, (uint32_t)gbytes,
+                         &bars[B_RAW_FULL + slot]);
+              }
+              issued = i + 1;
+            }
+          }
+          go = __shfl_sync(0xffffffffu, go, 0);
+        }
+        if (!go) break;
+      }
+      // every copy this CTA started has landed before it exits
+      if (lane == 0)
+        for (int i = issued - NRAW < 0 ? 0 : issued - NRAW; i < issued; ++i)
+          mbar_wait(&bars[B_RAW_FULL + i % NRAW], (i / NRAW) & 1);
+    }
+  } else if (tid >= DQ0) {
     // ------------------------------------------------ tile producers
     const int t = tid - DQ0;
-    {  // query rows -> Q tile (rotated for history, raw for the window)
-      const __half* qrow =
-          a.qh + ((size_t)(win ? 1 : 0) * a.B * Hkv + bk) * RP * D + (size_t)(rt * PF_ROWS + t) * D;
-#pragma unroll
-      for (int c16 = 0; c16 < 16; ++c16) {
-        const uint4 x = *(const uint4*)(qrow + 8 * c16);
-        *(uint4*)(smem + OFF_Q + (c16 >> 3) * (PF_ROWS * 128) + t * 128 + (((c16 & 7) ^ (t & 7)) << 4)) = x;
-      }
-      // ones row (row sums) and zero rows below the 128 channels of every V^T buffer
+    const int lg = 31 - __clz(cv.g), NG = D >> lg;
+    // ones row (row sums) and zero rows below the 128 channels of every V^T
+    // buffer (made visible to the tensor cores with the buffer's first tile)
+    if (t < 128)
       for (int kb = 0; kb < NKV; ++kb) {
         const uint32_t v = (t < 8) ? 0x3C003C00u : 0u;
         *(uint4*)(smem + OFF_KV + kb * KV_BYTES + K_BYTES + 128 * 128 + 16 * t) = make_uint4(v, v, v, v);
       }
-      fence_proxy_async();
-      arrive(&bars[B_Q_FULL]);
-    }
     uint2* pairs0 = (uint2*)(smem + OFF_PAIRS);
-    for (int i = 0; i < n; ++i) {
+    int nn = n;
+    // the (s, z) pair table of page i is built one page ahead (page 0 here)
+    if (!win && n > 0) {
+      if (producers_all(wait_bar(&bars[B_RAW_FULL], 0, abort_flag)))
+        build_pairs(smem + tc::OFF_RAW, pairs0, NG, t);
+      else
+        nn = 0;
+    }
+    for (int i = 0; i < nn; ++i) {
       const int kb = i % NKV;
       uint8_t* Kt = smem + OFF_KV + kb * KV_BYTES;
       uint8_t* Vt = Kt + K_BYTES;
       bool okw = i < NKV || wait_bar(&bars[B_KV_EMPTY + kb], ((i / NKV) - 1) & 1, abort_flag);
-      if (!win) okw = okw && wait_bar(&bars[B_RAW_FULL + i % NRAW], (i / NRAW) & 1, abort_flag);
+      if (!win && i + 1 < n) okw = okw && wait_bar(&bars[B_RAW_FULL + (i + 1) % NRAW], ((i + 1) / NRAW) & 1, abort_flag);
+      // also: every producer is done with page i - 1 and with the pair table of page i
       if (!producers_all(okw)) break;
       uint64_t mask;
       int causal = 0;
       if (!win) {
         const int slot = i % NRAW;
+        if (i + 1 < n) build_pairs(smem + tc::OFF_RAW + ((i + 1) % NRAW) * RAW_SLOT, pairs0 + ((i + 1) & 1) * 128, NG, t);
         const int pg = p0 + i;
         int nv = pg == pages - 1 ? hist - pg * PAGE : PAGE;
         if (misc[2 + slot]) nv = 0;
-        dequant_page(Kt, Vt, smem + tc::OFF_RAW + slot * RAW_SLOT, pairs0 + (i & 1) * 128, cv.g, nv, t);
+        const uint8_t* raw = smem + tc::OFF_RAW + slot * RAW_SLOT;
+        if (nv == PAGE)
+          dequant_page<true>(Kt, Vt, raw, pairs0 + (i & 1) * 128, lg, NG, nv, t);
+        else
+          dequant_page<false>(Kt, Vt, raw, pairs0 + (i & 1) * 128, lg, NG, nv, t);
         mask = low_mask(nv);
-        arrive(&bars[B_RAW_EMPTY + slot]);
       } else {
         const int kind = kinds[i];
         const __nv_bfloat16 *Kb, *Vb;
@@ -1033,62 +1056,101 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(PrefillArgs 
       }
       fence_proxy_async();
       arrive(&bars[B_KV_FULL + kb]);
+      if (!win) {  // raw slot of page i free again
+        __syncwarp();
+        if (lane == 0) arrive(&bars[B_RAW_EMPTY + i % NRAW]);
+      }
     }
   } else {
-    // ------------------------------------------------ softmax, one row per thread
-    const int row = tid;  // = TMEM lane
+    // ------------------------------------------------ softmax: warpgroup wg takes pages wg, wg + 2, ...
+    const int wg = warp >> 2;
+    const int row = tid & 127;  // = TMEM lane
     const int grow = rt * PF_ROWS + row;
     const float al = a.alpha[(size_t)bk * RP + grow];
     const int trow = grow / G;
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t oa = tmem + lane_base + O_COL0 + 160 * wg;
+    const uint32_t sa = tmem + lane_base + S_COL0 + 64 * wg;
+    if (wg == 0) {  // this row of Q (rotated for history, raw for the window) -> TMEM
+      const uint4* qrow = (const uint4*)(a.qh + ((size_t)(win ? 1 : 0) * a.B * Hkv + bk) * RP * D + (size_t)grow * D);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t v[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 x = qrow[8 * h + c];
+          v[4 * c] = x.x;
+          v[4 * c + 1] = x.y;
+          v[4 * c + 2] = x.z;
+          v[4 * c + 3] = x.w;
+        }
+        tmem_st32(tmem + lane_base + Q_COL + 32 * h, v);
+      }
+      tmem_st_wait();
+      fence_before();
+      __syncwarp();
+      if (lane == 0) arrive(&bars[B_Q_FULL]);
+    }
     float m_run = -1e30f;
     bool ok = true;
-    for (int i = 0; i < n; ++i) {
-      const int kb = i % NKV, sb = i & 1;
+    for (int k = 0;; ++k) {
+      const int i = 2 * k + wg;
+      if (i >= n) break;
+      const int kb = i % NKV;
       if (!__all_sync(0xffffffffu, wait_bar(&bars[B_KV_FULL + kb], (i / NKV) & 1, abort_flag))) {
         ok = false;
         break;
       }
       const uint64_t mask = *(const uint64_t*)(info + kb * 16);
       const bool causal = *(const int*)(info + kb * 16 + 8) != 0;
-      if (!__all_sync(0xffffffffu, wait_bar(&bars[B_S_FULL + sb], (i >> 1) & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, wait_bar(&bars[B_S_FULL + wg], k & 1, abort_flag))) {
         ok = false;
         break;
       }
       fence_after();
-      const uint32_t sa = tmem + lane_base + S_COL0 + 128 * sb;
       uint32_t r0[32], r1[32];
       tmem_ld32(sa, r0);
       tmem_ld32(sa + 32, r1);
       tmem_ld_wait_regs(r0);
       regs_after(r1);
+      // raw logits (the row factor al > 0 is applied with the exponent)
       float x[64];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        x[j] = __uint_as_float(r0[j]) * al;
-        x[32 + j] = __uint_as_float(r1[j]) * al;
+        x[j] = __uint_as_float(r0[j]);
+        x[32 + j] = __uint_as_float(r1[j]);
       }
       if (mask != ~0ull || causal) {
 #pragma unroll
         for (int j = 0; j < 64; ++j)
           if (!((mask >> j) & 1ull) || (causal && j > trow)) x[j] = -INFINITY;
       }
-      float mx = x[0];
+      float m8[8];
 #pragma unroll
-      for (int j = 1; j < 64; ++j) mx = fmaxf(mx, x[j]);
-      if (i == 0) {
+      for (int j = 0; j < 8; ++j) m8[j] = fmaxf(x[j], x[8 + j]);
+#pragma unroll
+      for (int j = 16; j < 64; ++j) m8[j & 7] = fmaxf(m8[j & 7], x[j]);
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * al;  // -inf stays -inf
+      bool resc = false;
+      float f = 1.f;
+      if (k == 0) {
         m_run = fmaxf(m_run, mx);
       } else if (__any_sync(0xffffffffu, mx > m_run + LAZY)) {
-        // O must hold P(i-1)·V(i-1) before it is rescaled
-        if (!__all_sync(0xffffffffu, wait_bar(&bars[B_O_DONE], (i - 1) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
-        fence_after();
         const float m_new = fmaxf(m_run, mx);
-        const float f = ex2(m_run - m_new);
+        f = ex2(m_run - m_new);
         m_run = m_new;
-        const uint32_t oa = tmem + lane_base + O_COL;
+        resc = true;
+      }
+      {
+        uint32_t p[32];
+        const float nm = -m_run;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) p[j] = ex2_h2(f2_to_h2(fmaf(x[2 * j], al, nm), fmaf(x[2 * j + 1], al, nm)));
+        tmem_st32(sa, p);
+      }
+      if (resc) {
+        // S(i) is complete, so is every MMA issued before it: O_wg holds P(i-2)·V(i-2)
 #pragma unroll 1
         for (int c = 0; c < 160; c += 32) {  // columns 0..159 (the 144 in use and 16 unused)
           uint32_t v[32];
@@ -1100,21 +1162,17 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(PrefillArgs 
           tmem_st_wait();
         }
       }
-      uint32_t p[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) p[j] = ex2_h2(f2_to_h2(x[2 * j] - m_run, x[2 * j + 1] - m_run));
-      tmem_st32(sa, p);
       tmem_st_wait();
       fence_before();
       __syncwarp();
-      if (lane == 0) arrive(&bars[B_P_FULL + sb]);
+      if (lane == 0) arrive(&bars[B_P_FULL + wg]);
     }
-    // the partial record: m (log2 units), l, o (unnormalised)
-    if (ok && n > 0) ok = __all_sync(0xffffffffu, wait_bar(&bars[B_O_FINAL], 0, abort_flag));
-    float* rec = a.part + (((size_t)tile * (a.NS + 1) + split) * PF_ROWS + row) * PART_STRIDE;
-    if (ok && n > 0) {
+    // this warpgroup's partial record: m (log2 units), l, o (unnormalised)
+    const bool has = n > wg;
+    if (ok && has) ok = __all_sync(0xffffffffu, wait_bar(&bars[B_O_FINAL + wg], 0, abort_flag));
+    float* rec = a.part + ((((size_t)tile * (a.NS + 1) + split) * 2 + wg) * PF_ROWS + row) * PART_STRIDE;
+    if (ok && has) {
       fence_after();
-      const uint32_t oa = tmem + lane_base + O_COL;
 #pragma unroll 1
       for (int c = 0; c < 160; c += 32) {
         uint32_t v[32];
@@ -1132,7 +1190,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(PrefillArgs 
           }
         }
       }
-    } else if (grow < R) {  // nothing here (or aborted): an empty partial
+    } else if (grow < R) {  // no pages for this warpgroup (or aborted): an empty partial
       rec[0] = -1e30f;
       rec[1] = 0.f;
       for (int j = 0; j < D; j += 4) *(float4*)(rec + PART_O + j) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1161,7 +1219,7 @@ PrefillScratch prefill_scratch_layout(int B, int Hkv, int G, int T, int NS) {
   };
   L.off_qh = take((size_t)2 * B * Hkv * RP * D * sizeof(__half));
   L.off_alpha = take((size_t)B * Hkv * RP * sizeof(float));
-  L.off_part = take((size_t)B * Hkv * RT * (NS + 1) * PF_ROWS * PART_STRIDE * sizeof(float));
+  L.off_part = take((size_t)B * Hkv * RT * (NS + 1) * 2 * PF_ROWS * PART_STRIDE * sizeof(float));
   L.total = off;
   return L;
 }
@@ -1196,19 +1254,21 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st, Profiler* prof
   cudaError_t e = ensure_prefill_smem();
   if (e != cudaSuccess) return e;
   const int tiles = a.B * a.cv.Hkv * a.RT;
+  PrefillArgs b = a;
+  b.rpc = a.impl == OSCAR_PREFILL_MMA_SYNC ? 1 : 2;
   prof_begin(prof, OSCAR_KERNEL_PREFILL_PREP, st);
-  e = launch_pdl(prefill_prep_kernel, dim3(a.B * a.cv.Hkv, a.RT * (PF_ROWS / 8)), dim3(128), 0, st, a);
+  e = launch_pdl(prefill_prep_kernel, dim3(a.B * a.cv.Hkv, a.RT * (PF_ROWS / 8)), dim3(128), 0, st, b);
   prof_end(prof, OSCAR_KERNEL_PREFILL_PREP, st);
   if (e != cudaSuccess) return e;
   prof_begin(prof, OSCAR_KERNEL_PREFILL_ATTN, st);
   if (a.impl == OSCAR_PREFILL_MMA_SYNC)
-    e = launch_pdl(prefill_attn_kernel, dim3(tiles, a.NS + 1), dim3(PF_THREADS), PF_SMEM, st, a);
+    e = launch_pdl(prefill_attn_kernel, dim3(tiles, a.NS + 1), dim3(PF_THREADS), PF_SMEM, st, b);
   else
-    e = launch_pdl(prefill_tc_kernel, dim3(tiles, a.NS + 1), dim3(tc::THREADS), tc::SMEM, st, a);
+    e = launch_pdl(prefill_tc_kernel, dim3(tiles, a.NS + 1), dim3(tc::THREADS), tc::SMEM, st, b);
   prof_end(prof, OSCAR_KERNEL_PREFILL_ATTN, st);
   if (e != cudaSuccess) return e;
   prof_begin(prof, OSCAR_KERNEL_PREFILL_MERGE, st);
-  e = launch_pdl(prefill_merge_kernel, dim3(tiles, PF_ROWS / MERGE_ROWS), dim3(128), 0, st, a);
+  e = launch_pdl(prefill_merge_kernel, dim3(tiles, PF_ROWS / MERGE_ROWS), dim3(128), 0, st, b);
   prof_end(prof, OSCAR_KERNEL_PREFILL_MERGE, st);
   return e;
 }
