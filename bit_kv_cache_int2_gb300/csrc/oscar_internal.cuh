@@ -583,10 +583,9 @@ struct PrefillArgs {
   float* lse;              // [B][T][Hq] or null
   __half* qh;              // scratch [2][B*Hkv][RT*128][128]: q·R_K, q (both * 2^-sigma)
   float* alpha;            // scratch [B*Hkv][RT*128]: 2^sigma * log2(e) / sqrt(d)
-  float* part;             // scratch [B*Hkv*RT][(NS+1)*rpc][128][PART_STRIDE]
+  float* part;             // scratch [B*Hkv*RT][NS+1][128][PART_STRIDE]
   int B, T, RT, NS;
   int impl;  // an oscar_prefill_impl value
-  int rpc;   // partial records per attention CTA (the tcgen05 kernel writes one per softmax warpgroup)
   LayerRot rot;
 };
 

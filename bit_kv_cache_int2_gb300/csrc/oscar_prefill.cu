@@ -36,7 +36,6 @@ constexpr int OFF_RAW = 4 * TILE_BYTES;
 constexpr int OFF_BAR = OFF_RAW + PF_DEPTH * RAW_SLOT;
 constexpr int OFF_INFO = OFF_BAR + PF_DEPTH * 8;  // u64 mask[2], int causal[2], int bad[PF_DEPTH]
 constexpr int PF_SMEM = OFF_INFO + 64;
-constexpr int MERGE_ROWS = 8;
 static_assert(RAW_SLOT >= int2_head_bytes(32), "raw slot holds a g32 head block");
 
 __device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
@@ -260,21 +259,35 @@ __device__ __forceinline__ uint64_t low_mask(int n) {
 }
 
 // --------------------------------------------------------------- kernels
-__global__ void __launch_bounds__(128) prefill_prep_kernel(PrefillArgs a) {
-  __shared__ float xs[8][D];
-  __shared__ float nrm[8];
+constexpr int PREP_ROWS = 16;  // query rows per prep CTA
+constexpr int PREP_SMEM = (D * D + PREP_ROWS * D + PREP_ROWS) * 4;
+
+// 16 query rows of one kv head by 256 threads: thread (c, h) forms channel c
+// of rows 8h .. 8h + 7 from the R_K staged in shared memory.
+__global__ void __launch_bounds__(256) prefill_prep_kernel(PrefillArgs a) {
+  extern __shared__ __align__(16) float psm[];
+  float* Rs = psm;              // [128][128] R_K
+  float* xs = Rs + D * D;       // [16][128] q rows
+  float* nrm = xs + PREP_ROWS * D;
   const CacheView& cv = a.cv;
   const int bk = blockIdx.x, b = bk / cv.Hkv, kvh = bk % cv.Hkv, G = cv.G;
-  const int R = a.T * G, RP = a.RT * PF_ROWS, r0 = 8 * blockIdx.y;
-  const int c = threadIdx.x, w = c >> 5, lane = c & 31;
-  const float* Rk = a.rot.R_K + (size_t)kvh * D * D + c;
+  const int R = a.T * G, RP = a.RT * PF_ROWS, r0 = PREP_ROWS * blockIdx.y;
+  const int tid = threadIdx.x, c = tid & 127, h = tid >> 7, w = tid >> 5, lane = tid & 31;
+  {  // the rotation table is written synchronously by oscar_set_rotation: load it before the wait
+    const float4* Rg = (const float4*)(a.rot.R_K + (size_t)kvh * D * D);
+    float4 rv[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) rv[j] = __ldg(Rg + tid + 256 * j);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) ((float4*)Rs)[tid + 256 * j] = rv[j];
+  }
   pdl_wait();
   pdl_launch_dependents();
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const int r = r0 + j;
-    xs[j][c] = r < R ? __bfloat162float(a.q[(((size_t)b * a.T + r / G) * cv.Hq + kvh * G + r % G) * D + c])
-                     : 0.f;
+    const int r = r0 + 8 * h + j;
+    xs[(8 * h + j) * D + c] =
+        r < R ? __bfloat162float(a.q[(((size_t)b * a.T + r / G) * cv.Hq + kvh * G + r % G) * D + c]) : 0.f;
   }
   __syncthreads();
 #pragma unroll
@@ -282,7 +295,7 @@ __global__ void __launch_bounds__(128) prefill_prep_kernel(PrefillArgs a) {
     const int j = 2 * w + jj;
     float sq = 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) sq = fmaf(xs[j][lane + 32 * k], xs[j][lane + 32 * k], sq);
+    for (int k = 0; k < 4; ++k) sq = fmaf(xs[j * D + lane + 32 * k], xs[j * D + lane + 32 * k], sq);
 #pragma unroll
     for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
     if (lane == 0) nrm[j] = sqrtf(sq);
@@ -291,24 +304,26 @@ __global__ void __launch_bounds__(128) prefill_prep_kernel(PrefillArgs a) {
   float acc[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-#pragma unroll 4
+  const float* xh = xs + 8 * h * D;
+#pragma unroll 8
   for (int k = 0; k < D; ++k) {
-    const float rk = __ldg(Rk + (size_t)k * D);
+    const float rk = Rs[k * D + c];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = fmaf(xs[j][k], rk, acc[j]);
+    for (int j = 0; j < 8; ++j) acc[j] = fmaf(xh[j * D + k], rk, acc[j]);
   }
   const size_t vstride = (size_t)a.B * cv.Hkv * RP * D;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const int r = r0 + j;
+    const int r = r0 + 8 * h + j;
+    const float nj = nrm[8 * h + j];
     // |q'_c| and |q_c| are both at most |q| (R_K is orthogonal): 2^-sigma
     // brings them below 2^14 in fp16
     int ex = 0;
-    frexpf(nrm[j], &ex);
-    const int sig = nrm[j] > 0.f ? ex - 14 : 0;
+    frexpf(nj, &ex);
+    const int sig = nj > 0.f ? ex - 14 : 0;
     const size_t e = ((size_t)bk * RP + r) * D + c;
     a.qh[e] = __float2half_rn(ldexpf(acc[j], -sig));
-    a.qh[vstride + e] = __float2half_rn(ldexpf(xs[j][c], -sig));
+    a.qh[vstride + e] = __float2half_rn(ldexpf(xh[j * D + c], -sig));
     if (c == 0) a.alpha[(size_t)bk * RP + r] = ldexpf(1.f, sig) * LOG2E * INV_SQRT_D;
   }
 }
@@ -473,27 +488,42 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_attn_kernel(PrefillArgs
   }
 }
 
-__global__ void __launch_bounds__(128) prefill_merge_kernel(PrefillArgs a) {
-  __shared__ float xs[MERGE_ROWS][D];
-  __shared__ float wsh[MERGE_ROWS][2 * (PF_MAX_SPLITS + 1)];
-  __shared__ float linv[MERGE_ROWS], lsev[MERGE_ROWS];
+constexpr int MROWS = 16;  // rows per merge CTA
+constexpr int MERGE_SMEM = (D * D + MROWS * D) * 4;
+
+// 16 rows of one tile by 256 threads: combine the history splits and the
+// window partial, un-rotate the history part by R_V^T (staged in shared
+// memory) and write out and lse.
+__global__ void __launch_bounds__(256) prefill_merge_kernel(PrefillArgs a) {
+  extern __shared__ __align__(16) float msm[];
+  float* Rs = msm;         // [128][128] R_V^T: row k = column k of R_V
+  float* xs = Rs + D * D;  // [16][128] combined history o'
+  __shared__ float wsh[MROWS][PF_MAX_SPLITS + 1];
+  __shared__ float linv[MROWS], lsev[MROWS];
   const CacheView& cv = a.cv;
   const int tile = blockIdx.x, bk = tile / a.RT, rt = tile % a.RT;
   const int b = bk / cv.Hkv, kvh = bk % cv.Hkv, G = cv.G;
-  // records per tile: rpc per attention CTA; the last rpc are the window's
-  const int R = a.T * G, NH = a.NS * a.rpc, NSP = (a.NS + 1) * a.rpc;
-  const int i0 = MERGE_ROWS * blockIdx.y;
-  const int c = threadIdx.x, warp = c >> 5, lane = c & 31;
+  const int R = a.T * G, NS = a.NS, NSP = NS + 1;
+  const int i0 = MROWS * blockIdx.y;
+  const int tid = threadIdx.x, c = tid & 127, h = tid >> 7, warp = tid >> 5, lane = tid & 31;
+  {  // the rotation table is written synchronously by oscar_set_rotation: load it before the wait
+    const float4* Rg = (const float4*)(a.rot.RVt + (size_t)kvh * D * D);
+    float4 rv[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) rv[j] = __ldg(Rg + tid + 256 * j);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) ((float4*)Rs)[tid + 256 * j] = rv[j];
+  }
   pdl_wait();
   pdl_launch_dependents();
   if (rt * PF_ROWS + i0 >= R) return;
   const float* base = a.part + (size_t)tile * NSP * PF_ROWS * PART_STRIDE;
   const size_t ss = (size_t)PF_ROWS * PART_STRIDE;  // between splits
-  for (int j = warp; j < MERGE_ROWS; j += 4) {
+  for (int j = warp; j < MROWS; j += 8) {  // softmax weights of the partials, warp per row
     const float* rb = base + (size_t)(i0 + j) * PART_STRIDE;
-    float mv[5], lv[5], M = -INFINITY;
+    float mv[3], lv[3], M = -INFINITY;
 #pragma unroll
-    for (int q = 0; q < 5; ++q) {
+    for (int q = 0; q < 3; ++q) {
       const int s = lane + 32 * q;
       mv[q] = s < NSP ? rb[s * ss] : -INFINITY;
       lv[q] = s < NSP ? rb[s * ss + 1] : 0.f;
@@ -503,7 +533,7 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(PrefillArgs a) {
     for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float L = 0.f;
 #pragma unroll
-    for (int q = 0; q < 5; ++q) {
+    for (int q = 0; q < 3; ++q) {
       const int s = lane + 32 * q;
       if (s < NSP) {
         const float w = ex2(mv[q] - M);
@@ -519,35 +549,46 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(PrefillArgs a) {
     }
   }
   __syncthreads();
-  float ow[MERGE_ROWS];
+  // thread (c, h): rows 8h .. 8h + 7; the loads of four splits at a time are in flight together
+  float acc[8], ow[8];
+  const float* cb = base + (size_t)(i0 + 8 * h) * PART_STRIDE + PART_O + c;
 #pragma unroll
-  for (int j = 0; j < MERGE_ROWS; ++j) {
-    const float* rb = base + (size_t)(i0 + j) * PART_STRIDE + PART_O + c;
-    float acc = 0.f, aw = 0.f;
-    for (int s = 0; s < NH; ++s) acc = fmaf(wsh[j][s], rb[s * ss], acc);
-    for (int s = NH; s < NSP; ++s) aw = fmaf(wsh[j][s], rb[s * ss], aw);
-    xs[j][c] = acc;
-    ow[j] = aw;
+  for (int j = 0; j < 8; ++j) {
+    acc[j] = 0.f;
+    ow[j] = wsh[8 * h + j][NS] * cb[(size_t)j * PART_STRIDE + NS * ss];
   }
+  for (int s = 0; s < NS; s += 4) {
+    float v[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[u][j] = s + u < NS ? cb[(size_t)j * PART_STRIDE + (s + u) * ss] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = fmaf(s + u < NS ? wsh[8 * h + j][s + u] : 0.f, v[u][j], acc[j]);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) xs[(8 * h + j) * D + c] = acc[j];
   __syncthreads();
-  // o = o'·R_V^T: y_c = sum_k o'_k R_V[c][k], RVt row k = column k of R_V^T
-  const float* Rt = a.rot.RVt + (size_t)kvh * D * D + c;
-  float y[MERGE_ROWS];
+  // o = o'·R_V^T: y_c = sum_k o'_k R_V[c][k]
+  float y[8];
 #pragma unroll
-  for (int j = 0; j < MERGE_ROWS; ++j) y[j] = 0.f;
-#pragma unroll 4
+  for (int j = 0; j < 8; ++j) y[j] = 0.f;
+  const float* xh = xs + 8 * h * D;
+#pragma unroll 8
   for (int k = 0; k < D; ++k) {
-    const float r = __ldg(Rt + (size_t)k * D);
+    const float r = Rs[k * D + c];
 #pragma unroll
-    for (int j = 0; j < MERGE_ROWS; ++j) y[j] = fmaf(xs[j][k], r, y[j]);
+    for (int j = 0; j < 8; ++j) y[j] = fmaf(xh[j * D + k], r, y[j]);
   }
 #pragma unroll
-  for (int j = 0; j < MERGE_ROWS; ++j) {
-    const int r = rt * PF_ROWS + i0 + j;
+  for (int j = 0; j < 8; ++j) {
+    const int r = rt * PF_ROWS + i0 + 8 * h + j;
     if (r >= R) continue;
     const size_t row = ((size_t)b * a.T + r / G) * cv.Hq + kvh * G + r % G;
-    a.out[row * D + c] = __float2bfloat16_rn((y[j] + ow[j]) * linv[j]);
-    if (c == 0 && a.lse) a.lse[row] = lsev[j];
+    a.out[row * D + c] = __float2bfloat16_rn((y[j] + ow[j]) * linv[8 * h + j]);
+    if (c == 0 && a.lse) a.lse[row] = lsev[8 * h + j];
   }
 }
 
@@ -561,8 +602,9 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(PrefillArgs a) {
 //   warps 0-7  softmax, two warpgroups taking alternate pages, one query
 //              row per thread (row = TMEM lane), each with its own O
 //              accumulator (the two are merged like history splits)
-//   warps 8-15 tile producers: dequantise a copied INT2 page (or convert BF16
-//              window rows) into the K and V^T tiles
+//   warps 8-15 tile producers, two groups of four warps taking alternate
+//              pages: dequantise a copied INT2 page (or convert BF16 window
+//              rows) into the K and V^T tiles
 //   warp 16    TMEM allocation and the tcgen05.mma issue (one thread)
 //   warp 17    bulk copies of the INT2 pages into shared memory
 // V^T carries 16 extra rows: a row of ones, whose O column accumulates the
@@ -572,7 +614,6 @@ __global__ void __launch_bounds__(128) prefill_merge_kernel(PrefillArgs a) {
 namespace tc {
 constexpr int THREADS = 576;
 constexpr int DQ0 = 256;    // first producer thread
-constexpr int NPROD = 256;  // producer threads (warps 8-15)
 constexpr int MMA_WARP = 16, TMA_WARP = 17;
 constexpr int NKV = 4, NRAW = 8;
 constexpr int VT_ROWS = 144;
@@ -581,8 +622,9 @@ constexpr int VT_BYTES = VT_ROWS * 128;     // channels (+16) x 64 tokens
 constexpr int KV_BYTES = K_BYTES + VT_BYTES;
 constexpr int OFF_KV = 0;
 constexpr int OFF_RAW = OFF_KV + NKV * KV_BYTES;
-constexpr int OFF_PAIRS = OFF_RAW + NRAW * RAW_SLOT;  // [2][4 groups][32 token pairs] (s2, z2)
-constexpr int OFF_BAR = OFF_PAIRS + 2 * 4 * 32 * 8;
+// (s2, z2) token-pair tables: [producer group][2][4 channel groups][32 token pairs]
+constexpr int OFF_PAIRS = OFF_RAW + NRAW * RAW_SLOT;
+constexpr int OFF_BAR = OFF_PAIRS + 2 * 2 * 4 * 32 * 8;
 // barriers
 constexpr int B_RAW_FULL = 0, B_RAW_EMPTY = B_RAW_FULL + NRAW, B_KV_FULL = B_RAW_EMPTY + NRAW,
               B_KV_EMPTY = B_KV_FULL + NKV,
@@ -678,15 +720,16 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   return false;
 }
 
-// The producer threads agree on a wait's outcome (named barrier 2): all go
-// on or all stop, so none is left behind at a later barrier.
-__device__ __forceinline__ bool producers_all(bool ok) {
+// The 128 threads of a producer group agree on a wait's outcome (named
+// barrier `id`): all go on or all stop, so none is left behind at a later
+// barrier.
+__device__ __forceinline__ bool group_all(uint32_t id, bool ok) {
   uint32_t r;
   asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 2, 256, p;\n"
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %2, 0;\n bar.red.and.pred q, %1, 128, p;\n"
       " selp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(r)
-      : "r"((uint32_t)ok)
+      : "r"(id), "r"((uint32_t)ok)
       : "memory");
   return r != 0;
 }
@@ -747,47 +790,53 @@ __device__ __forceinline__ void build_pairs(const uint8_t* raw, uint2* pairs, in
 }
 
 // Dequantise one INT2 head block into K (two 64-channel regions) and V^T
-// tiles with 16-byte stores, by the 256 producer threads (t = 0..255): value
-// = s·code + z with the group's fp16 scale and zero, rounded once to fp16.
-// g = 2^lg channels per group, NG = 128 / g groups; pairs = the block's
-// build_pairs table; nv = valid tokens; FULL: all 64 are.
+// tiles with 16-byte stores, by the 128 threads of a producer group
+// (t = 0..127): value = s·code + z with the group's fp16 scale and zero,
+// rounded once to fp16.  g = 2^lg channels per group, NG = 128 / g groups;
+// pairs = the block's build_pairs table; nv = valid tokens; FULL: all 64 are.
 template <bool FULL>
 __device__ __forceinline__ void dequant_page(uint8_t* Kt, uint8_t* Vt, const uint8_t* raw, const uint2* pairs,
                                              int lg, int NG, int nv, int t) {
-  {  // K: token tr, channel half A, chunks 4Ih .. 4Ih + 3
-    const int tr = t & 63, A = (t >> 7) & 1, Ih = (t >> 6) & 1;
+  {  // K: token tr, chunks 4Ih .. 4Ih + 3 of both 64-channel halves
+    const int tr = t & 63, Ih = t >> 6;
     const uint4 lo = *(const uint4*)(raw + tr * 32), hi = *(const uint4*)(raw + tr * 32 + 16);
-    const uint32_t w0 = A ? lo.y : lo.x, w1 = A ? lo.w : lo.z, w2 = A ? hi.y : hi.x, w3 = A ? hi.w : hi.z;
-    const uint32_t sz = ((const uint32_t*)(raw + off_k_sz()))[tr * NG + ((64 * A + 32 * Ih) >> lg)];
-    const uint32_t s2 = prmt(sz, sz, 0x1010u), z2 = prmt(sz, sz, 0x3232u);
+    const uint32_t* ksz = (const uint32_t*)(raw + off_k_sz()) + tr * NG;
+    const uint32_t sz0 = ksz[(32 * Ih) >> lg], sz1 = ksz[(64 + 32 * Ih) >> lg];
+    const uint32_t s0 = prmt(sz0, sz0, 0x1010u), z0 = prmt(sz0, sz0, 0x3232u);
+    const uint32_t s1 = prmt(sz1, sz1, 0x1010u), z1 = prmt(sz1, sz1, 0x3232u);
     const bool ok = FULL || tr < nv;
     if (Ih == 0) {
-      k_chunk<0>(Kt, tr, A, w0, w1, w2, w3, s2, z2, ok);
-      k_chunk<1>(Kt, tr, A, w0, w1, w2, w3, s2, z2, ok);
-      k_chunk<2>(Kt, tr, A, w0, w1, w2, w3, s2, z2, ok);
-      k_chunk<3>(Kt, tr, A, w0, w1, w2, w3, s2, z2, ok);
+      k_chunk<0>(Kt, tr, 0, lo.x, lo.z, hi.x, hi.z, s0, z0, ok);
+      k_chunk<0>(Kt, tr, 1, lo.y, lo.w, hi.y, hi.w, s1, z1, ok);
+      k_chunk<1>(Kt, tr, 0, lo.x, lo.z, hi.x, hi.z, s0, z0, ok);
+      k_chunk<1>(Kt, tr, 1, lo.y, lo.w, hi.y, hi.w, s1, z1, ok);
+      k_chunk<2>(Kt, tr, 0, lo.x, lo.z, hi.x, hi.z, s0, z0, ok);
+      k_chunk<2>(Kt, tr, 1, lo.y, lo.w, hi.y, hi.w, s1, z1, ok);
+      k_chunk<3>(Kt, tr, 0, lo.x, lo.z, hi.x, hi.z, s0, z0, ok);
+      k_chunk<3>(Kt, tr, 1, lo.y, lo.w, hi.y, hi.w, s1, z1, ok);
     } else {
-      k_chunk<4>(Kt, tr, A, w0, w1, w2, w3, s2, z2, ok);
-      k_chunk<5>(Kt, tr, A, w0, w1, w2, w3, s2, z2, ok);
-      k_chunk<6>(Kt, tr, A, w0, w1, w2, w3, s2, z2, ok);
-      k_chunk<7>(Kt, tr, A, w0, w1, w2, w3, s2, z2, ok);
+      k_chunk<4>(Kt, tr, 0, lo.x, lo.z, hi.x, hi.z, s0, z0, ok);
+      k_chunk<4>(Kt, tr, 1, lo.y, lo.w, hi.y, hi.w, s1, z1, ok);
+      k_chunk<5>(Kt, tr, 0, lo.x, lo.z, hi.x, hi.z, s0, z0, ok);
+      k_chunk<5>(Kt, tr, 1, lo.y, lo.w, hi.y, hi.w, s1, z1, ok);
+      k_chunk<6>(Kt, tr, 0, lo.x, lo.z, hi.x, hi.z, s0, z0, ok);
+      k_chunk<6>(Kt, tr, 1, lo.y, lo.w, hi.y, hi.w, s1, z1, ok);
+      k_chunk<7>(Kt, tr, 0, lo.x, lo.z, hi.x, hi.z, s0, z0, ok);
+      k_chunk<7>(Kt, tr, 1, lo.y, lo.w, hi.y, hi.w, s1, z1, ok);
     }
   }
-  {  // V: channel ch, chunks 4Ih .. 4Ih + 3
-    const int ch = t & 127, Ih = t >> 7;
+  {  // V: channel t, all eight chunks
+    const int ch = t;
     const uint4 w = *(const uint4*)(raw + 2048 + ch * 16);
     const uint2* pr = pairs + ((ch >> lg) << 5);
-    if (Ih == 0) {
-      v_chunk<0, FULL>(Vt, ch, w, pr, nv);
-      v_chunk<1, FULL>(Vt, ch, w, pr, nv);
-      v_chunk<2, FULL>(Vt, ch, w, pr, nv);
-      v_chunk<3, FULL>(Vt, ch, w, pr, nv);
-    } else {
-      v_chunk<4, FULL>(Vt, ch, w, pr, nv);
-      v_chunk<5, FULL>(Vt, ch, w, pr, nv);
-      v_chunk<6, FULL>(Vt, ch, w, pr, nv);
-      v_chunk<7, FULL>(Vt, ch, w, pr, nv);
-    }
+    v_chunk<0, FULL>(Vt, ch, w, pr, nv);
+    v_chunk<1, FULL>(Vt, ch, w, pr, nv);
+    v_chunk<2, FULL>(Vt, ch, w, pr, nv);
+    v_chunk<3, FULL>(Vt, ch, w, pr, nv);
+    v_chunk<4, FULL>(Vt, ch, w, pr, nv);
+    v_chunk<5, FULL>(Vt, ch, w, pr, nv);
+    v_chunk<6, FULL>(Vt, ch, w, pr, nv);
+    v_chunk<7, FULL>(Vt, ch, w, pr, nv);
   }
 }
 
@@ -796,16 +845,16 @@ __device__ __forceinline__ void dequant_page(uint8_t* Kt, uint8_t* Vt, const uin
 __device__ __forceinline__ void convert_bf16(uint8_t* Kt, uint8_t* Vt, const __nv_bfloat16* Kb,
                                              const __nv_bfloat16* Vb, size_t stride, uint64_t valid, int t) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int u = t + NPROD * j, tok = u >> 4, c16 = u & 15;
+  for (int j = 0; j < 8; ++j) {
+    const int u = t + 128 * j, tok = u >> 4, c16 = u & 15;
     uint4 x = make_uint4(0u, 0u, 0u, 0u);
     if ((valid >> tok) & 1ull) x = *(const uint4*)(Kb + tok * stride + 8 * c16);
     const uint4 y = make_uint4(bf2_to_h2(x.x), bf2_to_h2(x.y), bf2_to_h2(x.z), bf2_to_h2(x.w));
     *(uint4*)(Kt + (c16 >> 3) * (PAGE * 128) + tok * 128 + (((c16 & 7) ^ (tok & 7)) << 4)) = y;
   }
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int u = t + NPROD * j, jp = u & 31, k8 = u >> 5;
+  for (int j = 0; j < 4; ++j) {
+    const int u = t + 128 * j, jp = u & 31, k8 = u >> 5;
     uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
     if ((valid >> (2 * jp)) & 1ull) x0 = *(const uint4*)(Vb + (2 * jp) * stride + 8 * k8);
     if ((valid >> (2 * jp + 1)) & 1ull) x1 = *(const uint4*)(Vb + (2 * jp + 1) * stride + 8 * k8);
@@ -853,10 +902,10 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(PrefillArgs 
   if (tid == 0) {
     for (int i = 0; i < NRAW; ++i) {
       mbar_init(&bars[B_RAW_FULL + i], 1);
-      mbar_init(&bars[B_RAW_EMPTY + i], NPROD / 32);
+      mbar_init(&bars[B_RAW_EMPTY + i], 4);  // the four warps of the page's producer group
     }
     for (int i = 0; i < NKV; ++i) {
-      mbar_init(&bars[B_KV_FULL + i], NPROD);
+      mbar_init(&bars[B_KV_FULL + i], 128);  // the page's producer group
       mbar_init(&bars[B_KV_EMPTY + i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -995,36 +1044,42 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(PrefillArgs 
         const uint32_t v = (t < 8) ? 0x3C003C00u : 0u;
         *(uint4*)(smem + OFF_KV + kb * KV_BYTES + K_BYTES + 128 * 128 + 16 * t) = make_uint4(v, v, v, v);
       }
-    uint2* pairs0 = (uint2*)(smem + OFF_PAIRS);
+    const int pg = t >> 7, tq = t & 127;  // producer group (pages pg, pg + 2, ...), thread in it
+    const uint32_t gbar = 5 + pg;         // the group's named barrier
+    uint2* pairs0 = (uint2*)(smem + OFF_PAIRS) + pg * 256;
     int nn = n;
-    // the (s, z) pair table of page i is built one page ahead (page 0 here)
-    if (!win && n > 0) {
-      if (producers_all(wait_bar(&bars[B_RAW_FULL], 0, abort_flag)))
-        build_pairs(smem + tc::OFF_RAW, pairs0, NG, t);
+    // the (s, z) pair table of a page is built one page ahead (the first one here)
+    if (!win && n > pg) {
+      if (group_all(gbar, wait_bar(&bars[B_RAW_FULL + pg], 0, abort_flag)))
+        build_pairs(smem + tc::OFF_RAW + pg * RAW_SLOT, pairs0, NG, tq);
       else
         nn = 0;
     }
-    for (int i = 0; i < nn; ++i) {
+    for (int k = 0;; ++k) {
+      const int i = 2 * k + pg;
+      if (i >= nn) break;
       const int kb = i % NKV;
       uint8_t* Kt = smem + OFF_KV + kb * KV_BYTES;
       uint8_t* Vt = Kt + K_BYTES;
       bool okw = i < NKV || wait_bar(&bars[B_KV_EMPTY + kb], ((i / NKV) - 1) & 1, abort_flag);
-      if (!win && i + 1 < n) okw = okw && wait_bar(&bars[B_RAW_FULL + (i + 1) % NRAW], ((i + 1) / NRAW) & 1, abort_flag);
-      // also: every producer is done with page i - 1 and with the pair table of page i
-      if (!producers_all(okw)) break;
+      if (!win && i + 2 < n)
+        okw = okw && wait_bar(&bars[B_RAW_FULL + (i + 2) % NRAW], ((i + 2) / NRAW) & 1, abort_flag);
+      // also: the group is done with its previous page and with this page's pair table
+      if (!group_all(gbar, okw)) break;
       uint64_t mask;
       int causal = 0;
       if (!win) {
         const int slot = i % NRAW;
-        if (i + 1 < n) build_pairs(smem + tc::OFF_RAW + ((i + 1) % NRAW) * RAW_SLOT, pairs0 + ((i + 1) & 1) * 128, NG, t);
-        const int pg = p0 + i;
-        int nv = pg == pages - 1 ? hist - pg * PAGE : PAGE;
+        if (i + 2 < n)
+          build_pairs(smem + tc::OFF_RAW + ((i + 2) % NRAW) * RAW_SLOT, pairs0 + ((k + 1) & 1) * 128, NG, tq);
+        const int pgn = p0 + i;
+        int nv = pgn == pages - 1 ? hist - pgn * PAGE : PAGE;
         if (misc[2 + slot]) nv = 0;
         const uint8_t* raw = smem + tc::OFF_RAW + slot * RAW_SLOT;
         if (nv == PAGE)
-          dequant_page<true>(Kt, Vt, raw, pairs0 + (i & 1) * 128, lg, NG, nv, t);
+          dequant_page<true>(Kt, Vt, raw, pairs0 + (k & 1) * 128, lg, NG, nv, tq);
         else
-          dequant_page<false>(Kt, Vt, raw, pairs0 + (i & 1) * 128, lg, NG, nv, t);
+          dequant_page<false>(Kt, Vt, raw, pairs0 + (k & 1) * 128, lg, NG, nv, tq);
         mask = low_mask(nv);
       } else {
         const int kind = kinds[i];
@@ -1048,9 +1103,9 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(PrefillArgs 
           Kb = a.k + ((size_t)b * a.T * Hkv + kvh) * D;
           Vb = a.v + ((size_t)b * a.T * Hkv + kvh) * D;
         }
-        convert_bf16(Kt, Vt, Kb, Vb, stride, mask, t);
+        convert_bf16(Kt, Vt, Kb, Vb, stride, mask, tq);
       }
-      if (t == 0) {
+      if (tq == 0) {
         *(uint64_t*)(info + kb * 16) = mask;
         *(int*)(info + kb * 16 + 8) = causal;
       }
@@ -1167,33 +1222,86 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(PrefillArgs 
       __syncwarp();
       if (lane == 0) arrive(&bars[B_P_FULL + wg]);
     }
-    // this warpgroup's partial record: m (log2 units), l, o (unnormalised)
-    const bool has = n > wg;
-    if (ok && has) ok = __all_sync(0xffffffffu, wait_bar(&bars[B_O_FINAL + wg], 0, abort_flag));
-    float* rec = a.part + ((((size_t)tile * (a.NS + 1) + split) * 2 + wg) * PF_ROWS + row) * PART_STRIDE;
-    if (ok && has) {
+    // one partial record per CTA: m (log2 units), l, o (unnormalised).  With
+    // two or more pages both warpgroups hold a partial: warpgroup 1 hands its
+    // row to warpgroup 0 through the (then idle) first K/V buffers.
+    float* rec = a.part + (((size_t)tile * (a.NS + 1) + split) * PF_ROWS + row) * PART_STRIDE;
+    if (n >= 2) {
+      float* xch = (float*)(smem + OFF_KV) + row * PART_STRIDE;
+      ok = ok && __all_sync(0xffffffffu, wait_bar(&bars[B_O_FINAL], 0, abort_flag));
+      ok = ok && __all_sync(0xffffffffu, wait_bar(&bars[B_O_FINAL + 1], 0, abort_flag));
       fence_after();
+      if (wg == 1) {
 #pragma unroll 1
-      for (int c = 0; c < 160; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(oa + c, v);
-        tmem_ld_wait_regs(v);
-        if (grow < R) {
+        for (int c = 0; c < 160; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(oa + c, v);
+          tmem_ld_wait_regs(v);
           if (c < 128) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
-              *(float4*)(rec + PART_O + c + j) = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+              *(float4*)(xch + PART_O + c + j) = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
                                                              __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
           } else {
-            rec[0] = m_run;
-            rec[1] = __uint_as_float(v[0]);
+            xch[0] = ok ? m_run : -1e30f;
+            xch[1] = ok ? __uint_as_float(v[0]) : 0.f;
           }
         }
       }
-    } else if (grow < R) {  // no pages for this warpgroup (or aborted): an empty partial
-      rec[0] = -1e30f;
-      rec[1] = 0.f;
-      for (int j = 0; j < D; j += 4) *(float4*)(rec + PART_O + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+      asm volatile("bar.sync 3, 256;\n" ::: "memory");  // the two softmax warpgroups
+      if (wg == 0) {
+        uint32_t lv[32];
+        tmem_ld32(oa + 128, lv);
+        tmem_ld_wait_regs(lv);
+        const float m0 = ok ? m_run : -1e30f, l0 = ok ? __uint_as_float(lv[0]) : 0.f;
+        const float m1 = xch[0], l1 = xch[1];
+        const float M = fmaxf(m0, m1), w0 = ex2(m0 - M), w1 = ex2(m1 - M);
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(oa + c, v);
+          tmem_ld_wait_regs(v);
+          if (grow < R) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              const float4 x1 = *(const float4*)(xch + PART_O + c + j);
+              *(float4*)(rec + PART_O + c + j) =
+                  make_float4(w0 * __uint_as_float(v[j]) + w1 * x1.x, w0 * __uint_as_float(v[j + 1]) + w1 * x1.y,
+                              w0 * __uint_as_float(v[j + 2]) + w1 * x1.z, w0 * __uint_as_float(v[j + 3]) + w1 * x1.w);
+            }
+          }
+        }
+        if (grow < R) {
+          rec[0] = M;
+          rec[1] = w0 * l0 + w1 * l1;
+        }
+      }
+    } else if (wg == 0) {
+      if (ok && n == 1) ok = __all_sync(0xffffffffu, wait_bar(&bars[B_O_FINAL], 0, abort_flag));
+      if (ok && n == 1) {
+        fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 160; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(oa + c, v);
+          tmem_ld_wait_regs(v);
+          if (grow < R) {
+            if (c < 128) {
+#pragma unroll
+              for (int j = 0; j < 32; j += 4)
+                *(float4*)(rec + PART_O + c + j) = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                                               __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+            } else {
+              rec[0] = m_run;
+              rec[1] = __uint_as_float(v[0]);
+            }
+          }
+        }
+      } else if (grow < R) {  // no pages (or aborted): an empty partial
+        rec[0] = -1e30f;
+        rec[1] = 0.f;
+        for (int j = 0; j < D; j += 4) *(float4*)(rec + PART_O + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   }
   fence_before();
@@ -1219,7 +1327,7 @@ PrefillScratch prefill_scratch_layout(int B, int Hkv, int G, int T, int NS) {
   };
   L.off_qh = take((size_t)2 * B * Hkv * RP * D * sizeof(__half));
   L.off_alpha = take((size_t)B * Hkv * RP * sizeof(float));
-  L.off_part = take((size_t)B * Hkv * RT * (NS + 1) * 2 * PF_ROWS * PART_STRIDE * sizeof(float));
+  L.off_part = take((size_t)B * Hkv * RT * (NS + 1) * PF_ROWS * PART_STRIDE * sizeof(float));
   L.total = off;
   return L;
 }
@@ -1235,6 +1343,10 @@ static cudaError_t ensure_prefill_smem() {
   static int done = 0;  // per process; the attribute is per device function
   if (done) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(prefill_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(prefill_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MERGE_SMEM);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM);
   if (e == cudaSuccess) done = 1;
@@ -1254,10 +1366,10 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st, Profiler* prof
   cudaError_t e = ensure_prefill_smem();
   if (e != cudaSuccess) return e;
   const int tiles = a.B * a.cv.Hkv * a.RT;
-  PrefillArgs b = a;
-  b.rpc = a.impl == OSCAR_PREFILL_MMA_SYNC ? 1 : 2;
+  const PrefillArgs& b = a;
   prof_begin(prof, OSCAR_KERNEL_PREFILL_PREP, st);
-  e = launch_pdl(prefill_prep_kernel, dim3(a.B * a.cv.Hkv, a.RT * (PF_ROWS / 8)), dim3(128), 0, st, b);
+  e = launch_pdl(prefill_prep_kernel, dim3(a.B * a.cv.Hkv, a.RT * (PF_ROWS / PREP_ROWS)), dim3(256), PREP_SMEM, st,
+                 b);
   prof_end(prof, OSCAR_KERNEL_PREFILL_PREP, st);
   if (e != cudaSuccess) return e;
   prof_begin(prof, OSCAR_KERNEL_PREFILL_ATTN, st);
@@ -1268,7 +1380,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st, Profiler* prof
   prof_end(prof, OSCAR_KERNEL_PREFILL_ATTN, st);
   if (e != cudaSuccess) return e;
   prof_begin(prof, OSCAR_KERNEL_PREFILL_MERGE, st);
-  e = launch_pdl(prefill_merge_kernel, dim3(tiles, PF_ROWS / MERGE_ROWS), dim3(128), 0, st, b);
+  e = launch_pdl(prefill_merge_kernel, dim3(tiles, PF_ROWS / MROWS), dim3(256), MERGE_SMEM, st, b);
   prof_end(prof, OSCAR_KERNEL_PREFILL_MERGE, st);
   return e;
 }
