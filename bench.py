@@ -545,8 +545,9 @@ def run_ours(args, wl):
                     "flops_per_call": pf_flops, "tflops": pf_flops / (pf_us * 1e-6) / 1e12,
                     "attn_tflops": pf_attn_tf, "peak_tflops": tpk, "peak_kind": tpk_kind,
                     "attn_frac": pf_attn_tf / tpk,
-                    "note": "64 new tokens per request over the same 100K cache; fp16 mma.sync "
-                            "(legacy tensor path), bound: tensor"},
+                    "note": "64 new tokens per request attending to the same 100K cache; tcgen05.mma "
+                            "kind::f16 (M=128) with Q, S, P, O in tensor memory; bound: tensor; peak = "
+                            "dense bf16 burst (fp16 runs at the same rate)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(), "kernel": "decode_main",
                      "bytes_per_launch": bytes_main, "peak_kind": peak_kind},

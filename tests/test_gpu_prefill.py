@@ -163,3 +163,32 @@ def test_prefill_qwen3_8b_100k_sampled(impl):
             assert np.abs(lse[0, toks, h * G:(h + 1) * G].cpu().numpy() - rlse).max() <= LSE_TOL, h
     finally:
         sc.close()
+
+
+@pytest.mark.parametrize("impl", IMPLS, ids=["tcgen05", "mma_sync"])
+def test_prefill_missing_history_page_reports_and_skips_it(impl):
+    """A history page whose table entry is -1: the call records OSCAR_ERR_NO_PAGE
+    and the page's 64 tokens take no part; everything else is still exact."""
+    T = 16
+    sc = GS.build("pf_hole", [2000], Hq=4, Hkv=1, g=64, extra_tokens=T, calib_n=512)
+    try:
+        q, k, v = chunk_inputs(sc, T, seed=35)
+        hc = GS.HostCache(sc)  # before the hole
+        hole = 7
+        sc.cache["page_table"][0, hole] = -1
+        out, lse = run_prefill(sc, q, k, v, impl=impl)
+        assert oscar.oscar_get_error(sc.ctx) == oscar.ERR_NO_PAGE
+        f = hc.history_int2(0, 0, sc.g)
+        keep = np.ones(len(f["k_codes"]), dtype=bool)
+        keep[hole * 64:(hole + 1) * 64] = False
+        hk = O.dequantize(f["k_codes"][keep], f["k_s"][keep], f["k_z"][keep], sc.g)
+        hv = O.dequantize(f["v_codes"][keep], f["v_s"][keep], f["v_z"][keep], sc.g)
+        wk, wv = hc.window(0, 0)
+        ref, rlse = O.chunk_prefill_attention(q[0].float().cpu().numpy(), k[0, :, 0].float().cpu().numpy(),
+                                              v[0, :, 0].float().cpu().numpy(), wk, wv, hk, hv,
+                                              O.rotation(sc.U_K[0], sc.mode), O.rotation(sc.U_V[0], sc.mode))
+        got = out[0].float().cpu().numpy()
+        assert _rel(got, ref) <= REL_TOL, _rel(got, ref)
+        assert np.abs(lse[0].cpu().numpy() - rlse).max() <= LSE_TOL
+    finally:
+        sc.close()
