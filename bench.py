@@ -241,6 +241,40 @@ def oracle_sample(cache_host, wl, U, q, heads, budget_s=20.0, demote_tokens=None
     return el / done * Hkv, done
 
 
+def oracle_prefill_sample(cache_host, wl, U, q, k, v, tokens=(0, 63)):
+    """Times the oracle's chunked prefill for KV head 0 of one request on a
+    sample of chunk tokens and scales it to the whole call: the history
+    dequantisation once per KV head, the attention once per (token, KV head).
+    q [T][Hq][128], k, v [T][Hkv][128] float64."""
+    import numpy as np
+
+    import oracle as O
+
+    pool, pt, sink_k, sink_v, ring_k, ring_v, L, H = cache_host
+    g, Hkv, G = wl["g"], wl["Hkv"], wl["Hq"] // wl["Hkv"]
+    T = q.shape[0]
+    head_bytes = O.int2_head_block_bytes(g)
+    page_bytes = head_bytes * Hkv
+    h = 0
+    t0 = time.perf_counter()
+    pages = (H + 63) // 64
+    blocks = np.stack([pool[int(p) * page_bytes + h * head_bytes:int(p) * page_bytes + (h + 1) * head_bytes]
+                       for p in pt[:pages]])
+    f = O.parse_head_block(blocks, g)
+    hk = O.dequantize(f["k_codes"].reshape(-1, 128)[:H], f["k_s"].reshape(-1, 128 // g)[:H],
+                      f["k_z"].reshape(-1, 128 // g)[:H], g)
+    hv = O.dequantize(f["v_codes"].reshape(-1, 128)[:H], f["v_s"].reshape(-1, 128 // g)[:H],
+                      f["v_z"].reshape(-1, 128 // g)[:H], g)
+    slots = [(p - 64) % 256 for p in range(64 + H, L)]
+    wk = np.concatenate([sink_k[h, :min(L, 64)], ring_k[h, slots]])
+    wv = np.concatenate([sink_v[h, :min(L, 64)], ring_v[h, slots]])
+    t1 = time.perf_counter()
+    O.chunk_prefill_attention(q[:, h * G:(h + 1) * G], k[:, h], v[:, h], wk, wv, hk, hv,
+                              O.rotation(U[0][h]), O.rotation(U[1][h]), tokens=list(tokens))
+    t2 = time.perf_counter()
+    return Hkv * (t1 - t0) + Hkv * T * (t2 - t1) / len(tokens)
+
+
 def blas_threads():
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         if os.environ.get(var):
@@ -511,6 +545,7 @@ def run_ours(args, wl):
     d2h = q.numel() * 2
     # ---- CPU oracle on the GPU's own cache (bounded sample)
     cpu = None
+    prefill_cpu = None
     if rank == 0:
         c0 = wk["copies"][0]
         L = int(c0["seq_lens"][0])
@@ -524,6 +559,11 @@ def run_ours(args, wl):
                                   list(range(Hkv)), budget_s=args.cpu_budget)
         cpu = {"value": sec * 1e6, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
                "sample": f"{done} of {Hkv} KV heads of one decode step on the GPU-built cache, scaled to {Hkv}"}
+        psec = oracle_prefill_sample(host, wl, wk["U"], q_pf[0].float().cpu().numpy().astype(np.float64),
+                                     k_pf[0].float().cpu().numpy().astype(np.float64),
+                                     v_pf[0].float().cpu().numpy().astype(np.float64))
+        prefill_cpu = {"value": psec * 1e6, "unit": "us/call", "cores": blas_threads(), "kind": "oracle",
+                       "sample": f"KV head 0, chunk tokens 0 and 63; scaled to {T_pf} tokens x {Hkv} KV heads"}
     n_launch = 3 * K  # append + q rotation, decode, merge per step
     value = ms_per_step * 1e3 / world
     line = {
@@ -544,7 +584,7 @@ def run_ours(args, wl):
         "prefill": {"chunk_tokens": T_pf, "us_per_call": pf_us, "kernels_us": pf_prof,
                     "flops_per_call": pf_flops, "tflops": pf_flops / (pf_us * 1e-6) / 1e12,
                     "attn_tflops": pf_attn_tf, "peak_tflops": tpk, "peak_kind": tpk_kind,
-                    "attn_frac": pf_attn_tf / tpk,
+                    "attn_frac": pf_attn_tf / tpk, "cpu_baseline": prefill_cpu,
                     "note": "64 new tokens per request attending to the same 100K cache; tcgen05.mma "
                             "kind::f16 (M=128) with Q, S, P, O in tensor memory; bound: tensor; peak = "
                             "dense bf16 burst (fp16 runs at the same rate)"},

@@ -524,3 +524,54 @@ def logit_error_trace(Q, K, K_hat) -> float:
     Q = np.asarray(Q, dtype=np.float64)
     E = np.asarray(K, dtype=np.float64) - np.asarray(K_hat, dtype=np.float64)
     return float(np.trace(E @ (Q.T @ Q) @ E.T))
+
+
+# --------------------------------------------------------------------------
+# Clip search  [Blog, "OSCAR把旋转对准attention": rotation and clipping
+#               thresholds are fixed offline per layer and head; News, "OSCAR
+#               的不同之处": the key error that matters is the logit error]
+# --------------------------------------------------------------------------
+# Reading: a clip ratio is chosen from a candidate grid by the error it leaves
+# in what attention computes -- for keys the logit error ||Q K^T - Q K_hat^T||_F^2
+# over the calibration queries of all G heads, for values the output error
+# sum_h ||S_h V - S_h V_hat||_F^2 with S_h the causal scores of head h.  Both are
+# taken in the rotated basis, where they are equal to the unrotated ones
+# (R is orthogonal and Q K^T = (Q R)(K R)^T).
+
+def quantize_dequantize_rows(X, g: int, clip: float) -> np.ndarray:
+    """Each row quantised with the demotion's quantiser and dequantised, float64."""
+    X = np.asarray(X, dtype=np.float32)
+    out = np.zeros(X.shape, dtype=np.float64)
+    for n in range(X.shape[0]):
+        codes, s, z = quantize_vector(X[n], g, clip)
+        out[n] = dequantize(codes, s, z, g)
+    return out
+
+
+def key_clip_error(Q, K, R_K, g: int, clip: float) -> float:
+    """||Q' K'^T - Q' K_hat'^T||_F^2, Q' = Q R_K over the G heads' calibration
+    queries (Q [G][N][d] or [rows][d]), K' = K R_K in fp32 as the demotion
+    rotates, K_hat' its quantised and dequantised copy with ratio `clip`."""
+    Qr = np.asarray(Q, dtype=np.float64).reshape(-1, np.shape(Q)[-1]) @ np.asarray(R_K, dtype=np.float64)
+    Kr = rotate_to_f32(K, R_K)
+    return logit_error_direct(Qr, Kr.astype(np.float64), quantize_dequantize_rows(Kr, g, clip))
+
+
+def value_clip_error(Q, K, V, R_V, g: int, clip: float) -> float:
+    """sum_h ||S_h (V' - V_hat')||_F^2, S_h = causal_scores(Q_h, K) (unrotated
+    scores), V' = V R_V in fp32, V_hat' quantised and dequantised with `clip`."""
+    Vr = rotate_to_f32(V, R_V)
+    E = Vr.astype(np.float64) - quantize_dequantize_rows(Vr, g, clip)
+    Q = np.asarray(Q, dtype=np.float64)
+    total = 0.0
+    for h in range(Q.shape[0]):
+        Y = causal_scores(Q[h], K) @ E
+        total += float(np.sum(Y * Y))
+    return total
+
+
+def clip_search(Q, K, V, R_K, R_V, g: int, ratios):
+    """Errors of every candidate ratio and the argmin for keys and values."""
+    ek = [key_clip_error(Q, K, R_K, g, c) for c in ratios]
+    ev = [value_clip_error(Q, K, V, R_V, g, c) for c in ratios]
+    return np.array(ek), np.array(ev), int(np.argmin(ek)), int(np.argmin(ev))

@@ -491,3 +491,72 @@ def test_rotation_ordering_aligned_reading():
     mean = {k: np.mean([r[k] for r in res]) for k in res[0]}
     print("ordering aligned g=128:", mean)
     assert mean["none"] > mean["hadamard"] > mean["oscar"]
+
+
+# ------------------------------------------------------------------ clip search
+def _calib_set(seed, G=2, N=24, d=128):
+    rng = np.random.default_rng(seed)
+    Q = rng.standard_normal((G, N, d)).astype(np.float32)
+    K = rng.standard_normal((N, d)).astype(np.float32)
+    K[:, 5] *= 20.0  # an outlier channel, so clipping matters
+    V = rng.standard_normal((N, d)).astype(np.float32)
+    to_bf16 = lambda a: ((a.view(np.uint32) + 0x8000) & 0xFFFF0000).view(np.float32)
+    return to_bf16(Q), to_bf16(K), to_bf16(V)
+
+
+def test_key_clip_error_brute_force_tiny():
+    """The logit error of the chosen quantisation, summed (q'.(k' - k_hat'))^2 by
+    explicit loops over every (query row, key) pair."""
+    Q, K, V = _calib_set(1, G=2, N=6)
+    R = O.rotation(np.eye(128), O.ROT_HADAMARD)
+    for clip in (1.0, 0.8):
+        Kr = O.rotate_to_f32(K, R)
+        Kh = O.quantize_dequantize_rows(Kr, 32, clip)
+        Qr = Q.reshape(-1, 128).astype(np.float64) @ R
+        tot = 0.0
+        for r in range(Qr.shape[0]):
+            for n in range(Kr.shape[0]):
+                dlt = sum(Qr[r, c] * (float(Kr[n, c]) - Kh[n, c]) for c in range(128))
+                tot += dlt * dlt
+        assert O.key_clip_error(Q, K, R, 32, clip) == pytest.approx(tot, rel=1e-10)
+
+
+def test_clip_errors_vanish_on_the_quantiser_grid():
+    """Rows whose every group already holds 4 equally spaced levels (min and max
+    present) quantise exactly at clip 1.0: both errors are zero."""
+    rng = np.random.default_rng(3)
+    N, g = 8, 32
+    V = np.zeros((N, 128), dtype=np.float32)
+    for n in range(N):
+        for gr in range(128 // g):
+            base, step = rng.integers(-8, 8) * 0.25, 0.25 * rng.integers(1, 4)
+            lv = base + step * rng.integers(0, 4, g)
+            lv[0], lv[1] = base, base + 3 * step
+            V[n, gr * g:(gr + 1) * g] = lv
+    I = np.eye(128)
+    Q = rng.standard_normal((2, N, 128)).astype(np.float32)
+    assert O.value_clip_error(Q, V, V, I, g, 1.0) == 0.0
+    assert O.key_clip_error(Q, V, I, g, 1.0) == 0.0
+    assert O.value_clip_error(Q, V, V, I, g, 0.7) > 0.0
+
+
+def test_value_clip_error_single_token_is_plain_squared_error():
+    """With one calibration token the causal scores are [[1]]: the value error is
+    G times the squared quantisation error of that token."""
+    Q, K, V = _calib_set(4, G=3, N=1)
+    R = O.rotation(np.eye(128), O.ROT_HADAMARD)
+    Vr = O.rotate_to_f32(V, R)
+    e = Vr.astype(np.float64) - O.quantize_dequantize_rows(Vr, 64, 0.9)
+    assert O.value_clip_error(Q, K, V, R, 64, 0.9) == pytest.approx(3 * float(np.sum(e * e)), rel=1e-12)
+
+
+def test_clip_search_prefers_clipping_on_outlier_keys():
+    """With a x20 outlier channel, the Hadamard rotation spreads it over all
+    channels; plain uniform INT2 (no rotation) then does better with some
+    clipping than with none -- the search finds a ratio below 1 and its error
+    is the minimum of the grid."""
+    Q, K, V = _calib_set(5, G=2, N=32)
+    ratios = [1.0, 0.95, 0.9, 0.85, 0.8, 0.7]
+    ek, ev, ik, iv = O.clip_search(Q, K, V, np.eye(128), np.eye(128), 128, ratios)
+    assert ek[ik] == ek.min() and ev[iv] == ev.min()
+    assert ratios[ik] < 1.0
