@@ -273,6 +273,7 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(PrefillArgs a) {
   const int bk = blockIdx.x, b = bk / cv.Hkv, kvh = bk % cv.Hkv, G = cv.G;
   const int R = a.T * G, RP = a.RT * PF_ROWS, r0 = PREP_ROWS * blockIdx.y;
   const int tid = threadIdx.x, c = tid & 127, h = tid >> 7, w = tid >> 5, lane = tid & 31;
+  const int lgG = __ffs(G) - 1;  // G is a power of two
   {  // the rotation table is written synchronously by oscar_set_rotation: load it before the wait
     const float4* Rg = (const float4*)(a.rot.R_K + (size_t)kvh * D * D);
     float4 rv[16];
@@ -287,7 +288,8 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(PrefillArgs a) {
   for (int j = 0; j < 8; ++j) {
     const int r = r0 + 8 * h + j;
     xs[(8 * h + j) * D + c] =
-        r < R ? __bfloat162float(a.q[(((size_t)b * a.T + r / G) * cv.Hq + kvh * G + r % G) * D + c]) : 0.f;
+        r < R ? __bfloat162float(a.q[(((size_t)b * a.T + (r >> lgG)) * cv.Hq + kvh * G + (r & (G - 1))) * D + c])
+              : 0.f;
   }
   __syncthreads();
 #pragma unroll
@@ -305,11 +307,14 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(PrefillArgs a) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j] = 0.f;
   const float* xh = xs + 8 * h * D;
-#pragma unroll 8
-  for (int k = 0; k < D; ++k) {
-    const float rk = Rs[k * D + c];
+#pragma unroll 2
+  for (int k = 0; k < D; k += 4) {
+    const float r0 = Rs[k * D + c], r1 = Rs[(k + 1) * D + c], r2 = Rs[(k + 2) * D + c], r3 = Rs[(k + 3) * D + c];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = fmaf(xh[j * D + k], rk, acc[j]);
+    for (int j = 0; j < 8; ++j) {
+      const float4 x = *(const float4*)(xh + j * D + k);  // same address across the warp: one broadcast
+      acc[j] = fmaf(x.x, r0, fmaf(x.y, r1, fmaf(x.z, r2, fmaf(x.w, r3, acc[j]))));
+    }
   }
   const size_t vstride = (size_t)a.B * cv.Hkv * RP * D;
 #pragma unroll
@@ -576,17 +581,21 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(PrefillArgs a) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) y[j] = 0.f;
   const float* xh = xs + 8 * h * D;
-#pragma unroll 8
-  for (int k = 0; k < D; ++k) {
-    const float r = Rs[k * D + c];
+#pragma unroll 2
+  for (int k = 0; k < D; k += 4) {
+    const float r0 = Rs[k * D + c], r1 = Rs[(k + 1) * D + c], r2 = Rs[(k + 2) * D + c], r3 = Rs[(k + 3) * D + c];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) y[j] = fmaf(xh[j * D + k], r, y[j]);
+    for (int j = 0; j < 8; ++j) {
+      const float4 x = *(const float4*)(xh + j * D + k);  // same address across the warp: one broadcast
+      y[j] = fmaf(x.x, r0, fmaf(x.y, r1, fmaf(x.z, r2, fmaf(x.w, r3, y[j]))));
+    }
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int r = rt * PF_ROWS + i0 + 8 * h + j;
     if (r >= R) continue;
-    const size_t row = ((size_t)b * a.T + r / G) * cv.Hq + kvh * G + r % G;
+    const int lgG = __ffs(G) - 1;  // G is a power of two
+    const size_t row = ((size_t)b * a.T + (r >> lgG)) * cv.Hq + kvh * G + (r & (G - 1));
     a.out[row * D + c] = __float2bfloat16_rn((y[j] + ow[j]) * linv[8 * h + j]);
     if (c == 0 && a.lse) a.lse[row] = lsev[8 * h + j];
   }
@@ -694,6 +703,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       : "memory");
 }
 #undef OSCAR_W8
+// One 32-bit TMEM column of this warp's 32 lanes (waits for it).
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n" : "=r"(r) : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" : "+r"(r)::"memory");
+  return __uint_as_float(r);
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t ex2_h2(uint32_t x) {
@@ -945,15 +961,16 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(PrefillArgs 
   const int recent = Lq > SINK ? Lq - SINK - hist : 0;
   const int h0 = ((hist % RECENT) + RECENT) % RECENT;
   int p0 = 0, n = 0;
-  int kinds[6];
+  uint32_t kinds = 0;  // window: bit k set when tile kind k (0 sink, 1..4 ring quarters, 5 chunk) is present
   if (!win) {
     p0 = (int)((long long)split * pages / a.NS);
     n = (int)((long long)(split + 1) * pages / a.NS) - p0;
   } else {
-    if (nsink > 0) kinds[n++] = 0;
+    kinds = (nsink > 0 ? 1u : 0u) | (1u << 5);
+#pragma unroll
     for (int q = 0; q < 4; ++q)
-      if (ring_meets(h0, recent, 64 * q)) kinds[n++] = 1 + q;
-    kinds[n++] = 5;
+      if (ring_meets(h0, recent, 64 * q)) kinds |= 2u << q;
+    n = __popc(kinds);
   }
   const int gbytes = cv.head_bytes;
   const int32_t* ptab = cv.page_table + (size_t)b * cv.max_pages_per_req;
@@ -1055,21 +1072,16 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(PrefillArgs 
       else
         nn = 0;
     }
-    for (int k = 0;; ++k) {
-      const int i = 2 * k + pg;
-      if (i >= nn) break;
-      const int kb = i % NKV;
-      uint8_t* Kt = smem + OFF_KV + kb * KV_BYTES;
-      uint8_t* Vt = Kt + K_BYTES;
-      bool okw = i < NKV || wait_bar(&bars[B_KV_EMPTY + kb], ((i / NKV) - 1) & 1, abort_flag);
-      if (!win && i + 2 < n)
-        okw = okw && wait_bar(&bars[B_RAW_FULL + (i + 2) % NRAW], ((i + 2) / NRAW) & 1, abort_flag);
-      // also: the group is done with its previous page and with this page's pair table
-      if (!group_all(gbar, okw)) break;
-      uint64_t mask;
-      int causal = 0;
-      if (!win) {
-        const int slot = i % NRAW;
+    if (!win) {
+      for (int k = 0;; ++k) {  // history pages pg, pg + 2, ...
+        const int i = 2 * k + pg;
+        if (i >= nn) break;
+        const int kb = i % NKV, slot = i % NRAW;
+        uint8_t* Kt = smem + OFF_KV + kb * KV_BYTES;
+        bool okw = i < NKV || wait_bar(&bars[B_KV_EMPTY + kb], ((i / NKV) - 1) & 1, abort_flag);
+        if (i + 2 < n) okw = okw && wait_bar(&bars[B_RAW_FULL + (i + 2) % NRAW], ((i + 2) / NRAW) & 1, abort_flag);
+        // also: the group is done with its previous page and with this page's pair table
+        if (!group_all(gbar, okw)) break;
         if (i + 2 < n)
           build_pairs(smem + tc::OFF_RAW + ((i + 2) % NRAW) * RAW_SLOT, pairs0 + ((k + 1) & 1) * 128, NG, tq);
         const int pgn = p0 + i;
@@ -1077,12 +1089,29 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(PrefillArgs 
         if (misc[2 + slot]) nv = 0;
         const uint8_t* raw = smem + tc::OFF_RAW + slot * RAW_SLOT;
         if (nv == PAGE)
-          dequant_page<true>(Kt, Vt, raw, pairs0 + (k & 1) * 128, lg, NG, nv, tq);
+          dequant_page<true>(Kt, Kt + K_BYTES, raw, pairs0 + (k & 1) * 128, lg, NG, nv, tq);
         else
-          dequant_page<false>(Kt, Vt, raw, pairs0 + (k & 1) * 128, lg, NG, nv, tq);
-        mask = low_mask(nv);
-      } else {
-        const int kind = kinds[i];
+          dequant_page<false>(Kt, Kt + K_BYTES, raw, pairs0 + (k & 1) * 128, lg, NG, nv, tq);
+        if (tq == 0) {
+          *(uint64_t*)(info + kb * 16) = low_mask(nv);
+          *(int*)(info + kb * 16 + 8) = 0;
+        }
+        fence_proxy_async();
+        arrive(&bars[B_KV_FULL + kb]);
+        __syncwarp();
+        if (lane == 0) arrive(&bars[B_RAW_EMPTY + slot]);  // raw slot of page i free again
+      }
+    } else {
+      for (int k = 0;; ++k) {  // window tiles pg, pg + 2, ...
+        const int i = 2 * k + pg;
+        if (i >= nn) break;
+        const int kb = i % NKV;
+        uint8_t* Kt = smem + OFF_KV + kb * KV_BYTES;
+        const bool okw = i < NKV || wait_bar(&bars[B_KV_EMPTY + kb], ((i / NKV) - 1) & 1, abort_flag);
+        if (!group_all(gbar, okw)) break;
+        const int kind = __fns(kinds, 0, i + 1);  // the (i+1)-th present kind
+        uint64_t mask;
+        int causal = 0;
         const __nv_bfloat16 *Kb, *Vb;
         size_t stride = D;
         if (kind == 0) {
@@ -1103,17 +1132,13 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(PrefillArgs 
           Kb = a.k + ((size_t)b * a.T * Hkv + kvh) * D;
           Vb = a.v + ((size_t)b * a.T * Hkv + kvh) * D;
         }
-        convert_bf16(Kt, Vt, Kb, Vb, stride, mask, tq);
-      }
-      if (tq == 0) {
-        *(uint64_t*)(info + kb * 16) = mask;
-        *(int*)(info + kb * 16 + 8) = causal;
-      }
-      fence_proxy_async();
-      arrive(&bars[B_KV_FULL + kb]);
-      if (!win) {  // raw slot of page i free again
-        __syncwarp();
-        if (lane == 0) arrive(&bars[B_RAW_EMPTY + i % NRAW]);
+        convert_bf16(Kt, Kt + K_BYTES, Kb, Vb, stride, mask, tq);
+        if (tq == 0) {
+          *(uint64_t*)(info + kb * 16) = mask;
+          *(int*)(info + kb * 16 + 8) = causal;
+        }
+        fence_proxy_async();
+        arrive(&bars[B_KV_FULL + kb]);
       }
     }
   } else {
@@ -1233,27 +1258,23 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(PrefillArgs 
       fence_after();
       if (wg == 1) {
 #pragma unroll 1
-        for (int c = 0; c < 160; c += 32) {
+        for (int c = 0; c < 128; c += 32) {
           uint32_t v[32];
           tmem_ld32(oa + c, v);
           tmem_ld_wait_regs(v);
-          if (c < 128) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              *(float4*)(xch + PART_O + c + j) = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                                             __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-          } else {
-            xch[0] = ok ? m_run : -1e30f;
-            xch[1] = ok ? __uint_as_float(v[0]) : 0.f;
-          }
+          for (int j = 0; j < 32; j += 4)
+            *(float4*)(xch + PART_O + c + j) = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                                           __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
         }
+        const float l1 = tmem_ld1(oa + 128);
+        xch[0] = ok ? m_run : -1e30f;
+        xch[1] = ok ? l1 : 0.f;
       }
       asm volatile("bar.sync 3, 256;\n" ::: "memory");  // the two softmax warpgroups
       if (wg == 0) {
-        uint32_t lv[32];
-        tmem_ld32(oa + 128, lv);
-        tmem_ld_wait_regs(lv);
-        const float m0 = ok ? m_run : -1e30f, l0 = ok ? __uint_as_float(lv[0]) : 0.f;
+        const float l0r = tmem_ld1(oa + 128);
+        const float m0 = ok ? m_run : -1e30f, l0 = ok ? l0r : 0.f;
         const float m1 = xch[0], l1 = xch[1];
         const float M = fmaxf(m0, m1), w0 = ex2(m0 - M), w1 = ex2(m1 - M);
 #pragma unroll 1
@@ -1281,21 +1302,21 @@ __global__ void __launch_bounds__(tc::THREADS, 1) prefill_tc_kernel(PrefillArgs 
       if (ok && n == 1) {
         fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 160; c += 32) {
+        for (int c = 0; c < 128; c += 32) {
           uint32_t v[32];
           tmem_ld32(oa + c, v);
           tmem_ld_wait_regs(v);
           if (grow < R) {
-            if (c < 128) {
 #pragma unroll
-              for (int j = 0; j < 32; j += 4)
-                *(float4*)(rec + PART_O + c + j) = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                                               __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-            } else {
-              rec[0] = m_run;
-              rec[1] = __uint_as_float(v[0]);
-            }
+            for (int j = 0; j < 32; j += 4)
+              *(float4*)(rec + PART_O + c + j) = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                                             __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
           }
+        }
+        const float l0 = tmem_ld1(oa + 128);
+        if (grow < R) {
+          rec[0] = m_run;
+          rec[1] = l0;
         }
       } else if (grow < R) {  // no pages (or aborted): an empty partial
         rec[0] = -1e30f;
