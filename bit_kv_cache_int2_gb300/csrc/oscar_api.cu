@@ -610,6 +610,98 @@ oscar_status oscar_prefill(oscar_ctx* ctx, int layer, const oscar_cache* cache, 
   return cuda_status(launch_prefill(a, (cudaStream_t)stream, &ctx->prof));
 }
 
+size_t oscar_calibration_scratch_bytes(int G, int N, int M) {
+  if (G < 1 || N < 1 || M < 0) return 0;
+  return calib_scratch_layout(G, N, M).total;
+}
+
+namespace {
+// Column-major eigenvectors of ascending eigenvalues -> row-major U with
+// column i = eigenvector of the i-th largest, largest-|.| entry positive.
+void order_eigenvectors(const double* evec, float* U) {
+  for (int i = 0; i < D; ++i) {
+    const double* v = evec + (size_t)(D - 1 - i) * D;
+    int arg = 0;
+    for (int r = 1; r < D; ++r)
+      if (fabs(v[r]) > fabs(v[arg])) arg = r;
+    const double sg = v[arg] < 0 ? -1.0 : 1.0;
+    for (int r = 0; r < D; ++r) U[(size_t)r * D + i] = (float)(sg * v[r]);
+  }
+}
+}  // namespace
+
+oscar_status oscar_calibrate(oscar_ctx* ctx, const void* Q, const void* K, const void* V, int N, float* U_K,
+                             float* U_V, double* C_Q, double* C_S, void* scratch, size_t scratch_bytes,
+                             oscar_stream_t stream) {
+  if (!ctx || !Q || !K || !V || !U_K || !U_V || !scratch || N < 1) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned(scratch, 256) || !aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16)) return OSCAR_ERR_INVALID_ARG;
+  const int G = ctx->G;
+  const CalibScratch L = calib_scratch_layout(G, N, 0);
+  if (scratch_bytes < L.total) return OSCAR_ERR_INVALID_ARG;
+  const cudaStream_t st = (cudaStream_t)stream;
+  uint8_t* sp = (uint8_t*)scratch;
+  cudaError_t e = calib_covariances((const __nv_bfloat16*)Q, (const __nv_bfloat16*)K, (const __nv_bfloat16*)V, G, N,
+                                    sp, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  const double* dC = (const double*)(sp + L.off_c);
+  if (C_Q || C_S) {
+    std::vector<double> h(2 * D * D);
+    e = cudaMemcpyAsync(h.data(), dC, h.size() * sizeof(double), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_status(e);
+    const double inv = 1.0 / ((double)G * N);
+    for (int i = 0; i < D * D; ++i) {
+      if (C_Q) C_Q[i] = h[i] * inv;
+      if (C_S) C_S[i] = h[D * D + i] * inv;
+    }
+  }
+  std::vector<double> evec(D * D);
+  for (int t = 0; t < 2; ++t) {
+    int ce = 0;
+    const oscar_status s = calib_eigh(dC + (size_t)t * D * D, evec.data(), st, &ce);
+    if (s == OSCAR_ERR_CUDA && ce) return cuda_status((cudaError_t)ce);
+    if (s != OSCAR_OK) return s;
+    order_eigenvectors(evec.data(), t == 0 ? U_K : U_V);
+  }
+  return OSCAR_OK;
+}
+
+oscar_status oscar_clip_errors(oscar_ctx* ctx, int layer, int kv_head, const void* Q, const void* K, const void* V,
+                               int N, const float* ratios, int M, double* err_k, double* err_v, int* best_k,
+                               int* best_v, void* scratch, size_t scratch_bytes, oscar_stream_t stream) {
+  if (!ctx || !Q || !K || !V || !ratios || !err_k || !err_v || !scratch || N < 1 || M < 1)
+    return OSCAR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= ctx->cfg.num_layers || kv_head < 0 || kv_head >= ctx->cfg.num_kv_heads)
+    return OSCAR_ERR_INVALID_ARG;
+  if (!aligned(scratch, 256) || !aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16)) return OSCAR_ERR_INVALID_ARG;
+  for (int m = 0; m < M; ++m)
+    if (!(ratios[m] > 0.f && ratios[m] <= 1.f)) return OSCAR_ERR_INVALID_ARG;
+  const int G = ctx->G;
+  const CalibScratch L = calib_scratch_layout(G, N, M);
+  if (scratch_bytes < L.total) return OSCAR_ERR_INVALID_ARG;
+  const cudaStream_t st = (cudaStream_t)stream;
+  const LayerRot r = layer_rot(ctx, layer);
+  uint8_t* sp = (uint8_t*)scratch;
+  cudaError_t e = calib_clip_errors(r.R_K + (size_t)kv_head * D * D, r.R_V + (size_t)kv_head * D * D,
+                                    (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K, (const __nv_bfloat16*)V, G, N,
+                                    ctx->cfg.group_size, ratios, M, sp, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  std::vector<double> h(2 * (size_t)M);
+  e = cudaMemcpyAsync(h.data(), sp + L.off_err, h.size() * sizeof(double), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_status(e);
+  int bk = 0, bv = 0;
+  for (int m = 0; m < M; ++m) {
+    err_k[m] = h[m];
+    err_v[m] = h[M + m];
+    if (h[m] < h[bk]) bk = m;
+    if (h[M + m] < h[M + bv]) bv = m;
+  }
+  if (best_k) *best_k = bk;
+  if (best_v) *best_v = bv;
+  return OSCAR_OK;
+}
+
 oscar_status oscar_decode_noalloc(oscar_ctx* ctx, int layer, const oscar_cache* cache,
                                   const void* q, void* out, float* lse, int batch,
                                   oscar_stream_t stream) {

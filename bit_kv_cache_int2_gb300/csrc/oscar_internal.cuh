@@ -597,6 +597,25 @@ int prefill_max_splits(int B, int Hkv, int G, int T);  // NS bound the scratch i
 cudaError_t prefill_ctas_per_sm(int* n, int impl);        // resident attention CTAs per SM
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t st, Profiler* prof);
 
+// ------------------------------------------------------------- calibration
+// Offline: covariances, eigenbases and clip errors of one (layer, kv head).
+struct CalibScratch {
+  size_t off_c, off_cf, off_err, off_clips, off_y, off_kr, off_vr, off_e, total;
+};
+CalibScratch calib_scratch_layout(int G, int N, int M);
+// Unnormalised sums into scratch: C_Q = Σ qᵀq over the G·N rows of Q, then
+// C_S = Σ_h (S_h V)ᵀ(S_h V) (fp64 [2][128][128] at off_c).
+cudaError_t calib_covariances(const __nv_bfloat16* Q, const __nv_bfloat16* K, const __nv_bfloat16* V, int G, int N,
+                              uint8_t* scratch, cudaStream_t st);
+// Eigenvectors of the symmetric fp64 device matrix dC (column i of the
+// column-major result = eigenvector of the i-th smallest eigenvalue), copied to
+// host memory; synchronises st.  OSCAR_ERR_UNSUPPORTED when cuSOLVER is absent.
+oscar_status calib_eigh(const double* dC, double* evec_host, cudaStream_t st, int* cuda_err);
+// Key and value clip errors of M candidate ratios into scratch (fp64 [2][M] at off_err).
+cudaError_t calib_clip_errors(const float* R_K, const float* R_V, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                              const __nv_bfloat16* V, int G, int N, int g, const float* clips_host, int M,
+                              uint8_t* scratch, cudaStream_t st);
+
 cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* k,
                           const __nv_bfloat16* v, int B, int do_append, int* req_counter,
                           cudaStream_t st, Profiler* prof);

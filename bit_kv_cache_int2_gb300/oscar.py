@@ -110,6 +110,14 @@ _SIGS = {
     "oscar_prefill": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(oscar_cache), ctypes.c_void_p, ctypes.c_void_p,
                        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                        ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
+    "oscar_calibration_scratch_bytes": ([ctypes.c_int, ctypes.c_int, ctypes.c_int], ctypes.c_size_t),
+    "oscar_calibrate": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                         ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
+    "oscar_clip_errors": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                           ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                           ctypes.c_void_p], ctypes.c_int),
     "oscar_profile_enable": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "oscar_profile_read": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                             ctypes.POINTER(ctypes.c_double), ctypes.c_int], ctypes.c_int),
@@ -250,6 +258,48 @@ def oscar_decode(ctx, layer, cache: dict, q, out, lse, scratch, batch, stream=No
     _check(lib().oscar_decode(ctx, layer, ctypes.byref(cs), _ptr(q), _ptr(out), _ptr(lse), _ptr(scratch),
                               scratch.numel() * scratch.element_size(), batch, _stream(stream)),
            "oscar_decode")
+
+
+def calibration_scratch(G, N, M=0, device="cuda"):
+    import torch
+
+    n = lib().oscar_calibration_scratch_bytes(G, N, M)
+    return torch.empty((n + 255) // 256 * 256, dtype=torch.uint8, device=device)
+
+
+def _np_ptr(a):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def oscar_calibrate(ctx, Q, K, V, N, scratch, stream=None):
+    """Q device bf16 [G][N][128]; K, V device bf16 [N][128].  Returns host
+    (U_K, U_V) float32 [128][128] and (C_Q, C_S) float64 [128][128]."""
+    import numpy as np
+
+    U_K = np.zeros((128, 128), dtype=np.float32)
+    U_V = np.zeros((128, 128), dtype=np.float32)
+    C_Q = np.zeros((128, 128), dtype=np.float64)
+    C_S = np.zeros((128, 128), dtype=np.float64)
+    _check(lib().oscar_calibrate(ctx, _ptr(Q), _ptr(K), _ptr(V), N, _np_ptr(U_K), _np_ptr(U_V), _np_ptr(C_Q),
+                                 _np_ptr(C_S), _ptr(scratch), scratch.numel() * scratch.element_size(),
+                                 _stream(stream)), "oscar_calibrate")
+    return U_K, U_V, C_Q, C_S
+
+
+def oscar_clip_errors(ctx, layer, kv_head, Q, K, V, N, ratios, scratch, stream=None):
+    """Errors of each candidate clip ratio for keys and values with the layer's
+    loaded rotation.  Returns (err_k, err_v, best_k, best_v)."""
+    import numpy as np
+
+    r = np.ascontiguousarray(ratios, dtype=np.float32)
+    M = len(r)
+    ek = np.zeros(M, dtype=np.float64)
+    ev = np.zeros(M, dtype=np.float64)
+    bk, bv = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().oscar_clip_errors(ctx, layer, kv_head, _ptr(Q), _ptr(K), _ptr(V), N, _np_ptr(r), M, _np_ptr(ek),
+                                   _np_ptr(ev), ctypes.byref(bk), ctypes.byref(bv), _ptr(scratch),
+                                   scratch.numel() * scratch.element_size(), _stream(stream)), "oscar_clip_errors")
+    return ek, ev, bk.value, bv.value
 
 
 def oscar_prefill(ctx, layer, cache: dict, q, k, v, T, out, lse, scratch, batch, stream=None):

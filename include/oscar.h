@@ -296,6 +296,50 @@ oscar_status oscar_prefill(oscar_ctx* ctx, int layer, const oscar_cache* cache, 
                            void* scratch, size_t scratch_bytes, int batch,
                            oscar_stream_t stream);
 
+/* Offline calibration on the GPU for one (layer, kv head) [News, "OSCAR 的不同之处":
+ * keys are rotated into the eigenbasis of the query covariance
+ * C_Q = (1/N) Σ qᵀq, values into that of C_S = (1/N) VᵀSᵀSV with S the
+ * attention scores; Blog, "OSCAR把旋转对准attention": fixed offline per layer
+ * and head].  From N calibration tokens:
+ *   C_Q = (1/(G N)) Σ_h Σ_n q_{h,n}ᵀ q_{h,n}   (the G query heads of the kv head pooled)
+ *   C_S = (1/(G N)) Σ_h (S_h V)ᵀ (S_h V),  S_h = causal softmax(Q_h Kᵀ / √d)
+ * and their eigenvectors (cuSOLVER dsyevd in fp64; the library opens cuSOLVER
+ * at the first call and returns OSCAR_ERR_UNSUPPORTED if it cannot).
+ *   Q : device bf16 [G][N][128], G = num_q_heads / num_kv_heads
+ *   K, V : device bf16 [N][128]
+ *   U_K, U_V : host float [128][128] out, row-major, column i = eigenvector of
+ *              the i-th largest eigenvalue of C_Q (C_S), signed so that its
+ *              largest-magnitude entry (lowest index on ties) is positive: the
+ *              U_K / U_V that oscar_set_rotation takes
+ *   C_Q, C_S : host double [128][128] out, or NULL
+ *   scratch : device, at least oscar_calibration_scratch_bytes(G, N, 0) bytes,
+ *             256-byte aligned.
+ * Synchronises `stream`.  Allocates cuSOLVER's workspace (this call is
+ * offline; the decode path allocates nothing). */
+size_t oscar_calibration_scratch_bytes(int G, int N, int M);
+oscar_status oscar_calibrate(oscar_ctx* ctx, const void* Q, const void* K, const void* V, int N,
+                             float* U_K, float* U_V, double* C_Q, double* C_S, void* scratch,
+                             size_t scratch_bytes, oscar_stream_t stream);
+
+/* Clip search for one (layer, kv head) with the rotation loaded by
+ * oscar_set_rotation [Blog, "OSCAR把旋转对准attention": clipping thresholds are
+ * fixed offline].  For each candidate ratio c_m the calibration keys and values
+ * are rotated (x' = x·R, fp32) and quantised and dequantised by the
+ * demotion's quantiser at ratio c_m, and the error left in what attention
+ * computes is measured (the library's reading; the pages name no objective):
+ *   err_k[m] = ||Q' K'ᵀ - Q' K̂'ᵀ||²_F, Q' = Q·R_K over the G heads' queries
+ *              (computed as Σ_n e_n (Q'ᵀQ') e_nᵀ, e_n = k'_n - k̂'_n)
+ *   err_v[m] = Σ_h ||S_h (V' - V̂')||²_F, S_h the causal scores of head h
+ * best_k, best_v = the index of the smallest error (first on ties).
+ *   Q, K, V as in oscar_calibrate; ratios : host float [M] in (0, 1], M >= 1;
+ *   err_k, err_v : host double [M] out; best_k, best_v : host int out (or NULL);
+ *   scratch : at least oscar_calibration_scratch_bytes(G, N, M) bytes.
+ * Synchronises `stream`. */
+oscar_status oscar_clip_errors(oscar_ctx* ctx, int layer, int kv_head, const void* Q, const void* K,
+                               const void* V, int N, const float* ratios, int M, double* err_k,
+                               double* err_v, int* best_k, int* best_v, void* scratch,
+                               size_t scratch_bytes, oscar_stream_t stream);
+
 /* Decode without any device allocation (the pages have no counterpart: this
  * is a deployment convenience of this library).  Same computation, arguments
  * and results as oscar_decode, but the working memory comes from a buffer of

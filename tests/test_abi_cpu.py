@@ -22,7 +22,7 @@ def lib():
 def header_functions():
     with open(os.path.join(ROOT, "include", "oscar.h")) as f:
         text = f.read()
-    return sorted(set(re.findall(r"^\s*(?:oscar_status|int|const char\*)\s+(oscar_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:oscar_status|int|size_t|const char\*)\s+(oscar_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_boundary():
