@@ -275,6 +275,23 @@ def oracle_prefill_sample(cache_host, wl, U, q, k, v, tokens=(0, 63)):
     return Hkv * (t1 - t0) + Hkv * T * (t2 - t1) / len(tokens)
 
 
+def oracle_calibration_sample(cal_set, ratios, n_heads):
+    """The oracle's calibration (covariances + eigenbases) of one kv head and its
+    clip search for one ratio, scaled to every kv head and ratio of the bench."""
+    import oracle as O
+
+    Q, K, V = (t.float().cpu().numpy() for t in cal_set)
+    t0 = time.perf_counter()
+    U_K, U_V = O.calibrate(Q, K, V)
+    t1 = time.perf_counter()
+    O.key_clip_error(Q, K, O.rotation(U_K), 128, ratios[0])
+    O.value_clip_error(Q, K, V, O.rotation(U_V), 128, ratios[0])
+    t2 = time.perf_counter()
+    return {"calibrate_ms": (t1 - t0) * 1e3 * n_heads, "clip_search_ms": (t2 - t1) * 1e3 * n_heads * len(ratios),
+            "cores": blas_threads(), "kind": "oracle",
+            "sample": f"kv head 0 (calibration) and ratio 1.0 (clip search), scaled to {n_heads} kv heads and every ratio"}
+
+
 def blas_threads():
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         if os.environ.get(var):
@@ -519,6 +536,27 @@ def run_ours(args, wl):
     pf_flops = statistics.mean(prefill_flops([L // Bsz] * Bsz, T_pf, wl["Hq"]) for L in pf_lens)
     tpk, tpk_kind = tensor_peak()
     pf_attn_tf = pf_flops / (pf_prof["prefill_attn"] * 1e-6) / 1e12
+    # ---- offline calibration on the GPU: bases of every kv head, then the clip search
+    from bit_kv_cache_int2_gb300 import synth
+
+    G_cal, N_cal = wl["Hq"] // Hkv, 2048
+    ratios = [1.0, 0.975, 0.95, 0.925, 0.9, 0.85, 0.8, 0.7]
+    cal_sets = [tuple(t.to(dev).contiguous() for t in synth.calibration_set(0, "bench", 0, h, wk["stats"][h],
+                                                                            G=G_cal, n=N_cal)) for h in range(Hkv)]
+    cscr = oscar.calibration_scratch(G_cal, N_cal, len(ratios), dev)
+    oscar.oscar_calibrate(ctx, *cal_sets[0], N_cal, cscr)  # warm-up (opens cuSOLVER)
+    oscar.oscar_clip_errors(ctx, 0, 0, *cal_sets[0], N_cal, ratios, cscr)
+    t0 = time.perf_counter()
+    for h in range(Hkv):
+        oscar.oscar_calibrate(ctx, *cal_sets[h], N_cal, cscr)
+    t1 = time.perf_counter()
+    for h in range(Hkv):
+        oscar.oscar_clip_errors(ctx, 0, h, *cal_sets[h], N_cal, ratios, cscr)
+    t2 = time.perf_counter()
+    causal_pairs = N_cal * (N_cal + 1) / 2
+    cal_flops = Hkv * (2 * 2 * G_cal * N_cal * 128 * 128 + G_cal * causal_pairs * 128 * 4)
+    clip_flops = Hkv * (2 * G_cal * N_cal * 128 * 128 + len(ratios) * (2 * N_cal * 128 * 128 + G_cal * causal_pairs * 128 * 4))
+    fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12  # FMA lanes x 2 FLOP x max SM clock
     # ---- end to end through the public API with host buffers
     q_h = q.cpu().pin_memory()
     out_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
@@ -546,6 +584,7 @@ def run_ours(args, wl):
     # ---- CPU oracle on the GPU's own cache (bounded sample)
     cpu = None
     prefill_cpu = None
+    calib_cpu = None
     if rank == 0:
         c0 = wk["copies"][0]
         L = int(c0["seq_lens"][0])
@@ -564,6 +603,7 @@ def run_ours(args, wl):
                                      v_pf[0].float().cpu().numpy().astype(np.float64))
         prefill_cpu = {"value": psec * 1e6, "unit": "us/call", "cores": blas_threads(), "kind": "oracle",
                        "sample": f"KV head 0, chunk tokens 0 and 63; scaled to {T_pf} tokens x {Hkv} KV heads"}
+        calib_cpu = oracle_calibration_sample(cal_sets[0], ratios, Hkv)
     n_launch = 3 * K  # append + q rotation, decode, merge per step
     value = ms_per_step * 1e3 / world
     line = {
@@ -588,6 +628,12 @@ def run_ours(args, wl):
                     "note": "64 new tokens per request attending to the same 100K cache; tcgen05.mma "
                             "kind::f16 (M=128) with Q, S, P, O in tensor memory; bound: tensor; peak = "
                             "dense bf16 burst (fp16 runs at the same rate)"},
+        "calibration": {"kv_heads": Hkv, "tokens": N_cal, "query_heads_per_kv": G_cal, "ratios": len(ratios),
+                        "calibrate_ms": (t1 - t0) * 1e3, "clip_search_ms": (t2 - t1) * 1e3,
+                        "tflops": (cal_flops + clip_flops) / (t2 - t0) / 1e12, "bound": "alu",
+                        "peak_tflops": fp32_peak, "frac": (cal_flops + clip_flops) / (t2 - t0) / 1e12 / fp32_peak,
+                        "cpu_baseline": calib_cpu,
+                        "note": "offline; fp32 CUDA-core kernels + cuSOLVER dsyevd; wall time of the synchronous calls"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(), "kernel": "decode_main",
                      "bytes_per_launch": bytes_main, "peak_kind": peak_kind},

@@ -293,41 +293,59 @@ cudaError_t calib_covariances(const __nv_bfloat16* Q, const __nv_bfloat16* K, co
   return cudaGetLastError();
 }
 
+// The cuSOLVER handle and the device buffers of the 128x128 problem are made
+// once per process and reused (calibration runs on one device at a time).
+struct EighState {
+  cusolverDnHandle_t hd = nullptr;
+  double *A = nullptr, *W = nullptr, *work = nullptr;
+  int* info = nullptr;
+  int lwork = 0;
+};
+
 oscar_status calib_eigh(const double* dC, double* evec_host, cudaStream_t st, int* cuda_err) {
   Solver& s = solver();
   if (!s.ok) return OSCAR_ERR_UNSUPPORTED;
-  cusolverDnHandle_t hd = nullptr;
-  if (s.create(&hd) != CUSOLVER_STATUS_SUCCESS) return OSCAR_ERR_CUDA;
+  static EighState es;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  cudaError_t e = cudaSuccess;
+  if (!es.hd) {
+    if (s.create(&es.hd) != CUSOLVER_STATUS_SUCCESS) {
+      es.hd = nullptr;
+      return OSCAR_ERR_CUDA;
+    }
+    e = cudaMalloc((void**)&es.A, D * D * sizeof(double));
+    if (e == cudaSuccess) e = cudaMalloc((void**)&es.W, D * sizeof(double));
+    if (e == cudaSuccess) e = cudaMalloc((void**)&es.info, sizeof(int));
+    if (e == cudaSuccess &&
+        s.bufsize(es.hd, CUSOLVER_EIG_MODE_VECTOR, CUBLAS_FILL_MODE_LOWER, D, es.A, D, es.W, &es.lwork) !=
+            CUSOLVER_STATUS_SUCCESS) {
+      *cuda_err = 0;
+      return OSCAR_ERR_CUDA;
+    }
+    if (e == cudaSuccess) e = cudaMalloc((void**)&es.work, (size_t)(es.lwork > 0 ? es.lwork : 1) * sizeof(double));
+    if (e != cudaSuccess) {
+      *cuda_err = (int)e;
+      return OSCAR_ERR_CUDA;
+    }
+  }
+  int hinfo = 0;
   oscar_status status = OSCAR_OK;
-  double *A = nullptr, *W = nullptr, *work = nullptr;
-  int* info = nullptr;
-  int lwork = 0, hinfo = 0;
-  cudaError_t e = cudaMalloc((void**)&A, D * D * sizeof(double));
-  if (e == cudaSuccess) e = cudaMalloc((void**)&W, D * sizeof(double));
-  if (e == cudaSuccess) e = cudaMalloc((void**)&info, sizeof(int));
-  if (e == cudaSuccess) e = cudaMemcpyAsync(A, dC, D * D * sizeof(double), cudaMemcpyDeviceToDevice, st);
-  if (e == cudaSuccess && s.set_stream(hd, st) != CUSOLVER_STATUS_SUCCESS) status = OSCAR_ERR_CUDA;
+  e = cudaMemcpyAsync(es.A, dC, D * D * sizeof(double), cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && s.set_stream(es.hd, st) != CUSOLVER_STATUS_SUCCESS) status = OSCAR_ERR_CUDA;
   if (e == cudaSuccess && status == OSCAR_OK &&
-      s.bufsize(hd, CUSOLVER_EIG_MODE_VECTOR, CUBLAS_FILL_MODE_LOWER, D, A, D, W, &lwork) != CUSOLVER_STATUS_SUCCESS)
+      s.syevd(es.hd, CUSOLVER_EIG_MODE_VECTOR, CUBLAS_FILL_MODE_LOWER, D, es.A, D, es.W, es.work, es.lwork,
+              es.info) != CUSOLVER_STATUS_SUCCESS)
     status = OSCAR_ERR_CUDA;
-  if (e == cudaSuccess && status == OSCAR_OK) e = cudaMalloc((void**)&work, (size_t)(lwork > 0 ? lwork : 1) * sizeof(double));
-  if (e == cudaSuccess && status == OSCAR_OK &&
-      s.syevd(hd, CUSOLVER_EIG_MODE_VECTOR, CUBLAS_FILL_MODE_LOWER, D, A, D, W, work, lwork, info) !=
-          CUSOLVER_STATUS_SUCCESS)
-    status = OSCAR_ERR_CUDA;
-  if (e == cudaSuccess && status == OSCAR_OK) e = cudaMemcpyAsync(evec_host, A, D * D * sizeof(double), cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess && status == OSCAR_OK) e = cudaMemcpyAsync(&hinfo, info, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && status == OSCAR_OK)
+    e = cudaMemcpyAsync(evec_host, es.A, D * D * sizeof(double), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && status == OSCAR_OK) e = cudaMemcpyAsync(&hinfo, es.info, sizeof(int), cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  if (e == cudaSuccess && status == OSCAR_OK && hinfo != 0) status = OSCAR_ERR_STATE;
-  cudaFree(A);
-  cudaFree(W);
-  cudaFree(work);
-  cudaFree(info);
-  s.destroy(hd);
   if (e != cudaSuccess) {
     *cuda_err = (int)e;
     return OSCAR_ERR_CUDA;
   }
+  if (status == OSCAR_OK && hinfo != 0) status = OSCAR_ERR_STATE;
   return status;
 }
 

@@ -610,7 +610,7 @@ cudaError_t calib_covariances(const __nv_bfloat16* Q, const __nv_bfloat16* K, co
 // Eigenvectors of the symmetric fp64 device matrix dC (column i of the
 // column-major result = eigenvector of the i-th smallest eigenvalue), copied to
 // host memory; synchronises st.  OSCAR_ERR_UNSUPPORTED when cuSOLVER is absent.
-oscar_status calib_eigh(const double* dC, double* evec_host, cudaStream_t st, int* cuda_err);
+oscar_status calib_eigh(const double* dC, double* evec_host, cudaStream_t st, int* cuda_err);  // process-wide solver state
 // Key and value clip errors of M candidate ratios into scratch (fp64 [2][M] at off_err).
 cudaError_t calib_clip_errors(const float* R_K, const float* R_V, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                               const __nv_bfloat16* V, int G, int N, int g, const float* clips_host, int M,
