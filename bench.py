@@ -80,6 +80,25 @@ def prefill_flops(lengths, T, Hq):
     return sum(Hq * 4 * 128 * (L + t + 1) for L in lengths for t in range(T))
 
 
+# --------------------------------------------------------------- multi-rank
+def rank_env():
+    """(world size, rank, local rank) from the launcher's environment (1, 0, 0 alone)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time: every rank gets the maximum (one all-reduce, then
+    a barrier).  dist None means one process."""
+    import torch
+
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.barrier()
+    return float(t.item())
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
@@ -382,9 +401,7 @@ def run_ours(args, wl):
     from bit_kv_cache_int2_gb300 import build as B
     from bit_kv_cache_int2_gb300 import oscar
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -444,11 +461,7 @@ def run_ours(args, wl):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    t_ms = torch.tensor([ms], device=dev)
-    if dist:
-        dist.all_reduce(t_ms, op=dist.ReduceOp.MAX)
-        dist.barrier()
-    ms = float(t_ms.item())
+    ms = max_over_ranks(ms, dist, dev)
     ms_per_step = ms / K
     err = oscar.oscar_get_error(ctx)
     assert err == 0, f"device error {err}"
