@@ -587,8 +587,10 @@ oscar_status oscar_prefill(oscar_ctx* ctx, int layer, const oscar_cache* cache, 
   const cudaError_t oe = prefill_ctas_per_sm(&occ, ctx->prefill_impl);
   if (oe != cudaSuccess) return cuda_status(oe);
   if (occ < 1) occ = 1;
-  // history splits: history + window CTAs fill one wave over the SMs, within the scratch bound
-  int ns = (ctx->num_sms * occ) / tiles - 1;
+  // history splits: the history CTAs fill one wave over the SMs; the light
+  // window CTAs (blockIdx.y = NS, launched after every history CTA) take the
+  // SMs left over and whatever frees up first, within the scratch bound
+  int ns = (ctx->num_sms * occ) / tiles;
   const int cap = prefill_max_splits(batch, Hkv, G, T);
   a.NS = ns < 1 ? 1 : ns > cap ? cap : ns;
   const PrefillScratch L = prefill_scratch_layout(batch, Hkv, G, T, a.NS);
