@@ -294,8 +294,10 @@ cudaError_t calib_covariances(const __nv_bfloat16* Q, const __nv_bfloat16* K, co
 }
 
 // The cuSOLVER handle and the device buffers of the 128x128 problem are made
-// once per process and reused (calibration runs on one device at a time).
+// once and reused while the calls stay on the same device; a call on another
+// device makes them again there (the old ones are released).
 struct EighState {
+  int device = -1;
   cusolverDnHandle_t hd = nullptr;
   double *A = nullptr, *W = nullptr, *work = nullptr;
   int* info = nullptr;
@@ -309,25 +311,46 @@ oscar_status calib_eigh(const double* dC, double* evec_host, cudaStream_t st, in
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   cudaError_t e = cudaSuccess;
-  if (!es.hd) {
-    if (s.create(&es.hd) != CUSOLVER_STATUS_SUCCESS) {
-      es.hd = nullptr;
-      return OSCAR_ERR_CUDA;
-    }
-    e = cudaMalloc((void**)&es.A, D * D * sizeof(double));
-    if (e == cudaSuccess) e = cudaMalloc((void**)&es.W, D * sizeof(double));
-    if (e == cudaSuccess) e = cudaMalloc((void**)&es.info, sizeof(int));
-    if (e == cudaSuccess &&
-        s.bufsize(es.hd, CUSOLVER_EIG_MODE_VECTOR, CUBLAS_FILL_MODE_LOWER, D, es.A, D, es.W, &es.lwork) !=
-            CUSOLVER_STATUS_SUCCESS) {
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) {
+    *cuda_err = (int)e;
+    return OSCAR_ERR_CUDA;
+  }
+  auto release = [&](EighState& x) {  // on the device that owns x
+    if (!x.hd && !x.A && !x.W && !x.work && !x.info) return;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    if (x.device >= 0) cudaSetDevice(x.device);
+    if (x.hd) s.destroy(x.hd);
+    cudaFree(x.A);
+    cudaFree(x.W);
+    cudaFree(x.work);
+    cudaFree(x.info);
+    cudaSetDevice(cur);
+    x = EighState();
+  };
+  if (es.hd && es.device != dev) release(es);
+  if (!es.hd) {  // build the state whole, or leave none
+    EighState n;
+    n.device = dev;
+    if (s.create(&n.hd) != CUSOLVER_STATUS_SUCCESS) {
       *cuda_err = 0;
       return OSCAR_ERR_CUDA;
     }
-    if (e == cudaSuccess) e = cudaMalloc((void**)&es.work, (size_t)(es.lwork > 0 ? es.lwork : 1) * sizeof(double));
-    if (e != cudaSuccess) {
+    e = cudaMalloc((void**)&n.A, D * D * sizeof(double));
+    if (e == cudaSuccess) e = cudaMalloc((void**)&n.W, D * sizeof(double));
+    if (e == cudaSuccess) e = cudaMalloc((void**)&n.info, sizeof(int));
+    bool ok = e == cudaSuccess &&
+              s.bufsize(n.hd, CUSOLVER_EIG_MODE_VECTOR, CUBLAS_FILL_MODE_LOWER, D, n.A, D, n.W, &n.lwork) ==
+                  CUSOLVER_STATUS_SUCCESS;
+    if (ok) e = cudaMalloc((void**)&n.work, (size_t)(n.lwork > 0 ? n.lwork : 1) * sizeof(double));
+    ok = ok && e == cudaSuccess;
+    if (!ok) {
+      release(n);
       *cuda_err = (int)e;
       return OSCAR_ERR_CUDA;
     }
+    es = n;
   }
   int hinfo = 0;
   oscar_status status = OSCAR_OK;
