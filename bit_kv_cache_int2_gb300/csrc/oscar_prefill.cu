@@ -322,14 +322,14 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(PrefillArgs a) {
     const int r = r0 + 8 * h + j;
     const float nj = nrm[8 * h + j];
     // |q'_c| and |q_c| are both at most |q| (R_K is orthogonal): 2^-sigma
-    // brings them below 2^14 in fp16
-    int ex = 0;
-    frexpf(nj, &ex);
+    // brings them below 2^14 in fp16 (exact power-of-two scalings)
+    const int ex = ((__float_as_int(nj) >> 23) & 0xFF) - 126;  // nj = m·2^ex, m in [0.5, 1)
     const int sig = nj > 0.f ? ex - 14 : 0;
+    const float down = __int_as_float((127 - sig) << 23), up = __int_as_float((127 + sig) << 23);
     const size_t e = ((size_t)bk * RP + r) * D + c;
-    a.qh[e] = __float2half_rn(ldexpf(acc[j], -sig));
-    a.qh[vstride + e] = __float2half_rn(ldexpf(xh[j * D + c], -sig));
-    if (c == 0) a.alpha[(size_t)bk * RP + r] = ldexpf(1.f, sig) * LOG2E * INV_SQRT_D;
+    a.qh[e] = __float2half_rn(acc[j] * down);
+    a.qh[vstride + e] = __float2half_rn(xh[j * D + c] * down);
+    if (c == 0) a.alpha[(size_t)bk * RP + r] = up * LOG2E * INV_SQRT_D;
   }
 }
 
