@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(PrefillArgs a) {
     // |q'_c| and |q_c| are both at most |q| (R_K is orthogonal): 2^-sigma
     // brings them below 2^14 in fp16 (exact power-of-two scalings)
     const int ex = ((__float_as_int(nj) >> 23) & 0xFF) - 126;  // nj = m·2^ex, m in [0.5, 1)
-    const int sig = nj > 0.f ? ex - 14 : 0;
+    const int sig = nj > 0.f ? min(max(ex - 14, -120), 120) : 0;  // 2^±sig stay normal floats
     const float down = __int_as_float((127 - sig) << 23), up = __int_as_float((127 + sig) << 23);
     const size_t e = ((size_t)bk * RP + r) * D + c;
     a.qh[e] = __float2half_rn(acc[j] * down);
