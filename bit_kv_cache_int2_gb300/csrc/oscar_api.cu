@@ -545,6 +545,17 @@ oscar_status oscar_import_bf16_history(oscar_ctx* ctx, const oscar_cache* cache,
   return import_common(ctx, 0, cache, K, V, batch, n, stream, 1);
 }
 
+oscar_status oscar_append_bf16_history(oscar_ctx* ctx, const oscar_cache* cache, const void* k_new,
+                                       const void* v_new, int batch, oscar_stream_t stream) {
+  if (!ctx || !cache_ok(cache, true) || !k_new || !v_new) return OSCAR_ERR_INVALID_ARG;
+  if (batch < 0 || batch > ctx->cfg.max_batch || !aligned(k_new, 16) || !aligned(v_new, 16))
+    return OSCAR_ERR_INVALID_ARG;
+  if (batch == 0) return OSCAR_OK;
+  const CacheView cv = make_view(ctx, cache, true);
+  return cuda_status(launch_append_bf16(cv, (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, batch,
+                                        (cudaStream_t)stream, &ctx->prof));
+}
+
 oscar_status oscar_decode(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* q,
                           void* out, float* lse, void* scratch, size_t scratch_bytes, int batch,
                           oscar_stream_t stream) {

@@ -624,6 +624,9 @@ cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_b
 cudaError_t launch_step(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* k,
                         const __nv_bfloat16* v, int B, int* req_counter, const DecodeArgs& a,
                         cudaStream_t st, Profiler* prof);
+// One token per request into a BF16-history cache (cv over the BF16 pool).
+cudaError_t launch_append_bf16(const CacheView& cv, const __nv_bfloat16* k, const __nv_bfloat16* v, int B,
+                               cudaStream_t st, Profiler* prof);
 cudaError_t launch_import(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* K,
                           const __nv_bfloat16* V, int B, int n, int bf16_history,
                           cudaStream_t st, Profiler* prof);

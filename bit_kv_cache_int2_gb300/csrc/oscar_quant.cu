@@ -332,6 +332,46 @@ __global__ void __launch_bounds__(256) import_bf16_pages_kernel(CacheView cv,
   }
 }
 
+// One token per request appended to a BF16-history cache (the baseline's
+// layout: history pages of unrotated bf16 K and V rows, no quantisation).  As
+// in the INT2 append, a full recent window first moves its oldest token (ring
+// slot hist % 256) into history slot hist; then the new token takes sink slot
+// L (L < 64) or ring slot (L - 64) % 256.  One CTA of 256 threads per request,
+// 16-byte copies; a missing history page leaves the request unchanged.
+__global__ void __launch_bounds__(256) append_bf16_kernel(CacheView cv, const __nv_bfloat16* __restrict__ k,
+                                                          const __nv_bfloat16* __restrict__ v) {
+  const int b = blockIdx.x, Hkv = cv.Hkv;
+  const int L = cv.seq_lens[b], H = cv.hist_lens[b];
+  const int recent = L > SINK ? L - SINK - H : 0;
+  const bool demote = recent >= RECENT;
+  const int rows = Hkv * 2 * (D * 2 / 16);  // uint4 copies per token: every kv head, K and V
+  if (demote) {
+    uint8_t* page = lookup_page(cv, b, H / PAGE, threadIdx.x == 0);
+    if (!page) return;  // uniform: every thread sees the same table entry
+    const int slot = H % RECENT, row = H % PAGE;
+    for (int i = threadIdx.x; i < rows; i += blockDim.x) {
+      const int h = i / 32, isv = (i / 16) & 1, c = i % 16;
+      const size_t src = ((size_t)(b * Hkv + h) * RECENT + slot) * D;
+      const uint4* from = (const uint4*)((isv ? cv.ring_v : cv.ring_k) + src) + c;
+      uint4* to = (uint4*)(page + (size_t)h * BF16_HEAD_BYTES + (size_t)isv * PAGE * D * 2 + (size_t)row * D * 2) + c;
+      *to = *from;
+    }
+  }
+  __syncthreads();  // the demoted slot is the one the new token takes when the window is full
+  const bool in_sink = L < SINK;
+  for (int i = threadIdx.x; i < rows; i += blockDim.x) {
+    const int h = i / 32, isv = (i / 16) & 1, c = i % 16;
+    const size_t head = (size_t)b * Hkv + h;
+    const size_t dst = in_sink ? (head * SINK + L) * D : (head * RECENT + (L - SINK) % RECENT) * D;
+    uint4* to = (uint4*)((isv ? (in_sink ? cv.sink_v : cv.ring_v) : (in_sink ? cv.sink_k : cv.ring_k)) + dst) + c;
+    *to = *((const uint4*)((isv ? v : k) + head * D) + c);
+  }
+  if (threadIdx.x == 0) {
+    cv.seq_lens[b] = L + 1;
+    if (demote) cv.hist_lens[b] = H + 1;
+  }
+}
+
 __global__ void import_set_lengths_kernel(int32_t* seq, int32_t* hist, int B, int n) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
@@ -403,6 +443,14 @@ cudaError_t launch_step(const CacheView& cv, const LayerRot& rot, const __nv_bfl
       launch_pdl(step_kernel, dim3(B * cv.Hkv, 3), dim3(512), 0, st, cv, rot, k, v, req_counter, a);
   prof_end(prof, OSCAR_KERNEL_STEP, st);
   return e;
+}
+
+cudaError_t launch_append_bf16(const CacheView& cv, const __nv_bfloat16* k, const __nv_bfloat16* v, int B,
+                               cudaStream_t st, Profiler* prof) {
+  prof_begin(prof, OSCAR_KERNEL_APPEND, st);
+  append_bf16_kernel<<<B, 256, 0, st>>>(cv, k, v);
+  prof_end(prof, OSCAR_KERNEL_APPEND, st);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_import(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* K,

@@ -110,6 +110,8 @@ _SIGS = {
     "oscar_prefill": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(oscar_cache), ctypes.c_void_p, ctypes.c_void_p,
                        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                        ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
+    "oscar_append_bf16_history": ([ctypes.c_void_p, ctypes.POINTER(oscar_cache), ctypes.c_void_p, ctypes.c_void_p,
+                                   ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
     "oscar_calibration_scratch_bytes": ([ctypes.c_int, ctypes.c_int, ctypes.c_int], ctypes.c_size_t),
     "oscar_calibrate": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -258,6 +260,12 @@ def oscar_decode(ctx, layer, cache: dict, q, out, lse, scratch, batch, stream=No
     _check(lib().oscar_decode(ctx, layer, ctypes.byref(cs), _ptr(q), _ptr(out), _ptr(lse), _ptr(scratch),
                               scratch.numel() * scratch.element_size(), batch, _stream(stream)),
            "oscar_decode")
+
+
+def oscar_append_bf16_history(ctx, cache: dict, k_new, v_new, batch, stream=None):
+    cs = _cache_struct(cache)
+    _check(lib().oscar_append_bf16_history(ctx, ctypes.byref(cs), _ptr(k_new), _ptr(v_new), batch, _stream(stream)),
+           "oscar_append_bf16_history")
 
 
 def calibration_scratch(G, N, M=0, device="cuda"):

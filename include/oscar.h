@@ -384,6 +384,18 @@ oscar_status oscar_import_bf16_history(oscar_ctx* ctx, const oscar_cache* cache,
                                        const void* K, const void* V, int batch,
                                        int n, oscar_stream_t stream);
 
+/* One token per request appended to a BF16-history cache (cache->pool a BF16
+ * pool; the baseline's counterpart of oscar_append, no rotation and no
+ * quantisation): if the recent window holds 256 tokens, its oldest token
+ * (ring slot hist_lens[b] % 256) is first copied into history slot
+ * hist_lens[b] (hist_lens[b] += 1); then the new token is written to sink[L]
+ * (L < 64) or ring slot (L - 64) % 256, and seq_lens[b] += 1.
+ *   k_new, v_new : device bf16 [batch][num_kv_heads][128].
+ * Device errors: OSCAR_ERR_NO_PAGE / OSCAR_ERR_RANGE for a missing or bad
+ * history page; the request is then left unchanged. */
+oscar_status oscar_append_bf16_history(oscar_ctx* ctx, const oscar_cache* cache, const void* k_new,
+                                       const void* v_new, int batch, oscar_stream_t stream);
+
 /* Test hook: the demotion's quantiser and packer on given rotated fp32
  * vectors, so that codes and bytes can be compared bit for bit.
  *   x : device float [n][128] rotated channels
