@@ -311,6 +311,70 @@ def oracle_calibration_sample(cal_set, ratios, n_heads):
             "sample": f"kv head 0 (calibration) and ratio 1.0 (clip search), scaled to {n_heads} kv heads and every ratio"}
 
 
+def serving_measurement(wl, dev, n_req=48, gen=64, lo=8192, hi=24576, budget_requests=4, seed=0):
+    """The same request list run by the synthetic serving loop under one KV
+    memory budget, with INT2 history and with BF16 history.  The budget is what
+    `budget_requests` average requests need in BF16 (history pages plus their
+    BF16 sink/recent windows); each format gets as many batch slots and pages
+    as fit in it.  Returns the bench's `serving` object."""
+    import numpy as np
+    import torch
+
+    from bit_kv_cache_int2_gb300 import oscar, serving, synth
+
+    Hq, Hkv, g = wl["Hq"], wl["Hkv"], wl["g"]
+    G = Hq // Hkv
+    rng = np.random.default_rng(seed)
+    lengths = [int(x) for x in rng.integers(lo, hi + 1, n_req)]
+    stats = [synth.head_stats(seed, "serve", 0, h, n_out=wl["n_out"], f_key=wl["f_key"]) for h in range(Hkv)]
+    streams = {}
+    for i, L in enumerate(lengths):
+        n = L + gen
+        K = torch.stack([synth.draw_keys(stats[h], n, synth.stream_seed(seed, "sK", i, h), dev) for h in range(Hkv)])
+        V = torch.stack([synth.draw_values(stats[h], n, synth.stream_seed(seed, "sV", i, h), dev) for h in range(Hkv)])
+        Q = torch.stack([synth.draw_queries(stats[h], gen * G, synth.stream_seed(seed, "sQ", i, h), dev).view(gen, G, 128)
+                         for h in range(Hkv)], dim=1).reshape(gen, Hq, 128)
+        streams[i] = (K.contiguous(), V.contiguous(), Q.contiguous())
+    window_bytes = Hkv * 320 * 128 * 2 * 2  # sink + recent K and V per slot
+    page_bytes = {"int2": Hkv * (4096 + 64 * (128 // g) * 8), "bf16": Hkv * 64 * 128 * 2 * 2}
+    mean_pages = float(np.mean([serving.pages_needed(L, gen) for L in lengths]))
+    budget = budget_requests * (mean_pages * page_bytes["bf16"] + window_bytes)
+    mpr = max(serving.pages_needed(L, gen) for L in lengths)
+    res = {}
+    for fmt in ("int2", "bf16"):
+        per_req = mean_pages * page_bytes[fmt] + window_bytes
+        slots = int(max(1, min(64, budget // per_req)))
+        pool_pages = int((budget - slots * window_bytes) // page_bytes[fmt])
+        cfg = oscar.make_config(1, Hq, Hkv, g, max_batch=slots, max_pages_per_req=mpr, num_pages=pool_pages)
+        ctx = oscar.oscar_create(cfg)
+        eye = np.stack([np.eye(128, dtype=np.float32)] * Hkv)
+        oscar.oscar_set_rotation(ctx, 0, eye, eye, [wl["clip"]] * Hkv, [wl["clip"]] * Hkv,
+                                 oscar.ROT_HADAMARD if fmt == "int2" else oscar.ROT_NONE)
+        cache = oscar.alloc_cache(cfg, dev, bf16_history=(fmt == "bf16"))
+        batches = []
+        backend = serving.DeviceBackend(fmt, ctx, cfg, cache, lambda r: streams[r.rid],
+                                        on_step=lambda active, q, out: batches.append(len(active)), time_steps=True)
+        reqs = [serving.Request(rid=i, prefix=L, gen=gen) for i, L in enumerate(lengths)]
+        done, steps, sec = serving.run_job(backend, pool_pages, slots, mpr, reqs)
+        assert oscar.oscar_get_error(ctx) == 0 and len(done) == n_req
+        dsec = serving.step_seconds(backend)
+        res[fmt] = {"slots": slots, "pool_pages": pool_pages, "steps": steps, "seconds": sec,
+                    "tokens_per_s": n_req * gen / sec, "decode_seconds": dsec,
+                    "decode_tokens_per_s": n_req * gen / dsec, "mean_batch": float(np.mean(batches)),
+                    "max_batch": int(max(batches))}
+        oscar.oscar_destroy(ctx)
+        del cache, backend
+    torch.cuda.empty_cache()
+    return {"requests": n_req, "generated_per_request": gen, "prefix_tokens": [lo, hi],
+            "budget_mb": budget / 1e6, **res,
+            "throughput_ratio": res["int2"]["tokens_per_s"] / res["bf16"]["tokens_per_s"],
+            "decode_throughput_ratio": res["int2"]["decode_tokens_per_s"] / res["bf16"]["decode_tokens_per_s"],
+            "note": "synthetic, one Qwen3-8B-shaped layer; each request imports its prefix (standing in for a "
+                    "prefix-cache hit) and decodes with append + attention per step. tokens_per_s: wall time of the "
+                    "whole job (imports, host scheduler in Python, steps); decode_tokens_per_s: device time of the "
+                    "decode steps only (CUDA events around each step)"}
+
+
 def blas_threads():
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         if os.environ.get(var):
@@ -585,6 +649,8 @@ def run_ours(args, wl):
     cal_flops = Hkv * (2 * 2 * G_cal * N_cal * 128 * 128 + G_cal * causal_pairs * 128 * 4)
     clip_flops = Hkv * (2 * G_cal * N_cal * 128 * 128 + len(ratios) * (2 * N_cal * 128 * 128 + G_cal * causal_pairs * 128 * 4))
     fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12  # FMA lanes x 2 FLOP x max SM clock
+    # ---- synthetic serving loop under one KV memory budget, INT2 vs BF16 history
+    serve = serving_measurement(wl, dev)
     # ---- end to end through the public API with host buffers: each step's q,
     # k_new and v_new sit in one pinned host record, copied with one transfer
     nq, nk = q.numel(), kv_new[0][0].numel()
@@ -658,6 +724,7 @@ def run_ours(args, wl):
                     "note": "64 new tokens per request attending to the same 100K cache; tcgen05.mma "
                             "kind::f16 (M=128) with Q, S, P, O in tensor memory; bound: tensor; peak = "
                             "dense bf16 burst (fp16 runs at the same rate)"},
+        "serving": serve,
         "calibration": {"kv_heads": Hkv, "tokens": N_cal, "query_heads_per_kv": G_cal, "ratios": len(ratios),
                         "calibrate_ms": (t1 - t0) * 1e3, "clip_search_ms": (t2 - t1) * 1e3,
                         "tflops": (cal_flops + clip_flops) / (t2 - t0) / 1e12, "bound": "alu",

@@ -141,7 +141,7 @@ class DeviceBackend:
     [Hkv][prefix + gen][128] and Q bf16 [gen][Hq][128] device tensors, drawn at
     admission and dropped at retirement.  fmt is "int2" or "bf16"."""
 
-    def __init__(self, fmt, ctx, cfg, cache, draw, on_step=None):
+    def __init__(self, fmt, ctx, cfg, cache, draw, on_step=None, time_steps=False):
         import torch
 
         self.fmt, self.ctx, self.cfg, self.cache = fmt, ctx, cfg, cache
@@ -154,6 +154,7 @@ class DeviceBackend:
         self.out = torch.empty_like(self.q)
         self.scratch = oscar.alloc_scratch(cfg, dev)
         self.streams = {}
+        self.step_events = [] if time_steps else None
 
     def _view(self, slot):
         v = dict(self.cache)
@@ -193,16 +194,28 @@ class DeviceBackend:
         torch.stack([s[0][:, r.prefix + r.done] for s, r in zip(st, active)], out=self.k[:n])
         torch.stack([s[1][:, r.prefix + r.done] for s, r in zip(st, active)], out=self.v[:n])
         torch.stack([s[2][r.done] for s, r in zip(st, active)], out=self.q[:n])
+        if self.step_events is not None:
+            ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            ev[0].record()
         if self.fmt == "int2":
             oscar.oscar_decode_step(self.ctx, 0, self.cache, self.k, self.v, self.q, self.out, None, self.scratch, n)
         else:
             oscar.oscar_append_bf16_history(self.ctx, self.cache, self.k, self.v, n)
             oscar.oscar_decode_bf16_history(self.ctx, self.cache, self.q, self.out, None, self.scratch, n)
+        if self.step_events is not None:
+            ev[1].record()
+            self.step_events.append(ev)
         if self.on_step is not None:
             self.on_step(active, self.q[:n], self.out[:n])
         for r in active:
             if r.done + 1 >= r.gen:
                 self.streams.pop(r.rid, None)
+
+
+def step_seconds(backend):
+    """Device time of the decode steps (append + attention), summed, when the
+    backend was made with time_steps=True."""
+    return sum(a.elapsed_time(b) for a, b in backend.step_events) * 1e-3
 
 
 def run_job(backend, pool_pages, max_batch, max_pages_per_req, requests):
