@@ -538,30 +538,35 @@ def logit_error_trace(Q, K, K_hat) -> float:
 # taken in the rotated basis, where they are equal to the unrotated ones
 # (R is orthogonal and Q K^T = (Q R)(K R)^T).
 
-def quantize_dequantize_rows(X, g: int, clip: float) -> np.ndarray:
-    """Each row quantised with the demotion's quantiser and dequantised, float64."""
+def quantize_dequantize_rows(X, g: int, clip: float, codebook=None) -> np.ndarray:
+    """Each row quantised with the demotion's quantiser and dequantised,
+    float64; codebook = (a, b) uses the Lloyd-Max levels instead (below)."""
     X = np.asarray(X, dtype=np.float32)
     out = np.zeros(X.shape, dtype=np.float64)
     for n in range(X.shape[0]):
-        codes, s, z = quantize_vector(X[n], g, clip)
-        out[n] = dequantize(codes, s, z, g)
+        if codebook is None:
+            codes, s, z = quantize_vector(X[n], g, clip)
+            out[n] = dequantize(codes, s, z, g)
+        else:
+            codes, s, z = quantize_vector_codebook(X[n], g, clip, *codebook)
+            out[n] = dequantize_codebook(codes, s, z, g, *codebook)
     return out
 
 
-def key_clip_error(Q, K, R_K, g: int, clip: float) -> float:
+def key_clip_error(Q, K, R_K, g: int, clip: float, codebook=None) -> float:
     """||Q' K'^T - Q' K_hat'^T||_F^2, Q' = Q R_K over the G heads' calibration
     queries (Q [G][N][d] or [rows][d]), K' = K R_K in fp32 as the demotion
     rotates, K_hat' its quantised and dequantised copy with ratio `clip`."""
     Qr = np.asarray(Q, dtype=np.float64).reshape(-1, np.shape(Q)[-1]) @ np.asarray(R_K, dtype=np.float64)
     Kr = rotate_to_f32(K, R_K)
-    return logit_error_direct(Qr, Kr.astype(np.float64), quantize_dequantize_rows(Kr, g, clip))
+    return logit_error_direct(Qr, Kr.astype(np.float64), quantize_dequantize_rows(Kr, g, clip, codebook))
 
 
-def value_clip_error(Q, K, V, R_V, g: int, clip: float) -> float:
+def value_clip_error(Q, K, V, R_V, g: int, clip: float, codebook=None) -> float:
     """sum_h ||S_h (V' - V_hat')||_F^2, S_h = causal_scores(Q_h, K) (unrotated
     scores), V' = V R_V in fp32, V_hat' quantised and dequantised with `clip`."""
     Vr = rotate_to_f32(V, R_V)
-    E = Vr.astype(np.float64) - quantize_dequantize_rows(Vr, g, clip)
+    E = Vr.astype(np.float64) - quantize_dequantize_rows(Vr, g, clip, codebook)
     Q = np.asarray(Q, dtype=np.float64)
     total = 0.0
     for h in range(Q.shape[0]):
@@ -570,8 +575,142 @@ def value_clip_error(Q, K, V, R_V, g: int, clip: float) -> float:
     return total
 
 
-def clip_search(Q, K, V, R_K, R_V, g: int, ratios):
+def clip_search(Q, K, V, R_K, R_V, g: int, ratios, codebook_k=None, codebook_v=None):
     """Errors of every candidate ratio and the argmin for keys and values."""
-    ek = [key_clip_error(Q, K, R_K, g, c) for c in ratios]
-    ev = [value_clip_error(Q, K, V, R_V, g, c) for c in ratios]
+    ek = [key_clip_error(Q, K, R_K, g, c, codebook_k) for c in ratios]
+    ev = [value_clip_error(Q, K, V, R_V, g, c, codebook_v) for c in ratios]
     return np.array(ek), np.array(ev), int(np.argmin(ek)), int(np.argmin(ev))
+
+
+# --------------------------------------------------------------------------
+# Lloyd-Max codebook  [Blog, closing paragraph on TurboQuant: the released code
+#                      already pairs the attention-aware rotation with a
+#                      Lloyd-Max codebook]
+# --------------------------------------------------------------------------
+# The pages name the codebook and nothing more.  Reading taken:
+# * the group's scale and zero point are the uniform quantiser's, and so is the
+#   normalised value t = (x - z)/s (float32); only the four values t is
+#   rounded to change;
+# * the levels are symmetric about 1.5: {1.5-b, 1.5-a, 1.5+a, 1.5+b} with
+#   0 <= a < b.  Min-max normalisation centres t on 1.5 when the rotated
+#   coordinates are symmetric about 0, which the rotation makes them;
+# * a code is the level nearest to t, ties to the even code.  With the
+#   midpoint m = (a + b)/2 that is: code = [t > 1.5-m] + [t >= 1.5] + [t > 1.5+m]
+#   (float32), which for a = 1/2, b = 3/2 is clamp(rint(t), 0, 3) exactly;
+# * fitting is Lloyd-Max -- alternate nearest-level cells and centroid levels
+#   to lower the mean squared error of t -- which for symmetric levels is a
+#   two-level problem on the folded value f = |t - 1.5|: a is the mean of f
+#   over the inner cell (f <= m), b over the outer cell (f > m).  It starts
+#   from the uniform levels and stops once the cells repeat, so the result is
+#   a fixed point: each level is the centroid of its cell.  Groups with a zero
+#   scale (all codes 0) carry no t and are left out.
+
+UNIFORM_CODEBOOK = (0.5, 1.5)
+
+
+def codebook_levels(a: float, b: float) -> np.ndarray:
+    """The four levels of t for codes 0..3, float64."""
+    return np.array([1.5 - b, 1.5 - a, 1.5 + a, 1.5 + b], dtype=np.float64)
+
+
+def codebook_thresholds(a: float, b: float):
+    """(lower, upper) float32 thresholds 1.5 -/+ m, m = (a + b)/2 in float32."""
+    m = np.float32(np.float32(np.float32(a) + np.float32(b)) * np.float32(0.5))
+    return np.float32(np.float32(1.5) - m), np.float32(np.float32(1.5) + m)
+
+
+def codes_from_t(t, a: float, b: float) -> np.ndarray:
+    """Nearest symmetric level for float32 t, ties to the even code."""
+    t = np.asarray(t, dtype=np.float32)
+    lo, hi = codebook_thresholds(a, b)
+    return ((t > lo).astype(np.uint8) + (t >= np.float32(1.5)).astype(np.uint8) + (t > hi).astype(np.uint8))
+
+
+def group_t(x, clip: float):
+    """(t, s, z) of one group: the uniform quantiser's scale, zero point and
+    float32 normalised values; t is None when the scale is zero."""
+    x = np.asarray(x, dtype=np.float32)
+    c = np.float32(clip)
+    mx_c = np.float32(c * np.float32(x.max()))
+    mn_c = np.float32(c * np.float32(x.min()))
+    s = half_rn_sat(np.float32(np.float32(mx_c - mn_c) / np.float32(3.0)))
+    z = half_rn_sat(mn_c)
+    if np.float32(s) == 0:
+        return None, s, z
+    t = (x - np.float32(z)) / np.float32(s)
+    assert t.dtype == np.float32
+    return t, s, z
+
+
+def quantize_group_codebook(x, clip: float, a: float, b: float):
+    """One group -> (codes, s, z) with the symmetric codebook (a, b)."""
+    t, s, z = group_t(x, clip)
+    if t is None:
+        return np.zeros(np.shape(x), dtype=np.uint8), s, z
+    return codes_from_t(t, a, b), s, z
+
+
+def quantize_vector_codebook(x, g: int, clip: float, a: float, b: float):
+    """A rotated d-vector -> codes [d], s [d/g], z [d/g] with the codebook."""
+    x = np.asarray(x, dtype=np.float32)
+    d = x.shape[0]
+    codes = np.zeros(d, dtype=np.uint8)
+    s = np.zeros(d // g, dtype=np.float16)
+    z = np.zeros(d // g, dtype=np.float16)
+    for gr in range(d // g):
+        c, si, zi = quantize_group_codebook(x[gr * g:(gr + 1) * g], clip, a, b)
+        codes[gr * g:(gr + 1) * g] = c
+        s[gr] = si
+        z[gr] = zi
+    return codes, s, z
+
+
+def dequantize_codebook(codes, s, z, g: int, a: float, b: float) -> np.ndarray:
+    """x_hat = level[code]*s + z per group, float64."""
+    lv = codebook_levels(float(np.float32(a)), float(np.float32(b)))[np.asarray(codes, dtype=np.int64)]
+    sg = np.repeat(np.asarray(s, dtype=np.float64), g, axis=-1)
+    zg = np.repeat(np.asarray(z, dtype=np.float64), g, axis=-1)
+    return lv * sg + zg
+
+
+def folded_values(X, g: int, clip: float) -> np.ndarray:
+    """f = |t - 1.5| (float32 subtraction) of every channel of every row of
+    rotated float32 X [n][d], groups with a zero scale left out."""
+    X = np.asarray(X, dtype=np.float32)
+    out = []
+    for n in range(X.shape[0]):
+        for gr in range(X.shape[1] // g):
+            t, _, _ = group_t(X[n, gr * g:(gr + 1) * g], clip)
+            if t is not None:
+                out.append(np.abs(t - np.float32(1.5)))
+    return np.concatenate(out) if out else np.zeros(0, dtype=np.float32)
+
+
+def lloyd_max_folded(f, max_iters: int = 100):
+    """Two-level Lloyd-Max on folded values f >= 0, float64.
+
+    Returns (a, b, updates): the inner and outer levels and how many centroid
+    updates ran before the cells repeated (or max_iters)."""
+    f = np.asarray(f, dtype=np.float64)
+    a, b = UNIFORM_CODEBOOK
+    prev = -1
+    updates = 0
+    for _ in range(max_iters):
+        m = (a + b) / 2.0
+        inner = f <= m
+        n_in = int(np.count_nonzero(inner))
+        if n_in == prev:
+            break  # same cells as last time: a and b are their centroids
+        if n_in > 0:
+            a = float(np.sum(f[inner])) / n_in
+        if n_in < f.size:
+            b = float(np.sum(f[~inner])) / (f.size - n_in)
+        prev = n_in
+        updates += 1
+    return a, b, updates
+
+
+def fit_codebook(X_rot, g: int, clip: float, max_iters: int = 100):
+    """The codebook (a, b) of one (layer, kv head, K or V) from rotated float32
+    calibration rows, with the head's clip ratio."""
+    return lloyd_max_folded(folded_values(X_rot, g, clip), max_iters)

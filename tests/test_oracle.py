@@ -560,3 +560,150 @@ def test_clip_search_prefers_clipping_on_outlier_keys():
     ek, ev, ik, iv = O.clip_search(Q, K, V, np.eye(128), np.eye(128), 128, ratios)
     assert ek[ik] == ek.min() and ev[iv] == ev.min()
     assert ratios[ik] < 1.0
+
+
+# ------------------------------------------------------- Lloyd-Max codebook
+
+def test_uniform_codebook_reproduces_the_uniform_quantiser():
+    """a = 1/2, b = 3/2 is the uniform grid {0, 1, 2, 3}: the codebook
+    quantiser must give the rint/clamp quantiser's codes on random groups and
+    on exact ties (t = 0.5 -> 0, 1.5 -> 2, 2.5 -> 2, round half to even)."""
+    rng = np.random.default_rng(3)
+    for g in (32, 64, 128):
+        for clip in (1.0, 0.9, 0.73):
+            for _ in range(20):
+                x = (rng.standard_normal(128) * rng.uniform(0.01, 20)).astype(np.float32)
+                c0, s0, z0 = O.quantize_vector(x, g, clip)
+                c1, s1, z1 = O.quantize_vector_codebook(x, g, clip, *O.UNIFORM_CODEBOOK)
+                np.testing.assert_array_equal(c0, c1)
+                np.testing.assert_array_equal(s0, s1)
+                np.testing.assert_array_equal(z0, z1)
+    # min 0, max 3, clip 1: s = 1, z = 0, so t = x exactly
+    x = np.array([0, 3, 0.5, 1.5, 2.5, 0.49999997, 0.50000006, 2.4999998, 2.5000002, 1.4999999] + [1.0] * 22,
+                 dtype=np.float32)
+    codes, s, z = O.quantize_group_codebook(x, 1.0, 0.5, 1.5)
+    assert float(s) == 1.0 and float(z) == 0.0
+    assert list(codes[:10]) == [0, 3, 0, 2, 2, 0, 1, 2, 3, 1]
+    np.testing.assert_array_equal(codes, O.quantize_group(x, 1.0)[0])
+
+
+def test_codebook_code_is_the_nearest_level():
+    """Brute force: the threshold rule picks the level nearest to t."""
+    rng = np.random.default_rng(5)
+    for a, b in [(0.45, 1.51), (0.2, 0.9), (0.0, 1.2), (0.7, 2.4)]:
+        t = rng.uniform(-1, 4, 20000).astype(np.float32)
+        lv = O.codebook_levels(a, b)
+        dist = np.abs(t.astype(np.float64)[:, None] - lv[None, :])
+        got = O.codes_from_t(t, a, b)
+        lo, hi = O.codebook_thresholds(a, b)
+        near_tie = (np.abs(t - lo) < 1e-6) | (np.abs(t - 1.5) < 1e-6) | (np.abs(t - hi) < 1e-6)
+        # the chosen level is at the smallest distance (a = 0 makes two levels equal)
+        chosen = dist[np.arange(t.size), got]
+        assert np.array_equal(chosen[~near_tie], dist.min(axis=1)[~near_tie])
+
+
+def test_codebook_dequantizes_to_the_symmetric_levels():
+    codes = np.array([0, 1, 2, 3] * 32, dtype=np.uint8)
+    s = np.array([0.5], dtype=np.float16)
+    z = np.array([-1.0], dtype=np.float16)
+    x = O.dequantize_codebook(codes, s, z, 128, 0.25, 1.25)
+    np.testing.assert_allclose(x[:4], [0.25 * 0.5 - 1, 1.25 * 0.5 - 1, 1.75 * 0.5 - 1, 2.75 * 0.5 - 1])
+
+
+def test_lloyd_max_gaussian_matches_max_table():
+    """Folded quantiles of N(0, 1): the four-level Lloyd-Max quantiser of the
+    unit Gaussian has levels +-0.4528 and +-1.510 and threshold 0.9816 (J. Max,
+    "Quantizing for minimum distortion", 1960, table for N = 4); the same
+    fixed point also follows from the truncated-normal centroid formulas."""
+    from scipy.stats import norm
+
+    n = 200000
+    f = np.abs(norm.ppf((np.arange(n) + 0.5) / n))
+    a, b, _ = O.lloyd_max_folded(f, 500)
+    assert abs(a - 0.4528) < 2e-4 and abs(b - 1.510) < 1e-3 and abs((a + b) / 2 - 0.9816) < 1e-3
+    # continuous fixed point: a = E[|X| : |X| <= m], b = E[|X| : |X| > m]
+    m = 1.0
+    for _ in range(200):
+        ac = (norm.pdf(0) - norm.pdf(m)) / (norm.cdf(m) - 0.5)
+        bc = norm.pdf(m) / (1 - norm.cdf(m))
+        m = (ac + bc) / 2
+    assert abs(a - ac) < 1e-4 and abs(b - bc) < 1e-4
+
+
+def test_lloyd_max_uniform_closed_form():
+    """t uniform on [0, 3] (f uniform on [0, 1.5]): the optimum is the uniform
+    quantiser with cells of width 3/4, levels 3/8 and 9/8 from the centre."""
+    n = 100000
+    f = (np.arange(n) + 0.5) / n * 1.5
+    a, b, _ = O.lloyd_max_folded(f, 500)
+    assert abs(a - 0.375) < 1e-4 and abs(b - 1.125) < 1e-4
+
+
+def test_lloyd_max_tiny_brute_force():
+    """On tiny sets the result is a centroid-consistent split found by
+    enumerating every split of the sorted values, and its error is no larger
+    than the uniform start's (Lloyd iterations never raise the error)."""
+    rng = np.random.default_rng(9)
+    for trial in range(300):
+        n = int(rng.integers(1, 9))
+        f = np.sort(np.abs(rng.normal(0, 1, n)) * rng.uniform(0.2, 2))
+        a, b, _ = O.lloyd_max_folded(f, 1000)
+
+        def err(a_, b_):
+            return float(np.sum(np.minimum((f - a_) ** 2, (f - b_) ** 2)))
+
+        consistent = []
+        for k in range(0, n + 1):
+            ak = f[:k].mean() if k else None
+            bk = f[k:].mean() if k < n else None
+            if ak is None or bk is None:
+                continue
+            mk = (ak + bk) / 2
+            if f[k - 1] <= mk < f[k]:
+                consistent.append((ak, bk))
+        m = (a + b) / 2
+        if f[-1] <= m:  # every value in the inner cell: the outer level kept its start
+            assert abs(a - f.mean()) < 1e-12 and b == O.UNIFORM_CODEBOOK[1]
+        elif f[0] > m:  # every value in the outer cell
+            assert abs(b - f.mean()) < 1e-12 and a == O.UNIFORM_CODEBOOK[0]
+        else:
+            assert any(abs(a - ak) < 1e-12 and abs(b - bk) < 1e-12 for ak, bk in consistent), (trial, f)
+        assert err(a, b) <= err(*O.UNIFORM_CODEBOOK) + 1e-12
+        assert a < b
+
+
+def test_fit_codebook_is_a_fixed_point_and_lowers_the_error():
+    """On rotated Gaussian-like rows: the fitted levels are the centroids of
+    their own cells, the reconstruction error of t drops against the uniform
+    levels, and the levels are those of the folded values of every group."""
+    rng = np.random.default_rng(11)
+    X = (rng.standard_normal((300, 128)) @ O.rotation(np.eye(128), O.ROT_HADAMARD)).astype(np.float32)
+    g, clip = 64, 0.9
+    a, b, it = O.fit_codebook(X, g, clip)
+    f = O.folded_values(X, g, clip).astype(np.float64)
+    assert f.size == 300 * 128 and it >= 2
+    m = (a + b) / 2
+    assert abs(f[f <= m].mean() - a) < 1e-12 and abs(f[f > m].mean() - b) < 1e-12
+
+    def t_err(a_, b_):
+        tot = 0.0
+        for n in range(X.shape[0]):
+            for gr in range(128 // g):
+                t, _, _ = O.group_t(X[n, gr * g:(gr + 1) * g], clip)
+                lv = O.codebook_levels(a_, b_)[O.codes_from_t(t, a_, b_)]
+                tot += float(np.sum((t.astype(np.float64) - lv) ** 2))
+        return tot
+
+    assert t_err(a, b) < t_err(*O.UNIFORM_CODEBOOK)
+    # the codebook lowers the key-side quantisation error of these rows too
+    xu = O.quantize_dequantize_rows(X, g, clip)
+    xc = O.quantize_dequantize_rows(X, g, clip, (a, b))
+    assert np.sum((xc - X) ** 2) < np.sum((xu - X) ** 2)
+
+
+def test_zero_scale_groups_carry_no_folded_values():
+    X = np.zeros((2, 128), dtype=np.float32)
+    X[1, :64] = np.linspace(-1, 1, 64)
+    f = O.folded_values(X, 64, 1.0)
+    assert f.size == 64
+    assert O.lloyd_max_folded(np.zeros(0))[:2] == O.UNIFORM_CODEBOOK
