@@ -649,6 +649,63 @@ def run_ours(args, wl):
     cal_flops = Hkv * (2 * 2 * G_cal * N_cal * 128 * 128 + G_cal * causal_pairs * 128 * 4)
     clip_flops = Hkv * (2 * G_cal * N_cal * 128 * 128 + len(ratios) * (2 * N_cal * 128 * 128 + G_cal * causal_pairs * 128 * 4))
     fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12  # FMA lanes x 2 FLOP x max SM clock
+    # ---- Lloyd-Max codebook: per-head fits on the calibration keys and values,
+    # the attention errors they leave against the uniform levels, and the decode
+    # over cache copies written with them (a second context)
+    cctx = oscar.oscar_create(cfg)
+    oscar.oscar_set_rotation(cctx, 0, wk["U"][0], wk["U"][1], [wl["clip"]] * Hkv, [wl["clip"]] * Hkv,
+                             oscar.ROT_OSCAR)
+    fscr = oscar.codebook_scratch(N_cal, dev)
+    oscar.oscar_fit_codebook(cctx, 0, 0, 0, cal_sets[0][1], N_cal, fscr)  # warm-up
+    t3 = time.perf_counter()
+    kab, vab, ups = [], [], []
+    for h in range(Hkv):
+        for which, dst in ((0, kab), (1, vab)):
+            a_, b_, u_ = oscar.oscar_fit_codebook(cctx, 0, h, which, cal_sets[h][1 + which], N_cal, fscr)
+            dst.append((a_, b_))
+            ups.append(u_)
+    t4 = time.perf_counter()
+    oscar.oscar_set_codebook(cctx, 0, kab, vab)
+    err = {"uniform": [0.0, 0.0], "codebook": [0.0, 0.0]}
+    for name, cx in (("uniform", ctx), ("codebook", cctx)):
+        for h in range(Hkv):
+            ek_, ev_, _, _ = oscar.oscar_clip_errors(cx, 0, h, *cal_sets[h], N_cal, [wl["clip"]], cscr)
+            err[name][0] += float(ek_[0])
+            err[name][1] += float(ev_[0])
+    cb_base = oscar.alloc_cache(cfg, dev)
+    cb_base["page_table"].copy_(wk["copies"][0]["page_table"])
+    oscar.oscar_import_tokens(cctx, 0, cb_base, wk["K"][:, :, :L0].contiguous(), wk["V"][:, :, :L0].contiguous(),
+                              Bsz, L0)
+    torch.cuda.synchronize()
+    cb_copies = [cb_base] + [{k: v.clone() for k, v in cb_base.items()} for _ in range(n_copies - 1)]
+    cdec = [oscar.bind_decode(cctx, 0, cb_copies[c], q, out, lse, scratch, Bsz) for c in range(n_copies)]
+    for i in range(5):
+        cdec[i % n_copies]()
+    cb_us = time_calls(lambda i: cdec[i % n_copies](), nd)
+    oscar.oscar_profile_enable(cctx, True)
+    for i in range(50):
+        cdec[i % n_copies]()
+    ncb, tcb = oscar.oscar_profile_read(cctx, oscar.KERNEL_DECODE_MAIN, reset=True)
+    oscar.oscar_profile_enable(cctx, False)
+    cb_main_us = tcb * 1e3 / max(ncb, 1)
+    cb_bytes = algorithmic_bytes(L0 - 320, L0, Hkv, g) * Bsz
+    assert oscar.oscar_get_error(cctx) == 0
+    assert torch.isfinite(out.float()).all()
+    codebook = {"fit_ms": (t4 - t3) * 1e3, "fits": 2 * Hkv, "mean_updates": float(np.mean(ups)),
+                "k_ab": [[round(a_, 5), round(b_, 5)] for a_, b_ in kab],
+                "v_ab": [[round(a_, 5), round(b_, 5)] for a_, b_ in vab],
+                "logit_error_ratio": err["codebook"][0] / err["uniform"][0],
+                "output_error_ratio": err["codebook"][1] / err["uniform"][1],
+                "decode_us": cb_us, "decode_main_us": cb_main_us,
+                "decode_main_hbm_gbs": cb_bytes / (cb_main_us * 1e-6) / 1e9,
+                "decode_main_frac": cb_bytes / (cb_main_us * 1e-6) / 1e9 / peak,
+                "vs_uniform_decode": cb_us / int2_us,
+                "note": "symmetric 4-level Lloyd-Max levels per kv head for K and V, fitted on the GPU from the "
+                        "2048-token calibration sets at the workload's clip ratio; errors are the clip-search "
+                        "objectives summed over kv heads (codebook / uniform); the codebook decode takes two "
+                        "tensor-core products per operand (bit planes) over the same cache bytes"}
+    del cb_copies, cb_base, cdec
+    oscar.oscar_destroy(cctx)
     # ---- synthetic serving loop under one KV memory budget, INT2 vs BF16 history
     serve = serving_measurement(wl, dev)
     # ---- end to end through the public API with host buffers: each step's q,
@@ -725,6 +782,7 @@ def run_ours(args, wl):
                             "kind::f16 (M=128) with Q, S, P, O in tensor memory; bound: tensor; peak = "
                             "dense bf16 burst (fp16 runs at the same rate)"},
         "serving": serve,
+        "codebook": codebook,
         "calibration": {"kv_heads": Hkv, "tokens": N_cal, "query_heads_per_kv": G_cal, "ratios": len(ratios),
                         "calibrate_ms": (t1 - t0) * 1e3, "clip_search_ms": (t2 - t1) * 1e3,
                         "tflops": (cal_flops + clip_flops) / (t2 - t0) / 1e12, "bound": "alu",

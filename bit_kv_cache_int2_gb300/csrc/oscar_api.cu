@@ -1,6 +1,7 @@
 // Host side of the liboscar C ABI: argument checks, context, rotation tables
 // and kernel launches.  See include/oscar.h for the contract of each call.
 #include <math.h>
+#include <cmath>
 #include <stdlib.h>
 #include <string.h>
 
@@ -55,7 +56,10 @@ struct oscar_ctx {
   int G = 0, NG = 0;
   float* d_rot = nullptr;  // [layers][4][Hkv][128 * 128 words]: R_K, R_V, R_V fragments, R_V^T
   float* d_clip = nullptr;  // [layers][2][Hkv]
+  float* d_cb = nullptr;    // [layers][2][Hkv][CB_WORDS] codebook records (uniform by default)
   std::vector<int> mode;
+  std::vector<int> has_cb;        // [layers] a non-uniform codebook is set: decode variant 4
+  std::vector<float> clip_host;   // [layers][2][Hkv] copy of d_clip
   int* d_err = nullptr;
   int* d_req_counter = nullptr;  // [max_batch]
   int impl = 0;
@@ -93,10 +97,12 @@ size_t scratch_for(const oscar_ctx* ctx, int B, int target) {
   return decode_scratch_bytes(B, ctx->cfg.num_q_heads, ctx->cfg.num_kv_heads, ctx->G, target);
 }
 
-// Decode kernel variant: 1 CUDA-core INT2; 3 tensor cores, pages in pairs as
+// Decode kernel variant: 4 tensor cores with the layer's Lloyd-Max codebook
+// (whatever the option); 1 CUDA-core INT2; 3 tensor cores, pages in pairs as
 // two softmax streams per tile (needs G <= 4); 0 tensor cores, one page at a
-// time.
-int kernel_impl(const oscar_ctx* ctx) {
+// time.  layer < 0: the variant without a codebook.
+int kernel_impl(const oscar_ctx* ctx, int layer = -1) {
+  if (layer >= 0 && ctx->has_cb[layer]) return 4;
   if (ctx->impl == OSCAR_DECODE_CUDA_CORE) return 1;
   if (ctx->impl == OSCAR_DECODE_TENSOR_SINGLE || ctx->G > 4) return 0;
   return 3;
@@ -104,21 +110,21 @@ int kernel_impl(const oscar_ctx* ctx) {
 
 // Persistent decode CTAs per SM: the option, capped by what the kernel variant
 // for this call can keep resident.
-int decode_ctas(const oscar_ctx* ctx, int batch, bool bf16_history) {
+int decode_ctas(const oscar_ctx* ctx, int batch, bool bf16_history, int layer = -1) {
   DecodeArgs a = {};
   a.cv.head_bytes = bf16_history ? BF16_HEAD_BYTES : int2_head_bytes(ctx->cfg.group_size);
   a.cv.NG = ctx->NG;
   a.cv.G = ctx->G;
   a.B = batch;
-  a.impl = kernel_impl(ctx);
+  a.impl = bf16_history ? 0 : kernel_impl(ctx, layer);
   a.bf16_history = bf16_history ? 1 : 0;
   int occ = decode_ctas_per_sm(a);
   if (occ < 1) occ = 1;
   return ctx->ctas_per_sm < occ ? ctx->ctas_per_sm : occ;
 }
 
-int target_items(const oscar_ctx* ctx, int batch, bool bf16_history) {
-  int t = ctx->num_sms * decode_ctas(ctx, batch, bf16_history) * ctx->items_per_cta;
+int target_items(const oscar_ctx* ctx, int batch, bool bf16_history, int layer = -1) {
+  int t = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, layer) * ctx->items_per_cta;
   if (t > MAX_TARGET_ITEMS) t = MAX_TARGET_ITEMS;
   if (t < 1) t = 1;
   return t;
@@ -236,6 +242,22 @@ void build_layer_table(const float* U_K, const float* U_V, int mode, int Hkv, st
   }
 }
 
+// The device record of codebook (a, b): thresholds and decode constants in
+// float32, lo/hi = 1.5 -/+ m with m = (a + b)/2.
+void codebook_record(float a, float b, float* rec) {
+  const float m = (a + b) * 0.5f;  // the halving is exact
+  for (int i = 0; i < CB_WORDS; ++i) rec[i] = 0.f;
+  rec[CB_A] = a;
+  rec[CB_B] = b;
+  rec[CB_LO] = 1.5f - m;
+  rec[CB_HI] = 1.5f + m;
+  rec[CB_C0] = 1.5f - b;
+  rec[CB_ALPHA] = b - a;
+  rec[CB_BETA_HALF] = m;
+}
+
+bool codebook_ok(float a, float b) { return std::isfinite(a) && std::isfinite(b) && a >= 0.f && a < b && b <= 3.f; }
+
 LayerRot layer_rot(const oscar_ctx* ctx, int layer) {
   const size_t mat = (size_t)ctx->cfg.num_kv_heads * D * D;
   LayerRot r;
@@ -245,6 +267,7 @@ LayerRot layer_rot(const oscar_ctx* ctx, int layer) {
   r.RVt = r.R_V + 2 * mat;
   r.clip_k = ctx->d_clip + (size_t)layer * 2 * ctx->cfg.num_kv_heads;
   r.clip_v = r.clip_k + ctx->cfg.num_kv_heads;
+  r.cb = ctx->d_cb + (size_t)layer * 2 * ctx->cfg.num_kv_heads * CB_WORDS;
   r.mode = ctx->mode[layer];
   return r;
 }
@@ -270,7 +293,8 @@ oscar_status decode_args(oscar_ctx* ctx, int layer, const oscar_cache* cache, co
       (lse && !aligned(lse, 4)))
     return OSCAR_ERR_INVALID_ARG;
   if (batch == 0) return OSCAR_ERR_STATE;
-  const int target = target_items(ctx, batch, bf16_history);
+  const int vlayer = bf16_history ? -1 : layer;  // BF16 history has no codes, so no codebook
+  const int target = target_items(ctx, batch, bf16_history, vlayer);
   if (scratch_bytes < scratch_for(ctx, batch, target)) return OSCAR_ERR_INVALID_ARG;
   a.cv = make_view(ctx, cache, bf16_history);
   a.q = (const __nv_bfloat16*)q;
@@ -286,14 +310,14 @@ oscar_status decode_args(oscar_ctx* ctx, int layer, const oscar_cache* cache, co
   a.part = (float*)(sp + sl.off_part);
   a.B = batch;
   a.target_items = target;
-  a.impl = kernel_impl(ctx);
+  a.impl = bf16_history ? 0 : kernel_impl(ctx, vlayer);
   a.bf16_history = bf16_history ? 1 : 0;
   a.rot = layer_rot(ctx, layer);
   // heads per merge CTA: halve while the merge would not cover the SMs
   a.merge_hpc = ctx->G;
   while (a.merge_hpc % 2 == 0 && batch * ctx->cfg.num_kv_heads * (ctx->G / a.merge_hpc) < ctx->num_sms)
     a.merge_hpc /= 2;
-  grid = ctx->num_sms * decode_ctas(ctx, batch, bf16_history);
+  grid = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, vlayer);
   return OSCAR_OK;
 }
 
@@ -397,6 +421,8 @@ oscar_status oscar_create(const oscar_config* cfg, oscar_ctx** out) {
   ctx->G = cfg->num_q_heads / cfg->num_kv_heads;
   ctx->NG = D / cfg->group_size;
   ctx->mode.assign(cfg->num_layers, (int)OSCAR_ROT_NONE);
+  ctx->has_cb.assign(cfg->num_layers, 0);
+  ctx->clip_host.assign((size_t)cfg->num_layers * 2 * cfg->num_kv_heads, 1.f);
   cudaError_t e = cudaGetDevice(&ctx->device);
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device);
@@ -405,6 +431,8 @@ oscar_status oscar_create(const oscar_config* cfg, oscar_ctx** out) {
   const size_t clip_bytes = (size_t)cfg->num_layers * 2 * cfg->num_kv_heads * sizeof(float);
   if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_rot, rot_bytes);
   if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_clip, clip_bytes);
+  const size_t cb_floats = (size_t)cfg->num_layers * 2 * cfg->num_kv_heads * CB_WORDS;
+  if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_cb, cb_floats * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_err, sizeof(int));
   if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_req_counter, sizeof(int) * cfg->max_batch);
   if (e == cudaSuccess) e = cudaMemset(ctx->d_err, 0, sizeof(int));
@@ -419,6 +447,10 @@ oscar_status oscar_create(const oscar_config* cfg, oscar_ctx** out) {
     std::vector<float> ones((size_t)cfg->num_layers * 2 * cfg->num_kv_heads, 1.f);
     if (e == cudaSuccess)
       e = cudaMemcpy(ctx->d_clip, ones.data(), clip_bytes, cudaMemcpyHostToDevice);
+    std::vector<float> cb(cb_floats);
+    for (size_t i = 0; i < cb_floats; i += CB_WORDS) codebook_record(0.5f, 1.5f, &cb[i]);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(ctx->d_cb, cb.data(), cb_floats * sizeof(float), cudaMemcpyHostToDevice);
   }
   if (e != cudaSuccess) {
     oscar_destroy(ctx);
@@ -433,6 +465,7 @@ oscar_status oscar_destroy(oscar_ctx* ctx) {
   cudaDeviceSynchronize();
   if (ctx->d_rot) cudaFree(ctx->d_rot);
   if (ctx->d_clip) cudaFree(ctx->d_clip);
+  if (ctx->d_cb) cudaFree(ctx->d_cb);
   if (ctx->d_err) cudaFree(ctx->d_err);
   if (ctx->d_req_counter) cudaFree(ctx->d_req_counter);
   for (cudaEvent_t e : ctx->prof.pool) cudaEventDestroy(e);
@@ -492,6 +525,7 @@ oscar_status oscar_set_rotation(oscar_ctx* ctx, int layer, const float* U_K, con
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return OSCAR_ERR_CUDA;
   ctx->mode[layer] = rot_mode;
+  memcpy(ctx->clip_host.data() + (size_t)layer * 2 * Hkv, clips.data(), 2 * Hkv * sizeof(float));
   return OSCAR_OK;
 }
 
@@ -589,6 +623,7 @@ oscar_status oscar_prefill(oscar_ctx* ctx, int layer, const oscar_cache* cache, 
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
       !aligned(scratch, 256) || (lse && !aligned(lse, 4)))
     return OSCAR_ERR_INVALID_ARG;
+  if (ctx->has_cb[layer]) return OSCAR_ERR_UNSUPPORTED;  // the prefill dequantises uniform codes only
   if (batch == 0) return OSCAR_OK;
   const int Hkv = ctx->cfg.num_kv_heads, G = ctx->G;
   PrefillArgs a;
@@ -697,7 +732,8 @@ oscar_status oscar_clip_errors(oscar_ctx* ctx, int layer, int kv_head, const voi
   uint8_t* sp = (uint8_t*)scratch;
   cudaError_t e = calib_clip_errors(r.R_K + (size_t)kv_head * D * D, r.R_V + (size_t)kv_head * D * D,
                                     (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K, (const __nv_bfloat16*)V, G, N,
-                                    ctx->cfg.group_size, ratios, M, sp, st);
+                                    ctx->cfg.group_size, ratios, M, r.cb + (size_t)kv_head * CB_WORDS,
+                                    r.cb + (size_t)(ctx->cfg.num_kv_heads + kv_head) * CB_WORDS, sp, st);
   if (e != cudaSuccess) return cuda_status(e);
   std::vector<double> h(2 * (size_t)M);
   e = cudaMemcpyAsync(h.data(), sp + L.off_err, h.size() * sizeof(double), cudaMemcpyDeviceToHost, st);
@@ -719,7 +755,8 @@ oscar_status oscar_decode_noalloc(oscar_ctx* ctx, int layer, const oscar_cache* 
                                   const void* q, void* out, float* lse, int batch,
                                   oscar_stream_t stream) {
   if (!ctx || batch < 0 || batch > ctx->cfg.max_batch) return OSCAR_ERR_INVALID_ARG;
-  if (scratch_for(ctx, batch, target_items(ctx, batch, false)) > (size_t)OSCAR_NOALLOC_SCRATCH_BYTES)
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
+  if (scratch_for(ctx, batch, target_items(ctx, batch, false, layer)) > (size_t)OSCAR_NOALLOC_SCRATCH_BYTES)
     return OSCAR_ERR_TOO_LARGE;
   void* scratch = nullptr;
   const oscar_status st = noalloc_scratch(&scratch);
@@ -744,8 +781,76 @@ oscar_status oscar_quantize_rotated_f32(const float* x, int n, int group_size, f
   if (!(clip > 0.f && clip <= 1.f)) return OSCAR_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(sz, 4)) return OSCAR_ERR_INVALID_ARG;
   if (n == 0) return OSCAR_OK;
-  return cuda_status(
-      launch_quantize_hook(x, n, group_size, clip, which, codes, (__half2*)sz, (cudaStream_t)stream));
+  return cuda_status(launch_quantize_hook(x, n, group_size, clip, which, 0.5f, 2.5f, codes, (__half2*)sz,
+                                          (cudaStream_t)stream));
+}
+
+oscar_status oscar_quantize_codebook_f32(const float* x, int n, int group_size, float clip, float a, float b,
+                                         int which, uint8_t* codes, void* sz, oscar_stream_t stream) {
+  if (!x || !codes || !sz || n < 0) return OSCAR_ERR_INVALID_ARG;
+  if (group_size != 32 && group_size != 64 && group_size != 128) return OSCAR_ERR_UNSUPPORTED;
+  if (which != 0 && which != 1) return OSCAR_ERR_INVALID_ARG;
+  if (which == 1 && (n % PAGE)) return OSCAR_ERR_INVALID_ARG;
+  if (!(clip > 0.f && clip <= 1.f) || !codebook_ok(a, b)) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(sz, 4)) return OSCAR_ERR_INVALID_ARG;
+  if (n == 0) return OSCAR_OK;
+  float rec[CB_WORDS];
+  codebook_record(a, b, rec);
+  return cuda_status(launch_quantize_hook(x, n, group_size, clip, which, rec[CB_LO], rec[CB_HI], codes,
+                                          (__half2*)sz, (cudaStream_t)stream));
+}
+
+oscar_status oscar_set_codebook(oscar_ctx* ctx, int layer, const float* k_ab, const float* v_ab,
+                                oscar_stream_t stream) {
+  if (!ctx || layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
+  const int Hkv = ctx->cfg.num_kv_heads;
+  std::vector<float> rec((size_t)2 * Hkv * CB_WORDS);
+  bool any = false;
+  for (int side = 0; side < 2; ++side) {
+    const float* ab = side == 0 ? k_ab : v_ab;
+    for (int h = 0; h < Hkv; ++h) {
+      const float a = ab ? ab[2 * h] : 0.5f, b = ab ? ab[2 * h + 1] : 1.5f;
+      if (!codebook_ok(a, b)) return OSCAR_ERR_INVALID_ARG;
+      if (a != 0.5f || b != 1.5f) any = true;
+      codebook_record(a, b, &rec[((size_t)side * Hkv + h) * CB_WORDS]);
+    }
+  }
+  const cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(ctx->d_cb + (size_t)layer * rec.size(), rec.data(), rec.size() * sizeof(float),
+                                  cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_status(e);
+  ctx->has_cb[layer] = any ? 1 : 0;
+  return OSCAR_OK;
+}
+
+size_t oscar_codebook_scratch_bytes(int N) {
+  if (N < 1 || N > OSCAR_CODEBOOK_MAX_ROWS) return 0;
+  return codebook_scratch_bytes(N);
+}
+
+oscar_status oscar_fit_codebook(oscar_ctx* ctx, int layer, int kv_head, int which, const void* X, int N,
+                                int max_iters, void* scratch, size_t scratch_bytes, float* ab, int* updates,
+                                oscar_stream_t stream) {
+  if (!ctx || !X || !scratch || !ab || (which != 0 && which != 1)) return OSCAR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= ctx->cfg.num_layers || kv_head < 0 || kv_head >= ctx->cfg.num_kv_heads)
+    return OSCAR_ERR_INVALID_ARG;
+  if (N < 1 || N > OSCAR_CODEBOOK_MAX_ROWS || max_iters < 1) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned(scratch, 256) || !aligned(X, 16)) return OSCAR_ERR_INVALID_ARG;
+  if (scratch_bytes < codebook_scratch_bytes(N)) return OSCAR_ERR_INVALID_ARG;
+  const int Hkv = ctx->cfg.num_kv_heads;
+  const LayerRot r = layer_rot(ctx, layer);
+  const float* R = (which == 0 ? r.R_K : r.R_V) + (size_t)kv_head * D * D;
+  const float clip = ctx->clip_host[(size_t)layer * 2 * Hkv + (size_t)which * Hkv + kv_head];
+  double h[2];
+  int up = 0;
+  const cudaError_t e = calib_fit_codebook(R, (const __nv_bfloat16*)X, N, ctx->cfg.group_size, clip, max_iters,
+                                           (uint8_t*)scratch, h, &up, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  ab[0] = (float)h[0];
+  ab[1] = (float)h[1];
+  if (updates) *updates = up;
+  return OSCAR_OK;
 }
 
 oscar_status oscar_debug_rotate(oscar_ctx* ctx, int layer, int which, int kv_head, const void* x,

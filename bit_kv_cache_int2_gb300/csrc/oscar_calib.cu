@@ -177,17 +177,21 @@ __global__ void __launch_bounds__(256, 1) causal_attn_kernel(const __nv_bfloat16
 }
 
 // E[m][n][c] = x'[n][c] - x̂'[n][c], x̂' the demotion quantiser's dequantised
-// value of row n at clip ratio clips[m] (code·s + z, one fp32 rounding).
+// value of row n at clip ratio clips[m]: level(code)·s + z with the head's
+// codebook record cb (level = code for the uniform codebook).
 __global__ void __launch_bounds__(128) quant_err_kernel(const float* __restrict__ Xr, int N, int g,
-                                                        const float* __restrict__ clips, float* E) {
+                                                        const float* __restrict__ clips,
+                                                        const float* __restrict__ cb, float* E) {
   __shared__ float red[8];
   const int n = blockIdx.x, m = blockIdx.y, j = threadIdx.x;
   const float x = Xr[(size_t)n * D + j];
   float mn, mx;
   group_minmax(x, j, g, red, 1, mn, mx);
   const QParams p = quant_params(mn, mx, clips[m]);
-  const uint32_t code = quant_code(x, p);
-  const float xh = fmaf((float)code, __half2float(p.s), __half2float(p.z));
+  const uint32_t code = quant_code(x, p, quant_thr(cb));
+  const float lvl = fmaf(2.f * __ldg(cb + CB_BETA_HALF), (float)(code >> 1),
+                         fmaf(__ldg(cb + CB_ALPHA), (float)(code & 1u), __ldg(cb + CB_C0)));
+  const float xh = fmaf(lvl, __half2float(p.s), __half2float(p.z));
   E[((size_t)m * N + n) * D + j] = x - xh;
 }
 
@@ -208,6 +212,102 @@ __global__ void __launch_bounds__(128) key_err_kernel(const float* __restrict__ 
   if ((c & 31) == 0) part[c >> 5] = v;
   __syncthreads();
   if (c == 0) atomicAdd(&err[m], (double)((part[0] + part[1]) + (part[2] + part[3])));
+}
+
+// Lloyd-Max codebook fit ----------------------------------------------------
+// In place over rotated rows X' [N][128]: f = |t - 1.5| with t = (x - z)/s the
+// quantiser's normalised value at clip ratio `clip`, or -1 where the group's
+// scale is zero (no t).
+__global__ void __launch_bounds__(128) fold_kernel(float* X, int g, float clip) {
+  __shared__ float red[8];
+  const int n = blockIdx.x, j = threadIdx.x;
+  float* px = X + (size_t)n * D + j;
+  const float x = *px;
+  float mn, mx;
+  group_minmax(x, j, g, red, 1, mn, mx);
+  const QParams p = quant_params(mn, mx, clip);
+  const float sf = __half2float(p.s);
+  float f = -1.f;
+  if (sf != 0.f) f = fabsf(__fsub_rn(__fdiv_rn(__fsub_rn(x, __half2float(p.z)), sf), 1.5f));
+  *px = f;
+}
+
+// Two-level Lloyd-Max on the n folded values (one CTA): inner level a = mean
+// of f <= m, outer level b = mean of f > m, m = (a + b)/2, from a = 1/2,
+// b = 3/2 until the inner count repeats.  fp64 sums in a fixed order.
+// out: a, b, number of centroid updates.
+__global__ void __launch_bounds__(1024) lloyd_kernel(const float* __restrict__ F, int n, int max_iters,
+                                                     double* out) {
+  __shared__ double rs[2][32];
+  __shared__ int rc[2][32];
+  __shared__ double ab[2];
+  __shared__ int stop;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  double a = 0.5, b = 1.5;
+  int prev = -1, updates = 0;  // thread 0's
+  for (int it = 0; it < max_iters; ++it) {
+    const double m = (a + b) * 0.5;
+    double si = 0.0, so = 0.0;
+    int ci = 0, co = 0;
+    for (int i = t; i < n; i += 1024) {
+      const float f = F[i];
+      if (f < 0.f) continue;
+      if ((double)f <= m) {
+        si += (double)f;
+        ++ci;
+      } else {
+        so += (double)f;
+        ++co;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      si += __shfl_xor_sync(0xffffffffu, si, o);
+      so += __shfl_xor_sync(0xffffffffu, so, o);
+      ci += __shfl_xor_sync(0xffffffffu, ci, o);
+      co += __shfl_xor_sync(0xffffffffu, co, o);
+    }
+    if (lane == 0) {
+      rs[0][w] = si;
+      rs[1][w] = so;
+      rc[0][w] = ci;
+      rc[1][w] = co;
+    }
+    __syncthreads();
+    if (t == 0) {
+      double SI = 0.0, SO = 0.0;
+      int CI = 0, CO = 0;
+      for (int k = 0; k < 32; ++k) {
+        SI += rs[0][k];
+        SO += rs[1][k];
+        CI += rc[0][k];
+        CO += rc[1][k];
+      }
+      int st = 0;
+      if (CI == prev) {
+        st = 1;  // same cells as last time: a and b are their centroids
+      } else {
+        if (CI > 0) a = SI / CI;
+        if (CO > 0) b = SO / CO;
+        prev = CI;
+        ++updates;
+      }
+      ab[0] = a;
+      ab[1] = b;
+      stop = st;
+    }
+    __syncthreads();
+    a = ab[0];
+    b = ab[1];
+    const int st = stop;
+    __syncthreads();  // everyone has read ab and stop before the next round writes them
+    if (st) break;
+  }
+  if (t == 0) {
+    out[0] = a;
+    out[1] = b;
+    out[2] = (double)updates;
+  }
 }
 
 __global__ void to_f32_kernel(const double* __restrict__ a, float* b, int n) {
@@ -374,7 +474,7 @@ oscar_status calib_eigh(const double* dC, double* evec_host, cudaStream_t st, in
 
 cudaError_t calib_clip_errors(const float* R_K, const float* R_V, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                               const __nv_bfloat16* V, int G, int N, int g, const float* clips_host, int M,
-                              uint8_t* scratch, cudaStream_t st) {
+                              const float* cb_k, const float* cb_v, uint8_t* scratch, cudaStream_t st) {
   const CalibScratch L = calib_scratch_layout(G, N, M);
   double* C = (double*)(scratch + L.off_c);
   float* Cf = (float*)(scratch + L.off_cf);
@@ -396,11 +496,11 @@ cudaError_t calib_clip_errors(const float* R_K, const float* R_V, const __nv_bfl
   // keys: Σ_n e_n (Q'ᵀQ') e_nᵀ
   gram_kernel<float><<<(rows + GRAM_ROWS - 1) / GRAM_ROWS, 256, 0, st>>>(Qr, rows, C);
   to_f32_kernel<<<(D * D + 255) / 256, 256, 0, st>>>(C, Cf, D * D);
-  quant_err_kernel<<<dim3(N, M), 128, 0, st>>>(Kr, N, g, clips, E);
+  quant_err_kernel<<<dim3(N, M), 128, 0, st>>>(Kr, N, g, clips, cb_k, E);
   key_err_kernel<<<dim3(N, M), 128, 0, st>>>(E, N, Cf, err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // values: Σ_h ||S_h E_m||²_F
-  quant_err_kernel<<<dim3(N, M), 128, 0, st>>>(Vr, N, g, clips, E);
+  quant_err_kernel<<<dim3(N, M), 128, 0, st>>>(Vr, N, g, clips, cb_v, E);
   e = cudaFuncSetAttribute(causal_attn_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM);
   if (e != cudaSuccess) return e;
   for (int m = 0; m < M; ++m) {
@@ -408,6 +508,27 @@ cudaError_t calib_clip_errors(const float* R_K, const float* R_V, const __nv_bfl
         Q, K, E + (size_t)m * N * D, N, nullptr, err + M + m);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  return cudaSuccess;
+}
+
+size_t codebook_scratch_bytes(int N) { return ((size_t)N * D * 4 + 255) / 256 * 256 + 256; }
+
+cudaError_t calib_fit_codebook(const float* R, const __nv_bfloat16* X, int N, int g, float clip, int max_iters,
+                               uint8_t* scratch, double* ab_host, int* updates_host, cudaStream_t st) {
+  float* F = (float*)scratch;
+  double* out = (double*)(scratch + ((size_t)N * D * 4 + 255) / 256 * 256);
+  cudaError_t e = launch_debug_rotate(R, X, F, N, st);  // the demotion's fp32 rotation
+  if (e != cudaSuccess) return e;
+  fold_kernel<<<N, 128, 0, st>>>(F, g, clip);
+  lloyd_kernel<<<1, 1024, 0, st>>>(F, N * D, max_iters, out);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  double h[3];
+  e = cudaMemcpyAsync(h, out, sizeof(h), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return e;
+  ab_host[0] = h[0];
+  ab_host[1] = h[1];
+  *updates_host = (int)h[2];
   return cudaSuccess;
 }
 

@@ -48,7 +48,8 @@ struct SmemLayout {
   int off_stage, off_mbar, off_qpk, off_qf, off_vs, off_pre, off_red, off_misc, total;
 };
 
-// impl: 0 tensor-core INT2, 1 CUDA-core INT2, 2 BF16 history (no INT2 pages)
+// impl: 0 tensor-core INT2, 1 CUDA-core INT2, 2 BF16 history (no INT2 pages),
+// 3 tensor-core page pairs, 4 tensor-core with a Lloyd-Max codebook
 __host__ __device__ inline SmemLayout smem_layout(int head_bytes, int B, int impl, int G) {
   SmemLayout L;
   // BF16 paths read global memory directly; only INT2 pages use stages
@@ -65,6 +66,7 @@ __host__ __device__ inline SmemLayout smem_layout(int head_bytes, int B, int imp
   o += NW * DEPTH * 8;  // pipeline stages
   L.off_qpk = o;        // tensor-core paths: the G packed query records of the item's kv head
   if (impl == 0 || impl == 3) o += G * QPACK_BYTES;
+  if (impl == 4) o += G * QPACK_CB_BYTES;
   L.off_qf = o;
   if (impl == 1) o += MAX_G * D * 4 + MAX_G * 4 * 4;  // fp32 q' in K storage order + z weights
   L.off_vs = o;
@@ -237,6 +239,171 @@ __device__ __forceinline__ void int2_page_mma(Int2State<NG>& S, const uint8_t* s
           default: a0 = code_pair<6>(vw[j][0]); a1 = code_pair<6>(vw[j][1]); a2 = code_pair<7>(vw[j][0]); a3 = code_pair<7>(vw[j][1]); break;
         }
         mma_f16(S.oacc[j], a0, a1, a2, a3, b0, b1);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------- Lloyd-Max codebook pages
+// With a codebook a code's level is c0 + alpha*bit0 + beta*bit1 (symmetric
+// levels have no bit0*bit1 term), so a page takes two tensor-core products
+// per operand instead of one: the low bit planes against q' * alpha (resp.
+// p * s * alpha) and the high bit planes against q' * beta / 2 (resp.
+// p * s * beta / 2), into the same accumulators.  c0 moves into the logit
+// offset (keys) and into the zero-point sums (values).
+struct CbExtra {
+  uint32_t bq2[8][2];  // q' B fragments of the high bit plane (qb of the record)
+  float va, vb, vc0;   // alpha_V, beta_half_V, c0_V
+};
+
+// The four A registers of bit plane P for code positions 2q, 2q + 1 (q = 0..3)
+// of words x (rows gid) and y (rows gid + 8).
+template <int P>
+__device__ __forceinline__ void plane_frag(int q, uint32_t x, uint32_t y, uint32_t& a0, uint32_t& a1,
+                                           uint32_t& a2, uint32_t& a3) {
+  switch (q) {
+    case 0: a0 = code_plane<0, P>(x); a1 = code_plane<0, P>(y); a2 = code_plane<1, P>(x); a3 = code_plane<1, P>(y); break;
+    case 1: a0 = code_plane<2, P>(x); a1 = code_plane<2, P>(y); a2 = code_plane<3, P>(x); a3 = code_plane<3, P>(y); break;
+    case 2: a0 = code_plane<4, P>(x); a1 = code_plane<4, P>(y); a2 = code_plane<5, P>(x); a3 = code_plane<5, P>(y); break;
+    default: a0 = code_plane<6, P>(x); a1 = code_plane<6, P>(y); a2 = code_plane<7, P>(x); a3 = code_plane<7, P>(y); break;
+  }
+}
+
+template <int NG, bool FULL>
+__device__ __forceinline__ void int2_page_mma_cb(Int2State<NG>& S, const CbExtra& X, const uint8_t* stage,
+                                                 int nv, int lane) {
+  const int gid = lane >> 2, tq = lane & 3;
+  constexpr int KPG = 8 / NG;
+  constexpr int MPG = 8 / NG;
+  const uint8_t* kc = stage;
+  const uint8_t* vc = stage + 2048;
+  const __half2* ksz = (const __half2*)(stage + 4096);
+  const __half2* vsz = (const __half2*)(stage + 4096 + PAGE * NG * 4);
+
+  uint2 wa[4], wb[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    wa[s] = *(const uint2*)(kc + (16 * s + gid) * 32 + 8 * tq);
+    wb[s] = *(const uint2*)(kc + (16 * s + gid + 8) * 32 + 8 * tq);
+  }
+  float acc[4][NG][4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s)
+#pragma unroll
+    for (int gr = 0; gr < NG; ++gr) acc[s][gr][0] = acc[s][gr][1] = acc[s][gr][2] = acc[s][gr][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const uint32_t xa = kk < 4 ? wa[s].x : wa[s].y;
+      const uint32_t xb = kk < 4 ? wb[s].x : wb[s].y;
+      uint32_t a0, a1, a2, a3;
+      plane_frag<0>(kk & 3, xa, xb, a0, a1, a2, a3);
+      mma_f16(acc[s][kk / KPG], a0, a1, a2, a3, S.bq[kk][0], S.bq[kk][1]);
+      plane_frag<1>(kk & 3, xa, xb, a0, a1, a2, a3);
+      mma_f16(acc[s][kk / KPG], a0, a1, a2, a3, X.bq2[kk][0], X.bq2[kk][1]);
+    }
+  }
+  float lam[4][4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int ta = 16 * s + gid, tb = ta + 8;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int row = e < 2 ? ta : tb;
+      const int hc = e & 1;
+      float v = 0.f;
+#pragma unroll
+      for (int gr = 0; gr < NG; ++gr) {
+        const float2 sz = __half22float2(ksz[row * NG + gr]);
+        v = fmaf(sz.x, fmaf(acc[s][gr][e], S.ka[hc], S.kb[hc][gr]), fmaf(sz.y, S.kg[hc][gr], v));
+      }
+      lam[s][e] = (FULL || row < nv) ? v : -INFINITY;
+    }
+  }
+  float pm[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int s = 0; s < 4; ++s)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pm[e & 1] = fmaxf(pm[e & 1], lam[s][e]);
+#pragma unroll
+  for (int hc = 0; hc < 2; ++hc) {
+    pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 4));
+    pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 8));
+    pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 16));
+  }
+  {
+    const float mn0 = fmaxf(S.m[0], pm[0]), mn1 = fmaxf(S.m[1], pm[1]);
+    const bool moved = (mn0 > S.m[0]) || (mn1 > S.m[1]);
+    if (__any_sync(0xffffffffu, moved)) {
+      const float al0 = ex2(S.m[0] - mn0), al1 = ex2(S.m[1] - mn1);
+      S.m[0] = mn0;
+      S.m[1] = mn1;
+      S.l[0] *= al0;
+      S.l[1] *= al1;
+#pragma unroll
+      for (int gr = 0; gr < NG; ++gr) {
+        S.bs[0][gr] *= al0;
+        S.zs[0][gr] *= al0;
+        S.bs[1][gr] *= al1;
+        S.zs[1][gr] *= al1;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        S.oacc[j][0] *= al0;
+        S.oacc[j][2] *= al0;
+        S.oacc[j][1] *= al1;
+        S.oacc[j][3] *= al1;
+      }
+    }
+  }
+  uint32_t vw[8][2];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    vw[j][0] = *(const uint32_t*)(vc + (16 * j + gid) * 16 + 4 * tq);
+    vw[j][1] = *(const uint32_t*)(vc + (16 * j + 8 + gid) * 16 + 4 * tq);
+  }
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int ta = 16 * s + gid, tb = ta + 8;
+    const bool va = FULL || ta < nv, vb = FULL || tb < nv;
+    float p[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      p[e] = ex2(lam[s][e] - S.m[e & 1]);
+      S.l[e & 1] += p[e];
+    }
+    const float fa = (float)(1 << (8 - code_exp_rt(2 * s)));
+    const float fb = (float)(1 << (8 - code_exp_rt(2 * s + 1)));
+#pragma unroll
+    for (int gr = 0; gr < NG; ++gr) {
+      const float2 sa = __half22float2(vsz[ta * NG + gr]);
+      const float2 sb = __half22float2(vsz[tb * NG + gr]);
+      const float s_a = va ? sa.x * fa : 0.f, z_a = va ? fmaf(X.vc0, sa.x, sa.y) : 0.f;
+      const float s_b = vb ? sb.x * fb : 0.f, z_b = vb ? fmaf(X.vc0, sb.x, sb.y) : 0.f;
+      const float sa0 = s_a * X.va, sa1 = s_a * X.vb, sb0 = s_b * X.va, sb1 = s_b * X.vb;
+      const __half2 h0 = __floats2half2_rn(p[0] * sa0, p[1] * sa0);
+      const __half2 h1 = __floats2half2_rn(p[2] * sb0, p[3] * sb0);
+      const __half2 g0 = __floats2half2_rn(p[0] * sa1, p[1] * sa1);
+      const __half2 g1 = __floats2half2_rn(p[2] * sb1, p[3] * sb1);
+      const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+      const float2 e0 = __half22float2(g0), e1 = __half22float2(g1);
+      S.bs[0][gr] += (f0.x + f1.x) + (e0.x + e1.x);
+      S.bs[1][gr] += (f0.y + f1.y) + (e0.y + e1.y);
+      S.zs[0][gr] = fmaf(p[0], z_a, fmaf(p[2], z_b, S.zs[0][gr]));
+      S.zs[1][gr] = fmaf(p[1], z_a, fmaf(p[3], z_b, S.zs[1][gr]));
+      const uint32_t b0 = movmatrix_t(*(const uint32_t*)&h0);
+      const uint32_t b1 = movmatrix_t(*(const uint32_t*)&h1);
+      const uint32_t c0 = movmatrix_t(*(const uint32_t*)&g0);
+      const uint32_t c1 = movmatrix_t(*(const uint32_t*)&g1);
+#pragma unroll
+      for (int jj = 0; jj < MPG; ++jj) {
+        const int j = gr * MPG + jj;
+        uint32_t a0, a1, a2, a3;
+        plane_frag<0>(s, vw[j][0], vw[j][1], a0, a1, a2, a3);
+        mma_f16(S.oacc[j], a0, a1, a2, a3, b0, b1);
+        plane_frag<1>(s, vw[j][0], vw[j][1], a0, a1, a2, a3);
+        mma_f16(S.oacc[j], a0, a1, a2, a3, c0, c1);
       }
     }
   }
@@ -1085,7 +1252,7 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
 // IMPL: 0 INT2 history on tensor cores, 1 INT2 history on CUDA cores,
 // 2 BF16 history (the baseline; no INT2 code, double-buffered BF16 tiles).
 template <int NG, int IMPL>
-__global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3 || IMPL == 4) ? 3 : 2) decode_kernel(DecodeArgs a) {
   constexpr bool BF16H = (IMPL == 2);
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheView& cv = a.cv;
@@ -1277,16 +1444,19 @@ __global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) dec
       }
       bool timed_out = false;
       int k_fail = 0;
-      if constexpr (IMPL == 0 || IMPL == 3) {
-        // IMPL 3: pages in pairs, two streams per tile (G <= 4)
+      if constexpr (IMPL == 0 || IMPL == 3 || IMPL == 4) {
+        // IMPL 3: pages in pairs, two streams per tile (G <= 4); IMPL 4: one
+        // page at a time with the layer's Lloyd-Max codebook
         constexpr bool PAIR = (IMPL == 3);
+        constexpr bool CB = (IMPL == 4);
+        constexpr int QREC = CB ? QPACK_CB_BYTES : QPACK_BYTES;
         // the kv head's G packed query records, copied to shared memory by warp
         // 0 with coalesced 16-byte loads (every warp of every CTA reads them;
         // scattered per-lane loads pile the whole grid onto a few L2 lines,
         // and a bulk copy would queue behind this CTA's page copies)
         if (warp == 0) {
-          const uint4* src = (const uint4*)(a.qpack + ((size_t)b * cv.Hq + kvh * G) * QPACK_BYTES);
-          for (int e = lane; e < G * QPACK_BYTES / 16; e += 32) ((uint4*)qpk)[e] = __ldcg(src + e);
+          const uint4* src = (const uint4*)(a.qpack + ((size_t)b * cv.Hq + kvh * G) * QREC);
+          for (int e = lane; e < G * QREC / 16; e += 32) ((uint4*)qpk)[e] = __ldcg(src + e);
         }
         for (int k = EARLY; k < DEPTH && k < nw_pages; ++k) {
           const int pid = page_id_at(P, k);
@@ -1294,38 +1464,56 @@ __global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) dec
         }
         __syncthreads();
         Int2State<NG> S;
+        CbExtra X;
 #pragma unroll
         for (int j = 0; j < 8; ++j) S.oacc[j][0] = S.oacc[j][1] = S.oacc[j][2] = S.oacc[j][3] = 0.f;
         {
+          constexpr int O_ALPHA = CB ? QPACK_CB_ALPHA : QPACK_ALPHA;
+          constexpr int O_QSUM = CB ? QPACK_CB_QSUM : QPACK_QSUM;
+          constexpr int O_PSUM = CB ? QPACK_CB_PSUM : QPACK_PSUM;
+          float kc0 = 0.f;  // codebook: c0_K, the level of code 0
+          if constexpr (CB) {
+            const float* ck = a.rot.cb + (size_t)kvh * CB_WORDS;
+            const float* cvr = a.rot.cb + (size_t)(Hkv + kvh) * CB_WORDS;
+            kc0 = __ldg(ck + CB_C0);
+            X.va = __ldg(cvr + CB_ALPHA);
+            X.vb = __ldg(cvr + CB_BETA_HALF);
+            X.vc0 = __ldg(cvr + CB_C0);
+          }
           // B column gid carries head gid (PAIR: head gid & 3 in both halves)
           const int qh = PAIR ? (gid & 3) : gid;
           const bool qv = qh < G;
-          const __half* qbh = (const __half*)(qpk + (qv ? qh : 0) * QPACK_BYTES);
+          const __half* qbh = (const __half*)(qpk + (qv ? qh : 0) * QREC);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             S.bq[kk][0] = qv ? *(const unsigned int*)(qbh + 16 * kk + 2 * tq) : 0u;
             S.bq[kk][1] = qv ? *(const unsigned int*)(qbh + 16 * kk + 8 + 2 * tq) : 0u;
+            if constexpr (CB) {
+              const __half* q2 = qbh + QPACK_CB_QB / 2;
+              X.bq2[kk][0] = qv ? *(const unsigned int*)(q2 + 16 * kk + 2 * tq) : 0u;
+              X.bq2[kk][1] = qv ? *(const unsigned int*)(q2 + 16 * kk + 8 + 2 * tq) : 0u;
+            }
           }
 #pragma unroll
           for (int hc = 0; hc < 2; ++hc) {
             const int n = PAIR ? ((2 * tq + hc) & 3) : 2 * tq + hc;
             const bool hv = n < G;
-            const uint8_t* r = qpk + (hv ? n : 0) * QPACK_BYTES;
+            const uint8_t* r = qpk + (hv ? n : 0) * QREC;
             S.m[hc] = PAIR ? -1e30f : -INFINITY;
             S.l[hc] = 0.f;
-            const float al = hv ? *(const float*)(r + QPACK_ALPHA) : 0.f;
+            const float al = hv ? *(const float*)(r + O_ALPHA) : 0.f;
             S.ka[hc] = al;
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
               float qs = 0.f, ps = 0.f;
 #pragma unroll
               for (int k = gr * (4 / NG); k < (gr + 1) * (4 / NG); ++k) {
-                qs += hv ? ((const float*)(r + QPACK_QSUM))[k] : 0.f;
-                ps += hv ? ((const float*)(r + QPACK_PSUM))[k] : 0.f;
+                qs += hv ? ((const float*)(r + O_QSUM))[k] : 0.f;
+                ps += hv ? ((const float*)(r + O_PSUM))[k] : 0.f;
               }
               S.bs[hc][gr] = 0.f;
               S.zs[hc][gr] = 0.f;
-              S.kb[hc][gr] = -1024.f * qs * al;
+              S.kb[hc][gr] = CB ? fmaf(kc0 * ps, LOG2E * INV_SQRT_D, -1024.f * qs * al) : -1024.f * qs * al;
               S.kg[hc][gr] = ps * LOG2E * INV_SQRT_D;
             }
           }
@@ -1381,10 +1569,16 @@ __global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3) ? 3 : 2) dec
             const int pid = page_id_at(P, k);
             if (pid >= 0 && pid < cv.num_pages) {
               const int nv = (p == pages_b - 1) ? hist_b - p * PAGE : PAGE;
-              if (nv == PAGE)
+              if constexpr (CB) {
+                if (nv == PAGE)
+                  int2_page_mma_cb<NG, true>(S, X, my_stage + (size_t)st * L.stage_bytes, nv, lane);
+                else
+                  int2_page_mma_cb<NG, false>(S, X, my_stage + (size_t)st * L.stage_bytes, nv, lane);
+              } else if (nv == PAGE) {
                 int2_page_mma<NG, true>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
-              else
+              } else {
                 int2_page_mma<NG, false>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
+              }
               if ((k & 7) == 7) flush_v_offset<NG>(S);
             }
             __syncwarp();
@@ -1563,7 +1757,7 @@ ScratchLayout scratch_layout(int B, int Hq, int Hkv, int G, int max_target_items
   s.off_done = 256;
   s.off_qrot = s.off_done + up((size_t)B * Hkv * 4);
   s.off_qpack = s.off_qrot + up((size_t)B * Hq * D * 4);
-  s.off_part = s.off_qpack + up((size_t)B * Hq * QPACK_BYTES);
+  s.off_part = s.off_qpack + up((size_t)B * Hq * QPACK_CB_BYTES);  // room for codebook records
   const size_t slots = (size_t)max_target_items + 2 * (size_t)B * Hkv;
   s.total = s.off_part + slots * G * PART_STRIDE * 4;
   return s;
@@ -1600,6 +1794,7 @@ int decode_ctas_per_sm(const DecodeArgs& a) {
   if (a.bf16_history) return occupancy_t<1, 2>(a);
   if (a.impl == 1) return NG == 1 ? occupancy_t<1, 1>(a) : NG == 2 ? occupancy_t<2, 1>(a) : occupancy_t<4, 1>(a);
   if (a.impl == 3) return NG == 1 ? occupancy_t<1, 3>(a) : NG == 2 ? occupancy_t<2, 3>(a) : occupancy_t<4, 3>(a);
+  if (a.impl == 4) return NG == 1 ? occupancy_t<1, 4>(a) : NG == 2 ? occupancy_t<2, 4>(a) : occupancy_t<4, 4>(a);
   return NG == 1 ? occupancy_t<1, 0>(a) : NG == 2 ? occupancy_t<2, 0>(a) : occupancy_t<4, 0>(a);
 }
 
@@ -1617,6 +1812,10 @@ cudaError_t launch_decode_after_prep(const DecodeArgs& a, int grid, cudaStream_t
     if (cv.NG == 1) e = launch_decode_t<1, 3>(a, grid, st);
     else if (cv.NG == 2) e = launch_decode_t<2, 3>(a, grid, st);
     else e = launch_decode_t<4, 3>(a, grid, st);
+  } else if (a.impl == 4) {
+    if (cv.NG == 1) e = launch_decode_t<1, 4>(a, grid, st);
+    else if (cv.NG == 2) e = launch_decode_t<2, 4>(a, grid, st);
+    else e = launch_decode_t<4, 4>(a, grid, st);
   } else {
     if (cv.NG == 1) e = launch_decode_t<1, 0>(a, grid, st);
     else if (cv.NG == 2) e = launch_decode_t<2, 0>(a, grid, st);

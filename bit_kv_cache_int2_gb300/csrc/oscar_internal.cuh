@@ -25,6 +25,13 @@ constexpr int PART_STRIDE = D + 4;  // partial record per head: m, l, 2 pad, o[1
 constexpr int PART_O = 4;            // offset of o in a partial record
 constexpr int MAX_TARGET_ITEMS = 2048;
 constexpr int QPACK_BYTES = 320;  // packed query record per (request, query head)
+constexpr int QPACK_CB_BYTES = 576;  // the same with a Lloyd-Max codebook (two B operands)
+// Per-head codebook record (floats): the levels of the normalised value t are
+// {1.5-b, 1.5-a, 1.5+a, 1.5+b}; a code is [t > lo] + [t >= 1.5] + [t > hi]
+// with lo/hi = 1.5 -/+ (a+b)/2; c0, alpha = b - a and beta_half = (a + b)/2
+// give level(code) = c0 + alpha*bit0 + 2*beta_half*bit1.  Uniform: a = 0.5, b = 1.5.
+constexpr int CB_WORDS = 8;
+enum { CB_A = 0, CB_B, CB_LO, CB_HI, CB_C0, CB_ALPHA, CB_BETA_HALF };
 constexpr int WIN_BYTES_PER_HEAD = (SINK + RECENT) * D * 2 * 2;  // K and V
 constexpr int BF16_HEAD_BYTES = PAGE * D * 2 * 2;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -58,6 +65,7 @@ struct LayerRot {
   const float* RVt;         // [Hkv][128][128]  R_V^T, row i = column i of R_V (coalesced un-rotation)
   const float* clip_k;      // [Hkv]
   const float* clip_v;      // [Hkv]
+  const float* cb;          // [2][Hkv][CB_WORDS] codebook records, K then V
   int mode;
 };
 
@@ -137,12 +145,25 @@ __device__ __forceinline__ QParams quant_params(float mn, float mx, float clip) 
   return p;
 }
 
-__device__ __forceinline__ uint32_t quant_code(float x, QParams p) {
+// Thresholds of the codes on t = (x - z)/s: the nearest of the four levels,
+// ties to the even code.  For the uniform levels {0, 1, 2, 3} (lo = 0.5,
+// hi = 2.5) this is clamp(rint(t), 0, 3) for every float t.
+struct QThr {
+  float lo, hi;
+};
+
+__device__ __forceinline__ QThr quant_thr(const float* cb_rec) {
+  QThr q;
+  q.lo = __ldg(cb_rec + CB_LO);
+  q.hi = __ldg(cb_rec + CB_HI);
+  return q;
+}
+
+__device__ __forceinline__ uint32_t quant_code(float x, QParams p, QThr th) {
   const float sf = __half2float(p.s);
   if (sf == 0.f) return 0u;
   const float t = __fdiv_rn(__fsub_rn(x, __half2float(p.z)), sf);
-  const float r = fminf(fmaxf(rintf(t), 0.f), 3.f);
-  return (uint32_t)r;
+  return (uint32_t)(t > th.lo) + (uint32_t)(t >= 1.5f) + (uint32_t)(t > th.hi);
 }
 
 // min and max over each group of g consecutive channels (g = 32, 64, 128),
@@ -233,6 +254,17 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t w) {
                          : (I == 1 || I == 3 || I == 6) ? 0x00C000C0u
                                                         : 0x03000300u;
   // w << 4 as a multiply (FMA pipe), w >> 6 as a shift
+  const uint32_t src = (I <= 1) ? (w * 16u) : (I <= 4) ? w : (w >> 6);
+  return and_or(src, M, 0x64006400u);
+}
+// One bit of each of the two codes code_pair<I> takes: bit plane P (0 = low
+// bit, 1 = high bit) as 1024 + bit * 2^(E + P) in each fp16 half.
+template <int I, int P>
+__device__ __forceinline__ uint32_t code_plane(uint32_t w) {
+  constexpr uint32_t M = ((I == 0 || I == 2 || I == 5) ? 0x00300030u
+                          : (I == 1 || I == 3 || I == 6) ? 0x00C000C0u
+                                                         : 0x03000300u) &
+                         (P ? 0xAAAAAAAAu : 0x55555555u);
   const uint32_t src = (I <= 1) ? (w * 16u) : (I <= 4) ? w : (w >> 6);
   return and_or(src, M, 0x64006400u);
 }
@@ -449,7 +481,8 @@ struct DecodeArgs {
   int* done;               // scratch [B][Hkv] finished-item counters
   int B;
   int target_items;
-  int impl;  // decode kernel variant: 0 tensor-core, 1 CUDA-core, 3 tensor-core page pairs
+  int impl;  // decode kernel variant: 0 tensor-core, 1 CUDA-core, 3 tensor-core page pairs,
+             // 4 tensor-core with a Lloyd-Max codebook
   int bf16_history;
   int merge_hpc;  // query heads per merge CTA (divides G)
   LayerRot rot;
@@ -463,6 +496,11 @@ struct DecodeArgs {
 // A group of g channels takes its logit offset -1024 * alpha * (sum of qb) and
 // its zero-point weight (sum of q') * log2(e) / sqrt(d) from g / 32 quarters.
 constexpr int QPACK_ALPHA = 256, QPACK_QSUM = 260, QPACK_PSUM = 276;
+// With a Lloyd-Max codebook (decode variant 4) the record is QPACK_CB_BYTES:
+//   half  qa[128]   q'_c * 2^-sigma * 2^(8 - E(c)) * alpha_K   (low code bit)
+//   half  qb[128]   the same times beta_half_K                  (high code bit)
+//   float alpha, float qsum[4] (sums of qa + qb), float psum[4] as above.
+constexpr int QPACK_CB_QB = 256, QPACK_CB_ALPHA = 512, QPACK_CB_QSUM = 516, QPACK_CB_PSUM = 532;
 
 struct PrepSmem {
   float xs[MAX_G][D];
@@ -538,19 +576,32 @@ __device__ __forceinline__ void prep_body(const DecodeArgs& a, int bk, int cq, i
     int ex = 0;
     frexpf(am, &ex);
     const int sig = am > 0.f ? ex - 10 : 0;
-    const __half hb = __float2half_rn(ldexpf(y, -sig) * f);
-    uint8_t* rec = a.qpack + row * QPACK_BYTES;
-    ((__half*)rec)[c] = hb;
-    float bs = __half2float(hb), ps = y;
+    const float yq = ldexpf(y, -sig) * f;
+    const bool cbrec = a.impl == 4;
+    uint8_t* rec = a.qpack + row * (cbrec ? QPACK_CB_BYTES : QPACK_BYTES);
+    float bs, ps = y;
+    if (!cbrec) {
+      const __half hb = __float2half_rn(yq);
+      ((__half*)rec)[c] = hb;
+      bs = __half2float(hb);
+    } else {
+      const float* cbk = a.rot.cb + (size_t)kvh * CB_WORDS;
+      const __half ha = __float2half_rn(yq * __ldg(cbk + CB_ALPHA));
+      const __half hb = __float2half_rn(yq * __ldg(cbk + CB_BETA_HALF));
+      ((__half*)rec)[c] = ha;
+      ((__half*)(rec + QPACK_CB_QB))[c] = hb;
+      bs = __half2float(ha) + __half2float(hb);
+    }
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
       bs += __shfl_xor_sync(0xffffffffu, bs, o);
       ps += __shfl_xor_sync(0xffffffffu, ps, o);
     }
     if (lane == 0) {
-      ((float*)(rec + QPACK_QSUM))[cq] = bs;
-      ((float*)(rec + QPACK_PSUM))[cq] = ps;
-      if (cq == 0) *(float*)(rec + QPACK_ALPHA) = ldexpf(1.f, sig) * LOG2E * INV_SQRT_D * (1.f / 256.f);
+      ((float*)(rec + (cbrec ? QPACK_CB_QSUM : QPACK_QSUM)))[cq] = bs;
+      ((float*)(rec + (cbrec ? QPACK_CB_PSUM : QPACK_PSUM)))[cq] = ps;
+      if (cq == 0)
+        *(float*)(rec + (cbrec ? QPACK_CB_ALPHA : QPACK_ALPHA)) = ldexpf(1.f, sig) * LOG2E * INV_SQRT_D * (1.f / 256.f);
     }
   }
 }
@@ -612,9 +663,17 @@ cudaError_t calib_covariances(const __nv_bfloat16* Q, const __nv_bfloat16* K, co
 // host memory; synchronises st.  OSCAR_ERR_UNSUPPORTED when cuSOLVER is absent.
 oscar_status calib_eigh(const double* dC, double* evec_host, cudaStream_t st, int* cuda_err);  // process-wide solver state
 // Key and value clip errors of M candidate ratios into scratch (fp64 [2][M] at off_err).
+// cb_k, cb_v: the head's codebook records (device), applied by the quantiser.
 cudaError_t calib_clip_errors(const float* R_K, const float* R_V, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                               const __nv_bfloat16* V, int G, int N, int g, const float* clips_host, int M,
-                              uint8_t* scratch, cudaStream_t st);
+                              const float* cb_k, const float* cb_v, uint8_t* scratch, cudaStream_t st);
+// Lloyd-Max codebook of one (kv head, K or V) from N calibration rows X
+// rotated by R: folded values into scratch, then the two-level iteration.
+// Scratch: codebook_scratch_bytes(N).  ab_host receives (a, b) as doubles and
+// updates_host the number of centroid updates; synchronises st.
+size_t codebook_scratch_bytes(int N);
+cudaError_t calib_fit_codebook(const float* R, const __nv_bfloat16* X, int N, int g, float clip, int max_iters,
+                               uint8_t* scratch, double* ab_host, int* updates_host, cudaStream_t st);
 
 cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* k,
                           const __nv_bfloat16* v, int B, int do_append, int* req_counter,
@@ -630,8 +689,8 @@ cudaError_t launch_append_bf16(const CacheView& cv, const __nv_bfloat16* k, cons
 cudaError_t launch_import(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* K,
                           const __nv_bfloat16* V, int B, int n, int bf16_history,
                           cudaStream_t st, Profiler* prof);
-cudaError_t launch_quantize_hook(const float* x, int n, int g, float clip, int which,
-                                 uint8_t* codes, __half2* sz, cudaStream_t st);
+cudaError_t launch_quantize_hook(const float* x, int n, int g, float clip, int which, float thr_lo,
+                                 float thr_hi, uint8_t* codes, __half2* sz, cudaStream_t st);
 cudaError_t launch_debug_rotate(const float* R, const __nv_bfloat16* x, float* y, int n,
                                 cudaStream_t st);
 

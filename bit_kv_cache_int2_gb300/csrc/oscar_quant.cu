@@ -17,13 +17,13 @@ namespace {
 // code in a K row (kw: 8 words of smem, zeroed) or in a V block word in smem
 // (vblk: 512 words, channel-major, zeroed) for token row t.  Writes (s, z)
 // through sz_out (token row t of an [64][NG] half2 array) for the group leader.
-__device__ __forceinline__ void quant_pack(float y, int j, int g, float clip, float* red, int bar,
+__device__ __forceinline__ void quant_pack(float y, int j, int g, float clip, QThr th, float* red, int bar,
                                            bool is_v, int t, uint32_t* kw, uint32_t* vblk,
                                            __half2* sz_row) {
   float mn, mx;
   group_minmax(y, j, g, red, bar, mn, mx);
   const QParams qp = quant_params(mn, mx, clip);
-  const uint32_t code = quant_code(y, qp);
+  const uint32_t code = quant_code(y, qp, th);
   if (!is_v) {
     atomicOr(&kw[k_word(j)], code << k_bit(j));
   } else {
@@ -34,13 +34,13 @@ __device__ __forceinline__ void quant_pack(float y, int j, int g, float clip, fl
 
 // Same, but writing a single token's V code straight into a V block in global
 // memory with a read-modify-write of the owning word (one writer per word).
-__device__ __forceinline__ void quant_store_v_global(float y, int j, int g, float clip, float* red,
+__device__ __forceinline__ void quant_store_v_global(float y, int j, int g, float clip, QThr th, float* red,
                                                      int bar, int t, uint32_t* vblk_g,
                                                      __half2* sz_row) {
   float mn, mx;
   group_minmax(y, j, g, red, bar, mn, mx);
   const QParams qp = quant_params(mn, mx, clip);
-  const uint32_t code = quant_code(y, qp);
+  const uint32_t code = quant_code(y, qp, th);
   uint32_t* wp = vblk_g + j * 4 + v_word(t);
   const uint32_t sh = (uint32_t)v_bit(t);
   *wp = (*wp & ~(3u << sh)) | (code << sh);
@@ -124,15 +124,16 @@ __device__ __forceinline__ void append_body(const CacheView& cv, const LayerRot&
     if (pp == 0) {
       const float y = (part[0][j] + part[1][j]) + (part[2][j] + part[3][j]);
       const float clip = (isv ? rot.clip_v : rot.clip_k)[h];
+      const QThr th = quant_thr(rot.cb + (size_t)(isv * cv.Hkv + h) * CB_WORDS);
       uint8_t* blk = cv.pool + (size_t)page * cv.page_bytes + (size_t)h * cv.head_bytes;
       const int tr = H % PAGE;
       if (!isv) {
-        quant_pack(y, j, cv.g, clip, red, 1, false, tr, kw, nullptr,
+        quant_pack(y, j, cv.g, clip, th, red, 1, false, tr, kw, nullptr,
                    (__half2*)(blk + off_k_sz()) + tr * cv.NG);
         group_sync(1);
         if (t < 8) ((uint32_t*)(blk + tr * 32))[t] = kw[t];
       } else {
-        quant_store_v_global(y, j, cv.g, clip, red, 1, tr, (uint32_t*)(blk + 2048),
+        quant_store_v_global(y, j, cv.g, clip, th, red, 1, tr, (uint32_t*)(blk + 2048),
                              (__half2*)(blk + off_v_sz(cv.g)) + tr * cv.NG);
       }
     }
@@ -274,6 +275,7 @@ __global__ void __launch_bounds__(256) import_int2_pages_kernel(CacheView cv, La
   const __nv_bfloat16* src = (grp == 0 ? K : V) + (head * (size_t)n + SINK + t0) * D;
   const float* R = (grp == 0 ? rot.R_K : rot.R_V) + (size_t)h * D * D;
   const float clip = (grp == 0 ? rot.clip_k : rot.clip_v)[h];
+  const QThr th = quant_thr(rot.cb + (size_t)(grp * cv.Hkv + h) * CB_WORDS);
   __syncthreads();
   for (int tb = 0; tb < nt; tb += IMP_NT) {
     const int cnt = (nt - tb) < IMP_NT ? nt - tb : IMP_NT;
@@ -291,7 +293,7 @@ __global__ void __launch_bounds__(256) import_int2_pages_kernel(CacheView cv, La
     for (int k = 0; k < cnt; ++k) {
       const float y = acc[k];
       const int t = tb + k;
-      quant_pack(y, j, cv.g, clip, red[grp], bar, grp == 1, t, kwords + t * 8, vwords,
+      quant_pack(y, j, cv.g, clip, th, red[grp], bar, grp == 1, t, kwords + t * 8, vwords,
                  &szs[grp][t * cv.NG]);
     }
     group_sync(bar);
@@ -383,7 +385,7 @@ __global__ void import_set_lengths_kernel(int32_t* seq, int32_t* hist, int B, in
 // --------------------------------------------------------------- test hooks
 // grid = ceil(n / 64), block 128: each CTA quantises up to 64 rotated vectors.
 __global__ void __launch_bounds__(128) quantize_hook_kernel(const float* __restrict__ x, int n,
-                                                            int g, float clip, int which,
+                                                            int g, float clip, QThr th, int which,
                                                             uint8_t* __restrict__ codes,
                                                             __half2* __restrict__ sz) {
   __shared__ float red[8];
@@ -398,7 +400,7 @@ __global__ void __launch_bounds__(128) quantize_hook_kernel(const float* __restr
   __syncthreads();
   for (int t = 0; t < cnt; ++t) {
     const float y = x[(size_t)(i0 + t) * D + j];
-    quant_pack(y, j, g, clip, red, 1, which == 1, t, kwords + t * 8, vwords,
+    quant_pack(y, j, g, clip, th, red, 1, which == 1, t, kwords + t * 8, vwords,
                sz + (size_t)(i0 + t) * NG);
   }
   __syncthreads();
@@ -476,9 +478,12 @@ cudaError_t launch_import(const CacheView& cv, const LayerRot& rot, const __nv_b
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_hook(const float* x, int n, int g, float clip, int which,
-                                 uint8_t* codes, __half2* sz, cudaStream_t st) {
-  quantize_hook_kernel<<<(n + PAGE - 1) / PAGE, 128, 0, st>>>(x, n, g, clip, which, codes, sz);
+cudaError_t launch_quantize_hook(const float* x, int n, int g, float clip, int which, float thr_lo,
+                                 float thr_hi, uint8_t* codes, __half2* sz, cudaStream_t st) {
+  QThr th;
+  th.lo = thr_lo;
+  th.hi = thr_hi;
+  quantize_hook_kernel<<<(n + PAGE - 1) / PAGE, 128, 0, st>>>(x, n, g, clip, th, which, codes, sz);
   return cudaGetLastError();
 }
 

@@ -29,6 +29,8 @@ ERR_CUDA = 6
 ERR_STATE = 7
 ERR_TOO_LARGE = 8
 NOALLOC_SCRATCH_BYTES = 8 << 20
+CODEBOOK_MAX_ROWS = 1 << 20
+UNIFORM_CODEBOOK = (0.5, 1.5)  # (a, b) of the levels {0, 1, 2, 3}
 
 ROT_OSCAR = 0
 ROT_HADAMARD = 1
@@ -120,6 +122,15 @@ _SIGS = {
                            ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                            ctypes.c_void_p], ctypes.c_int),
+    "oscar_set_codebook": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
+                           ctypes.c_int),
+    "oscar_codebook_scratch_bytes": ([ctypes.c_int], ctypes.c_size_t),
+    "oscar_fit_codebook": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                            ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                            ctypes.POINTER(ctypes.c_int), ctypes.c_void_p], ctypes.c_int),
+    "oscar_quantize_codebook_f32": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                     ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
+                                    ctypes.c_int),
     "oscar_profile_enable": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "oscar_profile_read": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                             ctypes.POINTER(ctypes.c_double), ctypes.c_int], ctypes.c_int),
@@ -310,6 +321,39 @@ def oscar_clip_errors(ctx, layer, kv_head, Q, K, V, N, ratios, scratch, stream=N
     return ek, ev, bk.value, bv.value
 
 
+def oscar_set_codebook(ctx, layer, k_ab=None, v_ab=None, stream=None):
+    """Lloyd-Max codebooks of a layer: k_ab, v_ab [Hkv][2] (a, b) pairs, or
+    None for the uniform levels."""
+    import numpy as np
+
+    k = None if k_ab is None else np.ascontiguousarray(k_ab, dtype=np.float32)
+    v = None if v_ab is None else np.ascontiguousarray(v_ab, dtype=np.float32)
+    _check(lib().oscar_set_codebook(ctx, layer, None if k is None else _np_ptr(k), None if v is None else _np_ptr(v),
+                                    _stream(stream)), "oscar_set_codebook")
+
+
+def codebook_scratch(N, device="cuda"):
+    import torch
+
+    n = lib().oscar_codebook_scratch_bytes(N)
+    if n == 0:
+        raise OscarError(ERR_INVALID_ARG, "codebook_scratch")
+    return torch.empty((n + 255) // 256 * 256, dtype=torch.uint8, device=device)
+
+
+def oscar_fit_codebook(ctx, layer, kv_head, which, X, N, scratch, max_iters=100, stream=None):
+    """Lloyd-Max fit of one (layer, kv head) for keys (which=0) or values
+    (which=1).  Returns (a, b, updates)."""
+    import numpy as np
+
+    ab = np.zeros(2, dtype=np.float32)
+    up = ctypes.c_int(0)
+    _check(lib().oscar_fit_codebook(ctx, layer, kv_head, which, _ptr(X), N, max_iters, _ptr(scratch),
+                                    scratch.numel() * scratch.element_size(), _np_ptr(ab), ctypes.byref(up),
+                                    _stream(stream)), "oscar_fit_codebook")
+    return float(ab[0]), float(ab[1]), up.value
+
+
 def oscar_prefill(ctx, layer, cache: dict, q, k, v, T, out, lse, scratch, batch, stream=None):
     """Chunked prefill: T new tokens per request attend to the cache and
     causally to each other (the chunk is not stored)."""
@@ -396,6 +440,11 @@ def oscar_import_bf16_history(ctx, cache: dict, K, V, batch, n, stream=None):
 def oscar_quantize_rotated_f32(x, group_size, clip, which, codes, sz, stream=None):
     _check(lib().oscar_quantize_rotated_f32(_ptr(x), x.shape[0], group_size, float(clip), which, _ptr(codes),
                                             _ptr(sz), _stream(stream)), "oscar_quantize_rotated_f32")
+
+
+def oscar_quantize_codebook_f32(x, group_size, clip, a, b, which, codes, sz, stream=None):
+    _check(lib().oscar_quantize_codebook_f32(_ptr(x), x.shape[0], group_size, float(clip), float(a), float(b), which,
+                                             _ptr(codes), _ptr(sz), _stream(stream)), "oscar_quantize_codebook_f32")
 
 
 def oscar_debug_rotate(ctx, layer, which, kv_head, x, x_rot, stream=None):

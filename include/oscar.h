@@ -108,6 +108,8 @@ typedef enum {
   OSCAR_DECODE_CUDA_CORE = 1,     /* fp32 CUDA cores, one page per warp at a time */
   OSCAR_DECODE_TENSOR_SINGLE = 2  /* tensor cores, one page per tile at any group size */
 } oscar_decode_impl;
+/* (A layer with a Lloyd-Max codebook, oscar_set_codebook, always decodes with
+ * the codebook kernel: tensor cores, one page per tile.) */
 
 /* Prefill attention kernels (oscar_prefill). */
 typedef enum {
@@ -289,7 +291,8 @@ oscar_status oscar_decode_step(oscar_ctx* ctx, int layer, const oscar_cache* cac
  *             bytes, 256-byte aligned, no initial contents needed; not to be
  *             shared by calls that may overlap.
  * q, k, v, out 16-byte aligned.  Returns OSCAR_ERR_INVALID_ARG for T outside
- * 1..64.  Device errors as oscar_decode (OSCAR_ERR_NO_PAGE / OSCAR_ERR_RANGE
+ * 1..64 and OSCAR_ERR_UNSUPPORTED on a layer with a non-uniform Lloyd-Max
+ * codebook (oscar_set_codebook).  Device errors as oscar_decode (OSCAR_ERR_NO_PAGE / OSCAR_ERR_RANGE
  * for a bad history page, whose tokens are then left out). */
 oscar_status oscar_prefill(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* q,
                            const void* k, const void* v, int T, void* out, float* lse,
@@ -339,6 +342,55 @@ oscar_status oscar_clip_errors(oscar_ctx* ctx, int layer, int kv_head, const voi
                                const void* V, int N, const float* ratios, int M, double* err_k,
                                double* err_v, int* best_k, int* best_v, void* scratch,
                                size_t scratch_bytes, oscar_stream_t stream);
+
+/* Lloyd-Max codebook [Blog, closing paragraph on TurboQuant: the released
+ * code pairs the attention-aware rotation with a Lloyd-Max codebook; the
+ * pages give no formula, so the following is the library's reading].
+ * A group keeps the uniform quantiser's fp16 scale s and zero point z and its
+ * normalised value t = (x - z)/s (fp32); only the four values t is rounded to
+ * change.  They are symmetric about 1.5,
+ *   level(code) = {1.5 - b, 1.5 - a, 1.5 + a, 1.5 + b},  0 <= a < b <= 3,
+ * and x_hat = level(code)·s + z.  A code is the nearest level, ties to the
+ * even code: code = [t > 1.5 - m] + [t >= 1.5] + [t > 1.5 + m], m = (a + b)/2
+ * in fp32.  (a, b) = (0.5, 1.5) is the uniform quantiser exactly. */
+#define OSCAR_CODEBOOK_MAX_ROWS (1 << 20)
+
+/* Sets the codebooks of one layer, per kv head, for keys and for values:
+ *   k_ab, v_ab : host float [num_kv_heads][2] = (a, b) pairs, or NULL for the
+ *                uniform levels (0.5, 1.5) on that side.
+ * From then on the demotion, the bulk import, oscar_clip_errors and the decode
+ * of this layer use them.  While any head of the layer has a non-uniform
+ * codebook the decode runs the codebook kernel (two tensor-core products per
+ * operand, whatever OSCAR_OPT_DECODE_IMPL says) and oscar_prefill on the layer
+ * returns OSCAR_ERR_UNSUPPORTED.  Codes already in the cache are not
+ * re-quantised: set the codebook before the layer's tokens are written.
+ * OSCAR_ERR_INVALID_ARG if a pair is outside 0 <= a < b <= 3 or not finite
+ * (nothing is changed then).  Synchronises `stream`. */
+oscar_status oscar_set_codebook(oscar_ctx* ctx, int layer, const float* k_ab, const float* v_ab,
+                                oscar_stream_t stream);
+
+/* Fits the codebook of one (layer, kv head) for keys (which = 0) or values
+ * (which = 1) by Lloyd-Max: the N calibration rows are rotated by the layer's
+ * R_K or R_V (x' = x·R, fp32) and every group is normalised to t at the
+ * head's clip ratio (groups with a zero scale are left out); with the folded
+ * value f = |t - 1.5| the two levels alternate between a = mean of f <= m and
+ * b = mean of f > m, m = (a + b)/2 (fp64), from (0.5, 1.5) until the inner
+ * cell's count repeats or max_iters updates ran.  The layer's codebook is not
+ * changed (pass the result to oscar_set_codebook; b above 3 is refused there).
+ *   X : device bf16 [N][128], 1 <= N <= OSCAR_CODEBOOK_MAX_ROWS
+ *   scratch : device, 256-byte aligned, at least oscar_codebook_scratch_bytes(N)
+ *   ab : host float [2] out = (a, b);  updates : host int out (or NULL), the
+ *        number of centroid updates.
+ * Synchronises `stream`. */
+size_t oscar_codebook_scratch_bytes(int N);
+oscar_status oscar_fit_codebook(oscar_ctx* ctx, int layer, int kv_head, int which, const void* X, int N,
+                                int max_iters, void* scratch, size_t scratch_bytes, float* ab, int* updates,
+                                oscar_stream_t stream);
+
+/* Test hook: the demotion's quantiser with codebook (a, b) on given rotated
+ * fp32 vectors; arguments and layouts as oscar_quantize_rotated_f32. */
+oscar_status oscar_quantize_codebook_f32(const float* x, int n, int group_size, float clip, float a, float b,
+                                         int which, uint8_t* codes, void* sz, oscar_stream_t stream);
 
 /* Decode without any device allocation (the pages have no counterpart: this
  * is a deployment convenience of this library).  Same computation, arguments

@@ -29,6 +29,14 @@ class Scenario:
     V: list
     stats: list  # per kv head HeadStats
     bf16_history: bool = False
+    codebook: tuple = None  # (k_ab, v_ab), each [Hkv][2] (a, b), or None (uniform levels)
+
+    def cb(self, which, h):
+        """(a, b) of kv head h for "k" or "v", None for the uniform quantiser."""
+        if self.codebook is None:
+            return None
+        ab = self.codebook[0 if which == "k" else 1]
+        return None if ab is None else (float(np.float32(ab[h][0])), float(np.float32(ab[h][1])))
 
     @property
     def B(self):
@@ -60,7 +68,7 @@ def calibrate_heads(base, wl, layer, Hkv, G, stats, calib_n=2048):
 
 def build(wl: str, lengths, Hq=4, Hkv=1, g=128, clip_k=0.95, clip_v=0.95, n_out=4, f_key=20.0,
           seed=0, interleave=False, mode=oscar.ROT_OSCAR, extra_tokens=0, calib_n=2048,
-          bf16_history=False, device="cuda", spare_pages=2, U=None) -> Scenario:
+          bf16_history=False, device="cuda", spare_pages=2, U=None, codebook=None) -> Scenario:
     """Import every request's prefix (lengths[b] tokens) into a fresh cache.
 
     extra_tokens: how many more tokens per request to draw (for later appends)."""
@@ -82,6 +90,8 @@ def build(wl: str, lengths, Hq=4, Hkv=1, g=128, clip_k=0.95, clip_v=0.95, n_out=
     else:
         U_K, U_V = U
     oscar.oscar_set_rotation(ctx, 0, U_K, U_V, [clip_k] * Hkv, [clip_v] * Hkv, mode)
+    if codebook is not None:
+        oscar.oscar_set_codebook(ctx, 0, codebook[0], codebook[1])
     cache = oscar.alloc_cache(cfg, device, bf16_history=bf16_history)
     pt = synth.page_table(num_pages, pages_per_req, synth.stream_seed(seed, wl, "pages"), interleave, mpr)
     cache["page_table"].copy_(pt.to(device))
@@ -104,7 +114,7 @@ def build(wl: str, lengths, Hq=4, Hkv=1, g=128, clip_k=0.95, clip_v=0.95, n_out=
                 oscar.oscar_import_tokens(ctx, 0, view, kin, vin, 1, L)
     torch.cuda.synchronize()
     return Scenario(cfg, ctx, cache, list(lengths), Hq, Hkv, g, U_K, U_V, clip_k, clip_v, mode, Ks, Vs,
-                    stats, bf16_history)
+                    stats, bf16_history, codebook)
 
 
 def queries(sc: Scenario, seed=0, tag="Q"):
@@ -197,8 +207,12 @@ def oracle_decode(sc: Scenario, hc: HostCache, q_np, b):
             if f is None:
                 hk = hv = np.zeros((0, 128))
             else:
-                hk = O.dequantize(f["k_codes"], f["k_s"], f["k_z"], sc.g)
-                hv = O.dequantize(f["v_codes"], f["v_s"], f["v_z"], sc.g)
+                cbf = getattr(sc, "cb", None)  # views without codebooks use the uniform levels
+                ck, cv = (cbf("k", h), cbf("v", h)) if cbf else (None, None)
+                hk = (O.dequantize(f["k_codes"], f["k_s"], f["k_z"], sc.g) if ck is None
+                      else O.dequantize_codebook(f["k_codes"], f["k_s"], f["k_z"], sc.g, *ck))
+                hv = (O.dequantize(f["v_codes"], f["v_s"], f["v_z"], sc.g) if cv is None
+                      else O.dequantize_codebook(f["v_codes"], f["v_s"], f["v_z"], sc.g, *cv))
             o, l = O.three_region_attention(qg, wk, wv, hk, hv, O.rotation(sc.U_K[h], sc.mode),
                                             O.rotation(sc.U_V[h], sc.mode))
         outs.append(o)
@@ -217,8 +231,12 @@ def expected_codes(sc: Scenario, b, h, positions, which):
     ng = 128 // sc.g
     s = np.zeros((len(positions), ng), dtype=np.float16)
     z = np.zeros((len(positions), ng), dtype=np.float16)
+    cb = sc.cb(which, h)
     for i in range(len(positions)):
-        codes[i], s[i], z[i] = O.quantize_vector(xr[i], sc.g, clip)
+        if cb is None:
+            codes[i], s[i], z[i] = O.quantize_vector(xr[i], sc.g, clip)
+        else:
+            codes[i], s[i], z[i] = O.quantize_vector_codebook(xr[i], sc.g, clip, *cb)
     return xr, codes, s, z
 
 
@@ -229,6 +247,7 @@ def compare_history(sc: Scenario, hc: HostCache, b, h, positions, hist_slots):
     n_codes = 0
     n_bad = 0
     for which in ("k", "v"):
+        cb = sc.cb(which, h)
         xr, codes, s, z = expected_codes(sc, b, h, positions, which)
         gc = f[which + "_codes"][hist_slots]
         gs = f[which + "_s"][hist_slots]
@@ -263,6 +282,10 @@ def compare_history(sc: Scenario, hc: HostCache, b, h, positions, hist_slots):
                 continue  # explained by its group's scale / zero differing by an ulp
             sf, zf = np.float32(s[i, gr]), np.float32(z[i, gr])
             t = (float(xr[i, c]) - float(zf)) / float(sf)
-            frac = t - np.floor(t)
-            assert abs(frac - 0.5) < 1e-4 or abs(t - 3.5) < 1e-4, (which, i, c, t, gc[i, c], codes[i, c])
+            if cb is None:
+                frac = t - np.floor(t)
+                assert abs(frac - 0.5) < 1e-4 or abs(t - 3.5) < 1e-4, (which, i, c, t, gc[i, c], codes[i, c])
+            else:  # next to one of the codebook's thresholds
+                lo, hi = O.codebook_thresholds(*cb)
+                assert min(abs(t - float(lo)), abs(t - 1.5), abs(t - float(hi))) < 1e-4, (which, i, c, t)
     return n_codes, n_bad

@@ -93,6 +93,15 @@ def test_null_and_bad_arguments_rejected_on_host(lib):
     assert L.oscar_quantize_rotated_f32(fake, 64, 128, 1.5, 1, fake, fake, None) == oscar.ERR_INVALID_ARG
     assert L.oscar_quantize_rotated_f32(fake, 64, 128, 0.0, 0, fake, fake, None) == oscar.ERR_INVALID_ARG
     assert L.oscar_quantize_rotated_f32(None, 64, 128, 1.0, 0, fake, fake, None) == oscar.ERR_INVALID_ARG
+    # codebook: pairs outside 0 <= a < b <= 3 (or not finite) are refused on the host
+    for a, b in ((0.6, 0.5), (0.5, 3.5), (-0.1, 1.0), (float("nan"), 1.0), (0.5, float("inf"))):
+        assert L.oscar_quantize_codebook_f32(fake, 64, 128, 1.0, a, b, 0, fake, fake, None) == oscar.ERR_INVALID_ARG
+    assert L.oscar_quantize_codebook_f32(fake, 64, 16, 1.0, 0.5, 1.5, 0, fake, fake, None) == oscar.ERR_UNSUPPORTED
+    assert L.oscar_set_codebook(None, 0, None, None, None) == oscar.ERR_INVALID_ARG
+    assert L.oscar_fit_codebook(None, 0, 0, 0, fake, 4, 10, fake, 1 << 20, fake, None, None) == oscar.ERR_INVALID_ARG
+    assert L.oscar_codebook_scratch_bytes(0) == 0
+    assert L.oscar_codebook_scratch_bytes(oscar.CODEBOOK_MAX_ROWS + 1) == 0
+    assert L.oscar_codebook_scratch_bytes(100) >= 100 * 128 * 4 + 24
 
 
 def test_create_without_gpu_reports_cuda_error(lib):
