@@ -64,7 +64,7 @@ struct oscar_ctx {
   int* d_req_counter = nullptr;  // [max_batch]
   int impl = 0;
   int ctas_per_sm = 4;
-  int items_per_cta = 1;
+  int items_per_cta = 0;  // 0: automatic (make_sched)
   int prefill_impl = OSCAR_PREFILL_TCGEN05;
   Profiler prof;
 };
@@ -124,7 +124,8 @@ int decode_ctas(const oscar_ctx* ctx, int batch, bool bf16_history, int layer = 
 }
 
 int target_items(const oscar_ctx* ctx, int batch, bool bf16_history, int layer = -1) {
-  int t = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, layer) * ctx->items_per_cta;
+  const int per = ctx->items_per_cta ? ctx->items_per_cta : AUTO_ITEMS_PER_CTA;
+  int t = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, layer) * per;
   if (t > MAX_TARGET_ITEMS) t = MAX_TARGET_ITEMS;
   if (t < 1) t = 1;
   return t;
@@ -318,6 +319,7 @@ oscar_status decode_args(oscar_ctx* ctx, int layer, const oscar_cache* cache, co
   while (a.merge_hpc % 2 == 0 && batch * ctx->cfg.num_kv_heads * (ctx->G / a.merge_hpc) < ctx->num_sms)
     a.merge_hpc /= 2;
   grid = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, vlayer);
+  a.resident = ctx->items_per_cta == 0 ? grid : 0;
   return OSCAR_OK;
 }
 
@@ -486,7 +488,7 @@ oscar_status oscar_set_option(oscar_ctx* ctx, int option, int value) {
       ctx->ctas_per_sm = value;
       return OSCAR_OK;
     case OSCAR_OPT_ITEMS_PER_CTA:
-      if (value < 1 || value > 8) return OSCAR_ERR_INVALID_ARG;
+      if (value < 0 || value > 8) return OSCAR_ERR_INVALID_ARG;
       ctx->items_per_cta = value;
       return OSCAR_OK;
     case OSCAR_OPT_PREFILL_IMPL:

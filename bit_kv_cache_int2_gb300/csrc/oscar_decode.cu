@@ -1052,7 +1052,7 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
   // history lengths come from earlier stream work: the work list can be
   // derived before the wait
   const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
-  const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, unit, pre, red);
+  const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
   const int pages_b = (cv.hist_lens[b] + PAGE - 1) / PAGE;
   const int nb = (pages_b + sc.S - 1) / sc.S;
   const int base = pre[b] + kvh * nb;
@@ -1280,7 +1280,7 @@ __global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3 || IMPL == 4)
   // history lengths and page tables come from earlier stream work: readable
   // before the wait on prep_kernel
   const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
-  const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, unit, pre, red);
+  const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
   const int total = sc.n_hist + sc.n_win;
   uint32_t seq = 0;  // stages consumed by this warp so far
   bool waited = false;

@@ -392,9 +392,19 @@ struct Sched {
   int win_first;    // window items are handed out before history items
 };
 
+// Automatic item sizing (resident > 0): one item per resident CTA while that
+// keeps items at most AUTO_WAVE_PAGES pages (small work: per-item start and
+// merge costs dominate); beyond that, items for up to target / resident per
+// CTA, at least AUTO_MIN_PAGES pages each, balanced through the work counter.
+constexpr int AUTO_ITEMS_PER_CTA = 4;
+constexpr int AUTO_WAVE_PAGES = 40;
+constexpr int AUTO_MIN_PAGES = 28;
+
 // pre: smem int[B + 1]; filled with Hkv * (history items of requests < b).
+// target: the most items the list may hold; resident: the decode CTAs that
+// run at once, or 0 to size items for `target` items in total.
 // Must be called by all threads of the block.
-__device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int target,
+__device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int target, int resident,
                                    int hist_item_unit_bytes, int* pre, int* red) {
   const int tid = threadIdx.x;
   // total history pages (over requests), times Hkv
@@ -409,14 +419,22 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
   __syncthreads();
   total *= Hkv;
   Sched s;
-  // small batches split each 320-token window into its 5 chunks so that no
-  // single window item outlasts the history items
-  s.wch = (5LL * B * Hkv * 4 <= target) ? 5 : 1;
-  s.n_win = B * Hkv * s.wch;
-  int th = target - s.n_win;
-  if (th < (target + 1) / 2) th = (target + 1) / 2;
-  long long S = (total + th - 1) / th;
-  if (S < 1) S = 1;
+  // items = the list size aimed for; small batches split each 320-token
+  // window into its 5 chunks so that no single window item outlasts the
+  // history items
+  auto pages_per_item = [&](int items) {
+    s.wch = (5LL * B * Hkv * 4 <= items) ? 5 : 1;
+    s.n_win = B * Hkv * s.wch;
+    int th = items - s.n_win;
+    if (th < (items + 1) / 2) th = (items + 1) / 2;
+    const long long S = (total + th - 1) / th;
+    return S < 1 ? 1LL : S;
+  };
+  long long S = pages_per_item(resident > 0 ? resident : target);
+  if (resident > 0 && S > AUTO_WAVE_PAGES) {
+    S = pages_per_item(target);
+    if (S < AUTO_MIN_PAGES) S = AUTO_MIN_PAGES;
+  }
   s.S = (int)S;
   if (tid == 0) {
     // per-request rounding can add up to B*Hkv items: grow S until they fit
@@ -481,6 +499,7 @@ struct DecodeArgs {
   int* done;               // scratch [B][Hkv] finished-item counters
   int B;
   int target_items;
+  int resident;  // resident decode CTAs for automatic item sizing, 0: fixed items per CTA
   int impl;  // decode kernel variant: 0 tensor-core, 1 CUDA-core, 3 tensor-core page pairs,
              // 4 tensor-core with a Lloyd-Max codebook
   int bf16_history;

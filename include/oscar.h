@@ -120,7 +120,9 @@ typedef enum {
 typedef enum {
   OSCAR_OPT_DECODE_IMPL = 0, /* an oscar_decode_impl value (default OSCAR_DECODE_TENSOR) */
   OSCAR_OPT_CTAS_PER_SM = 1, /* persistent decode CTAs per SM, 1..4 (default 4), capped by occupancy */
-  OSCAR_OPT_ITEMS_PER_CTA = 2, /* work items per decode CTA the scheduler aims for, 1..8 (default 1) */
+  OSCAR_OPT_ITEMS_PER_CTA = 2, /* work items per decode CTA the scheduler aims for, 1..8, or 0
+                                  (default): automatic -- one item per CTA while items stay small,
+                                  else up to 4 per CTA of at least 28 pages, balanced at run time */
   OSCAR_OPT_PREFILL_IMPL = 3 /* an oscar_prefill_impl value (default OSCAR_PREFILL_TCGEN05) */
 } oscar_option;
 
