@@ -215,6 +215,127 @@ def build_workload(wl, dev, n_copies, extra, seed=0, bf16_copies=0):
     return dict(cfg=cfg, ctx=ctx, copies=copies, K=Ks, V=Vs, q=qs, U=(UK, UV), bf=bf, bctx=bctx, stats=stats)
 
 
+BATCHED = {
+    # Qwen3-4B-shaped layer, batch 32, per-request context uniform in [8K, 32K]
+    "qwen3_4b_b32_8k_32k": dict(B=32, Hq=32, Hkv=8, g=128, lens=(8192, 32768), clip=0.95, n_out=4, f_key=20.0,
+                                bf16=False),
+    # Qwen3-32B-shaped layer (GQA 8), batch 8 at 131,072 tokens, INT2 and BF16 history
+    "qwen3_32b_b8_131k": dict(B=8, Hq=64, Hkv=8, g=128, lens=(131072, 131072), clip=0.9, n_out=8, f_key=30.0,
+                              bf16=True),
+    # one layer of the Qwen3-8B-shaped stack: batch 16 at 65,536 tokens, g = 32
+    "qwen3_8b_layer_b16_64k_g32": dict(B=16, Hq=32, Hkv=8, g=32, lens=(65536, 65536), clip=0.95, n_out=4,
+                                       f_key=20.0, bf16=False),
+}
+
+
+def batched_measurement(dev, peak, steps=120, seed=0):
+    """Decode step (append with demotion + attention) and attention alone at
+    the batched configurations, rotating over cache copies larger than 3x L2.
+    Rotations are Hadamard-only: the kernels' work does not depend on R."""
+    import numpy as np
+    import torch
+
+    from bit_kv_cache_int2_gb300 import oscar, synth
+
+    l2 = torch.cuda.get_device_properties(torch.device(dev)).L2_cache_size
+    res = {}
+    for name, c in BATCHED.items():
+        Bsz, Hq, Hkv, g = c["B"], c["Hq"], c["Hkv"], c["g"]
+        rng = np.random.default_rng(synth.stream_seed(seed, name, "lens"))
+        lens = [int(x) for x in rng.integers(c["lens"][0], c["lens"][1] + 1, Bsz)]
+        hist = [max(L - 320, 0) for L in lens]
+        per_copy = sum(algorithmic_bytes(H, L, Hkv, g) for H, L in zip(hist, lens))
+        n_copies = max(2, -(-3 * l2 // per_copy))
+        extra = steps // n_copies + 8
+        ppr = [(L + extra - 320 + 63) // 64 for L in lens]
+        mpr, npages = max(ppr), sum(ppr)
+        cfg = oscar.make_config(1, Hq, Hkv, g, max_batch=Bsz, max_pages_per_req=mpr, num_pages=npages)
+        ctx = oscar.oscar_create(cfg)
+        eye = np.stack([np.eye(128, dtype=np.float32)] * Hkv)
+        oscar.oscar_set_rotation(ctx, 0, eye, eye, [c["clip"]] * Hkv, [c["clip"]] * Hkv, oscar.ROT_HADAMARD)
+        base = oscar.alloc_cache(cfg, dev)
+        base["page_table"].copy_(synth.page_table(npages, ppr, synth.stream_seed(seed, name, "pages"), True,
+                                                  mpr).to(dev))
+        stats = [synth.head_stats(seed, name, 0, h, n_out=c["n_out"], f_key=c["f_key"]) for h in range(Hkv)]
+        bctx = oscar.oscar_create(cfg) if c["bf16"] else None
+        bbase = oscar.alloc_cache(cfg, dev, bf16_history=True) if c["bf16"] else None
+        if bbase is not None:
+            bbase["page_table"].copy_(base["page_table"])
+        knew = torch.empty(extra, Bsz, Hkv, 128, dtype=torch.bfloat16, device=dev)
+        vnew = torch.empty_like(knew)
+        for b, L in enumerate(lens):
+            K = torch.stack([synth.draw_keys(stats[h], L + extra, synth.stream_seed(seed, name, b, h, "K"), dev)
+                             for h in range(Hkv)])
+            V = torch.stack([synth.draw_values(stats[h], L + extra, synth.stream_seed(seed, name, b, h, "V"), dev)
+                             for h in range(Hkv)])
+            knew[:, b] = K[:, L:].permute(1, 0, 2)
+            vnew[:, b] = V[:, L:].permute(1, 0, 2)
+            for cache, cx, bf in ((base, ctx, False), (bbase, bctx, True)):
+                if cache is None:
+                    continue
+                view = {k: (v[b:b + 1] if k in ("page_table", "sink_k", "sink_v", "ring_k", "ring_v", "seq_lens",
+                                                "hist_lens") else v) for k, v in cache.items()}
+                Kp, Vp = K[:, :L].unsqueeze(0).contiguous(), V[:, :L].unsqueeze(0).contiguous()
+                if bf:
+                    oscar.oscar_import_bf16_history(cx, view, Kp, Vp, 1, L)
+                else:
+                    oscar.oscar_import_tokens(cx, 0, view, Kp, Vp, 1, L)
+            del K, V
+        torch.cuda.synchronize()
+        copies = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n_copies - 1)]
+        q = torch.stack([torch.cat([synth.draw_queries(stats[h], Hq // Hkv, synth.stream_seed(seed, name, "Q", b, h),
+                                                       dev) for h in range(Hkv)]) for b in range(Bsz)]).contiguous()
+        out = torch.empty_like(q)
+        scratch = oscar.alloc_scratch(cfg, dev)
+        dec = [oscar.bind_decode(ctx, 0, cc, q, out, None, scratch, Bsz) for cc in copies]
+        stp = [oscar.bind_decode_step(ctx, 0, cc, q, out, None, scratch, Bsz) for cc in copies]
+        nstep = [0] * n_copies
+        tok = Bsz * Hkv * 128 * 2
+
+        def step(i):
+            j = i % n_copies
+            stp[j](knew.data_ptr() + nstep[j] * tok, vnew.data_ptr() + nstep[j] * tok)
+            nstep[j] += 1
+
+        def timed(fn, n):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for i in range(n):
+                fn(i)
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) * 1e3 / n
+
+        for i in range(n_copies):
+            step(i)
+        us_step = timed(step, steps - n_copies)
+        for i in range(5):
+            dec[i % n_copies]()
+        us_dec = timed(lambda i: dec[i % n_copies](), 100)
+        assert oscar.oscar_get_error(ctx) == 0 and torch.isfinite(out.float()).all()
+        r = {"batch": Bsz, "q_heads": Hq, "kv_heads": Hkv, "group_size": g, "context": list(c["lens"]),
+             "tokens": sum(lens), "step_us": us_step, "decode_us": us_dec, "bytes_per_decode": per_copy,
+             "decode_hbm_gbs": per_copy / (us_dec * 1e-6) / 1e9, "decode_frac": per_copy / (us_dec * 1e-6) / 1e9 / peak,
+             "tokens_per_s": Bsz / (us_step * 1e-6), "cache_copies": n_copies}
+        del dec, stp, copies
+        if bbase is not None:
+            bcopies = [bbase, {k: v.clone() for k, v in bbase.items()}]
+            bscr = oscar.alloc_scratch(cfg, dev)
+            for i in range(3):
+                oscar.oscar_decode_bf16_history(bctx, bcopies[i % 2], q, out, None, bscr, Bsz)
+            us_bf = timed(lambda i: oscar.oscar_decode_bf16_history(bctx, bcopies[i % 2], q, out, None, bscr, Bsz), 20)
+            r["bf16_history_decode_us"] = us_bf
+            r["speedup_vs_bf16"] = us_bf / us_dec
+            del bcopies
+            oscar.oscar_destroy(bctx)
+        del base, bbase, knew, vnew
+        oscar.oscar_destroy(ctx)
+        torch.cuda.empty_cache()
+        res[name] = r
+    return res
+
+
 def synth_queries(st, T, G, b, h, dev):
     """Seeded prefill queries of KV head h of request b: [T][G][128]."""
     from bit_kv_cache_int2_gb300 import synth
@@ -706,6 +827,8 @@ def run_ours(args, wl):
                         "tensor-core products per operand (bit planes) over the same cache bytes"}
     del cb_copies, cb_base, cdec
     oscar.oscar_destroy(cctx)
+    # ---- the batched configurations (parity-test shapes), timed here too
+    batched = batched_measurement(dev, peak)
     # ---- synthetic serving loop under one KV memory budget, INT2 vs BF16 history
     serve = serving_measurement(wl, dev)
     # ---- end to end through the public API with host buffers: each step's q,
@@ -782,6 +905,7 @@ def run_ours(args, wl):
                             "kind::f16 (M=128) with Q, S, P, O in tensor memory; bound: tensor; peak = "
                             "dense bf16 burst (fp16 runs at the same rate)"},
         "serving": serve,
+        "batched": batched,
         "codebook": codebook,
         "calibration": {"kv_heads": Hkv, "tokens": N_cal, "query_heads_per_kv": G_cal, "ratios": len(ratios),
                         "calibrate_ms": (t1 - t0) * 1e3, "clip_search_ms": (t2 - t1) * 1e3,
