@@ -388,6 +388,23 @@ def bind_decode_step(ctx, layer, cache: dict, q, out, lse, scratch, batch, strea
     return call
 
 
+def bind_decode_step_ptrs(ctx, layer, cache: dict, out, lse, scratch, batch, stream=None):
+    """As bind_decode_step, with q passed per call too: returns
+    f(k_new_ptr, v_new_ptr, q_ptr) taking raw addresses (ints) of device or
+    pinned host memory."""
+    cs = _cache_struct(cache)
+    head = (ctx, layer, ctypes.byref(cs))
+    tail = (_ptr(out), _ptr(lse), _ptr(scratch), scratch.numel() * scratch.element_size(), batch, _stream(stream))
+    fn = lib().oscar_decode_step
+
+    def call(k_ptr: int, v_ptr: int, q_ptr: int):
+        _check(fn(*head, ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr), ctypes.c_void_p(q_ptr), *tail),
+               "oscar_decode_step")
+
+    call._keep = cs
+    return call
+
+
 def bind_append(ctx, layer, cache: dict, batch, stream=None):
     """oscar_append with the cache and stream marshalled once, for tight loops:
     returns f(k_new_ptr, v_new_ptr) taking raw device addresses (ints)."""

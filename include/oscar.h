@@ -31,6 +31,13 @@
  *  - Device pointers are raw CUDA device addresses; host pointers are marked
  *    "host".  BF16 and FP16 data are passed as their 16-bit patterns (void*).
  *    All arrays are dense, row-major, and must be 16-byte aligned.
+ *  - The per-step operands of the append and decode calls (k_new, v_new, q,
+ *    out, lse) may also be pinned host memory (cudaHostAlloc, or
+ *    cudaHostRegister'ed), passed by its host address: with unified addressing
+ *    the kernels read and write it in place over the host link (NVLink-C2C on
+ *    Grace), with no copy call.  Results written there are complete once the
+ *    stream has been synchronised.  Pools, page tables, windows, lengths and
+ *    scratch must be device memory.
  *  - Calls that take a stream are asynchronous on that stream (NULL = legacy
  *    default stream).  Argument errors are detected on the host and reported
  *    before anything is launched.  Errors found by a kernel (a page-table

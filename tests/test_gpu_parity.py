@@ -260,6 +260,37 @@ def test_decode_step_equals_append_then_decode():
             s_.close()
 
 
+def test_decode_step_with_pinned_host_operands():
+    """k_new, v_new, q, out and lse in pinned host memory, read and written by
+    the kernels in place, give the same cache and results, bit for bit, as
+    device buffers."""
+    lengths = [300, 1500]
+    scs = [GS.build("pinned", lengths, Hq=8, Hkv=2, g=128, extra_tokens=20, calib_n=512) for _ in range(2)]
+    try:
+        scratch = [oscar.alloc_scratch(s_.cfg) for s_ in scs]
+        for t in range(20):
+            k = torch.stack([scs[0].K[i][:, lengths[i] + t] for i in range(2)]).contiguous()
+            v = torch.stack([scs[0].V[i][:, lengths[i] + t] for i in range(2)]).contiguous()
+            q = GS.queries(scs[0], seed=500 + t)
+            out_d = torch.empty_like(q)
+            lse_d = torch.empty(2, 8, dtype=torch.float32, device="cuda")
+            oscar.oscar_decode_step(scs[0].ctx, 0, scs[0].cache, k, v, q, out_d, lse_d, scratch[0], 2)
+            kh, vh, qh = (x.cpu().pin_memory() for x in (k, v, q))
+            out_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+            lse_h = torch.empty(2, 8, dtype=torch.float32).pin_memory()
+            oscar.oscar_decode_step(scs[1].ctx, 0, scs[1].cache, kh, vh, qh, out_h, lse_h, scratch[1], 2)
+            torch.cuda.synchronize()
+            assert torch.equal(out_d.cpu(), out_h), t
+            assert torch.equal(lse_d.cpu(), lse_h), t
+        for s_ in scs:
+            assert oscar.oscar_get_error(s_.ctx) == 0
+        for key in ("pool", "sink_k", "sink_v", "ring_k", "ring_v", "seq_lens", "hist_lens"):
+            assert torch.equal(scs[0].cache[key], scs[1].cache[key]), key
+    finally:
+        for s_ in scs:
+            s_.close()
+
+
 def test_demote_then_append():
     sc = GS.build("demote", [400], Hq=4, Hkv=1, g=128, extra_tokens=10, calib_n=512)
     try:
