@@ -336,6 +336,99 @@ def batched_measurement(dev, peak, steps=120, seed=0):
     return res
 
 
+def stack_measurement(dev, peak, layers=36, Bsz=16, L=65536, g=32, steps=64, warm=3, seed=0):
+    """The Qwen3-8B-shaped decode-attention stack: `layers` layers of 32 query /
+    8 KV heads, batch 16 at 65,536 tokens, group size 32, per-layer rotations
+    calibrated on the GPU from seeded synthetic calibration sets; `steps`
+    consecutive decode steps, each running every layer's oscar_decode_step
+    (append with one demotion per request, then attention).  Steady-state
+    us per step (all layers) and HBM GB/s of the decode's algorithmic bytes."""
+    import numpy as np
+    import torch
+
+    from bit_kv_cache_int2_gb300 import oscar, synth
+
+    Hq, Hkv = 32, 8
+    G = Hq // Hkv
+    ppr = (L + warm + steps - 320 + 63) // 64
+    cfg = oscar.make_config(layers, Hq, Hkv, g, max_batch=Bsz, max_pages_per_req=ppr, num_pages=Bsz * ppr)
+    ctx = oscar.oscar_create(cfg)
+    cscr = oscar.calibration_scratch(G, 2048, 0, dev)
+    caches, calls = [], []
+    scratch = oscar.alloc_scratch(cfg, dev)
+    out = torch.empty(Bsz, Hq, 128, dtype=torch.bfloat16, device=dev)
+    n_new = warm + steps
+    knew = torch.empty(layers, n_new, Bsz, Hkv, 128, dtype=torch.bfloat16, device=dev)
+    vnew = torch.empty_like(knew)
+    qs = torch.empty(layers, n_new, Bsz, Hq, 128, dtype=torch.bfloat16, device=dev)
+    t0 = time.perf_counter()
+    for layer in range(layers):
+        stats = [synth.head_stats(seed, "stack", layer, h, n_out=4, f_key=20.0) for h in range(Hkv)]
+        UK, UV = [], []
+        for h in range(Hkv):
+            Qc, Kc, Vc = (t.to(dev).contiguous() for t in synth.calibration_set(seed, "stack", layer, h, stats[h],
+                                                                              G=G, n=2048))
+            uk, uv, _, _ = oscar.oscar_calibrate(ctx, Qc, Kc, Vc, 2048, cscr)
+            UK.append(uk)
+            UV.append(uv)
+        oscar.oscar_set_rotation(ctx, layer, np.stack(UK), np.stack(UV), [0.95] * Hkv, [0.95] * Hkv,
+                                 oscar.ROT_OSCAR)
+        cache = oscar.alloc_cache(cfg, dev)
+        cache["page_table"].copy_(synth.page_table(Bsz * ppr, [ppr] * Bsz, synth.stream_seed(seed, "stack", layer),
+                                                   True, ppr).to(dev))
+        K = torch.empty(Bsz, Hkv, L + n_new, 128, dtype=torch.bfloat16, device=dev)
+        V = torch.empty_like(K)
+        for b in range(Bsz):
+            for h in range(Hkv):
+                K[b, h] = synth.draw_keys(stats[h], L + n_new, synth.stream_seed(seed, "stack", layer, b, h, "K"), dev)
+                V[b, h] = synth.draw_values(stats[h], L + n_new, synth.stream_seed(seed, "stack", layer, b, h, "V"),
+                                            dev)
+        oscar.oscar_import_tokens(ctx, layer, cache, K[:, :, :L].contiguous(), V[:, :, :L].contiguous(), Bsz, L)
+        knew[layer] = K[:, :, L:].permute(2, 0, 1, 3)
+        vnew[layer] = V[:, :, L:].permute(2, 0, 1, 3)
+        qs[layer] = torch.stack([torch.cat([synth.draw_queries(stats[h], n_new * G, synth.stream_seed(
+            seed, "stackQ", layer, b, h), dev).view(n_new, G, 128) for h in range(Hkv)], dim=1)
+            for b in range(Bsz)], dim=1)
+        del K, V
+        caches.append(cache)
+        calls.append(oscar.bind_decode_step_ptrs(ctx, layer, cache, out, None, scratch, Bsz))
+    torch.cuda.synchronize()
+    setup_s = time.perf_counter() - t0
+    tok = Bsz * Hkv * 128 * 2
+    qb = Bsz * Hq * 128 * 2
+
+    def step(t):
+        for layer in range(layers):
+            calls[layer](knew[layer, t].data_ptr(), vnew[layer, t].data_ptr(), qs[layer, t].data_ptr())
+
+    for t in range(warm):
+        step(t)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for t in range(warm, n_new):
+        step(t)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / steps
+    assert oscar.oscar_get_error(ctx) == 0 and torch.isfinite(out.float()).all()
+    H_mid = L + warm + steps // 2 - 320
+    per_layer = Bsz * algorithmic_bytes(H_mid, L + warm + steps // 2, Hkv, g)
+    res = {"layers": layers, "batch": Bsz, "context": L, "group_size": g, "steps": steps, "us_per_step": us,
+           "us_per_layer": us / layers, "bytes_per_step": layers * per_layer,
+           "hbm_gbs": layers * per_layer / (us * 1e-6) / 1e9,
+           "frac": layers * per_layer / (us * 1e-6) / 1e9 / peak, "tokens_per_s": Bsz / (us * 1e-6),
+           "cache_gb": layers * sum(v.numel() * v.element_size() for v in caches[0].values()) / 1e9,
+           "setup_s": setup_s,
+           "note": "every step runs oscar_decode_step on each layer in turn (append with one demotion per request, "
+                   "then attention); the 36 layers' caches (~29 GB) stream from HBM each step; bytes are the "
+                   "decode's algorithmic bytes at the mid-run length"}
+    del caches, calls, knew, vnew, qs
+    oscar.oscar_destroy(ctx)
+    torch.cuda.empty_cache()
+    return res
+
+
 def synth_queries(st, T, G, b, h, dev):
     """Seeded prefill queries of KV head h of request b: [T][G][128]."""
     from bit_kv_cache_int2_gb300 import synth
@@ -829,6 +922,7 @@ def run_ours(args, wl):
     oscar.oscar_destroy(cctx)
     # ---- the batched configurations (parity-test shapes), timed here too
     batched = batched_measurement(dev, peak)
+    batched["qwen3_8b_stack_36x_b16_64k_g32"] = stack_measurement(dev, peak)
     # ---- synthetic serving loop under one KV memory budget, INT2 vs BF16 history
     serve = serving_measurement(wl, dev)
     # ---- end to end through the public API with host buffers.  Each step's q,
