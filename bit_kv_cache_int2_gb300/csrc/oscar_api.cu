@@ -99,14 +99,12 @@ size_t scratch_for(const oscar_ctx* ctx, int B, int target) {
 
 // Decode kernel variant: 4 tensor cores with the layer's Lloyd-Max codebook
 // (whatever the option); 1 CUDA-core INT2; 3 tensor cores, pages in pairs as
-// two softmax streams per tile (needs G <= 4, used at g >= 64); 0 tensor
-// cores, one page at a time.  layer < 0: the variant without a codebook.
+// two softmax streams per tile (needs G <= 4); 0 tensor cores, one page at a
+// time.  layer < 0: the variant without a codebook.
 int kernel_impl(const oscar_ctx* ctx, int layer = -1) {
   if (layer >= 0 && ctx->has_cb[layer]) return 4;
   if (ctx->impl == OSCAR_DECODE_CUDA_CORE) return 1;
-  // pairs carry four (s, z) groups per token poorly at g = 32 (register
-  // spills): one page at a time measured 1.2x faster there
-  if (ctx->impl == OSCAR_DECODE_TENSOR_SINGLE || ctx->G > 4 || ctx->NG == 4) return 0;
+  if (ctx->impl == OSCAR_DECODE_TENSOR_SINGLE || ctx->G > 4) return 0;
   return 3;
 }
 

@@ -1252,7 +1252,10 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
 // IMPL: 0 INT2 history on tensor cores, 1 INT2 history on CUDA cores,
 // 2 BF16 history (the baseline; no INT2 code, double-buffered BF16 tiles).
 template <int NG, int IMPL>
-__global__ void __launch_bounds__(NW * 32, (IMPL == 0 || IMPL == 3 || IMPL == 4) ? 3 : 2) decode_kernel(DecodeArgs a) {
+// Three CTAs per SM fit the shared memory of g = 128 pages only (4608-byte
+// stages); at g = 64 and 32 two do, and the register budget follows.
+__global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 || IMPL == 4)) ? 3 : 2)
+    decode_kernel(DecodeArgs a) {
   constexpr bool BF16H = (IMPL == 2);
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheView& cv = a.cv;

@@ -110,9 +110,8 @@ typedef enum {
 
 /* INT2 history decode kernels (the BF16-history baseline has one kernel). */
 typedef enum {
-  OSCAR_DECODE_TENSOR = 0,        /* tensor cores; with at most 4 query heads per kv head and
-                                     group size 64 or 128 a warp takes two pages per tile as two
-                                     softmax streams, else one page per tile (default) */
+  OSCAR_DECODE_TENSOR = 0,        /* tensor cores; with at most 4 query heads per kv head a warp
+                                     takes two pages per tile as two softmax streams (default) */
   OSCAR_DECODE_CUDA_CORE = 1,     /* fp32 CUDA cores, one page per warp at a time */
   OSCAR_DECODE_TENSOR_SINGLE = 2  /* tensor cores, one page per tile at any group size */
 } oscar_decode_impl;
