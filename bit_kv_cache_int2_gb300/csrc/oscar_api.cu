@@ -625,14 +625,16 @@ oscar_status oscar_prefill(oscar_ctx* ctx, int layer, const oscar_cache* cache, 
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
       !aligned(scratch, 256) || (lse && !aligned(lse, 4)))
     return OSCAR_ERR_INVALID_ARG;
-  if (ctx->has_cb[layer]) return OSCAR_ERR_UNSUPPORTED;  // the prefill dequantises uniform codes only
   if (batch == 0) return OSCAR_OK;
+  // a layer with a Lloyd-Max codebook runs the mma.sync kernel, whose tile
+  // fill dequantises codebook levels (the tcgen05 producers do uniform codes)
+  const int impl = ctx->has_cb[layer] ? (int)OSCAR_PREFILL_MMA_SYNC : ctx->prefill_impl;
   const int Hkv = ctx->cfg.num_kv_heads, G = ctx->G;
   PrefillArgs a;
   a.RT = (T * G + PF_ROWS - 1) / PF_ROWS;
   const int tiles = batch * Hkv * a.RT;
   int occ = 0;
-  const cudaError_t oe = prefill_ctas_per_sm(&occ, ctx->prefill_impl);
+  const cudaError_t oe = prefill_ctas_per_sm(&occ, impl);
   if (oe != cudaSuccess) return cuda_status(oe);
   if (occ < 1) occ = 1;
   // history splits: the history CTAs fill one wave over the SMs; the light
@@ -655,7 +657,8 @@ oscar_status oscar_prefill(oscar_ctx* ctx, int layer, const oscar_cache* cache, 
   a.part = (float*)(sp + L.off_part);
   a.B = batch;
   a.T = T;
-  a.impl = ctx->prefill_impl;
+  a.impl = impl;
+  a.codebook = ctx->has_cb[layer];
   a.rot = layer_rot(ctx, layer);
   return cuda_status(launch_prefill(a, (cudaStream_t)stream, &ctx->prof));
 }

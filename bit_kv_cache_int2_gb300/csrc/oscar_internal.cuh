@@ -656,6 +656,7 @@ struct PrefillArgs {
   float* part;             // scratch [B*Hkv*RT][NS+1][128][PART_STRIDE]
   int B, T, RT, NS;
   int impl;  // an oscar_prefill_impl value
+  int codebook;  // the layer has a Lloyd-Max codebook (mma.sync kernel only)
   LayerRot rot;
 };
 

@@ -67,6 +67,35 @@ __device__ __forceinline__ uint32_t codes_f16x2(uint32_t w) {
   return hfma2u(code_pair<I>(w), SC, OF);
 }
 
+// Lloyd-Max codebook of one side (keys or values) of the item's kv head as
+// f16x2 constants: level(code) = c0 + alpha*bit0 + beta_half*(2*bit1).
+struct CbLevels {
+  uint32_t c0, al, bh;
+};
+
+__device__ __forceinline__ CbLevels cb_levels(const float* rec) {
+  CbLevels L;
+  const __half2 c0 = __float2half2_rn(__ldg(rec + CB_C0));
+  const __half2 al = __float2half2_rn(__ldg(rec + CB_ALPHA));
+  const __half2 bh = __float2half2_rn(__ldg(rec + CB_BETA_HALF));
+  L.c0 = *(const uint32_t*)&c0;
+  L.al = *(const uint32_t*)&al;
+  L.bh = *(const uint32_t*)&bh;
+  return L;
+}
+
+// The levels of code_pair<I>'s two codes: each bit plane gives its bit
+// exactly (0 or 1, and 0 or 2 for the high bit), then two fp16 FMAs.
+template <int I>
+__device__ __forceinline__ uint32_t levels_f16x2(uint32_t w, const CbLevels& L) {
+  constexpr int E = code_exp<I>();
+  constexpr uint32_t SC = E == 4 ? 0x2C002C00u : E == 6 ? 0x24002400u : 0x1C001C00u;   // 2^-E
+  constexpr uint32_t OF = E == 4 ? 0xD400D400u : E == 6 ? 0xCC00CC00u : 0xC400C400u;   // -1024·2^-E
+  const uint32_t b0 = hfma2u(code_plane<I, 0>(w), SC, OF);
+  const uint32_t b1x2 = hfma2u(code_plane<I, 1>(w), SC, OF);
+  return hfma2u(b1x2, L.bh, hfma2u(b0, L.al, L.c0));
+}
+
 // ------------------------------------------------------------ tile filling
 // K tile: row = token (256 B), 16-byte chunk j of row t stored at j ^ (t & 7).
 // V^T tile: row = channel (128 B), chunk j of row c stored at j ^ (c & 7).
@@ -74,25 +103,30 @@ __device__ __forceinline__ uint32_t codes_f16x2(uint32_t w) {
 
 // Dequantise one INT2 head block (raw, in shared memory) into the K and V^T
 // tiles: value = s·code + z with the group's fp16 scale and zero, rounded
-// once to fp16.  nv = valid tokens (rows 0..nv-1).
-template <int I>
+// once to fp16 (CB: s·level(code) + z with the codebook's fp16 levels).
+// nv = valid tokens (rows 0..nv-1).
+template <int I, bool CB>
 __device__ __forceinline__ void k_store(uint8_t* Kt, int tr, int A, int dq, uint32_t w, uint32_t s2,
-                                        uint32_t z2, bool ok) {
-  const uint32_t val = ok ? hfma2u(codes_f16x2<I>(w), s2, z2) : 0u;
+                                        uint32_t z2, bool ok, const CbLevels& L) {
+  const uint32_t c = CB ? levels_f16x2<I>(w, L) : codes_f16x2<I>(w);
+  const uint32_t val = ok ? hfma2u(c, s2, z2) : 0u;
   *(uint32_t*)(Kt + tr * 256 + ((((8 * A + I) ^ (tr & 7))) << 4) + 4 * dq) = val;
 }
 
-template <int I>
+template <int I, bool CB>
 __device__ __forceinline__ void v_store(uint8_t* Vt, int ch, int T4, uint32_t w, const uint32_t* vsz,
-                                        int NG, int grp, int nv) {
+                                        int NG, int grp, int nv, const CbLevels& L) {
   const int t = 8 * I + 2 * T4;  // token slot of the low half; t + 1 in the high half
   const uint32_t a = vsz[t * NG + grp], b = vsz[(t + 1) * NG + grp];
-  uint32_t val = hfma2u(codes_f16x2<I>(w), prmt(a, b, 0x5410u), prmt(a, b, 0x7632u));
+  const uint32_t c = CB ? levels_f16x2<I>(w, L) : codes_f16x2<I>(w);
+  uint32_t val = hfma2u(c, prmt(a, b, 0x5410u), prmt(a, b, 0x7632u));
   if (t + 1 >= nv) val = t < nv ? (val & 0xFFFFu) : 0u;
   *(uint32_t*)(Vt + ch * 128 + (((I ^ (ch & 7))) << 4) + 4 * T4) = val;
 }
 
-__device__ __forceinline__ void fill_int2(uint8_t* smem, int buf, const uint8_t* raw, int g, int nv) {
+template <bool CB>
+__device__ __forceinline__ void fill_int2(uint8_t* smem, int buf, const uint8_t* raw, int g, int nv,
+                                          const CbLevels& LK, const CbLevels& LV) {
   const int tid = threadIdx.x, NG = D / g;
   uint8_t* Kt = smem + OFF_TILES + buf * 2 * TILE_BYTES;
   uint8_t* Vt = Kt + TILE_BYTES;
@@ -107,14 +141,14 @@ __device__ __forceinline__ void fill_int2(uint8_t* smem, int buf, const uint8_t*
       const uint32_t lo = ksz[(64 * A) / g], hi = ksz[(64 * A + 32) / g];  // groups of I < 4, I >= 4
       const uint32_t s0 = prmt(lo, lo, 0x1010u), z0 = prmt(lo, lo, 0x3232u);
       const uint32_t s1 = prmt(hi, hi, 0x1010u), z1 = prmt(hi, hi, 0x3232u);
-      k_store<0>(Kt, tr, A, dq, w, s0, z0, ok);
-      k_store<1>(Kt, tr, A, dq, w, s0, z0, ok);
-      k_store<2>(Kt, tr, A, dq, w, s0, z0, ok);
-      k_store<3>(Kt, tr, A, dq, w, s0, z0, ok);
-      k_store<4>(Kt, tr, A, dq, w, s1, z1, ok);
-      k_store<5>(Kt, tr, A, dq, w, s1, z1, ok);
-      k_store<6>(Kt, tr, A, dq, w, s1, z1, ok);
-      k_store<7>(Kt, tr, A, dq, w, s1, z1, ok);
+      k_store<0, CB>(Kt, tr, A, dq, w, s0, z0, ok, LK);
+      k_store<1, CB>(Kt, tr, A, dq, w, s0, z0, ok, LK);
+      k_store<2, CB>(Kt, tr, A, dq, w, s0, z0, ok, LK);
+      k_store<3, CB>(Kt, tr, A, dq, w, s0, z0, ok, LK);
+      k_store<4, CB>(Kt, tr, A, dq, w, s1, z1, ok, LK);
+      k_store<5, CB>(Kt, tr, A, dq, w, s1, z1, ok, LK);
+      k_store<6, CB>(Kt, tr, A, dq, w, s1, z1, ok, LK);
+      k_store<7, CB>(Kt, tr, A, dq, w, s1, z1, ok, LK);
     }
   }
   {  // V: channel ch, word T4 holds token slots 8I + 2T4 + E
@@ -125,14 +159,14 @@ __device__ __forceinline__ void fill_int2(uint8_t* smem, int buf, const uint8_t*
       const int ch = (tid >> 2) + 64 * hc;
       const uint32_t w = *(const uint32_t*)(raw + 2048 + ch * 16 + 4 * T4);
       const int grp = ch / g;
-      v_store<0>(Vt, ch, T4, w, vsz, NG, grp, nv);
-      v_store<1>(Vt, ch, T4, w, vsz, NG, grp, nv);
-      v_store<2>(Vt, ch, T4, w, vsz, NG, grp, nv);
-      v_store<3>(Vt, ch, T4, w, vsz, NG, grp, nv);
-      v_store<4>(Vt, ch, T4, w, vsz, NG, grp, nv);
-      v_store<5>(Vt, ch, T4, w, vsz, NG, grp, nv);
-      v_store<6>(Vt, ch, T4, w, vsz, NG, grp, nv);
-      v_store<7>(Vt, ch, T4, w, vsz, NG, grp, nv);
+      v_store<0, CB>(Vt, ch, T4, w, vsz, NG, grp, nv, LV);
+      v_store<1, CB>(Vt, ch, T4, w, vsz, NG, grp, nv, LV);
+      v_store<2, CB>(Vt, ch, T4, w, vsz, NG, grp, nv, LV);
+      v_store<3, CB>(Vt, ch, T4, w, vsz, NG, grp, nv, LV);
+      v_store<4, CB>(Vt, ch, T4, w, vsz, NG, grp, nv, LV);
+      v_store<5, CB>(Vt, ch, T4, w, vsz, NG, grp, nv, LV);
+      v_store<6, CB>(Vt, ch, T4, w, vsz, NG, grp, nv, LV);
+      v_store<7, CB>(Vt, ch, T4, w, vsz, NG, grp, nv, LV);
     }
   }
 }
@@ -359,6 +393,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_attn_kernel(PrefillArgs
 
   // this CTA's tiles
   const size_t head = (size_t)b * Hkv + kvh;
+  // Lloyd-Max codebook levels of the kv head (used when a.codebook is set)
+  const CbLevels cbk = cb_levels(a.rot.cb + (size_t)kvh * CB_WORDS);
+  const CbLevels cbv = cb_levels(a.rot.cb + (size_t)(Hkv + kvh) * CB_WORDS);
   const int hist = cv.hist_lens[b];
   int pages = hist > 0 ? (hist + PAGE - 1) / PAGE : 0;
   if (pages > cv.max_pages_per_req) {  // inconsistent state: stay inside the page table
@@ -399,7 +436,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_attn_kernel(PrefillArgs
       ok = ok && !sbad[slot];
       const int pg = p0 + i;
       const int nv = pg == pages - 1 ? hist - pg * PAGE : PAGE;
-      if (ok) fill_int2(smem, buf, smem + OFF_RAW + slot * RAW_SLOT, cv.g, nv);
+      if (ok) {
+        if (a.codebook)
+          fill_int2<true>(smem, buf, smem + OFF_RAW + slot * RAW_SLOT, cv.g, nv, cbk, cbv);
+        else
+          fill_int2<false>(smem, buf, smem + OFF_RAW + slot * RAW_SLOT, cv.g, nv, cbk, cbv);
+      }
       if (tid == 0) {
         tmask[buf] = ok ? low_mask(nv) : 0ull;
         tcausal[buf] = 0;

@@ -300,8 +300,9 @@ oscar_status oscar_decode_step(oscar_ctx* ctx, int layer, const oscar_cache* cac
  *             bytes, 256-byte aligned, no initial contents needed; not to be
  *             shared by calls that may overlap.
  * q, k, v, out 16-byte aligned.  Returns OSCAR_ERR_INVALID_ARG for T outside
- * 1..64 and OSCAR_ERR_UNSUPPORTED on a layer with a non-uniform Lloyd-Max
- * codebook (oscar_set_codebook).  Device errors as oscar_decode (OSCAR_ERR_NO_PAGE / OSCAR_ERR_RANGE
+ * 1..64.  On a layer with a non-uniform Lloyd-Max codebook
+ * (oscar_set_codebook) the mma.sync kernel runs whatever OSCAR_OPT_PREFILL_IMPL
+ * says, dequantising s·level(code) + z.  Device errors as oscar_decode (OSCAR_ERR_NO_PAGE / OSCAR_ERR_RANGE
  * for a bad history page, whose tokens are then left out). */
 oscar_status oscar_prefill(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* q,
                            const void* k, const void* v, int T, void* out, float* lse,
@@ -370,8 +371,8 @@ oscar_status oscar_clip_errors(oscar_ctx* ctx, int layer, int kv_head, const voi
  * From then on the demotion, the bulk import, oscar_clip_errors and the decode
  * of this layer use them.  While any head of the layer has a non-uniform
  * codebook the decode runs the codebook kernel (two tensor-core products per
- * operand, whatever OSCAR_OPT_DECODE_IMPL says) and oscar_prefill on the layer
- * returns OSCAR_ERR_UNSUPPORTED.  Codes already in the cache are not
+ * operand, whatever OSCAR_OPT_DECODE_IMPL says) and oscar_prefill runs its
+ * mma.sync kernel.  Codes already in the cache are not
  * re-quantised: set the codebook before the layer's tokens are written.
  * OSCAR_ERR_INVALID_ARG if a pair is outside 0 <= a < b <= 3 or not finite
  * (nothing is changed then).  Synchronises `stream`. */

@@ -1,8 +1,9 @@
 """GPU parity of the Lloyd-Max codebook path through the C ABI: the
 quantiser's codes and scales bit for bit, the codebook fit, the decode over a
 cache written with a codebook (import, append with demotion, the fused step),
-the clip errors with a codebook, and the host-side rules (uniform levels keep
-the default kernels, prefill refuses, bad pairs are rejected)."""
+the chunked prefill over it, the clip errors with a codebook, and the
+host-side rules (uniform levels keep the default kernels, bad pairs are
+rejected)."""
 import numpy as np
 import pytest
 import torch
@@ -259,10 +260,10 @@ def test_codebook_host_rules():
         k = torch.zeros(1, 4, 2, 128, dtype=torch.bfloat16, device="cuda")
         out = torch.empty_like(q)
         scratch = oscar.alloc_scratch(cfg, "cuda", prefill=True)
-        with pytest.raises(oscar.OscarError) as e:
+        for impl in (oscar.PREFILL_TCGEN05, oscar.PREFILL_MMA_SYNC):  # both run (the mma.sync kernel)
+            oscar.oscar_set_option(ctx, oscar.OPT_PREFILL_IMPL, impl)
             oscar.oscar_prefill(ctx, 0, cache, q, k, k, 4, out, None, scratch, 1)
-        assert e.value.status == oscar.ERR_UNSUPPORTED
-        oscar.oscar_set_codebook(ctx, 0, None, None)  # back to uniform: prefill runs again
+        oscar.oscar_set_codebook(ctx, 0, None, None)  # back to uniform
         oscar.oscar_prefill(ctx, 0, cache, q, k, k, 4, out, None, scratch, 1)
         torch.cuda.synchronize()
         X = torch.zeros(16, 128, dtype=torch.bfloat16, device="cuda")
@@ -275,3 +276,22 @@ def test_codebook_host_rules():
         assert (a, b, up) == O.lloyd_max_folded(np.zeros(0))
     finally:
         oscar.oscar_destroy(ctx)
+
+
+@pytest.mark.parametrize("G,g,T", [(4, 128, 64), (8, 32, 17), (2, 64, 40)])
+def test_codebook_prefill_matches_oracle(G, g, T):
+    """Chunked prefill over caches written with per-head codebooks (the
+    mma.sync kernel dequantises s·level(code) + z) against the oracle."""
+    from test_gpu_prefill import check_all, chunk_inputs, run_prefill
+
+    lengths = [0, 330, 1000, 64 * 7 + 320 + 9]
+    sc = GS.build(f"cbpf{G}{g}", lengths, Hq=2 * G, Hkv=2, g=g, interleave=True, calib_n=512, extra_tokens=T,
+                  codebook=_codebooks(2, 31 * G + g))
+    try:
+        q, k, v = chunk_inputs(sc, T, seed=G + g)
+        for impl in (oscar.PREFILL_TCGEN05, oscar.PREFILL_MMA_SYNC):
+            out, lse = run_prefill(sc, q, k, v, impl=impl)
+            assert oscar.oscar_get_error(sc.ctx) == 0
+            check_all(sc, q, k, v, out, lse)
+    finally:
+        sc.close()

@@ -64,8 +64,11 @@ def oracle_prefill(sc, hc, q, k, v, b, h, tokens=None):
     if f is None:
         hk = hv = np.zeros((0, 128))
     else:
-        hk = O.dequantize(f["k_codes"], f["k_s"], f["k_z"], sc.g)
-        hv = O.dequantize(f["v_codes"], f["v_s"], f["v_z"], sc.g)
+        ck, cv = sc.cb("k", h), sc.cb("v", h)  # Lloyd-Max levels, or None for the uniform ones
+        hk = (O.dequantize(f["k_codes"], f["k_s"], f["k_z"], sc.g) if ck is None
+              else O.dequantize_codebook(f["k_codes"], f["k_s"], f["k_z"], sc.g, *ck))
+        hv = (O.dequantize(f["v_codes"], f["v_s"], f["v_z"], sc.g) if cv is None
+              else O.dequantize_codebook(f["v_codes"], f["v_s"], f["v_z"], sc.g, *cv))
     return O.chunk_prefill_attention(qn, kc, vc, wk, wv, hk, hv, O.rotation(sc.U_K[h], sc.mode),
                                      O.rotation(sc.U_V[h], sc.mode), tokens=tokens)
 
