@@ -1050,6 +1050,65 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
+def run_codebook_leg(args, wl):
+    """Only the Lloyd-Max codebook decode on the workload: fits from the
+    calibration sets, a cache written with them, and --steps timed decodes
+    over copies larger than 3x L2.  A short command for profiling that kernel
+    (the full bench reaches it after every other leg)."""
+    import numpy as np
+    import torch
+
+    from bit_kv_cache_int2_gb300 import build as B
+    from bit_kv_cache_int2_gb300 import oscar, synth
+
+    B.build()
+    dev = "cuda:0"
+    Hkv, g, Bsz = wl["Hkv"], wl["g"], wl["B"]
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    per_copy = algorithmic_bytes(wl["L"] - 320, wl["L"], Hkv, g) * Bsz
+    n_copies = max(2, -(-3 * l2 // per_copy))
+    wk = build_workload(wl, dev, 1, 16)
+    cfg, L0 = wk["cfg"], wl["L"]
+    cctx = oscar.oscar_create(cfg)
+    oscar.oscar_set_rotation(cctx, 0, wk["U"][0], wk["U"][1], [wl["clip"]] * Hkv, [wl["clip"]] * Hkv,
+                             oscar.ROT_OSCAR)
+    G_cal, N_cal = wl["Hq"] // Hkv, 2048
+    fscr = oscar.codebook_scratch(N_cal, dev)
+    kab, vab = [], []
+    for h in range(Hkv):
+        _, Kc, Vc = (t.to(dev).contiguous() for t in synth.calibration_set(0, "bench", 0, h, wk["stats"][h], G=G_cal,
+                                                                         n=N_cal))
+        kab.append(oscar.oscar_fit_codebook(cctx, 0, h, 0, Kc, N_cal, fscr)[:2])
+        vab.append(oscar.oscar_fit_codebook(cctx, 0, h, 1, Vc, N_cal, fscr)[:2])
+    oscar.oscar_set_codebook(cctx, 0, kab, vab)
+    base = oscar.alloc_cache(cfg, dev)
+    base["page_table"].copy_(wk["copies"][0]["page_table"])
+    oscar.oscar_import_tokens(cctx, 0, base, wk["K"][:, :, :L0].contiguous(), wk["V"][:, :, :L0].contiguous(), Bsz,
+                              L0)
+    torch.cuda.synchronize()
+    copies = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n_copies - 1)]
+    q = wk["q"]
+    out = torch.empty_like(q)
+    scratch = oscar.alloc_scratch(cfg, dev)
+    dec = [oscar.bind_decode(cctx, 0, c, q, out, None, scratch, Bsz) for c in copies]
+    for i in range(args.warmup):
+        dec[i % n_copies]()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        dec[i % n_copies]()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    assert oscar.oscar_get_error(cctx) == 0 and bool(torch.isfinite(out.float()).all())
+    print(json.dumps({"leg": "codebook_decode", "workload": args.workload, "us_per_call": us,
+                      "bytes_per_call": per_copy, "hbm_gbs": per_copy / (us * 1e-6) / 1e9, "cache_copies": n_copies,
+                      "k_ab": np.round(np.array(kab), 5).tolist(), "v_ab": np.round(np.array(vab), 5).tolist()}),
+          flush=True)
+    oscar.oscar_destroy(cctx)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1058,11 +1117,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_8b_100k", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--leg", choices=["all", "codebook"], default="all",
+                    help="codebook: only the Lloyd-Max codebook decode (a short command to profile it)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, wl)
+    elif args.leg == "codebook":
+        run_codebook_leg(args, wl)
     else:
         run_ours(args, wl)
 
