@@ -165,6 +165,31 @@ def test_decode_gqa_and_group_sizes(G, g, impl):
         sc.close()
 
 
+@pytest.mark.parametrize("items", [0, 1, 3, 8])
+def test_decode_item_sizing_options(items):
+    """The work list's item sizing (0 = automatic, else fixed items per CTA)
+    changes only how the history is split: every setting matches the oracle
+    on a ragged batch long enough for the automatic rule to split finely."""
+    lengths = [9000, 320, 40000, 12345, 0, 700, 25000, 64 * 50 + 320 + 3]
+    sc = GS.build("items", lengths, Hq=8, Hkv=2, g=128, interleave=True, calib_n=512)
+    try:
+        oscar.oscar_set_option(sc.ctx, oscar.OPT_ITEMS_PER_CTA, items)
+        q = GS.queries(sc, seed=8)
+        out, lse = GS.decode(sc, q)
+        assert oscar.oscar_get_error(sc.ctx) == 0
+        hc = GS.HostCache(sc)
+        qn = q.float().cpu().numpy()
+        for b, L in enumerate(lengths):
+            if L == 0:
+                assert np.all(out[b].float().cpu().numpy() == 0)
+                continue
+            ref, rlse = GS.oracle_decode(sc, hc, qn, b)
+            assert _rel(out[b].float().cpu().numpy(), ref) <= REL_TOL, (items, b)
+            assert np.abs(lse[b].cpu().numpy() - rlse).max() <= LSE_TOL
+    finally:
+        sc.close()
+
+
 def test_bf16_history_baseline_matches_dense_attention():
     lengths = [1, 300, 321, 1000, 2000]
     sc = GS.build("bf16h", lengths, Hq=8, Hkv=2, bf16_history=True, mode=oscar.ROT_NONE)
