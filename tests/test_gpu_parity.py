@@ -170,8 +170,9 @@ def test_decode_item_sizing_options(items):
     """The work list's item sizing (0 = automatic, else fixed items per CTA)
     changes only how the history is split: every setting matches the oracle
     on a ragged batch long enough for the automatic rule to split finely."""
-    lengths = [9000, 320, 40000, 12345, 0, 700, 25000, 64 * 50 + 320 + 3]
-    sc = GS.build("items", lengths, Hq=8, Hkv=2, g=128, interleave=True, calib_n=512)
+    # ~21K history pages x kv heads: past the automatic rule's single-wave limit
+    lengths = [9000, 320, 140000, 62345, 0, 700, 125000, 64 * 50 + 320 + 3]
+    sc = GS.build("items", lengths, Hq=16, Hkv=4, g=128, interleave=True, calib_n=512)
     try:
         oscar.oscar_set_option(sc.ctx, oscar.OPT_ITEMS_PER_CTA, items)
         q = GS.queries(sc, seed=8)
