@@ -572,8 +572,9 @@ def serving_measurement(wl, dev, n_req=48, gen=64, lo=8192, hi=24576, budget_req
         done, steps, sec = serving.run_job(backend, pool_pages, slots, mpr, reqs)
         assert oscar.oscar_get_error(ctx) == 0 and len(done) == n_req
         dsec = serving.step_seconds(backend)
+        isec = serving.import_seconds(backend)
         res[fmt] = {"slots": slots, "pool_pages": pool_pages, "steps": steps, "seconds": sec,
-                    "tokens_per_s": n_req * gen / sec, "decode_seconds": dsec,
+                    "tokens_per_s": n_req * gen / sec, "decode_seconds": dsec, "import_seconds": isec,
                     "decode_tokens_per_s": n_req * gen / dsec, "mean_batch": float(np.mean(batches)),
                     "max_batch": int(max(batches))}
         oscar.oscar_destroy(ctx)
@@ -583,10 +584,11 @@ def serving_measurement(wl, dev, n_req=48, gen=64, lo=8192, hi=24576, budget_req
             "budget_mb": budget / 1e6, **res,
             "throughput_ratio": res["int2"]["tokens_per_s"] / res["bf16"]["tokens_per_s"],
             "decode_throughput_ratio": res["int2"]["decode_tokens_per_s"] / res["bf16"]["decode_tokens_per_s"],
-            "note": "synthetic, one Qwen3-8B-shaped layer; each request imports its prefix (standing in for a "
-                    "prefix-cache hit) and decodes with append + attention per step. tokens_per_s: wall time of the "
-                    "whole job (imports, host scheduler in Python, steps); decode_tokens_per_s: device time of the "
-                    "decode steps only (CUDA events around each step)"}
+            "note": "synthetic, one Qwen3-8B-shaped layer; each request imports its prefix from BF16 (standing in "
+                    "for a prefix-cache hit; the INT2 import quantises it, which a stored INT2 prefix would not need) "
+                    "and decodes with append + attention per step. tokens_per_s: wall time of the whole job (imports, "
+                    "host scheduler in Python, steps); decode_tokens_per_s: device time of the decode steps only; "
+                    "import_seconds: device time of the imports (CUDA events around each call)"}
 
 
 def blas_threads():

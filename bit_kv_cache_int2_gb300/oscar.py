@@ -405,6 +405,33 @@ def bind_decode_step_ptrs(ctx, layer, cache: dict, out, lse, scratch, batch, str
     return call
 
 
+def bind_step_any_batch(ctx, layer, cache: dict, out, lse, scratch, bf16_history=False, stream=None):
+    """One decode step with the cache and outputs marshalled once and the
+    batch given per call: returns f(k_ptr, v_ptr, q_ptr, batch) taking raw
+    addresses.  INT2 history: oscar_decode_step; BF16 history:
+    oscar_append_bf16_history then oscar_decode_bf16_history."""
+    cs = _cache_struct(cache)
+    L = lib()
+    st = _stream(stream)
+    o, ls, sc, nb = _ptr(out), _ptr(lse), _ptr(scratch), scratch.numel() * scratch.element_size()
+    P = ctypes.c_void_p
+    if not bf16_history:
+        fn = L.oscar_decode_step
+
+        def call(k_ptr: int, v_ptr: int, q_ptr: int, batch: int):
+            _check(fn(ctx, layer, ctypes.byref(cs), P(k_ptr), P(v_ptr), P(q_ptr), o, ls, sc, nb, batch, st),
+                   "oscar_decode_step")
+    else:
+        fa, fd = L.oscar_append_bf16_history, L.oscar_decode_bf16_history
+
+        def call(k_ptr: int, v_ptr: int, q_ptr: int, batch: int):
+            _check(fa(ctx, ctypes.byref(cs), P(k_ptr), P(v_ptr), batch, st), "oscar_append_bf16_history")
+            _check(fd(ctx, ctypes.byref(cs), P(q_ptr), o, ls, sc, nb, batch, st), "oscar_decode_bf16_history")
+
+    call._keep = cs
+    return call
+
+
 def bind_append(ctx, layer, cache: dict, batch, stream=None):
     """oscar_append with the cache and stream marshalled once, for tight loops:
     returns f(k_new_ptr, v_new_ptr) taking raw device addresses (ints)."""

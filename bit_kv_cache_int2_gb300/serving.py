@@ -138,23 +138,45 @@ class DeviceBackend:
     """One layer's cache on the GPU, driven through the C ABI.
 
     draw(req) -> (K, V, Q): the request's synthetic stream, K and V bf16
-    [Hkv][prefix + gen][128] and Q bf16 [gen][Hq][128] device tensors, drawn at
-    admission and dropped at retirement.  fmt is "int2" or "bf16"."""
+    [Hkv][prefix + gen][128] and Q bf16 [gen][Hq][128] device tensors.  At
+    admission the prefix is imported and the request's future tokens are
+    copied into its batch slot's buffers; a step then gathers every active
+    slot's next token with one indexed read per operand and runs one
+    pre-marshalled library call.  fmt is "int2" or "bf16"."""
 
-    def __init__(self, fmt, ctx, cfg, cache, draw, on_step=None, time_steps=False):
+    def __init__(self, fmt, ctx, cfg, cache, draw, on_step=None, time_steps=False, max_gen=64):
         import torch
 
         self.fmt, self.ctx, self.cfg, self.cache = fmt, ctx, cfg, cache
         self.draw, self.on_step = draw, on_step
         B, Hq, Hkv = cfg.max_batch, cfg.num_q_heads, cfg.num_kv_heads
         dev = cache["seq_lens"].device
-        self.q = torch.empty(B, Hq, 128, dtype=torch.bfloat16, device=dev)
-        self.k = torch.empty(B, Hkv, 128, dtype=torch.bfloat16, device=dev)
-        self.v = torch.empty_like(self.k)
-        self.out = torch.empty_like(self.q)
+        self.dev = dev
+        self.out = torch.empty(B, Hq, 128, dtype=torch.bfloat16, device=dev)
         self.scratch = oscar.alloc_scratch(cfg, dev)
-        self.streams = {}
+        self.gen_cap = 0
+        self._grow(max_gen)
+        self.pos = torch.zeros(B, dtype=torch.long, device=dev)  # next token of each slot
+        self.slots = torch.arange(B, device=dev)
+        self.call = oscar.bind_step_any_batch(ctx, 0, cache, self.out, None, self.scratch,
+                                              bf16_history=(fmt == "bf16"))
         self.step_events = [] if time_steps else None
+        self.import_events = [] if time_steps else None
+
+    def _grow(self, gen):
+        """Slot buffers for up to `gen` future tokens per request, keeping the
+        tokens already held."""
+        import torch
+
+        B, Hq, Hkv = self.cfg.max_batch, self.cfg.num_q_heads, self.cfg.num_kv_heads
+        bufs = (torch.zeros(B, gen, Hkv, 128, dtype=torch.bfloat16, device=self.dev),
+                torch.zeros(B, gen, Hkv, 128, dtype=torch.bfloat16, device=self.dev),
+                torch.zeros(B, gen, Hq, 128, dtype=torch.bfloat16, device=self.dev))
+        if self.gen_cap:
+            for new, old in zip(bufs, (self.kbuf, self.vbuf, self.qbuf)):
+                new[:, :self.gen_cap] = old
+        self.kbuf, self.vbuf, self.qbuf = bufs
+        self.gen_cap = gen
 
     def _view(self, slot):
         v = dict(self.cache)
@@ -165,57 +187,72 @@ class DeviceBackend:
     def admit(self, slot, req):
         import torch
 
+        if req.gen > self.gen_cap:
+            self._grow(req.gen)
         K, V, Q = self.draw(req)
-        self.streams[req.rid] = (K, V, Q)
+        P, n = req.prefix, req.gen
+        self.kbuf[slot, :n] = K[:, P:P + n].permute(1, 0, 2)
+        self.vbuf[slot, :n] = V[:, P:P + n].permute(1, 0, 2)
+        self.qbuf[slot, :n] = Q[:n]
+        self.pos[slot] = 0
         row = self.cache["page_table"][slot]
         row.fill_(-1)
         if req.pages:
-            row[:len(req.pages)] = torch.tensor(req.pages, dtype=torch.int32, device=row.device)
+            # pinned and non-blocking: a pageable copy would wait for all queued GPU work
+            ids = torch.tensor(req.pages, dtype=torch.int32).pin_memory()
+            row[:len(req.pages)].copy_(ids, non_blocking=True)
         self.cache["seq_lens"][slot] = 0
         self.cache["hist_lens"][slot] = 0
-        if req.prefix:
+        if P:
             view = self._view(slot)
-            Kp = K[:, :req.prefix].unsqueeze(0).contiguous()
-            Vp = V[:, :req.prefix].unsqueeze(0).contiguous()
+            Kp = K[:, :P].unsqueeze(0).contiguous()
+            Vp = V[:, :P].unsqueeze(0).contiguous()
+            if self.import_events is not None:
+                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ev[0].record()
             if self.fmt == "int2":
-                oscar.oscar_import_tokens(self.ctx, 0, view, Kp, Vp, 1, req.prefix)
+                oscar.oscar_import_tokens(self.ctx, 0, view, Kp, Vp, 1, P)
             else:
-                oscar.oscar_import_bf16_history(self.ctx, view, Kp, Vp, 1, req.prefix)
+                oscar.oscar_import_bf16_history(self.ctx, view, Kp, Vp, 1, P)
+            if self.import_events is not None:
+                ev[1].record()
+                self.import_events.append(ev)
 
     def move(self, src, dst):
         for key in ("page_table", "sink_k", "sink_v", "ring_k", "ring_v", "seq_lens", "hist_lens"):
             self.cache[key][dst].copy_(self.cache[key][src])
+        for buf in (self.kbuf, self.vbuf, self.qbuf, self.pos):
+            buf[dst].copy_(buf[src])
 
     def step(self, active):
         import torch
 
         n = len(active)
-        st = [self.streams[r.rid] for r in active]
-        torch.stack([s[0][:, r.prefix + r.done] for s, r in zip(st, active)], out=self.k[:n])
-        torch.stack([s[1][:, r.prefix + r.done] for s, r in zip(st, active)], out=self.v[:n])
-        torch.stack([s[2][r.done] for s, r in zip(st, active)], out=self.q[:n])
+        sl, ps = self.slots[:n], self.pos[:n]
+        k = self.kbuf[sl, ps]
+        v = self.vbuf[sl, ps]
+        q = self.qbuf[sl, ps]
         if self.step_events is not None:
             ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             ev[0].record()
-        if self.fmt == "int2":
-            oscar.oscar_decode_step(self.ctx, 0, self.cache, self.k, self.v, self.q, self.out, None, self.scratch, n)
-        else:
-            oscar.oscar_append_bf16_history(self.ctx, self.cache, self.k, self.v, n)
-            oscar.oscar_decode_bf16_history(self.ctx, self.cache, self.q, self.out, None, self.scratch, n)
+        self.call(k.data_ptr(), v.data_ptr(), q.data_ptr(), n)
         if self.step_events is not None:
             ev[1].record()
             self.step_events.append(ev)
+        self.pos[:n] += 1
         if self.on_step is not None:
-            self.on_step(active, self.q[:n], self.out[:n])
-        for r in active:
-            if r.done + 1 >= r.gen:
-                self.streams.pop(r.rid, None)
+            self.on_step(active, q, self.out[:n])
 
 
 def step_seconds(backend):
     """Device time of the decode steps (append + attention), summed, when the
     backend was made with time_steps=True."""
     return sum(a.elapsed_time(b) for a, b in backend.step_events) * 1e-3
+
+
+def import_seconds(backend):
+    """Device time of the prefix imports, summed (time_steps=True)."""
+    return sum(a.elapsed_time(b) for a, b in backend.import_events) * 1e-3
 
 
 def run_job(backend, pool_pages, max_batch, max_pages_per_req, requests):
