@@ -493,6 +493,20 @@ def test_rotation_ordering_aligned_reading():
     assert mean["none"] > mean["hadamard"] > mean["oscar"]
 
 
+def test_rotation_ordering_other_readings_reported():
+    """The other readings of the query distribution, reported as measured
+    (the distribution is not tuned to them): with a Haar-random query basis at
+    g = 128 no rotation is still the worst but Hadamard-only beats OSCAR; with
+    the aligned basis at g = 32 OSCAR is better than both by more than 10x."""
+    haar = [_ordering_trial(seed, 128, "haar") for seed in range(8)]
+    mh = {k: np.mean([r[k] for r in haar]) for k in haar[0]}
+    al32 = [_ordering_trial(seed, 32, "aligned") for seed in range(8)]
+    ma = {k: np.mean([r[k] for r in al32]) for k in al32[0]}
+    print("ordering haar g=128:", mh, " aligned g=32:", ma)
+    assert mh["none"] > max(mh["hadamard"], mh["oscar"])
+    assert ma["oscar"] * 10 < min(ma["none"], ma["hadamard"])
+
+
 # ------------------------------------------------------------------ clip search
 def _calib_set(seed, G=2, N=24, d=128):
     rng = np.random.default_rng(seed)
