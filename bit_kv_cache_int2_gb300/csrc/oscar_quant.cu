@@ -33,7 +33,9 @@ __device__ __forceinline__ void quant_pack(float y, int j, int g, float clip, QT
 }
 
 // Same, but writing a single token's V code straight into a V block in global
-// memory with a read-modify-write of the owning word (one writer per word).
+// memory: its two bits of the owning word are cleared and set by two atomic
+// reductions (one writer per word; same-address atomics of a thread keep their
+// order), so no load of the word sits on the demotion's critical path.
 __device__ __forceinline__ void quant_store_v_global(float y, int j, int g, float clip, QThr th, float* red,
                                                      int bar, int t, uint32_t* vblk_g,
                                                      __half2* sz_row) {
@@ -43,7 +45,8 @@ __device__ __forceinline__ void quant_store_v_global(float y, int j, int g, floa
   const uint32_t code = quant_code(y, qp, th);
   uint32_t* wp = vblk_g + j * 4 + v_word(t);
   const uint32_t sh = (uint32_t)v_bit(t);
-  *wp = (*wp & ~(3u << sh)) | (code << sh);
+  atomicAnd(wp, ~(3u << sh));
+  atomicOr(wp, code << sh);
   if ((j % g) == 0) sz_row[j / g] = __halves2half2(qp.s, qp.z);
 }
 
