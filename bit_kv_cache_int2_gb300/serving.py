@@ -199,8 +199,10 @@ class DeviceBackend:
         row.fill_(-1)
         if req.pages:
             # pinned and non-blocking: a pageable copy would wait for all queued GPU work
-            ids = torch.tensor(req.pages, dtype=torch.int32).pin_memory()
-            row[:len(req.pages)].copy_(ids, non_blocking=True)
+            ids = torch.tensor(req.pages, dtype=torch.int32)
+            if row.is_cuda:
+                ids = ids.pin_memory()
+            row[:len(req.pages)].copy_(ids, non_blocking=row.is_cuda)
         self.cache["seq_lens"][slot] = 0
         self.cache["hist_lens"][slot] = 0
         if P:

@@ -109,3 +109,75 @@ def test_scheduler_rejects_a_request_that_never_fits():
     sched = Scheduler(PagePool(4), 2, FakeBackend(4), max_pages_per_req=64)
     with pytest.raises(ValueError):
         sched.submit(Request(rid=0, prefix=320 + 64 * 5, gen=1))
+
+
+def test_device_backend_feeds_each_slot_its_own_next_token(monkeypatch):
+    """DeviceBackend's slot buffers on CPU tensors, with the library calls
+    replaced by recorders: every step's k, v and q rows are the active
+    requests' own tokens at position prefix + done, through admissions, slot
+    moves and retirements."""
+    import ctypes
+    import types
+
+    import numpy as np
+    import torch
+
+    from bit_kv_cache_int2_gb300 import serving
+
+    Hq, Hkv, B = 4, 2, 3
+    cfg = types.SimpleNamespace(max_batch=B, num_q_heads=Hq, num_kv_heads=Hkv)
+    cache = {"page_table": torch.full((B, 8), -1, dtype=torch.int32),
+             "sink_k": torch.zeros(B, 1), "sink_v": torch.zeros(B, 1), "ring_k": torch.zeros(B, 1),
+             "ring_v": torch.zeros(B, 1), "seq_lens": torch.zeros(B, dtype=torch.int32),
+             "hist_lens": torch.zeros(B, dtype=torch.int32)}
+    seen = []
+
+    def bind(ctx, layer, cache_, out, lse, scratch, bf16_history=False):
+        def call(k_ptr, v_ptr, q_ptr, n):
+            grab = lambda p, heads: np.frombuffer(ctypes.string_at(p, n * heads * 128 * 2), dtype=np.uint16
+                                                  ).reshape(n, heads, 128).copy()
+            seen.append((grab(k_ptr, Hkv), grab(v_ptr, Hkv), grab(q_ptr, Hq)))
+        return call
+
+    fake = types.SimpleNamespace(alloc_scratch=lambda c, d: torch.zeros(1), bind_step_any_batch=bind,
+                                 oscar_import_tokens=lambda *a: None, oscar_import_bf16_history=lambda *a: None)
+    monkeypatch.setattr(serving, "oscar", fake)
+
+    def tok(rid, pos, which, h):
+        # a distinct value per (request, position, operand, head), exact in bf16:
+        # a power of two times a 7-bit mantissa
+        i = ((rid * 16 + pos) * 3 + which) * 4 + h
+        return 2.0 ** (i // 128 - 4) * (1 + (i % 128) / 128)
+
+    def draw(req):
+        n = req.prefix + req.gen
+        K = torch.tensor([[[tok(req.rid, p, 0, h)] * 128 for p in range(n)] for h in range(Hkv)]).to(torch.bfloat16)
+        V = torch.tensor([[[tok(req.rid, p, 1, h)] * 128 for p in range(n)] for h in range(Hkv)]).to(torch.bfloat16)
+        Q = torch.tensor([[[tok(req.rid, req.prefix + t, 2, h)] * 128 for h in range(Hq)]
+                          for t in range(req.gen)]).to(torch.bfloat16)
+        return K, V, Q
+
+    checks = []
+
+    def on_step(active, q, out):
+        k, v, qq = seen[-1]
+        as_f = lambda a: (a.astype(np.uint32) << 16).view(np.float32)
+        for i, r in enumerate(active):
+            p = r.prefix + r.done
+            for h in range(Hkv):
+                assert as_f(k[i, h, 0]) == np.float32(tok(r.rid, p, 0, h)), (r.rid, p, h)
+                assert as_f(v[i, h, 0]) == np.float32(tok(r.rid, p, 1, h)), (r.rid, p, h)
+            for h in range(Hq):
+                assert as_f(qq[i, h, 0]) == np.float32(tok(r.rid, p, 2, h)), (r.rid, p, h)
+        checks.append(len(active))
+
+    backend = serving.DeviceBackend("int2", None, cfg, cache, draw, on_step=on_step, max_gen=4)
+    reqs = [Request(rid=0, prefix=3, gen=2), Request(rid=1, prefix=0, gen=5), Request(rid=2, prefix=1, gen=3),
+            Request(rid=3, prefix=2, gen=6), Request(rid=4, prefix=0, gen=1)]
+    sched = Scheduler(PagePool(40), B, backend, max_pages_per_req=8)
+    for r in reqs:
+        sched.submit(r)
+    done = sched.run()
+    assert sorted(r.rid for r in done) == [0, 1, 2, 3, 4]
+    assert sum(checks) == sum(r.gen for r in reqs) and max(checks) == B
+    assert backend.gen_cap == 6  # grew for the 6-token request
