@@ -119,3 +119,43 @@ def test_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(oscar, "LIB_PATH", "/nonexistent/liboscar.so")
     with pytest.raises(RuntimeError):
         oscar.lib()
+
+
+def test_header_is_plain_c_and_the_library_is_callable_from_c(lib, tmp_path):
+    """A C99 program (-pedantic -Werror) built against include/oscar.h and
+    linked to liboscar.so calls the host-only entry points: the boundary needs
+    neither C++ nor Python."""
+    import shutil
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "abi.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "oscar.h"
+int main(void) {
+  oscar_config c = {0};
+  oscar_layout_info info;
+  if (oscar_version() < 10000) return 1;
+  if (strcmp(oscar_status_string(OSCAR_OK), "ok") != 0) return 2;
+  if (oscar_codebook_scratch_bytes(0) != 0) return 3;
+  if (oscar_codebook_scratch_bytes(16) < (size_t)16 * 128 * 4) return 4;
+  c.num_layers = 1; c.num_q_heads = 32; c.num_kv_heads = 8; c.head_dim = 128; c.group_size = 128;
+  c.page_size = 64; c.sink_tokens = 64; c.recent_tokens = 256; c.max_batch = 2;
+  c.max_pages_per_req = 100; c.num_pages = 200;
+  if (oscar_layout(&c, &info) != OSCAR_OK) return 5;
+  if (info.int2_head_bytes != 4608 || info.int2_page_bytes != 8 * 4608) return 6;
+  c.group_size = 16;
+  if (oscar_layout(&c, &info) != OSCAR_ERR_UNSUPPORTED) return 7;
+  puts("abi ok");
+  return 0;
+}
+""")
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(oscar.LIB_PATH)
+    subprocess.run([gcc, "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), oscar.LIB_PATH, f"-Wl,-rpath,{libdir}"], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and "abi ok" in r.stdout, (r.returncode, r.stdout, r.stderr)
