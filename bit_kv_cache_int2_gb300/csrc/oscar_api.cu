@@ -9,6 +9,8 @@
 #include <mutex>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "oscar_internal.cuh"
 
 using namespace oscar;
@@ -72,6 +74,15 @@ struct oscar_ctx {
 namespace {
 
 constexpr int VERSION = 10000;
+
+// An NVTX range named after the ABI call, for timeline tools (a no-op unless
+// a tool is attached; NVTX 3 is header-only).
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
@@ -413,6 +424,7 @@ oscar_status oscar_layout(const oscar_config* cfg, oscar_layout_info* out) {
 }
 
 oscar_status oscar_create(const oscar_config* cfg, oscar_ctx** out) {
+  const CallRange nvtx_range("oscar_create");
   if (!out) return OSCAR_ERR_INVALID_ARG;
   *out = nullptr;
   const oscar_status s = check_cfg(cfg);
@@ -463,6 +475,7 @@ oscar_status oscar_create(const oscar_config* cfg, oscar_ctx** out) {
 }
 
 oscar_status oscar_destroy(oscar_ctx* ctx) {
+  const CallRange nvtx_range("oscar_destroy");
   if (!ctx) return OSCAR_ERR_INVALID_ARG;
   cudaDeviceSynchronize();
   if (ctx->d_rot) cudaFree(ctx->d_rot);
@@ -503,6 +516,7 @@ oscar_status oscar_set_option(oscar_ctx* ctx, int option, int value) {
 oscar_status oscar_set_rotation(oscar_ctx* ctx, int layer, const float* U_K, const float* U_V,
                                 const float* clip_k, const float* clip_v, int rot_mode,
                                 oscar_stream_t stream) {
+  const CallRange nvtx_range("oscar_set_rotation");
   if (!ctx || layer < 0 || layer >= ctx->cfg.num_layers || !clip_k || !clip_v)
     return OSCAR_ERR_INVALID_ARG;
   if (rot_mode != OSCAR_ROT_OSCAR && rot_mode != OSCAR_ROT_HADAMARD && rot_mode != OSCAR_ROT_NONE)
@@ -547,11 +561,13 @@ static oscar_status append_common(oscar_ctx* ctx, int layer, const oscar_cache* 
 
 oscar_status oscar_append(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* k_new,
                           const void* v_new, int batch, oscar_stream_t stream) {
+  const CallRange nvtx_range("oscar_append");
   return append_common(ctx, layer, cache, k_new, v_new, batch, stream, 1);
 }
 
 oscar_status oscar_demote(oscar_ctx* ctx, int layer, const oscar_cache* cache, int batch,
                           oscar_stream_t stream) {
+  const CallRange nvtx_range("oscar_demote");
   return append_common(ctx, layer, cache, nullptr, nullptr, batch, stream, 0);
 }
 
@@ -573,16 +589,19 @@ static oscar_status import_common(oscar_ctx* ctx, int layer, const oscar_cache* 
 
 oscar_status oscar_import_tokens(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* K,
                                  const void* V, int batch, int n, oscar_stream_t stream) {
+  const CallRange nvtx_range("oscar_import_tokens");
   return import_common(ctx, layer, cache, K, V, batch, n, stream, 0);
 }
 
 oscar_status oscar_import_bf16_history(oscar_ctx* ctx, const oscar_cache* cache, const void* K,
                                        const void* V, int batch, int n, oscar_stream_t stream) {
+  const CallRange nvtx_range("oscar_import_bf16_history");
   return import_common(ctx, 0, cache, K, V, batch, n, stream, 1);
 }
 
 oscar_status oscar_append_bf16_history(oscar_ctx* ctx, const oscar_cache* cache, const void* k_new,
                                        const void* v_new, int batch, oscar_stream_t stream) {
+  const CallRange nvtx_range("oscar_append_bf16_history");
   if (!ctx || !cache_ok(cache, true) || !k_new || !v_new) return OSCAR_ERR_INVALID_ARG;
   if (batch < 0 || batch > ctx->cfg.max_batch || !aligned(k_new, 16) || !aligned(v_new, 16))
     return OSCAR_ERR_INVALID_ARG;
@@ -595,6 +614,7 @@ oscar_status oscar_append_bf16_history(oscar_ctx* ctx, const oscar_cache* cache,
 oscar_status oscar_decode(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* q,
                           void* out, float* lse, void* scratch, size_t scratch_bytes, int batch,
                           oscar_stream_t stream) {
+  const CallRange nvtx_range("oscar_decode");
   return decode_common(ctx, layer, cache, q, out, lse, scratch, scratch_bytes, batch, stream, false);
 }
 
@@ -602,6 +622,7 @@ oscar_status oscar_decode_step(oscar_ctx* ctx, int layer, const oscar_cache* cac
                                const void* k_new, const void* v_new, const void* q, void* out,
                                float* lse, void* scratch, size_t scratch_bytes, int batch,
                                oscar_stream_t stream) {
+  const CallRange nvtx_range("oscar_decode_step");
   if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return OSCAR_ERR_INVALID_ARG;
   DecodeArgs a;
   int grid = 0;
@@ -619,6 +640,7 @@ oscar_status oscar_decode_step(oscar_ctx* ctx, int layer, const oscar_cache* cac
 oscar_status oscar_prefill(oscar_ctx* ctx, int layer, const oscar_cache* cache, const void* q,
                            const void* k, const void* v, int T, void* out, float* lse,
                            void* scratch, size_t scratch_bytes, int batch, oscar_stream_t stream) {
+  const CallRange nvtx_range("oscar_prefill");
   if (!ctx || !cache_ok(cache, true) || !q || !k || !v || !out || !scratch) return OSCAR_ERR_INVALID_ARG;
   if (layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
   if (batch < 0 || batch > ctx->cfg.max_batch || T < 1 || T > PF_MAX_T) return OSCAR_ERR_INVALID_ARG;
@@ -686,6 +708,7 @@ void order_eigenvectors(const double* evec, float* U) {
 oscar_status oscar_calibrate(oscar_ctx* ctx, const void* Q, const void* K, const void* V, int N, float* U_K,
                              float* U_V, double* C_Q, double* C_S, void* scratch, size_t scratch_bytes,
                              oscar_stream_t stream) {
+  const CallRange nvtx_range("oscar_calibrate");
   if (!ctx || !Q || !K || !V || !U_K || !U_V || !scratch || N < 1) return OSCAR_ERR_INVALID_ARG;
   if (!aligned(scratch, 256) || !aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16)) return OSCAR_ERR_INVALID_ARG;
   const int G = ctx->G;
@@ -722,6 +745,7 @@ oscar_status oscar_calibrate(oscar_ctx* ctx, const void* Q, const void* K, const
 oscar_status oscar_clip_errors(oscar_ctx* ctx, int layer, int kv_head, const void* Q, const void* K, const void* V,
                                int N, const float* ratios, int M, double* err_k, double* err_v, int* best_k,
                                int* best_v, void* scratch, size_t scratch_bytes, oscar_stream_t stream) {
+  const CallRange nvtx_range("oscar_clip_errors");
   if (!ctx || !Q || !K || !V || !ratios || !err_k || !err_v || !scratch || N < 1 || M < 1)
     return OSCAR_ERR_INVALID_ARG;
   if (layer < 0 || layer >= ctx->cfg.num_layers || kv_head < 0 || kv_head >= ctx->cfg.num_kv_heads)
@@ -759,6 +783,7 @@ oscar_status oscar_clip_errors(oscar_ctx* ctx, int layer, int kv_head, const voi
 oscar_status oscar_decode_noalloc(oscar_ctx* ctx, int layer, const oscar_cache* cache,
                                   const void* q, void* out, float* lse, int batch,
                                   oscar_stream_t stream) {
+  const CallRange nvtx_range("oscar_decode_noalloc");
   if (!ctx || batch < 0 || batch > ctx->cfg.max_batch) return OSCAR_ERR_INVALID_ARG;
   if (layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
   if (scratch_for(ctx, batch, target_items(ctx, batch, false, layer)) > (size_t)OSCAR_NOALLOC_SCRATCH_BYTES)
@@ -773,6 +798,7 @@ oscar_status oscar_decode_noalloc(oscar_ctx* ctx, int layer, const oscar_cache* 
 oscar_status oscar_decode_bf16_history(oscar_ctx* ctx, const oscar_cache* cache, const void* q,
                                        void* out, float* lse, void* scratch, size_t scratch_bytes,
                                        int batch, oscar_stream_t stream) {
+  const CallRange nvtx_range("oscar_decode_bf16_history");
   return decode_common(ctx, 0, cache, q, out, lse, scratch, scratch_bytes, batch, stream, true);
 }
 
@@ -807,6 +833,7 @@ oscar_status oscar_quantize_codebook_f32(const float* x, int n, int group_size, 
 
 oscar_status oscar_set_codebook(oscar_ctx* ctx, int layer, const float* k_ab, const float* v_ab,
                                 oscar_stream_t stream) {
+  const CallRange nvtx_range("oscar_set_codebook");
   if (!ctx || layer < 0 || layer >= ctx->cfg.num_layers) return OSCAR_ERR_INVALID_ARG;
   const int Hkv = ctx->cfg.num_kv_heads;
   std::vector<float> rec((size_t)2 * Hkv * CB_WORDS);
@@ -837,6 +864,7 @@ size_t oscar_codebook_scratch_bytes(int N) {
 oscar_status oscar_fit_codebook(oscar_ctx* ctx, int layer, int kv_head, int which, const void* X, int N,
                                 int max_iters, void* scratch, size_t scratch_bytes, float* ab, int* updates,
                                 oscar_stream_t stream) {
+  const CallRange nvtx_range("oscar_fit_codebook");
   if (!ctx || !X || !scratch || !ab || (which != 0 && which != 1)) return OSCAR_ERR_INVALID_ARG;
   if (layer < 0 || layer >= ctx->cfg.num_layers || kv_head < 0 || kv_head >= ctx->cfg.num_kv_heads)
     return OSCAR_ERR_INVALID_ARG;

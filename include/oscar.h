@@ -44,6 +44,8 @@
  *    entry that is -1 or out of range, a window overflow, a scale out of the
  *    kernel's range, a wait that timed out) are written to a per-context
  *    device error word; kernels never trap.  oscar_get_error reads it.
+ *  - Tracing: each call that launches device work runs inside an NVTX range
+ *    named after the call (NVTX 3, header-only: free unless a tool attaches).
  *  - Ownership: the caller allocates and owns every device buffer it passes
  *    (page pools, page tables, windows, lengths, q, out, scratch).  The
  *    context owns only its rotation tables and its error word, which
