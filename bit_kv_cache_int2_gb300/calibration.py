@@ -45,3 +45,56 @@ def calibrate_kv_head(Q: np.ndarray, K: np.ndarray, V: np.ndarray):
         C_S += SV.T @ SV
     C_S /= G * N
     return _eig_desc(C_Q).astype(np.float32), _eig_desc(C_S).astype(np.float32)
+
+
+# ---------------------------------------------------------------- checkpoint
+# What calibration produces is the only state that outlives a process: per
+# layer the rotation bases and clip ratios, fixed offline [Blog, section
+# "OSCAR把旋转对准attention"], and optionally the Lloyd-Max codebooks.  The
+# KV cache itself lives in the caller's memory.
+
+CHECKPOINT_VERSION = 1
+
+
+def save_layer_params(path, layers) -> None:
+    """Writes per-layer calibration results to one .npz file.
+
+    layers: list (one entry per layer) of dicts with U_K, U_V (float32
+    [Hkv][128][128]), clip_k, clip_v (float32 [Hkv]), mode (an oscar rotation
+    mode) and, optionally, k_ab / v_ab (float32 [Hkv][2] codebooks or None)."""
+    arrays = {"version": np.array(CHECKPOINT_VERSION), "num_layers": np.array(len(layers))}
+    for i, L in enumerate(layers):
+        arrays[f"l{i}_U_K"] = np.asarray(L["U_K"], dtype=np.float32)
+        arrays[f"l{i}_U_V"] = np.asarray(L["U_V"], dtype=np.float32)
+        arrays[f"l{i}_clip_k"] = np.asarray(L["clip_k"], dtype=np.float32)
+        arrays[f"l{i}_clip_v"] = np.asarray(L["clip_v"], dtype=np.float32)
+        arrays[f"l{i}_mode"] = np.array(int(L["mode"]))
+        for key in ("k_ab", "v_ab"):
+            if L.get(key) is not None:
+                arrays[f"l{i}_{key}"] = np.asarray(L[key], dtype=np.float32)
+    np.savez(path, **arrays)
+
+
+def load_layer_params(path):
+    """Reads a file written by save_layer_params; returns the list of dicts
+    (k_ab / v_ab None where no codebook was stored)."""
+    with np.load(path) as f:
+        if int(f["version"]) != CHECKPOINT_VERSION:
+            raise ValueError(f"unsupported calibration checkpoint version {int(f['version'])}")
+        layers = []
+        for i in range(int(f["num_layers"])):
+            L = {k: f[f"l{i}_{k}"].copy() for k in ("U_K", "U_V", "clip_k", "clip_v")}
+            L["mode"] = int(f[f"l{i}_mode"])
+            for key in ("k_ab", "v_ab"):
+                L[key] = f[f"l{i}_{key}"].copy() if f"l{i}_{key}" in f.files else None
+            layers.append(L)
+    return layers
+
+
+def apply_layer_params(ctx, layers) -> None:
+    """Loads every layer's rotation, clips and codebooks into a context."""
+    from . import oscar
+
+    for i, L in enumerate(layers):
+        oscar.oscar_set_rotation(ctx, i, L["U_K"], L["U_V"], L["clip_k"], L["clip_v"], L["mode"])
+        oscar.oscar_set_codebook(ctx, i, L.get("k_ab"), L.get("v_ab"))
