@@ -898,6 +898,34 @@ oscar_status oscar_debug_rotate(oscar_ctx* ctx, int layer, int which, int kv_hea
                                          (cudaStream_t)stream));
 }
 
+oscar_status oscar_check_cache_host(const oscar_config* cfg, const int32_t* seq_lens, const int32_t* hist_lens,
+                                    const int32_t* page_table, int batch, int* bad_request) {
+  if (bad_request) *bad_request = -1;
+  const oscar_status cs = check_cfg(cfg);
+  if (cs != OSCAR_OK) return cs;
+  if (!seq_lens || !hist_lens || !page_table || batch < 0 || batch > cfg->max_batch) return OSCAR_ERR_INVALID_ARG;
+  std::vector<int32_t> owner((size_t)cfg->num_pages, -1);
+  for (int b = 0; b < batch; ++b) {
+    const long long L = seq_lens[b], H = hist_lens[b];
+    oscar_status st = OSCAR_OK;
+    const long long lo = L > SINK + RECENT ? L - SINK - RECENT : 0, hi = L > SINK ? L - SINK : 0;
+    if (L < 0 || H < lo || H > hi) st = OSCAR_ERR_STATE;
+    const long long pages = (H + PAGE - 1) / PAGE;
+    if (st == OSCAR_OK && pages > cfg->max_pages_per_req) st = OSCAR_ERR_RANGE;
+    for (long long p = 0; st == OSCAR_OK && p < pages; ++p) {
+      const int32_t id = page_table[(size_t)b * cfg->max_pages_per_req + p];
+      if (id < 0) st = OSCAR_ERR_NO_PAGE;
+      else if (id >= cfg->num_pages || owner[id] >= 0) st = OSCAR_ERR_RANGE;
+      else owner[id] = b;
+    }
+    if (st != OSCAR_OK) {
+      if (bad_request) *bad_request = b;
+      return st;
+    }
+  }
+  return OSCAR_OK;
+}
+
 int oscar_last_cuda_error(void) { return g_last_cuda_error; }
 
 oscar_status oscar_get_error(oscar_ctx* ctx, oscar_stream_t stream, int* code) {

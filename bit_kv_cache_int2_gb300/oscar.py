@@ -131,6 +131,8 @@ _SIGS = {
     "oscar_quantize_codebook_f32": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_float,
                                      ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
                                     ctypes.c_int),
+    "oscar_check_cache_host": ([ctypes.POINTER(oscar_config), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                ctypes.c_int, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
     "oscar_profile_enable": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "oscar_profile_read": ([ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                             ctypes.POINTER(ctypes.c_double), ctypes.c_int], ctypes.c_int),
@@ -484,6 +486,21 @@ def oscar_import_bf16_history(ctx, cache: dict, K, V, batch, n, stream=None):
 def oscar_quantize_rotated_f32(x, group_size, clip, which, codes, sz, stream=None):
     _check(lib().oscar_quantize_rotated_f32(_ptr(x), x.shape[0], group_size, float(clip), which, _ptr(codes),
                                             _ptr(sz), _stream(stream)), "oscar_quantize_rotated_f32")
+
+
+def check_cache(cfg, cache: dict, batch: int):
+    """Debug aid: copies the cache's lengths and page table to the host and
+    checks them (oscar_check_cache_host).  Returns (status, first bad request
+    or -1); status OK when the state is consistent."""
+    import numpy as np
+
+    seq = np.ascontiguousarray(cache["seq_lens"].cpu().numpy(), dtype=np.int32)
+    hist = np.ascontiguousarray(cache["hist_lens"].cpu().numpy(), dtype=np.int32)
+    pt = np.ascontiguousarray(cache["page_table"].cpu().numpy(), dtype=np.int32)
+    bad = ctypes.c_int(-1)
+    st = lib().oscar_check_cache_host(ctypes.byref(cfg), _np_ptr(seq), _np_ptr(hist), _np_ptr(pt), batch,
+                                      ctypes.byref(bad))
+    return st, bad.value
 
 
 def oscar_quantize_codebook_f32(x, group_size, clip, a, b, which, codes, sz, stream=None):

@@ -478,6 +478,20 @@ oscar_status oscar_debug_rotate(oscar_ctx* ctx, int layer, int which,
                                 int kv_head, const void* x, float* x_rot,
                                 int n, oscar_stream_t stream);
 
+/* Debug aid: checks host copies of a cache's lengths and page table against
+ * the configuration, without touching the device.  For every request b < batch:
+ *   max(L - 320, 0) <= H <= max(L - 64, 0), L = seq_lens[b], H = hist_lens[b]
+ *   (the recent window holds 0..256 tokens), ceil(H / 64) <= max_pages_per_req,
+ *   and each of its first ceil(H / 64) page-table entries is in [0, num_pages)
+ *   and used by no other history slot of the batch.
+ *   seq_lens, hist_lens : host int32 [batch]
+ *   page_table : host int32 [batch][max_pages_per_req]
+ *   bad_request : host int out (or NULL), the first failing request, -1 if none.
+ * Returns OSCAR_OK, OSCAR_ERR_STATE (lengths), OSCAR_ERR_NO_PAGE (a -1 entry)
+ * or OSCAR_ERR_RANGE (an id out of range, shared, or too many pages). */
+oscar_status oscar_check_cache_host(const oscar_config* cfg, const int32_t* seq_lens, const int32_t* hist_lens,
+                                    const int32_t* page_table, int batch, int* bad_request);
+
 /* Synchronise `stream`, return the first device-side error recorded since
  * the last call in *code (OSCAR_OK if none) and clear it. */
 oscar_status oscar_get_error(oscar_ctx* ctx, oscar_stream_t stream, int* code);

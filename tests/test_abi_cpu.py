@@ -159,3 +159,37 @@ int main(void) {
                     str(src), "-o", str(exe), oscar.LIB_PATH, f"-Wl,-rpath,{libdir}"], check=True)
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0 and "abi ok" in r.stdout, (r.returncode, r.stdout, r.stderr)
+
+
+def _state(B, mpr, pages_of, L, H):
+    import torch
+
+    pt = torch.full((B, mpr), -1, dtype=torch.int32)
+    for b, ids in enumerate(pages_of):
+        pt[b, :len(ids)] = torch.tensor(ids, dtype=torch.int32)
+    return {"seq_lens": torch.tensor(L, dtype=torch.int32), "hist_lens": torch.tensor(H, dtype=torch.int32),
+            "page_table": pt}
+
+
+def test_cache_state_check_on_host(lib):
+    """oscar_check_cache_host: lengths within the three-region rules, page
+    ids present, in range and owned by one history slot only."""
+    cfg = oscar.make_config(1, 8, 2, 128, max_batch=3, max_pages_per_req=4, num_pages=8)
+    ok = _state(3, 4, [[5, 1], [0], []], [320 + 100, 320 + 64, 200], [100, 64, 0])
+    assert oscar.check_cache(cfg, ok, 3) == (oscar.OK, -1)
+    # demotes shrink the window: history up to L - 64 is still consistent
+    assert oscar.check_cache(cfg, _state(1, 4, [[2, 3, 4]], [200], [136]), 1) == (oscar.OK, -1)
+    cases = [
+        (_state(2, 4, [[1, 3], [2]], [420, 1000], [100, 600]), (oscar.ERR_STATE, 1)),     # history too short
+        (_state(1, 4, [[1, 2, 3]], [200], [137]), (oscar.ERR_STATE, 0)),                  # more than L - 64
+        (_state(1, 4, [[1, -1]], [320 + 100], [100]), (oscar.ERR_NO_PAGE, 0)),            # missing page
+        (_state(1, 4, [[1, 8]], [320 + 100], [100]), (oscar.ERR_RANGE, 0)),               # id out of range
+        (_state(2, 4, [[1, 2], [2]], [420, 330], [100, 10]), (oscar.ERR_RANGE, 1)),       # page shared
+        (_state(1, 4, [[1, 1]], [420], [100]), (oscar.ERR_RANGE, 0)),                     # page twice
+        (_state(1, 4, [[0, 1, 2, 3]], [320 + 4 * 64 + 1], [4 * 64 + 1]), (oscar.ERR_RANGE, 0)),  # > max pages
+        (_state(1, 4, [[]], [-1], [0]), (oscar.ERR_STATE, 0)),
+    ]
+    for st, want in cases:
+        assert oscar.check_cache(cfg, st, st["seq_lens"].numel()) == want, want
+    # entries beyond a request's history pages are not looked at
+    assert oscar.check_cache(cfg, _state(1, 4, [[1, 7, 9, 9]], [320 + 70], [70]), 1) == (oscar.OK, -1)
