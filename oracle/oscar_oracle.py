@@ -31,7 +31,12 @@ all-zero codes; groups are g consecutive channels after P_br; eigenvectors in
 descending eigenvalue order, each column signed so its largest-|.| entry is
 positive; C_Q and C_S pool the G query heads of a kv head; S is the causal
 softmax(QK^T/sqrt(d)); softmax scale 1/sqrt(d); the recent window holds the
-newest 256 tokens including the one just appended.
+newest 256 tokens including the one just appended.  The clip search and the
+Lloyd-Max codebook (symmetric levels on the uniform quantiser's normalised
+value, fitted by the two-level fold) carry their readings in their sections
+below.  Every function here is pinned by tests/test_oracle.py (closed forms,
+worked examples, textbook tables, brute force); beyond the stated tolerances
+only the bf16 rounding of decode outputs is unpinned.
 """
 from __future__ import annotations
 
