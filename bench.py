@@ -173,7 +173,7 @@ def build_workload(wl, dev, n_copies, extra, seed=0, bf16_copies=0):
     import numpy as np
     import torch
 
-    from bit_kv_cache_int2_gb300 import calibration, oscar, synth
+    from bit_kv_cache_int2_gb300 import oscar, synth
 
     B, Hq, Hkv, g, L = wl["B"], wl["Hq"], wl["Hkv"], wl["g"], wl["L"]
     G = Hq // Hkv
@@ -181,12 +181,17 @@ def build_workload(wl, dev, n_copies, extra, seed=0, bf16_copies=0):
     cfg = oscar.make_config(1, Hq, Hkv, g, max_batch=B, max_pages_per_req=pages, num_pages=pages * B)
     ctx = oscar.oscar_create(cfg)
     stats = [synth.head_stats(seed, "bench", 0, h, n_out=wl["n_out"], f_key=wl["f_key"]) for h in range(Hkv)]
+    # rotation bases from the library's GPU calibration (covariances on the
+    # device, eigenvectors by cuSOLVER) on 2048 seeded calibration tokens
     UK, UV = [], []
+    cscr = oscar.calibration_scratch(G, 2048, 0, dev)
     for h in range(Hkv):
-        Qc, Kc, Vc = synth.calibration_set(seed, "bench", 0, h, stats[h], G=G, n=2048)
-        uq, us = calibration.calibrate_kv_head(Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy())
+        Qc, Kc, Vc = (t.to(dev).contiguous() for t in synth.calibration_set(seed, "bench", 0, h, stats[h], G=G,
+                                                                          n=2048))
+        uq, us, _, _ = oscar.oscar_calibrate(ctx, Qc, Kc, Vc, 2048, cscr)
         UK.append(uq)
         UV.append(us)
+    del cscr
     UK, UV = np.stack(UK), np.stack(UV)
     oscar.oscar_set_rotation(ctx, 0, UK, UV, [wl["clip"]] * Hkv, [wl["clip"]] * Hkv, oscar.ROT_OSCAR)
     base = oscar.alloc_cache(cfg, dev)
@@ -1055,6 +1060,128 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
+def percentiles(xs):
+    """median, p10, p90 of a list of per-call times."""
+    import numpy as np
+
+    a = np.asarray(xs, dtype=np.float64)
+    return float(np.median(a)), float(np.percentile(a, 10)), float(np.percentile(a, 90))
+
+
+def per_call_times(fn, n, stream):
+    """CUDA-event time of each of n back-to-back calls on `stream` (µs): one
+    event before every call and one after the last, so call i spans events i
+    and i + 1.  The host enqueues ahead of the device, so each interval is the
+    call's device time (an event between two calls ends their programmatic
+    overlap, which a bulk-timed run keeps)."""
+    import torch
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    torch.cuda.synchronize()
+    for i in range(n):
+        ev[i].record(stream)
+        fn(i)
+    ev[n].record(stream)
+    torch.cuda.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(n)]
+
+
+LEGS = ("decode", "step", "bf16", "append", "cuda_core", "tensor_single", "prefill")
+
+
+def run_leg(args, wl):
+    """One operation of the hot path on the 100K workload, alone: --warmup
+    untimed calls, then --steps calls timed one by one with CUDA events,
+    rotating over cache copies larger than 3x L2.  A short command for
+    profiling one kernel (the full bench runs every other measurement too).
+      decode        oscar_decode (INT2, default implementation)
+      step          oscar_decode_step (append with its demotion + decode)
+      bf16          oscar_decode_bf16_history (the BF16-history baseline)
+      append        oscar_append (one token per request and kv head, each demoting one)
+      cuda_core     oscar_decode with OSCAR_DECODE_CUDA_CORE
+      tensor_single oscar_decode with OSCAR_DECODE_TENSOR_SINGLE
+      prefill       oscar_prefill, a 64-token chunk"""
+    import torch
+
+    from bit_kv_cache_int2_gb300 import build as B
+    from bit_kv_cache_int2_gb300 import oscar
+
+    B.build()
+    dev = "cuda:0"
+    stream = torch.cuda.current_stream()
+    Hkv, g, Bsz, L0 = wl["Hkv"], wl["g"], wl["B"], wl["L"]
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    bf16 = args.leg == "bf16"
+    per_copy = (Hkv * Bsz * ((L0 - 320) * 512 + 320 * 512) + ((L0 - 320 + 63) // 64) * 4 if bf16 else
+                algorithmic_bytes(L0 - 320, L0, Hkv, g) * Bsz)
+    n_copies = max(2, -(-3 * l2 // per_copy))
+    n_calls = args.warmup + args.steps
+    appends = args.leg in ("step", "append")
+    extra = max(n_calls // n_copies + 16, 80) if appends else 16
+    wk = build_workload(wl, dev, 1 if bf16 else n_copies, extra, bf16_copies=n_copies if bf16 else 0)
+    ctx, cfg, q = wk["ctx"], wk["cfg"], wk["q"]
+    out = torch.empty_like(q)
+    scratch = oscar.alloc_scratch(cfg, dev, prefill=args.leg == "prefill")
+    if args.leg == "cuda_core":
+        oscar.oscar_set_option(ctx, oscar.OPT_DECODE_IMPL, 1)
+    if args.leg == "tensor_single":
+        oscar.oscar_set_option(ctx, oscar.OPT_DECODE_IMPL, 2)
+    tok_bytes = Bsz * Hkv * 128 * 2
+    kv_new = (wk["K"][:, :, L0:L0 + extra].permute(2, 0, 1, 3).contiguous(),
+              wk["V"][:, :, L0:L0 + extra].permute(2, 0, 1, 3).contiguous())
+    k_base, v_base = kv_new[0].data_ptr(), kv_new[1].data_ptr()
+    cnt = [0] * n_copies
+    bytes_per_call = per_copy
+    if args.leg in ("decode", "cuda_core", "tensor_single"):
+        calls = [oscar.bind_decode(ctx, 0, c, q, out, None, scratch, Bsz) for c in wk["copies"]]
+        fn = lambda i: calls[i % n_copies]()
+    elif args.leg == "bf16":
+        fn = lambda i: oscar.oscar_decode_bf16_history(wk["bctx"], wk["bf"][i % n_copies], q, out, None, scratch,
+                                                       Bsz)
+    elif args.leg in ("step", "append"):
+        calls = [oscar.bind_decode_step(ctx, 0, c, q, out, None, scratch, Bsz) if args.leg == "step" else
+                 oscar.bind_append(ctx, 0, c, Bsz) for c in wk["copies"]]
+
+        def fn(i):
+            c = i % n_copies
+            calls[c](k_base + cnt[c] * tok_bytes, v_base + cnt[c] * tok_bytes)
+            cnt[c] += 1
+        if args.leg == "append":
+            bytes_per_call = Bsz * Hkv * 2 * (3 * 256 + 32 + (128 // g) * 4)
+    else:  # prefill
+        T_pf = 64
+        q_pf = torch.stack([torch.cat([synth_queries(wk["stats"][h], T_pf, wl["Hq"] // Hkv, b, h, dev)
+                                       for h in range(Hkv)], dim=1) for b in range(Bsz)]).contiguous()
+        k_pf = wk["K"][:, :, L0:L0 + T_pf].permute(0, 2, 1, 3).contiguous()
+        v_pf = wk["V"][:, :, L0:L0 + T_pf].permute(0, 2, 1, 3).contiguous()
+        out_pf = torch.empty_like(q_pf)
+        fn = lambda i: oscar.oscar_prefill(ctx, 0, wk["copies"][i % n_copies], q_pf, k_pf, v_pf, T_pf, out_pf, None,
+                                           scratch, Bsz)
+        bytes_per_call = None
+    for i in range(args.warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.warmup, n_calls):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    mean_us = e0.elapsed_time(e1) * 1e3 / args.steps
+    err = oscar.oscar_get_error(wk["bctx"] if bf16 else ctx)
+    assert err == 0, f"device error {err}"
+    line = {"leg": args.leg, "workload": args.workload, "calls": args.steps, "mean_us": mean_us,
+            "cache_copies": n_copies}
+    if not appends:  # a second pass, timed call by call
+        med, p10, p90 = percentiles(per_call_times(lambda i: fn(args.warmup + i), args.steps, stream))
+        line.update({"median_us": med, "p10_us": p10, "p90_us": p90})
+    if bytes_per_call:
+        peak, kind = peaks()
+        line.update({"bytes_per_call": bytes_per_call, "hbm_gbs": bytes_per_call / (mean_us * 1e-6) / 1e9,
+                     "frac_of_" + kind + "_hbm": bytes_per_call / (mean_us * 1e-6) / 1e9 / peak})
+    print(json.dumps(line), flush=True)
+
+
 def run_codebook_leg(args, wl):
     """Only the Lloyd-Max codebook decode on the workload: fits from the
     calibration sets, a cache written with them, and --steps timed decodes
@@ -1122,8 +1249,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_8b_100k", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--leg", choices=["all", "codebook"], default="all",
-                    help="codebook: only the Lloyd-Max codebook decode (a short command to profile it)")
+    ap.add_argument("--leg", choices=["all", "codebook"] + list(LEGS), default="all",
+                    help="one operation alone on the workload, a short command to profile it (see run_leg); "
+                         "codebook: only the Lloyd-Max codebook decode")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = WORKLOADS[args.workload]
@@ -1131,6 +1259,8 @@ def main():
         run_reference(args, wl)
     elif args.leg == "codebook":
         run_codebook_leg(args, wl)
+    elif args.leg in LEGS:
+        run_leg(args, wl)
     else:
         run_ours(args, wl)
 

@@ -359,9 +359,13 @@ constexpr int NOALLOC_MAX_DEVICES = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
 
-oscar_status noalloc_scratch(void** out) {
+// The buffer of the context's device.  The address is looked up with that
+// device current, so the call is refused when another device is current: the
+// lookup would give the other device's copy of the buffer.
+oscar_status noalloc_scratch(const oscar_ctx* ctx, void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return cuda_status(cudaErrorInvalidDevice);
+  if (dev != ctx->device) return OSCAR_ERR_INVALID_ARG;
   if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return OSCAR_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (!g_noalloc_ptr[dev]) {
@@ -789,7 +793,7 @@ oscar_status oscar_decode_noalloc(oscar_ctx* ctx, int layer, const oscar_cache* 
   if (scratch_for(ctx, batch, target_items(ctx, batch, false, layer)) > (size_t)OSCAR_NOALLOC_SCRATCH_BYTES)
     return OSCAR_ERR_TOO_LARGE;
   void* scratch = nullptr;
-  const oscar_status st = noalloc_scratch(&scratch);
+  const oscar_status st = noalloc_scratch(ctx, &scratch);
   if (st != OSCAR_OK) return st;
   return decode_common(ctx, layer, cache, q, out, lse, scratch, OSCAR_NOALLOC_SCRATCH_BYTES, batch,
                        stream, false);

@@ -1720,12 +1720,8 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
 // share it).
 template <int NG, int IMPL>
 cudaError_t ensure_decode_smem(int bytes) {
-  static int current = -1;
-  if (bytes <= current) return cudaSuccess;
-  const cudaError_t e =
-      cudaFuncSetAttribute(decode_kernel<NG, IMPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) current = bytes;
-  return e;
+  static int limit[MAX_DEVICES];
+  return raise_smem_limit(decode_kernel<NG, IMPL>, limit, bytes);
 }
 
 template <int NG, int IMPL>
@@ -1741,13 +1737,9 @@ cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t st) {
   const MergeLayout ML = merge_layout(a.B);
   if ((ML.off_mbar % 8) || (ML.off_y % 16) || (ML.off_to % 16) || (ML.off_wo % 16)) return cudaErrorInvalidValue;
   if (a.merge_hpc < 1 || a.cv.G % a.merge_hpc) return cudaErrorInvalidValue;
-  static int configured = -1;  // dynamic shared memory size the kernel was last configured for
-  if (configured < ML.total) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ML.total);
-    if (e != cudaSuccess) return e;
-    configured = ML.total;
-  }
+  static int limit[MAX_DEVICES];
+  const cudaError_t e = raise_smem_limit(merge_kernel, limit, ML.total);
+  if (e != cudaSuccess) return e;
   return launch_pdl(merge_kernel, dim3(a.B * a.cv.Hkv * (a.cv.G / a.merge_hpc)), dim3(MW * 32), ML.total, st, a);
 }
 
@@ -1774,9 +1766,14 @@ size_t decode_scratch_bytes(int B, int Hq, int Hkv, int G, int max_target_items)
 // (cached per kernel variant and shared-memory size).
 template <int NG, int IMPL>
 int occupancy_t(const DecodeArgs& a) {
-  static int cached_smem = -1, cached_occ = 0;
+  static int cached_smem[MAX_DEVICES], cached_occ[MAX_DEVICES];
   const SmemLayout L = smem_layout(a.cv.head_bytes, a.B, IMPL, a.cv.G);
-  if (cached_smem == L.total) return cached_occ;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  if (cached_smem[dev] == L.total) return cached_occ[dev];
   if (ensure_decode_smem<NG, IMPL>(L.total) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
@@ -1787,8 +1784,8 @@ int occupancy_t(const DecodeArgs& a) {
     (void)cudaGetLastError();
     return 0;
   }
-  cached_occ = n;
-  cached_smem = L.total;
+  cached_occ[dev] = n;
+  cached_smem[dev] = L.total;
   return n;
 }
 

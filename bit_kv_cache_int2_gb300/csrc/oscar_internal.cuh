@@ -304,6 +304,26 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...);
 }
 
+// -------------------------------------------- per-device kernel attributes
+// cudaFuncSetAttribute applies to the current device only, so a raised
+// dynamic shared-memory limit is remembered per device ordinal: `limit` is a
+// zero-initialised array of MAX_DEVICES entries owned by the caller (one per
+// kernel).  The limit is only ever raised.  Concurrent callers may both set
+// the attribute, which is harmless.
+constexpr int MAX_DEVICES = 64;
+
+template <typename Kernel>
+cudaError_t raise_smem_limit(Kernel kernel, int* limit, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+  if (bytes <= limit[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) limit[dev] = bytes;
+  return e;
+}
+
 // ----------------------------------------------------- bounded mbarrier use
 __device__ __forceinline__ void mbar_init(uint64_t* bar, int count) {
   uint32_t a = (uint32_t)__cvta_generic_to_shared(bar);

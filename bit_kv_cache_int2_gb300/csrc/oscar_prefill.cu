@@ -1403,16 +1403,11 @@ int prefill_max_splits(int B, int Hkv, int G, int T) {
 }
 
 static cudaError_t ensure_prefill_smem() {
-  static int done = 0;  // per process; the attribute is per device function
-  if (done) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(prefill_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(prefill_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MERGE_SMEM);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM);
-  if (e == cudaSuccess) done = 1;
+  static int l_attn[MAX_DEVICES], l_prep[MAX_DEVICES], l_merge[MAX_DEVICES], l_tc[MAX_DEVICES];
+  cudaError_t e = raise_smem_limit(prefill_attn_kernel, l_attn, PF_SMEM);
+  if (e == cudaSuccess) e = raise_smem_limit(prefill_prep_kernel, l_prep, PREP_SMEM);
+  if (e == cudaSuccess) e = raise_smem_limit(prefill_merge_kernel, l_merge, MERGE_SMEM);
+  if (e == cudaSuccess) e = raise_smem_limit(prefill_tc_kernel, l_tc, tc::SMEM);
   return e;
 }
 

@@ -416,9 +416,12 @@ oscar_status oscar_quantize_codebook_f32(const float* x, int n, int group_size, 
  * device, and plain C callers with no device allocator of their own.
  *  - Every GPU that loads the library holds this buffer until the process
  *    exits, whether or not the call is used.
- *  - The first call on each device (the device current at the call) looks up
- *    the buffer's device address once; make that first call before any
- *    stream capture begins.
+ *  - The context's device must be the current device
+ *    (OSCAR_ERR_INVALID_ARG otherwise).  The first call on each device looks
+ *    up the buffer's device address once and keeps it; make that first call
+ *    before any stream capture begins.  The kept address belongs to the
+ *    device's primary context: after a device reset it is stale, so do not
+ *    call this entry point again in that process.
  *  - All calls share the one buffer and it keeps the last call's contents.
  *    The kernels reset everything that must start at zero themselves.  Calls
  *    that may run at the same time on the GPU (different streams, different

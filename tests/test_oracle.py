@@ -63,6 +63,39 @@ def test_rotation_factors_in_order():
         np.testing.assert_allclose(R[:, j], H[:, O.bit_reverse(j, 3)])
 
 
+def test_rotation_equalises_channel_importance():
+    # [News, "OSCAR 的不同之处"; Blog, "OSCAR把旋转对准attention"]: after the
+    # eigenbasis U of C, the Hadamard factor spreads every eigen-direction
+    # evenly over the channels.  With R = U H P, R^T C R = P^T H^T diag(lambda) H P,
+    # whose diagonal is tr(C)/d in every channel.  A U placed to the right of H
+    # (H U P) leaves an uneven diagonal, so this pins the factor order with U != I.
+    rng = np.random.default_rng(21)
+    A = rng.standard_normal((128, 40)) * np.linspace(0.1, 5.0, 40)
+    C = A @ A.T / 40
+    U = O.eigenbasis(C)
+    R = O.rotation(U, O.ROT_OSCAR)
+    diag = np.diag(R.T @ C @ R)
+    np.testing.assert_allclose(diag, np.full(128, np.trace(C) / 128), rtol=0, atol=1e-10 * np.trace(C))
+    H = scipy.linalg.hadamard(128) / np.sqrt(128)
+    P = O.bit_reversal_matrix(128)
+    wrong = H @ U @ P
+    assert np.ptp(np.diag(wrong.T @ C @ wrong)) > 1e-3 * np.trace(C) / 128
+
+
+def test_rotation_with_a_permutation_basis_reorders_rows():
+    # U a permutation (U[i, pi(i)] = 1): row i of U H P is row pi(i) of H P, and
+    # (H P)[k, j] = H[k, bitrev(j)], built here from scipy's Hadamard matrix.
+    rng = np.random.default_rng(22)
+    pi = rng.permutation(16)
+    U = np.zeros((16, 16))
+    U[np.arange(16), pi] = 1.0
+    R = O.rotation(U, O.ROT_OSCAR)
+    H = scipy.linalg.hadamard(16) / 4.0
+    for i in range(16):
+        for j in range(16):
+            assert R[i, j] == H[pi[i], O.bit_reverse(j, 4)]
+
+
 # ------------------------------------------------------------- calibration
 
 def test_query_covariance_brute_force():
@@ -257,6 +290,58 @@ def test_v_layout_hand_positions():
     codes[16, 5] = 2  # channel 5 row, token 16 -> word 0 bit 4
     blk = O.pack_v_block(codes)
     assert blk[5 * 16] == 2 << 4 and blk.sum() == 2 << 4
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+def test_head_block_sizes_match_the_documented_layout(g):
+    # include/oscar.h: 4608 B per head at g = 128, 5120 B at g = 64, 6144 B at g = 32
+    assert O.int2_head_block_bytes(g) == {128: 4608, 64: 5120, 32: 6144}[g]
+
+
+def test_parse_head_block_reads_hand_placed_fields():
+    # A g = 32 head block written byte by byte at the offsets the page-layout
+    # comment of include/oscar.h gives, worked by hand (not through the oracle's
+    # packers):
+    #  * K code 3 for token 5, channel 77 = 64*1 + 16*0 + 8*1 + 2*2 + 1
+    #    (A=1, B=0, C=1, D=2, E=1) -> word 2D+A = 5, bit 16E+2(2B+C) = 18
+    #    -> byte 5*32 + 4*5 + 2 = 182, bits 2..3.
+    #  * V code 2 for channel 100, token 45 = 16*2 + 8*1 + 2*2 + 1
+    #    (S=2, A=1, T=2, E=1) -> word 2, bit 16 + 2*(2*2+1) = 26
+    #    -> byte 2048 + 100*16 + 4*2 + 3 = 3659, bits 2..3.
+    #  * K (s, z) of token 9, group 3: 4096 + (9*4 + 3)*4 = 4252 (s), 4254 (z).
+    #  * V (s, z) of token 5, group 1: V table at 4096 + 64*4*4 = 5120;
+    #    5120 + (5*4 + 1)*4 = 5204 (s), 5206 (z).
+    blk = np.zeros(6144, dtype=np.uint8)
+    blk[182] = 3 << 2
+    blk[3659] = 2 << 2
+    blk[4252:4254] = np.frombuffer(np.float16(0.375).tobytes(), np.uint8)
+    blk[4254:4256] = np.frombuffer(np.float16(-1.5).tobytes(), np.uint8)
+    blk[5204:5206] = np.frombuffer(np.float16(2.25).tobytes(), np.uint8)
+    blk[5206:5208] = np.frombuffer(np.float16(-0.125).tobytes(), np.uint8)
+    d = O.parse_head_block(blk, 32)
+    kc = np.zeros((64, 128), np.uint8)
+    kc[5, 77] = 3
+    vc = np.zeros((64, 128), np.uint8)
+    vc[45, 100] = 2
+    np.testing.assert_array_equal(d["k_codes"], kc)
+    np.testing.assert_array_equal(d["v_codes"], vc)
+    for name, tok, grp, val in (("k_s", 9, 3, 0.375), ("k_z", 9, 3, -1.5), ("v_s", 5, 1, 2.25),
+                                ("v_z", 5, 1, -0.125)):
+        ref = np.zeros((64, 4), np.float16)
+        ref[tok, grp] = val
+        np.testing.assert_array_equal(d[name], ref, err_msg=name)
+
+
+def test_parse_head_block_g128_sz_tables_do_not_overlap_the_codes():
+    # g = 128: one group, K s/z at 4096 + 4*t and V s/z at 4096 + 256 + 4*t
+    blk = np.zeros(4608, dtype=np.uint8)
+    blk[4096 + 4 * 63:4096 + 4 * 63 + 2] = np.frombuffer(np.float16(1.0).tobytes(), np.uint8)
+    blk[4352 + 4 * 0 + 2:4352 + 4 * 0 + 4] = np.frombuffer(np.float16(-3.0).tobytes(), np.uint8)
+    d = O.parse_head_block(blk, 128)
+    assert d["k_s"][63, 0] == 1.0 and np.count_nonzero(d["k_s"]) == 1
+    assert d["v_z"][0, 0] == -3.0 and np.count_nonzero(d["v_z"]) == 1
+    assert not d["k_z"].any() and not d["v_s"].any()
+    assert not d["k_codes"].any() and not d["v_codes"].any()
 
 
 def test_layouts_are_bijections():
