@@ -1086,7 +1086,7 @@ def per_call_times(fn, n, stream):
     return [ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(n)]
 
 
-LEGS = ("decode", "step", "bf16", "append", "cuda_core", "tensor_single", "prefill")
+LEGS = ("decode", "step", "bf16", "append", "cuda_core", "tensor_single", "tcgen05", "prefill")
 
 
 def run_leg(args, wl):
@@ -1100,6 +1100,7 @@ def run_leg(args, wl):
       append        oscar_append (one token per request and kv head, each demoting one)
       cuda_core     oscar_decode with OSCAR_DECODE_CUDA_CORE
       tensor_single oscar_decode with OSCAR_DECODE_TENSOR_SINGLE
+      tcgen05       oscar_decode with OSCAR_DECODE_TCGEN05
       prefill       oscar_prefill, a 64-token chunk"""
     import torch
 
@@ -1126,13 +1127,15 @@ def run_leg(args, wl):
         oscar.oscar_set_option(ctx, oscar.OPT_DECODE_IMPL, 1)
     if args.leg == "tensor_single":
         oscar.oscar_set_option(ctx, oscar.OPT_DECODE_IMPL, 2)
+    if args.leg == "tcgen05":
+        oscar.oscar_set_option(ctx, oscar.OPT_DECODE_IMPL, 3)
     tok_bytes = Bsz * Hkv * 128 * 2
     kv_new = (wk["K"][:, :, L0:L0 + extra].permute(2, 0, 1, 3).contiguous(),
               wk["V"][:, :, L0:L0 + extra].permute(2, 0, 1, 3).contiguous())
     k_base, v_base = kv_new[0].data_ptr(), kv_new[1].data_ptr()
     cnt = [0] * n_copies
     bytes_per_call = per_copy
-    if args.leg in ("decode", "cuda_core", "tensor_single"):
+    if args.leg in ("decode", "cuda_core", "tensor_single", "tcgen05"):
         calls = [oscar.bind_decode(ctx, 0, c, q, out, None, scratch, Bsz) for c in wk["copies"]]
         fn = lambda i: calls[i % n_copies]()
     elif args.leg == "bf16":

@@ -114,6 +114,7 @@ size_t scratch_for(const oscar_ctx* ctx, int B, int target) {
 // time.  layer < 0: the variant without a codebook.
 int kernel_impl(const oscar_ctx* ctx, int layer = -1) {
   if (layer >= 0 && ctx->has_cb[layer]) return 4;
+  if (ctx->impl == OSCAR_DECODE_TCGEN05) return 5;
   if (ctx->impl == OSCAR_DECODE_CUDA_CORE) return 1;
   if (ctx->impl == OSCAR_DECODE_TENSOR_SINGLE || ctx->G > 4) return 0;
   return 3;
@@ -135,6 +136,10 @@ int decode_ctas(const oscar_ctx* ctx, int batch, bool bf16_history, int layer = 
 }
 
 int target_items(const oscar_ctx* ctx, int batch, bool bf16_history, int layer = -1) {
+  // the tensor-memory kernel: one history record per (CTA, segment) pair and
+  // five window records per segment, i.e. num_sms + 6 B Hkv partial records
+  // (the scratch layout adds 2 B Hkv to the target)
+  if (!bf16_history && kernel_impl(ctx, layer) == 5) return ctx->num_sms + 4 * batch * ctx->cfg.num_kv_heads;
   const int per = ctx->items_per_cta ? ctx->items_per_cta : AUTO_ITEMS_PER_CTA;
   int t = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, layer) * per;
   if (t > MAX_TARGET_ITEMS) t = MAX_TARGET_ITEMS;
@@ -329,6 +334,19 @@ oscar_status decode_args(oscar_ctx* ctx, int layer, const oscar_cache* cache, co
   a.merge_hpc = ctx->G;
   while (a.merge_hpc % 2 == 0 && batch * ctx->cfg.num_kv_heads * (ctx->G / a.merge_hpc) < ctx->num_sms)
     a.merge_hpc /= 2;
+  a.balanced = 0;
+  a.bal_grid = 0;
+  a.bal_wch = 0;
+  if (a.impl == 5) {
+    // one CTA per SM (the kernel holds all 512 tensor-memory columns)
+    if (decode_tc_smem_bytes(a.cv.head_bytes, batch) > 227 * 1024) return OSCAR_ERR_UNSUPPORTED;
+    a.balanced = 1;
+    a.bal_grid = ctx->num_sms;
+    a.bal_wch = decode_tc_window_weight();
+    grid = ctx->num_sms;
+    a.resident = 0;
+    return OSCAR_OK;
+  }
   grid = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, vlayer);
   a.resident = ctx->items_per_cta == 0 ? grid : 0;
   return OSCAR_OK;
@@ -414,8 +432,11 @@ oscar_status oscar_layout(const oscar_config* cfg, oscar_layout_info* out) {
   out->bf16_page_bytes = (size_t)BF16_HEAD_BYTES * cfg->num_kv_heads;
   out->sink_bytes = (size_t)cfg->max_batch * cfg->num_kv_heads * SINK * D * 2;
   out->ring_bytes = (size_t)cfg->max_batch * cfg->num_kv_heads * RECENT * D * 2;
-  out->decode_scratch_bytes = decode_scratch_bytes(cfg->max_batch, cfg->num_q_heads,
-                                                   cfg->num_kv_heads, G, MAX_TARGET_ITEMS);
+  // enough partial records for every decode kernel: the item list of the
+  // mma.sync kernels (at most MAX_TARGET_ITEMS) and the tensor-memory
+  // kernel's (one per SM, at most MAX_TARGET_ITEMS SMs, plus 4 B Hkv)
+  out->decode_scratch_bytes = decode_scratch_bytes(cfg->max_batch, cfg->num_q_heads, cfg->num_kv_heads, G,
+                                                   MAX_TARGET_ITEMS + 4 * cfg->max_batch * cfg->num_kv_heads);
   // the split count (and so the partials) is not monotone in the batch: take the largest
   size_t pf = 0;
   for (int b = 1; b <= cfg->max_batch; ++b) {
@@ -496,7 +517,8 @@ oscar_status oscar_set_option(oscar_ctx* ctx, int option, int value) {
   if (!ctx) return OSCAR_ERR_INVALID_ARG;
   switch (option) {
     case OSCAR_OPT_DECODE_IMPL:
-      if (value != OSCAR_DECODE_TENSOR && value != OSCAR_DECODE_CUDA_CORE && value != OSCAR_DECODE_TENSOR_SINGLE)
+      if (value != OSCAR_DECODE_TENSOR && value != OSCAR_DECODE_CUDA_CORE && value != OSCAR_DECODE_TENSOR_SINGLE &&
+          value != OSCAR_DECODE_TCGEN05)
         return OSCAR_ERR_INVALID_ARG;
       ctx->impl = value;
       return OSCAR_OK;

@@ -21,6 +21,7 @@
 //                  finish an item of a (request, kv head) merges its partials,
 //                  un-rotates the history part by R_V^T and writes the output.
 #include "oscar_internal.cuh"
+#include "oscar_window.cuh"
 
 namespace oscar {
 
@@ -746,142 +747,6 @@ __device__ __forceinline__ void int2_page_core(CoreState& S, const uint8_t* stag
   __syncwarp();
 }
 
-// ------------------------------------------------------ BF16 chunk (mma)
-struct Bf16State {
-  float oacc[8][4];  // o^T: m-tile j rows channel 16gid+2j / 16gid+2j+1, cols heads 2tq, 2tq+1
-  float m[2];
-  float l[2];
-  uint32_t bq[8][2];  // raw q (bf16) B fragments, column = head gid
-};
-
-__device__ __forceinline__ uint4 ldg_nc(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
-// One 16-token tile of BF16 keys/values in registers: the rows this thread
-// feeds to the tensor cores.
-struct Bf16Tile {
-  uint4 ka[4], kb[4];  // K rows 16s+gid and 16s+gid+8, channels 32tq..32tq+31
-  uint4 vv[4][2];      // V rows of tokens 16s+{2tq, 2tq+1, 2tq+8, 2tq+9}, channels 16gid..16gid+15
-};
-
-__device__ __forceinline__ void bf16_tile_load(Bf16Tile& T, const __nv_bfloat16* Kb,
-                                               const __nv_bfloat16* Vb, uint64_t valid, int s,
-                                               int gid, int tq) {
-  const int ta = 16 * s + gid, tb = ta + 8;
-#pragma unroll
-  for (int qd = 0; qd < 4; ++qd) {
-    T.ka[qd] = ldg_nc(Kb + ta * D + 32 * tq + 8 * qd);
-    T.kb[qd] = ldg_nc(Kb + tb * D + 32 * tq + 8 * qd);
-  }
-  const int t0 = 16 * s + 2 * tq, t2 = t0 + 8;
-  const int tk[4] = {t0, t0 + 1, t2, t2 + 1};
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const bool ok = (valid >> tk[u]) & 1;
-    const __nv_bfloat16* src = Vb + tk[u] * D + 16 * gid;
-    T.vv[u][0] = ok ? ldg_nc(src) : make_uint4(0, 0, 0, 0);
-    T.vv[u][1] = ok ? ldg_nc(src + 8) : make_uint4(0, 0, 0, 0);
-  }
-}
-
-__device__ __forceinline__ void bf16_tile_compute(Bf16State& S, const Bf16Tile& T, uint64_t valid,
-                                                  int s, int gid) {
-  const float cst = LOG2E * INV_SQRT_D;
-  const int ta = 16 * s + gid, tb = ta + 8;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint4& xa = T.ka[kk >> 1];
-    const uint4& xb = T.kb[kk >> 1];
-    const uint32_t a0 = (kk & 1) ? xa.z : xa.x, a2 = (kk & 1) ? xa.w : xa.y;
-    const uint32_t a1 = (kk & 1) ? xb.z : xb.x, a3 = (kk & 1) ? xb.w : xb.y;
-    mma_bf16(acc, a0, a1, a2, a3, S.bq[kk][0], S.bq[kk][1]);
-  }
-  const bool va = (valid >> ta) & 1, vb = (valid >> tb) & 1;
-  float lam[4];
-  lam[0] = va ? acc[0] * cst : -INFINITY;
-  lam[1] = va ? acc[1] * cst : -INFINITY;
-  lam[2] = vb ? acc[2] * cst : -INFINITY;
-  lam[3] = vb ? acc[3] * cst : -INFINITY;
-#pragma unroll
-  for (int hc = 0; hc < 2; ++hc) {
-    float pm = fmaxf(lam[hc], lam[hc + 2]);
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-    const float mn = fmaxf(S.m[hc], pm);
-    if (mn > S.m[hc]) {  // rescale only when the running max moves
-      const float al = ex2(S.m[hc] - mn);
-      S.m[hc] = mn;
-      S.l[hc] *= al;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        S.oacc[j][hc] *= al;
-        S.oacc[j][hc + 2] *= al;
-      }
-    }
-  }
-  float p[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) p[e] = ex2(lam[e] - S.m[e & 1]);
-  const __nv_bfloat162 h0 = __floats2bfloat162_rn(p[0], p[1]);
-  const __nv_bfloat162 h1 = __floats2bfloat162_rn(p[2], p[3]);
-  const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
-  S.l[0] += f0.x + f1.x;
-  S.l[1] += f0.y + f1.y;
-  const uint32_t b0 = movmatrix_t(*(const uint32_t*)&h0);
-  const uint32_t b1 = movmatrix_t(*(const uint32_t*)&h1);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t x0 = ((const uint32_t*)&T.vv[0][j >> 2])[j & 3];
-    const uint32_t x1 = ((const uint32_t*)&T.vv[1][j >> 2])[j & 3];
-    const uint32_t x2 = ((const uint32_t*)&T.vv[2][j >> 2])[j & 3];
-    const uint32_t x3 = ((const uint32_t*)&T.vv[3][j >> 2])[j & 3];
-    mma_bf16(S.oacc[j], prmt(x0, x1, 0x5410), prmt(x0, x1, 0x7632), prmt(x2, x3, 0x5410),
-             prmt(x2, x3, 0x7632), b0, b1);
-  }
-}
-
-// Tiles s0 .. s0+ns-1 (16 tokens each) of 64 BF16 keys/values, row-major
-// [64][128] at Kb / Vb; token t is used iff bit t of `valid` is set.  With DB
-// the next tile's loads are in flight while the current one is computed (more
-// registers); without, tiles are loaded one at a time.
-template <bool DB>
-__device__ __forceinline__ void bf16_span_mma(Bf16State& S, const __nv_bfloat16* Kb,
-                                              const __nv_bfloat16* Vb, uint64_t valid, int lane,
-                                              int s0, int ns) {
-  const int gid = lane >> 2, tq = lane & 3;
-  if (DB) {
-    Bf16Tile A, Bt;
-    bf16_tile_load(A, Kb, Vb, valid, s0, gid, tq);
-    for (int s = s0; s < s0 + ns; s += 2) {
-      if (s + 1 < s0 + ns) bf16_tile_load(Bt, Kb, Vb, valid, s + 1, gid, tq);
-      if ((valid >> (16 * s)) & 0xFFFFull) bf16_tile_compute(S, A, valid, s, gid);
-      if (s + 2 < s0 + ns) bf16_tile_load(A, Kb, Vb, valid, s + 2, gid, tq);
-      if (s + 1 < s0 + ns && ((valid >> (16 * (s + 1))) & 0xFFFFull))
-        bf16_tile_compute(S, Bt, valid, s + 1, gid);
-    }
-  } else {
-    for (int s = s0; s < s0 + ns; ++s) {
-      if (!((valid >> (16 * s)) & 0xFFFFull)) continue;
-      Bf16Tile A;
-      bf16_tile_load(A, Kb, Vb, valid, s, gid, tq);
-      bf16_tile_compute(S, A, valid, s, gid);
-    }
-  }
-}
-
-template <bool DB>
-__device__ __forceinline__ void bf16_chunk_mma(Bf16State& S, const __nv_bfloat16* Kb,
-                                               const __nv_bfloat16* Vb, uint64_t valid, int lane) {
-  bf16_span_mma<DB>(S, Kb, Vb, valid, lane, 0, 4);
-}
-
 // Page ids of a warp's pages k = 0, 1, ... (page p0 + warp + k*NW of request
 // b), held 32 at a time in registers (lane i keeps page 32*blk + i) so that
 // no page waits on a dependent page-table load.
@@ -1009,8 +874,8 @@ __host__ __device__ inline MergeLayout merge_layout(int B) {
   o = L.off_mbar + 16;
   L.off_red = o;
   o += 64 * 4;
-  L.off_pre = o;
-  o += ((B + 1) * 4 + 15) & ~15;
+  L.off_pre = (o + 7) & ~7;
+  o = L.off_pre + (((B + 1) * 8 + 15) & ~15);  // int[B + 1], or long long[B + 1] for the balanced list
   L.total = o;
   return L;
 }
@@ -1051,15 +916,39 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
   }
   // history lengths come from earlier stream work: the work list can be
   // derived before the wait
-  const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
-  const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
-  const int pages_b = (cv.hist_lens[b] + PAGE - 1) / PAGE;
-  const int nb = (pages_b + sc.S - 1) / sc.S;
-  const int base = pre[b] + kvh * nb;
-  const int wslot = sc.n_hist + (b * Hkv + kvh) * sc.wch;
+  int nb, base, wslot, wch;
+  unsigned wmask;  // window records that exist
+  if (a.balanced) {
+    // the tensor-memory kernel's list: the history records of the CTAs
+    // owning this segment's pages, then one record per non-empty window chunk
+    long long* pre64 = (long long*)(smem + ML.off_pre);
+    const Balanced bl = make_balanced(cv.seq_lens, cv.hist_lens, a.B, Hkv, a.bal_wch, a.bal_grid, pre64);
+    const int H = cv.hist_lens[b], Lq = cv.seq_lens[b];
+    const int P = H > 0 ? (H + PAGE - 1) / PAGE : 0;
+    wmask = window_chunk_mask(Lq, H);
+    const long long seg = pre64[b] + (long long)kvh * (P + bl.wch * __popc(wmask));
+    nb = 0;
+    base = 0;
+    if (P > 0) {
+      const int i0 = balanced_owner(bl, seg), i1 = balanced_owner(bl, seg + P - 1);
+      nb = i1 - i0 + 1;
+      base = i0 + b * Hkv + kvh;
+    }
+    wch = WIN_CHUNKS;
+    wslot = bl.n + a.B * Hkv + WIN_CHUNKS * (b * Hkv + kvh);
+  } else {
+    const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
+    const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
+    const int pages_b = (cv.hist_lens[b] + PAGE - 1) / PAGE;
+    nb = (pages_b + sc.S - 1) / sc.S;
+    base = pre[b] + kvh * nb;
+    wch = sc.wch;
+    wslot = sc.n_hist + (b * Hkv + kvh) * sc.wch;
+    wmask = (1u << sc.wch) - 1u;
+  }
   const int WPH = MW / HPC;  // warps per head
   const int n = warp / WPH, r = warp % WPH;  // head h0 + n of the kv group
-  if (n < HPC && lane == 0 && r < nb + sc.wch) {
+  if (n < HPC && lane == 0 && r < nb + wch) {
     // warm the address translation of this warp's records while the decode
     // kernel finishes (the line is written again before it is read)
     const int slot = r < nb ? base + r : wslot + (r - nb);
@@ -1075,18 +964,19 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
   if (n < HPC) {
     float M = -INFINITY, Ls = 0.f, Mw = -INFINITY, Lw = 0.f;
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f), OW = O;
-    const int nrec = nb + sc.wch;
+    const int nrec = nb + wch;
     for (int q0 = r; q0 < nrec; q0 += WPH * MERGE_MQ) {
       float mq[MERGE_MQ], lq[MERGE_MQ];
       float4 oq[MERGE_MQ];
 #pragma unroll
       for (int u = 0; u < MERGE_MQ; ++u) {
         const int q = q0 + u * WPH;
+        const bool have = q < nb || (q < nrec && ((wmask >> (q - nb)) & 1u));
         const int slot = q < nb ? base + q : wslot + (q - nb);
-        const float* rec = a.part + ((size_t)(q < nrec ? slot : base) * G + h0 + n) * PART_STRIDE;
-        mq[u] = q < nrec ? __ldcg(rec) : -INFINITY;
-        lq[u] = q < nrec ? __ldcg(rec + 1) : 0.f;
-        oq[u] = q < nrec ? __ldcg((const float4*)(rec + PART_O) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* rec = a.part + ((size_t)(have ? slot : 0) * G + h0 + n) * PART_STRIDE;
+        mq[u] = have ? __ldcg(rec) : -INFINITY;
+        lq[u] = have ? __ldcg(rec + 1) : 0.f;
+        oq[u] = have ? __ldcg((const float4*)(rec + PART_O) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
       float mx = M, mxw = Mw;
 #pragma unroll
@@ -1792,6 +1682,7 @@ int occupancy_t(const DecodeArgs& a) {
 int decode_ctas_per_sm(const DecodeArgs& a) {
   const int NG = a.cv.NG;
   if (a.bf16_history) return occupancy_t<1, 2>(a);
+  if (a.impl == 5) return 1;  // the tensor-memory kernel holds all of an SM's tensor memory
   if (a.impl == 1) return NG == 1 ? occupancy_t<1, 1>(a) : NG == 2 ? occupancy_t<2, 1>(a) : occupancy_t<4, 1>(a);
   if (a.impl == 3) return NG == 1 ? occupancy_t<1, 3>(a) : NG == 2 ? occupancy_t<2, 3>(a) : occupancy_t<4, 3>(a);
   if (a.impl == 4) return NG == 1 ? occupancy_t<1, 4>(a) : NG == 2 ? occupancy_t<2, 4>(a) : occupancy_t<4, 4>(a);
@@ -1802,7 +1693,9 @@ cudaError_t launch_decode_after_prep(const DecodeArgs& a, int grid, cudaStream_t
   const CacheView& cv = a.cv;
   cudaError_t e;
   prof_begin(prof, OSCAR_KERNEL_DECODE_MAIN, st);
-  if (a.bf16_history) {
+  if (a.impl == 5 && !a.bf16_history) {
+    e = launch_decode_tc(a, st);
+  } else if (a.bf16_history) {
     e = launch_decode_t<1, 2>(a, grid, st);
   } else if (a.impl == 1) {
     if (cv.NG == 1) e = launch_decode_t<1, 1>(a, grid, st);

@@ -501,6 +501,84 @@ __device__ __forceinline__ void hist_item_coords(int q, const int* pre, int B, i
   j = r % nb;
 }
 
+// ------------------------------------------- balanced partition (tcgen05)
+// The tensor-memory decode kernel runs one CTA per SM and splits the work
+// evenly without a work counter.  The work is a sequence of segments, one per
+// (request b, kv head) in order.  Segment (b, kvh) holds request b's history
+// pages (weight 1 each), then its non-empty BF16 window chunks (chunk 0 is the
+// sink, chunks 1..4 the four 64-slot quarters of the ring; weight `wch` each).
+// With W the total weight and n = min(CTAs, W) CTAs taking part, CTA i takes
+// the units whose position lies in [floor(i W / n), floor((i + 1) W / n)):
+// never an empty range, since n <= W.  Its pages of a segment form one
+// history item with partial record i + (b Hkv + kvh) (distinct over all
+// (CTA, segment) pairs, because a later segment's pages never go to an
+// earlier CTA); window chunk c of the segment is taken by the CTA whose range
+// holds the chunk's first position and has partial record
+// n + B Hkv + 5 (b Hkv + kvh) + c.  The merge derives the same list.
+constexpr int WIN_CHUNKS = 5;
+
+// Bit c set when window chunk c of a request with L tokens, hist of them in
+// history, holds a valid token.
+__host__ __device__ __forceinline__ unsigned window_chunk_mask(int L, int hist) {
+  unsigned m = L > 0 ? 1u : 0u;
+  const int recent = L > SINK ? L - SINK - hist : 0;
+  if (recent > 0) {
+    const int h0 = hist % RECENT;
+    for (int c = 1; c < WIN_CHUNKS; ++c) {
+      const int d = (64 * (c - 1) - h0 + RECENT) % RECENT;  // offset of the chunk's first slot from h0
+      if (d < recent || d > RECENT - 64) m |= 1u << c;       // d > 192: the chunk wraps through h0
+    }
+  }
+  return m;
+}
+
+struct Balanced {
+  long long W;  // total weight
+  int n;        // CTAs taking part (min(grid, W))
+  int wch;      // weight of a window chunk
+};
+
+// pre[b] = Hkv * (weights of requests < b), pre[B] = W (smem, B + 1 entries).
+// All threads of the block call it.
+__device__ inline Balanced make_balanced(const int32_t* seq_lens, const int32_t* hist_lens, int B, int Hkv,
+                                         int wch, int grid, long long* pre) {
+  if (threadIdx.x == 0) {
+    long long acc = 0;
+    for (int b = 0; b < B; ++b) {
+      pre[b] = acc;
+      const int L = seq_lens[b], H = hist_lens[b];
+      const int pages = H > 0 ? (H + PAGE - 1) / PAGE : 0;
+      acc += (long long)Hkv * (pages + wch * __popc(window_chunk_mask(L, H)));
+    }
+    pre[B] = acc;
+  }
+  __syncthreads();
+  Balanced bl;
+  bl.W = pre[B];
+  bl.n = (int)(bl.W < grid ? bl.W : grid);
+  bl.wch = wch;
+  return bl;
+}
+
+__host__ __device__ __forceinline__ long long balanced_lo(const Balanced& bl, int i) {
+  return (long long)i * bl.W / bl.n;
+}
+
+// The CTA whose range holds position x (0 <= x < W).
+__host__ __device__ __forceinline__ int balanced_owner(const Balanced& bl, long long x) {
+  return (int)(((x + 1) * bl.n + bl.W - 1) / bl.W - 1);
+}
+
+// Largest b with pre[b] <= x (pre non-decreasing, pre[0] = 0 <= x < pre[B]).
+__device__ __forceinline__ int balanced_request(const long long* pre, int B, long long x) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // ------------------------------------------------------------- launchers
 // Optional per-kernel event recording (see oscar_profile_enable).
 struct Profiler;
@@ -521,9 +599,12 @@ struct DecodeArgs {
   int target_items;
   int resident;  // resident decode CTAs for automatic item sizing, 0: fixed items per CTA
   int impl;  // decode kernel variant: 0 tensor-core, 1 CUDA-core, 3 tensor-core page pairs,
-             // 4 tensor-core with a Lloyd-Max codebook
+             // 4 tensor-core with a Lloyd-Max codebook, 5 tcgen05 with tensor memory
   int bf16_history;
   int merge_hpc;  // query heads per merge CTA (divides G)
+  int balanced;   // 1: the tensor-memory kernel's balanced partition (decode grid in bal_grid)
+  int bal_grid;
+  int bal_wch;
   LayerRot rot;
 };
 
@@ -646,6 +727,10 @@ __device__ __forceinline__ void prep_body(const DecodeArgs& a, int bk, int cq, i
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof);
+// The tensor-memory decode kernel (impl 5, oscar_decode_tc.cu): grid a.bal_grid, balanced partition.
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
+int decode_tc_smem_bytes(int head_bytes, int B);
+int decode_tc_window_weight();
 // The decode kernel and the merge only (the caller ran the packed query).
 cudaError_t launch_decode_after_prep(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof);
 int decode_ctas_per_sm(const DecodeArgs& a);  // resident CTAs per SM of the decode kernel (0: error)

@@ -40,6 +40,7 @@ OPT_DECODE_IMPL = 0
 DECODE_TENSOR = 0  # tensor cores; two pages per tile at G <= 4
 DECODE_CUDA_CORE = 1
 DECODE_TENSOR_SINGLE = 2  # tensor cores, one page per tile
+DECODE_TCGEN05 = 3  # tcgen05.mma, codes unpacked into tensor memory, one CTA per SM
 OPT_CTAS_PER_SM = 1
 OPT_ITEMS_PER_CTA = 2
 OPT_PREFILL_IMPL = 3

@@ -115,7 +115,10 @@ typedef enum {
   OSCAR_DECODE_TENSOR = 0,        /* tensor cores; with at most 4 query heads per kv head a warp
                                      takes two pages per tile as two softmax streams (default) */
   OSCAR_DECODE_CUDA_CORE = 1,     /* fp32 CUDA cores, one page per warp at a time */
-  OSCAR_DECODE_TENSOR_SINGLE = 2  /* tensor cores, one page per tile at any group size */
+  OSCAR_DECODE_TENSOR_SINGLE = 2, /* tensor cores, one page per tile at any group size */
+  OSCAR_DECODE_TCGEN05 = 3        /* tcgen05.mma with the codes unpacked into tensor memory:
+                                     warp-specialised, one CTA per SM, 128-token tiles, an even
+                                     static split of the work over the SMs */
 } oscar_decode_impl;
 /* (A layer with a Lloyd-Max codebook, oscar_set_codebook, always decodes with
  * the codebook kernel: tensor cores, one page per tile.) */

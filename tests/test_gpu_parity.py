@@ -110,7 +110,7 @@ def test_cfg1_import_append_demote_and_decode():
         assert bad <= 1e-4 * n
         q = GS.queries(sc, seed=1)
         qn = q.float().cpu().numpy()
-        for impl in (oscar.DECODE_TENSOR, oscar.DECODE_CUDA_CORE, oscar.DECODE_TENSOR_SINGLE):
+        for impl in (oscar.DECODE_TENSOR, oscar.DECODE_CUDA_CORE, oscar.DECODE_TENSOR_SINGLE, oscar.DECODE_TCGEN05):
             out, lse = GS.decode(sc, q, impl)
             ref, rlse = GS.oracle_decode(sc, hc, qn, 0)
             assert _rel(out[0].float().cpu().numpy(), ref) <= REL_TOL
@@ -124,7 +124,7 @@ def test_cfg1_import_append_demote_and_decode():
 EDGE_LENGTHS = [0, 1, 2, 63, 64, 65, 100, 319, 320, 321, 383, 384, 385, 447, 448, 449, 700, 1024, 1100]
 
 
-@pytest.mark.parametrize("impl", [0, 1, 2])
+@pytest.mark.parametrize("impl", [0, 1, 2, 3])
 def test_decode_edge_lengths_gqa4_g128(impl):
     sc = GS.build("edge", EDGE_LENGTHS, Hq=8, Hkv=2, g=128, interleave=True, calib_n=512)
     try:
@@ -146,7 +146,7 @@ def test_decode_edge_lengths_gqa4_g128(impl):
 
 
 @pytest.mark.parametrize("G,g", [(1, 32), (2, 64), (8, 32), (8, 128), (4, 64), (1, 128)])
-@pytest.mark.parametrize("impl", [0, 1, 2])
+@pytest.mark.parametrize("impl", [0, 1, 2, 3])
 def test_decode_gqa_and_group_sizes(G, g, impl):
     lengths = [333, 1000, 64 * 9 + 320 + 17]
     sc = GS.build(f"gq{G}{g}", lengths, Hq=2 * G, Hkv=2, g=g, calib_n=512)
