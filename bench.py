@@ -1110,6 +1110,8 @@ def run_leg(args, wl):
     B.build()
     dev = "cuda:0"
     stream = torch.cuda.current_stream()
+    if args.context:
+        wl = dict(wl, L=args.context)
     Hkv, g, Bsz, L0 = wl["Hkv"], wl["g"], wl["B"], wl["L"]
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     bf16 = args.leg == "bf16"
@@ -1173,7 +1175,7 @@ def run_leg(args, wl):
     mean_us = e0.elapsed_time(e1) * 1e3 / args.steps
     err = oscar.oscar_get_error(wk["bctx"] if bf16 else ctx)
     assert err == 0, f"device error {err}"
-    line = {"leg": args.leg, "workload": args.workload, "calls": args.steps, "mean_us": mean_us,
+    line = {"leg": args.leg, "workload": args.workload, "context": L0, "calls": args.steps, "mean_us": mean_us,
             "cache_copies": n_copies}
     if not appends:  # a second pass, timed call by call
         med, p10, p90 = percentiles(per_call_times(lambda i: fn(args.warmup + i), args.steps, stream))
@@ -1252,6 +1254,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_8b_100k", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--context", type=int, default=0,
+                    help="single-operation legs: context length instead of the workload's (0: the workload's)")
     ap.add_argument("--leg", choices=["all", "codebook"] + list(LEGS), default="all",
                     help="one operation alone on the workload, a short command to profile it (see run_leg); "
                          "codebook: only the Lloyd-Max codebook decode")

@@ -12,7 +12,9 @@ import ctypes
 import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "liboscar.so")
+# the in-tree build; OSCAR_LIBRARY names another build of the same library
+# (for example one compiled with different options) to load instead
+LIB_PATH = os.environ.get("OSCAR_LIBRARY") or os.path.join(PKG, "liboscar.so")
 
 HEAD_DIM = 128
 PAGE_SIZE = 64
