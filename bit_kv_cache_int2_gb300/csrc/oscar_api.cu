@@ -116,8 +116,8 @@ int kernel_impl(const oscar_ctx* ctx, int layer = -1) {
   if (layer >= 0 && ctx->has_cb[layer]) return 4;
   if (ctx->impl == OSCAR_DECODE_TCGEN05) return 5;
   if (ctx->impl == OSCAR_DECODE_CUDA_CORE) return 1;
-  if (ctx->impl == OSCAR_DECODE_TENSOR_SINGLE || ctx->G > 4) return 0;
-  return 3;
+  if (ctx->impl == OSCAR_DECODE_TENSOR_SINGLE) return 0;
+  return ctx->G > 4 ? 6 : 3;  // the ring kernel: page pairs at G <= 4, single pages at G = 8
 }
 
 // Persistent decode CTAs per SM: the option, capped by what the kernel variant
@@ -144,6 +144,10 @@ int target_items(const oscar_ctx* ctx, int batch, bool bf16_history, int layer =
   int t = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, layer) * per;
   if (t > MAX_TARGET_ITEMS) t = MAX_TARGET_ITEMS;
   if (t < 1) t = 1;
+  // the ring kernel keeps five window records per (request, kv head) beside
+  // its history items: room for at least one history item per pair
+  const int impl = bf16_history ? 0 : kernel_impl(ctx, layer);
+  if ((impl == 3 || impl == 6) && t < 4 * batch * ctx->cfg.num_kv_heads) t = 4 * batch * ctx->cfg.num_kv_heads;
   return t;
 }
 
@@ -334,6 +338,7 @@ oscar_status decode_args(oscar_ctx* ctx, int layer, const oscar_cache* cache, co
   a.merge_hpc = ctx->G;
   while (a.merge_hpc % 2 == 0 && batch * ctx->cfg.num_kv_heads * (ctx->G / a.merge_hpc) < ctx->num_sms)
     a.merge_hpc /= 2;
+  a.ring = (a.impl == 3 || a.impl == 6) ? 1 : 0;
   a.balanced = 0;
   a.bal_grid = 0;
   a.bal_wch = 0;

@@ -182,18 +182,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
 #undef OSCAR_W8
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
-// Two codes of bit pair I of each 16-bit half of w as fp16 subnormals
-// code * 2^(E(I) - 24): the pair is moved to bits E..E+1 (w * 16, w or
-// w >> 6) and masked.  E(I) = code_exp<I>().
-template <int I>
-__device__ __forceinline__ uint32_t code_sub(uint32_t w) {
-  constexpr uint32_t M = (I == 0 || I == 2 || I == 5) ? 0x00300030u
-                         : (I == 1 || I == 3 || I == 6) ? 0x00C000C0u
-                                                        : 0x03000300u;
-  const uint32_t src = (I <= 1) ? (w * 16u) : (I <= 4) ? w : (w >> 6);
-  return src & M;
-}
-
 // The 8 code pairs of word w into v[0..7] (v[I] = pair I).
 __device__ __forceinline__ void word_codes(uint32_t w, uint32_t* v) {
   v[0] = code_sub<0>(w);

@@ -268,6 +268,23 @@ __device__ __forceinline__ uint32_t code_plane(uint32_t w) {
   const uint32_t src = (I <= 1) ? (w * 16u) : (I <= 4) ? w : (w >> 6);
   return and_or(src, M, 0x64006400u);
 }
+// The same code pair as an fp16 subnormal: code * 2^(E(I) - 24), one AND
+// and no offset (the tensor cores take fp16 subnormals exactly).  Callers
+// fold 2^(24 - E) into the other operand or the epilogue.
+template <int I>
+__device__ __forceinline__ uint32_t code_sub(uint32_t w) {
+  constexpr uint32_t M = (I == 0 || I == 2 || I == 5) ? 0x00300030u
+                         : (I == 1 || I == 3 || I == 6) ? 0x00C000C0u
+                                                        : 0x03000300u;
+  const uint32_t src = (I <= 1) ? (w * 16u) : (I <= 4) ? w : (w >> 6);
+  return src & M;
+}
+// Code pair I of w, offset (1024 + code 2^E) or subnormal (code 2^(E - 24)).
+template <int I, bool SUB>
+__device__ __forceinline__ uint32_t code_fp16(uint32_t w) {
+  if constexpr (SUB) return code_sub<I>(w);
+  else return code_pair<I>(w);
+}
 template <int I>
 __host__ __device__ constexpr int code_exp() {
   return (I == 0 || I == 2 || I == 5) ? 4 : (I == 1 || I == 3 || I == 6) ? 6 : 8;
@@ -424,8 +441,12 @@ constexpr int AUTO_MIN_PAGES = 28;
 // target: the most items the list may hold; resident: the decode CTAs that
 // run at once, or 0 to size items for `target` items in total.
 // Must be called by all threads of the block.
+// ring: the list of the ring decode kernel, whose window chunks are jobs
+// outside the CTAs' item list: always five 64-token chunks per (request, kv
+// head), history items sized for all of `resident` (or `target`), and the
+// records (history items + 5 B Hkv window chunks) within target + 2 B Hkv.
 __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int target, int resident,
-                                   int hist_item_unit_bytes, int* pre, int* red) {
+                                   int hist_item_unit_bytes, int* pre, int* red, bool ring = false) {
   const int tid = threadIdx.x;
   // total history pages (over requests), times Hkv
   long long local = 0;
@@ -443,9 +464,9 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
   // window into its 5 chunks so that no single window item outlasts the
   // history items
   auto pages_per_item = [&](int items) {
-    s.wch = (5LL * B * Hkv * 4 <= items) ? 5 : 1;
+    s.wch = (ring || 5LL * B * Hkv * 4 <= items) ? 5 : 1;
     s.n_win = B * Hkv * s.wch;
-    int th = items - s.n_win;
+    int th = ring ? items : items - s.n_win;
     if (th < (items + 1) / 2) th = (items + 1) / 2;
     const long long S = (total + th - 1) / th;
     return S < 1 ? 1LL : S;
@@ -464,7 +485,7 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
         const int pages = (hist_lens[b] + PAGE - 1) / PAGE;
         n += (long long)Hkv * ((pages + s.S - 1) / s.S);
       }
-      if (n + s.n_win <= target || n <= (long long)B * Hkv) break;
+      if (n + (ring ? 3LL * B * Hkv : s.n_win) <= target || n <= (long long)B * Hkv) break;
       s.S += s.S / 8 > 1 ? s.S / 8 : 1;
     }
     int acc = 0;
@@ -598,10 +619,12 @@ struct DecodeArgs {
   int B;
   int target_items;
   int resident;  // resident decode CTAs for automatic item sizing, 0: fixed items per CTA
-  int impl;  // decode kernel variant: 0 tensor-core, 1 CUDA-core, 3 tensor-core page pairs,
-             // 4 tensor-core with a Lloyd-Max codebook, 5 tcgen05 with tensor memory
+  int impl;  // decode kernel variant: 0 tensor-core one page per warp, 1 CUDA-core, 3 ring kernel with
+             // page pairs, 4 tensor-core with a Lloyd-Max codebook, 5 tcgen05 with tensor memory,
+             // 6 ring kernel with one page per unit
   int bf16_history;
   int merge_hpc;  // query heads per merge CTA (divides G)
+  int ring;       // 1: the ring decode kernel's list (make_sched with ring)
   int balanced;   // 1: the tensor-memory kernel's balanced partition (decode grid in bal_grid)
   int bal_grid;
   int bal_wch;
@@ -658,7 +681,10 @@ __device__ __forceinline__ void prep_body(const DecodeArgs& a, int bk, int cq, i
   if (release) pdl_launch_dependents();
   if (t == 0 && cq == 0) {
     a.done[bk] = 0;
-    if (bk == 0) *a.counter = 0;
+    if (bk == 0) {
+      a.counter[0] = 0;  // history items after the first wave
+      a.counter[1] = 0;  // window chunks of the ring kernel
+    }
   }
   if (a.bf16_history) return;
   const __nv_bfloat16* qg = a.q + ((size_t)b * cv.Hq + kvh * G) * D;
@@ -727,6 +753,9 @@ __device__ __forceinline__ void prep_body(const DecodeArgs& a, int bk, int cq, i
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof);
+// The ring decode kernel (impl 3 and 6, oscar_decode_ring.cu).
+cudaError_t launch_decode_ring(const DecodeArgs& a, int grid, cudaStream_t st);
+int decode_ring_ctas_per_sm(const DecodeArgs& a);
 // The tensor-memory decode kernel (impl 5, oscar_decode_tc.cu): grid a.bal_grid, balanced partition.
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
 int decode_tc_smem_bytes(int head_bytes, int B);
