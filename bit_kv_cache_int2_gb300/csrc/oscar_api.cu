@@ -63,7 +63,7 @@ struct oscar_ctx {
   std::vector<int> has_cb;        // [layers] a non-uniform codebook is set: decode variant 4
   std::vector<float> clip_host;   // [layers][2][Hkv] copy of d_clip
   int* d_err = nullptr;
-  int* d_req_counter = nullptr;  // [max_batch]
+  int* d_req_counter = nullptr;  // [max_batch] requests, then [max_batch][Hkv] windows (decode step)
   int impl = 0;
   int ctas_per_sm = 4;
   int items_per_cta = 0;  // 0: automatic (make_sched)
@@ -116,8 +116,8 @@ int kernel_impl(const oscar_ctx* ctx, int layer = -1) {
   if (layer >= 0 && ctx->has_cb[layer]) return 4;
   if (ctx->impl == OSCAR_DECODE_TCGEN05) return 5;
   if (ctx->impl == OSCAR_DECODE_CUDA_CORE) return 1;
-  if (ctx->impl == OSCAR_DECODE_TENSOR_SINGLE) return 0;
-  return ctx->G > 4 ? 6 : 3;  // the ring kernel: page pairs at G <= 4, single pages at G = 8
+  if (ctx->impl == OSCAR_DECODE_TENSOR_SINGLE || ctx->G > 4) return 0;
+  return 3;
 }
 
 // Persistent decode CTAs per SM: the option, capped by what the kernel variant
@@ -144,10 +144,6 @@ int target_items(const oscar_ctx* ctx, int batch, bool bf16_history, int layer =
   int t = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, layer) * per;
   if (t > MAX_TARGET_ITEMS) t = MAX_TARGET_ITEMS;
   if (t < 1) t = 1;
-  // the ring kernel keeps five window records per (request, kv head) beside
-  // its history items: room for at least one history item per pair
-  const int impl = bf16_history ? 0 : kernel_impl(ctx, layer);
-  if ((impl == 3 || impl == 6) && t < 4 * batch * ctx->cfg.num_kv_heads) t = 4 * batch * ctx->cfg.num_kv_heads;
   return t;
 }
 
@@ -338,7 +334,8 @@ oscar_status decode_args(oscar_ctx* ctx, int layer, const oscar_cache* cache, co
   a.merge_hpc = ctx->G;
   while (a.merge_hpc % 2 == 0 && batch * ctx->cfg.num_kv_heads * (ctx->G / a.merge_hpc) < ctx->num_sms)
     a.merge_hpc /= 2;
-  a.ring = (a.impl == 3 || a.impl == 6) ? 1 : 0;
+  // the mma.sync INT2 kernels leave the BF16 window to the kernel before them
+  a.win_ext = (!bf16_history && a.impl != 5) ? 1 : 0;
   a.balanced = 0;
   a.bal_grid = 0;
   a.bal_wch = 0;
@@ -478,9 +475,10 @@ oscar_status oscar_create(const oscar_config* cfg, oscar_ctx** out) {
   const size_t cb_floats = (size_t)cfg->num_layers * 2 * cfg->num_kv_heads * CB_WORDS;
   if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_cb, cb_floats * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_err, sizeof(int));
-  if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_req_counter, sizeof(int) * cfg->max_batch);
+  const size_t counters = (size_t)cfg->max_batch * (1 + cfg->num_kv_heads);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_req_counter, sizeof(int) * counters);
   if (e == cudaSuccess) e = cudaMemset(ctx->d_err, 0, sizeof(int));
-  if (e == cudaSuccess) e = cudaMemset(ctx->d_req_counter, 0, sizeof(int) * cfg->max_batch);
+  if (e == cudaSuccess) e = cudaMemset(ctx->d_req_counter, 0, sizeof(int) * counters);
   if (e == cudaSuccess) {
     // identity rotation and clip 1.0 until oscar_set_rotation is called
     std::vector<float> eye;
@@ -663,7 +661,7 @@ oscar_status oscar_decode_step(oscar_ctx* ctx, int layer, const oscar_cache* cac
   if (s != OSCAR_OK) return s;
   const cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = launch_step(a.cv, a.rot, (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, batch,
-                              ctx->d_req_counter, a, st, &ctx->prof);
+                              ctx->d_req_counter, ctx->d_req_counter + ctx->cfg.max_batch, a, st, &ctx->prof);
   if (e == cudaSuccess) e = launch_decode_after_prep(a, grid, st, &ctx->prof);
   return cuda_status(e);
 }

@@ -44,6 +44,26 @@ __global__ void __launch_bounds__(128) prep_kernel(DecodeArgs a) {
   prep_body(a, blockIdx.x, blockIdx.y, threadIdx.x, sm, true);
 }
 
+// The same, with the BF16 window of (request, kv head) x as well (the decode
+// kernel then holds history items only).  grid (B * Hkv, 2), block 512: y = 0
+// computes the packed query (four 128-thread parts, one channel quarter
+// each), y = 1 attends the window (window_block).  Both release the decode
+// kernel as soon as they have waited for earlier stream work: the decode
+// kernel reads nothing this grid writes before its own wait.
+__global__ void __launch_bounds__(512) prep_window_kernel(DecodeArgs a) {
+  extern __shared__ __align__(16) float xs[];
+  __shared__ PrepSmem psm[4];
+  const int bk = blockIdx.x;
+  if (blockIdx.y == 0) {
+    prep_body(a, bk, threadIdx.x >> 7, threadIdx.x & 127, psm[threadIdx.x >> 7], true);
+  } else {
+    pdl_wait();  // the window's tokens and q come from earlier stream work
+    pdl_launch_dependents();
+    const int b = bk / a.cv.Hkv, kvh = bk % a.cv.Hkv;
+    window_block(a, b, kvh, a.cv.seq_lens[b], a.cv.hist_lens[b], window_slot(a, b, kvh), xs);
+  }
+}
+
 // ------------------------------------------------------------ smem layout
 struct SmemLayout {
   int stage_bytes;   // per stage
@@ -518,13 +538,18 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
     wslot = bl.n + a.B * Hkv + WIN_CHUNKS * (b * Hkv + kvh);
   } else {
     const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
-    const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red, a.ring != 0);
+    const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red, a.win_ext != 0);
     const int pages_b = (cv.hist_lens[b] + PAGE - 1) / PAGE;
     nb = (pages_b + sc.S - 1) / sc.S;
     base = pre[b] + kvh * nb;
-    wch = sc.wch;
-    wslot = sc.n_hist + (b * Hkv + kvh) * sc.wch;
-    wmask = (1u << sc.wch) - 1u;
+    if (a.win_ext) {  // one window record, written before the decode kernel
+      wch = 1;
+      wslot = window_slot(a, b, kvh);
+    } else {
+      wch = sc.wch;
+      wslot = sc.n_hist + (b * Hkv + kvh) * sc.wch;
+    }
+    wmask = (1u << wch) - 1u;
   }
   const int WPH = MW / HPC;  // warps per head
   const int n = warp / WPH, r = warp % WPH;  // head h0 + n of the kv group
@@ -724,7 +749,7 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
 template <int NG, int IMPL>
 // Three CTAs per SM fit the shared memory of g = 128 pages only (4608-byte
 // stages); at g = 64 and 32 two do, and the register budget follows.
-__global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 4)) ? 3 : 2)
+__global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 || IMPL == 4)) ? 3 : 2)
     decode_kernel(DecodeArgs a) {
   constexpr bool BF16H = (IMPL == 2);
   extern __shared__ __align__(128) uint8_t smem[];
@@ -753,7 +778,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 4))
   // history lengths and page tables come from earlier stream work: readable
   // before the wait on prep_kernel
   const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
-  const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
+  const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red, a.win_ext != 0);
   const int total = sc.n_hist + sc.n_win;
   uint32_t seq = 0;  // stages consumed by this warp so far
   bool waited = false;
@@ -917,8 +942,11 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 4))
       }
       bool timed_out = false;
       int k_fail = 0;
-      if constexpr (IMPL == 0 || IMPL == 4) {
-        // one page at a time; IMPL 4 with the layer's Lloyd-Max codebook
+      if constexpr (IMPL == 0 || IMPL == 3 || IMPL == 4) {
+        // IMPL 3: pages in pairs, two streams per tile (G <= 4), with the codes
+        // as fp16 subnormals; IMPL 0: one page at a time; IMPL 4: one page at
+        // a time with the layer's Lloyd-Max codebook
+        constexpr bool PAIR = (IMPL == 3);
         constexpr bool CB = (IMPL == 4);
         constexpr int QREC = CB ? QPACK_CB_BYTES : QPACK_BYTES;
         // the kv head's G packed query records, copied to shared memory by warp
@@ -951,8 +979,8 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 4))
             X.vb = __ldg(cvr + CB_BETA_HALF);
             X.vc0 = __ldg(cvr + CB_C0);
           }
-          // B column gid carries head gid
-          const int qh = gid;
+          // B column gid carries head gid (PAIR: head gid & 3 in both halves)
+          const int qh = PAIR ? (gid & 3) : gid;
           const bool qv = qh < G;
           const __half* qbh = (const __half*)(qpk + (qv ? qh : 0) * QREC);
 #pragma unroll
@@ -967,13 +995,13 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 4))
           }
 #pragma unroll
           for (int hc = 0; hc < 2; ++hc) {
-            const int n = 2 * tq + hc;
+            const int n = PAIR ? ((2 * tq + hc) & 3) : 2 * tq + hc;
             const bool hv = n < G;
             const uint8_t* r = qpk + (hv ? n : 0) * QREC;
-            S.m[hc] = -INFINITY;
+            S.m[hc] = PAIR ? -1e30f : -INFINITY;
             S.l[hc] = 0.f;
             const float al = hv ? *(const float*)(r + O_ALPHA) : 0.f;
-            S.ka[hc] = al;
+            S.ka[hc] = PAIR ? al * 16777216.f : al;  // subnormal codes carry 2^-24
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
               float qs = 0.f, ps = 0.f;
@@ -984,12 +1012,49 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 4))
               }
               S.bs[hc][gr] = 0.f;
               S.zs[hc][gr] = 0.f;
-              S.kb[hc][gr] = CB ? fmaf(kc0 * ps, LOG2E * INV_SQRT_D, -1024.f * qs * al) : -1024.f * qs * al;
+              S.kb[hc][gr] = CB ? fmaf(kc0 * ps, LOG2E * INV_SQRT_D, -1024.f * qs * al)
+                                : PAIR ? 0.f : -1024.f * qs * al;
               S.kg[hc][gr] = ps * LOG2E * INV_SQRT_D;
             }
           }
         }
-        {
+        if constexpr (PAIR) {
+          const uint32_t mA = gid < 4 ? 0xffffffffu : 0u;  // B columns 0..3: page A
+          for (int k = 0; k < nw_pages; k += 2) {
+            const bool hasB = k + 1 < nw_pages;
+            const int sa = (int)((seq + k) % DEPTH), sb = (int)((seq + k + 1) % DEPTH);
+            bool ok = mbar_wait2(&my_bar[sa], ((seq + k) / DEPTH) & 1u, &my_bar[hasB ? sb : sa],
+                                 (hasB ? (seq + k + 1) / DEPTH : (seq + k) / DEPTH) & 1u);
+            if (!__all_sync(0xffffffffu, ok)) {
+              timed_out = true;
+              k_fail = k;
+              break;
+            }
+            if (k > 0 && (k & 31) == 0) page_ids_advance(P, cv, b, p0 + warp, nw_pages, lane);
+            const int pa = p0 + warp + k * NW, pb = pa + NW;
+            const int pida = page_id_at(P, k);
+            const int pidb = page_id_at(P, hasB ? k + 1 : k);
+            const bool oka = pida >= 0 && pida < cv.num_pages;
+            const bool okb = hasB && pidb >= 0 && pidb < cv.num_pages;
+            const int nva = oka ? ((pa == pages_b - 1) ? hist_b - pa * PAGE : PAGE) : 0;
+            const int nvb = okb ? ((pb == pages_b - 1) ? hist_b - pb * PAGE : PAGE) : 0;
+            const uint8_t* sta = my_stage + (size_t)sa * L.stage_bytes;
+            const uint8_t* stb = hasB ? my_stage + (size_t)sb * L.stage_bytes : sta;
+            // one (masked) variant for full and partial pages keeps the
+            // unrolled loop body small enough for the instruction cache
+            if (nva > 0 || nvb > 0) int2_pair_mma<NG, false>(S, sta, nva, stb, nvb, hasB, lane, mA);
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              if (k + u + DEPTH < nw_pages) {
+                // the stage's generic-proxy reads have completed (their values
+                // were consumed before __syncwarp): no proxy fence is needed
+                const int pid_next = page_id_at(P, k + u + DEPTH);
+                if (lane == 0) issue(k + u + DEPTH, pid_next);
+              }
+            }
+          }
+        } else {
           for (int k = 0; k < nw_pages; ++k) {
             const int st = (int)((seq + k) % DEPTH);
             const uint32_t ph = ((seq + k) / DEPTH) & 1u;
@@ -1034,6 +1099,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 4))
             }
           }
         }
+        if constexpr (PAIR) merge_pair_streams<NG>(S);
         if (timed_out) {
           if (lane == 0) {
             record_error(cv.err, OSCAR_ERR_TIMEOUT);
@@ -1055,10 +1121,13 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 4))
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const int gr = j / (8 / NG);
-              const float off = 1024.f * S.bs[hc][gr];
+              // offset codes: o' = (O - 1024 sum B) / 256 + sum p z; subnormal
+              // codes (PAIR): o' = 2^16 O + sum p z
+              const float off = PAIR ? 0.f : 1024.f * S.bs[hc][gr];
+              const float sc = PAIR ? 65536.f : 1.f / 256.f;
               const float z = S.zs[hc][gr];
-              wo[(warp * MAX_G + n) * D + 16 * j + gid] = fmaf(S.oacc[j][hc] - off, 1.f / 256.f, z);
-              wo[(warp * MAX_G + n) * D + 16 * j + 8 + gid] = fmaf(S.oacc[j][hc + 2] - off, 1.f / 256.f, z);
+              wo[(warp * MAX_G + n) * D + 16 * j + gid] = fmaf(S.oacc[j][hc] - off, sc, z);
+              wo[(warp * MAX_G + n) * D + 16 * j + 8 + gid] = fmaf(S.oacc[j][hc + 2] - off, sc, z);
             }
           }
         }
@@ -1224,7 +1293,7 @@ int decode_ctas_per_sm(const DecodeArgs& a) {
   if (a.bf16_history) return occupancy_t<1, 2>(a);
   if (a.impl == 5) return 1;  // the tensor-memory kernel holds all of an SM's tensor memory
   if (a.impl == 1) return NG == 1 ? occupancy_t<1, 1>(a) : NG == 2 ? occupancy_t<2, 1>(a) : occupancy_t<4, 1>(a);
-  if (a.impl == 3 || a.impl == 6) return decode_ring_ctas_per_sm(a);
+  if (a.impl == 3) return NG == 1 ? occupancy_t<1, 3>(a) : NG == 2 ? occupancy_t<2, 3>(a) : occupancy_t<4, 3>(a);
   if (a.impl == 4) return NG == 1 ? occupancy_t<1, 4>(a) : NG == 2 ? occupancy_t<2, 4>(a) : occupancy_t<4, 4>(a);
   return NG == 1 ? occupancy_t<1, 0>(a) : NG == 2 ? occupancy_t<2, 0>(a) : occupancy_t<4, 0>(a);
 }
@@ -1235,14 +1304,16 @@ cudaError_t launch_decode_after_prep(const DecodeArgs& a, int grid, cudaStream_t
   prof_begin(prof, OSCAR_KERNEL_DECODE_MAIN, st);
   if (a.impl == 5 && !a.bf16_history) {
     e = launch_decode_tc(a, st);
-  } else if ((a.impl == 3 || a.impl == 6) && !a.bf16_history) {
-    e = launch_decode_ring(a, grid, st);
   } else if (a.bf16_history) {
     e = launch_decode_t<1, 2>(a, grid, st);
   } else if (a.impl == 1) {
     if (cv.NG == 1) e = launch_decode_t<1, 1>(a, grid, st);
     else if (cv.NG == 2) e = launch_decode_t<2, 1>(a, grid, st);
     else e = launch_decode_t<4, 1>(a, grid, st);
+  } else if (a.impl == 3) {
+    if (cv.NG == 1) e = launch_decode_t<1, 3>(a, grid, st);
+    else if (cv.NG == 2) e = launch_decode_t<2, 3>(a, grid, st);
+    else e = launch_decode_t<4, 3>(a, grid, st);
   } else if (a.impl == 4) {
     if (cv.NG == 1) e = launch_decode_t<1, 4>(a, grid, st);
     else if (cv.NG == 2) e = launch_decode_t<2, 4>(a, grid, st);
@@ -1262,7 +1333,15 @@ cudaError_t launch_decode_after_prep(const DecodeArgs& a, int grid, cudaStream_t
 
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof) {
   prof_begin(prof, OSCAR_KERNEL_DECODE_PREP, st);
-  const cudaError_t e = launch_pdl(prep_kernel, dim3(a.B * a.cv.Hkv, 4), dim3(128), 0, st, a);
+  cudaError_t e;
+  if (a.win_ext) {
+    static int limit[MAX_DEVICES];
+    e = raise_smem_limit(prep_window_kernel, limit, WINDOW_XCHG_BYTES);
+    if (e == cudaSuccess)
+      e = launch_pdl(prep_window_kernel, dim3(a.B * a.cv.Hkv, 2), dim3(512), WINDOW_XCHG_BYTES, st, a);
+  } else {
+    e = launch_pdl(prep_kernel, dim3(a.B * a.cv.Hkv, 4), dim3(128), 0, st, a);
+  }
   prof_end(prof, OSCAR_KERNEL_DECODE_PREP, st);
   if (e != cudaSuccess) return e;
   return launch_decode_after_prep(a, grid, st, prof);

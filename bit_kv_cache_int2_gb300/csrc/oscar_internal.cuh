@@ -441,12 +441,11 @@ constexpr int AUTO_MIN_PAGES = 28;
 // target: the most items the list may hold; resident: the decode CTAs that
 // run at once, or 0 to size items for `target` items in total.
 // Must be called by all threads of the block.
-// ring: the list of the ring decode kernel, whose window chunks are jobs
-// outside the CTAs' item list: always five 64-token chunks per (request, kv
-// head), history items sized for all of `resident` (or `target`), and the
-// records (history items + 5 B Hkv window chunks) within target + 2 B Hkv.
+// win_ext: the windows are attended before the decode kernel (window_slot);
+// the list holds history items only, sized for all of `resident` (or
+// `target`), and n_win = 0.
 __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int target, int resident,
-                                   int hist_item_unit_bytes, int* pre, int* red, bool ring = false) {
+                                   int hist_item_unit_bytes, int* pre, int* red, bool win_ext = false) {
   const int tid = threadIdx.x;
   // total history pages (over requests), times Hkv
   long long local = 0;
@@ -464,9 +463,9 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
   // window into its 5 chunks so that no single window item outlasts the
   // history items
   auto pages_per_item = [&](int items) {
-    s.wch = (ring || 5LL * B * Hkv * 4 <= items) ? 5 : 1;
+    s.wch = win_ext ? 0 : (5LL * B * Hkv * 4 <= items) ? 5 : 1;
     s.n_win = B * Hkv * s.wch;
-    int th = ring ? items : items - s.n_win;
+    int th = items - s.n_win;
     if (th < (items + 1) / 2) th = (items + 1) / 2;
     const long long S = (total + th - 1) / th;
     return S < 1 ? 1LL : S;
@@ -485,7 +484,7 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
         const int pages = (hist_lens[b] + PAGE - 1) / PAGE;
         n += (long long)Hkv * ((pages + s.S - 1) / s.S);
       }
-      if (n + (ring ? 3LL * B * Hkv : s.n_win) <= target || n <= (long long)B * Hkv) break;
+      if (n + s.n_win <= target || n <= (long long)B * Hkv) break;
       s.S += s.S / 8 > 1 ? s.S / 8 : 1;
     }
     int acc = 0;
@@ -624,7 +623,8 @@ struct DecodeArgs {
              // 6 ring kernel with one page per unit
   int bf16_history;
   int merge_hpc;  // query heads per merge CTA (divides G)
-  int ring;       // 1: the ring decode kernel's list (make_sched with ring)
+  int win_ext;    // 1: the BF16 window is attended before the decode kernel (prep / step kernel),
+                  // one record per (request, kv head) at window_slot()
   int balanced;   // 1: the tensor-memory kernel's balanced partition (decode grid in bal_grid)
   int bal_grid;
   int bal_wch;
@@ -753,9 +753,6 @@ __device__ __forceinline__ void prep_body(const DecodeArgs& a, int bk, int cq, i
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof);
-// The ring decode kernel (impl 3 and 6, oscar_decode_ring.cu).
-cudaError_t launch_decode_ring(const DecodeArgs& a, int grid, cudaStream_t st);
-int decode_ring_ctas_per_sm(const DecodeArgs& a);
 // The tensor-memory decode kernel (impl 5, oscar_decode_tc.cu): grid a.bal_grid, balanced partition.
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
 int decode_tc_smem_bytes(int head_bytes, int B);
@@ -834,8 +831,11 @@ cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_b
                           cudaStream_t st, Profiler* prof);
 // One decode step's first kernel: the append (as launch_append) and the packed
 // query (as prep_kernel) in one grid.
+// With a.win_ext the last of a (request, kv head)'s two append CTAs also
+// attends its window (win_counter: [B][Hkv] zero-initialised counters that
+// the kernel resets).
 cudaError_t launch_step(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* k,
-                        const __nv_bfloat16* v, int B, int* req_counter, const DecodeArgs& a,
+                        const __nv_bfloat16* v, int B, int* req_counter, int* win_counter, const DecodeArgs& a,
                         cudaStream_t st, Profiler* prof);
 // One token per request into a BF16-history cache (cv over the BF16 pool).
 cudaError_t launch_append_bf16(const CacheView& cv, const __nv_bfloat16* k, const __nv_bfloat16* v, int B,

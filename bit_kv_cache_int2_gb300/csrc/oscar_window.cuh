@@ -148,3 +148,130 @@ __device__ __forceinline__ void bf16_chunk_mma(Bf16State& S, const __nv_bfloat16
 
 
 }  // namespace oscar
+
+namespace oscar {
+
+// ------------------------------------------- whole window by one 512-thread block
+// The BF16 window of (request b, kv head kvh) -- sink and recent tokens, 20
+// tiles of 16 slots -- attended by the 16 warps of a 512-thread block for the
+// G query heads (unrotated q), written as ONE partial record at `slot`.  The
+// request's lengths after the step (L tokens, hist of them in history) are
+// passed in, so that it can run in the grid that appends the step's token.
+// Warp w takes tiles w and w + 16; the 16 warp states are then merged
+// pairwise through shared memory (`xs`, WINDOW_XCHG_BYTES).  All 512 threads
+// call it; it synchronises the block.
+constexpr int WINDOW_WARPS = 16;
+constexpr int WINDOW_XCHG_FLOATS = 36;  // m[2], l[2], oacc[8][4] per lane
+constexpr int WINDOW_XCHG_BYTES = (WINDOW_WARPS / 2) * 32 * WINDOW_XCHG_FLOATS * 4;
+
+__device__ __forceinline__ void window_block(const DecodeArgs& a, int b, int kvh, int L, int hist, int slot,
+                                             float* xs) {
+  const CacheView& cv = a.cv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tq = lane & 3;
+  const int G = cv.G, Hkv = cv.Hkv;
+  Bf16State S;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) S.oacc[j][0] = S.oacc[j][1] = S.oacc[j][2] = S.oacc[j][3] = 0.f;
+  S.m[0] = S.m[1] = -INFINITY;
+  S.l[0] = S.l[1] = 0.f;
+  {
+    const bool hv = gid < G;
+    const __nv_bfloat16* qrow = a.q + ((size_t)b * cv.Hq + kvh * G + (hv ? gid : 0)) * D + 32 * tq;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      S.bq[kk][0] = hv ? *(const uint32_t*)(qrow + 4 * kk) : 0u;
+      S.bq[kk][1] = hv ? *(const uint32_t*)(qrow + 4 * kk + 2) : 0u;
+    }
+  }
+  const size_t head = (size_t)b * Hkv + kvh;
+  const int nsink = L < SINK ? L : SINK;
+  const int recent = L > SINK ? L - SINK - hist : 0;
+  const int h0 = hist % RECENT;
+  for (int t = warp; t < 5 * 4; t += WINDOW_WARPS) {
+    const int ch = t >> 2, s = t & 3;  // chunk (0: sink, 1..4: ring quarters), 16-slot tile in it
+    uint64_t valid = 0;
+    const __nv_bfloat16 *Kb, *Vb;
+    if (ch == 0) {
+      valid = nsink >= 64 ? ~0ull : ((1ull << nsink) - 1ull);
+      Kb = cv.sink_k + head * SINK * D;
+      Vb = cv.sink_v + head * SINK * D;
+    } else {
+      const int s0 = 64 * (ch - 1);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int tt = lane + 32 * half;
+        const bool v = ((s0 + tt - h0 + RECENT) % RECENT) < recent;
+        valid |= (uint64_t)__ballot_sync(0xffffffffu, v) << (32 * half);
+      }
+      Kb = cv.ring_k + (head * RECENT + s0) * D;
+      Vb = cv.ring_v + (head * RECENT + s0) * D;
+    }
+    if ((valid >> (16 * s)) & 0xFFFFull) bf16_span_mma<false>(S, Kb, Vb, valid, lane, s, 1);
+  }
+  // pairwise merge: warps w + n take into warps w (n = 8, 4, 2, 1); lane
+  // layouts are the same in every warp and m is the same over a column's lanes
+  float* mine = xs + (size_t)lane * WINDOW_XCHG_FLOATS;
+  for (int n = WINDOW_WARPS / 2; n >= 1; n >>= 1) {
+    if (warp >= n && warp < 2 * n) {
+      float* d = mine + (size_t)(warp - n) * 32 * WINDOW_XCHG_FLOATS;
+      d[0] = S.m[0];
+      d[1] = S.m[1];
+      d[2] = S.l[0];
+      d[3] = S.l[1];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d[4 + 4 * j + e] = S.oacc[j][e];
+    }
+    __syncthreads();
+    if (warp < n) {
+      const float* d = mine + (size_t)warp * 32 * WINDOW_XCHG_FLOATS;
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        const float mo = d[hc], M = fmaxf(S.m[hc], mo);
+        const float fa = M == -INFINITY ? 0.f : ex2(S.m[hc] - M);
+        const float fb = M == -INFINITY ? 0.f : ex2(mo - M);
+        S.m[hc] = M;
+        S.l[hc] = S.l[hc] * fa + d[2 + hc] * fb;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          S.oacc[j][hc] = S.oacc[j][hc] * fa + d[4 + 4 * j + hc] * fb;
+          S.oacc[j][hc + 2] = S.oacc[j][hc + 2] * fa + d[4 + 4 * j + hc + 2] * fb;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (warp == 0) {
+#pragma unroll
+    for (int hc = 0; hc < 2; ++hc) {
+      S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 4);
+      S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 8);
+      S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 16);
+    }
+#pragma unroll
+    for (int hc = 0; hc < 2; ++hc) {
+      const int hn = 2 * tq + hc;
+      if (hn < G) {
+        float* rec = a.part + ((size_t)slot * G + hn) * PART_STRIDE;
+        if (gid == 0) {
+          rec[0] = S.m[hc];
+          rec[1] = S.l[hc];
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          rec[PART_O + 16 * gid + 2 * j] = S.oacc[j][hc];
+          rec[PART_O + 16 * gid + 2 * j + 1] = S.oacc[j][hc + 2];
+        }
+      }
+    }
+  }
+}
+
+// The record slot of the window of (request b, kv head kvh) when windows are
+// attended outside the decode kernel: the last B Hkv records of the scratch.
+__host__ __device__ __forceinline__ int window_slot(const DecodeArgs& a, int b, int kvh) {
+  return a.target_items + a.B * a.cv.Hkv + b * a.cv.Hkv + kvh;
+}
+
+}  // namespace oscar

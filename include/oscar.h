@@ -112,13 +112,10 @@ typedef enum {
 
 /* INT2 history decode kernels (the BF16-history baseline has one kernel). */
 typedef enum {
-  OSCAR_DECODE_TENSOR = 0,        /* tensor cores (default): the CTA's warps share a ring of page
-                                     stages and take work from it as they become free; with at most
-                                     4 query heads per kv head a warp takes two pages per tile as two
-                                     softmax streams, else one page; window chunks are single-warp
-                                     jobs for the warps that finish first */
+  OSCAR_DECODE_TENSOR = 0,        /* tensor cores; with at most 4 query heads per kv head a warp
+                                     takes two pages per tile as two softmax streams (default) */
   OSCAR_DECODE_CUDA_CORE = 1,     /* fp32 CUDA cores, one page per warp at a time */
-  OSCAR_DECODE_TENSOR_SINGLE = 2, /* tensor cores, each warp its own page stages, one page per tile */
+  OSCAR_DECODE_TENSOR_SINGLE = 2, /* tensor cores, one page per tile at any group size */
   OSCAR_DECODE_TCGEN05 = 3        /* tcgen05.mma with the codes unpacked into tensor memory:
                                      warp-specialised, one CTA per SM, 128-token tiles, an even
                                      static split of the work over the SMs */
