@@ -63,7 +63,7 @@ struct oscar_ctx {
   std::vector<int> has_cb;        // [layers] a non-uniform codebook is set: decode variant 4
   std::vector<float> clip_host;   // [layers][2][Hkv] copy of d_clip
   int* d_err = nullptr;
-  int* d_req_counter = nullptr;  // [max_batch] requests, then [max_batch][Hkv] windows (decode step)
+  int* d_req_counter = nullptr;  // [max_batch]
   int impl = 0;
   int ctas_per_sm = 4;
   int items_per_cta = 0;  // 0: automatic (make_sched)
@@ -334,7 +334,7 @@ oscar_status decode_args(oscar_ctx* ctx, int layer, const oscar_cache* cache, co
   a.merge_hpc = ctx->G;
   while (a.merge_hpc % 2 == 0 && batch * ctx->cfg.num_kv_heads * (ctx->G / a.merge_hpc) < ctx->num_sms)
     a.merge_hpc /= 2;
-  // the mma.sync INT2 kernels leave the BF16 window to the kernel before them
+  // the mma.sync INT2 kernels leave the BF16 window to the merge kernel
   a.win_ext = (!bf16_history && a.impl != 5) ? 1 : 0;
   a.balanced = 0;
   a.bal_grid = 0;
@@ -475,10 +475,9 @@ oscar_status oscar_create(const oscar_config* cfg, oscar_ctx** out) {
   const size_t cb_floats = (size_t)cfg->num_layers * 2 * cfg->num_kv_heads * CB_WORDS;
   if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_cb, cb_floats * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_err, sizeof(int));
-  const size_t counters = (size_t)cfg->max_batch * (1 + cfg->num_kv_heads);
-  if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_req_counter, sizeof(int) * counters);
+  if (e == cudaSuccess) e = cudaMalloc((void**)&ctx->d_req_counter, sizeof(int) * cfg->max_batch);
   if (e == cudaSuccess) e = cudaMemset(ctx->d_err, 0, sizeof(int));
-  if (e == cudaSuccess) e = cudaMemset(ctx->d_req_counter, 0, sizeof(int) * counters);
+  if (e == cudaSuccess) e = cudaMemset(ctx->d_req_counter, 0, sizeof(int) * cfg->max_batch);
   if (e == cudaSuccess) {
     // identity rotation and clip 1.0 until oscar_set_rotation is called
     std::vector<float> eye;
@@ -661,7 +660,7 @@ oscar_status oscar_decode_step(oscar_ctx* ctx, int layer, const oscar_cache* cac
   if (s != OSCAR_OK) return s;
   const cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = launch_step(a.cv, a.rot, (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, batch,
-                              ctx->d_req_counter, ctx->d_req_counter + ctx->cfg.max_batch, a, st, &ctx->prof);
+                              ctx->d_req_counter, a, st, &ctx->prof);
   if (e == cudaSuccess) e = launch_decode_after_prep(a, grid, st, &ctx->prof);
   return cuda_status(e);
 }

@@ -44,26 +44,6 @@ __global__ void __launch_bounds__(128) prep_kernel(DecodeArgs a) {
   prep_body(a, blockIdx.x, blockIdx.y, threadIdx.x, sm, true);
 }
 
-// The same, with the BF16 window of (request, kv head) x as well (the decode
-// kernel then holds history items only).  grid (B * Hkv, 2), block 512: y = 0
-// computes the packed query (four 128-thread parts, one channel quarter
-// each), y = 1 attends the window (window_block).  Both release the decode
-// kernel as soon as they have waited for earlier stream work: the decode
-// kernel reads nothing this grid writes before its own wait.
-__global__ void __launch_bounds__(512) prep_window_kernel(DecodeArgs a) {
-  extern __shared__ __align__(16) float xs[];
-  __shared__ PrepSmem psm[4];
-  const int bk = blockIdx.x;
-  if (blockIdx.y == 0) {
-    prep_body(a, bk, threadIdx.x >> 7, threadIdx.x & 127, psm[threadIdx.x >> 7], true);
-  } else {
-    pdl_wait();  // the window's tokens and q come from earlier stream work
-    pdl_launch_dependents();
-    const int b = bk / a.cv.Hkv, kvh = bk % a.cv.Hkv;
-    window_block(a, b, kvh, a.cv.seq_lens[b], a.cv.hist_lens[b], window_slot(a, b, kvh), xs);
-  }
-}
-
 // ------------------------------------------------------------ smem layout
 struct SmemLayout {
   int stage_bytes;   // per stage
@@ -450,7 +430,7 @@ constexpr int MW = 16;       // warps of the merge kernel
 constexpr int MERGE_MQ = 4;   // records per warp and round of loads
 
 struct MergeLayout {
-  int off_rv, off_y, off_tm, off_to, off_win, off_wo, off_h, off_mbar, off_red, off_pre, total;
+  int off_rv, off_y, off_tm, off_to, off_win, off_wo, off_h, off_mbar, off_red, off_pre, off_xs, total;
 };
 
 __host__ __device__ inline MergeLayout merge_layout(int B) {
@@ -476,6 +456,8 @@ __host__ __device__ inline MergeLayout merge_layout(int B) {
   o += 64 * 4;
   L.off_pre = (o + 7) & ~7;
   o = L.off_pre + (((B + 1) * 8 + 15) & ~15);  // int[B + 1], or long long[B + 1] for the balanced list
+  L.off_xs = (o + 15) & ~15;  // window attended here: the warps' exchange
+  o = L.off_xs + WINDOW_XCHG_BYTES;
   L.total = o;
   return L;
 }
@@ -542,13 +524,8 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
     const int pages_b = (cv.hist_lens[b] + PAGE - 1) / PAGE;
     nb = (pages_b + sc.S - 1) / sc.S;
     base = pre[b] + kvh * nb;
-    if (a.win_ext) {  // one window record, written before the decode kernel
-      wch = 1;
-      wslot = window_slot(a, b, kvh);
-    } else {
-      wch = sc.wch;
-      wslot = sc.n_hist + (b * Hkv + kvh) * sc.wch;
-    }
+    wch = sc.wch;  // 0 with win_ext: the window is attended here
+    wslot = sc.n_hist + (b * Hkv + kvh) * sc.wch;
     wmask = (1u << wch) - 1u;
   }
   const int WPH = MW / HPC;  // warps per head
@@ -558,6 +535,13 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
     // kernel finishes (the line is written again before it is read)
     const int slot = r < nb ? base + r : wslot + (r - nb);
     asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a.part + ((size_t)slot * G + h0 + n) * PART_STRIDE));
+  }
+  if (a.win_ext) {
+    // the BF16 window of (b, kvh), attended by this CTA's 16 warps while the
+    // decode kernel still runs: its tokens, q and the lengths are earlier
+    // stream work that was complete when the decode kernel released this grid
+    window_block(a, b, kvh, cv.seq_lens[b], cv.hist_lens[b], (float*)(smem + ML.off_xs), h0, HPC, wmv, wmv + MAX_G,
+                 wov);
   }
   pdl_wait();  // the decode kernel's partial records are complete and visible
 
@@ -654,11 +638,13 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
         OW = fma4(((const float4*)(tow + (h * WPH + k) * D))[lane], ww, OW);
       }
     }
-    if (lane == 0) {
-      wmv[h] = Mw;
-      wlv[h] = Lw;
+    if (!a.win_ext) {  // else the window state is already in place
+      if (lane == 0) {
+        wmv[h] = Mw;
+        wlv[h] = Lw;
+      }
+      ((float4*)(wov + h * D))[lane] = OW;
     }
-    ((float4*)(wov + h * D))[lane] = OW;
     const float4 Y = scale4(O, Ls > 0.f ? 1.f / Ls : 0.f);
     float am = fmaxf(fmaxf(fabsf(Y.x), fabsf(Y.y)), fmaxf(fabsf(Y.z), fabsf(Y.w)));
 #pragma unroll
@@ -768,7 +754,9 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
   const int gid = lane >> 2, tq = lane & 3;
   const int G = cv.G, Hkv = cv.Hkv;
 
-  pdl_launch_dependents();  // merge_kernel may be scheduled as CTAs of this grid retire
+  // merge_kernel is released once this CTA has waited for the kernel before
+  // it (pdl_once): the merge reads the window's tokens, q and the lengths
+  // before its own wait, and those are then complete
   if (threadIdx.x < NW * DEPTH) mbar_init(&mbar[threadIdx.x], 1);
   uint8_t* qpk = smem + L.off_qpk;
   if (threadIdx.x == 0) misc[1] = 0;
@@ -938,6 +926,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
       }
       if (!waited) {
         pdl_wait();  // q' (prep_kernel) is ready from here on
+        pdl_launch_dependents();
         waited = true;
       }
       bool timed_out = false;
@@ -1203,6 +1192,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
     cta_combine_write(a, wm, wl, wo, slot);
     if (!waited) {
       pdl_wait();
+      pdl_launch_dependents();
       waited = true;
     }
     if (misc[1]) break;
@@ -1211,7 +1201,10 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
     __syncthreads();
     it = misc[0];
   }
-  if (!waited) pdl_wait();
+  if (!waited) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
 }
 
 // Raise decode_kernel<NG, IMPL>'s dynamic shared-memory limit to `bytes` if it
@@ -1333,15 +1326,7 @@ cudaError_t launch_decode_after_prep(const DecodeArgs& a, int grid, cudaStream_t
 
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof) {
   prof_begin(prof, OSCAR_KERNEL_DECODE_PREP, st);
-  cudaError_t e;
-  if (a.win_ext) {
-    static int limit[MAX_DEVICES];
-    e = raise_smem_limit(prep_window_kernel, limit, WINDOW_XCHG_BYTES);
-    if (e == cudaSuccess)
-      e = launch_pdl(prep_window_kernel, dim3(a.B * a.cv.Hkv, 2), dim3(512), WINDOW_XCHG_BYTES, st, a);
-  } else {
-    e = launch_pdl(prep_kernel, dim3(a.B * a.cv.Hkv, 4), dim3(128), 0, st, a);
-  }
+  const cudaError_t e = launch_pdl(prep_kernel, dim3(a.B * a.cv.Hkv, 4), dim3(128), 0, st, a);
   prof_end(prof, OSCAR_KERNEL_DECODE_PREP, st);
   if (e != cudaSuccess) return e;
   return launch_decode_after_prep(a, grid, st, prof);

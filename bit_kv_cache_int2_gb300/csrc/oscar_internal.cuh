@@ -623,8 +623,8 @@ struct DecodeArgs {
              // 6 ring kernel with one page per unit
   int bf16_history;
   int merge_hpc;  // query heads per merge CTA (divides G)
-  int win_ext;    // 1: the BF16 window is attended before the decode kernel (prep / step kernel),
-                  // one record per (request, kv head) at window_slot()
+  int win_ext;    // 1: the BF16 window is attended by the merge kernel (before it waits for the
+                  // decode kernel), not by the decode kernel
   int balanced;   // 1: the tensor-memory kernel's balanced partition (decode grid in bal_grid)
   int bal_grid;
   int bal_wch;
@@ -831,11 +831,8 @@ cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_b
                           cudaStream_t st, Profiler* prof);
 // One decode step's first kernel: the append (as launch_append) and the packed
 // query (as prep_kernel) in one grid.
-// With a.win_ext the last of a (request, kv head)'s two append CTAs also
-// attends its window (win_counter: [B][Hkv] zero-initialised counters that
-// the kernel resets).
 cudaError_t launch_step(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* k,
-                        const __nv_bfloat16* v, int B, int* req_counter, int* win_counter, const DecodeArgs& a,
+                        const __nv_bfloat16* v, int B, int* req_counter, const DecodeArgs& a,
                         cudaStream_t st, Profiler* prof);
 // One token per request into a BF16-history cache (cv over the BF16 pool).
 cudaError_t launch_append_bf16(const CacheView& cv, const __nv_bfloat16* k, const __nv_bfloat16* v, int B,

@@ -8,7 +8,6 @@
 // OSCAR：一种面向长上下文 LLM 服务的注意力感知 2 位 KV 缓存量化系统", section
 // "服务系统：混合精度缓存布局".
 #include "oscar_internal.cuh"
-#include "oscar_window.cuh"
 
 namespace oscar {
 
@@ -187,36 +186,19 @@ __global__ void __launch_bounds__(512) append_kernel(CacheView cv, LayerRot rot,
 // each (as prep_kernel).  The query rotation does not depend on the append,
 // so the two run side by side.  Each CTA releases the decode kernel only once
 // its own writes are done and fenced: the decode kernel reads the cache state
-// (lengths, pages) before it waits for this grid.  With a.win_ext the later
-// of x's two append CTAs then attends x's window with the step's token in it
-// (window_block, the same computation as prep_window_kernel's).
+// (lengths, pages) before it waits for this grid.
 __global__ void __launch_bounds__(512) step_kernel(CacheView cv, LayerRot rot,
                                                    const __nv_bfloat16* __restrict__ knew,
                                                    const __nv_bfloat16* __restrict__ vnew,
-                                                   int* req_counter, int* win_counter, DecodeArgs a) {
-  extern __shared__ __align__(16) float xs[];
+                                                   int* req_counter, DecodeArgs a) {
   __shared__ PrepSmem psm[4];
-  __shared__ int last;
   const int bk = blockIdx.x;
   if (blockIdx.y < 2) {
     const int4 r = append_body(cv, rot, knew, vnew, 1, req_counter, bk, blockIdx.y, false);
     __syncthreads();
     __threadfence();
     pdl_launch_dependents();
-    if (a.win_ext) {
-      // release: this CTA's append is complete before the count; acquire:
-      // the later CTA reads the window after both appends
-      if (threadIdx.x == 0) {
-        last = atomic_add_acq_rel_gpu(&win_counter[bk], 1) == 1;
-        if (last) win_counter[bk] = 0;
-      }
-      __syncthreads();
-      if (last) {
-        const int b = bk / cv.Hkv, kvh = bk % cv.Hkv;
-        const int L = r.w ? r.x + 1 : r.x, H = r.w ? r.y + r.z : r.y;
-        window_block(a, b, kvh, L, H, window_slot(a, b, kvh), xs);
-      }
-    }
+    (void)r;
   } else {
     prep_body(a, bk, threadIdx.x >> 7, threadIdx.x & 127, psm[threadIdx.x >> 7], false);
     __syncthreads();
@@ -466,14 +448,11 @@ cudaError_t launch_append(const CacheView& cv, const LayerRot& rot, const __nv_b
 }
 
 cudaError_t launch_step(const CacheView& cv, const LayerRot& rot, const __nv_bfloat16* k,
-                        const __nv_bfloat16* v, int B, int* req_counter, int* win_counter, const DecodeArgs& a,
+                        const __nv_bfloat16* v, int B, int* req_counter, const DecodeArgs& a,
                         cudaStream_t st, Profiler* prof) {
-  static int limit[MAX_DEVICES];
-  cudaError_t e = raise_smem_limit(step_kernel, limit, WINDOW_XCHG_BYTES);
-  if (e != cudaSuccess) return e;
   prof_begin(prof, OSCAR_KERNEL_STEP, st);
-  e = launch_pdl(step_kernel, dim3(B * cv.Hkv, 3), dim3(512), a.win_ext ? WINDOW_XCHG_BYTES : 0, st, cv, rot, k, v,
-                 req_counter, win_counter, a);
+  const cudaError_t e =
+      launch_pdl(step_kernel, dim3(B * cv.Hkv, 3), dim3(512), 0, st, cv, rot, k, v, req_counter, a);
   prof_end(prof, OSCAR_KERNEL_STEP, st);
   return e;
 }

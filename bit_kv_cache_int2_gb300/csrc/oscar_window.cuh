@@ -154,18 +154,19 @@ namespace oscar {
 // ------------------------------------------- whole window by one 512-thread block
 // The BF16 window of (request b, kv head kvh) -- sink and recent tokens, 20
 // tiles of 16 slots -- attended by the 16 warps of a 512-thread block for the
-// G query heads (unrotated q), written as ONE partial record at `slot`.  The
-// request's lengths after the step (L tokens, hist of them in history) are
-// passed in, so that it can run in the grid that appends the step's token.
-// Warp w takes tiles w and w + 16; the 16 warp states are then merged
-// pairwise through shared memory (`xs`, WINDOW_XCHG_BYTES).  All 512 threads
-// call it; it synchronises the block.
+// G query heads (unrotated q); the request holds L tokens, hist of them in
+// history.  Warp w takes tiles w and w + 16; the 16 warp states are then
+// merged pairwise through shared memory (`xs`, WINDOW_XCHG_BYTES), and warp
+// 0 writes the result for query heads h0 .. h0 + nh - 1 of the kv head:
+// max m (log2 units), sum l and the unnormalised o to om[i], ol[i] and
+// oo[i * 128 + channel], i = head - h0.  All 512 threads call it; it
+// synchronises the block.
 constexpr int WINDOW_WARPS = 16;
 constexpr int WINDOW_XCHG_FLOATS = 36;  // m[2], l[2], oacc[8][4] per lane
 constexpr int WINDOW_XCHG_BYTES = (WINDOW_WARPS / 2) * 32 * WINDOW_XCHG_FLOATS * 4;
 
-__device__ __forceinline__ void window_block(const DecodeArgs& a, int b, int kvh, int L, int hist, int slot,
-                                             float* xs) {
+__device__ __forceinline__ void window_block(const DecodeArgs& a, int b, int kvh, int L, int hist, float* xs,
+                                             int h0, int nh, float* om, float* ol, float* oo) {
   const CacheView& cv = a.cv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tq = lane & 3;
   const int G = cv.G, Hkv = cv.Hkv;
@@ -186,7 +187,7 @@ __device__ __forceinline__ void window_block(const DecodeArgs& a, int b, int kvh
   const size_t head = (size_t)b * Hkv + kvh;
   const int nsink = L < SINK ? L : SINK;
   const int recent = L > SINK ? L - SINK - hist : 0;
-  const int h0 = hist % RECENT;
+  const int r0 = hist % RECENT;  // ring slot of the oldest recent token
   for (int t = warp; t < 5 * 4; t += WINDOW_WARPS) {
     const int ch = t >> 2, s = t & 3;  // chunk (0: sink, 1..4: ring quarters), 16-slot tile in it
     uint64_t valid = 0;
@@ -200,7 +201,7 @@ __device__ __forceinline__ void window_block(const DecodeArgs& a, int b, int kvh
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int tt = lane + 32 * half;
-        const bool v = ((s0 + tt - h0 + RECENT) % RECENT) < recent;
+        const bool v = ((s0 + tt - r0 + RECENT) % RECENT) < recent;
         valid |= (uint64_t)__ballot_sync(0xffffffffu, v) << (32 * half);
       }
       Kb = cv.ring_k + (head * RECENT + s0) * D;
@@ -251,27 +252,21 @@ __device__ __forceinline__ void window_block(const DecodeArgs& a, int b, int kvh
     }
 #pragma unroll
     for (int hc = 0; hc < 2; ++hc) {
-      const int hn = 2 * tq + hc;
-      if (hn < G) {
-        float* rec = a.part + ((size_t)slot * G + hn) * PART_STRIDE;
+      const int i = 2 * tq + hc - h0;
+      if (i >= 0 && i < nh && i + h0 < G) {
         if (gid == 0) {
-          rec[0] = S.m[hc];
-          rec[1] = S.l[hc];
+          om[i] = S.m[hc];
+          ol[i] = S.l[hc];
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          rec[PART_O + 16 * gid + 2 * j] = S.oacc[j][hc];
-          rec[PART_O + 16 * gid + 2 * j + 1] = S.oacc[j][hc + 2];
+          oo[i * D + 16 * gid + 2 * j] = S.oacc[j][hc];
+          oo[i * D + 16 * gid + 2 * j + 1] = S.oacc[j][hc + 2];
         }
       }
     }
   }
-}
-
-// The record slot of the window of (request b, kv head kvh) when windows are
-// attended outside the decode kernel: the last B Hkv records of the scratch.
-__host__ __device__ __forceinline__ int window_slot(const DecodeArgs& a, int b, int kvh) {
-  return a.target_items + a.B * a.cv.Hkv + b * a.cv.Hkv + kvh;
+  __syncthreads();
 }
 
 }  // namespace oscar
