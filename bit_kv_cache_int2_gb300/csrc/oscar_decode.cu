@@ -430,7 +430,7 @@ constexpr int MW = 16;       // warps of the merge kernel
 constexpr int MERGE_MQ = 4;   // records per warp and round of loads
 
 struct MergeLayout {
-  int off_rv, off_y, off_tm, off_to, off_win, off_wo, off_h, off_mbar, off_red, off_pre, off_xs, total;
+  int off_rv, off_y, off_tm, off_to, off_win, off_wo, off_h, off_mbar, off_red, off_pre, total;
 };
 
 __host__ __device__ inline MergeLayout merge_layout(int B) {
@@ -456,8 +456,6 @@ __host__ __device__ inline MergeLayout merge_layout(int B) {
   o += 64 * 4;
   L.off_pre = (o + 7) & ~7;
   o = L.off_pre + (((B + 1) * 8 + 15) & ~15);  // int[B + 1], or long long[B + 1] for the balanced list
-  L.off_xs = (o + 15) & ~15;  // window attended here: the warps' exchange
-  o = L.off_xs + WINDOW_XCHG_BYTES;
   L.total = o;
   return L;
 }
@@ -520,11 +518,11 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
     wslot = bl.n + a.B * Hkv + WIN_CHUNKS * (b * Hkv + kvh);
   } else {
     const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
-    const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red, a.win_ext != 0);
+    const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red, a.win_units != 0);
     const int pages_b = (cv.hist_lens[b] + PAGE - 1) / PAGE;
     nb = (pages_b + sc.S - 1) / sc.S;
     base = pre[b] + kvh * nb;
-    wch = sc.wch;  // 0 with win_ext: the window is attended here
+    wch = sc.wch;
     wslot = sc.n_hist + (b * Hkv + kvh) * sc.wch;
     wmask = (1u << wch) - 1u;
   }
@@ -535,13 +533,6 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
     // kernel finishes (the line is written again before it is read)
     const int slot = r < nb ? base + r : wslot + (r - nb);
     asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a.part + ((size_t)slot * G + h0 + n) * PART_STRIDE));
-  }
-  if (a.win_ext) {
-    // the BF16 window of (b, kvh), attended by this CTA's 16 warps while the
-    // decode kernel still runs: its tokens, q and the lengths are earlier
-    // stream work that was complete when the decode kernel released this grid
-    window_block(a, b, kvh, cv.seq_lens[b], cv.hist_lens[b], (float*)(smem + ML.off_xs), h0, HPC, wmv, wmv + MAX_G,
-                 wov);
   }
   pdl_wait();  // the decode kernel's partial records are complete and visible
 
@@ -638,13 +629,11 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
         OW = fma4(((const float4*)(tow + (h * WPH + k) * D))[lane], ww, OW);
       }
     }
-    if (!a.win_ext) {  // else the window state is already in place
-      if (lane == 0) {
-        wmv[h] = Mw;
-        wlv[h] = Lw;
-      }
-      ((float4*)(wov + h * D))[lane] = OW;
+    if (lane == 0) {
+      wmv[h] = Mw;
+      wlv[h] = Lw;
     }
+    ((float4*)(wov + h * D))[lane] = OW;
     const float4 Y = scale4(O, Ls > 0.f ? 1.f / Ls : 0.f);
     float am = fmaxf(fmaxf(fabsf(Y.x), fabsf(Y.y)), fmaxf(fabsf(Y.z), fabsf(Y.w)));
 #pragma unroll
@@ -754,9 +743,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
   const int gid = lane >> 2, tq = lane & 3;
   const int G = cv.G, Hkv = cv.Hkv;
 
-  // merge_kernel is released once this CTA has waited for the kernel before
-  // it (pdl_once): the merge reads the window's tokens, q and the lengths
-  // before its own wait, and those are then complete
+  pdl_launch_dependents();  // merge_kernel may be scheduled as CTAs of this grid retire
   if (threadIdx.x < NW * DEPTH) mbar_init(&mbar[threadIdx.x], 1);
   uint8_t* qpk = smem + L.off_qpk;
   if (threadIdx.x == 0) misc[1] = 0;
@@ -766,8 +753,17 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
   // history lengths and page tables come from earlier stream work: readable
   // before the wait on prep_kernel
   const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
-  const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red, a.win_ext != 0);
-  const int total = sc.n_hist + sc.n_win;
+  const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red, a.win_units != 0);
+  const int total = a.win_units ? sc.n_hist : sc.n_hist + sc.n_win;
+  // window units of this warp (win_units): unit u goes to CTA u % grid,
+  // warp (u / grid) % NW, and is attended right after the wait for the kernel
+  // before, while the warp's first pages are in flight
+  auto window_units = [&]() {
+    if (!a.win_units) return;
+    const int upw = sc.wch == 20 ? 1 : 4;
+    for (int u = blockIdx.x + (int)gridDim.x * warp; u < sc.n_win; u += (int)gridDim.x * NW)
+      window_unit(a, (u / sc.wch) / Hkv, (u / sc.wch) % Hkv, u % sc.wch, upw, sc.n_hist + u, lane);
+  };
   uint32_t seq = 0;  // stages consumed by this warp so far
   bool waited = false;
   int it = blockIdx.x;  // first item static, later ones from the work counter
@@ -925,9 +921,9 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
         if (lane == 0) issue(k, pid);
       }
       if (!waited) {
-        pdl_wait();  // q' (prep_kernel) is ready from here on
-        pdl_launch_dependents();
+        pdl_wait();  // q' (prep_kernel) and the window's tokens are ready from here on
         waited = true;
+        window_units();
       }
       bool timed_out = false;
       int k_fail = 0;
@@ -1192,8 +1188,8 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
     cta_combine_write(a, wm, wl, wo, slot);
     if (!waited) {
       pdl_wait();
-      pdl_launch_dependents();
       waited = true;
+      window_units();
     }
     if (misc[1]) break;
     __syncthreads();
@@ -1203,7 +1199,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
   }
   if (!waited) {
     pdl_wait();
-    pdl_launch_dependents();
+    window_units();
   }
 }
 
@@ -1245,7 +1241,10 @@ ScratchLayout scratch_layout(int B, int Hq, int Hkv, int G, int max_target_items
   s.off_qrot = s.off_done + up((size_t)B * Hkv * 4);
   s.off_qpack = s.off_qrot + up((size_t)B * Hq * D * 4);
   s.off_part = s.off_qpack + up((size_t)B * Hq * QPACK_CB_BYTES);  // room for codebook records
-  const size_t slots = (size_t)max_target_items + 2 * (size_t)B * Hkv;
+  // the item list (at most max_target_items history items, plus up to
+  // 2 B Hkv window items or records) and up to 20 window units per
+  // (request, kv head)
+  const size_t slots = (size_t)max_target_items + 22 * (size_t)B * Hkv;
   s.total = s.off_part + slots * G * PART_STRIDE * 4;
   return s;
 }

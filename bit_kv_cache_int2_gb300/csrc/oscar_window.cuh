@@ -151,25 +151,15 @@ __device__ __forceinline__ void bf16_chunk_mma(Bf16State& S, const __nv_bfloat16
 
 namespace oscar {
 
-// ------------------------------------------- whole window by one 512-thread block
-// The BF16 window of (request b, kv head kvh) -- sink and recent tokens, 20
-// tiles of 16 slots -- attended by the 16 warps of a 512-thread block for the
-// G query heads (unrotated q); the request holds L tokens, hist of them in
-// history.  Warp w takes tiles w and w + 16; the 16 warp states are then
-// merged pairwise through shared memory (`xs`, WINDOW_XCHG_BYTES), and warp
-// 0 writes the result for query heads h0 .. h0 + nh - 1 of the kv head:
-// max m (log2 units), sum l and the unnormalised o to om[i], ol[i] and
-// oo[i * 128 + channel], i = head - h0.  All 512 threads call it; it
-// synchronises the block.
-constexpr int WINDOW_WARPS = 16;
-constexpr int WINDOW_XCHG_FLOATS = 36;  // m[2], l[2], oacc[8][4] per lane
-constexpr int WINDOW_XCHG_BYTES = (WINDOW_WARPS / 2) * 32 * WINDOW_XCHG_FLOATS * 4;
-
-__device__ __forceinline__ void window_block(const DecodeArgs& a, int b, int kvh, int L, int hist, float* xs,
-                                             int h0, int nh, float* om, float* ol, float* oo) {
+// --------------------------------------------------- window units by one warp
+// The window of (request b, kv head kvh) -- 20 tiles of 16 slots: the sink,
+// then the four 64-slot quarters of the ring -- is attended in units of
+// `upw` tiles (1 or 4) by single warps, each unit written as its own partial
+// record (m, l, unnormalised o for the G heads; unrotated q).  Unit r of the
+// request covers tiles r * upw .. r * upw + upw - 1.
+__device__ __forceinline__ void window_unit(const DecodeArgs& a, int b, int kvh, int r, int upw, int slot, int lane) {
   const CacheView& cv = a.cv;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tq = lane & 3;
-  const int G = cv.G, Hkv = cv.Hkv;
+  const int gid = lane >> 2, tq = lane & 3, G = cv.G, Hkv = cv.Hkv;
   Bf16State S;
 #pragma unroll
   for (int j = 0; j < 8; ++j) S.oacc[j][0] = S.oacc[j][1] = S.oacc[j][2] = S.oacc[j][3] = 0.f;
@@ -185,88 +175,51 @@ __device__ __forceinline__ void window_block(const DecodeArgs& a, int b, int kvh
     }
   }
   const size_t head = (size_t)b * Hkv + kvh;
-  const int nsink = L < SINK ? L : SINK;
-  const int recent = L > SINK ? L - SINK - hist : 0;
+  const int Lq = cv.seq_lens[b], hist = cv.hist_lens[b];
+  const int nsink = Lq < SINK ? Lq : SINK;
+  const int recent = Lq > SINK ? Lq - SINK - hist : 0;
   const int r0 = hist % RECENT;  // ring slot of the oldest recent token
-  for (int t = warp; t < 5 * 4; t += WINDOW_WARPS) {
-    const int ch = t >> 2, s = t & 3;  // chunk (0: sink, 1..4: ring quarters), 16-slot tile in it
-    uint64_t valid = 0;
-    const __nv_bfloat16 *Kb, *Vb;
-    if (ch == 0) {
-      valid = nsink >= 64 ? ~0ull : ((1ull << nsink) - 1ull);
-      Kb = cv.sink_k + head * SINK * D;
-      Vb = cv.sink_v + head * SINK * D;
-    } else {
-      const int s0 = 64 * (ch - 1);
+  const int t0 = r * upw, ch = t0 >> 2, s0 = t0 & 3;  // first tile, its 64-slot chunk and place in it
+  uint64_t valid = 0;
+  const __nv_bfloat16 *Kb, *Vb;
+  if (ch == 0) {
+    valid = nsink >= 64 ? ~0ull : ((1ull << nsink) - 1ull);
+    Kb = cv.sink_k + head * SINK * D;
+    Vb = cv.sink_v + head * SINK * D;
+  } else {
+    const int c0 = 64 * (ch - 1);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int tt = lane + 32 * half;
-        const bool v = ((s0 + tt - r0 + RECENT) % RECENT) < recent;
-        valid |= (uint64_t)__ballot_sync(0xffffffffu, v) << (32 * half);
-      }
-      Kb = cv.ring_k + (head * RECENT + s0) * D;
-      Vb = cv.ring_v + (head * RECENT + s0) * D;
+    for (int half = 0; half < 2; ++half) {
+      const int tt = lane + 32 * half;
+      const bool v = ((c0 + tt - r0 + RECENT) % RECENT) < recent;
+      valid |= (uint64_t)__ballot_sync(0xffffffffu, v) << (32 * half);
     }
-    if ((valid >> (16 * s)) & 0xFFFFull) bf16_span_mma<false>(S, Kb, Vb, valid, lane, s, 1);
+    Kb = cv.ring_k + (head * RECENT + c0) * D;
+    Vb = cv.ring_v + (head * RECENT + c0) * D;
   }
-  // pairwise merge: warps w + n take into warps w (n = 8, 4, 2, 1); lane
-  // layouts are the same in every warp and m is the same over a column's lanes
-  float* mine = xs + (size_t)lane * WINDOW_XCHG_FLOATS;
-  for (int n = WINDOW_WARPS / 2; n >= 1; n >>= 1) {
-    if (warp >= n && warp < 2 * n) {
-      float* d = mine + (size_t)(warp - n) * 32 * WINDOW_XCHG_FLOATS;
-      d[0] = S.m[0];
-      d[1] = S.m[1];
-      d[2] = S.l[0];
-      d[3] = S.l[1];
+  bf16_span_mma<false>(S, Kb, Vb, valid, lane, s0, upw);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) d[4 + 4 * j + e] = S.oacc[j][e];
-    }
-    __syncthreads();
-    if (warp < n) {
-      const float* d = mine + (size_t)warp * 32 * WINDOW_XCHG_FLOATS;
-#pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        const float mo = d[hc], M = fmaxf(S.m[hc], mo);
-        const float fa = M == -INFINITY ? 0.f : ex2(S.m[hc] - M);
-        const float fb = M == -INFINITY ? 0.f : ex2(mo - M);
-        S.m[hc] = M;
-        S.l[hc] = S.l[hc] * fa + d[2 + hc] * fb;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          S.oacc[j][hc] = S.oacc[j][hc] * fa + d[4 + 4 * j + hc] * fb;
-          S.oacc[j][hc + 2] = S.oacc[j][hc + 2] * fa + d[4 + 4 * j + hc + 2] * fb;
-        }
-      }
-    }
-    __syncthreads();
+  for (int hc = 0; hc < 2; ++hc) {
+    S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 4);
+    S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 8);
+    S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 16);
   }
-  if (warp == 0) {
 #pragma unroll
-    for (int hc = 0; hc < 2; ++hc) {
-      S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 4);
-      S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 8);
-      S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 16);
-    }
+  for (int hc = 0; hc < 2; ++hc) {
+    const int n = 2 * tq + hc;
+    if (n < G) {
+      float* rec = a.part + ((size_t)slot * G + n) * PART_STRIDE;
+      if (gid == 0) {
+        rec[0] = S.m[hc];
+        rec[1] = S.l[hc];
+      }
 #pragma unroll
-    for (int hc = 0; hc < 2; ++hc) {
-      const int i = 2 * tq + hc - h0;
-      if (i >= 0 && i < nh && i + h0 < G) {
-        if (gid == 0) {
-          om[i] = S.m[hc];
-          ol[i] = S.l[hc];
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          oo[i * D + 16 * gid + 2 * j] = S.oacc[j][hc];
-          oo[i * D + 16 * gid + 2 * j + 1] = S.oacc[j][hc + 2];
-        }
+      for (int j = 0; j < 8; ++j) {
+        rec[PART_O + 16 * gid + 2 * j] = S.oacc[j][hc];
+        rec[PART_O + 16 * gid + 2 * j + 1] = S.oacc[j][hc + 2];
       }
     }
   }
-  __syncthreads();
 }
 
 }  // namespace oscar
