@@ -334,8 +334,6 @@ oscar_status decode_args(oscar_ctx* ctx, int layer, const oscar_cache* cache, co
   a.merge_hpc = ctx->G;
   while (a.merge_hpc % 2 == 0 && batch * ctx->cfg.num_kv_heads * (ctx->G / a.merge_hpc) < ctx->num_sms)
     a.merge_hpc /= 2;
-  // the mma.sync INT2 kernels attend the BF16 window in single-warp units
-  a.win_units = (!bf16_history && a.impl != 5) ? 1 : 0;
   a.balanced = 0;
   a.bal_grid = 0;
   a.bal_wch = 0;

@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
     wslot = bl.n + a.B * Hkv + WIN_CHUNKS * (b * Hkv + kvh);
   } else {
     const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
-    const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red, a.win_units != 0);
+    const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
     const int pages_b = (cv.hist_lens[b] + PAGE - 1) / PAGE;
     nb = (pages_b + sc.S - 1) / sc.S;
     base = pre[b] + kvh * nb;
@@ -753,17 +753,8 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
   // history lengths and page tables come from earlier stream work: readable
   // before the wait on prep_kernel
   const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
-  const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red, a.win_units != 0);
-  const int total = a.win_units ? sc.n_hist : sc.n_hist + sc.n_win;
-  // window units of this warp (win_units): unit u goes to CTA u % grid,
-  // warp (u / grid) % NW, and is attended right after the wait for the kernel
-  // before, while the warp's first pages are in flight
-  auto window_units = [&]() {
-    if (!a.win_units) return;
-    const int upw = sc.wch == 20 ? 1 : 4;
-    for (int u = blockIdx.x + (int)gridDim.x * warp; u < sc.n_win; u += (int)gridDim.x * NW)
-      window_unit(a, (u / sc.wch) / Hkv, (u / sc.wch) % Hkv, u % sc.wch, upw, sc.n_hist + u, lane);
-  };
+  const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
+  const int total = sc.n_hist + sc.n_win;
   uint32_t seq = 0;  // stages consumed by this warp so far
   bool waited = false;
   int it = blockIdx.x;  // first item static, later ones from the work counter
@@ -921,9 +912,8 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
         if (lane == 0) issue(k, pid);
       }
       if (!waited) {
-        pdl_wait();  // q' (prep_kernel) and the window's tokens are ready from here on
+        pdl_wait();  // q' (prep_kernel) is ready from here on
         waited = true;
-        window_units();
       }
       bool timed_out = false;
       int k_fail = 0;
@@ -1189,7 +1179,6 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
     if (!waited) {
       pdl_wait();
       waited = true;
-      window_units();
     }
     if (misc[1]) break;
     __syncthreads();
@@ -1197,10 +1186,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
     __syncthreads();
     it = misc[0];
   }
-  if (!waited) {
-    pdl_wait();
-    window_units();
-  }
+  if (!waited) pdl_wait();
 }
 
 // Raise decode_kernel<NG, IMPL>'s dynamic shared-memory limit to `bytes` if it
@@ -1241,10 +1227,7 @@ ScratchLayout scratch_layout(int B, int Hq, int Hkv, int G, int max_target_items
   s.off_qrot = s.off_done + up((size_t)B * Hkv * 4);
   s.off_qpack = s.off_qrot + up((size_t)B * Hq * D * 4);
   s.off_part = s.off_qpack + up((size_t)B * Hq * QPACK_CB_BYTES);  // room for codebook records
-  // the item list (at most max_target_items history items, plus up to
-  // 2 B Hkv window items or records) and up to 20 window units per
-  // (request, kv head)
-  const size_t slots = (size_t)max_target_items + 22 * (size_t)B * Hkv;
+  const size_t slots = (size_t)max_target_items + 2 * (size_t)B * Hkv;
   s.total = s.off_part + slots * G * PART_STRIDE * 4;
   return s;
 }

@@ -441,13 +441,8 @@ constexpr int AUTO_MIN_PAGES = 28;
 // target: the most items the list may hold; resident: the decode CTAs that
 // run at once, or 0 to size items for `target` items in total.
 // Must be called by all threads of the block.
-// win_units: the windows are single-warp units outside the CTAs' item list
-// (window_unit), wch per (request, kv head): 20 units of one 16-slot tile
-// while B Hkv 20 units fit 4 * resident warps, else 5 of four tiles; the
-// list holds history items only, sized for all of `resident` (or `target`),
-// and its records number at most target + 3 B Hkv besides the window's.
 __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int target, int resident,
-                                   int hist_item_unit_bytes, int* pre, int* red, bool win_units = false) {
+                                   int hist_item_unit_bytes, int* pre, int* red) {
   const int tid = threadIdx.x;
   // total history pages (over requests), times Hkv
   long long local = 0;
@@ -465,12 +460,9 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
   // window into its 5 chunks so that no single window item outlasts the
   // history items
   auto pages_per_item = [&](int items) {
-    if (win_units)
-      s.wch = (20LL * B * Hkv <= 4LL * (resident > 0 ? resident : target)) ? 20 : 5;
-    else
-      s.wch = (5LL * B * Hkv * 4 <= items) ? 5 : 1;
+    s.wch = (5LL * B * Hkv * 4 <= items) ? 5 : 1;
     s.n_win = B * Hkv * s.wch;
-    int th = win_units ? items : items - s.n_win;
+    int th = items - s.n_win;
     if (th < (items + 1) / 2) th = (items + 1) / 2;
     const long long S = (total + th - 1) / th;
     return S < 1 ? 1LL : S;
@@ -489,7 +481,7 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
         const int pages = (hist_lens[b] + PAGE - 1) / PAGE;
         n += (long long)Hkv * ((pages + s.S - 1) / s.S);
       }
-      if (n + (win_units ? 0 : s.n_win) <= target || n <= (long long)B * Hkv) break;
+      if (n + s.n_win <= target || n <= (long long)B * Hkv) break;
       s.S += s.S / 8 > 1 ? s.S / 8 : 1;
     }
     int acc = 0;
@@ -505,7 +497,7 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
   s.S = red[0];
   __syncthreads();
   s.n_hist = pre[B];
-  s.win_first = !win_units && (long long)WIN_BYTES_PER_HEAD / s.wch > (long long)s.S * hist_item_unit_bytes;
+  s.win_first = (long long)WIN_BYTES_PER_HEAD / s.wch > (long long)s.S * hist_item_unit_bytes;
   return s;
 }
 
@@ -628,7 +620,6 @@ struct DecodeArgs {
              // 6 ring kernel with one page per unit
   int bf16_history;
   int merge_hpc;  // query heads per merge CTA (divides G)
-  int win_units;  // 1: the BF16 window is attended in single-warp units (make_sched with win_units)
   int balanced;   // 1: the tensor-memory kernel's balanced partition (decode grid in bal_grid)
   int bal_grid;
   int bal_wch;

@@ -58,8 +58,7 @@ __device__ __forceinline__ void quant_store_v_global(float y, int j, int g, floa
 // Hkv + kv head, isv = 0 for K, 1 for V.  The body waits for earlier stream
 // work after issuing its rotation-table loads; with `release` it then lets
 // its dependents launch at once, otherwise the caller releases them later.
-// Returns (L, H, demote, ok) as read before the append.
-__device__ __forceinline__ int4 append_body(const CacheView& cv, const LayerRot& rot,
+__device__ __forceinline__ void append_body(const CacheView& cv, const LayerRot& rot,
                                             const __nv_bfloat16* __restrict__ knew,
                                             const __nv_bfloat16* __restrict__ vnew, int do_append,
                                             int* req_counter, int bk, int isv, bool release) {
@@ -168,7 +167,6 @@ __device__ __forceinline__ int4 append_body(const CacheView& cv, const LayerRot&
       }
     }
   }
-  return make_int4(L, H, demote, ok);
 }
 
 
@@ -194,17 +192,13 @@ __global__ void __launch_bounds__(512) step_kernel(CacheView cv, LayerRot rot,
   __shared__ PrepSmem psm[4];
   const int bk = blockIdx.x;
   if (blockIdx.y < 2) {
-    const int4 r = append_body(cv, rot, knew, vnew, 1, req_counter, bk, blockIdx.y, false);
-    __syncthreads();
-    __threadfence();
-    pdl_launch_dependents();
-    (void)r;
+    append_body(cv, rot, knew, vnew, 1, req_counter, bk, blockIdx.y, false);
   } else {
     prep_body(a, bk, threadIdx.x >> 7, threadIdx.x & 127, psm[threadIdx.x >> 7], false);
-    __syncthreads();
-    __threadfence();
-    pdl_launch_dependents();
   }
+  __syncthreads();
+  __threadfence();
+  pdl_launch_dependents();
 }
 
 // ------------------------------------------------------------------ import

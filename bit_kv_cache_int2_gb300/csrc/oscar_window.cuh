@@ -149,77 +149,3 @@ __device__ __forceinline__ void bf16_chunk_mma(Bf16State& S, const __nv_bfloat16
 
 }  // namespace oscar
 
-namespace oscar {
-
-// --------------------------------------------------- window units by one warp
-// The window of (request b, kv head kvh) -- 20 tiles of 16 slots: the sink,
-// then the four 64-slot quarters of the ring -- is attended in units of
-// `upw` tiles (1 or 4) by single warps, each unit written as its own partial
-// record (m, l, unnormalised o for the G heads; unrotated q).  Unit r of the
-// request covers tiles r * upw .. r * upw + upw - 1.
-__device__ __forceinline__ void window_unit(const DecodeArgs& a, int b, int kvh, int r, int upw, int slot, int lane) {
-  const CacheView& cv = a.cv;
-  const int gid = lane >> 2, tq = lane & 3, G = cv.G, Hkv = cv.Hkv;
-  Bf16State S;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) S.oacc[j][0] = S.oacc[j][1] = S.oacc[j][2] = S.oacc[j][3] = 0.f;
-  S.m[0] = S.m[1] = -INFINITY;
-  S.l[0] = S.l[1] = 0.f;
-  {
-    const bool hv = gid < G;
-    const __nv_bfloat16* qrow = a.q + ((size_t)b * cv.Hq + kvh * G + (hv ? gid : 0)) * D + 32 * tq;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      S.bq[kk][0] = hv ? *(const uint32_t*)(qrow + 4 * kk) : 0u;
-      S.bq[kk][1] = hv ? *(const uint32_t*)(qrow + 4 * kk + 2) : 0u;
-    }
-  }
-  const size_t head = (size_t)b * Hkv + kvh;
-  const int Lq = cv.seq_lens[b], hist = cv.hist_lens[b];
-  const int nsink = Lq < SINK ? Lq : SINK;
-  const int recent = Lq > SINK ? Lq - SINK - hist : 0;
-  const int r0 = hist % RECENT;  // ring slot of the oldest recent token
-  const int t0 = r * upw, ch = t0 >> 2, s0 = t0 & 3;  // first tile, its 64-slot chunk and place in it
-  uint64_t valid = 0;
-  const __nv_bfloat16 *Kb, *Vb;
-  if (ch == 0) {
-    valid = nsink >= 64 ? ~0ull : ((1ull << nsink) - 1ull);
-    Kb = cv.sink_k + head * SINK * D;
-    Vb = cv.sink_v + head * SINK * D;
-  } else {
-    const int c0 = 64 * (ch - 1);
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int tt = lane + 32 * half;
-      const bool v = ((c0 + tt - r0 + RECENT) % RECENT) < recent;
-      valid |= (uint64_t)__ballot_sync(0xffffffffu, v) << (32 * half);
-    }
-    Kb = cv.ring_k + (head * RECENT + c0) * D;
-    Vb = cv.ring_v + (head * RECENT + c0) * D;
-  }
-  bf16_span_mma<false>(S, Kb, Vb, valid, lane, s0, upw);
-#pragma unroll
-  for (int hc = 0; hc < 2; ++hc) {
-    S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 4);
-    S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 8);
-    S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], 16);
-  }
-#pragma unroll
-  for (int hc = 0; hc < 2; ++hc) {
-    const int n = 2 * tq + hc;
-    if (n < G) {
-      float* rec = a.part + ((size_t)slot * G + n) * PART_STRIDE;
-      if (gid == 0) {
-        rec[0] = S.m[hc];
-        rec[1] = S.l[hc];
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        rec[PART_O + 16 * gid + 2 * j] = S.oacc[j][hc];
-        rec[PART_O + 16 * gid + 2 * j + 1] = S.oacc[j][hc + 2];
-      }
-    }
-  }
-}
-
-}  // namespace oscar
