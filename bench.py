@@ -599,6 +599,37 @@ def serving_measurement(wl, dev, n_req=48, gen=64, lo=8192, hi=24576, budget_req
                     "import_seconds: device time of the imports (CUDA events around each call)"}
 
 
+def bench_config(args, wl):
+    """The workload description both arms print (identical, so that the two
+    lines name the same configuration)."""
+    return {"workload": args.workload, "batch": wl["B"], "q_heads": wl["Hq"], "kv_heads": wl["Hkv"], "head_dim": 128,
+            "context": wl["L"], "group_size": wl["g"], "clip": wl["clip"], "parallelism": "replicas",
+            "l2": "every timed call reads a cache copy other than the last few: the copies rotated over total at "
+                  "least 3x the L2 size (129 MB), so no call finds its inputs in L2"}
+
+
+def oracle_subprocess_seconds(host, wl, U, q, threads, budget_s):
+    """oracle_sample run in a fresh interpreter whose BLAS and OpenMP pools
+    are limited to `threads` (the pool size is fixed when numpy loads)."""
+    import numpy as np
+
+    with tempfile.TemporaryDirectory() as d:
+        f = os.path.join(d, "in.npz")
+        pool, pt, sk, sv, rk, rv, L, H = host
+        np.savez(f, pool=pool, pt=pt, sk=sk, sv=sv, rk=rk, rv=rv, L=L, H=H, UK=U[0], UV=U[1], q=q)
+        code = ("import json, sys, numpy as np; sys.path.insert(0, %r); import bench; d = np.load(%r); "
+                "h = (d['pool'], d['pt'], d['sk'], d['sv'], d['rk'], d['rv'], int(d['L']), int(d['H'])); "
+                "print(json.dumps(bench.oracle_sample(h, %r, (d['UK'], d['UV']), d['q'], list(range(%d)), "
+                "budget_s=%r)))") % (ROOT, f, wl, wl["Hkv"], budget_s)
+        env = dict(os.environ, OMP_NUM_THREADS=str(threads), OPENBLAS_NUM_THREADS=str(threads),
+                   MKL_NUM_THREADS=str(threads))
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+        if r.returncode != 0:
+            return None, 0
+        sec, done = json.loads(r.stdout.strip().splitlines()[-1])
+        return sec, done
+
+
 def blas_threads():
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         if os.environ.get(var):
@@ -682,16 +713,20 @@ def run_reference(args, wl):
         if i >= args.warmup:
             per_step.append(sec * scale)  # oracle_sample already scales one head to Hkv heads
     value = statistics.median(per_step) * 1e6
+    # the time the oracle actually took per sampled step, before any scaling
+    raw_us = value / (scale * Hkv)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "batch": wl["B"], "q_heads": Hq, "kv_heads": Hkv, "head_dim": 128,
-                   "context": L, "group_size": g, "clip": wl["clip"], "parallelism": "replicas"},
+        "config": bench_config(args, wl),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
                          "sample": f"per step: KV head 0 over {S} of the {H} history tokens (pages quantised by "
                                    f"the oracle from 1024 seeded tokens and tiled) + window + one demotion, "
-                                   f"scaled x{scale:.1f} (history) and x{Hkv} (heads)"},
+                                   f"scaled x{scale:.1f} (history) and x{Hkv} (heads): an extrapolation, not a "
+                                   f"timing of the whole step",
+                         "measured_us_per_sampled_step": raw_us, "sampled_history_tokens": S,
+                         "measured_us_per_sampled_history_token": raw_us / S, "extrapolated": True},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -718,9 +753,10 @@ def run_ours(args, wl):
     Hkv, g, Bsz = wl["Hkv"], wl["g"], wl["B"]
     per_copy = algorithmic_bytes(wl["L"] - 320, wl["L"], Hkv, g) * Bsz
     n_copies = max(2, -(-3 * l2 // per_copy))  # rotate over >= 3x L2 of caches
-    Kp, nd, ne = min(K, 2000), min(K, 1000), min(K, 1000)
+    Kp, nd, ne = min(K, 2000), max(200, min(K, 1000)), min(K, 1000)
     na = min(K, 200)  # demotion-only calls
-    total_appends = W + K + Kp + 2 * ne + na  # two end-to-end forms
+    n_pc = max(200, K)  # steps timed one by one for the percentiles
+    total_appends = W + K + n_pc + Kp + 2 * ne + na  # two end-to-end forms
     extra = max(total_appends // n_copies + 16, 80)  # appends per cache copy, with margin; >= a prefill chunk
     wk = build_workload(wl, dev, n_copies, extra, bf16_copies=2)
     ctx, cfg = wk["ctx"], wk["cfg"]
@@ -769,11 +805,15 @@ def run_ours(args, wl):
     err = oscar.oscar_get_error(ctx)
     assert err == 0, f"device error {err}"
     assert torch.isfinite(out.float()).all()
+    # ---- the same steps timed one by one: median and spread over >= 200 steps
+    pc_step = per_call_times(lambda i: step(W + K + i), n_pc, stream)
+    step_med, step_p10, step_p90 = percentiles(pc_step)
+    base_after_pc = W + K + n_pc
     # ---- per-kernel times over the same kind of steps (profiling pass)
     oscar.oscar_profile_enable(ctx, True)
     oscar.oscar_profile_read(ctx, 0, reset=True)
     lens_before = [int(c["hist_lens"][0]) for c in wk["copies"]]
-    for i in range(W + K, W + K + Kp):
+    for i in range(base_after_pc, base_after_pc + Kp):
         step(i)
     torch.cuda.synchronize()
     prof = {}
@@ -803,12 +843,26 @@ def run_ours(args, wl):
     for i in range(5):
         oscar.oscar_decode(ctx, 0, wk["copies"][i % n_copies], q, out, lse, scratch, Bsz)
     int2_us = time_calls(lambda i: decodes[i % n_copies](), nd)
+    int2_med, int2_p10, int2_p90 = percentiles(per_call_times(lambda i: decodes[i % n_copies](), nd, stream))
     bf_out = torch.empty_like(q)
     bscratch = oscar.alloc_scratch(cfg, dev)
     for i in range(5):
         oscar.oscar_decode_bf16_history(wk["bctx"], wk["bf"][i % 2], q, bf_out, None, bscratch, Bsz)
-    bf16_us = time_calls(lambda i: oscar.oscar_decode_bf16_history(wk["bctx"], wk["bf"][i % 2], q, bf_out, None,
-                                                                   bscratch, Bsz), min(nd, 200))
+    bf16_call = lambda i: oscar.oscar_decode_bf16_history(wk["bctx"], wk["bf"][i % 2], q, bf_out, None, bscratch, Bsz)
+    bf16_us = time_calls(bf16_call, nd)
+    bf16_med, bf16_p10, bf16_p90 = percentiles(per_call_times(bf16_call, nd, stream))
+    # ---- the other INT2 decode kernels on the same caches and q (the choice
+    # of the default is measured, not assumed)
+    variants = {}
+    for name, impl in (("tensor_single", oscar.DECODE_TENSOR_SINGLE), ("cuda_core", oscar.DECODE_CUDA_CORE),
+                       ("tcgen05", oscar.DECODE_TCGEN05)):
+        oscar.oscar_set_option(ctx, oscar.OPT_DECODE_IMPL, impl)
+        calls_v = [oscar.bind_decode(ctx, 0, wk["copies"][c], q, out, lse, scratch, Bsz) for c in range(n_copies)]
+        for i in range(3):
+            calls_v[i % n_copies]()
+        variants[name] = time_calls(lambda i: calls_v[i % n_copies](), 50 if name == "cuda_core" else 200)
+    oscar.oscar_set_option(ctx, oscar.OPT_DECODE_IMPL, oscar.DECODE_TENSOR)
+    assert oscar.oscar_get_error(ctx) == 0
     bf16_bytes = Hkv * Bsz * ((wl["L"] - 320) * 512 + 320 * 512) + ((wl["L"] - 320 + 63) // 64) * 4
     # ---- demotion alone (oscar_append; one token per request, each demoting one)
     appends = [oscar.bind_append(ctx, 0, wk["copies"][c], Bsz) for c in range(n_copies)]
@@ -1001,10 +1055,13 @@ def run_ours(args, wl):
                 c0["sink_v"][0].float().cpu().numpy().astype(np.float64),
                 c0["ring_k"][0].float().cpu().numpy().astype(np.float64),
                 c0["ring_v"][0].float().cpu().numpy().astype(np.float64), L, H)
-        sec, done = oracle_sample(host, wl, wk["U"], q[0].float().cpu().numpy().astype(np.float64),
-                                  list(range(Hkv)), budget_s=args.cpu_budget)
+        qh = q[0].float().cpu().numpy().astype(np.float64)
+        sec, done = oracle_sample(host, wl, wk["U"], qh, list(range(Hkv)), budget_s=args.cpu_budget)
+        sec1, done1 = oracle_subprocess_seconds(host, wl, wk["U"], qh, 1, args.cpu_budget)
         cpu = {"value": sec * 1e6, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-               "sample": f"{done} of {Hkv} KV heads of one decode step on the GPU-built cache, scaled to {Hkv}"}
+               "sample": f"{done} of {Hkv} KV heads of one decode step on the GPU-built cache, scaled to {Hkv}",
+               "single_thread_value": None if sec1 is None else sec1 * 1e6,
+               "single_thread_sample": f"{done1} of {Hkv} KV heads, one BLAS / OpenMP thread, scaled to {Hkv}"}
         psec = oracle_prefill_sample(host, wl, wk["U"], q_pf[0].float().cpu().numpy().astype(np.float64),
                                      k_pf[0].float().cpu().numpy().astype(np.float64),
                                      v_pf[0].float().cpu().numpy().astype(np.float64))
@@ -1013,15 +1070,25 @@ def run_ours(args, wl):
         calib_cpu = oracle_calibration_sample(cal_sets[0], ratios, Hkv)
     n_launch = 3 * K  # append + q rotation, decode, merge per step
     value = ms_per_step * 1e3 / world
+    vs_bf16 = {"int2_decode_us_median": int2_med, "bf16_history_decode_us_median": bf16_med,
+               "speedup_vs_bf16": bf16_med / int2_med, "int2_decode_us_mean": int2_us,
+               "bf16_history_decode_us_mean": bf16_us, "speedup_vs_bf16_mean": bf16_us / int2_us}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_per_step, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "int2 codes, f16/bf16 tensor-core MMA, fp32 accumulate", "data": "synthetic",
-        "config": {"workload": args.workload, "batch": Bsz, "q_heads": wl["Hq"], "kv_heads": Hkv, "head_dim": 128,
-                   "context": wl["L"], "group_size": g, "clip": wl["clip"], "parallelism": "replicas",
-                   "l2": f"rotating over {n_copies} cache copies ({n_copies * per_copy / 1e6:.0f} MB > 3x L2)"},
+        "config": bench_config(args, wl),
+        "step_us": {"mean": value, "median": step_med, "p10": step_p10, "p90": step_p90, "calls": n_pc,
+                    "note": "mean over the K bulk-timed steps (value); median and spread from a second run of "
+                            f"{n_pc} steps with an event around each (which ends the programmatic overlap "
+                            "between consecutive steps)"},
         "tokens_per_s": world * Bsz / (ms_per_step * 1e-3),
         "decode_us": int2_us, "bf16_history_decode_us": bf16_us, "speedup_vs_bf16": bf16_us / int2_us,
+        "decode_us_percentiles": {"int2": [int2_p10, int2_med, int2_p90], "bf16_history": [bf16_p10, bf16_med, bf16_p90],
+                                  "calls": nd, "order": "p10, median, p90"},
+        "decode_variants_us": dict(variants, tensor_pairs_default=int2_us,
+                                   note="oscar_decode on the same caches and q with OSCAR_OPT_DECODE_IMPL set to each "
+                                        "INT2 kernel (mean per call)"),
         "bf16_history_hbm_gbs": bf16_bytes / (bf16_us * 1e-6) / 1e9,
         "kernels_us": {k: round(v["avg_us"], 3) for k, v in prof.items()},
         "demotion": {"us_per_call": app_us, "bytes_per_call": app_bytes,
@@ -1046,13 +1113,15 @@ def run_ours(args, wl):
                         "note": "offline; fp32 CUDA-core kernels + cuSOLVER dsyevd; wall time of the synchronous calls"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(), "kernel": "decode_main",
-                     "bytes_per_launch": bytes_main, "peak_kind": peak_kind},
+                     "bytes_per_launch": bytes_main, "peak_kind": peak_kind, "kernel_us": main_us,
+                     "vs_bf16_history": vs_bf16},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "form": "pinned host record read and output written in place by the kernels over NVLink-C2C",
                 "with_copy_calls_us": e2e_copy_us, "outputs_finite": e2e_ok},
         "gpu_launches": n_launch,
         "clocks": clocks,
+        "vs_bf16_history": vs_bf16,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

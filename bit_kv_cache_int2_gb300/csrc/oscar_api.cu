@@ -68,6 +68,7 @@ struct oscar_ctx {
   int ctas_per_sm = 4;
   int items_per_cta = 0;  // 0: automatic (make_sched)
   int prefill_impl = OSCAR_PREFILL_TCGEN05;
+  int wait_polls = WAIT_POLLS;
   Profiler prof;
 };
 
@@ -331,6 +332,7 @@ oscar_status decode_args(oscar_ctx* ctx, int layer, const oscar_cache* cache, co
   a.bf16_history = bf16_history ? 1 : 0;
   a.rot = layer_rot(ctx, layer);
   // heads per merge CTA: halve while the merge would not cover the SMs
+  a.wait_polls = ctx->wait_polls;
   a.merge_hpc = ctx->G;
   while (a.merge_hpc % 2 == 0 && batch * ctx->cfg.num_kv_heads * (ctx->G / a.merge_hpc) < ctx->num_sms)
     a.merge_hpc /= 2;
@@ -533,6 +535,10 @@ oscar_status oscar_set_option(oscar_ctx* ctx, int option, int value) {
     case OSCAR_OPT_PREFILL_IMPL:
       if (value != OSCAR_PREFILL_TCGEN05 && value != OSCAR_PREFILL_MMA_SYNC) return OSCAR_ERR_INVALID_ARG;
       ctx->prefill_impl = value;
+      return OSCAR_OK;
+    case OSCAR_OPT_WAIT_POLLS:
+      if (value < 0) return OSCAR_ERR_INVALID_ARG;
+      ctx->wait_polls = value;
       return OSCAR_OK;
     default:
       return OSCAR_ERR_INVALID_ARG;

@@ -999,7 +999,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
             const bool hasB = k + 1 < nw_pages;
             const int sa = (int)((seq + k) % DEPTH), sb = (int)((seq + k + 1) % DEPTH);
             bool ok = mbar_wait2(&my_bar[sa], ((seq + k) / DEPTH) & 1u, &my_bar[hasB ? sb : sa],
-                                 (hasB ? (seq + k + 1) / DEPTH : (seq + k) / DEPTH) & 1u);
+                                 (hasB ? (seq + k + 1) / DEPTH : (seq + k) / DEPTH) & 1u, a.wait_polls);
             if (!__all_sync(0xffffffffu, ok)) {
               timed_out = true;
               k_fail = k;
@@ -1033,7 +1033,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
           for (int k = 0; k < nw_pages; ++k) {
             const int st = (int)((seq + k) % DEPTH);
             const uint32_t ph = ((seq + k) / DEPTH) & 1u;
-            if (!__all_sync(0xffffffffu, mbar_wait(&my_bar[st], ph))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&my_bar[st], ph, a.wait_polls))) {
               timed_out = true;
               k_fail = k;
               break;
@@ -1135,7 +1135,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
         for (int k = 0; k < nw_pages; ++k) {
           const int st = (int)((seq + k) % DEPTH);
           const uint32_t ph = ((seq + k) / DEPTH) & 1u;
-          if (!__all_sync(0xffffffffu, mbar_wait(&my_bar[st], ph))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&my_bar[st], ph, a.wait_polls))) {
             timed_out = true;
             k_fail = k;
             break;

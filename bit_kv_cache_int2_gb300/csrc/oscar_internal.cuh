@@ -353,14 +353,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
+constexpr int WAIT_POLLS = 1 << 22;  // iteration budget of a bounded wait
+
 // Both phases complete (the two polls are issued together); false when the
-// wait ran out of its iteration budget.
+// wait ran out of its iteration budget (`polls` polls; 0 gives up at once).
 __device__ __forceinline__ bool mbar_wait2(uint64_t* bar0, uint32_t phase0, uint64_t* bar1,
-                                           uint32_t phase1) {
+                                           uint32_t phase1, int polls = WAIT_POLLS) {
   const uint32_t a0 = (uint32_t)__cvta_generic_to_shared(bar0);
   const uint32_t a1 = (uint32_t)__cvta_generic_to_shared(bar1);
   uint32_t done0 = 0, done1 = 0;
-  for (int it = 0; it < (1 << 22); ++it) {
+  for (int it = 0; it < polls; ++it) {
     uint32_t ok0 = 1, ok1 = 1;
     if (!done0)
       asm volatile(
@@ -383,10 +385,11 @@ __device__ __forceinline__ bool mbar_wait2(uint64_t* bar0, uint32_t phase0, uint
   return false;
 }
 
-// Returns false when the wait ran out of its iteration budget.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase) {
+// Returns false when the wait ran out of its iteration budget (`polls` polls;
+// 0 gives up at once).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase, int polls = WAIT_POLLS) {
   uint32_t a = (uint32_t)__cvta_generic_to_shared(bar);
-  for (int it = 0; it < (1 << 22); ++it) {
+  for (int it = 0; it < polls; ++it) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -620,6 +623,7 @@ struct DecodeArgs {
              // 6 ring kernel with one page per unit
   int bf16_history;
   int merge_hpc;  // query heads per merge CTA (divides G)
+  int wait_polls; // budget of each page's first wait in decode_kernel (OSCAR_OPT_WAIT_POLLS)
   int balanced;   // 1: the tensor-memory kernel's balanced partition (decode grid in bal_grid)
   int bal_grid;
   int bal_wch;

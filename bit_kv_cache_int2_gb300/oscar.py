@@ -48,6 +48,8 @@ OPT_ITEMS_PER_CTA = 2
 OPT_PREFILL_IMPL = 3
 PREFILL_TCGEN05 = 0  # tcgen05.mma, S/P/O in tensor memory
 PREFILL_MMA_SYNC = 1  # mma.sync
+OPT_WAIT_POLLS = 4  # poll budget of each history page's first wait in the decode kernel
+WAIT_POLLS_DEFAULT = 1 << 22
 
 
 class OscarError(RuntimeError):

@@ -135,7 +135,13 @@ typedef enum {
   OSCAR_OPT_ITEMS_PER_CTA = 2, /* work items per decode CTA the scheduler aims for, 1..8, or 0
                                   (default): automatic -- one item per CTA while items stay small,
                                   else up to 4 per CTA of at least 28 pages, balanced at run time */
-  OSCAR_OPT_PREFILL_IMPL = 3 /* an oscar_prefill_impl value (default OSCAR_PREFILL_TCGEN05) */
+  OSCAR_OPT_PREFILL_IMPL = 3, /* an oscar_prefill_impl value (default OSCAR_PREFILL_TCGEN05) */
+  OSCAR_OPT_WAIT_POLLS = 4     /* iteration budget of the first wait for each history page of the
+                                  mma.sync and CUDA-core decode kernels (default 4194304 polls).
+                                  A wait that runs out records OSCAR_ERR_TIMEOUT; the kernel then
+                                  waits, with the full budget, for the copies it has in flight and
+                                  leaves.  0 makes every such wait give up at once: a way to
+                                  exercise that path.  Values < 0 are OSCAR_ERR_INVALID_ARG. */
 } oscar_option;
 
 typedef struct {

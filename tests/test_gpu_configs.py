@@ -101,25 +101,57 @@ def test_qwen3_32b_131k_b8_int2_and_bf16():
         sb.close()
 
 
-def test_qwen3_8b_stack_g32_two_layers_stepping():
+def _gpu_bases(wl, layer, Hq, Hkv, n=2048, seed=0):
+    """Per-kv-head bases from the library's GPU calibration (as the bench's
+    36-layer stack gets them) on the seeded calibration sets GS.build uses."""
+    G = Hq // Hkv
+    cfg = oscar.make_config(1, Hq, Hkv, 32, max_batch=1, max_pages_per_req=1, num_pages=1)
+    ctx = oscar.oscar_create(cfg)
+    try:
+        scr = oscar.calibration_scratch(G, n, 0)
+        UK, UV = [], []
+        for h in range(Hkv):
+            st = synth.head_stats(seed, wl, 0, h)
+            Qc, Kc, Vc = (t.cuda().contiguous() for t in synth.calibration_set(seed, wl, 0, h, st, G=G, n=n))
+            uk, uv, _, _ = oscar.oscar_calibrate(ctx, Qc, Kc, Vc, n, scr)
+            UK.append(uk)
+            UV.append(uv)
+        return np.stack(UK), np.stack(UV)
+    finally:
+        oscar.oscar_destroy(ctx)
+
+
+@pytest.mark.parametrize("layer", [0, 1])
+def test_qwen3_8b_stack_g32_two_layers_stepping(layer):
     """Two layers of the 36-layer g32 stack (batch 16, 65,536 tokens, own
-    rotations per layer): 8 steps of append + decode per layer; the last
-    step's outputs and every demoted token checked on sampled requests."""
+    GPU-calibrated rotations per layer): 64 decode steps (oscar_decode_step,
+    each appending one token per request and demoting one), as the bench's
+    stack runs them.  Requests 2 and 13 are checked against the oracle after
+    steps 0, 31 and 63, and every token request 2 demoted on kv head 6 is
+    checked against the oracle's quantisation of it."""
     lengths = [65536] * 16
-    steps = 8
-    for layer in range(2):
-        sc = GS.build(f"stack{layer}", lengths, Hq=32, Hkv=8, g=32, extra_tokens=steps, calib_n=1024)
-        try:
-            for t in range(steps):
-                _append_one(sc, [L + t for L in lengths])
-                q = GS.queries(sc, seed=100 + t)
-                out, lse = GS.decode(sc, q)
-            assert oscar.oscar_get_error(sc.ctx) == 0
-            hc = _check_requests(sc, q, out, lse, [2, 13])
-            H = int(hc.hist[2])
-            assert H == 65536 + steps - 320
-            slots = list(range(H - steps, H))
-            n, bad = GS.compare_history(sc, hc, 2, 6, [64 + s for s in slots], slots)
-            assert bad <= 1e-4 * n or bad == 0
-        finally:
-            sc.close()
+    steps = 64
+    wl = f"stack{layer}"
+    U = _gpu_bases(wl, layer, 32, 8)
+    sc = GS.build(wl, lengths, Hq=32, Hkv=8, g=32, extra_tokens=steps, U=U)
+    try:
+        scratch = oscar.alloc_scratch(sc.cfg)
+        for t in range(steps):
+            k = torch.stack([sc.K[b][:, L + t] for b, L in enumerate(lengths)]).contiguous()
+            v = torch.stack([sc.V[b][:, L + t] for b, L in enumerate(lengths)]).contiguous()
+            q = GS.queries(sc, seed=100 + t)
+            out = torch.empty_like(q)
+            lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+            oscar.oscar_decode_step(sc.ctx, 0, sc.cache, k, v, q, out, lse, scratch, len(lengths))
+            if t in (0, 31, 63):
+                torch.cuda.synchronize()
+                assert oscar.oscar_get_error(sc.ctx) == 0, t
+                _check_requests(sc, q, out, lse, [2, 13])
+        hc = GS.HostCache(sc)
+        H = int(hc.hist[2])
+        assert H == 65536 + steps - 320
+        slots = list(range(H - steps, H))
+        n, bad = GS.compare_history(sc, hc, 2, 6, [64 + s for s in slots], slots)
+        assert bad <= 1e-4 * n or bad == 0
+    finally:
+        sc.close()

@@ -398,3 +398,30 @@ def test_import_into_nonempty_request_is_a_state_error():
         assert int(sc.cache["seq_lens"][0]) == 400
     finally:
         sc.close()
+
+
+def test_wait_timeout_is_reported_and_recoverable():
+    """A page wait that runs out of its budget (OSCAR_OPT_WAIT_POLLS = 0: every
+    first wait gives up at once) is reported as OSCAR_ERR_TIMEOUT by each
+    decode kernel; the kernel drains its copies and returns, and with the
+    default budget the next decode matches the oracle."""
+    sc = GS.build("tmo", [5000, 1000], Hq=8, Hkv=2, g=128, calib_n=512)
+    try:
+        q = GS.queries(sc, seed=9)
+        oscar.oscar_set_option(sc.ctx, oscar.OPT_WAIT_POLLS, 0)
+        for impl in (oscar.DECODE_TENSOR, oscar.DECODE_TENSOR_SINGLE, oscar.DECODE_CUDA_CORE):
+            GS.decode(sc, q, impl)
+            assert oscar.oscar_get_error(sc.ctx) == oscar.ERR_TIMEOUT, impl
+        with pytest.raises(oscar.OscarError):
+            oscar.oscar_set_option(sc.ctx, oscar.OPT_WAIT_POLLS, -1)
+        oscar.oscar_set_option(sc.ctx, oscar.OPT_WAIT_POLLS, oscar.WAIT_POLLS_DEFAULT)
+        out, lse = GS.decode(sc, q, oscar.DECODE_TENSOR)
+        assert oscar.oscar_get_error(sc.ctx) == 0
+        hc = GS.HostCache(sc)
+        qn = q.float().cpu().numpy()
+        for b in range(2):
+            ref, rlse = GS.oracle_decode(sc, hc, qn, b)
+            assert _rel(out[b].float().cpu().numpy(), ref) <= REL_TOL
+            assert np.abs(lse[b].cpu().numpy() - rlse).max() <= LSE_TOL
+    finally:
+        sc.close()
