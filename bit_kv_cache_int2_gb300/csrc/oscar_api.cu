@@ -323,6 +323,8 @@ oscar_status decode_args(oscar_ctx* ctx, int layer, const oscar_cache* cache, co
   uint8_t* sp = (uint8_t*)scratch;
   a.counter = (int*)(sp + sl.off_counter);
   a.done = (int*)(sp + sl.off_done);
+  a.pred = (int32_t*)(sp + sl.off_pred);
+  a.step_pred = 0;
   a.qrot = (float*)(sp + sl.off_qrot);
   a.qpack = sp + sl.off_qpack;
   a.part = (float*)(sp + sl.off_part);
@@ -662,6 +664,8 @@ oscar_status oscar_decode_step(oscar_ctx* ctx, int layer, const oscar_cache* cac
       decode_args(ctx, layer, cache, q, out, lse, scratch, scratch_bytes, batch, false, a, grid);
   if (s == OSCAR_ERR_STATE) return OSCAR_OK;  // batch == 0: nothing to do
   if (s != OSCAR_OK) return s;
+  // the mma.sync decode kernels start on the step kernel's predicted lengths
+  a.step_pred = a.impl == 5 ? 0 : 1;
   const cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = launch_step(a.cv, a.rot, (const __nv_bfloat16*)k_new, (const __nv_bfloat16*)v_new, batch,
                               ctx->d_req_counter, a, st, &ctx->prof);

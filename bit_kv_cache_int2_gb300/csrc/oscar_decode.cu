@@ -518,8 +518,9 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
     wslot = bl.n + a.B * Hkv + WIN_CHUNKS * (b * Hkv + kvh);
   } else {
     const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
-    const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
-    const int pages_b = (cv.hist_lens[b] + PAGE - 1) / PAGE;
+    const int32_t* hl = a.step_pred ? a.pred + a.B : cv.hist_lens;  // as the decode kernel's
+    const Sched sc = make_sched(hl, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
+    const int pages_b = (hl[b] + PAGE - 1) / PAGE;
     nb = (pages_b + sc.S - 1) / sc.S;
     base = pre[b] + kvh * nb;
     wch = sc.wch;
@@ -743,18 +744,26 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
   const int gid = lane >> 2, tq = lane & 3;
   const int G = cv.G, Hkv = cv.Hkv;
 
-  pdl_launch_dependents();  // merge_kernel may be scheduled as CTAs of this grid retire
+  // merge_kernel may be scheduled as CTAs of this grid retire; in a decode
+  // step only after this CTA has waited for the step kernel (the merge reads
+  // the lengths before its own wait)
+  if (!a.step_pred) pdl_launch_dependents();
   if (threadIdx.x < NW * DEPTH) mbar_init(&mbar[threadIdx.x], 1);
   uint8_t* qpk = smem + L.off_qpk;
   if (threadIdx.x == 0) misc[1] = 0;
   fence_proxy_async();
   __syncthreads();
 
-  // history lengths and page tables come from earlier stream work: readable
-  // before the wait on prep_kernel
+  // history lengths and page tables come from earlier stream work (or, in a
+  // decode step, from the step kernel's prediction): readable before the wait
   const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
-  const Sched sc = make_sched(cv.hist_lens, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
+  const int32_t* hl = a.step_pred ? a.pred + a.B : cv.hist_lens;
+  const Sched sc = make_sched(hl, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
   const int total = sc.n_hist + sc.n_win;
+  auto wait_prev = [&]() {  // the wait for the kernel before, once
+    pdl_wait();
+    if (a.step_pred) pdl_launch_dependents();
+  };
   uint32_t seq = 0;  // stages consumed by this warp so far
   bool waited = false;
   int it = blockIdx.x;  // first item static, later ones from the work counter
@@ -777,14 +786,18 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
       wc = idx % sc.wch;
       slot = sc.n_hist + idx;
     } else {
-      hist_item_coords(idx, pre, a.B, Hkv, cv.hist_lens, sc.S, b, kvh, jj);
+      hist_item_coords(idx, pre, a.B, Hkv, hl, sc.S, b, kvh, jj);
       slot = idx;
     }
-    const int hist_b = cv.hist_lens[b];
+    const int hist_b = hl[b];
     const int pages_b = (hist_b + PAGE - 1) / PAGE;
 
     if (is_win || BF16H) {
       // ---------------------------------------------------- BF16 tokens
+      if (a.step_pred && !waited) {  // the step kernel writes the window
+        wait_prev();
+        waited = true;
+      }
       Bf16State S;
 #pragma unroll
       for (int j = 0; j < 8; ++j) S.oacc[j][0] = S.oacc[j][1] = S.oacc[j][2] = S.oacc[j][3] = 0.f;
@@ -907,13 +920,25 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
       // prep_kernel) and the rest once the packed query is in shared memory,
       // so that its load does not queue behind a full wave of page copies
       constexpr int EARLY = (IMPL == 1) ? DEPTH : 2;
+      // in a decode step the page that receives the demoted token is written
+      // by the step kernel: it is copied only after the wait
+      const int late_page = (a.step_pred && !waited && hl[b] > a.pred[2 * a.B + b]) ? a.pred[2 * a.B + b] / PAGE : -1;
+      int deferred = -1;
       for (int k = 0; k < EARLY && k < nw_pages; ++k) {
         const int pid = page_id_at(P, k);
+        if (p0 + warp + k * NW == late_page) {
+          deferred = k;
+          continue;
+        }
         if (lane == 0) issue(k, pid);
       }
       if (!waited) {
-        pdl_wait();  // q' (prep_kernel) is ready from here on
+        wait_prev();  // q' (prep or step kernel) is ready from here on
         waited = true;
+      }
+      if (deferred >= 0) {
+        const int pid = page_id_at(P, deferred);
+        if (lane == 0) issue(deferred, pid);
       }
       bool timed_out = false;
       int k_fail = 0;
@@ -1177,7 +1202,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
     __syncthreads();
     cta_combine_write(a, wm, wl, wo, slot);
     if (!waited) {
-      pdl_wait();
+      wait_prev();
       waited = true;
     }
     if (misc[1]) break;
@@ -1186,7 +1211,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
     __syncthreads();
     it = misc[0];
   }
-  if (!waited) pdl_wait();
+  if (!waited) wait_prev();
 }
 
 // Raise decode_kernel<NG, IMPL>'s dynamic shared-memory limit to `bytes` if it
@@ -1224,7 +1249,8 @@ ScratchLayout scratch_layout(int B, int Hq, int Hkv, int G, int max_target_items
   ScratchLayout s;
   s.off_counter = 0;
   s.off_done = 256;
-  s.off_qrot = s.off_done + up((size_t)B * Hkv * 4);
+  s.off_pred = s.off_done + up((size_t)B * Hkv * 4);
+  s.off_qrot = s.off_pred + up((size_t)3 * B * 4);
   s.off_qpack = s.off_qrot + up((size_t)B * Hq * D * 4);
   s.off_part = s.off_qpack + up((size_t)B * Hq * QPACK_CB_BYTES);  // room for codebook records
   const size_t slots = (size_t)max_target_items + 2 * (size_t)B * Hkv;

@@ -624,6 +624,13 @@ struct DecodeArgs {
   int bf16_history;
   int merge_hpc;  // query heads per merge CTA (divides G)
   int wait_polls; // budget of each page's first wait in decode_kernel (OSCAR_OPT_WAIT_POLLS)
+  // Decode step (step_kernel then decode_kernel): the step kernel writes the
+  // lengths its append will leave, pred[0..B) seq, pred[B..2B) hist and
+  // pred[2B..3B) the history length before the append, and releases the
+  // decode kernel at once; the decode kernel schedules from them and copies
+  // the page that receives the demoted token only after its wait.
+  int step_pred;
+  int32_t* pred;  // scratch [3][B]
   int balanced;   // 1: the tensor-memory kernel's balanced partition (decode grid in bal_grid)
   int bal_grid;
   int bal_wch;
@@ -760,9 +767,9 @@ int decode_tc_window_weight();
 cudaError_t launch_decode_after_prep(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof);
 int decode_ctas_per_sm(const DecodeArgs& a);  // resident CTAs per SM of the decode kernel (0: error)
 
-// Decode scratch: [work counter][done counters][q' fp32][packed q][partials]
+// Decode scratch: [work counter][done counters][predicted lengths][q' fp32][packed q][partials]
 struct ScratchLayout {
-  size_t off_counter, off_done, off_qrot, off_qpack, off_part, total;
+  size_t off_counter, off_done, off_pred, off_qrot, off_qpack, off_part, total;
 };
 ScratchLayout scratch_layout(int B, int Hq, int Hkv, int G, int max_target_items);
 size_t decode_scratch_bytes(int B, int Hq, int Hkv, int G, int max_target_items);

@@ -58,10 +58,15 @@ __device__ __forceinline__ void quant_store_v_global(float y, int j, int g, floa
 // Hkv + kv head, isv = 0 for K, 1 for V.  The body waits for earlier stream
 // work after issuing its rotation-table loads; with `release` it then lets
 // its dependents launch at once, otherwise the caller releases them later.
+// With `pred` (a decode step) the K CTA of kv head 0 first writes the lengths
+// this append will leave, pred[b] (sequence), pred[B + b] (history) and
+// pred[2B + b] (history before), and every CTA releases its dependents once
+// that is done and fenced.
 __device__ __forceinline__ void append_body(const CacheView& cv, const LayerRot& rot,
                                             const __nv_bfloat16* __restrict__ knew,
                                             const __nv_bfloat16* __restrict__ vnew, int do_append,
-                                            int* req_counter, int bk, int isv, bool release) {
+                                            int* req_counter, int bk, int isv, bool release,
+                                            int32_t* pred = nullptr, int B = 0) {
   __shared__ float xs[D];
   __shared__ float part[4][D];
   __shared__ float red[8];
@@ -79,7 +84,7 @@ __device__ __forceinline__ void append_body(const CacheView& cv, const LayerRot&
   // the new tokens, the lengths and the cache belong to earlier stream work;
   // the decode's prep_kernel waits for this grid before it reads anything
   pdl_wait();
-  if (release) pdl_launch_dependents();
+  if (release && !pred) pdl_launch_dependents();
   if (t == 0) {
     const int L = cv.seq_lens[b], H = cv.hist_lens[b];
     const int recent = L > SINK ? L - SINK - H : 0;
@@ -108,9 +113,17 @@ __device__ __forceinline__ void append_body(const CacheView& cv, const LayerRot&
     st[2] = ok && demote;
     st[3] = page;
     st[4] = ok;
+    if (pred && h == 0 && !isv) {
+      // the lengths the last CTA of the request writes below
+      pred[b] = ok ? L + do_append : L;
+      pred[B + b] = ok ? H + (demote ? 1 : 0) : H;
+      pred[2 * B + b] = H;
+      __threadfence();
+    }
   }
   if (t < 8) kw[t] = 0u;
   __syncthreads();
+  if (release && pred) pdl_launch_dependents();
   const int L = st[0], H = st[1], demote = st[2], page = st[3], ok = st[4];
   const size_t head = (size_t)(b * cv.Hkv + h);
   __nv_bfloat16* ring = isv ? cv.ring_v : cv.ring_k;
@@ -182,23 +195,31 @@ __global__ void __launch_bounds__(512) append_kernel(CacheView cv, LayerRot rot,
 // append K / V of (request, kv head) x (as append_kernel), y = 2 computes the
 // packed query of x, its four 128-thread parts taking one channel quarter
 // each (as prep_kernel).  The query rotation does not depend on the append,
-// so the two run side by side.  Each CTA releases the decode kernel only once
-// its own writes are done and fenced: the decode kernel reads the cache state
-// (lengths, pages) before it waits for this grid.
+// so the two run side by side.
+// With a.step_pred (the mma.sync decode kernels) every CTA releases the
+// decode kernel right after its wait, the K CTAs of kv head 0 once they have
+// published the lengths the append will leave; the decode kernel schedules
+// from those, copies the history pages the append does not write, and waits
+// for this grid before it reads anything else.  Otherwise (the tensor-memory
+// kernel reads the cache state before its wait) each CTA releases only once
+// its own writes are done and fenced.
 __global__ void __launch_bounds__(512) step_kernel(CacheView cv, LayerRot rot,
                                                    const __nv_bfloat16* __restrict__ knew,
                                                    const __nv_bfloat16* __restrict__ vnew,
                                                    int* req_counter, DecodeArgs a) {
   __shared__ PrepSmem psm[4];
   const int bk = blockIdx.x;
+  const bool early = a.step_pred != 0;
   if (blockIdx.y < 2) {
-    append_body(cv, rot, knew, vnew, 1, req_counter, bk, blockIdx.y, false);
+    append_body(cv, rot, knew, vnew, 1, req_counter, bk, blockIdx.y, early, early ? a.pred : nullptr, a.B);
   } else {
-    prep_body(a, bk, threadIdx.x >> 7, threadIdx.x & 127, psm[threadIdx.x >> 7], false);
+    prep_body(a, bk, threadIdx.x >> 7, threadIdx.x & 127, psm[threadIdx.x >> 7], early);
   }
-  __syncthreads();
-  __threadfence();
-  pdl_launch_dependents();
+  if (!early) {
+    __syncthreads();
+    __threadfence();
+    pdl_launch_dependents();
+  }
 }
 
 // ------------------------------------------------------------------ import
