@@ -322,7 +322,6 @@ oscar_status decode_args(oscar_ctx* ctx, int layer, const oscar_cache* cache, co
       scratch_layout(batch, ctx->cfg.num_q_heads, ctx->cfg.num_kv_heads, ctx->G, target);
   uint8_t* sp = (uint8_t*)scratch;
   a.counter = (int*)(sp + sl.off_counter);
-  a.done = (int*)(sp + sl.off_done);
   a.pred = (int32_t*)(sp + sl.off_pred);
   a.step_pred = 0;
   a.qrot = (float*)(sp + sl.off_qrot);

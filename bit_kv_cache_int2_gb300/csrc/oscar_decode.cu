@@ -1248,8 +1248,7 @@ ScratchLayout scratch_layout(int B, int Hq, int Hkv, int G, int max_target_items
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   ScratchLayout s;
   s.off_counter = 0;
-  s.off_done = 256;
-  s.off_pred = s.off_done + up((size_t)B * Hkv * 4);
+  s.off_pred = 256;
   s.off_qrot = s.off_pred + up((size_t)3 * B * 4);
   s.off_qpack = s.off_qrot + up((size_t)B * Hq * D * 4);
   s.off_part = s.off_qpack + up((size_t)B * Hq * QPACK_CB_BYTES);  // room for codebook records

@@ -614,13 +614,11 @@ struct DecodeArgs {
   uint8_t* qpack;          // scratch [B][Hq] packed query records
   float* part;             // scratch partials
   int* counter;            // scratch work counter
-  int* done;               // scratch [B][Hkv] finished-item counters
   int B;
   int target_items;
   int resident;  // resident decode CTAs for automatic item sizing, 0: fixed items per CTA
-  int impl;  // decode kernel variant: 0 tensor-core one page per warp, 1 CUDA-core, 3 ring kernel with
-             // page pairs, 4 tensor-core with a Lloyd-Max codebook, 5 tcgen05 with tensor memory,
-             // 6 ring kernel with one page per unit
+  int impl;  // decode kernel variant: 0 tensor-core one page per warp, 1 CUDA-core, 3 tensor-core
+             // with page pairs, 4 tensor-core with a Lloyd-Max codebook, 5 tcgen05 with tensor memory
   int bf16_history;
   int merge_hpc;  // query heads per merge CTA (divides G)
   int wait_polls; // budget of each page's first wait in decode_kernel (OSCAR_OPT_WAIT_POLLS)
@@ -685,13 +683,7 @@ __device__ __forceinline__ void prep_body(const DecodeArgs& a, int bk, int cq, i
   }
   pdl_wait();
   if (release) pdl_launch_dependents();
-  if (t == 0 && cq == 0) {
-    a.done[bk] = 0;
-    if (bk == 0) {
-      a.counter[0] = 0;  // history items after the first wave
-      a.counter[1] = 0;  // window chunks of the ring kernel
-    }
-  }
+  if (t == 0 && cq == 0 && bk == 0) a.counter[0] = 0;  // history items after the first wave
   if (a.bf16_history) return;
   const __nv_bfloat16* qg = a.q + ((size_t)b * cv.Hq + kvh * G) * D;
   for (int e = t; e < G * D; e += 128) sm.xs[e / D][e % D] = __bfloat162float(qg[e]);
@@ -767,9 +759,9 @@ int decode_tc_window_weight();
 cudaError_t launch_decode_after_prep(const DecodeArgs& a, int grid, cudaStream_t st, Profiler* prof);
 int decode_ctas_per_sm(const DecodeArgs& a);  // resident CTAs per SM of the decode kernel (0: error)
 
-// Decode scratch: [work counter][done counters][predicted lengths][q' fp32][packed q][partials]
+// Decode scratch: [work counter][predicted lengths][q' fp32][packed q][partials]
 struct ScratchLayout {
-  size_t off_counter, off_done, off_pred, off_qrot, off_qpack, off_part, total;
+  size_t off_counter, off_pred, off_qrot, off_qpack, off_part, total;
 };
 ScratchLayout scratch_layout(int B, int Hq, int Hkv, int G, int max_target_items);
 size_t decode_scratch_bytes(int B, int Hq, int Hkv, int G, int max_target_items);
