@@ -1200,6 +1200,9 @@ def run_leg(args, wl):
         oscar.oscar_set_option(ctx, oscar.OPT_DECODE_IMPL, 2)
     if args.leg == "tcgen05":
         oscar.oscar_set_option(ctx, oscar.OPT_DECODE_IMPL, 3)
+    part = {"auto": oscar.PARTITION_AUTO, "items": oscar.PARTITION_ITEMS,
+            "balanced": oscar.PARTITION_BALANCED}[args.partition]
+    oscar.oscar_set_option(ctx, oscar.OPT_DECODE_PARTITION, part)
     tok_bytes = Bsz * Hkv * 128 * 2
     kv_new = (wk["K"][:, :, L0:L0 + extra].permute(2, 0, 1, 3).contiguous(),
               wk["V"][:, :, L0:L0 + extra].permute(2, 0, 1, 3).contiguous())
@@ -1244,7 +1247,8 @@ def run_leg(args, wl):
     mean_us = e0.elapsed_time(e1) * 1e3 / args.steps
     err = oscar.oscar_get_error(wk["bctx"] if bf16 else ctx)
     assert err == 0, f"device error {err}"
-    line = {"leg": args.leg, "workload": args.workload, "context": L0, "calls": args.steps, "mean_us": mean_us,
+    line = {"leg": args.leg, "workload": args.workload, "context": L0, "partition": args.partition,
+            "calls": args.steps, "mean_us": mean_us,
             "cache_copies": n_copies}
     if not appends:  # a second pass, timed call by call
         med, p10, p90 = percentiles(per_call_times(lambda i: fn(args.warmup + i), args.steps, stream))
@@ -1325,6 +1329,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--context", type=int, default=0,
                     help="single-operation legs: context length instead of the workload's (0: the workload's)")
+    ap.add_argument("--partition", choices=["auto", "items", "balanced"], default="auto",
+                    help="single-operation legs: the decode kernels' work partition (OSCAR_OPT_DECODE_PARTITION)")
     ap.add_argument("--leg", choices=["all", "codebook"] + list(LEGS), default="all",
                     help="one operation alone on the workload, a short command to profile it (see run_leg); "
                          "codebook: only the Lloyd-Max codebook decode")

@@ -69,6 +69,7 @@ struct oscar_ctx {
   int items_per_cta = 0;  // 0: automatic (make_sched)
   int prefill_impl = OSCAR_PREFILL_TCGEN05;
   int wait_polls = WAIT_POLLS;
+  int partition = 0;  // OSCAR_OPT_DECODE_PARTITION
   Profiler prof;
 };
 
@@ -136,15 +137,33 @@ int decode_ctas(const oscar_ctx* ctx, int batch, bool bf16_history, int layer = 
   return ctx->ctas_per_sm < occ ? ctx->ctas_per_sm : occ;
 }
 
-int target_items(const oscar_ctx* ctx, int batch, bool bf16_history, int layer = -1) {
-  // the tensor-memory kernel: one history record per (CTA, segment) pair and
-  // five window records per segment, i.e. num_sms + 6 B Hkv partial records
-  // (the scratch layout adds 2 B Hkv to the target)
-  if (!bf16_history && kernel_impl(ctx, layer) == 5) return ctx->num_sms + 4 * batch * ctx->cfg.num_kv_heads;
+// decode_kernel's work partition (DecodeArgs::balanced): 0 the item list, 1
+// balanced, 2 decided on the device (balanced once the item list would give
+// a CTA more than a wave's worth of pages).
+int decode_partition(const oscar_ctx* ctx) {
+  return ctx->partition == 1 ? 0 : ctx->partition == 2 ? 1 : 2;
+}
+
+// The item list's size bound (make_sched's target).
+int list_items(const oscar_ctx* ctx, int batch, bool bf16_history, int layer = -1) {
   const int per = ctx->items_per_cta ? ctx->items_per_cta : AUTO_ITEMS_PER_CTA;
   int t = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, layer) * per;
   if (t > MAX_TARGET_ITEMS) t = MAX_TARGET_ITEMS;
   if (t < 1) t = 1;
+  return t;
+}
+
+// Partial records the decode may write, less the 2 B Hkv the scratch layout
+// adds.  A balanced partition (the tensor-memory kernel's always) writes one
+// history record per (CTA, segment) pair and five window records per
+// segment: CTAs + 6 B Hkv.
+int target_items(const oscar_ctx* ctx, int batch, bool bf16_history, int layer = -1) {
+  if (!bf16_history && kernel_impl(ctx, layer) == 5) return ctx->num_sms + 4 * batch * ctx->cfg.num_kv_heads;
+  const int t = list_items(ctx, batch, bf16_history, layer);
+  const int tb = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, layer) + 4 * batch * ctx->cfg.num_kv_heads;
+  const int part = decode_partition(ctx);
+  if (part == 1) return tb;
+  if (part == 2 && tb > t) return tb;
   return t;
 }
 
@@ -328,7 +347,7 @@ oscar_status decode_args(oscar_ctx* ctx, int layer, const oscar_cache* cache, co
   a.qpack = sp + sl.off_qpack;
   a.part = (float*)(sp + sl.off_part);
   a.B = batch;
-  a.target_items = target;
+  a.target_items = list_items(ctx, batch, bf16_history, vlayer);  // make_sched's bound
   a.impl = bf16_history ? 0 : kernel_impl(ctx, vlayer);
   a.bf16_history = bf16_history ? 1 : 0;
   a.rot = layer_rot(ctx, layer);
@@ -352,6 +371,9 @@ oscar_status decode_args(oscar_ctx* ctx, int layer, const oscar_cache* cache, co
   }
   grid = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, vlayer);
   a.resident = ctx->items_per_cta == 0 ? grid : 0;
+  a.balanced = decode_partition(ctx);
+  a.bal_grid = grid;
+  a.bal_wch = DEC_WIN_WEIGHT;
   return OSCAR_OK;
 }
 
@@ -540,6 +562,10 @@ oscar_status oscar_set_option(oscar_ctx* ctx, int option, int value) {
     case OSCAR_OPT_WAIT_POLLS:
       if (value < 0) return OSCAR_ERR_INVALID_ARG;
       ctx->wait_polls = value;
+      return OSCAR_OK;
+    case OSCAR_OPT_DECODE_PARTITION:
+      if (value < 0 || value > 2) return OSCAR_ERR_INVALID_ARG;
+      ctx->partition = value;
       return OSCAR_OK;
     default:
       return OSCAR_ERR_INVALID_ARG;

@@ -47,8 +47,210 @@ __global__ void __launch_bounds__(128) prep_kernel(DecodeArgs a) {
 // ------------------------------------------------------------ smem layout
 struct SmemLayout {
   int stage_bytes;   // per stage
-  int off_stage, off_mbar, off_qpk, off_qf, off_vs, off_pre, off_red, off_misc, total;
+  int off_stage, off_mbar, off_qpk, off_qf, off_vs, off_pre, off_red, off_misc, off_cursor, total;
 };
+
+// decode_kernel's position in its work list (shared memory, thread 0) and
+// the item it hands to the block.
+struct DecodeCursor {
+  long long lo, hi;        // balanced: this CTA's range of positions
+  int bal;                 // 1: balanced partition, 0: item list
+  int cb, ck, cc, phase;   // balanced: request, kv head, next window chunk, 0 windows / 1 history
+  int bl_n, bl_wch;        // balanced: CTAs taking part, window chunk weight
+  int it, first;           // item list: next index, the static first item still to take
+  int total, S, n_hist, n_win, lwch, win_first;  // item list: make_sched's list
+  int found, is_win, b, kvh, wc, wch, p0, p1, slot;  // the item
+};
+
+// The automatic partition: balanced once the item list would give a CTA more
+// than AUTO_WAVE_PAGES pages (several items per CTA, each paying a start).
+__device__ __forceinline__ bool use_balanced(const Sched& sc, int grid) {
+  return sc.pages > (long long)AUTO_WAVE_PAGES * grid;
+}
+
+__device__ inline void cursor_init_items(DecodeCursor& c, const Sched& sc, int cta) {
+  c.bal = 0;
+  c.first = 1;
+  c.it = cta;
+  c.total = sc.n_hist + sc.n_win;
+  c.S = sc.S;
+  c.n_hist = sc.n_hist;
+  c.n_win = sc.n_win;
+  c.lwch = sc.wch;
+  c.win_first = sc.win_first ? 1 : 0;
+}
+
+// Weight of (b, kvh) in the balanced list: history pages plus wch per
+// non-empty window chunk.
+__device__ __forceinline__ long long balanced_weight(const int32_t* hl, const int32_t* sl, int b, int wch,
+                                                     int* P, unsigned* mask) {
+  const int H = hl[b];
+  *P = H > 0 ? (H + PAGE - 1) / PAGE : 0;
+  *mask = window_chunk_mask(sl[b], H);
+  return *P + (long long)wch * __popc(*mask);
+}
+
+// Puts the cursor on the segment holding the range's first position.
+__device__ inline void cursor_restart(DecodeCursor& c, const long long* pre64, int B, const int32_t* hl,
+                                      const int32_t* sl) {
+  c.cb = c.lo < c.hi ? balanced_request(pre64, B, c.lo) : B;
+  c.ck = 0;
+  c.cc = 0;
+  if (c.cb < B) {
+    int P;
+    unsigned mask;
+    const long long wb = balanced_weight(hl, sl, c.cb, c.bl_wch, &P, &mask);
+    if (wb > 0 && c.lo > pre64[c.cb]) c.ck = (int)((c.lo - pre64[c.cb]) / wb);
+  }
+}
+
+__device__ inline void cursor_init_balanced(DecodeCursor& c, const Balanced& bl, const long long* pre64, int B,
+                                            int Hkv, const int32_t* hl, const int32_t* sl, int cta) {
+  (void)Hkv;
+  c.bal = 1;
+  c.bl_n = bl.n;
+  c.bl_wch = bl.wch;
+  c.lo = cta < bl.n ? balanced_lo(bl, cta) : 0;
+  c.hi = cta < bl.n ? balanced_lo(bl, cta + 1) : 0;
+  c.phase = 0;
+  cursor_restart(c, pre64, B, hl, sl);
+}
+
+// L2 prefetch of the BF16 window chunks whose positions lie in the cursor's
+// range (all threads; the cursor as cursor_init_balanced left it).
+__device__ inline void prefetch_range_windows(const DecodeCursor& c0, const CacheView& cv, int B,
+                                              const long long* pre64, const int32_t* hl, const int32_t* sl) {
+  const int Hkv = cv.Hkv;
+  if (c0.lo >= c0.hi) return;
+  int cb = c0.cb, ck = c0.ck;
+  for (int guard = 0; guard < 64 && cb < B && pre64[cb] < c0.hi; ++guard) {
+    int P;
+    unsigned mask;
+    const long long wb = balanced_weight(hl, sl, cb, c0.bl_wch, &P, &mask);
+    if (wb == 0 || ck >= Hkv) {
+      ++cb;
+      ck = 0;
+      continue;
+    }
+    const long long seg = pre64[cb] + (long long)ck * wb;
+    if (seg >= c0.hi) break;
+    const size_t head = (size_t)cb * Hkv + ck;
+    for (int ch = 0; ch < WIN_CHUNKS; ++ch) {
+      if (!((mask >> ch) & 1u)) continue;
+      const long long x = seg + P + (long long)c0.bl_wch * __popc(mask & ((1u << ch) - 1u));
+      if (x < c0.lo || x >= c0.hi) continue;
+      // 64 tokens x 256 bytes of K and of V: 128 lines each
+      const char* kb = (const char*)(ch == 0 ? cv.sink_k + head * SINK * D : cv.ring_k + (head * RECENT + 64 * (ch - 1)) * D);
+      const char* vb = (const char*)(ch == 0 ? cv.sink_v + head * SINK * D : cv.ring_v + (head * RECENT + 64 * (ch - 1)) * D);
+      for (int l = threadIdx.x; l < 128; l += blockDim.x) {
+        asm volatile("prefetch.global.L2 [%0];\n" ::"l"(kb + 128 * l));
+        asm volatile("prefetch.global.L2 [%0];\n" ::"l"(vb + 128 * l));
+      }
+    }
+    ++ck;
+  }
+}
+
+// The next item into c.found / c.is_win / ... (thread 0).
+__device__ inline void cursor_next(DecodeCursor& c, const DecodeArgs& a, const long long* pre64, const int* pre,
+                                   const int32_t* hl, const int32_t* sl) {
+  const int B = a.B, Hkv = a.cv.Hkv;
+  c.found = 0;
+  c.is_win = 0;
+  c.wc = 0;
+  c.p0 = c.p1 = 0;
+  if (!c.bal) {
+    int it;
+    if (c.first) {
+      it = c.it;
+      c.first = 0;
+    } else {
+      it = (int)gridDim.x + atomicAdd(a.counter, 1);
+    }
+    if (it >= c.total) return;
+    int idx;
+    bool is_win;
+    if (c.win_first) {
+      is_win = it < c.n_win;
+      idx = is_win ? it : it - c.n_win;
+    } else {
+      is_win = it >= c.n_hist;
+      idx = is_win ? it - c.n_hist : it;
+    }
+    c.found = 1;
+    c.is_win = is_win ? 1 : 0;
+    c.wch = c.lwch;
+    if (is_win) {
+      c.b = idx / (Hkv * c.lwch);
+      c.kvh = (idx / c.lwch) % Hkv;
+      c.wc = idx % c.lwch;
+      c.slot = c.n_hist + idx;
+    } else {
+      int b, kvh, jj;
+      hist_item_coords(idx, pre, B, Hkv, hl, c.S, b, kvh, jj);
+      c.b = b;
+      c.kvh = kvh;
+      c.p0 = jj * c.S;
+      c.p1 = c.p0 + c.S;
+      c.slot = idx;
+    }
+    return;
+  }
+  for (;;) {
+    if (c.cb >= B || pre64[c.cb] >= c.hi) {
+      if (c.phase == 1) return;
+      c.phase = 1;
+      cursor_restart(c, pre64, B, hl, sl);
+      continue;
+    }
+    int P;
+    unsigned mask;
+    const long long wb = balanced_weight(hl, sl, c.cb, c.bl_wch, &P, &mask);
+    if (wb == 0 || c.ck >= Hkv) {
+      ++c.cb;
+      c.ck = 0;
+      c.cc = 0;
+      continue;
+    }
+    const long long seg = pre64[c.cb] + (long long)c.ck * wb;
+    if (seg >= c.hi) {
+      c.cb = B;
+      continue;
+    }
+    if (c.phase == 0) {
+      while (c.cc < WIN_CHUNKS) {
+        const int ch = c.cc++;
+        if (!((mask >> ch) & 1u)) continue;
+        const long long x = seg + P + (long long)c.bl_wch * __popc(mask & ((1u << ch) - 1u));
+        if (x >= c.lo && x < c.hi) {
+          c.found = 1;
+          c.is_win = 1;
+          c.b = c.cb;
+          c.kvh = c.ck;
+          c.wc = ch;
+          c.wch = WIN_CHUNKS;
+          c.slot = c.bl_n + B * Hkv + WIN_CHUNKS * (c.cb * Hkv + c.ck) + ch;
+          return;
+        }
+      }
+      c.cc = 0;
+      ++c.ck;
+    } else {
+      const long long s0 = c.lo > seg ? c.lo : seg, e0 = c.hi < seg + P ? c.hi : seg + P;
+      const int kvh = c.ck++;
+      if (s0 < e0) {
+        c.found = 1;
+        c.b = c.cb;
+        c.kvh = kvh;
+        c.wch = WIN_CHUNKS;
+        c.p0 = (int)(s0 - seg);
+        c.p1 = (int)(e0 - seg);
+        c.slot = (int)blockIdx.x + c.cb * Hkv + kvh;
+        return;
+      }
+    }
+  }
+}
 
 // impl: 0 tensor-core INT2, 1 CUDA-core INT2, 2 BF16 history (no INT2 pages),
 // 3 tensor-core page pairs, 4 tensor-core with a Lloyd-Max codebook
@@ -74,11 +276,13 @@ __host__ __device__ inline SmemLayout smem_layout(int head_bytes, int B, int imp
   L.off_vs = o;
   if (impl == 1) o += NW * (MAX_G * PAGE + 2 * 4 * PAGE) * 4;  // CUDA-core per-warp p and s/z
   L.off_pre = o;
-  o += ((B + 1) * 4 + 15) & ~15;
+  o += ((B + 1) * 8 + 15) & ~15;  // int[B + 1], or long long[B + 1] for the balanced partition
   L.off_red = o;
   o += 2 * NW * 4;  // block reductions of the work-list derivation
   L.off_misc = o;
   o += 16;
+  L.off_cursor = o;
+  o += ((int)sizeof(DecodeCursor) + 15) & ~15;
   L.total = o;
   return L;
 }
@@ -496,14 +700,23 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
   }
   // history lengths come from earlier stream work: the work list can be
   // derived before the wait
+  const int32_t* hl = a.step_pred ? a.pred + a.B : cv.hist_lens;  // as the decode kernel's
+  const int32_t* sl = a.step_pred ? a.pred : cv.seq_lens;
   int nb, base, wslot, wch;
   unsigned wmask;  // window records that exist
-  if (a.balanced) {
-    // the tensor-memory kernel's list: the history records of the CTAs
-    // owning this segment's pages, then one record per non-empty window chunk
-    long long* pre64 = (long long*)(smem + ML.off_pre);
-    const Balanced bl = make_balanced(cv.seq_lens, cv.hist_lens, a.B, Hkv, a.bal_wch, a.bal_grid, pre64);
-    const int H = cv.hist_lens[b], Lq = cv.seq_lens[b];
+  long long* pre64 = (long long*)(smem + ML.off_pre);
+  const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
+  bool bal = a.balanced == 1;
+  Sched sc;
+  if (!bal) {
+    sc = make_sched(hl, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
+    bal = a.balanced == 2 && use_balanced(sc, a.bal_grid);  // as decode_kernel decides
+  }
+  if (bal) {
+    const Balanced bl = make_balanced(sl, hl, a.B, Hkv, a.bal_wch, a.bal_grid, pre64);
+    // the balanced partition's list: the history records of the CTAs owning
+    // this segment's pages, then one record per non-empty window chunk
+    const int H = hl[b], Lq = sl[b];
     const int P = H > 0 ? (H + PAGE - 1) / PAGE : 0;
     wmask = window_chunk_mask(Lq, H);
     const long long seg = pre64[b] + (long long)kvh * (P + bl.wch * __popc(wmask));
@@ -517,9 +730,6 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
     wch = WIN_CHUNKS;
     wslot = bl.n + a.B * Hkv + WIN_CHUNKS * (b * Hkv + kvh);
   } else {
-    const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
-    const int32_t* hl = a.step_pred ? a.pred + a.B : cv.hist_lens;  // as the decode kernel's
-    const Sched sc = make_sched(hl, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
     const int pages_b = (hl[b] + PAGE - 1) / PAGE;
     nb = (pages_b + sc.S - 1) / sc.S;
     base = pre[b] + kvh * nb;
@@ -758,39 +968,58 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
   // decode step, from the step kernel's prediction): readable before the wait
   const int unit = a.bf16_history ? BF16_HEAD_BYTES : cv.head_bytes;
   const int32_t* hl = a.step_pred ? a.pred + a.B : cv.hist_lens;
-  const Sched sc = make_sched(hl, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
-  const int total = sc.n_hist + sc.n_win;
+  const int32_t* sl = a.step_pred ? a.pred : cv.seq_lens;
   auto wait_prev = [&]() {  // the wait for the kernel before, once
     pdl_wait();
     if (a.step_pred) pdl_launch_dependents();
   };
   uint32_t seq = 0;  // stages consumed by this warp so far
   bool waited = false;
-  int it = blockIdx.x;  // first item static, later ones from the work counter
 
-  while (it < total) {
-    bool is_win;
-    int idx;
-    if (sc.win_first) {
-      is_win = it < sc.n_win;
-      idx = is_win ? it : it - sc.n_win;
-    } else {
-      is_win = it >= sc.n_hist;
-      idx = is_win ? it - sc.n_hist : it;
+  // The work list, one item at a time: a window item is chunk wc of (b,
+  // kvh)'s BF16 window (wch == 5: warp w takes its 16 tokens of the chunk;
+  // wch == 1: all five chunks, the warps in turn), a history item pages
+  // [p0, p1) of (b, kvh); each writes partial record slot.  Thread 0 derives
+  // the next item from a cursor kept in shared memory (nothing of it stays
+  // in registers across the page loop) and broadcasts it.
+  //  * item list: make_sched's items, the first one static (blockIdx.x),
+  //    later ones from the work counter;
+  //  * balanced: CTA i takes positions [lo_i, lo_i+1) of the list of all
+  //    (b, kvh) in order, each weighing its history pages plus bal_wch per
+  //    non-empty window chunk; first the window chunks whose position lies
+  //    in the range, then the history pages in it.
+  // a.balanced == 2 picks the balanced partition when the item list would
+  // give a CTA more than one wave's worth of pages (the merge decides alike).
+  DecodeCursor* cur = (DecodeCursor*)(smem + L.off_cursor);
+  {
+    bool bal = a.balanced == 1;
+    if (!bal) {
+      const Sched sc = make_sched(hl, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
+      bal = a.balanced == 2 && use_balanced(sc, gridDim.x);
+      if (!bal && threadIdx.x == 0) cursor_init_items(*cur, sc, blockIdx.x);
     }
-    int b, kvh, jj = 0, slot;
-    int wc = 0;  // window chunk of this item (wch == 5)
-    if (is_win) {
-      b = idx / (Hkv * sc.wch);
-      kvh = (idx / sc.wch) % Hkv;
-      wc = idx % sc.wch;
-      slot = sc.n_hist + idx;
-    } else {
-      hist_item_coords(idx, pre, a.B, Hkv, hl, sc.S, b, kvh, jj);
-      slot = idx;
+    if (bal) {
+      long long* pre64 = (long long*)pre;
+      const Balanced bl = make_balanced(sl, hl, a.B, Hkv, a.bal_wch, gridDim.x, pre64);
+      if (threadIdx.x == 0) cursor_init_balanced(*cur, bl, pre64, a.B, Hkv, hl, sl, blockIdx.x);
+      __syncthreads();
+      // the window chunks of the range are read with plain loads, which queue
+      // behind the whole grid's page copies: ask for all of them at once
+      prefetch_range_windows(*cur, cv, a.B, pre64, hl, sl);
     }
+    __syncthreads();
+  }
+
+  for (;;) {
+    if (threadIdx.x == 0) cursor_next(*cur, a, (long long*)pre, pre, hl, sl);
+    __syncthreads();
+    if (!cur->found) break;
+    const bool is_win = cur->is_win;
+    const int b = cur->b, kvh = cur->kvh, wc = cur->wc, wch = cur->wch, p0 = cur->p0, slot = cur->slot;
+    int p1 = cur->p1;
     const int hist_b = hl[b];
     const int pages_b = (hist_b + PAGE - 1) / PAGE;
+    if (p1 > pages_b) p1 = pages_b;
 
     if (is_win || BF16H) {
       // ---------------------------------------------------- BF16 tokens
@@ -820,8 +1049,8 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
         const int h0 = hist_b % RECENT;
         // wch == 1: warps take the 5 chunks in turn; wch == 5: this item is
         // chunk wc and warp w takes its 16-token tile w
-        const int ch_begin = sc.wch == 1 ? warp : wc;
-        const int ch_step = sc.wch == 1 ? NW : 5;
+        const int ch_begin = wch == 1 ? warp : wc;
+        const int ch_step = wch == 1 ? NW : 5;
         for (int ch = ch_begin; ch < 5; ch += ch_step) {
           uint64_t valid = 0;
           const __nv_bfloat16 *Kb, *Vb;
@@ -842,16 +1071,13 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
             Kb = cv.ring_k + (head * RECENT + s0) * D;
             Vb = cv.ring_v + (head * RECENT + s0) * D;
           }
-          if (sc.wch == 1) {
+          if (wch == 1) {
             if (valid) bf16_chunk_mma<BF16H>(S, Kb, Vb, valid, lane);
           } else if ((valid >> (16 * warp)) & 0xFFFFull) {
             bf16_span_mma<BF16H>(S, Kb, Vb, valid, lane, warp, 1);
           }
         }
       } else {
-        const int p0 = jj * sc.S;
-        int p1 = p0 + sc.S;
-        if (p1 > pages_b) p1 = pages_b;
         const int nwp = (p1 - p0 - warp + NW - 1) / NW > 0 ? (p1 - p0 - warp + NW - 1) / NW : 0;
         PageIds P;
         page_ids_init(P, cv, b, p0 + warp, nwp, lane);
@@ -894,9 +1120,6 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
       }
     } else if constexpr (!BF16H) {
       // ------------------------------------------------------ INT2 history
-      const int p0 = jj * sc.S;
-      int p1 = p0 + sc.S;
-      if (p1 > pages_b) p1 = pages_b;
       const int nw_pages = (p1 - p0 - warp + NW - 1) / NW > 0 ? (p1 - p0 - warp + NW - 1) / NW : 0;
       uint8_t* my_stage = smem + L.off_stage + (size_t)warp * DEPTH * L.stage_bytes;
       uint64_t* my_bar = mbar + warp * DEPTH;
@@ -1206,10 +1429,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
       waited = true;
     }
     if (misc[1]) break;
-    __syncthreads();
-    if (threadIdx.x == 0) misc[0] = (int)gridDim.x + atomicAdd(a.counter, 1);
-    __syncthreads();
-    it = misc[0];
+    __syncthreads();  // every thread has read the item before thread 0 moves the cursor
   }
   if (!waited) wait_prev();
 }

@@ -430,6 +430,7 @@ struct Sched {
   int n_win;        // number of window items (B * Hkv * wch)
   int wch;          // window items per (request, kv head): 5 (one per 64-token chunk) or 1
   int win_first;    // window items are handed out before history items
+  long long pages;  // history pages of all (request, kv head)
 };
 
 // Automatic item sizing (resident > 0): one item per resident CTA while that
@@ -437,6 +438,9 @@ struct Sched {
 // merge costs dominate); beyond that, items for up to target / resident per
 // CTA, at least AUTO_MIN_PAGES pages each, balanced through the work counter.
 constexpr int AUTO_ITEMS_PER_CTA = 4;
+// Weight of one BF16 window chunk (64 tokens of one kv head) in history pages
+// in decode_kernel's balanced partition.
+constexpr int DEC_WIN_WEIGHT = 12;
 constexpr int AUTO_WAVE_PAGES = 40;
 constexpr int AUTO_MIN_PAGES = 28;
 
@@ -500,6 +504,7 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
   s.S = red[0];
   __syncthreads();
   s.n_hist = pre[B];
+  s.pages = total;
   s.win_first = (long long)WIN_BYTES_PER_HEAD / s.wch > (long long)s.S * hist_item_unit_bytes;
   return s;
 }
@@ -629,7 +634,8 @@ struct DecodeArgs {
   // the page that receives the demoted token only after its wait.
   int step_pred;
   int32_t* pred;  // scratch [3][B]
-  int balanced;   // 1: the tensor-memory kernel's balanced partition (decode grid in bal_grid)
+  int balanced;   // work partition: 0 item list, 1 balanced (the tensor-memory kernel's always),
+                  // 2 decided on the device from the lengths (decode grid in bal_grid)
   int bal_grid;
   int bal_wch;
   LayerRot rot;

@@ -49,6 +49,8 @@ OPT_PREFILL_IMPL = 3
 PREFILL_TCGEN05 = 0  # tcgen05.mma, S/P/O in tensor memory
 PREFILL_MMA_SYNC = 1  # mma.sync
 OPT_WAIT_POLLS = 4  # poll budget of each history page's first wait in the decode kernel
+OPT_DECODE_PARTITION = 5  # 0 automatic, 1 item list, 2 balanced
+PARTITION_AUTO, PARTITION_ITEMS, PARTITION_BALANCED = 0, 1, 2
 WAIT_POLLS_DEFAULT = 1 << 22
 
 

@@ -136,12 +136,18 @@ typedef enum {
                                   (default): automatic -- one item per CTA while items stay small,
                                   else up to 4 per CTA of at least 28 pages, balanced at run time */
   OSCAR_OPT_PREFILL_IMPL = 3, /* an oscar_prefill_impl value (default OSCAR_PREFILL_TCGEN05) */
-  OSCAR_OPT_WAIT_POLLS = 4     /* iteration budget of the first wait for each history page of the
+  OSCAR_OPT_WAIT_POLLS = 4,    /* iteration budget of the first wait for each history page of the
                                   mma.sync and CUDA-core decode kernels (default 4194304 polls).
                                   A wait that runs out records OSCAR_ERR_TIMEOUT; the kernel then
                                   waits, with the full budget, for the copies it has in flight and
                                   leaves.  0 makes every such wait give up at once: a way to
                                   exercise that path.  Values < 0 are OSCAR_ERR_INVALID_ARG. */
+  OSCAR_OPT_DECODE_PARTITION = 5 /* how the mma.sync and CUDA-core decode kernels split the work:
+                                    0 (default) automatic -- balanced while each (request, kv head)
+                                    spans several CTAs, else the item list; 1 the item list
+                                    (OSCAR_OPT_ITEMS_PER_CTA); 2 balanced: CTA i takes an equal
+                                    share of all history pages and window chunks, in order.  The
+                                    outputs do not depend on the partition beyond rounding. */
 } oscar_option;
 
 typedef struct {

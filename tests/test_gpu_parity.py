@@ -124,10 +124,12 @@ def test_cfg1_import_append_demote_and_decode():
 EDGE_LENGTHS = [0, 1, 2, 63, 64, 65, 100, 319, 320, 321, 383, 384, 385, 447, 448, 449, 700, 1024, 1100]
 
 
+@pytest.mark.parametrize("part", [oscar.PARTITION_ITEMS, oscar.PARTITION_BALANCED])
 @pytest.mark.parametrize("impl", [0, 1, 2, 3])
-def test_decode_edge_lengths_gqa4_g128(impl):
+def test_decode_edge_lengths_gqa4_g128(impl, part):
     sc = GS.build("edge", EDGE_LENGTHS, Hq=8, Hkv=2, g=128, interleave=True, calib_n=512)
     try:
+        oscar.oscar_set_option(sc.ctx, oscar.OPT_DECODE_PARTITION, part)
         q = GS.queries(sc, seed=2)
         out, lse = GS.decode(sc, q, impl)
         assert oscar.oscar_get_error(sc.ctx) == 0
@@ -165,16 +167,21 @@ def test_decode_gqa_and_group_sizes(G, g, impl):
         sc.close()
 
 
-@pytest.mark.parametrize("items", [0, 1, 3, 8])
+@pytest.mark.parametrize("items", [0, 1, 3, 8, -1])
 def test_decode_item_sizing_options(items):
     """The work list's item sizing (0 = automatic, else fixed items per CTA)
     changes only how the history is split: every setting matches the oracle
-    on a ragged batch long enough for the automatic rule to split finely."""
+    on a ragged batch long enough for the automatic rule to split finely.
+    items < 0: the balanced partition instead of the item list."""
     # ~21K history pages x kv heads: past the automatic rule's single-wave limit
     lengths = [9000, 320, 140000, 62345, 0, 700, 125000, 64 * 50 + 320 + 3]
     sc = GS.build("items", lengths, Hq=16, Hkv=4, g=128, interleave=True, calib_n=512)
     try:
-        oscar.oscar_set_option(sc.ctx, oscar.OPT_ITEMS_PER_CTA, items)
+        if items < 0:
+            oscar.oscar_set_option(sc.ctx, oscar.OPT_DECODE_PARTITION, oscar.PARTITION_BALANCED)
+        else:
+            oscar.oscar_set_option(sc.ctx, oscar.OPT_DECODE_PARTITION, oscar.PARTITION_ITEMS)
+            oscar.oscar_set_option(sc.ctx, oscar.OPT_ITEMS_PER_CTA, items)
         q = GS.queries(sc, seed=8)
         out, lse = GS.decode(sc, q)
         assert oscar.oscar_get_error(sc.ctx) == 0
@@ -246,7 +253,8 @@ def test_append_stream_wraps_ring_and_matches_oracle():
         sc.close()
 
 
-def test_decode_step_equals_append_then_decode():
+@pytest.mark.parametrize("part", [oscar.PARTITION_ITEMS, oscar.PARTITION_BALANCED])
+def test_decode_step_equals_append_then_decode(part):
     """oscar_decode_step (append and query rotation in one kernel) gives the
     same cache and the same outputs, bit for bit, as oscar_append followed by
     oscar_decode, across ring wrap and demotions; the outputs match the oracle."""
@@ -254,6 +262,8 @@ def test_decode_step_equals_append_then_decode():
     scs = [GS.build("stepx", lengths, Hq=8, Hkv=2, g=128, extra_tokens=120, calib_n=512) for _ in range(2)]
     try:
         a, b = scs
+        for s_ in scs:
+            oscar.oscar_set_option(s_.ctx, oscar.OPT_DECODE_PARTITION, part)
         scratch = [oscar.alloc_scratch(s_.cfg) for s_ in scs]
         for t in range(120):
             k = torch.stack([a.K[i][:, lengths[i] + t] for i in range(3)]).contiguous()
