@@ -1202,7 +1202,8 @@ def run_leg(args, wl):
         oscar.oscar_set_option(ctx, oscar.OPT_DECODE_IMPL, 3)
     part = {"auto": oscar.PARTITION_AUTO, "items": oscar.PARTITION_ITEMS,
             "balanced": oscar.PARTITION_BALANCED}[args.partition]
-    oscar.oscar_set_option(ctx, oscar.OPT_DECODE_PARTITION, part)
+    if part != oscar.PARTITION_AUTO:
+        oscar.oscar_set_option(ctx, oscar.OPT_DECODE_PARTITION, part)
     tok_bytes = Bsz * Hkv * 128 * 2
     kv_new = (wk["K"][:, :, L0:L0 + extra].permute(2, 0, 1, 3).contiguous(),
               wk["V"][:, :, L0:L0 + extra].permute(2, 0, 1, 3).contiguous())

@@ -53,12 +53,9 @@ struct SmemLayout {
 // decode_kernel's position in its work list (shared memory, thread 0) and
 // the item it hands to the block.
 struct DecodeCursor {
-  long long lo, hi;        // balanced: this CTA's range of positions
-  int bal;                 // 1: balanced partition, 0: item list
-  int cb, ck, cc, phase;   // balanced: request, kv head, next window chunk, 0 windows / 1 history
-  int bl_n, bl_wch;        // balanced: CTAs taking part, window chunk weight
-  int it, first;           // item list: next index, the static first item still to take
-  int total, S, n_hist, n_win, lwch, win_first;  // item list: make_sched's list
+  long long lo, hi;        // this CTA's range of positions
+  int cb, ck, cc, phase;   // request, kv head, next window chunk, 0 windows / 1 history
+  int bl_n, bl_wch;        // CTAs taking part, window chunk weight
   int found, is_win, b, kvh, wc, wch, p0, p1, slot;  // the item
 };
 
@@ -66,18 +63,6 @@ struct DecodeCursor {
 // than AUTO_WAVE_PAGES pages (several items per CTA, each paying a start).
 __device__ __forceinline__ bool use_balanced(const Sched& sc, int grid) {
   return sc.pages > (long long)AUTO_WAVE_PAGES * grid;
-}
-
-__device__ inline void cursor_init_items(DecodeCursor& c, const Sched& sc, int cta) {
-  c.bal = 0;
-  c.first = 1;
-  c.it = cta;
-  c.total = sc.n_hist + sc.n_win;
-  c.S = sc.S;
-  c.n_hist = sc.n_hist;
-  c.n_win = sc.n_win;
-  c.lwch = sc.wch;
-  c.win_first = sc.win_first ? 1 : 0;
 }
 
 // Weight of (b, kvh) in the balanced list: history pages plus wch per
@@ -105,9 +90,7 @@ __device__ inline void cursor_restart(DecodeCursor& c, const long long* pre64, i
 }
 
 __device__ inline void cursor_init_balanced(DecodeCursor& c, const Balanced& bl, const long long* pre64, int B,
-                                            int Hkv, const int32_t* hl, const int32_t* sl, int cta) {
-  (void)Hkv;
-  c.bal = 1;
+                                            const int32_t* hl, const int32_t* sl, int cta) {
   c.bl_n = bl.n;
   c.bl_wch = bl.wch;
   c.lo = cta < bl.n ? balanced_lo(bl, cta) : 0;
@@ -116,11 +99,14 @@ __device__ inline void cursor_init_balanced(DecodeCursor& c, const Balanced& bl,
   cursor_restart(c, pre64, B, hl, sl);
 }
 
+struct WindowPtrs {
+  const __nv_bfloat16 *sink_k, *sink_v, *ring_k, *ring_v;
+};
+
 // L2 prefetch of the BF16 window chunks whose positions lie in the cursor's
 // range (all threads; the cursor as cursor_init_balanced left it).
-__device__ inline void prefetch_range_windows(const DecodeCursor& c0, const CacheView& cv, int B,
+__device__ inline void prefetch_range_windows(const DecodeCursor& c0, const WindowPtrs& w, int B, int Hkv,
                                               const long long* pre64, const int32_t* hl, const int32_t* sl) {
-  const int Hkv = cv.Hkv;
   if (c0.lo >= c0.hi) return;
   int cb = c0.cb, ck = c0.ck;
   for (int guard = 0; guard < 64 && cb < B && pre64[cb] < c0.hi; ++guard) {
@@ -140,8 +126,8 @@ __device__ inline void prefetch_range_windows(const DecodeCursor& c0, const Cach
       const long long x = seg + P + (long long)c0.bl_wch * __popc(mask & ((1u << ch) - 1u));
       if (x < c0.lo || x >= c0.hi) continue;
       // 64 tokens x 256 bytes of K and of V: 128 lines each
-      const char* kb = (const char*)(ch == 0 ? cv.sink_k + head * SINK * D : cv.ring_k + (head * RECENT + 64 * (ch - 1)) * D);
-      const char* vb = (const char*)(ch == 0 ? cv.sink_v + head * SINK * D : cv.ring_v + (head * RECENT + 64 * (ch - 1)) * D);
+      const char* kb = (const char*)(ch == 0 ? w.sink_k + head * SINK * D : w.ring_k + (head * RECENT + 64 * (ch - 1)) * D);
+      const char* vb = (const char*)(ch == 0 ? w.sink_v + head * SINK * D : w.ring_v + (head * RECENT + 64 * (ch - 1)) * D);
       for (int l = threadIdx.x; l < 128; l += blockDim.x) {
         asm volatile("prefetch.global.L2 [%0];\n" ::"l"(kb + 128 * l));
         asm volatile("prefetch.global.L2 [%0];\n" ::"l"(vb + 128 * l));
@@ -151,51 +137,31 @@ __device__ inline void prefetch_range_windows(const DecodeCursor& c0, const Cach
   }
 }
 
-// The next item into c.found / c.is_win / ... (thread 0).
-__device__ inline void cursor_next(DecodeCursor& c, const DecodeArgs& a, const long long* pre64, const int* pre,
-                                   const int32_t* hl, const int32_t* sl) {
-  const int B = a.B, Hkv = a.cv.Hkv;
+__device__ __noinline__ void cursor_next(DecodeCursor& c, int B, int Hkv, const long long* pre64,
+                                         const int32_t* hl, const int32_t* sl);
+
+// The balanced partition's start (all threads): the request weights, this
+// CTA's range, an L2 prefetch of its window chunks, and its first item.
+__device__ __noinline__ void balanced_setup(DecodeCursor& c, int B, int Hkv, int wch, WindowPtrs w,
+                                            long long* pre64, const int32_t* hl, const int32_t* sl) {
+  const Balanced bl = make_balanced(sl, hl, B, Hkv, wch, gridDim.x, pre64);
+  if (threadIdx.x == 0) cursor_init_balanced(c, bl, pre64, B, hl, sl, blockIdx.x);
+  __syncthreads();
+  // the window chunks of the range are read with plain loads, which queue
+  // behind the whole grid's page copies: ask for all of them at once
+  prefetch_range_windows(c, w, B, Hkv, pre64, hl, sl);
+  __syncthreads();  // the cursor is read before thread 0 moves it
+  if (threadIdx.x == 0) cursor_next(c, B, Hkv, pre64, hl, sl);
+  __syncthreads();
+}
+
+// The next item of the balanced range into c.found / c.is_win / ... (thread 0).
+__device__ __noinline__ void cursor_next(DecodeCursor& c, int B, int Hkv, const long long* pre64,
+                                         const int32_t* hl, const int32_t* sl) {
   c.found = 0;
   c.is_win = 0;
   c.wc = 0;
   c.p0 = c.p1 = 0;
-  if (!c.bal) {
-    int it;
-    if (c.first) {
-      it = c.it;
-      c.first = 0;
-    } else {
-      it = (int)gridDim.x + atomicAdd(a.counter, 1);
-    }
-    if (it >= c.total) return;
-    int idx;
-    bool is_win;
-    if (c.win_first) {
-      is_win = it < c.n_win;
-      idx = is_win ? it : it - c.n_win;
-    } else {
-      is_win = it >= c.n_hist;
-      idx = is_win ? it - c.n_hist : it;
-    }
-    c.found = 1;
-    c.is_win = is_win ? 1 : 0;
-    c.wch = c.lwch;
-    if (is_win) {
-      c.b = idx / (Hkv * c.lwch);
-      c.kvh = (idx / c.lwch) % Hkv;
-      c.wc = idx % c.lwch;
-      c.slot = c.n_hist + idx;
-    } else {
-      int b, kvh, jj;
-      hist_item_coords(idx, pre, B, Hkv, hl, c.S, b, kvh, jj);
-      c.b = b;
-      c.kvh = kvh;
-      c.p0 = jj * c.S;
-      c.p1 = c.p0 + c.S;
-      c.slot = idx;
-    }
-    return;
-  }
   for (;;) {
     if (c.cb >= B || pre64[c.cb] >= c.hi) {
       if (c.phase == 1) return;
@@ -991,32 +957,55 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
   // a.balanced == 2 picks the balanced partition when the item list would
   // give a CTA more than one wave's worth of pages (the merge decides alike).
   DecodeCursor* cur = (DecodeCursor*)(smem + L.off_cursor);
-  {
-    bool bal = a.balanced == 1;
-    if (!bal) {
-      const Sched sc = make_sched(hl, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
-      bal = a.balanced == 2 && use_balanced(sc, gridDim.x);
-      if (!bal && threadIdx.x == 0) cursor_init_items(*cur, sc, blockIdx.x);
-    }
-    if (bal) {
-      long long* pre64 = (long long*)pre;
-      const Balanced bl = make_balanced(sl, hl, a.B, Hkv, a.bal_wch, gridDim.x, pre64);
-      if (threadIdx.x == 0) cursor_init_balanced(*cur, bl, pre64, a.B, Hkv, hl, sl, blockIdx.x);
-      __syncthreads();
-      // the window chunks of the range are read with plain loads, which queue
-      // behind the whole grid's page copies: ask for all of them at once
-      prefetch_range_windows(*cur, cv, a.B, pre64, hl, sl);
-    }
-    __syncthreads();
+  Sched sc;
+  bool bal = a.balanced == 1;
+  if (!bal) {
+    sc = make_sched(hl, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
+    bal = a.balanced == 2 && use_balanced(sc, gridDim.x);
   }
+  if (bal)  // out of line: the item list's path stays short
+    balanced_setup(*cur, a.B, Hkv, a.bal_wch, WindowPtrs{cv.sink_k, cv.sink_v, cv.ring_k, cv.ring_v},
+                   (long long*)pre, hl, sl);
+  const int total = bal ? 0 : sc.n_hist + sc.n_win;
+  int it = blockIdx.x;  // item list: first item static, later ones from the work counter
 
   for (;;) {
-    if (threadIdx.x == 0) cursor_next(*cur, a, (long long*)pre, pre, hl, sl);
-    __syncthreads();
-    if (!cur->found) break;
-    const bool is_win = cur->is_win;
-    const int b = cur->b, kvh = cur->kvh, wc = cur->wc, wch = cur->wch, p0 = cur->p0, slot = cur->slot;
-    int p1 = cur->p1;
+    bool is_win;
+    int b, kvh, wc = 0, wch, p0 = 0, p1 = 0, slot;
+    if (bal) {
+      if (!cur->found) break;
+      is_win = cur->is_win;
+      b = cur->b;
+      kvh = cur->kvh;
+      wc = cur->wc;
+      wch = cur->wch;
+      p0 = cur->p0;
+      p1 = cur->p1;
+      slot = cur->slot;
+    } else {
+      if (it >= total) break;
+      int idx;
+      if (sc.win_first) {
+        is_win = it < sc.n_win;
+        idx = is_win ? it : it - sc.n_win;
+      } else {
+        is_win = it >= sc.n_hist;
+        idx = is_win ? it - sc.n_hist : it;
+      }
+      wch = sc.wch;
+      if (is_win) {
+        b = idx / (Hkv * sc.wch);
+        kvh = (idx / sc.wch) % Hkv;
+        wc = idx % sc.wch;
+        slot = sc.n_hist + idx;
+      } else {
+        int jj = 0;
+        hist_item_coords(idx, pre, a.B, Hkv, hl, sc.S, b, kvh, jj);
+        p0 = jj * sc.S;
+        p1 = p0 + sc.S;
+        slot = idx;
+      }
+    }
     const int hist_b = hl[b];
     const int pages_b = (hist_b + PAGE - 1) / PAGE;
     if (p1 > pages_b) p1 = pages_b;
@@ -1429,7 +1418,13 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
       waited = true;
     }
     if (misc[1]) break;
-    __syncthreads();  // every thread has read the item before thread 0 moves the cursor
+    __syncthreads();  // every thread has read the item before thread 0 moves on
+    if (threadIdx.x == 0) {
+      if (bal) cursor_next(*cur, a.B, Hkv, (long long*)pre, hl, sl);
+      else misc[0] = (int)gridDim.x + atomicAdd(a.counter, 1);
+    }
+    __syncthreads();
+    it = misc[0];
   }
   if (!waited) wait_prev();
 }
