@@ -139,9 +139,13 @@ int decode_ctas(const oscar_ctx* ctx, int batch, bool bf16_history, int layer = 
 
 // decode_kernel's work partition (DecodeArgs::balanced): 0 the item list, 1
 // balanced, 2 decided on the device (balanced once the item list would give
-// a CTA more than a wave's worth of pages).
-int decode_partition(const oscar_ctx* ctx) {
-  return ctx->partition == 1 ? 0 : ctx->partition == 2 ? 1 : 2;
+// a CTA more than a wave's worth of pages).  Automatic: the item list when
+// the (request, kv head) segments outnumber half the CTAs -- a balanced range
+// would then cross segments, each crossing paying an item start.
+int decode_partition(const oscar_ctx* ctx, int batch, int ctas) {
+  if (ctx->partition == 1) return 0;
+  if (ctx->partition == 2) return 1;
+  return 2 * batch * ctx->cfg.num_kv_heads <= ctas ? 2 : 0;
 }
 
 // The item list's size bound (make_sched's target).
@@ -160,8 +164,9 @@ int list_items(const oscar_ctx* ctx, int batch, bool bf16_history, int layer = -
 int target_items(const oscar_ctx* ctx, int batch, bool bf16_history, int layer = -1) {
   if (!bf16_history && kernel_impl(ctx, layer) == 5) return ctx->num_sms + 4 * batch * ctx->cfg.num_kv_heads;
   const int t = list_items(ctx, batch, bf16_history, layer);
-  const int tb = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, layer) + 4 * batch * ctx->cfg.num_kv_heads;
-  const int part = decode_partition(ctx);
+  const int ctas = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, layer);
+  const int tb = ctas + 4 * batch * ctx->cfg.num_kv_heads;
+  const int part = decode_partition(ctx, batch, ctas);
   if (part == 1) return tb;
   if (part == 2 && tb > t) return tb;
   return t;
@@ -371,7 +376,7 @@ oscar_status decode_args(oscar_ctx* ctx, int layer, const oscar_cache* cache, co
   }
   grid = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, vlayer);
   a.resident = ctx->items_per_cta == 0 ? grid : 0;
-  a.balanced = decode_partition(ctx);
+  a.balanced = decode_partition(ctx, batch, grid);
   a.bal_grid = grid;
   a.bal_wch = DEC_WIN_WEIGHT;
   return OSCAR_OK;
