@@ -1155,7 +1155,7 @@ def per_call_times(fn, n, stream):
     return [ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(n)]
 
 
-LEGS = ("decode", "step", "bf16", "append", "cuda_core", "tensor_single", "tcgen05", "prefill")
+LEGS = ("decode", "step", "bf16", "append", "cuda_core", "tensor_single", "tcgen05", "prefill", "calibration")
 
 
 def run_leg(args, wl):
@@ -1170,7 +1170,9 @@ def run_leg(args, wl):
       cuda_core     oscar_decode with OSCAR_DECODE_CUDA_CORE
       tensor_single oscar_decode with OSCAR_DECODE_TENSOR_SINGLE
       tcgen05       oscar_decode with OSCAR_DECODE_TCGEN05
-      prefill       oscar_prefill, a 64-token chunk"""
+      prefill       oscar_prefill, a 64-token chunk
+      calibration   oscar_calibrate then oscar_clip_errors (8 ratios) of one kv head's
+                    2048-token calibration set, the heads in turn"""
     import torch
 
     from bit_kv_cache_int2_gb300 import build as B
@@ -1190,6 +1192,8 @@ def run_leg(args, wl):
     n_calls = args.warmup + args.steps
     appends = args.leg in ("step", "append")
     extra = max(n_calls // n_copies + 16, 80) if appends else 16
+    if args.leg == "calibration":
+        n_copies = 1
     wk = build_workload(wl, dev, 1 if bf16 else n_copies, extra, bf16_copies=n_copies if bf16 else 0)
     ctx, cfg, q = wk["ctx"], wk["cfg"], wk["q"]
     out = torch.empty_like(q)
@@ -1226,6 +1230,21 @@ def run_leg(args, wl):
             cnt[c] += 1
         if args.leg == "append":
             bytes_per_call = Bsz * Hkv * 2 * (3 * 256 + 32 + (128 // g) * 4)
+    elif args.leg == "calibration":
+        from bit_kv_cache_int2_gb300 import synth
+
+        G_cal, N_cal = wl["Hq"] // Hkv, 2048
+        ratios = [1.0, 0.975, 0.95, 0.925, 0.9, 0.85, 0.8, 0.7]
+        cal_sets = [tuple(t.to(dev).contiguous() for t in synth.calibration_set(0, "bench", 0, h, wk["stats"][h],
+                                                                                G=G_cal, n=N_cal))
+                    for h in range(Hkv)]
+        cscr = oscar.calibration_scratch(G_cal, N_cal, len(ratios), dev)
+
+        def fn(i):
+            h = i % Hkv
+            oscar.oscar_calibrate(ctx, *cal_sets[h], N_cal, cscr)
+            oscar.oscar_clip_errors(ctx, 0, h, *cal_sets[h], N_cal, ratios, cscr)
+        bytes_per_call = None
     else:  # prefill
         T_pf = 64
         q_pf = torch.stack([torch.cat([synth_queries(wk["stats"][h], T_pf, wl["Hq"] // Hkv, b, h, dev)
