@@ -687,6 +687,21 @@ __device__ __forceinline__ void prep_body(const DecodeArgs& a, int bk, int cq, i
     const char* rv = (const char*)(a.rot.RV_frag + (size_t)kvh * RV_FRAG_WORDS) + (size_t)(cq * 128 + t) * 128;
     asm volatile("prefetch.global.L2 [%0];\n" ::"l"(rv));
   }
+  {
+    // The decode kernel's first reads are the lengths and request b's page
+    // table row, each a dependent round trip before its first page copy:
+    // bring them into L2 now (a hint only; their values are read after the
+    // waits that order them).  The row's 128-byte lines are spread over the
+    // request's Hkv x 4 CTAs.
+    const int per_req = cv.Hkv * 4, me = kvh * 4 + cq;
+    if (t == 0 && me == 0) {
+      asm volatile("prefetch.global.L2 [%0];\n" ::"l"(cv.hist_lens + b));
+      asm volatile("prefetch.global.L2 [%0];\n" ::"l"(cv.seq_lens + b));
+    }
+    const int lines = (cv.max_pages_per_req + 31) / 32;
+    for (int l = me + per_req * t; l < lines; l += per_req * 128)
+      asm volatile("prefetch.global.L2 [%0];\n" ::"l"(cv.page_table + (size_t)b * cv.max_pages_per_req + 32 * (size_t)l));
+  }
   pdl_wait();
   if (release) pdl_launch_dependents();
   if (t == 0 && cq == 0 && bk == 0) a.counter[0] = 0;  // history items after the first wave

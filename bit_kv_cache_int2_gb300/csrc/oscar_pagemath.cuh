@@ -11,6 +11,13 @@ namespace oscar {
 
 constexpr int DEC_NW = 4;  // warps per decode CTA
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // ------------------------------------------------- per-warp decode state
 template <int NG>
 struct Int2State {
@@ -282,14 +289,23 @@ __device__ __forceinline__ void int2_pair_mma(Int2State<NG>& S, const uint8_t* s
         const float2 sz = __half22float2(ksz[row * NG + gr]);
         v = fmaf(sz.x, fmaf(acc[s][gr][e], S.ka[hc], S.kb[hc][gr]), fmaf(sz.y, S.kg[hc][gr], v));
       }
-      lam[s][e] = (FULL || row < nv) ? v : -INFINITY;
+      lam[s][e] = v;
     }
   }
-  float pm[2] = {-INFINITY, -INFINITY};
+  if (!FULL && (nvA < PAGE || nvB < PAGE)) {  // warp-uniform: a partial page or no page B
 #pragma unroll
-  for (int s = 0; s < 4; ++s)
+    for (int s = 0; s < 4; ++s)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) pm[e & 1] = fmaxf(pm[e & 1], lam[s][e]);
+      for (int e = 0; e < 4; ++e)
+        if ((e < 2 ? 16 * s + gid : 16 * s + gid + 8) >= nv) lam[s][e] = -INFINITY;
+  }
+  float pm[2];
+#pragma unroll
+  for (int hc = 0; hc < 2; ++hc) {
+    float x = fmax3(lam[0][hc], lam[0][hc + 2], lam[1][hc]);
+    float y = fmax3(lam[1][hc + 2], lam[2][hc], lam[2][hc + 2]);
+    pm[hc] = fmax3(x, y, fmaxf(lam[3][hc], lam[3][hc + 2]));
+  }
 #pragma unroll
   for (int hc = 0; hc < 2; ++hc) {
     pm[hc] = fmaxf(pm[hc], __shfl_xor_sync(0xffffffffu, pm[hc], 4));
