@@ -815,9 +815,9 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
     float am = fmaxf(fmaxf(fabsf(Y.x), fabsf(Y.y)), fmaxf(fabsf(Y.z), fabsf(Y.w)));
 #pragma unroll
     for (int o = 16; o; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-    int ex = 0;
-    frexpf(am, &ex);
-    const float up = am > 0.f ? ldexpf(1.f, min(12 - ex, 100)) : 1.f;
+    // up = 2^(12 - ex) (at most 2^100), ex the frexp exponent of am, from its exponent bits
+    const int ex = (int)((__float_as_uint(am) >> 23) & 0xffu) - 126;
+    const float up = am > 0.f ? pow2i(min(12 - ex, 100)) : 1.f;
     if (lane == 0) {
       hM[h] = Ls > 0.f ? M : -INFINITY;
       hL[h] = Ls;

@@ -96,6 +96,10 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
   return old;
 }
 
+// 2^n for -126 <= n <= 127, from the exponent bits (the cold prologues stay
+// short: no library call).
+__device__ __forceinline__ float pow2i(int n) { return __uint_as_float((uint32_t)(127 + n) << 23); }
+
 __device__ __forceinline__ void record_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
@@ -452,13 +456,15 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
                                    int hist_item_unit_bytes, int* pre, int* red) {
   const int tid = threadIdx.x;
   // total history pages (over requests), times Hkv
-  long long local = 0;
+  int local = 0;
+#pragma unroll 1
   for (int b = tid; b < B; b += blockDim.x) local += (hist_lens[b] + PAGE - 1) / PAGE;
   // block reduce (red: one int per warp)
-  for (int o = 16; o; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
-  if ((tid & 31) == 0) red[tid >> 5] = (int)local;
+  local = __reduce_add_sync(0xffffffffu, local);
+  if ((tid & 31) == 0) red[tid >> 5] = local;
   __syncthreads();
-  long long total = 0;
+  int total = 0;
+#pragma unroll 1
   for (int w = 0; w < (int)(blockDim.x + 31) / 32; ++w) total += red[w];
   __syncthreads();
   total *= Hkv;
@@ -471,10 +477,10 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
     s.n_win = B * Hkv * s.wch;
     int th = items - s.n_win;
     if (th < (items + 1) / 2) th = (items + 1) / 2;
-    const long long S = (total + th - 1) / th;
-    return S < 1 ? 1LL : S;
+    const int S = (total + th - 1) / th;
+    return S < 1 ? 1 : S;
   };
-  long long S = pages_per_item(resident > 0 ? resident : target);
+  int S = pages_per_item(resident > 0 ? resident : target);
   if (resident > 0 && S > AUTO_WAVE_PAGES) {
     S = pages_per_item(target);
     if (S < AUTO_MIN_PAGES) S = AUTO_MIN_PAGES;
@@ -482,8 +488,10 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
   s.S = (int)S;
   if (tid == 0) {
     // per-request rounding can add up to B*Hkv items: grow S until they fit
+#pragma unroll 1
     for (int iter = 0; iter < 32; ++iter) {
       long long n = 0;
+#pragma unroll 1
       for (int b = 0; b < B; ++b) {
         const int pages = (hist_lens[b] + PAGE - 1) / PAGE;
         n += (long long)Hkv * ((pages + s.S - 1) / s.S);
@@ -492,6 +500,7 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
       s.S += s.S / 8 > 1 ? s.S / 8 : 1;
     }
     int acc = 0;
+#pragma unroll 1
     for (int b = 0; b < B; ++b) {
       pre[b] = acc;
       const int pages = (hist_lens[b] + PAGE - 1) / PAGE;
@@ -505,7 +514,7 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
   __syncthreads();
   s.n_hist = pre[B];
   s.pages = total;
-  s.win_first = (long long)WIN_BYTES_PER_HEAD / s.wch > (long long)s.S * hist_item_unit_bytes;
+  s.win_first = (long long)(WIN_BYTES_PER_HEAD / s.wch) > (long long)s.S * hist_item_unit_bytes;
   return s;
 }
 
@@ -738,10 +747,10 @@ __device__ __forceinline__ void prep_body(const DecodeArgs& a, int bk, int cq, i
     a.qrot[row * D + c] = y;
     // power-of-two prescale so that |q'| * 16 stays below 2^14 in fp16
     const float am = sm.nrm[n];
-    int ex = 0;
-    frexpf(am, &ex);
-    const int sig = am > 0.f ? ex - 10 : 0;
-    const float yq = ldexpf(y, -sig) * f;
+    // sig = frexp exponent of |q| less 10, from the exponent bits (|q| is a
+    // normal float in practice; the clamp keeps 2^-sig a normal float)
+    const int sig = am > 0.f ? max(-100, min(100, (int)((__float_as_uint(am) >> 23) & 0xffu) - 136)) : 0;
+    const float yq = y * pow2i(-sig) * f;
     const bool cbrec = a.impl == 4;
     uint8_t* rec = a.qpack + row * (cbrec ? QPACK_CB_BYTES : QPACK_BYTES);
     float bs, ps = y;
@@ -766,7 +775,7 @@ __device__ __forceinline__ void prep_body(const DecodeArgs& a, int bk, int cq, i
       ((float*)(rec + (cbrec ? QPACK_CB_QSUM : QPACK_QSUM)))[cq] = bs;
       ((float*)(rec + (cbrec ? QPACK_CB_PSUM : QPACK_PSUM)))[cq] = ps;
       if (cq == 0)
-        *(float*)(rec + (cbrec ? QPACK_CB_ALPHA : QPACK_ALPHA)) = ldexpf(1.f, sig) * LOG2E * INV_SQRT_D * (1.f / 256.f);
+        *(float*)(rec + (cbrec ? QPACK_CB_ALPHA : QPACK_ALPHA)) = pow2i(sig) * LOG2E * INV_SQRT_D * (1.f / 256.f);
     }
   }
 }
