@@ -81,6 +81,19 @@ __device__ __forceinline__ void append_body(const CacheView& cv, const LayerRot&
 #pragma unroll
     for (int k = 0; k < 32; ++k) u[k] = __ldg(R + k * D);
   }
+  // The lengths, the page-table entry and the ring slot are dependent round
+  // trips after the wait: bring their lines into L2 now (hints only; the
+  // values are read after the wait).  Thread t takes line t of this head's
+  // 64 KB ring block; the request's page-table row is spread over its 2 Hkv CTAs.
+  {
+    const __nv_bfloat16* rb = (isv ? cv.ring_v : cv.ring_k) + (size_t)(b * cv.Hkv + h) * RECENT * D;
+    if (t < RECENT * D * 2 / 128) asm volatile("prefetch.global.L2 [%0];\n" ::"l"((const char*)rb + 128 * t));
+    if (t == 0) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(cv.hist_lens + b));
+    const int per_req = 2 * cv.Hkv, me = 2 * h + isv;
+    const int lines = (cv.max_pages_per_req + 31) / 32;
+    for (int l = me + per_req * t; l < lines; l += per_req * (int)blockDim.x)
+      asm volatile("prefetch.global.L2 [%0];\n" ::"l"(cv.page_table + (size_t)b * cv.max_pages_per_req + 32 * (size_t)l));
+  }
   // the new tokens, the lengths and the cache belong to earlier stream work;
   // the decode's prep_kernel waits for this grid before it reads anything
   pdl_wait();
