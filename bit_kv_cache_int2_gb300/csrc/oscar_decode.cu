@@ -712,6 +712,12 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
     asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a.part + ((size_t)slot * G + h0 + n) * PART_STRIDE));
   }
   pdl_wait();  // the decode kernel's partial records are complete and visible
+  if (a.step_pred && t == 0 && kvh == 0 && h0 == 0) {
+    // decode step: the request's new lengths (the step kernel's append left
+    // them to this kernel, which runs once every reader of the old ones is done)
+    cv.seq_lens[b] = a.pred[b];
+    cv.hist_lens[b] = a.pred[a.B + b];
+  }
 
   // ---- team member: records q = r, r + WPH, ... of the list (history
   // partials 0..nb-1, then window partials nb..nb+wch-1)
@@ -1032,7 +1038,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
       }
       const size_t head = (size_t)b * Hkv + kvh;
       if (is_win) {
-        const int Lq = cv.seq_lens[b];
+        const int Lq = sl[b];
         const int nsink = Lq < SINK ? Lq : SINK;
         const int recent = Lq > SINK ? Lq - SINK - hist_b : 0;
         const int h0 = hist_b % RECENT;

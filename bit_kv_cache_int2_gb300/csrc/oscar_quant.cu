@@ -179,9 +179,10 @@ __device__ __forceinline__ void append_body(const CacheView& cv, const LayerRot&
     ((uint4*)dst)[t] = ((const uint4*)src)[t];
   }
   // The last CTA of request b to finish updates its lengths: every CTA of the
-  // request has read the old lengths before it increments the counter.
+  // request has read the old lengths before it increments the counter.  In a
+  // decode step (pred) the merge kernel writes them instead, from pred.
   __syncthreads();
-  if (t == 0) {
+  if (t == 0 && !pred) {
     // release: this CTA's reads of the old lengths come before the count;
     // acquire: the last CTA writes the lengths after every CTA's reads
     const int old = atomic_add_acq_rel_gpu(&req_counter[b], 1);
