@@ -152,9 +152,11 @@ def test_codebook_decode_matches_oracle(G, g):
     try:
         q = GS.queries(sc, seed=5)
         for impl in (oscar.DECODE_TENSOR, oscar.DECODE_CUDA_CORE):  # the option does not matter
-            out, lse = GS.decode(sc, q, impl)
-            assert oscar.oscar_get_error(sc.ctx) == 0
-            hc = _check_decode(sc, q, out, lse)
+            for part in (oscar.PARTITION_ITEMS, oscar.PARTITION_BALANCED):
+                oscar.oscar_set_option(sc.ctx, oscar.OPT_DECODE_PARTITION, part)
+                out, lse = GS.decode(sc, q, impl)
+                assert oscar.oscar_get_error(sc.ctx) == 0
+                hc = _check_decode(sc, q, out, lse)
         n, bad = GS.compare_history(sc, hc, 6, 1, list(range(64, 64 + 593)), list(range(593)))
         assert bad <= 1e-4 * n
     finally:

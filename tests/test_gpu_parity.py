@@ -147,12 +147,14 @@ def test_decode_edge_lengths_gqa4_g128(impl, part):
         sc.close()
 
 
+@pytest.mark.parametrize("part", [oscar.PARTITION_ITEMS, oscar.PARTITION_BALANCED])
 @pytest.mark.parametrize("G,g", [(1, 32), (2, 64), (8, 32), (8, 128), (4, 64), (1, 128)])
 @pytest.mark.parametrize("impl", [0, 1, 2, 3])
-def test_decode_gqa_and_group_sizes(G, g, impl):
+def test_decode_gqa_and_group_sizes(G, g, impl, part):
     lengths = [333, 1000, 64 * 9 + 320 + 17]
     sc = GS.build(f"gq{G}{g}", lengths, Hq=2 * G, Hkv=2, g=g, calib_n=512)
     try:
+        oscar.oscar_set_option(sc.ctx, oscar.OPT_DECODE_PARTITION, part)
         q = GS.queries(sc, seed=3)
         out, lse = GS.decode(sc, q, impl)
         hc = GS.HostCache(sc)
@@ -198,10 +200,12 @@ def test_decode_item_sizing_options(items):
         sc.close()
 
 
-def test_bf16_history_baseline_matches_dense_attention():
+@pytest.mark.parametrize("part", [oscar.PARTITION_ITEMS, oscar.PARTITION_BALANCED])
+def test_bf16_history_baseline_matches_dense_attention(part):
     lengths = [1, 300, 321, 1000, 2000]
     sc = GS.build("bf16h", lengths, Hq=8, Hkv=2, bf16_history=True, mode=oscar.ROT_NONE)
     try:
+        oscar.oscar_set_option(sc.ctx, oscar.OPT_DECODE_PARTITION, part)
         q = GS.queries(sc, seed=4)
         out, lse = GS.decode(sc, q)
         hc = GS.HostCache(sc)
