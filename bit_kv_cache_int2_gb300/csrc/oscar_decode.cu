@@ -1166,6 +1166,8 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
         // a time with the layer's Lloyd-Max codebook
         constexpr bool PAIR = (IMPL == 3);
         constexpr bool CB = (IMPL == 4);
+        // codes as fp16 subnormals (no offset to carry) in the uniform kernels
+        constexpr bool SUBC = (IMPL == 3 || IMPL == 0);
         constexpr int QREC = CB ? QPACK_CB_BYTES : QPACK_BYTES;
         // the kv head's G packed query records, copied to shared memory by warp
         // 0 with coalesced 16-byte loads (every warp of every CTA reads them;
@@ -1219,7 +1221,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
             S.m[hc] = PAIR ? -1e30f : -INFINITY;
             S.l[hc] = 0.f;
             const float al = hv ? *(const float*)(r + O_ALPHA) : 0.f;
-            S.ka[hc] = PAIR ? al * 16777216.f : al;  // subnormal codes carry 2^-24
+            S.ka[hc] = SUBC ? al * 16777216.f : al;  // subnormal codes carry 2^-24
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
               float qs = 0.f, ps = 0.f;
@@ -1231,7 +1233,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
               S.bs[hc][gr] = 0.f;
               S.zs[hc][gr] = 0.f;
               S.kb[hc][gr] = CB ? fmaf(kc0 * ps, LOG2E * INV_SQRT_D, -1024.f * qs * al)
-                                : PAIR ? 0.f : -1024.f * qs * al;
+                                : SUBC ? 0.f : -1024.f * qs * al;
               S.kg[hc][gr] = ps * LOG2E * INV_SQRT_D;
             }
           }
@@ -1292,11 +1294,11 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
                 else
                   int2_page_mma_cb<NG, false>(S, X, my_stage + (size_t)st * L.stage_bytes, nv, lane);
               } else if (nv == PAGE) {
-                int2_page_mma<NG, true>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
+                int2_page_mma<NG, true, SUBC>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
               } else {
-                int2_page_mma<NG, false>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
+                int2_page_mma<NG, false, SUBC>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
               }
-              if ((k & 7) == 7) flush_v_offset<NG>(S);
+              if (!SUBC && (k & 7) == 7) flush_v_offset<NG>(S);
             }
             __syncwarp();
             if (k + DEPTH < nw_pages) {
@@ -1341,8 +1343,8 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
               const int gr = j / (8 / NG);
               // offset codes: o' = (O - 1024 sum B) / 256 + sum p z; subnormal
               // codes (PAIR): o' = 2^16 O + sum p z
-              const float off = PAIR ? 0.f : 1024.f * S.bs[hc][gr];
-              const float sc = PAIR ? 65536.f : 1.f / 256.f;
+              const float off = SUBC ? 0.f : 1024.f * S.bs[hc][gr];
+              const float sc = SUBC ? 65536.f : 1.f / 256.f;
               const float z = S.zs[hc][gr];
               wo[(warp * MAX_G + n) * D + 16 * j + gid] = fmaf(S.oacc[j][hc] - off, sc, z);
               wo[(warp * MAX_G + n) * D + 16 * j + 8 + gid] = fmaf(S.oacc[j][hc + 2] - off, sc, z);
