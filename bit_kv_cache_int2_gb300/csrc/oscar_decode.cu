@@ -271,10 +271,10 @@ template <int P>
 __device__ __forceinline__ void plane_frag(int q, uint32_t x, uint32_t y, uint32_t& a0, uint32_t& a1,
                                            uint32_t& a2, uint32_t& a3) {
   switch (q) {
-    case 0: a0 = code_plane<0, P>(x); a1 = code_plane<0, P>(y); a2 = code_plane<1, P>(x); a3 = code_plane<1, P>(y); break;
-    case 1: a0 = code_plane<2, P>(x); a1 = code_plane<2, P>(y); a2 = code_plane<3, P>(x); a3 = code_plane<3, P>(y); break;
-    case 2: a0 = code_plane<4, P>(x); a1 = code_plane<4, P>(y); a2 = code_plane<5, P>(x); a3 = code_plane<5, P>(y); break;
-    default: a0 = code_plane<6, P>(x); a1 = code_plane<6, P>(y); a2 = code_plane<7, P>(x); a3 = code_plane<7, P>(y); break;
+    case 0: a0 = code_plane_sub<0, P>(x); a1 = code_plane_sub<0, P>(y); a2 = code_plane_sub<1, P>(x); a3 = code_plane_sub<1, P>(y); break;
+    case 1: a0 = code_plane_sub<2, P>(x); a1 = code_plane_sub<2, P>(y); a2 = code_plane_sub<3, P>(x); a3 = code_plane_sub<3, P>(y); break;
+    case 2: a0 = code_plane_sub<4, P>(x); a1 = code_plane_sub<4, P>(y); a2 = code_plane_sub<5, P>(x); a3 = code_plane_sub<5, P>(y); break;
+    default: a0 = code_plane_sub<6, P>(x); a1 = code_plane_sub<6, P>(y); a2 = code_plane_sub<7, P>(x); a3 = code_plane_sub<7, P>(y); break;
   }
 }
 
@@ -395,10 +395,6 @@ __device__ __forceinline__ void int2_page_mma_cb(Int2State<NG>& S, const CbExtra
       const __half2 h1 = __floats2half2_rn(p[2] * sb0, p[3] * sb0);
       const __half2 g0 = __floats2half2_rn(p[0] * sa1, p[1] * sa1);
       const __half2 g1 = __floats2half2_rn(p[2] * sb1, p[3] * sb1);
-      const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
-      const float2 e0 = __half22float2(g0), e1 = __half22float2(g1);
-      S.bs[0][gr] += (f0.x + f1.x) + (e0.x + e1.x);
-      S.bs[1][gr] += (f0.y + f1.y) + (e0.y + e1.y);
       S.zs[0][gr] = fmaf(p[0], z_a, fmaf(p[2], z_b, S.zs[0][gr]));
       S.zs[1][gr] = fmaf(p[1], z_a, fmaf(p[3], z_b, S.zs[1][gr]));
       const uint32_t b0 = movmatrix_t(*(const uint32_t*)&h0);
@@ -1166,8 +1162,8 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
         // a time with the layer's Lloyd-Max codebook
         constexpr bool PAIR = (IMPL == 3);
         constexpr bool CB = (IMPL == 4);
-        // codes as fp16 subnormals (no offset to carry) in the uniform kernels
-        constexpr bool SUBC = (IMPL == 3 || IMPL == 0);
+        // codes (codebook: bit planes) as fp16 subnormals: no offset to carry
+        constexpr bool SUBC = (IMPL == 3 || IMPL == 0 || IMPL == 4);
         constexpr int QREC = CB ? QPACK_CB_BYTES : QPACK_BYTES;
         // the kv head's G packed query records, copied to shared memory by warp
         // 0 with coalesced 16-byte loads (every warp of every CTA reads them;
@@ -1232,7 +1228,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
               }
               S.bs[hc][gr] = 0.f;
               S.zs[hc][gr] = 0.f;
-              S.kb[hc][gr] = CB ? fmaf(kc0 * ps, LOG2E * INV_SQRT_D, -1024.f * qs * al)
+              S.kb[hc][gr] = CB ? kc0 * ps * (LOG2E * INV_SQRT_D)
                                 : SUBC ? 0.f : -1024.f * qs * al;
               S.kg[hc][gr] = ps * LOG2E * INV_SQRT_D;
             }

@@ -272,6 +272,16 @@ __device__ __forceinline__ uint32_t code_plane(uint32_t w) {
   const uint32_t src = (I <= 1) ? (w * 16u) : (I <= 4) ? w : (w >> 6);
   return and_or(src, M, 0x64006400u);
 }
+// Bit plane P of code pair I as an fp16 subnormal: bit * 2^(E(I) + P - 24).
+template <int I, int P>
+__device__ __forceinline__ uint32_t code_plane_sub(uint32_t w) {
+  constexpr uint32_t M = ((I == 0 || I == 2 || I == 5) ? 0x00300030u
+                          : (I == 1 || I == 3 || I == 6) ? 0x00C000C0u
+                                                         : 0x03000300u) &
+                         (P ? 0xAAAAAAAAu : 0x55555555u);
+  const uint32_t src = (I <= 1) ? (w * 16u) : (I <= 4) ? w : (w >> 6);
+  return src & M;
+}
 // The same code pair as an fp16 subnormal: code * 2^(E(I) - 24), one AND
 // and no offset (the tensor cores take fp16 subnormals exactly).  Callers
 // fold 2^(24 - E) into the other operand or the epilogue.
