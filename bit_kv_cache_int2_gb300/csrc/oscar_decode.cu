@@ -352,9 +352,7 @@ __device__ __forceinline__ void int2_page_mma_cb(Int2State<NG>& S, const CbExtra
       S.l[1] *= al1;
 #pragma unroll
       for (int gr = 0; gr < NG; ++gr) {
-        S.bs[0][gr] *= al0;
         S.zs[0][gr] *= al0;
-        S.bs[1][gr] *= al1;
         S.zs[1][gr] *= al1;
       }
 #pragma unroll
@@ -1162,8 +1160,6 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
         // a time with the layer's Lloyd-Max codebook
         constexpr bool PAIR = (IMPL == 3);
         constexpr bool CB = (IMPL == 4);
-        // codes (codebook: bit planes) as fp16 subnormals: no offset to carry
-        constexpr bool SUBC = (IMPL == 3 || IMPL == 0 || IMPL == 4);
         constexpr int QREC = CB ? QPACK_CB_BYTES : QPACK_BYTES;
         // the kv head's G packed query records, copied to shared memory by warp
         // 0 with coalesced 16-byte loads (every warp of every CTA reads them;
@@ -1184,7 +1180,6 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
         for (int j = 0; j < 8; ++j) S.oacc[j][0] = S.oacc[j][1] = S.oacc[j][2] = S.oacc[j][3] = 0.f;
         {
           constexpr int O_ALPHA = CB ? QPACK_CB_ALPHA : QPACK_ALPHA;
-          constexpr int O_QSUM = CB ? QPACK_CB_QSUM : QPACK_QSUM;
           constexpr int O_PSUM = CB ? QPACK_CB_PSUM : QPACK_PSUM;
           float kc0 = 0.f;  // codebook: c0_K, the level of code 0
           if constexpr (CB) {
@@ -1217,19 +1212,15 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
             S.m[hc] = PAIR ? -1e30f : -INFINITY;
             S.l[hc] = 0.f;
             const float al = hv ? *(const float*)(r + O_ALPHA) : 0.f;
-            S.ka[hc] = SUBC ? al * 16777216.f : al;  // subnormal codes carry 2^-24
+            S.ka[hc] = al * 16777216.f;  // subnormal codes carry 2^-24
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
-              float qs = 0.f, ps = 0.f;
+              float ps = 0.f;
 #pragma unroll
-              for (int k = gr * (4 / NG); k < (gr + 1) * (4 / NG); ++k) {
-                qs += hv ? ((const float*)(r + O_QSUM))[k] : 0.f;
+              for (int k = gr * (4 / NG); k < (gr + 1) * (4 / NG); ++k)
                 ps += hv ? ((const float*)(r + O_PSUM))[k] : 0.f;
-              }
-              S.bs[hc][gr] = 0.f;
               S.zs[hc][gr] = 0.f;
-              S.kb[hc][gr] = CB ? kc0 * ps * (LOG2E * INV_SQRT_D)
-                                : SUBC ? 0.f : -1024.f * qs * al;
+              S.kb[hc][gr] = CB ? kc0 * ps * (LOG2E * INV_SQRT_D) : 0.f;
               S.kg[hc][gr] = ps * LOG2E * INV_SQRT_D;
             }
           }
@@ -1290,11 +1281,10 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
                 else
                   int2_page_mma_cb<NG, false>(S, X, my_stage + (size_t)st * L.stage_bytes, nv, lane);
               } else if (nv == PAGE) {
-                int2_page_mma<NG, true, SUBC>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
+                int2_page_mma<NG, true>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
               } else {
-                int2_page_mma<NG, false, SUBC>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
+                int2_page_mma<NG, false>(S, my_stage + (size_t)st * L.stage_bytes, nv, lane);
               }
-              if (!SUBC && (k & 7) == 7) flush_v_offset<NG>(S);
             }
             __syncwarp();
             if (k + DEPTH < nw_pages) {
@@ -1310,7 +1300,6 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
             S.l[hc] += __shfl_xor_sync(0xffffffffu, S.l[hc], o);
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
-              S.bs[hc][gr] += __shfl_xor_sync(0xffffffffu, S.bs[hc][gr], o);
               S.zs[hc][gr] += __shfl_xor_sync(0xffffffffu, S.zs[hc][gr], o);
             }
           }
@@ -1337,13 +1326,10 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const int gr = j / (8 / NG);
-              // offset codes: o' = (O - 1024 sum B) / 256 + sum p z; subnormal
-              // codes (PAIR): o' = 2^16 O + sum p z
-              const float off = SUBC ? 0.f : 1024.f * S.bs[hc][gr];
-              const float sc = SUBC ? 65536.f : 1.f / 256.f;
+              // subnormal codes: o' = 2^16 O + sum p z
               const float z = S.zs[hc][gr];
-              wo[(warp * MAX_G + n) * D + 16 * j + gid] = fmaf(S.oacc[j][hc] - off, sc, z);
-              wo[(warp * MAX_G + n) * D + 16 * j + 8 + gid] = fmaf(S.oacc[j][hc + 2] - off, sc, z);
+              wo[(warp * MAX_G + n) * D + 16 * j + gid] = fmaf(S.oacc[j][hc], 65536.f, z);
+              wo[(warp * MAX_G + n) * D + 16 * j + 8 + gid] = fmaf(S.oacc[j][hc + 2], 65536.f, z);
             }
           }
         }

@@ -24,17 +24,16 @@ struct Int2State {
   float oacc[8][4];  // o'^T: m-tile j, rows channels 16j+gid / 16j+8+gid, cols heads 2tq, 2tq+1
   float m[2];        // running max (log2 units) of heads 2tq, 2tq+1
   float l[2];        // this thread's part of the running sum
-  float bs[2][NG];   // this thread's part of sum of B_V values (offset removal)
   float zs[2][NG];   // this thread's part of sum p * z_v
   uint32_t bq[8][2];  // q' B fragments (column = head gid)
   float ka[2];        // logit scale per column head
-  float kb[2][NG];    // logit offset per column head and group
+  float kb[2][NG];    // logit offset per column head and group (codebook pages only)
   float kg[2][NG];    // z-term weight per column head and group
 };
 
 // One INT2 page (64 tokens) of one kv head on tensor cores.  stage: the page's
 // head block in smem; nv: valid tokens.
-template <int NG, bool FULL, bool SUB = false>
+template <int NG, bool FULL>
 __device__ __forceinline__ void int2_page_mma(Int2State<NG>& S, const uint8_t* stage, int nv,
                                               int lane) {
   const int gid = lane >> 2, tq = lane & 3;
@@ -66,10 +65,10 @@ __device__ __forceinline__ void int2_page_mma(Int2State<NG>& S, const uint8_t* s
       const uint32_t xb = kk < 4 ? wb[s].x : wb[s].y;
       uint32_t a0, a1, a2, a3;
       switch (kk & 3) {
-        case 0: a0 = code_fp16<0, SUB>(xa); a1 = code_fp16<0, SUB>(xb); a2 = code_fp16<1, SUB>(xa); a3 = code_fp16<1, SUB>(xb); break;
-        case 1: a0 = code_fp16<2, SUB>(xa); a1 = code_fp16<2, SUB>(xb); a2 = code_fp16<3, SUB>(xa); a3 = code_fp16<3, SUB>(xb); break;
-        case 2: a0 = code_fp16<4, SUB>(xa); a1 = code_fp16<4, SUB>(xb); a2 = code_fp16<5, SUB>(xa); a3 = code_fp16<5, SUB>(xb); break;
-        default: a0 = code_fp16<6, SUB>(xa); a1 = code_fp16<6, SUB>(xb); a2 = code_fp16<7, SUB>(xa); a3 = code_fp16<7, SUB>(xb); break;
+        case 0: a0 = code_sub<0>(xa); a1 = code_sub<0>(xb); a2 = code_sub<1>(xa); a3 = code_sub<1>(xb); break;
+        case 1: a0 = code_sub<2>(xa); a1 = code_sub<2>(xb); a2 = code_sub<3>(xa); a3 = code_sub<3>(xb); break;
+        case 2: a0 = code_sub<4>(xa); a1 = code_sub<4>(xb); a2 = code_sub<5>(xa); a3 = code_sub<5>(xb); break;
+        default: a0 = code_sub<6>(xa); a1 = code_sub<6>(xb); a2 = code_sub<7>(xa); a3 = code_sub<7>(xb); break;
       }
       mma_f16(acc[s][kk / KPG], a0, a1, a2, a3, S.bq[kk][0], S.bq[kk][1]);
     }
@@ -87,7 +86,7 @@ __device__ __forceinline__ void int2_page_mma(Int2State<NG>& S, const uint8_t* s
 #pragma unroll
       for (int gr = 0; gr < NG; ++gr) {
         const float2 sz = __half22float2(ksz[row * NG + gr]);
-        v = fmaf(sz.x, fmaf(acc[s][gr][e], S.ka[hc], S.kb[hc][gr]), fmaf(sz.y, S.kg[hc][gr], v));
+        v = fmaf(sz.x, acc[s][gr][e] * S.ka[hc], fmaf(sz.y, S.kg[hc][gr], v));
       }
       lam[s][e] = (FULL || row < nv) ? v : -INFINITY;
     }
@@ -116,9 +115,7 @@ __device__ __forceinline__ void int2_page_mma(Int2State<NG>& S, const uint8_t* s
       S.l[1] *= al1;
 #pragma unroll
       for (int gr = 0; gr < NG; ++gr) {
-        S.bs[0][gr] *= al0;
         S.zs[0][gr] *= al0;
-        S.bs[1][gr] *= al1;
         S.zs[1][gr] *= al1;
       }
 #pragma unroll
@@ -158,11 +155,6 @@ __device__ __forceinline__ void int2_page_mma(Int2State<NG>& S, const uint8_t* s
       const float s_b = vb ? sb.x * fb : 0.f, z_b = vb ? sb.y : 0.f;
       const __half2 h0 = __floats2half2_rn(p[0] * s_a, p[1] * s_a);
       const __half2 h1 = __floats2half2_rn(p[2] * s_b, p[3] * s_b);
-      if constexpr (!SUB) {  // the offset form carries 1024 * (sum of B) in O
-        const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
-        S.bs[0][gr] += f0.x + f1.x;
-        S.bs[1][gr] += f0.y + f1.y;
-      }
       S.zs[0][gr] = fmaf(p[0], z_a, fmaf(p[2], z_b, S.zs[0][gr]));
       S.zs[1][gr] = fmaf(p[1], z_a, fmaf(p[3], z_b, S.zs[1][gr]));
       const uint32_t b0 = movmatrix_t(*(const uint32_t*)&h0);
@@ -172,38 +164,12 @@ __device__ __forceinline__ void int2_page_mma(Int2State<NG>& S, const uint8_t* s
         const int j = gr * MPG + jj;
         uint32_t a0, a1, a2, a3;
         switch (s) {
-          case 0: a0 = code_fp16<0, SUB>(vw[j][0]); a1 = code_fp16<0, SUB>(vw[j][1]); a2 = code_fp16<1, SUB>(vw[j][0]); a3 = code_fp16<1, SUB>(vw[j][1]); break;
-          case 1: a0 = code_fp16<2, SUB>(vw[j][0]); a1 = code_fp16<2, SUB>(vw[j][1]); a2 = code_fp16<3, SUB>(vw[j][0]); a3 = code_fp16<3, SUB>(vw[j][1]); break;
-          case 2: a0 = code_fp16<4, SUB>(vw[j][0]); a1 = code_fp16<4, SUB>(vw[j][1]); a2 = code_fp16<5, SUB>(vw[j][0]); a3 = code_fp16<5, SUB>(vw[j][1]); break;
-          default: a0 = code_fp16<6, SUB>(vw[j][0]); a1 = code_fp16<6, SUB>(vw[j][1]); a2 = code_fp16<7, SUB>(vw[j][0]); a3 = code_fp16<7, SUB>(vw[j][1]); break;
+          case 0: a0 = code_sub<0>(vw[j][0]); a1 = code_sub<0>(vw[j][1]); a2 = code_sub<1>(vw[j][0]); a3 = code_sub<1>(vw[j][1]); break;
+          case 1: a0 = code_sub<2>(vw[j][0]); a1 = code_sub<2>(vw[j][1]); a2 = code_sub<3>(vw[j][0]); a3 = code_sub<3>(vw[j][1]); break;
+          case 2: a0 = code_sub<4>(vw[j][0]); a1 = code_sub<4>(vw[j][1]); a2 = code_sub<5>(vw[j][0]); a3 = code_sub<5>(vw[j][1]); break;
+          default: a0 = code_sub<6>(vw[j][0]); a1 = code_sub<6>(vw[j][1]); a2 = code_sub<7>(vw[j][0]); a3 = code_sub<7>(vw[j][1]); break;
         }
         mma_f16(S.oacc[j], a0, a1, a2, a3, b0, b1);
-      }
-    }
-  }
-}
-
-// The SV accumulators carry 1024 * (sum of B values) on top of the signal;
-// over hundreds of pages that offset would cost fp32 accuracy, so it is moved
-// out of them every few pages: oacc -= 1024 * sum_B (all rows of the page
-// group), and the running sum of B restarts at 0.
-template <int NG>
-__device__ __forceinline__ void flush_v_offset(Int2State<NG>& S) {
-  constexpr int MPG = 8 / NG;
-#pragma unroll
-  for (int hc = 0; hc < 2; ++hc) {
-#pragma unroll
-    for (int gr = 0; gr < NG; ++gr) {
-      float t = S.bs[hc][gr];
-      t += __shfl_xor_sync(0xffffffffu, t, 4);
-      t += __shfl_xor_sync(0xffffffffu, t, 8);
-      t += __shfl_xor_sync(0xffffffffu, t, 16);
-      S.bs[hc][gr] = 0.f;
-      const float off = 1024.f * t;
-#pragma unroll
-      for (int jj = 0; jj < MPG; ++jj) {
-        S.oacc[gr * MPG + jj][hc] -= off;
-        S.oacc[gr * MPG + jj][hc + 2] -= off;
       }
     }
   }
@@ -287,7 +253,7 @@ __device__ __forceinline__ void int2_pair_mma(Int2State<NG>& S, const uint8_t* s
 #pragma unroll
       for (int gr = 0; gr < NG; ++gr) {
         const float2 sz = __half22float2(ksz[row * NG + gr]);
-        v = fmaf(sz.x, fmaf(acc[s][gr][e], S.ka[hc], S.kb[hc][gr]), fmaf(sz.y, S.kg[hc][gr], v));
+        v = fmaf(sz.x, acc[s][gr][e] * S.ka[hc], fmaf(sz.y, S.kg[hc][gr], v));
       }
       lam[s][e] = v;
     }
@@ -323,9 +289,7 @@ __device__ __forceinline__ void int2_pair_mma(Int2State<NG>& S, const uint8_t* s
       S.l[1] *= al1;
 #pragma unroll
       for (int gr = 0; gr < NG; ++gr) {
-        S.bs[0][gr] *= al0;
         S.zs[0][gr] *= al0;
-        S.bs[1][gr] *= al1;
         S.zs[1][gr] *= al1;
       }
 #pragma unroll
@@ -415,7 +379,6 @@ __device__ __forceinline__ void merge_pair_streams(Int2State<NG>& S) {
     S.l[hc] = S.l[hc] * fa + __shfl_xor_sync(0xffffffffu, S.l[hc], 2) * fb;
 #pragma unroll
     for (int gr = 0; gr < NG; ++gr) {
-      S.bs[hc][gr] = S.bs[hc][gr] * fa + __shfl_xor_sync(0xffffffffu, S.bs[hc][gr], 2) * fb;
       S.zs[hc][gr] = S.zs[hc][gr] * fa + __shfl_xor_sync(0xffffffffu, S.zs[hc][gr], 2) * fb;
     }
 #pragma unroll
