@@ -1118,9 +1118,9 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
         const int st = (int)((seq + k) % DEPTH);
         if (pid >= 0 && pid < cv.num_pages) {
           mbar_expect_tx(&my_bar[st], (uint32_t)cv.head_bytes);
-          bulk_g2s(my_stage + (size_t)st * L.stage_bytes,
-                   cv.pool + (size_t)pid * cv.page_bytes + (size_t)kvh * cv.head_bytes,
-                   (uint32_t)cv.head_bytes, &my_bar[st]);
+          bulk_g2s_hint(my_stage + (size_t)st * L.stage_bytes,
+                        cv.pool + (size_t)pid * cv.page_bytes + (size_t)kvh * cv.head_bytes,
+                        (uint32_t)cv.head_bytes, &my_bar[st], l2_evict_first_policy());
         } else {
           record_error(cv.err, pid < 0 ? OSCAR_ERR_NO_PAGE : OSCAR_ERR_RANGE);
           mbar_expect_tx(&my_bar[st], 0u);

@@ -418,6 +418,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase, int pol
 
 // Plain (non-multicast) bulk copy global -> this CTA's shared memory,
 // completing on an mbarrier.  dst, src 16-byte aligned; bytes a multiple of 16.
+// An L2 policy that marks lines for eviction first: a decode reads each
+// history page once per call, so its copies should not displace the lines
+// that stay hot (partial records, page tables, windows, query records).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
+// bulk_g2s with an L2 cache policy (l2_evict_first_policy for streamed pages)
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar, uint64_t policy) {
+  uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  uint32_t b = (uint32_t)__cvta_generic_to_shared(bar);
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, "
+      "[%3], %4;\n" ::"r"(d),
+      "l"(src), "r"(bytes), "r"(b), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
                                          uint64_t* bar) {
   uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
