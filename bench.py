@@ -605,7 +605,9 @@ def bench_config(args, wl):
     return {"workload": args.workload, "batch": wl["B"], "q_heads": wl["Hq"], "kv_heads": wl["Hkv"], "head_dim": 128,
             "context": wl["L"], "group_size": wl["g"], "clip": wl["clip"], "parallelism": "replicas",
             "l2": "every timed call reads a cache copy other than the last few: the copies rotated over total at "
-                  "least 3x the L2 size (129 MB), so no call finds its inputs in L2"}
+                  "least 3x the L2 size (129 MB), so no call finds its history pages in L2 (the page copies are "
+                  "marked evict-first; the copies' BF16 windows, 2% of a call's bytes, may stay in L2 between "
+                  "calls, as a layer's windows can between decode steps)"}
 
 
 def oracle_subprocess_seconds(host, wl, U, q, threads, budget_s):
