@@ -139,13 +139,17 @@ int decode_ctas(const oscar_ctx* ctx, int batch, bool bf16_history, int layer = 
 
 // decode_kernel's work partition (DecodeArgs::balanced): 0 the item list, 1
 // balanced, 2 decided on the device (balanced once the item list would give
-// a CTA more than a wave's worth of pages).  Automatic: the item list when
-// the (request, kv head) segments outnumber half the CTAs -- a balanced range
-// would then cross segments, each crossing paying an item start.
-int decode_partition(const oscar_ctx* ctx, int batch, int ctas) {
+// a CTA more than a wave's worth of pages).  Automatic: balanced from 16
+// (request, kv head) segments on; below that the device decides.  With few
+// segments the balanced ranges hand every window chunk of a kv head to the
+// CTA or two at the head's end, where the item list spreads them over
+// distinct CTAs (batch 1 at 100K: 27.9 us with items, 33.5 balanced); from
+// two requests on the balanced ranges measured faster at every batched shape
+// tried (batch 2 to 128, 2K to 131K tokens).
+int decode_partition(const oscar_ctx* ctx, int batch) {
   if (ctx->partition == 1) return 0;
   if (ctx->partition == 2) return 1;
-  return 2 * batch * ctx->cfg.num_kv_heads <= ctas ? 2 : 0;
+  return batch * ctx->cfg.num_kv_heads >= 16 ? 1 : 2;
 }
 
 // The item list's size bound (make_sched's target).
@@ -166,7 +170,7 @@ int target_items(const oscar_ctx* ctx, int batch, bool bf16_history, int layer =
   const int t = list_items(ctx, batch, bf16_history, layer);
   const int ctas = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, layer);
   const int tb = ctas + 4 * batch * ctx->cfg.num_kv_heads;
-  const int part = decode_partition(ctx, batch, ctas);
+  const int part = decode_partition(ctx, batch);
   if (part == 1) return tb;
   if (part == 2 && tb > t) return tb;
   return t;
@@ -376,7 +380,7 @@ oscar_status decode_args(oscar_ctx* ctx, int layer, const oscar_cache* cache, co
   }
   grid = ctx->num_sms * decode_ctas(ctx, batch, bf16_history, vlayer);
   a.resident = ctx->items_per_cta == 0 ? grid : 0;
-  a.balanced = decode_partition(ctx, batch, grid);
+  a.balanced = decode_partition(ctx, batch);
   a.bal_grid = grid;
   a.bal_wch = DEC_WIN_WEIGHT;
   return OSCAR_OK;

@@ -143,13 +143,12 @@ typedef enum {
                                   leaves.  0 makes every such wait give up at once: a way to
                                   exercise that path.  Values < 0 are OSCAR_ERR_INVALID_ARG. */
   OSCAR_OPT_DECODE_PARTITION = 5 /* how the mma.sync and CUDA-core decode kernels split the work:
-                                    0 (default) automatic -- balanced when a CTA would get more
-                                    than 40 history pages of the item list and the (request, kv
-                                    head) pairs are at most half the CTAs, else the item list; 1 the
-                                    item list
-                                    (OSCAR_OPT_ITEMS_PER_CTA); 2 balanced: CTA i takes an equal
-                                    share of all history pages and window chunks, in order.  The
-                                    outputs do not depend on the partition beyond rounding. */
+                                    0 (default) automatic -- balanced when the call has at least
+                                    16 (request, kv head) pairs, or when a CTA would get more than
+                                    40 history pages of the item list, else the item list; 1 the
+                                    item list (OSCAR_OPT_ITEMS_PER_CTA); 2 balanced: CTA i takes an
+                                    equal share of all history pages and window chunks, in order.
+                                    The outputs do not depend on the partition beyond rounding. */
 } oscar_option;
 
 typedef struct {
