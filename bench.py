@@ -236,10 +236,12 @@ BATCHED = {
 }
 
 
-def batched_measurement(dev, peak, steps=120, seed=0):
+def batched_measurement(dev, peak, steps=120, seed=0, configs=None, decode_warmup=5, decode_calls=100,
+                        partition=0):
     """Decode step (append with demotion + attention) and attention alone at
-    the batched configurations, rotating over cache copies larger than 3x L2.
-    Rotations are Hadamard-only: the kernels' work does not depend on R."""
+    the batched configurations (`configs`, default BATCHED), rotating over
+    cache copies larger than 3x L2.  Rotations are Hadamard-only: the
+    kernels' work does not depend on R."""
     import numpy as np
     import torch
 
@@ -247,7 +249,7 @@ def batched_measurement(dev, peak, steps=120, seed=0):
 
     l2 = torch.cuda.get_device_properties(torch.device(dev)).L2_cache_size
     res = {}
-    for name, c in BATCHED.items():
+    for name, c in (BATCHED if configs is None else configs).items():
         Bsz, Hq, Hkv, g = c["B"], c["Hq"], c["Hkv"], c["g"]
         rng = np.random.default_rng(synth.stream_seed(seed, name, "lens"))
         lens = [int(x) for x in rng.integers(c["lens"][0], c["lens"][1] + 1, Bsz)]
@@ -259,6 +261,8 @@ def batched_measurement(dev, peak, steps=120, seed=0):
         mpr, npages = max(ppr), sum(ppr)
         cfg = oscar.make_config(1, Hq, Hkv, g, max_batch=Bsz, max_pages_per_req=mpr, num_pages=npages)
         ctx = oscar.oscar_create(cfg)
+        if partition:
+            oscar.oscar_set_option(ctx, oscar.OPT_DECODE_PARTITION, partition)
         eye = np.stack([np.eye(128, dtype=np.float32)] * Hkv)
         oscar.oscar_set_rotation(ctx, 0, eye, eye, [c["clip"]] * Hkv, [c["clip"]] * Hkv, oscar.ROT_HADAMARD)
         base = oscar.alloc_cache(cfg, dev)
@@ -318,9 +322,9 @@ def batched_measurement(dev, peak, steps=120, seed=0):
         for i in range(n_copies):
             step(i)
         us_step = timed(step, steps - n_copies)
-        for i in range(5):
+        for i in range(decode_warmup):
             dec[i % n_copies]()
-        us_dec = timed(lambda i: dec[i % n_copies](), 100)
+        us_dec = timed(lambda i: dec[i % n_copies](), decode_calls)
         assert oscar.oscar_get_error(ctx) == 0 and torch.isfinite(out.float()).all()
         r = {"batch": Bsz, "q_heads": Hq, "kv_heads": Hkv, "group_size": g, "context": list(c["lens"]),
              "tokens": sum(lens), "step_us": us_step, "decode_us": us_dec, "bytes_per_decode": per_copy,
@@ -569,6 +573,8 @@ def serving_measurement(wl, dev, n_req=48, gen=64, lo=8192, hi=24576, budget_req
         pool_pages = int((budget - slots * window_bytes) // page_bytes[fmt])
         cfg = oscar.make_config(1, Hq, Hkv, g, max_batch=slots, max_pages_per_req=mpr, num_pages=pool_pages)
         ctx = oscar.oscar_create(cfg)
+        if partition:
+            oscar.oscar_set_option(ctx, oscar.OPT_DECODE_PARTITION, partition)
         eye = np.stack([np.eye(128, dtype=np.float32)] * Hkv)
         oscar.oscar_set_rotation(ctx, 0, eye, eye, [wl["clip"]] * Hkv, [wl["clip"]] * Hkv,
                                  oscar.ROT_HADAMARD if fmt == "int2" else oscar.ROT_NONE)
@@ -1282,6 +1288,31 @@ def run_leg(args, wl):
     print(json.dumps(line), flush=True)
 
 
+def run_batched_leg(args):
+    """One batched configuration alone (--config, a BATCHED name; INT2 only):
+    16 decode steps (append with demotion + attention), then --warmup untimed
+    and --steps timed oscar_decode calls over cache copies larger than 3x L2.
+    A short command for profiling the decode kernel at that configuration:
+    the timed decode launches follow 16 + --warmup others."""
+    from bit_kv_cache_int2_gb300 import build as B
+
+    B.build()
+    name = args.config
+    if name not in BATCHED:
+        raise SystemExit(f"--config must be one of {sorted(BATCHED)}")
+    peak, kind = peaks()
+    from bit_kv_cache_int2_gb300 import oscar
+
+    part = {"auto": oscar.PARTITION_AUTO, "items": oscar.PARTITION_ITEMS,
+            "balanced": oscar.PARTITION_BALANCED}[args.partition]
+    r = batched_measurement("cuda:0", peak, steps=16, configs={name: dict(BATCHED[name], bf16=False)},
+                            decode_warmup=args.warmup, decode_calls=args.steps, partition=part)[name]
+    print(json.dumps({"leg": "batched", "config": name, "partition": args.partition, "calls": args.steps,
+                      "step_us": r["step_us"], "decode_us": r["decode_us"], "bytes_per_decode": r["bytes_per_decode"],
+                      "hbm_gbs": r["decode_hbm_gbs"], "frac_of_" + kind + "_hbm": r["decode_frac"],
+                      "cache_copies": r["cache_copies"]}), flush=True)
+
+
 def run_codebook_leg(args, wl):
     """Only the Lloyd-Max codebook decode on the workload: fits from the
     calibration sets, a cache written with them, and --steps timed decodes
@@ -1353,9 +1384,12 @@ def main():
                     help="single-operation legs: context length instead of the workload's (0: the workload's)")
     ap.add_argument("--partition", choices=["auto", "items", "balanced"], default="auto",
                     help="single-operation legs: the decode kernels' work partition (OSCAR_OPT_DECODE_PARTITION)")
-    ap.add_argument("--leg", choices=["all", "codebook"] + list(LEGS), default="all",
+    ap.add_argument("--leg", choices=["all", "codebook", "batched"] + list(LEGS), default="all",
                     help="one operation alone on the workload, a short command to profile it (see run_leg); "
-                         "codebook: only the Lloyd-Max codebook decode")
+                         "codebook: only the Lloyd-Max codebook decode; batched: one batched configuration "
+                         "(--config)")
+    ap.add_argument("--config", default="qwen3_32b_b8_131k", choices=sorted(BATCHED),
+                    help="--leg batched: the batched configuration")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = WORKLOADS[args.workload]
@@ -1363,6 +1397,8 @@ def main():
         run_reference(args, wl)
     elif args.leg == "codebook":
         run_codebook_leg(args, wl)
+    elif args.leg == "batched":
+        run_batched_leg(args)
     elif args.leg in LEGS:
         run_leg(args, wl)
     else:
