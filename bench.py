@@ -573,8 +573,6 @@ def serving_measurement(wl, dev, n_req=48, gen=64, lo=8192, hi=24576, budget_req
         pool_pages = int((budget - slots * window_bytes) // page_bytes[fmt])
         cfg = oscar.make_config(1, Hq, Hkv, g, max_batch=slots, max_pages_per_req=mpr, num_pages=pool_pages)
         ctx = oscar.oscar_create(cfg)
-        if partition:
-            oscar.oscar_set_option(ctx, oscar.OPT_DECODE_PARTITION, partition)
         eye = np.stack([np.eye(128, dtype=np.float32)] * Hkv)
         oscar.oscar_set_rotation(ctx, 0, eye, eye, [wl["clip"]] * Hkv, [wl["clip"]] * Hkv,
                                  oscar.ROT_HADAMARD if fmt == "int2" else oscar.ROT_NONE)
