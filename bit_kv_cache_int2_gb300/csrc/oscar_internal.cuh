@@ -708,10 +708,11 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) 
 // 28.6 against 27.2 us), and than none (27.9 us).  Every thread derives the
 // item size S as make_sched does, from the lengths as they are now: they may
 // be a step old, and nothing depends on the prefetches but timing.  The
-// balanced partition and the BF16-history decode prefetch nothing here.
+// BF16-history decode (the same item list over BF16 page blocks) takes the
+// same prefetch; the balanced partition takes none.
 __device__ inline void prefetch_first_pages(const DecodeArgs& a, int b, int kvh, int cq, int t) {
   const CacheView& cv = a.cv;
-  if (a.balanced == 1 || a.bf16_history) return;
+  if (a.balanced == 1) return;
   const int B = a.B, Hkv = cv.Hkv;
   const int32_t* hl = cv.hist_lens;
   int total = 0;
