@@ -669,7 +669,7 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
   bool bal = a.balanced == 1;
   Sched sc;
   if (!bal) {
-    sc = make_sched(hl, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
+    sc = make_sched(hl, a.B, Hkv, a.target_items, a.resident, unit, pre, red, pages_granule(a.impl));
     bal = a.balanced == 2 && use_balanced(sc, a.bal_grid);  // as decode_kernel decides
   }
   if (bal) {
@@ -960,7 +960,7 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
   Sched sc;
   bool bal = a.balanced == 1;
   if (!bal) {
-    sc = make_sched(hl, a.B, Hkv, a.target_items, a.resident, unit, pre, red);
+    sc = make_sched(hl, a.B, Hkv, a.target_items, a.resident, unit, pre, red, pages_granule(a.impl));
     bal = a.balanced == 2 && use_balanced(sc, gridDim.x);
   }
   if (bal)  // out of line: the item list's path stays short

@@ -477,12 +477,22 @@ constexpr int DEC_WIN_WEIGHT = 12;
 constexpr int AUTO_WAVE_PAGES = 40;
 constexpr int AUTO_MIN_PAGES = 28;
 
+// Item size granule of the one-item-per-CTA list: the page-pair kernel
+// (impl 3) rounds items up to whole pairs for each of its 4 warps (8 pages):
+// no item ends in a half-empty pair, and fewer items leave fewer partial
+// records to merge (batch 1, 10K: step 17.2 -> 14.3 us; 100K: decode 27.3 ->
+// 27.0 us, step unchanged within 0.2 us).  The one-page-per-tile kernels keep
+// exact sizes (the codebook kernel measured 38.6 -> 39.3 us with 8 in one
+// run, within that leg's run-to-run spread).
+__host__ __device__ __forceinline__ int pages_granule(int impl) { return impl == 3 ? 8 : 1; }
+
 // pre: smem int[B + 1]; filled with Hkv * (history items of requests < b).
 // target: the most items the list may hold; resident: the decode CTAs that
-// run at once, or 0 to size items for `target` items in total.
+// run at once, or 0 to size items for `target` items in total.  granule:
+// with one item per CTA, items are a multiple of it (pages_granule()).
 // Must be called by all threads of the block.
 __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int target, int resident,
-                                   int hist_item_unit_bytes, int* pre, int* red) {
+                                   int hist_item_unit_bytes, int* pre, int* red, int granule) {
   const int tid = threadIdx.x;
   // total history pages (over requests), times Hkv
   int local = 0;
@@ -513,6 +523,8 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
   if (resident > 0 && S > AUTO_WAVE_PAGES) {
     S = pages_per_item(target);
     if (S < AUTO_MIN_PAGES) S = AUTO_MIN_PAGES;
+  } else if (resident > 0) {
+    S = (S + granule - 1) / granule * granule;
   }
   s.S = (int)S;
   if (tid == 0) {
@@ -733,6 +745,9 @@ __device__ inline void prefetch_first_pages(const DecodeArgs& a, int b, int kvh,
   if (a.resident > 0 && S > AUTO_WAVE_PAGES) {
     S = pages_per_item(a.target_items);
     if (S < AUTO_MIN_PAGES) S = AUTO_MIN_PAGES;
+  } else if (a.resident > 0) {
+    const int gr = pages_granule(a.impl);
+    S = (S + gr - 1) / gr * gr;
   }
 #pragma unroll 1
   for (int iter = 0; iter < 32; ++iter) {
