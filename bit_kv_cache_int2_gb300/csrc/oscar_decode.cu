@@ -60,9 +60,9 @@ struct DecodeCursor {
 };
 
 // The automatic partition: balanced once the item list would give a CTA more
-// than AUTO_WAVE_PAGES pages (several items per CTA, each paying a start).
-__device__ __forceinline__ bool use_balanced(const Sched& sc, int grid) {
-  return sc.pages > (long long)AUTO_WAVE_PAGES * grid;
+// than auto_wave_pages() pages (several items per CTA, each paying a start).
+__device__ __forceinline__ bool use_balanced(const Sched& sc, int grid, bool bf16_history) {
+  return sc.pages > (long long)auto_wave_pages(bf16_history) * grid;
 }
 
 // Weight of (b, kvh) in the balanced list: history pages plus wch per
@@ -669,8 +669,9 @@ __global__ void __launch_bounds__(MW * 32) merge_kernel(DecodeArgs a) {
   bool bal = a.balanced == 1;
   Sched sc;
   if (!bal) {
-    sc = make_sched(hl, a.B, Hkv, a.target_items, a.resident, unit, pre, red, pages_granule(a.impl));
-    bal = a.balanced == 2 && use_balanced(sc, a.bal_grid);  // as decode_kernel decides
+    sc = make_sched(hl, a.B, Hkv, a.target_items, a.resident, unit, pre, red, pages_granule(a.impl),
+                    auto_wave_pages(a.bf16_history));
+    bal = a.balanced == 2 && use_balanced(sc, a.bal_grid, a.bf16_history);  // as decode_kernel decides
   }
   if (bal) {
     const Balanced bl = make_balanced(sl, hl, a.B, Hkv, a.bal_wch, a.bal_grid, pre64);
@@ -960,8 +961,9 @@ __global__ void __launch_bounds__(NW * 32, (NG == 1 && (IMPL == 0 || IMPL == 3 |
   Sched sc;
   bool bal = a.balanced == 1;
   if (!bal) {
-    sc = make_sched(hl, a.B, Hkv, a.target_items, a.resident, unit, pre, red, pages_granule(a.impl));
-    bal = a.balanced == 2 && use_balanced(sc, gridDim.x);
+    sc = make_sched(hl, a.B, Hkv, a.target_items, a.resident, unit, pre, red, pages_granule(a.impl),
+                    auto_wave_pages(a.bf16_history));
+    bal = a.balanced == 2 && use_balanced(sc, gridDim.x, a.bf16_history);
   }
   if (bal)  // out of line: the item list's path stays short
     balanced_setup(*cur, a.B, Hkv, a.bal_wch, WindowPtrs{cv.sink_k, cv.sink_v, cv.ring_k, cv.ring_v},

@@ -467,14 +467,19 @@ struct Sched {
 };
 
 // Automatic item sizing (resident > 0): one item per resident CTA while that
-// keeps items at most AUTO_WAVE_PAGES pages (small work: per-item start and
-// merge costs dominate); beyond that, items for up to target / resident per
-// CTA, at least AUTO_MIN_PAGES pages each, balanced through the work counter.
+// keeps items at most auto_wave_pages() pages (per-item start and merge costs
+// favour few items); beyond that, items for up to target / resident per CTA,
+// at least AUTO_MIN_PAGES pages each, balanced through the work counter.  The
+// automatic partition switches to the balanced one at the same size
+// (use_balanced).  INT2 kernels, batch 1, one item per CTA against the
+// balanced partition: 150K 34.1 / 40.7 us, 200K 41.4 / 46.4, 300K 55.7 /
+// 57.8, 400K 70.0 / 68.4; the BF16-history kernel keeps 40 pages (at 200K
+// one item per CTA took 136.9 us against 130.8 balanced).
 constexpr int AUTO_ITEMS_PER_CTA = 4;
 // Weight of one BF16 window chunk (64 tokens of one kv head) in history pages
 // in decode_kernel's balanced partition.
 constexpr int DEC_WIN_WEIGHT = 12;
-constexpr int AUTO_WAVE_PAGES = 40;
+__host__ __device__ __forceinline__ int auto_wave_pages(bool bf16_history) { return bf16_history ? 40 : 96; }
 constexpr int AUTO_MIN_PAGES = 28;
 
 // Item size granule of the one-item-per-CTA list: the page-pair kernel
@@ -490,9 +495,10 @@ __host__ __device__ __forceinline__ int pages_granule(int impl) { return impl ==
 // target: the most items the list may hold; resident: the decode CTAs that
 // run at once, or 0 to size items for `target` items in total.  granule:
 // with one item per CTA, items are a multiple of it (pages_granule()).
+// wave_pages: auto_wave_pages().
 // Must be called by all threads of the block.
 __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int target, int resident,
-                                   int hist_item_unit_bytes, int* pre, int* red, int granule) {
+                                   int hist_item_unit_bytes, int* pre, int* red, int granule, int wave_pages) {
   const int tid = threadIdx.x;
   // total history pages (over requests), times Hkv
   int local = 0;
@@ -520,7 +526,7 @@ __device__ inline Sched make_sched(const int32_t* hist_lens, int B, int Hkv, int
     return S < 1 ? 1 : S;
   };
   int S = pages_per_item(resident > 0 ? resident : target);
-  if (resident > 0 && S > AUTO_WAVE_PAGES) {
+  if (resident > 0 && S > wave_pages) {
     S = pages_per_item(target);
     if (S < AUTO_MIN_PAGES) S = AUTO_MIN_PAGES;
   } else if (resident > 0) {
@@ -731,7 +737,8 @@ __device__ inline void prefetch_first_pages(const DecodeArgs& a, int b, int kvh,
 #pragma unroll 1
   for (int i = 0; i < B; ++i) total += (hl[i] + PAGE - 1) / PAGE;
   total *= Hkv;
-  if (total <= 0 || (a.balanced == 2 && (long long)total > (long long)AUTO_WAVE_PAGES * a.bal_grid)) return;
+  const int wave = auto_wave_pages(a.bf16_history);
+  if (total <= 0 || (a.balanced == 2 && (long long)total > (long long)wave * a.bal_grid)) return;
   int wch = 5, n_win = 0;
   auto pages_per_item = [&](int items) {
     wch = (5LL * B * Hkv * 4 <= items) ? 5 : 1;
@@ -742,7 +749,7 @@ __device__ inline void prefetch_first_pages(const DecodeArgs& a, int b, int kvh,
     return S < 1 ? 1 : S;
   };
   int S = pages_per_item(a.resident > 0 ? a.resident : a.target_items);
-  if (a.resident > 0 && S > AUTO_WAVE_PAGES) {
+  if (a.resident > 0 && S > wave) {
     S = pages_per_item(a.target_items);
     if (S < AUTO_MIN_PAGES) S = AUTO_MIN_PAGES;
   } else if (a.resident > 0) {

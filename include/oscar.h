@@ -145,7 +145,8 @@ typedef enum {
   OSCAR_OPT_DECODE_PARTITION = 5 /* how the mma.sync and CUDA-core decode kernels split the work:
                                     0 (default) automatic -- balanced when the call has at least
                                     16 (request, kv head) pairs, or when a CTA would get more than
-                                    40 history pages of the item list, else the item list; 1 the
+                                    96 history pages of the item list (40 for the BF16-history
+                                    decode), else the item list; 1 the
                                     item list (OSCAR_OPT_ITEMS_PER_CTA); 2 balanced: CTA i takes an
                                     equal share of all history pages and window chunks, in order.
                                     The outputs do not depend on the partition beyond rounding. */
