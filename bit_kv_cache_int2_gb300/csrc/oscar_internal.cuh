@@ -724,10 +724,11 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) 
 // CTA takes first (items below the decode grid; later ones go by the work
 // counter).  All eight pages measured slower than four (100K batch 1: decode
 // 28.6 against 27.2 us), and than none (27.9 us).  Every thread derives the
-// item size S as make_sched does, from the lengths as they are now: they may
-// be a step old, and nothing depends on the prefetches but timing.  The
+// work plan as the decode does, from the lengths as they are now: they may be
+// a step old, and nothing depends on the prefetches but timing.  The
 // BF16-history decode (the same item list over BF16 page blocks) takes the
-// same prefetch; the balanced partition takes none.
+// same prefetch; the balanced partition takes it only with fewer than 16
+// (request, kv head) segments (below).
 __device__ inline void prefetch_first_pages(const DecodeArgs& a, int b, int kvh, int cq, int t) {
   const CacheView& cv = a.cv;
   if (a.balanced == 1) return;
@@ -738,7 +739,49 @@ __device__ inline void prefetch_first_pages(const DecodeArgs& a, int b, int kvh,
   for (int i = 0; i < B; ++i) total += (hl[i] + PAGE - 1) / PAGE;
   total *= Hkv;
   const int wave = auto_wave_pages(a.bf16_history);
-  if (total <= 0 || (a.balanced == 2 && (long long)total > (long long)wave * a.bal_grid)) return;
+  if (total <= 0) return;
+  const int32_t* row = cv.page_table + (size_t)b * cv.max_pages_per_req;
+  const int pages_b = (hl[b] + PAGE - 1) / PAGE;
+  auto fetch = [&](int p) {
+    if (p < 0 || p >= pages_b || p >= cv.max_pages_per_req) return;
+    const int pid = row[p];
+    if (pid >= 0 && pid < cv.num_pages)
+      bulk_prefetch_l2(cv.pool + (size_t)pid * cv.page_bytes + (size_t)kvh * cv.head_bytes, (uint32_t)cv.head_bytes);
+  };
+  if (a.balanced == 2 && (long long)total > (long long)wave * a.bal_grid) {
+    // the balanced partition with few (request, kv head) segments (the host
+    // leaves the choice to the device below 16): segment (b', kvh') weighs its
+    // pages plus bal_wch per non-empty window chunk, CTA i starts at
+    // floor(i W / n); this quarter takes the CTAs i = cq (mod 4) whose range
+    // starts in (b, kvh)'s pages.  (With many segments this derivation, in
+    // every query CTA before its wait, cost more than it saved: batch 32 at
+    // 8K-32K, 130.9 -> 149.6 us.)
+    long long W = 0, seg = 0, wb = 0;
+#pragma unroll 1
+    for (int i = 0; i < B; ++i) {
+      const int H = hl[i], P = H > 0 ? (H + PAGE - 1) / PAGE : 0;
+      const long long w = P + (long long)a.bal_wch * __popc(window_chunk_mask(cv.seq_lens[i], H));
+      if (i < b) seg += Hkv * w;
+      if (i == b) wb = w;
+      W += Hkv * w;
+    }
+    seg += kvh * wb;
+    if (W <= 0 || pages_b <= 0) return;
+    Balanced bl;
+    bl.W = W;
+    bl.n = (int)(W < a.bal_grid ? W : a.bal_grid);
+    bl.wch = a.bal_wch;
+    int i0 = balanced_owner(bl, seg);
+    if (balanced_lo(bl, i0) < seg) ++i0;
+    const int i1 = balanced_owner(bl, seg + pages_b - 1);
+#pragma unroll 1
+    for (int e = t;; e += 128) {
+      const int i = i0 + cq + 4 * (e >> 2);
+      if (i > i1) break;
+      fetch((int)(balanced_lo(bl, i) - seg) + (e & 3));
+    }
+    return;
+  }
   int wch = 5, n_win = 0;
   auto pages_per_item = [&](int items) {
     wch = (5LL * B * Hkv * 4 <= items) ? 5 : 1;
@@ -767,18 +810,13 @@ __device__ inline void prefetch_first_pages(const DecodeArgs& a, int b, int kvh,
   int first = 0;  // the block that runs item 0 of (b, kvh)
 #pragma unroll 1
   for (int i = 0; i < b; ++i) first += Hkv * (((hl[i] + PAGE - 1) / PAGE + S - 1) / S);
-  const int pages_b = (hl[b] + PAGE - 1) / PAGE;
   const int nb = (pages_b + S - 1) / S;
   first += kvh * nb + ((long long)(WIN_BYTES_PER_HEAD / wch) > (long long)S * cv.head_bytes ? n_win : 0);
-  const int32_t* row = cv.page_table + (size_t)b * cv.max_pages_per_req;
 #pragma unroll 1
   for (int e = t;; e += 128) {
-    const int j = cq + 4 * (e >> 2), p = j * S + (e & 3);
+    const int j = cq + 4 * (e >> 2);
     if (j >= nb || first + j >= a.bal_grid) break;
-    if (p >= pages_b || p >= cv.max_pages_per_req) continue;
-    const int pid = row[p];
-    if (pid >= 0 && pid < cv.num_pages)
-      bulk_prefetch_l2(cv.pool + (size_t)pid * cv.page_bytes + (size_t)kvh * cv.head_bytes, (uint32_t)cv.head_bytes);
+    fetch(j * S + (e & 3));
   }
 }
 
